@@ -1,0 +1,312 @@
+"""CPU oracle for AWQ's per-layer activation-aware scale search and INT4 pack.
+
+TEST INFRASTRUCTURE ONLY. This is a plain, slow, fp64 numpy statement of what
+the library computes. Only the tests, the package's smoke check and the
+benchmark's CPU-baseline leg may import it; the CUDA path never does, and the
+two share no code. Every input comes from the seeded generator in
+``workloads``; nothing here reads a value produced by the CUDA path.
+
+Sources (web pages on AWQ, cited by title and section):
+
+* [AWQ-devto]  "AWQ: How Activation-Aware Quantization Saves 4-bit LLMs"
+  - "How does AWQ decide which weights to protect?" (channel_importance listing)
+  - "How does AWQ protect channels without mixed precision?" (search_scale
+    listing and the two remarks after it)
+  - "What do you actually deploy" (the quant_config listing: zero point on,
+    group size 128, 4 bits)
+* [AWQ-SWP]    "AWQ > Salient Weight Preservation": the step-size equation
+  (range over 2^b - 1 levels) and the scaling equation (w*s times x/s).
+* [AWQ-Sum]    "AWQ > Summary": "Salient weight identification" (mean absolute
+  activation) and "The scaling formula" (the exponent alpha).
+* [AWQ-Gloss]  "What is AWQ Quantization? Definition & 4-Bit Weight Compression
+  in Enterprise AI", step "INT4 Weight Packing & Export" (4-bit codes held in
+  INT32 containers).
+* [AWQ-Ref]    "AWQ (Activation-Aware Weight Quantization) - AI Glossary",
+  "Example: Where 4-bit memory saving comes from" (13e9-weight arithmetic).
+
+Readings taken where the pages are silent or disagree (each also listed in
+the design notes):
+
+* Quantiser: asymmetric min/max with a zero point [AWQ-SWP step-size equation;
+  AWQ-devto quant_config], not the symmetric max|w| form of [AWQ-devto, "Why
+  does naive 4-bit quantization wreck LLM accuracy?"].
+* Rounding is round-half-to-even; the zero point is rne(-vmin/delta), not
+  clamped; codes are clamped to [0, 2^b - 1]; a constant group gets
+  delta = max(delta, delta_floor).
+* Codes are decided in fp32 ("pinned" quantiser): every arithmetic step is done
+  in fp64 and rounded to the nearest fp32. For + - * / of fp32 operands this
+  equals the correctly rounded fp32 operation (fp64 has 53 >= 2*24 + 2 bits,
+  so the double rounding is innocuous), which is what the CUDA kernels use.
+* Scale normalisation s /= sqrt(max(s)*min(s)) is not on the pages; the
+  library applies it by specification. In exact arithmetic it leaves the
+  dequantised weight unchanged (Q(c*V) = c*Q(V) for c > 0 when the floor is
+  not hit); ``normalize=False`` turns it off.
+* Grid alpha_i = i / n_grid for i = 0..n_grid-1 (0 .. 0.95 at 20 points), and
+  the first strict minimum wins [AWQ-devto search_scale listing].
+* Packing: 8 codes per 32-bit word along the input dimension, code k of a word
+  in bits [4k, 4k+4), lowest column in the lowest nibble; scales and zeros are
+  stored as fp16 (round-to-nearest-even), one of each per group.
+"""
+from __future__ import annotations
+
+from typing import Callable, Dict, Optional
+
+import numpy as np
+
+__all__ = [
+    "f32",
+    "channel_importance",
+    "alpha_grid",
+    "awq_scales",
+    "quantize_groups",
+    "dequantize_groups",
+    "fake_quantize",
+    "output_mse",
+    "output_sq_err_sum",
+    "search_scale",
+    "pack_words",
+    "unpack_words",
+    "quantize_pack",
+    "packed_bytes",
+]
+
+
+def f32(x) -> np.ndarray:
+    """Round fp64 values to the nearest fp32 (ties to even); fp64 out."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def channel_importance(X) -> np.ndarray:
+    """Mean absolute activation of each input channel over the tokens.
+
+    [AWQ-devto, "How does AWQ decide which weights to protect?",
+    channel_importance listing; AWQ-Sum, "Salient weight identification"]
+    X: [n_tok, in]. Returns fp64 [in].
+    """
+    X = np.asarray(X, dtype=np.float64)
+    return np.abs(X).mean(axis=0)
+
+
+def alpha_grid(n_grid: int) -> np.ndarray:
+    """alpha_i = i / n_grid, i = 0..n_grid-1 [AWQ-devto, search_scale listing]."""
+    return np.array([i / n_grid for i in range(n_grid)], dtype=np.float64)
+
+
+def awq_scales(sx, alpha: float, clamp_min: float = 1e-4, normalize: bool = True) -> np.ndarray:
+    """Per-input-channel scale s = max(sx, clamp_min) ** alpha.
+
+    [AWQ-devto, search_scale listing: clamp then power; AWQ-Sum, "The scaling
+    formula": alpha sets how strongly high-activation channels are favoured.]
+    With ``normalize`` the vector is divided by sqrt(max(s) * min(s)) (library
+    specification, not on the pages).
+    """
+    base = np.maximum(np.asarray(sx, dtype=np.float64), clamp_min)
+    s = base ** float(alpha)
+    if normalize:
+        s = s / np.sqrt(s.max() * s.min())
+    return s
+
+
+def quantize_groups(
+    V,
+    w_bit: int = 4,
+    group: int = 128,
+    delta_floor: float = 1e-5,
+    pinned: bool = True,
+    round_fn: Callable[[np.ndarray], np.ndarray] = np.rint,
+):
+    """Group-wise asymmetric min/max quantisation of V [rows, in] along ``in``.
+
+    [AWQ-SWP, step-size equation: delta = (v_max - v_min) / (2^b - 1);
+    AWQ-devto quant_config: zero point on, groups of 128 along the input.]
+    Per group: delta = max((vmax - vmin) / (2^b - 1), delta_floor),
+    z = round(-vmin / delta), q = clamp(round(v / delta) + z, 0, 2^b - 1).
+    ``pinned`` rounds every step to fp32 (the precision the kernels decide
+    codes in); ``pinned=False`` is the same formula in fp64. ``round_fn`` is
+    round-half-to-even; a test may pass the identity to remove rounding.
+    Returns (q [rows, in], delta [rows, in/group], z [rows, in/group]).
+    """
+    V = np.asarray(V, dtype=np.float64)
+    rows, K = V.shape
+    if K % group:
+        raise ValueError("in_features must be a multiple of the group size")
+    r = f32 if pinned else (lambda a: np.asarray(a, dtype=np.float64))
+    qmax = float(2**w_bit - 1)
+    Vg = V.reshape(rows, K // group, group)
+    vmax = Vg.max(axis=2)
+    vmin = Vg.min(axis=2)
+    delta = r(r(vmax - vmin) / qmax)
+    delta = np.maximum(delta, r(np.float64(delta_floor)))
+    z = round_fn(r(-vmin / delta))
+    q = np.clip(round_fn(r(Vg / delta[:, :, None])) + z[:, :, None], 0.0, qmax)
+    return q.reshape(rows, K), delta, z
+
+
+def dequantize_groups(q, delta, z, group: int = 128) -> np.ndarray:
+    """(q - z) * delta per group, fp64."""
+    q = np.asarray(q, dtype=np.float64)
+    rows, K = q.shape
+    qg = q.reshape(rows, K // group, group)
+    return ((qg - z[:, :, None]) * delta[:, :, None]).reshape(rows, K)
+
+
+def fake_quantize(
+    W,
+    s,
+    w_bit: int = 4,
+    group: int = 128,
+    delta_floor: float = 1e-5,
+    pinned: bool = True,
+    round_fn: Callable[[np.ndarray], np.ndarray] = np.rint,
+) -> np.ndarray:
+    """W_hat = Q(W * s) / s: scale columns up, quantise, fold the scale back.
+
+    [AWQ-devto, search_scale listing: weight columns times s, quantize_fn,
+    then divide by s; AWQ-SWP scaling equation: w_ij*s_j times x_j/s_j keeps
+    y_i unchanged, so Q(W*s)/s is the effective weight.]
+    With ``pinned`` the scale is first rounded to fp32 and W*s is an fp32
+    product, as the kernels form it; the fold-back is fp64.
+    """
+    W = np.asarray(W, dtype=np.float64)
+    s = np.asarray(s, dtype=np.float64)
+    if pinned:
+        s = f32(s)
+        V = f32(W * s[None, :])
+    else:
+        V = W * s[None, :]
+    q, delta, z = quantize_groups(V, w_bit, group, delta_floor, pinned, round_fn)
+    return dequantize_groups(q, delta, z, group) / s[None, :]
+
+
+def output_mse(X, W, W_hat) -> float:
+    """mean((X W_hat^T - X W^T)^2) over tokens x outputs.
+
+    [AWQ-devto, search_scale listing: reference output from the unquantised
+    weight, then the squared error of the quantised layer's output, averaged.]
+    """
+    X = np.asarray(X, dtype=np.float64)
+    y_ref = X @ np.asarray(W, dtype=np.float64).T
+    y = X @ np.asarray(W_hat, dtype=np.float64).T
+    return float(np.mean((y - y_ref) ** 2))
+
+
+def output_sq_err_sum(X, W, W_hat) -> float:
+    """sum((X (W_hat - W)^T)^2): the same error, as a sum, by distributivity.
+
+    X W_hat^T - X W^T = X (W_hat - W)^T, so ``output_mse`` equals this sum over
+    n_tok * out. It takes one product instead of two, which makes full-size
+    layers affordable on the CPU; the tests pin the two forms together.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    E = np.asarray(W_hat, dtype=np.float64) - np.asarray(W, dtype=np.float64)
+    D = X @ E.T
+    return float(np.sum(D * D))
+
+
+def search_scale(
+    W,
+    X,
+    sx,
+    n_grid: int = 20,
+    clamp_min: float = 1e-4,
+    normalize: bool = True,
+    w_bit: int = 4,
+    group: int = 128,
+    delta_floor: float = 1e-5,
+    pinned: bool = True,
+    loss: Optional[Callable] = None,
+) -> Dict[str, object]:
+    """Grid search over alpha for the scale with the lowest output MSE.
+
+    [AWQ-devto, "How does AWQ protect channels without mixed precision?",
+    search_scale listing; AWQ-Sum, "Efficient algorithm": a per-layer grid
+    search over the exponent.] The first strict minimum wins.
+    Returns losses [n_grid], best_idx, best alpha, s_best (fp64) and all s.
+    """
+    loss = output_mse if loss is None else loss
+    best_err, best_i = float("inf"), -1
+    losses, scales = [], []
+    for i, alpha in enumerate(alpha_grid(n_grid)):
+        s = awq_scales(sx, alpha, clamp_min, normalize)
+        W_hat = fake_quantize(W, s, w_bit, group, delta_floor, pinned)
+        err = loss(X, W, W_hat)
+        losses.append(err)
+        scales.append(s)
+        if err < best_err:
+            best_err, best_i = err, i
+    return {
+        "losses": np.array(losses),
+        "best_idx": best_i,
+        "best_alpha": best_i / n_grid,
+        "s_best": scales[best_i],
+        "scales": np.stack(scales),
+    }
+
+
+def pack_words(q) -> np.ndarray:
+    """Pack codes [rows, in] (0..15) into int32 words [rows, in/8].
+
+    [AWQ-Gloss, "INT4 Weight Packing & Export": 4-bit codes in INT32
+    containers.] Code of column 8j+k goes to bits [4k, 4k+4) of word j.
+    """
+    q = np.asarray(q)
+    rows, K = q.shape
+    if K % 8:
+        raise ValueError("in_features must be a multiple of 8")
+    qi = q.astype(np.int64).reshape(rows, K // 8, 8)
+    if qi.min(initial=0) < 0 or qi.max(initial=0) > 15:
+        raise ValueError("codes outside [0, 15]")
+    words = np.zeros((rows, K // 8), dtype=np.int64)
+    for k in range(8):
+        words += qi[:, :, k] << (4 * k)
+    return words.astype(np.uint32).view(np.int32)
+
+
+def unpack_words(words, in_features: int) -> np.ndarray:
+    """Inverse of ``pack_words``: int32 [rows, in/8] -> codes int64 [rows, in]."""
+    w = np.asarray(words).view(np.uint32).astype(np.int64)
+    rows = w.shape[0]
+    out = np.zeros((rows, in_features // 8, 8), dtype=np.int64)
+    for k in range(8):
+        out[:, :, k] = (w >> (4 * k)) & 0xF
+    return out.reshape(rows, in_features)
+
+
+def quantize_pack(W, s, w_bit: int = 4, group: int = 128, delta_floor: float = 1e-5):
+    """Final codes of W * diag(s), packed, with fp16 group scales and zeros.
+
+    [AWQ-Gloss, "INT4 Weight Packing & Export"; AWQ-Ref, memory example: one
+    16-bit scale per group of 128; AWQ-devto quant_config: zero point on.]
+    Codes use the pinned fp32 quantiser on fl32(W * fl32(s)); the stored scale
+    is fp16(delta) and the stored zero fp16(z).
+    Returns dict(qweight int32 [out, in/8], scales fp16, zeros fp16, codes,
+    delta fp32-valued fp64, z).
+    """
+    if w_bit != 4:
+        raise ValueError("only 4-bit codes are packed")
+    W = np.asarray(W, dtype=np.float64)
+    s32 = f32(np.asarray(s, dtype=np.float64))
+    V = f32(W * s32[None, :])
+    q, delta, z = quantize_groups(V, w_bit, group, delta_floor, pinned=True)
+    return {
+        "qweight": pack_words(q),
+        "scales": delta.astype(np.float32).astype(np.float16),
+        "zeros": z.astype(np.float32).astype(np.float16),
+        "codes": q.astype(np.int64),
+        "delta": delta,
+        "z": z,
+    }
+
+
+def packed_bytes(out_features: int, in_features: int, group: int = 128, w_bit: int = 4,
+                 zero_point: bool = True) -> Dict[str, int]:
+    """Bytes of the packed layer: codes, fp16 scales, fp16 zeros.
+
+    [AWQ-Ref, "Example: Where 4-bit memory saving comes from": half a byte per
+    weight plus one 2-byte scale per group.]
+    """
+    n = out_features * in_features
+    codes = n * w_bit // 8
+    scales = (n // group) * 2
+    zeros = (n // group) * 2 if zero_point else 0
+    return {"codes": codes, "scales": scales, "zeros": zeros, "total": codes + scales + zeros}

@@ -1,0 +1,328 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test checks one part of ``oracle`` against a closed form, an invariant
+the pages state, an independent brute-force or native-fp32 restatement, or a
+printed worked example, so that a dropped term, a wrong sign or index, or a
+transposed operand in the oracle fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _small_layer(out=8, K=256, n=64, seed=3, outliers=(5, 130), factor=25.0, w_std=0.02):
+    rng = np.random.default_rng(seed)
+    W = (rng.standard_normal((out, K)) * w_std).astype(np.float32)
+    X = rng.standard_normal((n, K)).astype(np.float32)
+    for c in outliers:
+        X[:, c] *= factor
+    return W.astype(np.float64), workloads.round_to_bf16(X).astype(np.float64)
+
+
+# ---------------------------------------------------------------- rounding helpers
+
+
+def test_f32_rounds_ties_to_even():
+    one = 1.0
+    ulp = 2.0**-23
+    assert O.f32(one + ulp / 2) == one  # tie -> even (1.0)
+    assert O.f32(one + 1.5 * ulp) == one + 2 * ulp  # tie -> even mantissa
+    assert O.f32(one + 0.75 * ulp) == one + ulp
+    assert O.f32(-(one + ulp / 2)) == -one
+
+
+def test_fp16_storage_rounds_ties_to_even():
+    # 1 + 2^-11 is halfway between fp16 1.0 and 1 + 2^-10: ties go to 1.0.
+    vals = np.array([1 + 2.0**-11, 1 + 3 * 2.0**-11, 2.0**-20, 65504.0, 3.0], dtype=np.float32)
+    h = vals.astype(np.float16).astype(np.float64)
+    assert h[0] == 1.0
+    assert h[1] == 1 + 2 * 2.0**-10
+    assert h[2] == 2.0**-20  # fp16 subnormal, exact
+    assert h[3] == 65504.0
+    assert h[4] == 3.0
+
+
+# ---------------------------------------------------------------- statistics
+
+
+def test_channel_importance_brute_force():
+    rng = np.random.default_rng(0)
+    X = rng.standard_normal((5, 7))
+    got = O.channel_importance(X)
+    for j in range(7):
+        acc = 0.0
+        for t in range(5):
+            acc += abs(float(X[t, j]))
+        assert got[j] == pytest.approx(acc / 5, rel=1e-15)
+
+
+def test_alpha_grid_endpoints():
+    g = O.alpha_grid(20)
+    assert len(g) == 20 and g[0] == 0.0 and g[-1] == pytest.approx(0.95)
+    assert np.all(np.diff(g) > 0)
+
+
+def test_alpha_zero_gives_unit_scale_exactly():
+    sx = np.array([1e-7, 0.3, 7.0, 55.0])
+    for norm in (False, True):
+        s = O.awq_scales(sx, 0.0, normalize=norm)
+        assert np.all(s == 1.0)
+
+
+def test_scale_clamp_and_power_closed_form():
+    sx = np.array([1e-6, 0.5, 2.0, 40.0])
+    s = O.awq_scales(sx, 0.5, normalize=False)
+    expect = np.sqrt(np.array([1e-4, 0.5, 2.0, 40.0]))
+    np.testing.assert_allclose(s, expect, rtol=1e-15)
+    sn = O.awq_scales(sx, 0.5, normalize=True)
+    c = math.sqrt(expect.max() * expect.min())
+    np.testing.assert_allclose(sn, expect / c, rtol=1e-15)
+    assert sn.max() * sn.min() == pytest.approx(1.0, rel=1e-14)
+
+
+# ---------------------------------------------------------------- quantiser
+
+
+def _native_fp32_rtn_group(vals, floor=np.float32(1e-5)):
+    """Independent per-group asymmetric RTN in native fp32 scalar arithmetic."""
+    v = [np.float32(x) for x in vals]
+    hi, lo = max(v), min(v)
+    d = np.float32(np.float32(hi - lo) / np.float32(15.0))
+    if d < floor:
+        d = floor
+    z = np.float32(np.rint(np.float32(-lo / d)))
+    codes = []
+    for x in v:
+        c = np.float32(np.rint(np.float32(x / d))) + z
+        codes.append(min(max(float(c), 0.0), 15.0))
+    return codes, float(d), float(z)
+
+
+def test_alpha_zero_is_plain_rtn_native_fp32():
+    """alpha = 0 gives s = 1, so the search's quantiser is plain group RTN."""
+    W, X = _small_layer(out=6, K=256)
+    s = O.awq_scales(O.channel_importance(X), 0.0)
+    W_hat = O.fake_quantize(W, s)
+    for r in range(W.shape[0]):
+        for g in range(W.shape[1] // 128):
+            vals = W[r, g * 128:(g + 1) * 128]
+            codes, d, z = _native_fp32_rtn_group(vals)
+            expect = [(c - z) * d for c in codes]
+            np.testing.assert_array_equal(W_hat[r, g * 128:(g + 1) * 128], expect)
+
+
+def test_pinned_quantizer_matches_native_fp32_with_scales():
+    W, X = _small_layer(out=6, K=256, seed=11)
+    sx = O.channel_importance(X)
+    for alpha in (0.25, 0.6, 0.95):
+        s32 = O.f32(O.awq_scales(sx, alpha))
+        V = O.f32(W * s32[None, :])
+        q, d, z = O.quantize_groups(V)
+        for r in range(W.shape[0]):
+            for g in range(2):
+                vals = [np.float32(W[r, k]) * np.float32(s32[k]) for k in range(g * 128, (g + 1) * 128)]
+                codes, dn, zn = _native_fp32_rtn_group(vals)
+                assert d[r, g] == dn and z[r, g] == zn
+                np.testing.assert_array_equal(q[r, g * 128:(g + 1) * 128], codes)
+
+
+def test_scaling_cancels_without_rounding():
+    """Scaling identity: with rounding removed, Q(W*s)/s gives back W."""
+    W, X = _small_layer(out=5, K=256, seed=4)
+    sx = O.channel_importance(X)
+    ident = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    for alpha in (0.0, 0.3, 0.9):
+        s = O.awq_scales(sx, alpha)
+        W_hat = O.fake_quantize(W, s, pinned=False, round_fn=ident)
+        np.testing.assert_allclose(W_hat, W, rtol=1e-12, atol=1e-15)
+        # pinned (fp32) steps leave only fp32-rounding residue
+        W_hat32 = O.fake_quantize(W, s, pinned=True, round_fn=ident)
+        np.testing.assert_allclose(W_hat32, W, rtol=0, atol=1e-6 * np.abs(W).max())
+
+
+def test_error_at_most_half_a_step_and_codes_in_range():
+    W, X = _small_layer(out=16, K=384, seed=5)
+    sx = O.channel_importance(X)
+    for alpha in O.alpha_grid(20):
+        s32 = O.f32(O.awq_scales(sx, alpha))
+        V = O.f32(W * s32[None, :])
+        q, d, z = O.quantize_groups(V, group=128)
+        assert q.min() >= 0 and q.max() <= 15
+        assert np.all(z == np.round(z))
+        assert np.all(q == np.round(q))
+        dq = O.dequantize_groups(q, d, z, 128)
+        err = np.abs(V - dq).reshape(16, 3, 128)
+        bound = d[:, :, None] * (0.5 + 1e-5)
+        assert np.all(err <= bound)
+
+
+def test_hand_built_groups():
+    # all-zero group: delta hits the floor, zero point 0, codes 0, exact zeros back
+    V = np.zeros((1, 128))
+    q, d, z = O.quantize_groups(V)
+    assert d[0, 0] == O.f32(1e-5) and z[0, 0] == 0 and np.all(q == 0)
+    # exact ties: range [0, 15] gives delta = 1, z = 0; 2.5 -> 2, 3.5 -> 4 (half to even)
+    vals = np.zeros(128)
+    vals[1] = 15.0
+    vals[2] = 2.5
+    vals[3] = 3.5
+    vals[4] = 0.5
+    q, d, z = O.quantize_groups(vals[None, :])
+    assert d[0, 0] == 1.0 and z[0, 0] == 0.0
+    assert q[0, 1] == 15 and q[0, 2] == 2 and q[0, 3] == 4 and q[0, 4] == 0
+    # one-sign group: all positive, so the zero point is negative; codes still in range
+    vals = np.linspace(1.0, 2.0, 128)
+    q, d, z = O.quantize_groups(vals[None, :])
+    assert z[0, 0] < 0 and q.min() == 0 and q.max() == 15
+    dq = O.dequantize_groups(q, d, z)
+    assert np.all(np.abs(dq - vals) <= d[0, 0] * 0.5 * (1 + 1e-6))
+    # constant nonzero group: floor step, value recovered to within half a step
+    vals = np.full(128, 0.02)
+    q, d, z = O.quantize_groups(vals[None, :])
+    dq = O.dequantize_groups(q, d, z)
+    assert np.all(np.abs(dq - 0.02) <= d[0, 0] * 0.5)
+
+
+# ---------------------------------------------------------------- loss and search
+
+
+def test_loss_brute_force_tiny():
+    rng = np.random.default_rng(9)
+    X = rng.standard_normal((3, 128))
+    W = rng.standard_normal((4, 128)) * 0.02
+    W_hat = O.fake_quantize(W, np.ones(128))
+    acc = 0.0
+    for t in range(3):
+        for r in range(4):
+            y = sum(X[t, k] * W_hat[r, k] for k in range(128))
+            y0 = sum(X[t, k] * W[r, k] for k in range(128))
+            acc += (y - y0) ** 2
+    assert O.output_mse(X, W, W_hat) == pytest.approx(acc / 12, rel=1e-10)
+
+
+def test_literal_and_residual_loss_forms_agree():
+    L = workloads.make_layer("tiny")
+    W, X = L["W"].astype(np.float64), L["X"].astype(np.float64)
+    sx = O.channel_importance(X)
+    for alpha in (0.0, 0.5, 0.95):
+        W_hat = O.fake_quantize(W, O.awq_scales(sx, alpha))
+        a = O.output_mse(X, W, W_hat)
+        b = O.output_sq_err_sum(X, W, W_hat) / (X.shape[0] * W.shape[0])
+        assert a == pytest.approx(b, rel=1e-12)
+
+
+def test_normalisation_leaves_losses_unchanged():
+    W, X = _small_layer(out=8, K=256, seed=6)
+    sx = O.channel_importance(X)
+    a = O.search_scale(W, X, sx, normalize=True, pinned=False)
+    b = O.search_scale(W, X, sx, normalize=False, pinned=False)
+    np.testing.assert_allclose(a["losses"], b["losses"], rtol=1e-10)
+    assert a["best_idx"] == b["best_idx"]
+    # the pinned (fp32) quantiser moves at most a few codes at rounding ties
+    c = O.search_scale(W, X, sx, normalize=True, pinned=True)
+    d = O.search_scale(W, X, sx, normalize=False, pinned=True)
+    np.testing.assert_allclose(c["losses"], d["losses"], rtol=1e-3)
+
+
+def test_search_beats_rtn_with_interior_optimum():
+    L = workloads.make_layer("tiny")
+    W, X = L["W"].astype(np.float64), L["X"].astype(np.float64)
+    res = O.search_scale(W, X, O.channel_importance(X))
+    losses = res["losses"]
+    assert losses[res["best_idx"]] == losses.min()
+    assert res["best_idx"] > 0 and losses.min() < 0.9 * losses[0]
+    assert res["best_idx"] == int(np.argmin(losses))
+
+
+def test_first_strict_minimum_wins():
+    W, X = _small_layer(out=2, K=128, n=8, outliers=(5, 70))
+    res = O.search_scale(W, X, O.channel_importance(X), n_grid=5, loss=lambda X, W, Wh: 1.0)
+    assert res["best_idx"] == 0
+    vals = iter([3.0, 2.0, 1.0, 1.0, 5.0])
+    res = O.search_scale(W, X, O.channel_importance(X), n_grid=5, loss=lambda X, W, Wh: next(vals))
+    assert res["best_idx"] == 2
+
+
+def test_activation_salience_beats_weight_salience():
+    """Protecting the high-activation channel lowers output error more than
+    protecting the largest-weight channel, and the best single channel to
+    protect is an activation outlier (AWQ-devto, "How does AWQ decide which
+    weights to protect?")."""
+    rng = np.random.default_rng(21)
+    out, K, n = 8, 128, 64
+    W = rng.standard_normal((out, K)) * 0.02
+    X = rng.standard_normal((n, K))
+    act_out = [17, 90]
+    X[:, act_out] *= 30.0
+    big_w = 40  # a channel with large weights but ordinary activations
+    W[:, big_w] *= 4.0
+
+    def mse_protect(j, k):
+        s = np.ones(K)
+        s[j] = k
+        return O.output_mse(X, W, O.fake_quantize(W, s, pinned=False))
+
+    base = O.output_mse(X, W, O.fake_quantize(W, np.ones(K), pinned=False))
+    best = {}
+    for j in range(K):
+        best[j] = min(mse_protect(j, k) for k in (1.0, 2.0, 4.0, 8.0))
+    j_star = min(best, key=best.get)
+    assert j_star in act_out
+    act_rank = np.argsort(-np.abs(X).mean(axis=0))[0]
+    w_rank = np.argsort(-np.abs(W).mean(axis=0))[0]
+    assert act_rank in act_out and w_rank == big_w
+    assert best[act_rank] < best[w_rank] and best[act_rank] < base
+
+
+# ---------------------------------------------------------------- packing
+
+
+def test_pack_nibble_order_golden():
+    cases = json.load(open(os.path.join(GOLDEN, "pack_order.json")))["cases"]
+    for c in cases:
+        w = O.pack_words(np.array([c["codes"]]))
+        assert int(w.view(np.uint32)[0, 0]) == int(c["word_hex"], 16)
+
+
+def test_pack_roundtrip_and_dequant_bound():
+    W, X = _small_layer(out=9, K=256, seed=8)
+    s = O.awq_scales(O.channel_importance(X), 0.55)
+    p = O.quantize_pack(W, s)
+    assert p["qweight"].dtype == np.int32 and p["qweight"].shape == (9, 32)
+    np.testing.assert_array_equal(O.unpack_words(p["qweight"], 256), p["codes"])
+    V = O.f32(W * O.f32(s)[None, :])
+    sc = p["scales"].astype(np.float64)
+    zz = p["zeros"].astype(np.float64)
+    dq = O.dequantize_groups(p["codes"], sc, zz)
+    delta = p["delta"]
+    bound = (delta * 0.5 + delta * 2.0**-11 * 15)[:, :, None]
+    assert np.all(np.abs(V - dq).reshape(9, 2, 128) <= bound * (1 + 1e-6))
+
+
+def test_memory_arithmetic_13b_golden():
+    g = json.load(open(os.path.join(GOLDEN, "memory_13b.json")))
+    rows = g["weights"] // g["group"]
+    b = O.packed_bytes(rows, g["group"], group=g["group"])
+    assert rows * g["group"] * 2 == g["fp16_bytes"]
+    assert b["codes"] == g["int4_code_bytes"]
+    assert b["scales"] == pytest.approx(g["scale_bytes_approx"], rel=0.02)
+    assert b["codes"] + b["scales"] == pytest.approx(g["total_approx"], rel=0.005)
+    assert b["zeros"] == b["scales"]
+
+
+def test_generator_is_deterministic():
+    a = workloads.make_layer("tiny")
+    b = workloads.make_layer("tiny")
+    np.testing.assert_array_equal(a["W"], b["W"])
+    np.testing.assert_array_equal(a["X"], b["X"])
+    assert len(a["outlier_channels"]) == 3
+    # bf16-exact activations
+    workloads.bf16_bits(a["X"])
