@@ -1,0 +1,433 @@
+"""Benchmark: AWQ per-layer search + INT4 pack on B300, one JSON line.
+
+A step is one pass of the whole path over one synthetic layer, through the C
+ABI: activation statistics, the 20-point alpha search (scales, fake-quant,
+tcgen05 search product with fused squared-error epilogue, loss + argmin) and
+the final pack. Inputs are resident in HBM when the timed region starts; L2
+is flushed (a 512 MiB write) between steps, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, bounded sample
+
+With N > 1 (torchrun) every rank quantises its own copy of the layer
+(independent layers, no collective on the data path); value is the job's
+milliseconds per layer = max-over-ranks time / layers processed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ms per layer AWQ search+pack (20-pt α grid); % BF16 TC peak and % HBM BW"
+DEFAULT_WORKLOAD = "llama7b_q_proj"
+KERNELS_PER_STEP = 7  # stats partial+finalize, alpha scales, fake-quant, search product, loss select, pack
+FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["post_bit_weight_awq_b300/csrc/awq_search_gemm.cu", "post_bit_weight_awq_b300/csrc/awq_device.cuh"]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the search kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "search_gemm_kernel.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch\s*=\s*(\d+).*?workload\s*=\s*(\w+).*?source_sha256_16\s*=\s*(\w+)",
+                  text, flags=re.S)
+    if not m:
+        return None
+    if m.group(2) != workload or m.group(3) != source_digest(GEMM_SOURCES):
+        return None
+    return int(m.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out_path = os.path.join("/tmp", f"awq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.out_path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.out_path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.out_path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ------------------------------------------------------------------ oracle arm
+
+
+def oracle_layer(workload):
+    import workloads
+
+    return workloads.make_layer(workloads.WORKLOADS[workload][0])
+
+
+def oracle_sample(L, rows):
+    """Run the oracle's statistics, search and pack on the first ``rows``
+    output rows of layer ``L`` (all tokens, all input channels). Returns the
+    seconds taken and the factor that scales the sample to the whole layer."""
+    import numpy as np
+
+    import oracle as O
+
+    W = L["W"][:rows].astype(np.float64)
+    X = L["X"].astype(np.float64)
+    N = L["W"].shape[0]
+    t0 = time.perf_counter()
+    sx = O.channel_importance(X)
+    res = O.search_scale(W, X, sx)
+    O.quantize_pack(W, O.f32(res["s_best"]))
+    dt = time.perf_counter() - t0
+    return dt, N / rows
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        return max((p.get("num_threads", 1) for p in threadpool_info()), default=1)
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+def reference_arm(args, rank):
+    if rank != 0:
+        return
+    rows = args.oracle_rows
+    L = oracle_layer(args.workload)
+    for _ in range(args.warmup):
+        oracle_sample(L, rows)
+    times = []
+    scale = 1.0
+    for _ in range(args.steps):
+        dt, scale = oracle_sample(L, rows)
+        times.append(dt * scale * 1e3)
+    ms = statistics.mean(times)
+    cores = blas_threads()
+    sample = (f"oracle statistics+search+pack on output rows [0,{rows}) of the layer (all tokens), "
+              f"time scaled by out/rows = {scale:g} to one layer")
+    line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "n_grid": 20, "group": 128},
+            "cpu_baseline": {"value": ms, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import workloads
+    from post_bit_weight_awq_b300 import build, capi
+
+    build.build()
+    capi.lib()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    name = workloads.WORKLOADS[args.workload][0]
+    L = workloads.make_layer(name)
+    W32, X32 = L["W"], L["X"]
+    N, K = W32.shape
+    n = X32.shape[0]
+    cfg = capi.config()
+    G = cfg.n_grid
+
+    def to_dev_bf16(a):
+        return torch.from_numpy(workloads.bf16_bits(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    Wd = to_dev_bf16(W32) if L["w_dtype"] == "bf16" else torch.from_numpy(W32).to(dev)
+    Xd = to_dev_bf16(X32)
+    f32, i32, u8 = torch.float32, torch.int32, torch.uint8
+    mean_abs = torch.empty(K, dtype=f32, device=dev)
+    stats_ws = torch.empty(capi.awq_act_stats_workspace_size(n, K), dtype=u8, device=dev)
+    s = torch.empty(G, K, dtype=f32, device=dev)
+    inv = torch.empty_like(s)
+    op = torch.empty(G, N, K, dtype=torch.bfloat16, device=dev)
+    mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
+    parts = torch.empty(G, mt, nt, 4, dtype=f32, device=dev)
+    status = torch.zeros(4, dtype=i32, device=dev)
+    losses = torch.empty(G, dtype=f32, device=dev)
+    best = torch.empty(1, dtype=i32, device=dev)
+    s_best = torch.empty(K, dtype=f32, device=dev)
+    qw = torch.empty(N, K // 8, dtype=i32, device=dev)
+    sc = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+    zr = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=u8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        # the same kernels, in the same order, as awq_act_stats + awq_search_layer + awq_quantize_pack
+        if ev:
+            ev[0].record(stream)
+        capi.awq_act_stats(Xd, mean_abs, stats_ws, stream)
+        if ev:
+            ev[1].record(stream)
+        capi.awq_alpha_scales(mean_abs, cfg, s, inv, stream)
+        if ev:
+            ev[2].record(stream)
+        capi.awq_fakequant(Wd, s, inv, cfg, op, stream)
+        if ev:
+            ev[3].record(stream)
+        capi.awq_search_gemm(Xd, op, cfg, parts, status, stream, n_tok=n, in_features=K, out_features=N)
+        if ev:
+            ev[4].record(stream)
+        capi.awq_loss_select(parts, s, cfg, losses, best, s_best, status, stream, n_tok=n, out_features=N,
+                             in_features=K)
+        if ev:
+            ev[5].record(stream)
+        capi.awq_quantize_pack(Wd, s_best, cfg, qw, sc, zr, stream)
+        if ev:
+            ev[6].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0, capi.status_string(int(status[0]))
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        step(events[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    if int(status[0]) != 0:
+        raise RuntimeError("device status " + capi.status_string(int(status[0])))
+
+    stage_names = ["stats", "alpha_scales", "fakequant", "search_gemm", "loss_select", "pack"]
+    per_stage = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in events) for i, nm in enumerate(stage_names)}
+    step_ms = [e[0].elapsed_time(e[6]) for e in events]
+    ms_step = statistics.mean(step_ms)
+    t_total = sum(step_ms)
+    if dist:
+        tt = torch.tensor([t_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_total = float(tt.item())
+    layers = args.steps * world
+    value = t_total / layers
+
+    # ---------------------------------------------------------- end to end (host buffers)
+    pin = dict(pin_memory=True)
+    Wh = (torch.from_numpy(workloads.bf16_bits(W32).view(np.int16)).view(torch.bfloat16) if L["w_dtype"] == "bf16"
+          else torch.from_numpy(W32)).clone().pin_memory()
+    Xh = torch.from_numpy(workloads.bf16_bits(X32).view(np.int16)).view(torch.bfloat16).clone().pin_memory()
+    outs_h = {"qweight": torch.empty(N, K // 8, dtype=i32, **pin), "scales": torch.empty(N, K // 128,
+                                                                                      dtype=torch.float16, **pin),
+              "zeros": torch.empty(N, K // 128, dtype=torch.float16, **pin), "losses": torch.empty(G, dtype=f32, **pin),
+              "best_idx": torch.empty(1, dtype=i32, **pin), "s_best": torch.empty(K, dtype=f32, **pin)}
+    search_ws = torch.empty(max(capi.awq_workspace_size(n, N, K, cfg), stats_ws.numel()), dtype=u8, device=dev)
+    del op
+    W_in = torch.empty_like(Wd)
+    X_in = torch.empty_like(Xd)
+    h2d = Wh.numel() * Wh.element_size() + Xh.numel() * Xh.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+
+    def e2e_step():
+        W_in.copy_(Wh, non_blocking=True)
+        X_in.copy_(Xh, non_blocking=True)
+        capi.awq_act_stats(X_in, mean_abs, search_ws, stream)
+        capi.awq_search_layer(W_in, X_in, mean_abs, cfg, losses, best, s_best, search_ws, stream)
+        capi.awq_quantize_pack(W_in, s_best, cfg, qw, sc, zr, stream)
+        outs_h["qweight"].copy_(qw, non_blocking=True)
+        outs_h["scales"].copy_(sc, non_blocking=True)
+        outs_h["zeros"].copy_(zr, non_blocking=True)
+        outs_h["losses"].copy_(losses, non_blocking=True)
+        outs_h["best_idx"].copy_(best, non_blocking=True)
+        outs_h["s_best"].copy_(s_best, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        ee[k][0].record(stream)
+        e2e_step()
+        ee[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in ee)
+    if dist:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item()) / world
+    assert capi.awq_get_device_status(search_ws, stream) == capi.AWQ_OK
+
+    # ---------------------------------------------------------- parity spot check vs stored oracle losses
+    parity = None
+    gpath = os.path.join(ROOT, "tests", "golden", "oracle_losses.json")
+    if os.path.exists(gpath):
+        g = json.load(open(gpath)).get(name)
+        if g:
+            lo = np.array(g["losses"])
+            lg = outs_h["losses"].numpy().astype(np.float64)
+            parity = {"max_rel_loss_err": float(np.max(np.abs(lg - lo) / lo)),
+                      "gpu_best_idx": int(outs_h["best_idx"][0]), "oracle_best_idx": g["best_idx"],
+                      "oracle_loss_at_gpu_best_over_min": float(lo[int(outs_h["best_idx"][0])] / lo.min())}
+
+    if dist:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    pk = peaks()
+    flops = G * 2.0 * n * K * N
+    gemm_ms = per_stage["search_gemm"]
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    traffic = profiled_traffic(args.workload)
+    wbytes = 2 if L["w_dtype"] == "bf16" else 4
+    hbm_bytes = {
+        "stats": 2.0 * n * K,
+        "fakequant": wbytes * N * K + G * 2.0 * N * K,
+        "pack": wbytes * N * K + N * K / 2 + 4.0 * N * K / 128,
+    }
+    stages = {}
+    for nm, ms in per_stage.items():
+        d = {"ms": round(ms, 4)}
+        if nm in hbm_bytes:
+            gbs = hbm_bytes[nm] / (ms * 1e-3) / 1e9
+            d.update({"gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)})
+        if nm == "search_gemm":
+            d.update({"tflops": round(achieved, 1), "frac_bf16_burst": round(achieved / pk["bf16_tflops"], 3)})
+            if pk.get("bf16_tflops_sustained"):
+                d["frac_bf16_sustained"] = round(achieved / pk["bf16_tflops_sustained"], 3)
+        stages[nm] = d
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        dt, scale = oracle_sample(L, args.oracle_rows)
+        cpu = {"value": dt * scale * 1e3, "unit": "ms", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"oracle search+pack on output rows [0,{args.oracle_rows}) of the layer (all tokens), "
+                         f"{dt:.1f} s, scaled by out/rows = {scale:g} to one layer"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "layer": name, "W": [N, K], "X": [n, K], "w_dtype": L["w_dtype"],
+                   "n_grid": G, "group": 128, "loss_form": "residual", "parallelism": f"replicas{world}",
+                   "l2": "flushed between steps (512 MiB write outside the timed events)"},
+        "roofline": {"bound": "tensor", "kernel": "search_gemm_kernel", "achieved": round(achieved, 1),
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 3),
+                     "traffic": traffic, "peak_source": f"{pk['source']} bf16 burst",
+                     "algorithmic_flops_per_launch": flops},
+        "stages": stages,
+        "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+        "parity_vs_oracle": parity,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--oracle-rows", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    gpu_arm(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+/*
+ * awq.h - C ABI of the B300 (sm_103a) AWQ per-layer scale search and INT4 pack.
+ *
+ * What the library computes, for one linear layer with weights W[out, in] and
+ * calibration activations X[n_tok, in]:
+ *
+ *   1. sx[j]   = mean_t |X[t, j]|                               (awq_act_stats)
+ *   2. for alpha_i = i / n_grid, i = 0 .. n_grid-1:
+ *        s_i[j]  = max(sx[j], sx_clamp_min) ^ alpha_i, optionally divided by
+ *                  sqrt(max_j s_i * min_j s_i)
+ *        W_hat_i = Q(W * diag(s_i)) * diag(1 / s_i)
+ *        L_i     = mean over (t, r) of (X W_hat_i^T - X W^T)[t, r]^2
+ *      best = first i with the smallest L_i                     (awq_search_layer)
+ *   3. codes of W * diag(s_best) packed 8 per int32, fp16 group scales and
+ *      fp16 zero points                                         (awq_quantize_pack)
+ *
+ * Q is group-wise asymmetric min/max quantisation along `in` (groups of
+ * `group` weights): delta = max((vmax - vmin) / (2^w_bit - 1), delta_floor),
+ * z = rne(-vmin / delta), q = clamp(rne(v / delta) + z, 0, 2^w_bit - 1),
+ * dequantised value (q - z) * delta. Codes are decided in fp32 with correctly
+ * rounded operations in exactly that order; rne is round-half-to-even.
+ *
+ * Sources (web pages on AWQ, by title and section):
+ *   - "AWQ: How Activation-Aware Quantization Saves 4-bit LLMs":
+ *     "How does AWQ decide which weights to protect?" (mean |x| per input
+ *     channel), "How does AWQ protect channels without mixed precision?" (the
+ *     alpha grid search over s = sx^alpha against the output MSE of the
+ *     unquantised layer), and the deployment quant_config (4 bits, groups of
+ *     128, zero point on).
+ *   - "AWQ > Salient Weight Preservation": the step-size equation (range over
+ *     2^b - 1 levels) and the scaling equation (w*s times x/s leaves y alone).
+ *   - "AWQ > Summary": "The scaling formula" (alpha) and "Salient weight
+ *     identification" (mean absolute activation).
+ *   - "What is AWQ Quantization? Definition & 4-Bit Weight Compression in
+ *     Enterprise AI", step "INT4 Weight Packing & Export" (INT32 containers).
+ *   - "AWQ (Activation-Aware Weight Quantization) - AI Glossary", "Example:
+ *     Where 4-bit memory saving comes from" (one 16-bit scale per 128 weights).
+ *   The normalisation by sqrt(max * min) is not on the pages; it is part of
+ *   this library's specification and, in exact arithmetic, does not change
+ *   W_hat_i.
+ *
+ * Conventions for every call below:
+ *   - Pointers named X, W, s, mean_abs, losses, ... are DEVICE pointers unless
+ *     the comment says host. The caller owns every buffer; the library
+ *     allocates no device memory. Scratch memory comes from the caller through
+ *     `ws` / `ws_bytes`, sized with the *_workspace_size queries.
+ *   - Matrices are dense row-major: X[n_tok][in], W[out][in]; `in` is the
+ *     contiguous dimension. Device pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). Argument errors are detected on the host and returned
+ *     before anything is launched. Launch failures return AWQ_ERR_CUDA.
+ *     Conditions found on the device (a bounded wait that ran out, a
+ *     non-finite loss) are written to a device status word; read it with
+ *     awq_get_device_status, which synchronises the stream.
+ *   - Shapes: in % group == 0, group % 8 == 0 (group == 128 in this build),
+ *     w_bit == 4, zero_point == 1, 1 <= n_grid <= 64. n_tok and out are
+ *     arbitrary (>= 1); the loss divides by the true n_tok * out.
+ *   - The codes quantise W * diag(s): the caller folds 1/s into whatever
+ *     produces X (for a transformer, the preceding LayerNorm/RMSNorm weight,
+ *     as "AWQ > Salient Weight Preservation" describes). s_best is returned
+ *     for that purpose.
+ */
+#ifndef AWQ_B300_H
+#define AWQ_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define AWQ_API __attribute__((visibility("default")))
+#else
+#define AWQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t, declared here so the header needs no CUDA
+   include. */
+typedef struct CUstream_st* awq_stream_t;
+
+typedef enum {
+  AWQ_OK = 0,
+  AWQ_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad config */
+  AWQ_ERR_UNSUPPORTED = 2, /* valid but not built: w_bit != 4, group != 128 ... */
+  AWQ_ERR_MISALIGNED = 3,  /* a device pointer is not 16-byte aligned */
+  AWQ_ERR_WORKSPACE = 4,   /* ws_bytes below the size the query returns */
+  AWQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+  AWQ_ERR_TIMEOUT = 6,     /* device: a bounded wait ran out; results invalid */
+  AWQ_ERR_NONFINITE = 7    /* device: a loss was NaN or Inf */
+} awq_status;
+
+typedef enum { AWQ_BF16 = 0, AWQ_FP32 = 1 } awq_dtype;
+
+/* How the search scores each alpha. Both give the same number in exact
+   arithmetic, since X W_hat^T - X W^T = X (W_hat - W)^T.
+   RESIDUAL:  one bf16 product per alpha, X (W_hat - W)^T, squared and summed
+              in the GEMM epilogue (default, fastest).
+   REFERENCE: the output X W^T of the unquantised weight is computed once per
+              output tile, kept resident in tensor memory, and subtracted from
+              X W_hat^T in the epilogue, as the search_scale listing of the
+              first page writes it. */
+typedef enum { AWQ_LOSS_RESIDUAL = 0, AWQ_LOSS_REFERENCE = 1 } awq_loss_form;
+
+typedef struct {
+  int32_t w_bit;            /* 4 */
+  int32_t group;            /* 128: weights per scale/zero along `in` */
+  int32_t n_grid;           /* 20: alpha_i = i / n_grid, i < n_grid */
+  int32_t zero_point;       /* 1: asymmetric with zero point (only mode built) */
+  int32_t normalize;        /* 1: divide s by sqrt(max(s) * min(s)) */
+  float sx_clamp_min;       /* 1e-4: sx is clamped from below before the power */
+  float delta_floor;        /* 1e-5: lower bound of a group's step */
+  int32_t loss_form;        /* awq_loss_form */
+  uint32_t wait_timeout_ms; /* bound of each device-side wait; 0 = 2000 ms */
+} awq_config;
+
+/* Fill `cfg` with the defaults above. */
+AWQ_API void awq_config_default(awq_config* cfg);
+
+/* Static, NUL-terminated description of a status; never NULL. */
+AWQ_API const char* awq_status_string(int status);
+
+/* ---------------------------------------------------------------- step 1 */
+
+/* Device bytes of scratch that awq_act_stats needs for (n_tok, in). Host-only.
+   Returns AWQ_ERR_INVALID_ARG for non-positive sizes or a NULL `bytes`. */
+AWQ_API awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_t* bytes);
+
+/* mean_abs[j] = (1/n_tok) sum_t |X[t, j]|  (fp32 out, fp32 partial sums over
+   blocks of tokens, fp64 across blocks, fixed order: deterministic).
+   X: device bf16 [n_tok][in] (x_dtype must be AWQ_BF16). in % 8 == 0.
+   mean_abs: device fp32 [in]. ws: device scratch of at least the queried
+   size. Source: "AWQ: How Activation-Aware Quantization Saves 4-bit LLMs",
+   "How does AWQ decide which weights to protect?"; "AWQ > Summary",
+   "Salient weight identification". */
+AWQ_API awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, int64_t in,
+                         float* mean_abs, void* ws, size_t ws_bytes, awq_stream_t stream);
+
+/* ---------------------------------------------------------------- step 2 */
+
+/* Device bytes of scratch that awq_search_layer needs. Host-only. It holds a
+   status word, s and 1/s for every alpha ([n_grid][in] fp32 each), the bf16
+   search operand for every alpha ([n_grid (+1 in REFERENCE form)][out][in]),
+   and the per-tile partial sums. */
+AWQ_API awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, const awq_config* cfg,
+                              size_t* bytes);
+
+/* The alpha grid search of "AWQ: How Activation-Aware Quantization Saves
+   4-bit LLMs", "How does AWQ protect channels without mixed precision?"
+   (search_scale listing), with the quantiser above.
+   W: device [out][in], w_dtype AWQ_BF16 or AWQ_FP32. X: device bf16
+   [n_tok][in] (x_dtype AWQ_BF16). mean_abs: device fp32 [in] (from step 1).
+   losses: device fp32 [n_grid], the mean squared output error per alpha.
+   best_idx: device int32 [1], first index of the smallest loss.
+   s_best: device fp32 [in], s of that alpha (fold 1/s_best into X's producer).
+   ws/ws_bytes: scratch, at least awq_workspace_size(); its first 4 bytes are
+   the device status word read by awq_get_device_status.
+   The products run on bf16 tensor cores with fp32 accumulation; the step-2
+   output matrix never leaves the chip. */
+AWQ_API awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t in,
+                            const void* X, int32_t x_dtype, int64_t n_tok, const float* mean_abs,
+                            const awq_config* cfg, float* losses, int32_t* best_idx,
+                            float* s_best, void* ws, size_t ws_bytes, awq_stream_t stream);
+
+/* ---------------------------------------------------------------- step 3 */
+
+/* Final INT4 codes of W * diag(s) with the quantiser above, bit-exact with
+   respect to fp32 arithmetic ("What is AWQ Quantization? ...", "INT4 Weight
+   Packing & Export"; "AWQ (Activation-Aware Weight Quantization) - AI
+   Glossary", memory example).
+   W: device [out][in] (AWQ_BF16 or AWQ_FP32). s: device fp32 [in].
+   qweight: device int32 [out][in/8]; the code of column 8j+k sits in bits
+   [4k, 4k+4) of word j. scales_f16 / zeros_f16: device fp16 bit patterns
+   [out][in/group] holding fp16(delta) and fp16(z), round-to-nearest-even.
+   Needs no scratch. */
+AWQ_API awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out, int64_t in,
+                             const float* s, const awq_config* cfg, int32_t* qweight,
+                             uint16_t* scales_f16, uint16_t* zeros_f16, awq_stream_t stream);
+
+/* Bytes of the packed layer (codes + scales + zeros), host-only; 0 for
+   invalid arguments. */
+AWQ_API size_t awq_packed_bytes(int64_t out, int64_t in, const awq_config* cfg);
+
+/* Synchronise `stream`, read the status word at the start of `ws` (device)
+   into *status (host) and clear it. Returns AWQ_ERR_CUDA if the copy fails. */
+AWQ_API awq_status awq_get_device_status(const void* ws, awq_stream_t stream, awq_status* status);
+
+/* ------------------------------------------- stages of step 2, one by one
+   awq_search_layer runs exactly these four in this order on its workspace.
+   They are exported so that each kernel can be timed and checked alone. */
+
+/* s[i][j] and inv_s[i][j] = 1/s[i][j] for every alpha_i (device fp32
+   [n_grid][in]); the scale law of the search_scale listing and "AWQ >
+   Summary", "The scaling formula". */
+AWQ_API awq_status awq_alpha_scales(const float* mean_abs, int64_t in, const awq_config* cfg, float* s,
+                            float* inv_s, awq_stream_t stream);
+
+/* For every alpha_i: W_hat_i = Q(W * s_i) * inv_s_i. RESIDUAL form writes
+   bf16(W_hat_i - W) to op[i]; REFERENCE form writes bf16(W_hat_i) to op[i]
+   and bf16(W) to op[n_grid]. op: device bf16 bits [n_slots][out][in]. */
+AWQ_API awq_status awq_fakequant(const void* W, int32_t w_dtype, int64_t out, int64_t in, const float* s,
+                         const float* inv_s, const awq_config* cfg, uint16_t* op,
+                         awq_stream_t stream);
+
+/* Tile grid of the search product: the n_tok x out output of one alpha is
+   cut into m_tiles x n_tiles tiles of tile_m x tile_n. Host-only. */
+AWQ_API awq_status awq_search_tiles(int64_t n_tok, int64_t out, const awq_config* cfg, int64_t* m_tiles,
+                            int64_t* n_tiles, int32_t* tile_m, int32_t* tile_n);
+
+/* partials[i][mt][nt][q] = sum over the 32 tokens of lane quarter q of tile
+   (mt, nt) and over the tile's outputs of (X op_i^T)^2 (RESIDUAL) or of
+   (X op_i^T - X op_G^T)^2 (REFERENCE). X: device bf16 [n_tok][in]. op: as
+   written by awq_fakequant. partials: device fp32 [n_grid][m_tiles][n_tiles][4].
+   status: device uint32, set to AWQ_ERR_TIMEOUT if a wait ran out.
+   tcgen05 tensor cores (bf16 in, fp32 accumulate in tensor memory), operands
+   staged by TMA. */
+AWQ_API awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
+                           int64_t out, const awq_config* cfg, float* partials, uint32_t* status,
+                           awq_stream_t stream);
+
+/* Test aid: awq_search_gemm in RESIDUAL form that also stores the raw fp32
+   products D[i][t][r] = (X op_i^T)[t][r] to `dump` (device fp32
+   [n_grid][n_tok][out]), so the tensor-core data path can be checked element
+   by element against a plain matrix product on small shapes. The stores cost
+   n_grid * n_tok * out * 4 bytes of traffic; not for production use. */
+AWQ_API awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
+                                        int64_t out, const awq_config* cfg, float* partials,
+                                        uint32_t* status, float* dump, awq_stream_t stream);
+
+/* losses[i] = (sum of partials[i]) / (n_tok * out) (fp64 sum, fixed order);
+   best_idx = first i with the smallest loss; s_best = s[best_idx]. A
+   non-finite loss sets *status to AWQ_ERR_NONFINITE. */
+AWQ_API awq_status awq_loss_select(const float* partials, int64_t n_tok, int64_t out, int64_t in,
+                           const float* s, const awq_config* cfg, float* losses,
+                           int32_t* best_idx, float* s_best, uint32_t* status,
+                           awq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AWQ_B300_H */

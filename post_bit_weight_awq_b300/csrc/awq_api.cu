@@ -1,0 +1,296 @@
+// C ABI of the AWQ per-layer search and pack (declared in include/awq.h).
+// Host code only: argument checks (all before any CUDA call), workspace
+// carving, and the launch sequence of each step.
+#include <string.h>
+
+#include "awq.h"
+#include "awq_launch.h"
+
+using namespace awq;
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Largest sizes accepted: every index the kernels form stays below 2^31 per
+// matrix dimension, and the TMA coordinates are 32-bit.
+constexpr int64_t kMaxDim = (int64_t)1 << 30;
+
+awq_status check_cfg(const awq_config* cfg) {
+  if (cfg == nullptr) return AWQ_ERR_INVALID_ARG;
+  if (cfg->n_grid < 1 || cfg->n_grid > kMaxGrid) return AWQ_ERR_INVALID_ARG;
+  if (cfg->group <= 0 || cfg->w_bit <= 0) return AWQ_ERR_INVALID_ARG;
+  if (!(cfg->sx_clamp_min > 0.0f) || !(cfg->delta_floor > 0.0f)) return AWQ_ERR_INVALID_ARG;
+  if (cfg->loss_form != AWQ_LOSS_RESIDUAL && cfg->loss_form != AWQ_LOSS_REFERENCE) return AWQ_ERR_INVALID_ARG;
+  if (cfg->w_bit != 4 || cfg->group != kGroup || cfg->zero_point != 1) return AWQ_ERR_UNSUPPORTED;
+  return AWQ_OK;
+}
+
+awq_status check_dims(int64_t n_tok, int64_t out, int64_t in) {
+  if (n_tok < 1 || out < 1 || in < 1) return AWQ_ERR_INVALID_ARG;
+  if (n_tok > kMaxDim || out > kMaxDim || in > kMaxDim) return AWQ_ERR_INVALID_ARG;
+  if (in % kGroup != 0) return AWQ_ERR_INVALID_ARG;
+  if (out * in > ((int64_t)1 << 40)) return AWQ_ERR_INVALID_ARG;
+  return AWQ_OK;
+}
+
+awq_status check_wdtype(int32_t w_dtype) {
+  if (w_dtype == AWQ_BF16 || w_dtype == AWQ_FP32) return AWQ_OK;
+  return AWQ_ERR_INVALID_ARG;
+}
+
+awq_status check_xdtype(int32_t x_dtype) {
+  if (x_dtype == AWQ_BF16) return AWQ_OK;
+  if (x_dtype == AWQ_FP32) return AWQ_ERR_UNSUPPORTED;
+  return AWQ_ERR_INVALID_ARG;
+}
+
+awq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
+
+struct SearchLayout {
+  size_t status, s, inv_s, op, partials, total;
+  int64_t mt, nt;
+};
+
+SearchLayout search_layout(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg) {
+  SearchLayout L;
+  const int64_t G = cfg.n_grid;
+  const int64_t slots = cfg.loss_form == AWQ_LOSS_REFERENCE ? G + 1 : G;
+  L.mt = (n_tok + kTileM - 1) / kTileM;
+  L.nt = (out + kTileN - 1) / kTileN;
+  size_t off = 0;
+  L.status = off;
+  off = align_up(off + 256, kAlign);
+  L.s = off;
+  off = align_up(off + (size_t)G * in * 4, kAlign);
+  L.inv_s = off;
+  off = align_up(off + (size_t)G * in * 4, kAlign);
+  L.op = off;
+  off = align_up(off + (size_t)slots * out * in * 2, kAlign);
+  L.partials = off;
+  off = align_up(off + (size_t)G * L.mt * L.nt * 4 * 4, kAlign);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+void awq_config_default(awq_config* cfg) {
+  if (cfg == nullptr) return;
+  cfg->w_bit = 4;
+  cfg->group = 128;
+  cfg->n_grid = 20;
+  cfg->zero_point = 1;
+  cfg->normalize = 1;
+  cfg->sx_clamp_min = 1e-4f;
+  cfg->delta_floor = 1e-5f;
+  cfg->loss_form = AWQ_LOSS_RESIDUAL;
+  cfg->wait_timeout_ms = 0;
+}
+
+const char* awq_status_string(int status) {
+  switch (status) {
+    case AWQ_OK: return "ok";
+    case AWQ_ERR_INVALID_ARG: return "invalid argument";
+    case AWQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case AWQ_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case AWQ_ERR_WORKSPACE: return "workspace too small";
+    case AWQ_ERR_CUDA: return "CUDA runtime error";
+    case AWQ_ERR_TIMEOUT: return "device wait timed out";
+    case AWQ_ERR_NONFINITE: return "non-finite loss";
+    default: return "unknown status";
+  }
+}
+
+awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_t* bytes) {
+  if (bytes == nullptr || n_tok < 1 || in < 1 || n_tok > kMaxDim || in > kMaxDim) return AWQ_ERR_INVALID_ARG;
+  *bytes = align_up((size_t)stats_chunks(n_tok) * (size_t)in * 4, kAlign);
+  return AWQ_OK;
+}
+
+awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, int64_t in, float* mean_abs, void* ws,
+                         size_t ws_bytes, awq_stream_t stream) {
+  if (X == nullptr || mean_abs == nullptr || ws == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_xdtype(x_dtype);
+  if (st != AWQ_OK) return st;
+  if (n_tok < 1 || in < 1 || n_tok > kMaxDim || in > kMaxDim || in % 8 != 0) return AWQ_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(mean_abs) || !aligned16(ws)) return AWQ_ERR_MISALIGNED;
+  size_t need = 0;
+  awq_act_stats_workspace_size(n_tok, in, &need);
+  if (ws_bytes < need) return AWQ_ERR_WORKSPACE;
+  return from_cuda(launch_stats((const uint16_t*)X, n_tok, in, (float*)ws, mean_abs, (cudaStream_t)stream));
+}
+
+awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, const awq_config* cfg, size_t* bytes) {
+  if (bytes == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  *bytes = search_layout(n_tok, out, in, *cfg).total;
+  return AWQ_OK;
+}
+
+awq_status awq_search_tiles(int64_t n_tok, int64_t out, const awq_config* cfg, int64_t* m_tiles,
+                            int64_t* n_tiles, int32_t* tile_m, int32_t* tile_n) {
+  if (m_tiles == nullptr || n_tiles == nullptr || tile_m == nullptr || tile_n == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (n_tok < 1 || out < 1 || n_tok > kMaxDim || out > kMaxDim) return AWQ_ERR_INVALID_ARG;
+  *m_tiles = (n_tok + kTileM - 1) / kTileM;
+  *n_tiles = (out + kTileN - 1) / kTileN;
+  *tile_m = kTileM;
+  *tile_n = kTileN;
+  return AWQ_OK;
+}
+
+awq_status awq_alpha_scales(const float* mean_abs, int64_t in, const awq_config* cfg, float* s, float* inv_s,
+                            awq_stream_t stream) {
+  if (mean_abs == nullptr || s == nullptr || inv_s == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (in < 1 || in > kMaxDim || in % kGroup != 0) return AWQ_ERR_INVALID_ARG;
+  if (!aligned16(mean_abs) || !aligned16(s) || !aligned16(inv_s)) return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_alpha_scales(mean_abs, in, *cfg, s, inv_s, (cudaStream_t)stream));
+}
+
+awq_status awq_fakequant(const void* W, int32_t w_dtype, int64_t out, int64_t in, const float* s,
+                         const float* inv_s, const awq_config* cfg, uint16_t* op, awq_stream_t stream) {
+  if (W == nullptr || s == nullptr || inv_s == nullptr || op == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_wdtype(w_dtype);
+  if (st != AWQ_OK) return st;
+  st = check_dims(1, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(W) || !aligned16(s) || !aligned16(inv_s) || !aligned16(op)) return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_fakequant(W, w_dtype, out, in, s, inv_s, *cfg, op, (cudaStream_t)stream));
+}
+
+awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, const uint16_t* op, int64_t out,
+                           const awq_config* cfg, float* partials, uint32_t* status, awq_stream_t stream) {
+  if (X == nullptr || op == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(X) || !aligned16(op) || !aligned16(partials) || !aligned16(status)) return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status,
+                                      (cudaStream_t)stream));
+}
+
+awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op, int64_t out,
+                                const awq_config* cfg, float* partials, uint32_t* status, float* dump,
+                                awq_stream_t stream) {
+  if (dump == nullptr) return AWQ_ERR_INVALID_ARG;
+  if (cfg != nullptr && cfg->loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
+  if (X == nullptr || op == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(X) || !aligned16(op) || !aligned16(partials) || !aligned16(status) || !aligned16(dump))
+    return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status,
+                                      (cudaStream_t)stream, dump));
+}
+
+awq_status awq_loss_select(const float* partials, int64_t n_tok, int64_t out, int64_t in, const float* s,
+                           const awq_config* cfg, float* losses, int32_t* best_idx, float* s_best,
+                           uint32_t* status, awq_stream_t stream) {
+  if (partials == nullptr || s == nullptr || losses == nullptr || best_idx == nullptr || s_best == nullptr ||
+      status == nullptr)
+    return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(partials) || !aligned16(s) || !aligned16(s_best)) return AWQ_ERR_MISALIGNED;
+  const int64_t mt = (n_tok + kTileM - 1) / kTileM, nt = (out + kTileN - 1) / kTileN;
+  return from_cuda(launch_loss_select(partials, cfg->n_grid, mt * nt * 4, n_tok, out, s, in, losses, best_idx,
+                                      s_best, status, (cudaStream_t)stream));
+}
+
+awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X,
+                            int32_t x_dtype, int64_t n_tok, const float* mean_abs, const awq_config* cfg,
+                            float* losses, int32_t* best_idx, float* s_best, void* ws, size_t ws_bytes,
+                            awq_stream_t stream) {
+  if (W == nullptr || X == nullptr || mean_abs == nullptr || losses == nullptr || best_idx == nullptr ||
+      s_best == nullptr || ws == nullptr)
+    return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_wdtype(w_dtype);
+  if (st != AWQ_OK) return st;
+  st = check_xdtype(x_dtype);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(W) || !aligned16(X) || !aligned16(mean_abs) || !aligned16(s_best) || !aligned16(ws))
+    return AWQ_ERR_MISALIGNED;
+  const SearchLayout L = search_layout(n_tok, out, in, *cfg);
+  if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* base = (uint8_t*)ws;
+  uint32_t* status = (uint32_t*)(base + L.status);
+  float* sc = (float*)(base + L.s);
+  float* inv = (float*)(base + L.inv_s);
+  uint16_t* op = (uint16_t*)(base + L.op);
+  float* partials = (float*)(base + L.partials);
+
+  cudaError_t e = cudaMemsetAsync(status, 0, 4, s);
+  if (e == cudaSuccess) e = launch_alpha_scales(mean_abs, in, *cfg, sc, inv, s);
+  if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
+  if (e == cudaSuccess) e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s);
+  if (e == cudaSuccess)
+    e = launch_loss_select(partials, cfg->n_grid, L.mt * L.nt * 4, n_tok, out, sc, in, losses, best_idx, s_best,
+                           status, s);
+  return from_cuda(e);
+}
+
+awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out, int64_t in, const float* s,
+                             const awq_config* cfg, int32_t* qweight, uint16_t* scales_f16, uint16_t* zeros_f16,
+                             awq_stream_t stream) {
+  if (W == nullptr || s == nullptr || qweight == nullptr || scales_f16 == nullptr || zeros_f16 == nullptr)
+    return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_wdtype(w_dtype);
+  if (st != AWQ_OK) return st;
+  st = check_dims(1, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(W) || !aligned16(s) || !aligned16(qweight)) return AWQ_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(scales_f16) & 1u) || (reinterpret_cast<uintptr_t>(zeros_f16) & 1u))
+    return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_pack(W, w_dtype, out, in, s, *cfg, qweight, scales_f16, zeros_f16,
+                               (cudaStream_t)stream));
+}
+
+size_t awq_packed_bytes(int64_t out, int64_t in, const awq_config* cfg) {
+  if (check_cfg(cfg) != AWQ_OK || out < 1 || in < 1 || in % cfg->group != 0) return 0;
+  const size_t n = (size_t)out * (size_t)in;
+  const size_t codes = n * (size_t)cfg->w_bit / 8;
+  const size_t groups = n / (size_t)cfg->group;
+  return codes + groups * 2 + (cfg->zero_point ? groups * 2 : 0);
+}
+
+awq_status awq_get_device_status(const void* ws, awq_stream_t stream, awq_status* status) {
+  if (ws == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(const_cast<void*>(ws), 0, 4, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return AWQ_ERR_CUDA;
+  *status = (awq_status)word;
+  return AWQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,42 @@
+// Internal host-side launchers shared by the C ABI (awq_api.cu) and the
+// kernel translation units. Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "awq.h"
+
+namespace awq {
+
+constexpr int kGroup = 128;      // weights per quantisation group (only size built)
+constexpr int kMaxGrid = 64;     // largest alpha grid
+constexpr int kStatsRows = 128;  // tokens per statistics chunk
+
+// Search-product tiling (one CTA per SM, persistent).
+constexpr int kTileM = 128;  // tokens per tile (tensor-memory lanes)
+constexpr int kTileN = 256;  // output rows per tile (tensor-memory columns)
+constexpr int kTileK = 64;   // input channels per pipeline stage (128 B of bf16)
+
+inline int stats_chunks(int64_t n_tok) { return (int)((n_tok + kStatsRows - 1) / kStatsRows); }
+
+cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partials, float* mean_abs,
+                         cudaStream_t st);
+cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_config& cfg, float* s,
+                                float* inv_s, cudaStream_t st);
+cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,
+                             const float* inv_s, const awq_config& cfg, uint16_t* op, cudaStream_t st);
+cudaError_t launch_pack(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,
+                        const awq_config& cfg, int32_t* qweight, uint16_t* scales, uint16_t* zeros,
+                        cudaStream_t st);
+cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, int64_t n_tok, int64_t N,
+                               const float* s, int64_t K, float* losses, int32_t* best_idx, float* s_best,
+                               uint32_t* status, cudaStream_t st);
+
+// Returns cudaErrorInvalidValue (without launching) if a tensor map cannot
+// be encoded.
+cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
+                               const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
+                               float* dump = nullptr);
+
+}  // namespace awq

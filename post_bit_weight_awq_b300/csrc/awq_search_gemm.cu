@@ -1,0 +1,368 @@
+// Search product of the AWQ alpha grid on the 5th-generation tensor cores.
+//
+// For every alpha_i the search_scale listing of "AWQ: How Activation-Aware
+// Quantization Saves 4-bit LLMs" needs the mean of (X W_hat_i^T - X W^T)^2.
+// This kernel produces, per 128 x 256 output tile, the sum of those squares
+// without writing the product to memory:
+//
+//   RESIDUAL form:  D = X (W_hat_i - W)^T  (operand slot i = bf16(W_hat_i - W))
+//                   partial = sum D^2
+//   REFERENCE form: Y = X W^T is computed once per output tile into tensor
+//                   memory and stays resident; for each alpha, D_i = X W_hat_i^T
+//                   and partial_i = sum (D_i - Y)^2.
+//
+// Structure (one CTA per SM, persistent over tiles, 192 threads):
+//   warp 0, lane 0 : TMA producer. X tile [128 x 64] and operand tile
+//                    [256 x 64] per stage, 128-byte swizzle, 4-stage ring.
+//   warp 1         : allocates 512 tensor-memory columns; lane 0 issues
+//                    tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) and
+//                    commits completions to mbarriers.
+//   warps 2..5     : epilogue. Each warp owns one 32-lane quarter of the
+//                    accumulator (= 32 tokens), reads it with tcgen05.ld,
+//                    squares and sums, and writes one fp32 per quarter.
+// Tensor memory: two 256-column fp32 accumulators. RESIDUAL double-buffers
+// them so the epilogue of a tile overlaps the next tile's MMAs; REFERENCE
+// keeps Y in the second and accumulates X W_hat_i^T in the first.
+// Every wait is bounded (wall time and iteration count): on a timeout the
+// kernel records AWQ_ERR_TIMEOUT, stops all roles, lets its in-flight copies
+// and MMAs land, frees tensor memory and returns.
+#include "awq_device.cuh"
+#include "awq_launch.h"
+
+namespace awq {
+namespace {
+
+constexpr int BM = kTileM, BN = kTileN, BK = kTileK;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_THREADS = 192;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+constexpr uint32_t IDESC = umma_idesc_bf16_f32(BM, BN);
+constexpr int GROUP_M = 16;  // output-tile raster: 16 token tiles per column sweep
+
+struct Params {
+  int mt, nt;         // token tiles, output-row tiles
+  int kb;             // K blocks of 64
+  int G;              // alphas
+  int items;          // work items (RESIDUAL: G*mt*nt tiles; REFERENCE: mt*nt tiles)
+  uint64_t timeout_ns;
+  float* partials;    // [G][mt][nt][4]
+  uint32_t* status;
+  float* dump;        // optional raw products [G][n_tok][N] (RESIDUAL, test aid)
+  int n_tok, N;
+};
+
+__device__ __forceinline__ void decode_tile(int t, const Params& p, int& mb, int& nb) {
+  const int span = GROUP_M * p.nt;
+  const int grp = t / span;
+  const int first_m = grp * GROUP_M;
+  const int gm = min(GROUP_M, p.mt - first_m);
+  const int r = t - grp * span;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+template <bool REF>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    search_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
+                       const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (base_u32 & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* full = bars;               // [STAGES] TMA -> MMA
+  uint64_t* empty = bars + STAGES;     // [STAGES] MMA -> TMA
+  uint64_t* tfull = bars + 2 * STAGES; // [2] MMA -> epilogue
+  uint64_t* tempty = tfull + 2;        // [2] epilogue -> MMA
+  uint64_t* drain = tempty + 2;        // [1] final MMA completion
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int passes = REF ? p.G + 1 : 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t stage = 0, phase = 0;
+      uint32_t used = 0, last_par = 0;  // per-stage bit: stage used; parity of its last fill
+      bool ok = true;
+      for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x) {
+        int a = 0, t = it;
+        if (!REF) {
+          a = it / (p.mt * p.nt);
+          t = it - a * p.mt * p.nt;
+        }
+        int mb, nb;
+        decode_tile(t, p, mb, nb);
+        for (int pass = 0; pass < passes && ok; ++pass) {
+          const int slot = REF ? (pass == 0 ? p.G : pass - 1) : a;
+          for (int kb = 0; kb < p.kb; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+            tma_load_2d(sA + stage * A_BYTES, &tmX, &full[stage], kb * BK, mb * BM);
+            tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nb * BN, slot);
+            used |= 1u << stage;
+            last_par = (last_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // Every copy issued must have landed before shared memory goes away.
+      for (int s = 0; s < STAGES; ++s)
+        if (used & (1u << s)) mbar_wait(&full[s], (last_par >> s) & 1u, p.timeout_ns, nullptr, p.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      uint32_t stage = 0, phase = 0;
+      uint32_t ph = 0;  // bit b: parity of accumulator buffer b
+      uint32_t local = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x, ++local) {
+        for (int pass = 0; pass < passes && ok; ++pass) {
+          // RESIDUAL: alternate buffers per tile. REFERENCE: Y -> buffer 1, D_i -> buffer 0.
+          const int buf = REF ? (pass == 0 ? 1 : 0) : (int)(local & 1u);
+          if (!mbar_wait(&tempty[buf], ((ph >> buf) & 1u) ^ 1u, p.timeout_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+          for (int kb = 0; kb < p.kb; ++kb) {
+            if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t adesc = umma_desc_k_sw128(smem_u32(sA + stage * A_BYTES));
+            const uint64_t bdesc = umma_desc_k_sw128(smem_u32(sB + stage * B_BYTES));
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              umma_bf16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), IDESC,
+                        (kb > 0 || k > 0) ? 1u : 0u);
+            umma_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&tfull[buf]);
+          ph ^= 1u << buf;
+        }
+      }
+      // Let every MMA issued finish before tensor memory is released.
+      umma_commit(drain);
+      mbar_wait(drain, 0u, p.timeout_ns, nullptr, p.status);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t ph = 0;  // bit b: parity of accumulator buffer b
+    uint32_t local = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x, ++local) {
+      int a = 0, t = it;
+      if (!REF) {
+        a = it / (p.mt * p.nt);
+        t = it - a * p.mt * p.nt;
+      }
+      int mb, nb;
+      decode_tile(t, p, mb, nb);
+      if (REF) {
+        // All lanes wait; the warp goes on only if every lane saw the phase
+        // complete, so the warp-collective tensor-memory loads stay converged.
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[1], (ph >> 1) & 1u, p.timeout_ns, abort_flag, p.status)))
+          break;
+        tc_fence_after();
+      }
+      for (int pass = REF ? 1 : 0; pass < passes; ++pass) {
+        const int buf = REF ? 0 : (int)(local & 1u);
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&tfull[buf], (ph >> buf) & 1u, p.timeout_ns, abort_flag, p.status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc_addr = tmem_base + lane_base + (uint32_t)(buf * BN);
+        float ss = 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(acc_addr + (uint32_t)(c * 32), v);
+          if (REF) {
+            uint32_t y[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + (uint32_t)(BN + c * 32), y);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float d = __fsub_rn(__uint_as_float(v[i]), __uint_as_float(y[i]));
+              ss = fmaf(d, d, ss);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float d = __uint_as_float(v[i]);
+              ss = fmaf(d, d, ss);
+            }
+            if (p.dump != nullptr) {
+              const int row = mb * BM + q * 32 + lane;
+              const int col0 = nb * BN + c * 32;
+              if (row < p.n_tok)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col0 + i < p.N)
+                    p.dump[((size_t)a * p.n_tok + row) * p.N + col0 + i] = __uint_as_float(v[i]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        ph ^= 1u << buf;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const int alpha = REF ? pass - 1 : a;
+        if (lane == 0) p.partials[((((size_t)alpha * p.mt + mb) * p.nt + nb) << 2) + q] = ss;
+      }
+      if (REF && ok) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[1]);
+        ph ^= 2u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// bf16 tensor of rank 2 or 3, innermost dimension first, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t strides[2];
+  strides[0] = dims[0] * 2;
+  if (rank == 3) strides[1] = dims[0] * dims[1] * 2;
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
+                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
+                               const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
+                               float* dump) {
+  const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
+  const int G = cfg.n_grid;
+  const int slots = ref ? G + 1 : G;
+  CUtensorMap tmX, tmB;
+  const cuuint64_t xd[2] = {(cuuint64_t)K, (cuuint64_t)n_tok};
+  const cuuint32_t xb[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+  const cuuint64_t bd[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)slots};
+  const cuuint32_t bb[3] = {(cuuint32_t)BK, (cuuint32_t)BN, 1u};
+  if (!make_map(&tmX, X, 2, xd, xb) || !make_map(&tmB, op, 3, bd, bb)) return cudaErrorInvalidValue;
+
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+
+  Params p;
+  p.mt = (int)((n_tok + BM - 1) / BM);
+  p.nt = (int)((N + BN - 1) / BN);
+  p.kb = (int)(K / BK);
+  p.G = G;
+  p.items = ref ? p.mt * p.nt : G * p.mt * p.nt;
+  const uint32_t ms = cfg.wait_timeout_ms ? cfg.wait_timeout_ms : 2000u;
+  p.timeout_ns = (uint64_t)ms * 1000000ull;
+  p.partials = partials;
+  p.status = status;
+  p.dump = ref ? nullptr : dump;
+  p.n_tok = (int)n_tok;
+  p.N = (int)N;
+  const int grid = p.items < sms ? p.items : sms;
+
+  if (ref) {
+    e = cudaFuncSetAttribute(search_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    search_gemm_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);
+  } else {
+    e = cudaFuncSetAttribute(search_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    search_gemm_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace awq

@@ -1,0 +1,123 @@
+"""C-ABI checks that need no GPU: the library loads, exports exactly what
+include/awq.h declares, and rejects bad arguments on the host before any
+CUDA call (every call below passes stream 0 and fake pointers, so reaching a
+launch would fail loudly on a machine without a driver)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from post_bit_weight_awq_b300 import build, capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "awq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return capi.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^AWQ_API\s+[\w\s\*]+?\b(awq_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_binding_list():
+    assert header_functions() == sorted(capi.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {capi.LIB_PATH}").read()
+    exported = sorted(set(re.findall(r"\bT (awq_\w+)", out)))
+    assert exported == header_functions()
+
+
+def test_library_is_built_for_sm_103a(lib):
+    out = os.popen(f"cuobjdump --list-elf {capi.LIB_PATH} 2>&1").read()
+    assert "sm_103a" in out
+
+
+def test_config_default(lib):
+    c = capi.config()
+    assert (c.w_bit, c.group, c.n_grid, c.zero_point, c.normalize) == (4, 128, 20, 1, 1)
+    assert c.sx_clamp_min == pytest.approx(1e-4) and c.delta_floor == pytest.approx(1e-5)
+    assert c.loss_form == capi.AWQ_LOSS_RESIDUAL
+    assert ctypes.sizeof(capi.AwqConfig) == 36
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert capi.status_string(code)
+    assert capi.status_string(123) == "unknown status"
+
+
+def test_packed_bytes_matches_13b_arithmetic(lib):
+    cfg = capi.config()
+    rows = 13_000_000_000 // 128
+    b = capi.awq_packed_bytes(rows, 128, cfg)
+    assert b == 6_500_000_000 + 2 * (13_000_000_000 // 128) * 2
+
+
+def test_workspace_sizes(lib):
+    cfg = capi.config()
+    n, N, K = 4096, 4096, 4096
+    ws = capi.awq_workspace_size(n, N, K, cfg)
+    assert ws >= 20 * N * K * 2 + 2 * 20 * K * 4
+    ref = capi.awq_workspace_size(n, N, K, capi.config(loss_form=capi.AWQ_LOSS_REFERENCE))
+    assert ref >= ws + N * K * 2
+    assert capi.awq_act_stats_workspace_size(n, K) >= (n // 128) * K * 4
+    mt, nt, tm, tn = capi.awq_search_tiles(n, N, cfg)
+    assert (mt, nt) == ((n + tm - 1) // tm, (N + tn - 1) // tn)
+
+
+def _status_of(fn, *a, **k):
+    try:
+        fn(*a, **k)
+    except capi.AwqError as e:
+        return e.status
+    return capi.AWQ_OK
+
+
+def test_host_validation_of_act_stats(lib):
+    A, B, C = 0x1000, 0x2000, 0x3000
+    f = capi.awq_act_stats
+    kw = dict(n_tok=64, in_features=128, x_dtype=capi.AWQ_BF16, ws_bytes=1 << 20)
+    assert _status_of(f, 0, B, C, 0, **kw) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A, 0, C, 0, **kw) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A + 8, B, C, 0, **kw) == capi.AWQ_ERR_MISALIGNED
+    assert _status_of(f, A, B, C, 0, **{**kw, "x_dtype": capi.AWQ_FP32}) == capi.AWQ_ERR_UNSUPPORTED
+    assert _status_of(f, A, B, C, 0, **{**kw, "x_dtype": 7}) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A, B, C, 0, **{**kw, "in_features": 100}) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A, B, C, 0, **{**kw, "n_tok": 0}) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A, B, C, 0, **{**kw, "ws_bytes": 16}) == capi.AWQ_ERR_WORKSPACE
+
+
+def test_host_validation_of_search_and_pack(lib):
+    A, B, C, D = 0x1000, 0x2000, 0x3000, 0x4000
+    cfg = capi.config()
+    kw = dict(out_features=256, in_features=256, n_tok=128, w_dtype=capi.AWQ_BF16, x_dtype=capi.AWQ_BF16)
+    need = capi.awq_workspace_size(128, 256, 256, cfg)
+    s = capi.awq_search_layer
+    assert _status_of(s, A, B, C, cfg, D, D, D, 0, 0, ws_bytes=need, **kw) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(s, A, B, C, cfg, D, D, D, D, 0, ws_bytes=need - 1, **kw) == capi.AWQ_ERR_WORKSPACE
+    assert _status_of(s, A, B, C, capi.config(group=64), D, D, D, D, 0, ws_bytes=need, **kw) == \
+        capi.AWQ_ERR_UNSUPPORTED
+    assert _status_of(s, A, B, C, capi.config(n_grid=65), D, D, D, D, 0, ws_bytes=need, **kw) == \
+        capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(s, A, B, C, capi.config(loss_form=5), D, D, D, D, 0, ws_bytes=need, **kw) == \
+        capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(s, A, B, C, cfg, D, D, D, D + 4, 0, ws_bytes=need, **kw) == capi.AWQ_ERR_MISALIGNED
+    assert _status_of(s, A, B, C, cfg, D, D, D, D, 0, ws_bytes=need, **{**kw, "in_features": 200}) == \
+        capi.AWQ_ERR_INVALID_ARG
+    p = capi.awq_quantize_pack
+    pkw = dict(out_features=4, in_features=128, w_dtype=capi.AWQ_FP32)
+    assert _status_of(p, A, B, cfg, C, D, 0, 0, **pkw) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(p, A, B, cfg, C + 4, D, D, 0, **pkw) == capi.AWQ_ERR_MISALIGNED
+    assert _status_of(p, A, B, cfg, C, D + 1, D, 0, **pkw) == capi.AWQ_ERR_MISALIGNED
+    assert _status_of(p, A, B, capi.config(w_bit=8), C, D, D, 0, **pkw) == capi.AWQ_ERR_UNSUPPORTED
+    assert _status_of(p, A, B, cfg, C, D, D, 0, **{**pkw, "w_dtype": 3}) == capi.AWQ_ERR_INVALID_ARG

@@ -1,0 +1,202 @@
+"""End-to-end parity of the CUDA search + pack against the CPU oracle.
+
+Three levels, as the library promises them:
+  1. packed codes, scales and zeros are bit-exact when the pack is fed the
+     oracle's chosen scale;
+  2. every per-alpha loss is within 1e-2 (relative) of the oracle's;
+  3. the oracle's loss at the GPU's chosen alpha is within 0.5% of the
+     oracle's minimum.
+Small layers run the oracle in the test. Full-size layers compare with
+oracle losses stored in tests/golden/oracle_losses.json (written by
+tests/golden/make_oracle_losses.py, which calls only the oracle), plus
+oracle checks of sampled output tiles and sampled packed rows.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads
+from gpu_util import dev_bf16, dev_f32, dev_weight, save_debug
+from post_bit_weight_awq_b300 import build, capi, layer
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "oracle_losses.json")
+LOSS_RTOL = 1e-2
+ARGMIN_SLACK = 1.005
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build.build()
+    capi.lib()
+
+
+def _oracle_losses(W, X, **kw):
+    return O.search_scale(W.astype(np.float64), X.astype(np.float64), O.channel_importance(X), **kw)
+
+
+def _run_layer(L, cfg):
+    W = dev_weight(L)
+    X = dev_bf16(L["X"])
+    q = layer.quantize_layer(W, X, cfg)
+    torch.cuda.synchronize()
+    return q
+
+
+def _check_levels(losses_gpu, best_gpu, losses_oracle):
+    lo = np.asarray(losses_oracle, dtype=np.float64)
+    lg = np.asarray(losses_gpu, dtype=np.float64)
+    rel = np.abs(lg - lo) / lo
+    assert rel.max() <= LOSS_RTOL, f"per-alpha loss off by {rel.max():.3e}"
+    assert lo[best_gpu] <= ARGMIN_SLACK * lo.min()
+    return rel.max()
+
+
+def _check_pack(L, s32, rows=None):
+    W = L["W"]
+    N, K = W.shape
+    qw = torch.empty(N, K // 8, dtype=torch.int32, device="cuda")
+    sc = torch.empty(N, K // 128, dtype=torch.float16, device="cuda")
+    zr = torch.empty(N, K // 128, dtype=torch.float16, device="cuda")
+    capi.awq_quantize_pack(dev_weight(L), dev_f32(s32), capi.config(), qw, sc, zr)
+    torch.cuda.synchronize()
+    idx = np.arange(N) if rows is None else rows
+    ref = O.quantize_pack(W[idx].astype(np.float64), s32)
+    np.testing.assert_array_equal(qw.cpu().numpy()[idx], ref["qweight"])
+    np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint16)[idx], ref["scales"].view(np.uint16))
+    np.testing.assert_array_equal(zr.cpu().numpy().view(np.uint16)[idx], ref["zeros"].view(np.uint16))
+    # synthetic layers keep every zero point inside the code range
+    z = zr.cpu().numpy()[idx].astype(np.float64)
+    assert z.min() >= 0 and z.max() <= 15
+
+
+# ------------------------------------------------------------------ small layers, oracle in the test
+
+
+@pytest.mark.parametrize("form", [capi.AWQ_LOSS_RESIDUAL, capi.AWQ_LOSS_REFERENCE])
+def test_tiny_layer_all_levels(form):
+    L = workloads.make_layer("tiny")
+    res = _oracle_losses(L["W"], L["X"])
+    q = _run_layer(L, capi.config(loss_form=form))
+    np.testing.assert_allclose(q.mean_abs.cpu().numpy(), O.channel_importance(L["X"]), rtol=1e-5)
+    _check_levels(q.losses.cpu().numpy(), int(q.best_idx[0]), res["losses"])
+    _check_pack(L, O.f32(res["s_best"]))
+
+
+@pytest.mark.parametrize("n,N,K", [(1, 7, 128), (129, 130, 256), (257, 300, 384), (64, 1, 128), (300, 520, 1024)])
+def test_ragged_shapes(n, N, K):
+    L = workloads.make_layer("llama7b_q_proj", n_tok=n, out_features=N, in_features=K, seed=n + N)
+    res = _oracle_losses(L["W"], L["X"])
+    for form in (capi.AWQ_LOSS_RESIDUAL, capi.AWQ_LOSS_REFERENCE):
+        q = _run_layer(L, capi.config(loss_form=form))
+        _check_levels(q.losses.cpu().numpy(), int(q.best_idx[0]), res["losses"])
+    _check_pack(L, O.f32(res["s_best"]))
+
+
+def test_loss_forms_agree():
+    L = workloads.make_layer("llama7b_q_proj", n_tok=512, out_features=768, in_features=1024)
+    a = _run_layer(L, capi.config(loss_form=capi.AWQ_LOSS_RESIDUAL)).losses.cpu().numpy()
+    b = _run_layer(L, capi.config(loss_form=capi.AWQ_LOSS_REFERENCE)).losses.cpu().numpy()
+    np.testing.assert_allclose(a, b, rtol=5e-3)
+
+
+def test_search_is_deterministic():
+    L = workloads.make_layer("llama7b_q_proj", n_tok=512, out_features=1024, in_features=1024)
+    a = _run_layer(L, capi.config())
+    b = _run_layer(L, capi.config())
+    assert torch.equal(a.losses, b.losses) and torch.equal(a.qweight, b.qweight)
+
+
+def test_nonfinite_activation_sets_status():
+    L = workloads.make_layer("tiny")
+    X = L["X"].copy()
+    X[3, 17] = np.nan
+    W, Xd = dev_weight(L), dev_bf16(X)
+    cfg = capi.config()
+    N, K = L["W"].shape
+    n = X.shape[0]
+    ws = torch.empty(capi.awq_workspace_size(n, N, K, cfg), dtype=torch.uint8, device="cuda")
+    mean = dev_f32(O.f32(O.channel_importance(L["X"])))
+    losses = torch.empty(cfg.n_grid, dtype=torch.float32, device="cuda")
+    best = torch.empty(1, dtype=torch.int32, device="cuda")
+    s_best = torch.empty(K, dtype=torch.float32, device="cuda")
+    capi.awq_search_layer(W, Xd, mean, cfg, losses, best, s_best, ws)
+    assert capi.awq_get_device_status(ws) == capi.AWQ_ERR_NONFINITE
+    capi.awq_search_layer(W, dev_bf16(L["X"]), mean, cfg, losses, best, s_best, ws)
+    assert capi.awq_get_device_status(ws) == capi.AWQ_OK
+
+
+# ------------------------------------------------------------------ full-size layers
+
+
+def _golden():
+    return json.load(open(GOLDEN))
+
+
+FULL = ["llama7b_q_proj", "llama7b_mlp_up", "llama7b_mlp_down", "13b_up_proj", "70b_mlp"]
+
+
+def _tile_oracle(X, W, s32, mb, nb, tm, tn):
+    """Oracle squared-error sum over one output tile for scale s32."""
+    rows = slice(mb * tm, min(mb * tm + tm, X.shape[0]))
+    cols = slice(nb * tn, min(nb * tn + tn, W.shape[0]))
+    Wt = W[cols].astype(np.float64)
+    return O.output_sq_err_sum(X[rows].astype(np.float64), Wt, O.fake_quantize(Wt, s32))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_layer(name):
+    g = _golden()
+    if name not in g:
+        pytest.fail(f"no stored oracle losses for {name}")
+    g = g[name]
+    L = workloads.make_layer(name)
+    W, X = L["W"], L["X"]
+    n, K = X.shape
+    N = W.shape[0]
+    assert (g["n_tok"], g["out_features"], g["in_features"]) == (n, N, K)
+    cfg = capi.config()
+    G = cfg.n_grid
+
+    # level 2 and 3: the library's one-call path
+    q = _run_layer(L, cfg)
+    sx = O.channel_importance(X)
+    np.testing.assert_allclose(q.mean_abs.cpu().numpy(), sx, rtol=1e-5)
+    rel = _check_levels(q.losses.cpu().numpy(), int(q.best_idx[0]), g["losses"])
+    print(f"{name}: max rel loss err {rel:.2e}, gpu best {int(q.best_idx[0])}, oracle best {g['best_idx']}")
+
+    # sampled output tiles of the same launch configuration, alpha by alpha
+    Wd, Xd = dev_weight(L), dev_bf16(X)
+    mean = q.mean_abs
+    s = torch.empty(G, K, dtype=torch.float32, device="cuda")
+    inv = torch.empty_like(s)
+    op = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
+    mt, nt, tm, tn = capi.awq_search_tiles(n, N, cfg)
+    parts = torch.empty(G, mt, nt, 4, dtype=torch.float32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    capi.awq_alpha_scales(mean, cfg, s, inv)
+    capi.awq_fakequant(Wd, s, inv, cfg, op)
+    capi.awq_search_gemm(Xd, op, cfg, parts, status, n_tok=n, in_features=K, out_features=N)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    del op
+    P = parts.cpu().numpy().astype(np.float64).sum(axis=3)
+    rng = np.random.default_rng(123)
+    tiles = [(0, 0), (mt - 1, nt - 1)] + [(int(rng.integers(mt)), int(rng.integers(nt))) for _ in range(2)]
+    for i in sorted({0, 7, G - 1, g["best_idx"]}):
+        s32 = O.f32(O.awq_scales(sx, O.alpha_grid(G)[i]))
+        for mb, nb in tiles:
+            ref = _tile_oracle(X, W, s32, mb, nb, tm, tn)
+            assert P[i, mb, nb] == pytest.approx(ref, rel=LOSS_RTOL), (i, mb, nb)
+
+    # level 1: bit-exact pack with the oracle's chosen scale, sampled rows
+    s_best = O.f32(O.awq_scales(sx, O.alpha_grid(G)[g["best_idx"]]))
+    rows = np.unique(np.concatenate([np.arange(4), np.arange(N - 4, N), rng.integers(0, N, 120)]))
+    _check_pack(L, s_best, rows)
