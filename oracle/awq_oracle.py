@@ -41,6 +41,9 @@ the design notes):
   library applies it by specification. In exact arithmetic it leaves the
   dequantised weight unchanged (Q(c*V) = c*Q(V) for c > 0 when the floor is
   not hit); ``normalize=False`` turns it off.
+* The clamp constant of the statistic is 1e-4 rounded to fp32 (CLAMP_MIN):
+  the search_scale listing clamps a float tensor, where the constant takes
+  the tensor's precision, and the library's parameter is an fp32 value.
 * Grid alpha_i = i / n_grid for i = 0..n_grid-1 (0 .. 0.95 at 20 points), and
   the first strict minimum wins [AWQ-devto search_scale listing].
 * Packing: 8 codes per 32-bit word along the input dimension, code k of a word
@@ -54,6 +57,7 @@ from typing import Callable, Dict, Optional
 import numpy as np
 
 __all__ = [
+    "CLAMP_MIN",
     "f32",
     "channel_importance",
     "alpha_grid",
@@ -69,6 +73,9 @@ __all__ = [
     "quantize_pack",
     "packed_bytes",
 ]
+
+
+CLAMP_MIN = float(np.float32(1e-4))
 
 
 def f32(x) -> np.ndarray:
@@ -92,7 +99,7 @@ def alpha_grid(n_grid: int) -> np.ndarray:
     return np.array([i / n_grid for i in range(n_grid)], dtype=np.float64)
 
 
-def awq_scales(sx, alpha: float, clamp_min: float = 1e-4, normalize: bool = True) -> np.ndarray:
+def awq_scales(sx, alpha: float, clamp_min: float = CLAMP_MIN, normalize: bool = True) -> np.ndarray:
     """Per-input-channel scale s = max(sx, clamp_min) ** alpha.
 
     [AWQ-devto, search_scale listing: clamp then power; AWQ-Sum, "The scaling
@@ -208,7 +215,7 @@ def search_scale(
     X,
     sx,
     n_grid: int = 20,
-    clamp_min: float = 1e-4,
+    clamp_min: float = CLAMP_MIN,
     normalize: bool = True,
     w_bit: int = 4,
     group: int = 128,

@@ -80,7 +80,7 @@ def test_alpha_zero_gives_unit_scale_exactly():
 def test_scale_clamp_and_power_closed_form():
     sx = np.array([1e-6, 0.5, 2.0, 40.0])
     s = O.awq_scales(sx, 0.5, normalize=False)
-    expect = np.sqrt(np.array([1e-4, 0.5, 2.0, 40.0]))
+    expect = np.sqrt(np.array([O.CLAMP_MIN, 0.5, 2.0, 40.0]))
     np.testing.assert_allclose(s, expect, rtol=1e-15)
     sn = O.awq_scales(sx, 0.5, normalize=True)
     c = math.sqrt(expect.max() * expect.min())
