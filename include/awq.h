@@ -192,7 +192,9 @@ AWQ_API awq_status awq_get_device_status(const void* ws, awq_stream_t stream, aw
 
 /* s[i][j] and inv_s[i][j] = 1/s[i][j] for every alpha_i (device fp32
    [n_grid][in]); the scale law of the search_scale listing and "AWQ >
-   Summary", "The scaling formula". */
+   Summary", "The scaling formula". s is formed in fp64 (power, normaliser,
+   quotient) and rounded to fp32 once; inv_s is the correctly rounded fp32
+   reciprocal of that value. */
 AWQ_API awq_status awq_alpha_scales(const float* mean_abs, int64_t in, const awq_config* cfg, float* s,
                             float* inv_s, awq_stream_t stream);
 
@@ -228,8 +230,9 @@ AWQ_API awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in
                                         int64_t out, const awq_config* cfg, float* partials,
                                         uint32_t* status, float* dump, awq_stream_t stream);
 
-/* losses[i] = (sum of partials[i]) / (n_tok * out) (fp64 sum, fixed order);
-   best_idx = first i with the smallest loss; s_best = s[best_idx]. A
+/* losses[i] = (sum of partials[i]) / (n_tok * out): fp32 sums per thread
+   over a fixed stride, fp64 across threads in a fixed tree (deterministic);
+   best_idx = first i with the smallest fp32 loss; s_best = s[best_idx]. A
    non-finite loss sets *status to AWQ_ERR_NONFINITE. */
 AWQ_API awq_status awq_loss_select(const float* partials, int64_t n_tok, int64_t out, int64_t in,
                            const float* s, const awq_config* cfg, float* losses,

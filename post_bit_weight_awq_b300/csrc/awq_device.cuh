@@ -44,6 +44,42 @@ __device__ __forceinline__ float quant_code(float v, const GroupQ& g, float qmax
   return fminf(fmaxf(q, 0.0f), qmax);
 }
 
+// The same rounding decision without a division per weight.
+// With r = rn(1/delta) and t = rn(v * r):
+//   |t - rn(v/delta)| <= |v/delta| * (3 * 2^-24 + 2^-48) < |t| * 2^-20,
+// so when |t - rint(t)| < 1/2 - |t| * 2^-19 (twice that bound, with |t|
+// taken at the group's largest magnitude) the correctly rounded quotient
+// lies strictly inside (rint(t) - 1/2, rint(t) + 1/2) and rounds to rint(t).
+// t - rint(t) is exact in fp32. Only weights within that margin of a tie
+// (probability ~ |t| * 2^-18) take the IEEE division.
+struct GroupFast {
+  float delta;  // step
+  float r;      // rn(1 / delta)
+  float lo;     // -z:       smallest value of q - z
+  float hi;     // qmax - z: largest value of q - z
+  float edge;   // 1/2 - max|t| * 2^-20 over the group
+};
+
+__device__ __forceinline__ GroupFast group_fast(float vmin, float vmax, float qmax, float floor_) {
+  const GroupQ g = group_params(vmin, vmax, qmax, floor_);
+  GroupFast f;
+  f.delta = g.delta;
+  f.r = __frcp_rn(g.delta);
+  f.lo = -g.z;
+  f.hi = __fsub_rn(qmax, g.z);
+  const float tmax = __fmul_rn(fmaxf(fabsf(vmin), fabsf(vmax)), f.r);
+  f.edge = __fsub_rn(0.5f, __fmul_rn(tmax, 0x1p-19f));
+  return f;
+}
+
+// Returns q - z = clamp(rne(rn(v / delta)), -z, qmax - z) (an exact integer).
+__device__ __forceinline__ float quant_code_minus_z(float v, const GroupFast& f) {
+  const float t = __fmul_rn(v, f.r);
+  float k = rintf(t);
+  if (!(fabsf(__fsub_rn(t, k)) < f.edge)) k = rintf(__fdiv_rn(v, f.delta));
+  return fminf(fmaxf(k, f.lo), f.hi);
+}
+
 // ----------------------------------------------------------------- bf16 helpers
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

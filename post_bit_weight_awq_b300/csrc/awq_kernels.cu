@@ -20,8 +20,8 @@ namespace awq {
 // Block = 32 x 8 threads over a strip of 256 channels and a chunk of
 // kStatsRows tokens. Each thread reads 8 channels (16 B) of every 8th row of
 // the chunk, so a warp reads 512 contiguous bytes per row. The 8 row phases
-// are added in fixed order in shared memory; chunks are added in fp64 by the
-// finalize kernel in fixed order. The result is deterministic.
+// are added in fixed order in shared memory; the finalize kernel adds the
+// chunks with a compensated fp32 sum in fixed order. Deterministic.
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;
@@ -76,9 +76,15 @@ __global__ void __launch_bounds__(256) stats_finalize_kernel(const float* __rest
                                                              int n, int K, float* __restrict__ mean_abs) {
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= K) return;
-  double s = 0.0;
-  for (int i = 0; i < chunks; ++i) s += (double)partials[(size_t)i * K + c];
-  mean_abs[c] = (float)(s / (double)n);
+  // compensated (Neumaier) fp32 sum over the chunks, fixed order
+  float sum = 0.0f, comp = 0.0f;
+  for (int i = 0; i < chunks; ++i) {
+    const float x = partials[(size_t)i * K + c];
+    const float t = __fadd_rn(sum, x);
+    comp = __fadd_rn(comp, fabsf(sum) >= fabsf(x) ? __fadd_rn(__fsub_rn(sum, t), x) : __fadd_rn(__fsub_rn(x, t), sum));
+    sum = t;
+  }
+  mean_abs[c] = (float)(((double)sum + (double)comp) / (double)n);
 }
 
 cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partials, float* mean_abs,
@@ -93,23 +99,29 @@ cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partial
 
 // ============================================================== alpha scales
 //
-// One block per alpha_i = i / n_grid: s = max(sx, clamp)^alpha ("AWQ: How
-// Activation-Aware Quantization Saves 4-bit LLMs", search_scale listing;
-// "AWQ > Summary", "The scaling formula"), then optionally s /= sqrt(max(s) *
-// min(s)). alpha = 0 gives s = 1 exactly (pow(x, 0) = 1, and sqrt(1*1) = 1).
+// s_i = max(sx, clamp)^alpha_i ("AWQ: How Activation-Aware Quantization
+// Saves 4-bit LLMs", search_scale listing; "AWQ > Summary", "The scaling
+// formula"), alpha_i = i / n_grid, then optionally s_i /= sqrt(max(s_i) *
+// min(s_i)). The scale decides the codes, so it is formed in fp64 (pow,
+// product, sqrt, quotient) and rounded to fp32 once. Because x^alpha is
+// non-decreasing in x for alpha >= 0, max(s_i) and min(s_i) are the powers of
+// the largest and smallest clamped statistic; every block finds those two
+// with a fixed-order reduction and forms the normaliser itself.
+// Grid: (ceil(in / 256), n_grid). alpha = 0 gives s = 1 exactly.
 
 __global__ void __launch_bounds__(256) alpha_scales_kernel(const float* __restrict__ mean_abs, int K, int G,
-                                                           float clamp_min, int normalize,
+                                                           double clamp_min, int normalize,
                                                            float* __restrict__ s_out,
                                                            float* __restrict__ inv_out) {
   __shared__ float smax[8], smin[8];
-  const int i = blockIdx.x;
-  const float alpha = __fdiv_rn((float)i, (float)G);
+  __shared__ double norm_sh;
+  const int i = blockIdx.y;
+  const double alpha = (double)i / (double)G;
   float mx = -INFINITY, mn = INFINITY;
   for (int j = threadIdx.x; j < K; j += blockDim.x) {
-    const float sj = powf(fmaxf(mean_abs[j], clamp_min), alpha);
-    mx = fmaxf(mx, sj);
-    mn = fminf(mn, sj);
+    const float v = mean_abs[j];
+    mx = fmaxf(mx, v);
+    mn = fminf(mn, v);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -122,24 +134,34 @@ __global__ void __launch_bounds__(256) alpha_scales_kernel(const float* __restri
     smin[warp] = mn;
   }
   __syncthreads();
-  mx = smax[0];
-  mn = smin[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
-    mx = fmaxf(mx, smax[w]);
-    mn = fminf(mn, smin[w]);
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+      smax[0] = fmaxf(smax[0], smax[w]);
+      smin[0] = fminf(smin[0], smin[w]);
+    }
+    double c = 1.0;
+    if (normalize) {
+      const double hi = pow(fmax((double)smax[0], clamp_min), alpha);
+      const double lo = pow(fmax((double)smin[0], clamp_min), alpha);
+      c = sqrt(hi * lo);
+    }
+    norm_sh = c;
   }
-  const float c = normalize ? sqrtf(__fmul_rn(mx, mn)) : 1.0f;
-  for (int j = threadIdx.x; j < K; j += blockDim.x) {
-    const float sj = __fdiv_rn(powf(fmaxf(mean_abs[j], clamp_min), alpha), c);
-    s_out[(size_t)i * K + j] = sj;
-    inv_out[(size_t)i * K + j] = __fdiv_rn(1.0f, sj);
+  __syncthreads();
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j < K) {
+    const double sj = pow(fmax((double)mean_abs[j], clamp_min), alpha) / norm_sh;
+    const float s32 = (float)sj;
+    s_out[(size_t)i * K + j] = s32;
+    inv_out[(size_t)i * K + j] = __fdiv_rn(1.0f, s32);
   }
 }
 
 cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_config& cfg, float* s,
                                 float* inv_s, cudaStream_t st) {
-  alpha_scales_kernel<<<cfg.n_grid, 256, 0, st>>>(mean_abs, (int)K, cfg.n_grid, cfg.sx_clamp_min,
-                                                  cfg.normalize, s, inv_s);
+  dim3 grid((unsigned)((K + 255) / 256), (unsigned)cfg.n_grid);
+  alpha_scales_kernel<<<grid, 256, 0, st>>>(mean_abs, (int)K, cfg.n_grid, (double)cfg.sx_clamp_min,
+                                            cfg.normalize, s, inv_s);
   return cudaGetLastError();
 }
 
@@ -198,90 +220,106 @@ __device__ __forceinline__ void load8f(const float* p, float (&v)[8]) {
 // fold-back step of the search_scale listing ("AWQ: How Activation-Aware
 // Quantization Saves 4-bit LLMs"), justified by the scaling equation of "AWQ
 // > Salient Weight Preservation". A group of 128 weights is held by 16 lanes
-// (8 weights each, one 16-byte load); W is read once and all alphas are
-// produced from registers. RESIDUAL writes bf16(W_hat_i - W); REFERENCE
-// writes bf16(W_hat_i) and, in slot G, bf16(W).
+// with 8 weights each (one 16-byte load); each lane holds the same 8 columns
+// of kRows consecutive rows, so one load of s_i / (1/s_i) serves kRows groups.
+// W is read once and every alpha is produced from registers.
+// RESIDUAL writes bf16(W_hat_i - W); REFERENCE writes bf16(W_hat_i) and, in
+// slot G, bf16(W).
+
+constexpr int kFqRows = 2;
 
 template <typename WT, bool REF>
-__global__ void __launch_bounds__(256) fakequant_kernel(const WT* __restrict__ W, int64_t ngroups, int K, int G,
+__global__ void __launch_bounds__(256) fakequant_kernel(const WT* __restrict__ W, int N, int K, int G,
                                                         const float* __restrict__ s,
                                                         const float* __restrict__ inv_s, float qmax,
                                                         float floor_, uint16_t* __restrict__ op,
-                                                        int64_t slot_elems) {
+                                                        int64_t slot_elems, int64_t units) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t gid = t >> 4;
+  const int64_t unit = t >> 4;  // (row block, column group)
   const int sub = (int)(t & 15);
-  const bool valid = gid < ngroups;
-  const int64_t off = (valid ? gid : 0) * 128 + sub * 8;
-  const int col = (int)(off % K);
-  float w[8];
-  WLoad<WT>::load8(W + off, w);
-  if (REF && valid) {
-    uint4 o;
-    o.x = pack_bf16x2(w[0], w[1]);
-    o.y = pack_bf16x2(w[2], w[3]);
-    o.z = pack_bf16x2(w[4], w[5]);
-    o.w = pack_bf16x2(w[6], w[7]);
-    *reinterpret_cast<uint4*>(op + (size_t)G * slot_elems + off) = o;
+  const bool valid_unit = unit < units;
+  const int cgroups = K >> 7;
+  const int64_t u = valid_unit ? unit : 0;
+  const int row0 = (int)(u / cgroups) * kFqRows;
+  const int col = (int)(u % cgroups) * 128 + sub * 8;
+  float w[kFqRows][8];
+  bool rv[kFqRows];
+#pragma unroll
+  for (int i = 0; i < kFqRows; ++i) {
+    rv[i] = valid_unit && (row0 + i < N);
+    const int r = rv[i] ? row0 + i : 0;
+    WLoad<WT>::load8(W + (size_t)r * K + col, w[i]);
+    if (REF && rv[i]) {
+      uint4 o;
+      o.x = pack_bf16x2(w[i][0], w[i][1]);
+      o.y = pack_bf16x2(w[i][2], w[i][3]);
+      o.z = pack_bf16x2(w[i][4], w[i][5]);
+      o.w = pack_bf16x2(w[i][6], w[i][7]);
+      *reinterpret_cast<uint4*>(op + (size_t)G * slot_elems + (size_t)r * K + col) = o;
+    }
   }
   for (int a = 0; a < G; ++a) {
-    float sv[8], iv[8], v[8];
+    float sv[8], iv[8];
     load8f(s + (size_t)a * K + col, sv);
     load8f(inv_s + (size_t)a * K + col, iv);
-    float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      v[e] = __fmul_rn(w[e], sv[e]);
-      mn = fminf(mn, v[e]);
-      mx = fmaxf(mx, v[e]);
-    }
+    for (int i = 0; i < kFqRows; ++i) {
+      float v[8];
+      float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-    for (int o = 8; o; o >>= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    const GroupQ g = group_params(mn, mx, qmax, floor_);
-    float r[8];
+      for (int e = 0; e < 8; ++e) {
+        v[e] = __fmul_rn(w[i][e], sv[e]);
+        mn = fminf(mn, v[e]);
+        mx = fmaxf(mx, v[e]);
+      }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float q = quant_code(v[e], g, qmax);
-      const float wh = __fmul_rn(__fmul_rn(__fsub_rn(q, g.z), g.delta), iv[e]);
-      r[e] = REF ? wh : __fsub_rn(wh, w[e]);
-    }
-    if (valid) {
-      uint4 o;
-      o.x = pack_bf16x2(r[0], r[1]);
-      o.y = pack_bf16x2(r[2], r[3]);
-      o.z = pack_bf16x2(r[4], r[5]);
-      o.w = pack_bf16x2(r[6], r[7]);
-      *reinterpret_cast<uint4*>(op + (size_t)a * slot_elems + off) = o;
+      for (int o = 8; o; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      const GroupFast g = group_fast(mn, mx, qmax, floor_);
+      float r8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float qz = quant_code_minus_z(v[e], g);  // q - z
+        const float dq = __fmul_rn(qz, g.delta);      // dequantised, scaled space
+        r8[e] = REF ? __fmul_rn(dq, iv[e]) : fmaf(dq, iv[e], -w[i][e]);
+      }
+      if (rv[i]) {
+        uint4 o;
+        o.x = pack_bf16x2(r8[0], r8[1]);
+        o.y = pack_bf16x2(r8[2], r8[3]);
+        o.z = pack_bf16x2(r8[4], r8[5]);
+        o.w = pack_bf16x2(r8[6], r8[7]);
+        *reinterpret_cast<uint4*>(op + (size_t)a * slot_elems + (size_t)(row0 + i) * K + col) = o;
+      }
     }
   }
 }
 
 cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,
                              const float* inv_s, const awq_config& cfg, uint16_t* op, cudaStream_t st) {
-  const int64_t ngroups = N * K / 128;
-  const int64_t threads = ngroups * 16;
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  const int64_t units = (N + kFqRows - 1) / kFqRows * (K / 128);
+  const unsigned blocks = (unsigned)((units * 16 + 255) / 256);
   const float qmax = (float)((1 << cfg.w_bit) - 1);
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
   const int64_t slot = N * K;
+  const int n = (int)N, k = (int)K, g = cfg.n_grid;
+  const float fl = cfg.delta_floor;
   if (w_dtype == AWQ_BF16) {
     if (ref)
-      fakequant_kernel<uint16_t, true><<<blocks, 256, 0, st>>>((const uint16_t*)W, ngroups, (int)K, cfg.n_grid,
-                                                               s, inv_s, qmax, cfg.delta_floor, op, slot);
+      fakequant_kernel<uint16_t, true><<<blocks, 256, 0, st>>>((const uint16_t*)W, n, k, g, s, inv_s, qmax, fl, op,
+                                                               slot, units);
     else
-      fakequant_kernel<uint16_t, false><<<blocks, 256, 0, st>>>((const uint16_t*)W, ngroups, (int)K,
-                                                                cfg.n_grid, s, inv_s, qmax, cfg.delta_floor, op,
-                                                                slot);
+      fakequant_kernel<uint16_t, false><<<blocks, 256, 0, st>>>((const uint16_t*)W, n, k, g, s, inv_s, qmax, fl,
+                                                                op, slot, units);
   } else {
     if (ref)
-      fakequant_kernel<float, true><<<blocks, 256, 0, st>>>((const float*)W, ngroups, (int)K, cfg.n_grid, s,
-                                                            inv_s, qmax, cfg.delta_floor, op, slot);
+      fakequant_kernel<float, true><<<blocks, 256, 0, st>>>((const float*)W, n, k, g, s, inv_s, qmax, fl, op, slot,
+                                                            units);
     else
-      fakequant_kernel<float, false><<<blocks, 256, 0, st>>>((const float*)W, ngroups, (int)K, cfg.n_grid, s,
-                                                             inv_s, qmax, cfg.delta_floor, op, slot);
+      fakequant_kernel<float, false><<<blocks, 256, 0, st>>>((const float*)W, n, k, g, s, inv_s, qmax, fl, op,
+                                                             slot, units);
   }
   return cudaGetLastError();
 }
@@ -324,20 +362,21 @@ __global__ void __launch_bounds__(256) pack_kernel(const WT* __restrict__ W, int
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
-  const GroupQ g = group_params(mn, mx, qmax, floor_);
+  const GroupFast g = group_fast(mn, mx, qmax, floor_);
+  const float z = -g.lo;
   uint32_t words[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     uint32_t wd = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) wd |= (uint32_t)quant_code(v[k * 8 + e], g, qmax) << (4 * e);
+    for (int e = 0; e < 8; ++e) wd |= (uint32_t)__fadd_rn(quant_code_minus_z(v[k * 8 + e], g), z) << (4 * e);
     words[k] = wd;
   }
   if (valid) {
     *reinterpret_cast<uint4*>(qweight + gid * 16 + sub * 4) = make_uint4(words[0], words[1], words[2], words[3]);
     if (sub == 0) {
       scales[gid] = __half_as_ushort(__float2half_rn(g.delta));
-      zeros[gid] = __half_as_ushort(__float2half_rn(g.z));
+      zeros[gid] = __half_as_ushort(__float2half_rn(z));
     }
   }
 }
@@ -358,60 +397,63 @@ cudaError_t launch_pack(const void* W, int w_dtype, int64_t N, int64_t K, const 
 
 // ============================================================== loss + argmin
 //
-// L_i = (sum of the tile partials of alpha_i) / (n_tok * out), summed in
-// fp64 in a fixed order; the first strict minimum wins ("AWQ: How
-// Activation-Aware Quantization Saves 4-bit LLMs", search_scale listing:
-// keep an alpha only if its error is strictly lower). One block.
+// L_i = (sum of the tile partials of alpha_i) / (n_tok * out); the first
+// strict minimum wins ("AWQ: How Activation-Aware Quantization Saves 4-bit
+// LLMs", search_scale listing: an alpha replaces the best only if its error
+// is strictly lower). One block per alpha sums its partials (fp32 per
+// thread over a fixed stride, fp64 across threads in a fixed tree), then one
+// small grid picks the argmin and copies s of that alpha to s_best.
 
-__global__ void __launch_bounds__(1024) loss_select_kernel(const float* __restrict__ partials, int G,
-                                                           int64_t per_alpha, double denom,
-                                                           const float* __restrict__ s, int K,
-                                                           float* __restrict__ losses, int32_t* __restrict__ best_idx,
-                                                           float* __restrict__ s_best, uint32_t* status) {
-  __shared__ double wsum[32];
-  __shared__ double sums[kMaxGrid];
-  __shared__ int best_sh;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-  for (int a = 0; a < G; ++a) {
-    double acc = 0.0;
-    const float* p = partials + (size_t)a * per_alpha;
-    for (int64_t t = threadIdx.x; t < per_alpha; t += blockDim.x) acc += (double)p[t];
+__global__ void __launch_bounds__(256) loss_reduce_kernel(const float* __restrict__ partials, int64_t per_alpha,
+                                                          double denom, float* __restrict__ losses,
+                                                          uint32_t* status) {
+  __shared__ double wsum[8];
+  const int a = blockIdx.x;
+  const float* p = partials + (size_t)a * per_alpha;
+  float acc = 0.0f;
+  for (int64_t t = threadIdx.x; t < per_alpha; t += blockDim.x) acc += p[t];
+  double d = (double)acc;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) wsum[warp] = acc;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      double tot = 0.0;
-      for (int w = 0; w < nwarps; ++w) tot += wsum[w];
-      sums[a] = tot;
-      losses[a] = (float)(tot / denom);
-      if (!isfinite(tot)) set_status(status, AWQ_ERR_NONFINITE);
-    }
-    __syncthreads();
+  for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) wsum[warp] = d;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += wsum[w];
+    losses[a] = (float)(tot / denom);
+    if (!isfinite(tot)) set_status(status, AWQ_ERR_NONFINITE);
   }
+}
+
+__global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ losses, int G,
+                                                     const float* __restrict__ s, int K,
+                                                     int32_t* __restrict__ best_idx, float* __restrict__ s_best) {
+  __shared__ int best_sh;
   if (threadIdx.x == 0) {
     int b = -1;
-    double bv = INFINITY;
-    for (int a = 0; a < G; ++a)
-      if (sums[a] < bv) {
-        bv = sums[a];
+    float bv = INFINITY;
+    for (int a = 0; a < G; ++a) {
+      const float v = losses[a];
+      if (v < bv) {
+        bv = v;
         b = a;
       }
-    if (b < 0) b = 0;
+    }
+    if (b < 0) b = 0;  // every loss non-finite: the status word says so
     best_sh = b;
-    *best_idx = b;
+    if (blockIdx.x == 0) *best_idx = b;
   }
   __syncthreads();
-  const int b = best_sh;
-  for (int j = threadIdx.x; j < K; j += blockDim.x) s_best[j] = s[(size_t)b * K + j];
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j < K) s_best[j] = s[(size_t)best_sh * K + j];
 }
 
 cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, int64_t n_tok, int64_t N,
                                const float* s, int64_t K, float* losses, int32_t* best_idx, float* s_best,
                                uint32_t* status, cudaStream_t st) {
-  loss_select_kernel<<<1, 1024, 0, st>>>(partials, G, per_alpha, (double)n_tok * (double)N, s, (int)K, losses,
-                                         best_idx, s_best, status);
+  loss_reduce_kernel<<<G, 256, 0, st>>>(partials, per_alpha, (double)n_tok * (double)N, losses, status);
+  select_kernel<<<(unsigned)((K + 255) / 256), 256, 0, st>>>(losses, G, s, (int)K, best_idx, s_best);
   return cudaGetLastError();
 }
 
