@@ -190,7 +190,7 @@ def gpu_arm(args, rank, world, local_rank):
     import torch
 
     import workloads
-    from post_bit_weight_awq_b300 import build, capi
+    from post_bit_weight_awq_b300 import build, capi, multi
 
     build.build()
     capi.lib()
@@ -308,9 +308,7 @@ def gpu_arm(args, rank, world, local_rank):
     ms_step_eager = statistics.mean(e[0].elapsed_time(e[6]) for e in events)
     t_total = sum(step_ms)
     if dist:
-        tt = torch.tensor([t_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_total = float(tt.item())
+        t_total = multi.max_over_ranks(t_total, device=dev)
     layers = args.steps * world
     value = t_total / layers
 
@@ -355,9 +353,7 @@ def gpu_arm(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in ee)
     if dist:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item()) / world
+        e2e_ms = multi.max_over_ranks(e2e_ms, device=dev) / world
     assert capi.awq_get_device_status(search_ws, stream) == capi.AWQ_OK
 
     # ---------------------------------------------------------- parity spot check vs stored oracle losses
