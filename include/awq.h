@@ -127,8 +127,9 @@ AWQ_API const char* awq_status_string(int status);
    Returns AWQ_ERR_INVALID_ARG for non-positive sizes or a NULL `bytes`. */
 AWQ_API awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_t* bytes);
 
-/* mean_abs[j] = (1/n_tok) sum_t |X[t, j]|  (fp32 out, fp32 partial sums over
-   blocks of tokens, fp64 across blocks, fixed order: deterministic).
+/* mean_abs[j] = (1/n_tok) sum_t |X[t, j]|  (fp32 out; fp32 partial sums over
+   blocks of 128 tokens, a compensated fp32 sum across blocks, fixed order:
+   deterministic).
    X: device bf16 [n_tok][in] (x_dtype must be AWQ_BF16). in % 8 == 0.
    mean_abs: device fp32 [in]. ws: device scratch of at least the queried
    size. Source: "AWQ: How Activation-Aware Quantization Saves 4-bit LLMs",
@@ -229,6 +230,16 @@ AWQ_API awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, con
 AWQ_API awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
                                         int64_t out, const awq_config* cfg, float* partials,
                                         uint32_t* status, float* dump, awq_stream_t stream);
+
+/* Test aid for the bounded waits: awq_search_gemm with the first operand
+   fill of every CTA left out, so the MMA issuer's wait on that pipeline stage
+   can never complete. Each wait gives up after cfg->wait_timeout_ms; the
+   kernel then writes AWQ_ERR_TIMEOUT to *status, stops all its roles, lets
+   the copies and MMAs it did issue finish, frees its tensor memory and
+   returns, leaving the device usable. partials are not meaningful. */
+AWQ_API awq_status awq_search_gemm_withhold_fill(const void* X, int64_t n_tok, int64_t in,
+                                                 const uint16_t* op, int64_t out, const awq_config* cfg,
+                                                 float* partials, uint32_t* status, awq_stream_t stream);
 
 /* losses[i] = (sum of partials[i]) / (n_tok * out): fp32 sums per thread
    over a fixed stride, fp64 across threads in a fixed tree (deterministic);

@@ -44,6 +44,7 @@ EXPORTED = (
     "awq_search_tiles",
     "awq_search_gemm",
     "awq_search_gemm_dump",
+    "awq_search_gemm_withhold_fill",
     "awq_loss_select",
 )
 
@@ -101,6 +102,7 @@ def lib() -> ctypes.CDLL:
                                             ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
         "awq_search_gemm": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
         "awq_search_gemm_dump": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P, _P]),
+        "awq_search_gemm_withhold_fill": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
         "awq_loss_select": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _CFG, _P, _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
@@ -267,6 +269,15 @@ def awq_search_gemm_dump(X, op, cfg: AwqConfig, partials, status, dump, stream=N
     N = op.shape[-2] if out_features is None else out_features
     _check(lib().awq_search_gemm_dump(_ptr(X), n, K, _ptr(op), N, ctypes.byref(cfg), _ptr(partials), _ptr(status),
                                       _ptr(dump), _stream(stream)), "awq_search_gemm_dump")
+
+
+def awq_search_gemm_withhold_fill(X, op, cfg: AwqConfig, partials, status, stream=None, *, n_tok=None,
+                                  in_features=None, out_features=None) -> None:
+    n = X.shape[0] if n_tok is None else n_tok
+    K = X.shape[1] if in_features is None else in_features
+    N = op.shape[-2] if out_features is None else out_features
+    _check(lib().awq_search_gemm_withhold_fill(_ptr(X), n, K, _ptr(op), N, ctypes.byref(cfg), _ptr(partials),
+                                               _ptr(status), _stream(stream)), "awq_search_gemm_withhold_fill")
 
 
 def awq_loss_select(partials, s, cfg: AwqConfig, losses, best_idx, s_best, status, stream=None, *, n_tok,

@@ -200,6 +200,19 @@ awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const 
                                       (cudaStream_t)stream, dump));
 }
 
+awq_status awq_search_gemm_withhold_fill(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
+                                         int64_t out, const awq_config* cfg, float* partials, uint32_t* status,
+                                         awq_stream_t stream) {
+  if (X == nullptr || op == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(X) || !aligned16(op) || !aligned16(partials) || !aligned16(status)) return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status,
+                                      (cudaStream_t)stream, nullptr, 1));
+}
+
 awq_status awq_loss_select(const float* partials, int64_t n_tok, int64_t out, int64_t in, const float* s,
                            const awq_config* cfg, float* losses, int32_t* best_idx, float* s_best,
                            uint32_t* status, awq_stream_t stream) {

@@ -37,6 +37,6 @@ cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, 
 // be encoded.
 cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
                                const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
-                               float* dump = nullptr);
+                               float* dump = nullptr, int withhold_first_fill = 0);
 
 }  // namespace awq

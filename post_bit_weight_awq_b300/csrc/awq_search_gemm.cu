@@ -54,6 +54,7 @@ struct Params {
   uint32_t* status;
   float* dump;        // optional raw products [G][n_tok][N] (RESIDUAL, test aid)
   int n_tok, N;
+  int withhold_first_fill;  // test aid: leave out each CTA's first operand fill
 };
 
 __device__ __forceinline__ void decode_tile(int t, const Params& p, int& mb, int& nb) {
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t used = 0, last_par = 0;  // per-stage bit: stage used; parity of its last fill
       bool ok = true;
+      bool withhold = p.withhold_first_fill != 0;
       for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x) {
         int a = 0, t = it;
         if (!REF) {
@@ -135,11 +137,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-            tma_load_2d(sA + stage * A_BYTES, &tmX, &full[stage], kb * BK, mb * BM);
-            tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nb * BN, slot);
-            used |= 1u << stage;
-            last_par = (last_par & ~(1u << stage)) | (phase << stage);
+            if (withhold) {
+              // test aid: this stage is never filled, so the wait on it cannot complete
+              withhold = false;
+            } else {
+              mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+              tma_load_2d(sA + stage * A_BYTES, &tmX, &full[stage], kb * BK, mb * BM);
+              tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nb * BN, slot);
+              used |= 1u << stage;
+              last_par = (last_par & ~(1u << stage)) | (phase << stage);
+            }
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -320,7 +327,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
                                const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
-                               float* dump) {
+                               float* dump, int withhold_first_fill) {
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
   const int G = cfg.n_grid;
   const int slots = ref ? G + 1 : G;
@@ -350,6 +357,7 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
   p.dump = ref ? nullptr : dump;
   p.n_tok = (int)n_tok;
   p.N = (int)N;
+  p.withhold_first_fill = withhold_first_fill;
   const int grid = p.items < sms ? p.items : sms;
 
   if (ref) {

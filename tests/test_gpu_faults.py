@@ -1,0 +1,53 @@
+"""Failure detection on the GPU without a fault.
+
+A wait that can never complete (one pipeline stage is never filled) must end
+after the configured limit with AWQ_ERR_TIMEOUT in the status word, and the
+device, including tensor memory, must be usable by the next launch.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import dev_bf16
+from post_bit_weight_awq_b300 import build, capi
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build.build()
+    capi.lib()
+
+
+def test_stuck_wait_ends_with_timeout_status_and_device_stays_usable():
+    n, N, K, G = 512, 1024, 512, 2
+    rng = np.random.default_rng(3)
+    A = workloads.round_to_bf16(rng.standard_normal((n, K)).astype(np.float32))
+    B = workloads.round_to_bf16((rng.standard_normal((G, N, K)) * 0.05).astype(np.float32))
+    Ad, Bd = dev_bf16(A), dev_bf16(B.reshape(G * N, K))
+    cfg = capi.config(n_grid=G, wait_timeout_ms=100)
+    mt, nt, tm, tn = capi.awq_search_tiles(n, N, cfg)
+    partials = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    capi.awq_search_gemm_withhold_fill(Ad, Bd, cfg, partials, status, n_tok=n, in_features=K, out_features=N)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status[0]) == capi.AWQ_ERR_TIMEOUT
+    assert elapsed < 5.0
+    # the next launch on the same device is correct
+    status.zero_()
+    capi.awq_search_gemm(Ad, Bd, cfg, partials, status, n_tok=n, in_features=K, out_features=N)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    P = partials.cpu().numpy().astype(np.float64).sum(axis=(1, 2, 3))
+    for i in range(G):
+        ref = ((A.astype(np.float64) @ B[i].astype(np.float64).T) ** 2).sum()
+        assert P[i] == pytest.approx(ref, rel=1e-4)
