@@ -138,6 +138,26 @@ AWQ_API awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_
 AWQ_API awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, int64_t in,
                          float* mean_abs, void* ws, size_t ws_bytes, awq_stream_t stream);
 
+/* Largest ceil(n_tok / 128) * in that awq_act_stats_noalloc accepts (its
+   fixed scratch: 4 MiB of fp32 partial sums). */
+#define AWQ_NOALLOC_STATS_MAX_FLOATS (1u << 20)
+
+/* awq_act_stats for callers that cannot allocate device memory or pass a
+   scratch buffer (for example a plugin inside an engine that owns all device
+   memory and gives the plugin only its inputs and outputs, or a path where a
+   cudaMalloc, which may synchronise the device, is not allowed). The pages
+   have no counterpart: this is an interface variant of step 1, not part of
+   the method. Same arguments and result as awq_act_stats without ws/ws_bytes.
+   The partial sums live in a library-owned 4 MiB device array that every GPU
+   loading the library keeps until exit. Its address is looked up on the first
+   call made on each device (with that device current); make that first call
+   before any stream capture. All calls share the array, so calls that
+   overlap on the GPU race: serialise them. Calls allocate nothing.
+   Returns AWQ_ERR_WORKSPACE if ceil(n_tok/128) * in exceeds
+   AWQ_NOALLOC_STATS_MAX_FLOATS (e.g. n_tok = 16384 allows in <= 8192). */
+AWQ_API awq_status awq_act_stats_noalloc(const void* X, int32_t x_dtype, int64_t n_tok, int64_t in,
+                                         float* mean_abs, awq_stream_t stream);
+
 /* ---------------------------------------------------------------- step 2 */
 
 /* Device bytes of scratch that awq_search_layer needs. Host-only. It holds a

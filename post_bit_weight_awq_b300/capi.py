@@ -34,6 +34,7 @@ EXPORTED = (
     "awq_status_string",
     "awq_act_stats_workspace_size",
     "awq_act_stats",
+    "awq_act_stats_noalloc",
     "awq_workspace_size",
     "awq_search_layer",
     "awq_quantize_pack",
@@ -91,6 +92,7 @@ def lib() -> ctypes.CDLL:
         "awq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "awq_act_stats_workspace_size": (ctypes.c_int, [_I64, _I64, ctypes.POINTER(_SZ)]),
         "awq_act_stats": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _SZ, _P]),
+        "awq_act_stats_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P]),
         "awq_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _CFG, ctypes.POINTER(_SZ)]),
         "awq_search_layer": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _I64, _P, _CFG, _P, _P, _P, _P, _SZ, _P]),
         "awq_quantize_pack": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _CFG, _P, _P, _P, _P]),
@@ -207,6 +209,16 @@ def awq_act_stats(X, mean_abs, ws, stream=None, *, n_tok=None, in_features=None,
     xd = _dtype_code(X) if x_dtype is None else x_dtype
     wb = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check(lib().awq_act_stats(_ptr(X), xd, n, k, _ptr(mean_abs), _ptr(ws), wb, _stream(stream)), "awq_act_stats")
+
+
+def awq_act_stats_noalloc(X, mean_abs, stream=None, *, n_tok=None, in_features=None, x_dtype=None) -> None:
+    """awq_act_stats without caller scratch, for callers that cannot allocate
+    (library-owned fixed array; see include/awq.h for its size limit and the
+    rule that overlapping calls race)."""
+    n = X.shape[0] if n_tok is None else n_tok
+    k = X.shape[1] if in_features is None else in_features
+    xd = _dtype_code(X) if x_dtype is None else x_dtype
+    _check(lib().awq_act_stats_noalloc(_ptr(X), xd, n, k, _ptr(mean_abs), _stream(stream)), "awq_act_stats_noalloc")
 
 
 def awq_search_layer(W, X, mean_abs, cfg: AwqConfig, losses, best_idx, s_best, ws, stream=None, *,
