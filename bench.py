@@ -234,28 +234,30 @@ def gpu_arm(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
-        # the same kernels, in the same order, as awq_act_stats + awq_search_layer + awq_quantize_pack
+        # the same kernels, in the same order, as awq_act_stats + awq_search_layer + awq_quantize_pack;
+        # launched on the current stream (the capture stream while a CUDA graph is recorded)
+        st = torch.cuda.current_stream(dev)
         if ev:
-            ev[0].record(stream)
-        capi.awq_act_stats(Xd, mean_abs, stats_ws, stream)
+            ev[0].record(st)
+        capi.awq_act_stats(Xd, mean_abs, stats_ws, st)
         if ev:
-            ev[1].record(stream)
-        capi.awq_alpha_scales(mean_abs, cfg, s, inv, stream)
+            ev[1].record(st)
+        capi.awq_alpha_scales(mean_abs, cfg, s, inv, st)
         if ev:
-            ev[2].record(stream)
-        capi.awq_fakequant(Wd, s, inv, cfg, op, stream)
+            ev[2].record(st)
+        capi.awq_fakequant(Wd, s, inv, cfg, op, st)
         if ev:
-            ev[3].record(stream)
-        capi.awq_search_gemm(Xd, op, cfg, parts, status, stream, n_tok=n, in_features=K, out_features=N)
+            ev[3].record(st)
+        capi.awq_search_gemm(Xd, op, cfg, parts, status, st, n_tok=n, in_features=K, out_features=N)
         if ev:
-            ev[4].record(stream)
-        capi.awq_loss_select(parts, s, cfg, losses, best, s_best, status, stream, n_tok=n, out_features=N,
+            ev[4].record(st)
+        capi.awq_loss_select(parts, s, cfg, losses, best, s_best, status, st, n_tok=n, out_features=N,
                              in_features=K)
         if ev:
-            ev[5].record(stream)
-        capi.awq_quantize_pack(Wd, s_best, cfg, qw, sc, zr, stream)
+            ev[5].record(st)
+        capi.awq_quantize_pack(Wd, s_best, cfg, qw, sc, zr, st)
         if ev:
-            ev[6].record(stream)
+            ev[6].record(st)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -271,6 +273,13 @@ def gpu_arm(args, rank, world, local_rank):
         flush.zero_()
         graph.replay()
     torch.cuda.synchronize()
+    # the replayed graph must reproduce the eager step's results
+    losses_eager = losses.clone()
+    losses.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    if not torch.equal(losses, losses_eager):
+        raise RuntimeError("graph replay does not reproduce the eager step")
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]

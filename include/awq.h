@@ -213,9 +213,10 @@ AWQ_API awq_status awq_get_device_status(const void* ws, awq_stream_t stream, aw
 
 /* s[i][j] and inv_s[i][j] = 1/s[i][j] for every alpha_i (device fp32
    [n_grid][in]); the scale law of the search_scale listing and "AWQ >
-   Summary", "The scaling formula". s is formed in fp64 (power, normaliser,
-   quotient) and rounded to fp32 once; inv_s is the correctly rounded fp32
-   reciprocal of that value. */
+   Summary", "The scaling formula". s is formed in fp64 (b^(i/n_grid) as the
+   i-th power of b^(1/n_grid), times the fp64 reciprocal normaliser) and
+   rounded to fp32 once; inv_s is the correctly rounded fp32 reciprocal of
+   that value. */
 AWQ_API awq_status awq_alpha_scales(const float* mean_abs, int64_t in, const awq_config* cfg, float* s,
                             float* inv_s, awq_stream_t stream);
 
@@ -242,14 +243,18 @@ AWQ_API awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, con
                            int64_t out, const awq_config* cfg, float* partials, uint32_t* status,
                            awq_stream_t stream);
 
-/* Test aid: awq_search_gemm in RESIDUAL form that also stores the raw fp32
-   products D[i][t][r] = (X op_i^T)[t][r] to `dump` (device fp32
-   [n_grid][n_tok][out]), so the tensor-core data path can be checked element
-   by element against a plain matrix product on small shapes. The stores cost
-   n_grid * n_tok * out * 4 bytes of traffic; not for production use. */
+/* Test aid: awq_search_gemm in RESIDUAL form with a chosen cluster size
+   (cluster_m CTAs share each operand tile through TMA multicast: 1, 2 or 4;
+   0 = the size awq_search_gemm uses). If `dump` is not NULL the kernel also
+   stores the raw fp32 products D[i][t][r] = (X op_i^T)[t][r] there (device
+   fp32 [n_grid][n_tok][out]), so the tensor-core data path can be checked
+   element by element against a plain matrix product on small shapes; those
+   stores cost n_grid * n_tok * out * 4 bytes of traffic. Not for production
+   use. */
 AWQ_API awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
                                         int64_t out, const awq_config* cfg, float* partials,
-                                        uint32_t* status, float* dump, awq_stream_t stream);
+                                        uint32_t* status, float* dump, int32_t cluster_m,
+                                        awq_stream_t stream);
 
 /* Test aid for the bounded waits: awq_search_gemm with the first operand
    fill of every CTA left out, so the MMA issuer's wait on that pipeline stage

@@ -103,7 +103,7 @@ def lib() -> ctypes.CDLL:
         "awq_search_tiles": (ctypes.c_int, [_I64, _I64, _CFG, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                                             ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
         "awq_search_gemm": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
-        "awq_search_gemm_dump": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P, _P]),
+        "awq_search_gemm_dump": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P, _I32, _P]),
         "awq_search_gemm_withhold_fill": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
         "awq_loss_select": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _CFG, _P, _P, _P, _P, _P]),
     }
@@ -275,12 +275,12 @@ def awq_search_gemm(X, op, cfg: AwqConfig, partials, status, stream=None, *, n_t
 
 
 def awq_search_gemm_dump(X, op, cfg: AwqConfig, partials, status, dump, stream=None, *, n_tok=None,
-                         in_features=None, out_features=None) -> None:
+                         in_features=None, out_features=None, cluster_m=0) -> None:
     n = X.shape[0] if n_tok is None else n_tok
     K = X.shape[1] if in_features is None else in_features
     N = op.shape[-2] if out_features is None else out_features
     _check(lib().awq_search_gemm_dump(_ptr(X), n, K, _ptr(op), N, ctypes.byref(cfg), _ptr(partials), _ptr(status),
-                                      _ptr(dump), _stream(stream)), "awq_search_gemm_dump")
+                                      _ptr(dump), cluster_m, _stream(stream)), "awq_search_gemm_dump")
 
 
 def awq_search_gemm_withhold_fill(X, op, cfg: AwqConfig, partials, status, stream=None, *, n_tok=None,

@@ -186,8 +186,8 @@ awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, const uint1
 
 awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op, int64_t out,
                                 const awq_config* cfg, float* partials, uint32_t* status, float* dump,
-                                awq_stream_t stream) {
-  if (dump == nullptr) return AWQ_ERR_INVALID_ARG;
+                                int32_t cluster_m, awq_stream_t stream) {
+  if (cluster_m != 0 && cluster_m != 1 && cluster_m != 2 && cluster_m != 4) return AWQ_ERR_INVALID_ARG;
   if (cfg != nullptr && cfg->loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
   if (X == nullptr || op == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
@@ -197,7 +197,7 @@ awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const 
   if (!aligned16(X) || !aligned16(op) || !aligned16(partials) || !aligned16(status) || !aligned16(dump))
     return AWQ_ERR_MISALIGNED;
   return from_cuda(launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status,
-                                      (cudaStream_t)stream, dump));
+                                      (cudaStream_t)stream, dump, 0, cluster_m));
 }
 
 awq_status awq_search_gemm_withhold_fill(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,

@@ -39,25 +39,25 @@ __device__ __forceinline__ GroupQ group_params(float vmin, float vmax, float qma
   return g;
 }
 
-__device__ __forceinline__ float quant_code(float v, const GroupQ& g, float qmax) {
-  const float q = __fadd_rn(rintf(__fdiv_rn(v, g.delta)), g.z);
-  return fminf(fmaxf(q, 0.0f), qmax);
-}
-
-// The same rounding decision without a division per weight.
+// The rounding decision of q without a division per weight.
 // With r = rn(1/delta) and t = rn(v * r):
 //   |t - rn(v/delta)| <= |v/delta| * (3 * 2^-24 + 2^-48) < |t| * 2^-20,
 // so when |t - rint(t)| < 1/2 - |t| * 2^-19 (twice that bound, with |t|
 // taken at the group's largest magnitude) the correctly rounded quotient
 // lies strictly inside (rint(t) - 1/2, rint(t) + 1/2) and rounds to rint(t).
-// t - rint(t) is exact in fp32. Only weights within that margin of a tie
-// (probability ~ |t| * 2^-18) take the IEEE division.
+// t - rint(t) is exact in fp32. Only values within that margin of a tie
+// (probability ~ |t| * 2^-18 each) send their lane to the IEEE division.
+// Codes are monotone in v, and the smallest value of a group always gets
+// q - z = rne(rn(vmin/delta)) = -rne(rn(-vmin/delta)) = -z exactly, so the
+// clamp to [0, qmax] can only bind at the top; `clamp` records whether the
+// largest value's code exceeds qmax, decided once per group.
 struct GroupFast {
   float delta;  // step
   float r;      // rn(1 / delta)
   float lo;     // -z:       smallest value of q - z
   float hi;     // qmax - z: largest value of q - z
-  float edge;   // 1/2 - max|t| * 2^-20 over the group
+  float edge;   // 1/2 - max|t| * 2^-19 over the group
+  bool clamp;   // some code of the group lies above qmax before clamping
 };
 
 __device__ __forceinline__ GroupFast group_fast(float vmin, float vmax, float qmax, float floor_) {
@@ -69,15 +69,29 @@ __device__ __forceinline__ GroupFast group_fast(float vmin, float vmax, float qm
   f.hi = __fsub_rn(qmax, g.z);
   const float tmax = __fmul_rn(fmaxf(fabsf(vmin), fabsf(vmax)), f.r);
   f.edge = __fsub_rn(0.5f, __fmul_rn(tmax, 0x1p-19f));
+  f.clamp = rintf(__fdiv_rn(vmax, g.delta)) > f.hi;
   return f;
 }
 
-// Returns q - z = clamp(rne(rn(v / delta)), -z, qmax - z) (an exact integer).
-__device__ __forceinline__ float quant_code_minus_z(float v, const GroupFast& f) {
-  const float t = __fmul_rn(v, f.r);
-  float k = rintf(t);
-  if (!(fabsf(__fsub_rn(t, k)) < f.edge)) k = rintf(__fdiv_rn(v, f.delta));
-  return fminf(fmaxf(k, f.lo), f.hi);
+// q - z = clamp(rne(rn(v / delta)), -z, qmax - z) for N values of one group
+// (exact small integers in fp32).
+template <int N>
+__device__ __forceinline__ void quant_codes_minus_z(const float (&v)[N], const GroupFast& f, float (&k)[N]) {
+  float dmax = 0.0f;
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    const float t = __fmul_rn(v[e], f.r);
+    k[e] = rintf(t);
+    dmax = fmaxf(dmax, fabsf(__fsub_rn(t, k[e])));
+  }
+  if (!(dmax < f.edge)) {
+#pragma unroll
+    for (int e = 0; e < N; ++e) k[e] = rintf(__fdiv_rn(v[e], f.delta));
+  }
+  if (f.clamp) {
+#pragma unroll
+    for (int e = 0; e < N; ++e) k[e] = fminf(fmaxf(k[e], f.lo), f.hi);
+  }
 }
 
 // ----------------------------------------------------------------- bf16 helpers
@@ -184,6 +198,31 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Same 3D load, written to the same shared-memory offset in every CTA of the
+// cluster named in `mask`; each destination CTA's mbarrier at `bar`'s offset
+// receives the byte count of its copy.
+__device__ __forceinline__ void tma_load_3d_multicast(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                                      int y, int z, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+      "{%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(mask)
+      : "memory");
+}
+
+// ----------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA in the cluster arrives, then waits for all.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -246,6 +285,16 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// As umma_commit, but the arrival is delivered to the mbarrier at the same
+// shared-memory offset in every CTA of the cluster named in `mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
 }
 
 // Each lane of the warp reads 32 consecutive 32-bit columns of its own

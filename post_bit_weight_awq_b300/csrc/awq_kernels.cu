@@ -102,21 +102,22 @@ cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partial
 // s_i = max(sx, clamp)^alpha_i ("AWQ: How Activation-Aware Quantization
 // Saves 4-bit LLMs", search_scale listing; "AWQ > Summary", "The scaling
 // formula"), alpha_i = i / n_grid, then optionally s_i /= sqrt(max(s_i) *
-// min(s_i)). The scale decides the codes, so it is formed in fp64 (pow,
-// product, sqrt, quotient) and rounded to fp32 once. Because x^alpha is
-// non-decreasing in x for alpha >= 0, max(s_i) and min(s_i) are the powers of
-// the largest and smallest clamped statistic; every block finds those two
-// with a fixed-order reduction and forms the normaliser itself.
-// Grid: (ceil(in / 256), n_grid). alpha = 0 gives s = 1 exactly.
+// min(s_i)). The scale decides the codes, so it is formed in fp64 and rounded
+// to fp32 once. Since alpha_i = i / n_grid, b^alpha_i = (b^(1/n_grid))^i: one
+// pow per channel, then one fp64 product per alpha (the products drift from
+// a direct pow by at most ~n_grid fp64 ulps, which changes the fp32-rounded
+// scale only when it lies that close to an fp32 rounding boundary). x^alpha
+// is non-decreasing in x, so max(s_i) and min(s_i) are the powers of the
+// largest and smallest clamped statistic; each block finds those two with a
+// fixed-order reduction and forms 1 / sqrt(max * min) per alpha.
+// One thread per channel; alpha = 0 gives s = 1 exactly.
 
-__global__ void __launch_bounds__(256) alpha_scales_kernel(const float* __restrict__ mean_abs, int K, int G,
+__global__ void __launch_bounds__(128) alpha_scales_kernel(const float* __restrict__ mean_abs, int K, int G,
                                                            double clamp_min, int normalize,
                                                            float* __restrict__ s_out,
                                                            float* __restrict__ inv_out) {
-  __shared__ float smax[8], smin[8];
-  __shared__ double norm_sh;
-  const int i = blockIdx.y;
-  const double alpha = (double)i / (double)G;
+  __shared__ float smax[4], smin[4];
+  __shared__ double inv_norm[kMaxGrid];
   float mx = -INFINITY, mn = INFINITY;
   for (int j = threadIdx.x; j < K; j += blockDim.x) {
     const float v = mean_abs[j];
@@ -134,34 +135,38 @@ __global__ void __launch_bounds__(256) alpha_scales_kernel(const float* __restri
     smin[warp] = mn;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
-      smax[0] = fmaxf(smax[0], smax[w]);
-      smin[0] = fminf(smin[0], smin[w]);
-    }
+  if ((int)threadIdx.x < G) {
+    const int i = threadIdx.x;
     double c = 1.0;
     if (normalize) {
-      const double hi = pow(fmax((double)smax[0], clamp_min), alpha);
-      const double lo = pow(fmax((double)smin[0], clamp_min), alpha);
-      c = sqrt(hi * lo);
+      float bmx = smax[0], bmn = smin[0];
+      for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+        bmx = fmaxf(bmx, smax[w]);
+        bmn = fminf(bmn, smin[w]);
+      }
+      const double alpha = (double)i / (double)G;
+      c = sqrt(pow(fmax((double)bmx, clamp_min), alpha) * pow(fmax((double)bmn, clamp_min), alpha));
     }
-    norm_sh = c;
+    inv_norm[i] = 1.0 / c;
   }
   __syncthreads();
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j < K) {
-    const double sj = pow(fmax((double)mean_abs[j], clamp_min), alpha) / norm_sh;
-    const float s32 = (float)sj;
+  if (j >= K) return;
+  const double b = fmax((double)mean_abs[j], clamp_min);
+  const double root = pow(b, 1.0 / (double)G);
+  double p = 1.0;  // b^(i/G)
+  for (int i = 0; i < G; ++i) {
+    const float s32 = (float)(p * inv_norm[i]);
     s_out[(size_t)i * K + j] = s32;
     inv_out[(size_t)i * K + j] = __fdiv_rn(1.0f, s32);
+    p *= root;
   }
 }
 
 cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_config& cfg, float* s,
                                 float* inv_s, cudaStream_t st) {
-  dim3 grid((unsigned)((K + 255) / 256), (unsigned)cfg.n_grid);
-  alpha_scales_kernel<<<grid, 256, 0, st>>>(mean_abs, (int)K, cfg.n_grid, (double)cfg.sx_clamp_min,
-                                            cfg.normalize, s, inv_s);
+  alpha_scales_kernel<<<(unsigned)((K + 127) / 128), 128, 0, st>>>(mean_abs, (int)K, cfg.n_grid,
+                                                                   (double)cfg.sx_clamp_min, cfg.normalize, s, inv_s);
   return cudaGetLastError();
 }
 
@@ -214,112 +219,144 @@ __device__ __forceinline__ void load8f(const float* p, float (&v)[8]) {
   v[7] = b.w;
 }
 
+template <typename WT>
+__device__ __forceinline__ void load16w(const WT* p, float (&w)[16]) {
+  float a[8], b[8];
+  WLoad<WT>::load8(p, a);
+  WLoad<WT>::load8(p + 8, b);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    w[e] = a[e];
+    w[8 + e] = b[e];
+  }
+}
+
+__device__ __forceinline__ void load16f(const float* p, float (&v)[16]) {
+  float a[8], b[8];
+  load8f(p, a);
+  load8f(p + 8, b);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    v[e] = a[e];
+    v[8 + e] = b[e];
+  }
+}
+
+// Group min/max of 16 values per lane over the 8 lanes of a group.
+__device__ __forceinline__ void group_minmax16(const float (&v)[16], float& mn, float& mx) {
+  mn = v[0];
+  mx = v[0];
+#pragma unroll
+  for (int e = 1; e < 16; ++e) {
+    mn = fminf(mn, v[e]);
+    mx = fmaxf(mx, v[e]);
+  }
+#pragma unroll
+  for (int o = 4; o; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+}
+
 // ============================================================== fake-quant
 //
 // For every alpha_i: W_hat_i = Q(W * s_i) * (1 / s_i), the scale-quantise-
 // fold-back step of the search_scale listing ("AWQ: How Activation-Aware
 // Quantization Saves 4-bit LLMs"), justified by the scaling equation of "AWQ
-// > Salient Weight Preservation". A group of 128 weights is held by 16 lanes
-// with 8 weights each (one 16-byte load); each lane holds the same 8 columns
-// of kRows consecutive rows, so one load of s_i / (1/s_i) serves kRows groups.
-// W is read once and every alpha is produced from registers.
+// > Salient Weight Preservation". A group of 128 weights is held by 8 lanes
+// with 16 weights each (two 16-byte loads); W is read once and every alpha is
+// produced from registers, so per alpha a lane does two shuffle steps of the
+// group reduction, the group's step, zero point and clamp decision, and 16
+// division-free exact code decisions.
 // RESIDUAL writes bf16(W_hat_i - W); REFERENCE writes bf16(W_hat_i) and, in
 // slot G, bf16(W).
 
-constexpr int kFqRows = 2;
-
 template <typename WT, bool REF>
-__global__ void __launch_bounds__(256) fakequant_kernel(const WT* __restrict__ W, int N, int K, int G,
+__global__ void __launch_bounds__(256) fakequant_kernel(const WT* __restrict__ W, int64_t ngroups, int K, int G,
                                                         const float* __restrict__ s,
                                                         const float* __restrict__ inv_s, float qmax,
                                                         float floor_, uint16_t* __restrict__ op,
-                                                        int64_t slot_elems, int64_t units) {
+                                                        int64_t slot_elems) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t unit = t >> 4;  // (row block, column group)
-  const int sub = (int)(t & 15);
-  const bool valid_unit = unit < units;
-  const int cgroups = K >> 7;
-  const int64_t u = valid_unit ? unit : 0;
-  const int row0 = (int)(u / cgroups) * kFqRows;
-  const int col = (int)(u % cgroups) * 128 + sub * 8;
-  float w[kFqRows][8];
-  bool rv[kFqRows];
-#pragma unroll
-  for (int i = 0; i < kFqRows; ++i) {
-    rv[i] = valid_unit && (row0 + i < N);
-    const int r = rv[i] ? row0 + i : 0;
-    WLoad<WT>::load8(W + (size_t)r * K + col, w[i]);
-    if (REF && rv[i]) {
-      uint4 o;
-      o.x = pack_bf16x2(w[i][0], w[i][1]);
-      o.y = pack_bf16x2(w[i][2], w[i][3]);
-      o.z = pack_bf16x2(w[i][4], w[i][5]);
-      o.w = pack_bf16x2(w[i][6], w[i][7]);
-      *reinterpret_cast<uint4*>(op + (size_t)G * slot_elems + (size_t)r * K + col) = o;
-    }
+  const int64_t gid = t >> 3;
+  const int sub = (int)(t & 7);
+  const bool valid = gid < ngroups;
+  const int64_t off = (valid ? gid : 0) * 128 + sub * 16;
+  const int col = (int)(off % K);
+  float w[16];
+  load16w<WT>(W + off, w);
+  if (REF && valid) {
+    uint4 o0, o1;
+    o0.x = pack_bf16x2(w[0], w[1]);
+    o0.y = pack_bf16x2(w[2], w[3]);
+    o0.z = pack_bf16x2(w[4], w[5]);
+    o0.w = pack_bf16x2(w[6], w[7]);
+    o1.x = pack_bf16x2(w[8], w[9]);
+    o1.y = pack_bf16x2(w[10], w[11]);
+    o1.z = pack_bf16x2(w[12], w[13]);
+    o1.w = pack_bf16x2(w[14], w[15]);
+    uint4* dst = reinterpret_cast<uint4*>(op + (size_t)G * slot_elems + off);
+    dst[0] = o0;
+    dst[1] = o1;
   }
   for (int a = 0; a < G; ++a) {
-    float sv[8], iv[8];
-    load8f(s + (size_t)a * K + col, sv);
-    load8f(inv_s + (size_t)a * K + col, iv);
+    float v[16], sv[16];
+    load16f(s + (size_t)a * K + col, sv);
 #pragma unroll
-    for (int i = 0; i < kFqRows; ++i) {
-      float v[8];
-      float mn = INFINITY, mx = -INFINITY;
+    for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(w[e], sv[e]);
+    float mn, mx;
+    group_minmax16(v, mn, mx);
+    const GroupFast g = group_fast(mn, mx, qmax, floor_);
+    float k[16];
+    quant_codes_minus_z<16>(v, g, k);  // q - z
+    float iv[16];
+    load16f(inv_s + (size_t)a * K + col, iv);
+    float r[16];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        v[e] = __fmul_rn(w[i][e], sv[e]);
-        mn = fminf(mn, v[e]);
-        mx = fmaxf(mx, v[e]);
-      }
-#pragma unroll
-      for (int o = 8; o; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      }
-      const GroupFast g = group_fast(mn, mx, qmax, floor_);
-      float r8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float qz = quant_code_minus_z(v[e], g);  // q - z
-        const float dq = __fmul_rn(qz, g.delta);      // dequantised, scaled space
-        r8[e] = REF ? __fmul_rn(dq, iv[e]) : fmaf(dq, iv[e], -w[i][e]);
-      }
-      if (rv[i]) {
-        uint4 o;
-        o.x = pack_bf16x2(r8[0], r8[1]);
-        o.y = pack_bf16x2(r8[2], r8[3]);
-        o.z = pack_bf16x2(r8[4], r8[5]);
-        o.w = pack_bf16x2(r8[6], r8[7]);
-        *reinterpret_cast<uint4*>(op + (size_t)a * slot_elems + (size_t)(row0 + i) * K + col) = o;
-      }
+    for (int e = 0; e < 16; ++e) {
+      const float dq = __fmul_rn(k[e], g.delta);  // dequantised, scaled space
+      r[e] = REF ? __fmul_rn(dq, iv[e]) : fmaf(dq, iv[e], -w[e]);
+    }
+    if (valid) {
+      uint4 o0, o1;
+      o0.x = pack_bf16x2(r[0], r[1]);
+      o0.y = pack_bf16x2(r[2], r[3]);
+      o0.z = pack_bf16x2(r[4], r[5]);
+      o0.w = pack_bf16x2(r[6], r[7]);
+      o1.x = pack_bf16x2(r[8], r[9]);
+      o1.y = pack_bf16x2(r[10], r[11]);
+      o1.z = pack_bf16x2(r[12], r[13]);
+      o1.w = pack_bf16x2(r[14], r[15]);
+      uint4* dst = reinterpret_cast<uint4*>(op + (size_t)a * slot_elems + off);
+      dst[0] = o0;
+      dst[1] = o1;
     }
   }
 }
 
 cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,
                              const float* inv_s, const awq_config& cfg, uint16_t* op, cudaStream_t st) {
-  const int64_t units = (N + kFqRows - 1) / kFqRows * (K / 128);
-  const unsigned blocks = (unsigned)((units * 16 + 255) / 256);
+  const int64_t ngroups = N * K / 128;
+  const unsigned blocks = (unsigned)((ngroups * 8 + 255) / 256);
   const float qmax = (float)((1 << cfg.w_bit) - 1);
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
   const int64_t slot = N * K;
-  const int n = (int)N, k = (int)K, g = cfg.n_grid;
+  const int k = (int)K, g = cfg.n_grid;
   const float fl = cfg.delta_floor;
   if (w_dtype == AWQ_BF16) {
     if (ref)
-      fakequant_kernel<uint16_t, true><<<blocks, 256, 0, st>>>((const uint16_t*)W, n, k, g, s, inv_s, qmax, fl, op,
-                                                               slot, units);
+      fakequant_kernel<uint16_t, true><<<blocks, 256, 0, st>>>((const uint16_t*)W, ngroups, k, g, s, inv_s, qmax,
+                                                               fl, op, slot);
     else
-      fakequant_kernel<uint16_t, false><<<blocks, 256, 0, st>>>((const uint16_t*)W, n, k, g, s, inv_s, qmax, fl,
-                                                                op, slot, units);
+      fakequant_kernel<uint16_t, false><<<blocks, 256, 0, st>>>((const uint16_t*)W, ngroups, k, g, s, inv_s, qmax,
+                                                                fl, op, slot);
   } else {
     if (ref)
-      fakequant_kernel<float, true><<<blocks, 256, 0, st>>>((const float*)W, n, k, g, s, inv_s, qmax, fl, op, slot,
-                                                            units);
+      fakequant_kernel<float, true><<<blocks, 256, 0, st>>>((const float*)W, ngroups, k, g, s, inv_s, qmax, fl,
+                                                            op, slot);
     else
-      fakequant_kernel<float, false><<<blocks, 256, 0, st>>>((const float*)W, n, k, g, s, inv_s, qmax, fl, op,
-                                                             slot, units);
+      fakequant_kernel<float, false><<<blocks, 256, 0, st>>>((const float*)W, ngroups, k, g, s, inv_s, qmax, fl,
+                                                             op, slot);
   }
   return cudaGetLastError();
 }
@@ -329,8 +366,9 @@ cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, c
 // Final codes of W * diag(s) with the same quantiser, 8 codes per int32
 // ("What is AWQ Quantization? ...", "INT4 Weight Packing & Export"), one fp16
 // scale ("AWQ (Activation-Aware Weight Quantization) - AI Glossary", memory
-// example) and one fp16 zero per group. A group is held by 4 lanes with 32
-// weights each; every lane writes its 4 words with one 128-bit store.
+// example) and one fp16 zero per group. A group is held by 8 lanes with 16
+// weights (two words) each; even lanes collect their neighbour's two words
+// and write four words with one 128-bit store.
 
 template <typename WT>
 __global__ void __launch_bounds__(256) pack_kernel(const WT* __restrict__ W, int64_t ngroups, int K,
@@ -338,42 +376,33 @@ __global__ void __launch_bounds__(256) pack_kernel(const WT* __restrict__ W, int
                                                    int32_t* __restrict__ qweight, uint16_t* __restrict__ scales,
                                                    uint16_t* __restrict__ zeros) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t gid = t >> 2;
-  const int sub = (int)(t & 3);
+  const int64_t gid = t >> 3;
+  const int sub = (int)(t & 7);
   const bool valid = gid < ngroups;
-  const int64_t off = (valid ? gid : 0) * 128 + sub * 32;
+  const int64_t off = (valid ? gid : 0) * 128 + sub * 16;
   const int col = (int)(off % K);
-  float v[32];
-  float mn = INFINITY, mx = -INFINITY;
+  float v[16], sv[16];
+  load16w<WT>(W + off, v);
+  load16f(s + col, sv);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float w[8], sv[8];
-    WLoad<WT>::load8(W + off + c * 8, w);
-    load8f(s + col + c * 8, sv);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      v[c * 8 + e] = __fmul_rn(w[e], sv[e]);
-      mn = fminf(mn, v[c * 8 + e]);
-      mx = fmaxf(mx, v[c * 8 + e]);
-    }
-  }
-#pragma unroll
-  for (int o = 2; o; o >>= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
+  for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(v[e], sv[e]);
+  float mn, mx;
+  group_minmax16(v, mn, mx);
   const GroupFast g = group_fast(mn, mx, qmax, floor_);
   const float z = -g.lo;
-  uint32_t words[4];
+  float k[16];
+  quant_codes_minus_z<16>(v, g, k);
+  uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t wd = 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) wd |= (uint32_t)__fadd_rn(quant_code_minus_z(v[k * 8 + e], g), z) << (4 * e);
-    words[k] = wd;
+  for (int e = 0; e < 8; ++e) {
+    w0 |= (uint32_t)__fadd_rn(k[e], z) << (4 * e);
+    w1 |= (uint32_t)__fadd_rn(k[8 + e], z) << (4 * e);
   }
+  const uint32_t w2 = __shfl_down_sync(0xffffffffu, w0, 1);
+  const uint32_t w3 = __shfl_down_sync(0xffffffffu, w1, 1);
   if (valid) {
-    *reinterpret_cast<uint4*>(qweight + gid * 16 + sub * 4) = make_uint4(words[0], words[1], words[2], words[3]);
+    if ((sub & 1) == 0)
+      *reinterpret_cast<uint4*>(qweight + gid * 16 + sub * 2) = make_uint4(w0, w1, w2, w3);
     if (sub == 0) {
       scales[gid] = __half_as_ushort(__float2half_rn(g.delta));
       zeros[gid] = __half_as_ushort(__float2half_rn(z));
@@ -384,7 +413,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const WT* __restrict__ W, int
 cudaError_t launch_pack(const void* W, int w_dtype, int64_t N, int64_t K, const float* s, const awq_config& cfg,
                         int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
   const int64_t ngroups = N * K / 128;
-  const unsigned blocks = (unsigned)((ngroups * 4 + 255) / 256);
+  const unsigned blocks = (unsigned)((ngroups * 8 + 255) / 256);
   const float qmax = (float)((1 << cfg.w_bit) - 1);
   if (w_dtype == AWQ_BF16)
     pack_kernel<uint16_t><<<blocks, 256, 0, st>>>((const uint16_t*)W, ngroups, (int)K, s, qmax, cfg.delta_floor,

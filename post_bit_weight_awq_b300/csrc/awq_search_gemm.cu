@@ -14,6 +14,14 @@
 // Structure (one CTA per SM, persistent over tiles, 192 threads):
 //   warp 0, lane 0 : TMA producer. X tile [128 x 64] and operand tile
 //                    [256 x 64] per stage, 128-byte swizzle, 4-stage ring.
+//                    With a cluster of CM CTAs along the token dimension
+//                    (RESIDUAL form), the CM CTAs work on CM token tiles of
+//                    the same output-row block: each loads its own X tile
+//                    and one 1/CM slice of the shared operand tile, which
+//                    TMA multicasts into every CTA of the cluster, so L2
+//                    serves (16 + 32/CM) KiB per CTA per stage instead of
+//                    48 KiB. A stage is refilled only after the MMAs of
+//                    every CTA in the cluster have released it.
 //   warp 1         : allocates 512 tensor-memory columns; lane 0 issues
 //                    tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) and
 //                    commits completions to mbarriers.
@@ -48,7 +56,8 @@ struct Params {
   int mt, nt;         // token tiles, output-row tiles
   int kb;             // K blocks of 64
   int G;              // alphas
-  int items;          // work items (RESIDUAL: G*mt*nt tiles; REFERENCE: mt*nt tiles)
+  int mtg;            // token-tile groups of the cluster size: ceil(mt / CM)
+  int items;          // work items (RESIDUAL: G*mtg*nt; REFERENCE: mt*nt)
   uint64_t timeout_ns;
   float* partials;    // [G][mt][nt][4]
   uint32_t* status;
@@ -57,17 +66,19 @@ struct Params {
   int withhold_first_fill;  // test aid: leave out each CTA's first operand fill
 };
 
-__device__ __forceinline__ void decode_tile(int t, const Params& p, int& mb, int& nb) {
-  const int span = GROUP_M * p.nt;
+// Tile t of an m_tiles x nt grid, rastered in groups of `group` token tiles
+// so that concurrently running CTAs share operand panels in L2.
+__device__ __forceinline__ void decode_tile(int t, int m_tiles, int nt, int group, int& mb, int& nb) {
+  const int span = group * nt;
   const int grp = t / span;
-  const int first_m = grp * GROUP_M;
-  const int gm = min(GROUP_M, p.mt - first_m);
+  const int first_m = grp * group;
+  const int gm = min(group, m_tiles - first_m);
   const int r = t - grp * span;
   mb = first_m + r % gm;
   nb = r / gm;
 }
 
-template <bool REF>
+template <bool REF, int CM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     search_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                        const Params p) {
@@ -87,11 +98,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  static_assert(!REF || CM == 1, "the REFERENCE form runs without clusters");
+  constexpr uint16_t kMask = (uint16_t)((1u << CM) - 1u);
+  constexpr int kSliceRows = BN / CM;
+  const int rank = CM > 1 ? (int)cluster_ctarank() : 0;
+  const int cluster = blockIdx.x / CM;
+  const int nclusters = gridDim.x / CM;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CM);  // released by the MMAs of every CTA in the cluster
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -111,6 +128,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CM > 1) cluster_sync_all();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int passes = REF ? p.G + 1 : 1;
@@ -122,14 +140,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t used = 0, last_par = 0;  // per-stage bit: stage used; parity of its last fill
       bool ok = true;
       bool withhold = p.withhold_first_fill != 0;
-      for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x) {
+      for (int it = cluster; it < p.items && ok; it += nclusters) {
         int a = 0, t = it;
         if (!REF) {
-          a = it / (p.mt * p.nt);
-          t = it - a * p.mt * p.nt;
+          a = it / (p.mtg * p.nt);
+          t = it - a * p.mtg * p.nt;
         }
-        int mb, nb;
-        decode_tile(t, p, mb, nb);
+        int mg, nb;
+        decode_tile(t, p.mtg, p.nt, GROUP_M / CM, mg, nb);
+        const int mb = mg * CM + rank;
         for (int pass = 0; pass < passes && ok; ++pass) {
           const int slot = REF ? (pass == 0 ? p.G : pass - 1) : a;
           for (int kb = 0; kb < p.kb; ++kb) {
@@ -143,7 +162,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
               mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
               tma_load_2d(sA + stage * A_BYTES, &tmX, &full[stage], kb * BK, mb * BM);
-              tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nb * BN, slot);
+              if (CM == 1)
+                tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nb * BN, slot);
+              else
+                tma_load_3d_multicast(sB + stage * B_BYTES + rank * (kSliceRows * BK * 2), &tmB, &full[stage],
+                                      kb * BK, nb * BN + rank * kSliceRows, slot, kMask);
               used |= 1u << stage;
               last_par = (last_par & ~(1u << stage)) | (phase << stage);
             }
@@ -165,7 +188,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t ph = 0;  // bit b: parity of accumulator buffer b
       uint32_t local = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x, ++local) {
+      for (int it = cluster; it < p.items && ok; it += nclusters, ++local) {
         for (int pass = 0; pass < passes && ok; ++pass) {
           // RESIDUAL: alternate buffers per tile. REFERENCE: Y -> buffer 1, D_i -> buffer 0.
           const int buf = REF ? (pass == 0 ? 1 : 0) : (int)(local & 1u);
@@ -187,7 +210,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int k = 0; k < BK / 16; ++k)
               umma_bf16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), IDESC,
                         (kb > 0 || k > 0) ? 1u : 0u);
-            umma_commit(&empty[stage]);
+            if (CM == 1)
+              umma_commit(&empty[stage]);
+            else
+              umma_commit_multicast(&empty[stage], kMask);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -209,14 +235,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t ph = 0;  // bit b: parity of accumulator buffer b
     uint32_t local = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x, ++local) {
+    for (int it = cluster; it < p.items && ok; it += nclusters, ++local) {
       int a = 0, t = it;
       if (!REF) {
-        a = it / (p.mt * p.nt);
-        t = it - a * p.mt * p.nt;
+        a = it / (p.mtg * p.nt);
+        t = it - a * p.mtg * p.nt;
       }
-      int mb, nb;
-      decode_tile(t, p, mb, nb);
+      int mg, nb;
+      decode_tile(t, p.mtg, p.nt, GROUP_M / CM, mg, nb);
+      const int mb = mg * CM + rank;
       if (REF) {
         // All lanes wait; the warp goes on only if every lane saw the phase
         // complete, so the warp-collective tensor-memory loads stay converged.
@@ -270,7 +297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         const int alpha = REF ? pass - 1 : a;
-        if (lane == 0) p.partials[((((size_t)alpha * p.mt + mb) * p.nt + nb) << 2) + q] = ss;
+        if (lane == 0 && mb < p.mt) p.partials[((((size_t)alpha * p.mt + mb) * p.nt + nb) << 2) + q] = ss;
       }
       if (REF && ok) {
         tc_fence_before();
@@ -283,6 +310,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (CM > 1) cluster_sync_all();  // no peer still multicasts into this CTA or arrives on its barriers
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -323,19 +351,51 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
+template <int CM>
+cudaError_t launch_residual(const CUtensorMap& tmX, const CUtensorMap& tmB, Params p, int sms, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(search_gemm_kernel<false, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.blockDim = dim3(NUM_THREADS);
+  lc.dynamicSmemBytes = SMEM_BYTES;
+  lc.stream = st;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int clusters = sms / CM;
+  if (CM > 1) {
+    lc.gridDim = dim3(CM * clusters);
+    int active = 0;
+    e = cudaOccupancyMaxActiveClusters(&active, search_gemm_kernel<false, CM>, &lc);
+    if (e != cudaSuccess) return e;
+    if (active > 0 && active < clusters) clusters = active;
+  }
+  if (clusters > p.items) clusters = p.items;
+  lc.gridDim = dim3(CM * clusters);
+  return cudaLaunchKernelEx(&lc, search_gemm_kernel<false, CM>, tmX, tmB, p);
+}
+
 }  // namespace
 
 cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
                                const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
-                               float* dump, int withhold_first_fill) {
+                               float* dump, int withhold_first_fill, int cluster_m) {
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
   const int G = cfg.n_grid;
   const int slots = ref ? G + 1 : G;
+  int CM = cluster_m > 0 ? cluster_m : kDefaultClusterM;
+  if (ref || withhold_first_fill) CM = 1;
+  if (CM != 1 && CM != 2 && CM != 4) return cudaErrorInvalidValue;
   CUtensorMap tmX, tmB;
   const cuuint64_t xd[2] = {(cuuint64_t)K, (cuuint64_t)n_tok};
   const cuuint32_t xb[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
   const cuuint64_t bd[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)slots};
-  const cuuint32_t bb[3] = {(cuuint32_t)BK, (cuuint32_t)BN, 1u};
+  const cuuint32_t bb[3] = {(cuuint32_t)BK, (cuuint32_t)(BN / CM), 1u};
   if (!make_map(&tmX, X, 2, xd, xb) || !make_map(&tmB, op, 3, bd, bb)) return cudaErrorInvalidValue;
 
   int dev = 0, sms = 0;
@@ -347,9 +407,10 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
   Params p;
   p.mt = (int)((n_tok + BM - 1) / BM);
   p.nt = (int)((N + BN - 1) / BN);
+  p.mtg = (p.mt + CM - 1) / CM;
   p.kb = (int)(K / BK);
   p.G = G;
-  p.items = ref ? p.mt * p.nt : G * p.mt * p.nt;
+  p.items = ref ? p.mt * p.nt : G * p.mtg * p.nt;
   const uint32_t ms = cfg.wait_timeout_ms ? cfg.wait_timeout_ms : 2000u;
   p.timeout_ns = (uint64_t)ms * 1000000ull;
   p.partials = partials;
@@ -358,18 +419,19 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
   p.n_tok = (int)n_tok;
   p.N = (int)N;
   p.withhold_first_fill = withhold_first_fill;
-  const int grid = p.items < sms ? p.items : sms;
 
   if (ref) {
-    e = cudaFuncSetAttribute(search_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    search_gemm_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);
-  } else {
-    e = cudaFuncSetAttribute(search_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(search_gemm_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    search_gemm_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);
+    const int grid = p.items < sms ? p.items : sms;
+    search_gemm_kernel<true, 1><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);
+    return cudaGetLastError();
   }
+  if (CM == 1) e = launch_residual<1>(tmX, tmB, p, sms, st);
+  else if (CM == 2) e = launch_residual<2>(tmX, tmB, p, sms, st);
+  else e = launch_residual<4>(tmX, tmB, p, sms, st);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -51,13 +51,48 @@ def _run_layer(L, cfg):
     return q
 
 
-def _check_levels(losses_gpu, best_gpu, losses_oracle):
+def _check_levels(losses_gpu, best_gpu, losses_oracle, bound=None):
+    """Levels 2 and 3. ``bound`` (per alpha) is the loss error the kernels'
+    arithmetic allows; it replaces the 1e-2 figure only where it is larger,
+    which happens on layers too small for rounding errors to average out."""
     lo = np.asarray(losses_oracle, dtype=np.float64)
     lg = np.asarray(losses_gpu, dtype=np.float64)
-    rel = np.abs(lg - lo) / lo
-    assert rel.max() <= LOSS_RTOL, f"per-alpha loss off by {rel.max():.3e}"
-    assert lo[best_gpu] <= ARGMIN_SLACK * lo.min()
-    return rel.max()
+    tol = LOSS_RTOL * lo if bound is None else np.maximum(LOSS_RTOL * lo, bound)
+    err = np.abs(lg - lo)
+    assert np.all(err <= tol), f"per-alpha loss off by {np.max(err / lo):.3e} (allowed {np.min(tol / lo):.3e}+)"
+    i_min = int(np.argmin(lo))
+    slack = 0.0 if bound is None else bound[best_gpu] + bound[i_min]
+    assert lo[best_gpu] <= ARGMIN_SLACK * lo.min() + slack
+    return np.max(err / lo)
+
+
+def _arithmetic_bound(L, sx32, form):
+    """Largest |L_gpu - L_oracle| per alpha allowed by the GPU's arithmetic.
+
+    Each product element y = x . op differs from the exact one by at most
+    b = sum_k |x_k| * (operand rounding) + K * 2^-24 * sum_k |x_k| |op_k|
+    (bf16 operands: unit roundoff 2^-8; fp32 accumulation over K terms), so
+    the mean of y^2 moves by at most mean(2 |y| b + b^2)."""
+    W = L["W"].astype(np.float64)
+    X = L["X"].astype(np.float64)
+    n, K = X.shape
+    N = W.shape[0]
+    ax = np.abs(X)
+    w_is_bf16 = L["w_dtype"] == "bf16"
+    out = []
+    for a in O.alpha_grid(20):
+        Wh = O.fake_quantize(W, O.f32(O.awq_scales(sx32, a)))
+        E = Wh - W
+        y = X @ E.T
+        if form == capi.AWQ_LOSS_RESIDUAL:
+            rnd = 2.0**-8 * np.abs(E) + 2.0**-20 * (np.abs(W) + np.abs(Wh))
+            mag = np.abs(E)
+        else:
+            rnd = 2.0**-8 * np.abs(Wh) + (0.0 if w_is_bf16 else 2.0**-8 * np.abs(W))
+            mag = np.abs(Wh) + np.abs(W)
+        b = ax @ rnd.T + K * 2.0**-24 * (ax @ mag.T)
+        out.append(np.sum(2.0 * np.abs(y) * b + b * b) / (n * N))
+    return np.array(out)
 
 
 def _check_pack(L, s32, rows=None):
@@ -107,14 +142,18 @@ def _search_with_statistic(L, sx32, cfg):
 @pytest.mark.parametrize("n,N,K", [(1, 7, 128), (129, 130, 256), (257, 300, 384), (64, 1, 128), (300, 520, 1024)])
 def test_ragged_shapes(n, N, K):
     """Ragged tiles on every side, with both sides deciding codes from the
-    same fp32 statistic (tiny layers are otherwise dominated by single codes
-    that a one-ulp difference in the statistic can move)."""
+    same fp32 statistic. With a single token or a single output row the
+    rounding of the bf16 operands does not average out (the REFERENCE form
+    rounds W_hat itself to bf16), so those two shapes use the worst-case bound
+    derived from the arithmetic where it exceeds 1e-2; all others use 1e-2."""
     L = workloads.make_layer("llama7b_q_proj", n_tok=n, out_features=N, in_features=K, seed=n + N)
     sx32 = O.f32(O.channel_importance(L["X"]))
     res = _oracle_losses(L["W"], L["X"], sx=sx32)
+    degenerate = n == 1 or N == 1  # a single token or a single output: nothing averages
     for form in (capi.AWQ_LOSS_RESIDUAL, capi.AWQ_LOSS_REFERENCE):
         losses, best, s_best = _search_with_statistic(L, sx32, capi.config(loss_form=form))
-        _check_levels(losses, best, res["losses"])
+        bound = _arithmetic_bound(L, sx32, form) if degenerate else None
+        _check_levels(losses, best, res["losses"], bound=bound)
         if best == res["best_idx"]:
             np.testing.assert_array_equal(s_best, O.f32(res["s_best"]))
     _check_pack(L, O.f32(res["s_best"]))

@@ -114,9 +114,10 @@ def test_fakequant_codes_and_values(layer, rows, form):
 # ------------------------------------------------------------------ search product
 
 
+@pytest.mark.parametrize("cluster_m", [1, 2, 4])
 @pytest.mark.parametrize("n,N,K,G", [(128, 256, 128, 1), (300, 520, 384, 3), (1, 7, 128, 2), (257, 130, 256, 2),
                                      (512, 1024, 1024, 2)])
-def test_search_gemm_products_and_partials(n, N, K, G):
+def test_search_gemm_products_and_partials(n, N, K, G, cluster_m):
     rng = np.random.default_rng(n + 31 * N + 7 * K + G)
     A = _rand_bf16(rng, (n, K))
     B = _rand_bf16(rng, (G, N, K), 0.05)
@@ -126,7 +127,7 @@ def test_search_gemm_products_and_partials(n, N, K, G):
     dump = torch.zeros(G, n, N, dtype=torch.float32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
     capi.awq_search_gemm_dump(dev_bf16(A), dev_bf16(B.reshape(G * N, K)), cfg, partials, status, dump,
-                              n_tok=n, in_features=K, out_features=N)
+                              n_tok=n, in_features=K, out_features=N, cluster_m=cluster_m)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     D = dump.cpu().numpy().astype(np.float64)
@@ -137,7 +138,7 @@ def test_search_gemm_products_and_partials(n, N, K, G):
         scale = np.sqrt(K) * 0.05
         ok = np.allclose(D[i], ref, rtol=1e-5, atol=1e-5 * scale)
         if not ok:
-            save_debug(f"gemm_{n}_{N}_{K}_{G}_{i}", got=D[i], ref=ref, A=A, B=B[i])
+            save_debug(f"gemm_{n}_{N}_{K}_{G}_{i}_c{cluster_m}", got=D[i], ref=ref, A=A, B=B[i])
         assert ok, f"product of alpha {i} differs: max err {np.abs(D[i] - ref).max()}"
         sq = ref * ref
         for mb in range(mt):
@@ -147,7 +148,7 @@ def test_search_gemm_products_and_partials(n, N, K, G):
                     c0, c1 = nb * tn, min(nb * tn + tn, N)
                     expect = sq[r0:r1, c0:c1].sum() if r0 < n else 0.0
                     assert P[i, mb, nb, q] == pytest.approx(expect, rel=1e-4, abs=1e-6)
-    # the production entry point gives the same partials
+    # the production entry point (whatever cluster size it uses) gives the same partials
     partials2 = torch.zeros_like(partials)
     capi.awq_search_gemm(dev_bf16(A), dev_bf16(B.reshape(G * N, K)), cfg, partials2, status, n_tok=n,
                          in_features=K, out_features=N)
