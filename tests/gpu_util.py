@@ -7,8 +7,6 @@ import torch
 
 import workloads
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-
 
 def dev_bf16(a32: np.ndarray) -> torch.Tensor:
     """Upload float32 values that are exactly bf16 as a bf16 CUDA tensor."""
@@ -31,7 +29,8 @@ def host_bf16_to_f64(t: torch.Tensor) -> np.ndarray:
 
 
 def save_debug(name: str, **arrays) -> None:
-    """On a failing check, keep the arrays for offline diagnosis."""
-    out = os.path.join(ROOT, "gpurun_out")
-    if os.path.isdir(out):
+    """On a failing check, keep the arrays for offline diagnosis in the
+    folder named by AWQ_DEBUG_DIR (nothing is written when it is unset)."""
+    out = os.environ.get("AWQ_DEBUG_DIR")
+    if out and os.path.isdir(out):
         np.savez_compressed(os.path.join(out, f"debug_{name}.npz"), **arrays)
