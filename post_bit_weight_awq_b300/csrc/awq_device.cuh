@@ -1,5 +1,5 @@
 // Device-side helpers of the AWQ search/pack kernels for sm_103a:
-//   - the group quantiser, in correctly rounded fp32 steps;
+//   - bf16 and status helpers;
 //   - thin inline-PTX wrappers for mbarrier, TMA (cp.async.bulk.tensor) and
 //     the 5th-generation tensor core (tcgen05: MMA, tensor memory, commit);
 //   - bounded waits that give up with a status instead of spinning forever.
@@ -14,85 +14,6 @@
 #include "awq.h"
 
 namespace awq {
-
-// ----------------------------------------------------------------- quantiser
-//
-// Group-wise asymmetric min/max quantisation ("AWQ > Salient Weight
-// Preservation", step-size equation: the group's range over 2^b - 1 levels;
-// zero point on as in the deployment quant_config of "AWQ: How
-// Activation-Aware Quantization Saves 4-bit LLMs"). Every step is a correctly
-// rounded fp32 operation, in this order, so that codes are reproducible
-// bit for bit:
-//   delta = max(fl(fl(vmax - vmin) / qmax), floor)
-//   z     = rne(fl(-vmin / delta))
-//   q     = clamp(rne(fl(v / delta)) + z, 0, qmax)
-// rintf is round-half-to-even; __f*_rn forbid contraction into FMAs.
-struct GroupQ {
-  float delta;
-  float z;
-};
-
-__device__ __forceinline__ GroupQ group_params(float vmin, float vmax, float qmax, float floor_) {
-  GroupQ g;
-  g.delta = fmaxf(__fdiv_rn(__fsub_rn(vmax, vmin), qmax), floor_);
-  g.z = rintf(__fdiv_rn(-vmin, g.delta));
-  return g;
-}
-
-// The rounding decision of q without a division per weight.
-// With r = rn(1/delta) and t = rn(v * r):
-//   |t - rn(v/delta)| <= |v/delta| * (3 * 2^-24 + 2^-48) < |t| * 2^-20,
-// so when |t - rint(t)| < 1/2 - |t| * 2^-19 (twice that bound, with |t|
-// taken at the group's largest magnitude) the correctly rounded quotient
-// lies strictly inside (rint(t) - 1/2, rint(t) + 1/2) and rounds to rint(t).
-// t - rint(t) is exact in fp32. Only values within that margin of a tie
-// (probability ~ |t| * 2^-18 each) send their lane to the IEEE division.
-// Codes are monotone in v, and the smallest value of a group always gets
-// q - z = rne(rn(vmin/delta)) = -rne(rn(-vmin/delta)) = -z exactly, so the
-// clamp to [0, qmax] can only bind at the top; `clamp` records whether the
-// largest value's code exceeds qmax, decided once per group.
-struct GroupFast {
-  float delta;  // step
-  float r;      // rn(1 / delta)
-  float lo;     // -z:       smallest value of q - z
-  float hi;     // qmax - z: largest value of q - z
-  float edge;   // 1/2 - max|t| * 2^-19 over the group
-  bool clamp;   // some code of the group lies above qmax before clamping
-};
-
-__device__ __forceinline__ GroupFast group_fast(float vmin, float vmax, float qmax, float floor_) {
-  const GroupQ g = group_params(vmin, vmax, qmax, floor_);
-  GroupFast f;
-  f.delta = g.delta;
-  f.r = __frcp_rn(g.delta);
-  f.lo = -g.z;
-  f.hi = __fsub_rn(qmax, g.z);
-  const float tmax = __fmul_rn(fmaxf(fabsf(vmin), fabsf(vmax)), f.r);
-  f.edge = __fsub_rn(0.5f, __fmul_rn(tmax, 0x1p-19f));
-  f.clamp = rintf(__fdiv_rn(vmax, g.delta)) > f.hi;
-  return f;
-}
-
-// q - z = clamp(rne(rn(v / delta)), -z, qmax - z) for N values of one group
-// (exact small integers in fp32).
-template <int N>
-__device__ __forceinline__ void quant_codes_minus_z(const float (&v)[N], const GroupFast& f, float (&k)[N]) {
-  float dmax = 0.0f;
-#pragma unroll
-  for (int e = 0; e < N; ++e) {
-    const float t = __fmul_rn(v[e], f.r);
-    k[e] = rintf(t);
-    dmax = fmaxf(dmax, fabsf(__fsub_rn(t, k[e])));
-  }
-  if (!(dmax < f.edge)) {
-#pragma unroll
-    for (int e = 0; e < N; ++e) k[e] = rintf(__fdiv_rn(v[e], f.delta));
-  }
-  if (f.clamp) {
-#pragma unroll
-    for (int e = 0; e < N; ++e) k[e] = fminf(fmaxf(k[e], f.lo), f.hi);
-  }
-}
 
 // ----------------------------------------------------------------- bf16 helpers
 

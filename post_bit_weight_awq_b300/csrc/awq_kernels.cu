@@ -8,6 +8,7 @@
 
 #include "awq_device.cuh"
 #include "awq_launch.h"
+#include "awq_quant.cuh"
 
 namespace awq {
 
@@ -177,7 +178,7 @@ struct WLoad;
 
 template <>
 struct WLoad<uint16_t> {  // bf16 bits
-  static __device__ __forceinline__ void load8(const uint16_t* p, float (&w)[8]) {
+  static __device__ __forceinline__ void load8(const uint16_t* p, float* w) {
     const uint4 v = *reinterpret_cast<const uint4*>(p);
     w[0] = bf16_lo(v.x);
     w[1] = bf16_hi(v.x);
@@ -192,7 +193,7 @@ struct WLoad<uint16_t> {  // bf16 bits
 
 template <>
 struct WLoad<float> {
-  static __device__ __forceinline__ void load8(const float* p, float (&w)[8]) {
+  static __device__ __forceinline__ void load8(const float* p, float* w) {
     const float4 a = *reinterpret_cast<const float4*>(p);
     const float4 b = *reinterpret_cast<const float4*>(p + 4);
     w[0] = a.x;
@@ -206,7 +207,7 @@ struct WLoad<float> {
   }
 };
 
-__device__ __forceinline__ void load8f(const float* p, float (&v)[8]) {
+__device__ __forceinline__ void load8f(const float* p, float* v) {
   const float4 a = *reinterpret_cast<const float4*>(p);
   const float4 b = *reinterpret_cast<const float4*>(p + 4);
   v[0] = a.x;
@@ -219,38 +220,10 @@ __device__ __forceinline__ void load8f(const float* p, float (&v)[8]) {
   v[7] = b.w;
 }
 
-template <typename WT>
-__device__ __forceinline__ void load16w(const WT* p, float (&w)[16]) {
-  float a[8], b[8];
-  WLoad<WT>::load8(p, a);
-  WLoad<WT>::load8(p + 8, b);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    w[e] = a[e];
-    w[8 + e] = b[e];
-  }
-}
-
-__device__ __forceinline__ void load16f(const float* p, float (&v)[16]) {
-  float a[8], b[8];
-  load8f(p, a);
-  load8f(p + 8, b);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    v[e] = a[e];
-    v[8 + e] = b[e];
-  }
-}
-
-// Group min/max of 16 values per lane over the 8 lanes of a group.
+// Group minimum and maximum of 16 values per lane over the 8 lanes of a group
+// (lanes 8j .. 8j+7 of the warp).
 __device__ __forceinline__ void group_minmax16(const float (&v)[16], float& mn, float& mx) {
-  mn = v[0];
-  mx = v[0];
-#pragma unroll
-  for (int e = 1; e < 16; ++e) {
-    mn = fminf(mn, v[e]);
-    mx = fmaxf(mx, v[e]);
-  }
+  minmax_n<16>(v, mn, mx);
 #pragma unroll
   for (int o = 4; o; o >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
@@ -258,107 +231,235 @@ __device__ __forceinline__ void group_minmax16(const float (&v)[16], float& mn, 
   }
 }
 
+__device__ __forceinline__ uint4 pack_bf16x8(const float* r) {
+  uint4 o;
+  o.x = pack_bf16x2(r[0], r[1]);
+  o.y = pack_bf16x2(r[2], r[3]);
+  o.z = pack_bf16x2(r[4], r[5]);
+  o.w = pack_bf16x2(r[6], r[7]);
+  return o;
+}
+
 // ============================================================== fake-quant
 //
 // For every alpha_i: W_hat_i = Q(W * s_i) * (1 / s_i), the scale-quantise-
 // fold-back step of the search_scale listing ("AWQ: How Activation-Aware
 // Quantization Saves 4-bit LLMs"), justified by the scaling equation of "AWQ
-// > Salient Weight Preservation". A group of 128 weights is held by 8 lanes
-// with 16 weights each (two 16-byte loads); W is read once and every alpha is
-// produced from registers, so per alpha a lane does two shuffle steps of the
-// group reduction, the group's step, zero point and clamp decision, and 16
-// division-free exact code decisions.
+// > Salient Weight Preservation".
 // RESIDUAL writes bf16(W_hat_i - W); REFERENCE writes bf16(W_hat_i) and, in
 // slot G, bf16(W).
+//
+// A block owns a strip of 512 input channels (four groups) and a range of
+// output rows; each warp takes one row of the strip at a time, 8 lanes per
+// group and 16 weights per lane: lane l of a group holds channels
+// [8l, 8l+8) and [64+8l, 64+8l+8), so each 16-byte load or store of the warp
+// covers four whole 128-byte segments. The strip's s and 1/s for a chunk of
+// alphas are staged in shared memory once per block, in lane order (float4 q
+// of lane l at [q][l]) so that every 16-byte shared load of a warp reads 512
+// contiguous bytes without bank conflicts, and reused by every row. W is read
+// once (the next row's weights are loaded while the current row runs through
+// its alphas). Products, differences and the dequantisation run as packed
+// fp32 pairs (one instruction, two correctly rounded results).
+
+constexpr int kFqCols = 512;        // input channels per strip (4 groups)
+constexpr int kFqWarps = 8;         // rows in flight per block
+constexpr int kFqAlphaChunk = 20;   // alphas staged in shared memory at once
+constexpr int kFqSmem = 2 * kFqAlphaChunk * kFqCols * 4;  // s and 1/s: 80 KiB
+constexpr int kFqBlocksPerSm = 2;
+
+template <typename WT>
+struct RowRegs;
+template <>
+struct RowRegs<uint16_t> {
+  uint4 a, b;
+  __device__ __forceinline__ void load(const uint16_t* p) {
+    a = *reinterpret_cast<const uint4*>(p);
+    b = *reinterpret_cast<const uint4*>(p + 64);
+  }
+  __device__ __forceinline__ void unpack(float2 (&w)[8]) const {
+    const uint32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = make_float2(bf16_lo(x[i]), bf16_hi(x[i]));
+  }
+};
+template <>
+struct RowRegs<float> {
+  float4 a0, a1, b0, b1;
+  __device__ __forceinline__ void load(const float* p) {
+    a0 = *reinterpret_cast<const float4*>(p);
+    a1 = *reinterpret_cast<const float4*>(p + 4);
+    b0 = *reinterpret_cast<const float4*>(p + 64);
+    b1 = *reinterpret_cast<const float4*>(p + 68);
+  }
+  __device__ __forceinline__ void unpack(float2 (&w)[8]) const {
+    const float4 x[4] = {a0, a1, b0, b1};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[2 * i] = make_float2(x[i].x, x[i].y);
+      w[2 * i + 1] = make_float2(x[i].z, x[i].w);
+    }
+  }
+};
+
+// The 16 values of one lane from a lane-ordered shared-memory row [4][32] of float4.
+__device__ __forceinline__ void lds_lane16(const float4* row, int lane, float2 (&v)[8]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 x = row[q * 32 + lane];
+    v[2 * q] = make_float2(x.x, x.y);
+    v[2 * q + 1] = make_float2(x.z, x.w);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
 
 template <typename WT, bool REF>
-__global__ void __launch_bounds__(256) fakequant_kernel(const WT* __restrict__ W, int64_t ngroups, int K, int G,
-                                                        const float* __restrict__ s,
-                                                        const float* __restrict__ inv_s, float qmax,
-                                                        float floor_, uint16_t* __restrict__ op,
-                                                        int64_t slot_elems) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t gid = t >> 3;
-  const int sub = (int)(t & 7);
-  const bool valid = gid < ngroups;
-  const int64_t off = (valid ? gid : 0) * 128 + sub * 16;
-  const int col = (int)(off % K);
-  float w[16];
-  load16w<WT>(W + off, w);
-  if (REF && valid) {
-    uint4 o0, o1;
-    o0.x = pack_bf16x2(w[0], w[1]);
-    o0.y = pack_bf16x2(w[2], w[3]);
-    o0.z = pack_bf16x2(w[4], w[5]);
-    o0.w = pack_bf16x2(w[6], w[7]);
-    o1.x = pack_bf16x2(w[8], w[9]);
-    o1.y = pack_bf16x2(w[10], w[11]);
-    o1.z = pack_bf16x2(w[12], w[13]);
-    o1.w = pack_bf16x2(w[14], w[15]);
-    uint4* dst = reinterpret_cast<uint4*>(op + (size_t)G * slot_elems + off);
-    dst[0] = o0;
-    dst[1] = o1;
-  }
-  for (int a = 0; a < G; ++a) {
-    float v[16], sv[16];
-    load16f(s + (size_t)a * K + col, sv);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(w[e], sv[e]);
-    float mn, mx;
-    group_minmax16(v, mn, mx);
-    const GroupFast g = group_fast(mn, mx, qmax, floor_);
-    float k[16];
-    quant_codes_minus_z<16>(v, g, k);  // q - z
-    float iv[16];
-    load16f(inv_s + (size_t)a * K + col, iv);
-    float r[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float dq = __fmul_rn(k[e], g.delta);  // dequantised, scaled space
-      r[e] = REF ? __fmul_rn(dq, iv[e]) : fmaf(dq, iv[e], -w[e]);
+__global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
+    fakequant_kernel(const WT* __restrict__ W, int N, int K, int G, const float* __restrict__ s,
+                     const float* __restrict__ inv_s, float qmax, float floor_, uint16_t* __restrict__ op,
+                     int64_t slot_elems, int nstrips, int rows_per_block) {
+  extern __shared__ float4 fq_smem[];
+  float4* ss = fq_smem;                          // [chunk][4][32] float4
+  float4* si = fq_smem + kFqAlphaChunk * 128;    // same for 1/s
+  const int strip = blockIdx.x % nstrips;
+  const int col0 = strip * kFqCols;
+  const int ncols = min(kFqCols, K - col0);  // a multiple of 128
+  const int r_begin = (blockIdx.x / nstrips) * rows_per_block;
+  const int r_end = min(N, r_begin + rows_per_block);
+  if (r_begin >= r_end) return;  // uniform over the block
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane >> 3, sub = lane & 7;
+  // Groups past a partial strip repeat group 0's work and store nothing.
+  const bool active = grp * 128 < ncols;
+  const int slane = active ? lane : sub;
+  const int c_lo = (active ? grp * 128 : 0) + sub * 8;  // channels c_lo + [0,8) and c_lo + 64 + [0,8)
+
+  for (int a0 = 0; a0 < G; a0 += kFqAlphaChunk) {
+    const int gc = min(kFqAlphaChunk, G - a0);
+    __syncthreads();  // the previous chunk's scales are no longer read
+    const int c4n = ncols >> 2;
+    for (int i = threadIdx.x; i < gc * c4n; i += blockDim.x) {
+      const int a = i / c4n, c4 = i - a * c4n;
+      const int c = 4 * c4;  // channel within the strip -> (lane, float4 index q)
+      const int e = c & 127, h = e & 63;
+      const int ln = (c >> 7) * 8 + (h >> 3);
+      const int q = (e >> 6) * 2 + ((h & 7) >> 2);
+      const size_t g = (size_t)(a0 + a) * K + col0 + c;
+      ss[(a * 4 + q) * 32 + ln] = *reinterpret_cast<const float4*>(s + g);
+      si[(a * 4 + q) * 32 + ln] = *reinterpret_cast<const float4*>(inv_s + g);
     }
-    if (valid) {
-      uint4 o0, o1;
-      o0.x = pack_bf16x2(r[0], r[1]);
-      o0.y = pack_bf16x2(r[2], r[3]);
-      o0.z = pack_bf16x2(r[4], r[5]);
-      o0.w = pack_bf16x2(r[6], r[7]);
-      o1.x = pack_bf16x2(r[8], r[9]);
-      o1.y = pack_bf16x2(r[10], r[11]);
-      o1.z = pack_bf16x2(r[12], r[13]);
-      o1.w = pack_bf16x2(r[14], r[15]);
-      uint4* dst = reinterpret_cast<uint4*>(op + (size_t)a * slot_elems + off);
-      dst[0] = o0;
-      dst[1] = o1;
+    __syncthreads();
+
+    int row = r_begin + warp;
+    RowRegs<WT> nxt;
+    if (row < r_end) nxt.load(W + (size_t)row * K + col0 + c_lo);
+    for (; row < r_end; row += kFqWarps) {
+      float2 w[8];
+      nxt.unpack(w);
+      const size_t base = (size_t)row * K + col0 + c_lo;
+      if (row + kFqWarps < r_end) nxt.load(W + base + (size_t)kFqWarps * K);
+      if (REF && a0 == 0 && active) {
+        uint4* dst = reinterpret_cast<uint4*>(op + (size_t)G * slot_elems + base);
+        dst[0] = make_uint4(pack_bf16x2(w[0]), pack_bf16x2(w[1]), pack_bf16x2(w[2]), pack_bf16x2(w[3]));
+        dst[8] = make_uint4(pack_bf16x2(w[4]), pack_bf16x2(w[5]), pack_bf16x2(w[6]), pack_bf16x2(w[7]));
+      }
+      float2 nw[8];  // -w
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nw[i] = make_float2(-w[i].x, -w[i].y);
+#pragma unroll 1
+      for (int a = 0; a < gc; ++a) {
+        float2 v[8];
+        {
+          float2 sv[8];
+          lds_lane16(ss + a * 128, slane, sv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = __fmul2_rn(w[i], sv[i]);
+        }
+        float mn = fminf(v[0].x, v[0].y), mx = fmaxf(v[0].x, v[0].y);
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+          mn = fmin3f(mn, v[i].x, v[i].y);
+          mx = fmax3f(mx, v[i].x, v[i].y);
+        }
+#pragma unroll
+        for (int o = 4; o; o >>= 1) {
+          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        const GroupFast g = group_fast(mn, mx, qmax, floor_);
+        // q - z for the lane's 16 values (see quant_codes_minus_z), as pairs
+        float2 k[8];
+        float dmax = 0.0f;
+        const float2 r2 = make_float2(g.r, g.r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 t = __fmul2_rn(v[i], r2);
+          k[i] = make_float2(rintf(t.x), rintf(t.y));
+          const float2 d = __fadd2_rn(t, make_float2(-k[i].x, -k[i].y));
+          dmax = fmax3f(dmax, fabsf(d.x), fabsf(d.y));
+        }
+        if (!(dmax < g.edge)) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            k[i] = make_float2(rintf(__fdiv_rn(v[i].x, g.delta)), rintf(__fdiv_rn(v[i].y, g.delta)));
+        }
+        if (g.clamp) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) k[i] = make_float2(fminf(k[i].x, g.hi), fminf(k[i].y, g.hi));
+        }
+        float2 iv[8];
+        lds_lane16(si + a * 128, slane, iv);
+        const float2 d2 = make_float2(g.delta, g.delta);
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 dq = __fmul2_rn(k[i], d2);  // dequantised, scaled space
+          o[i] = pack_bf16x2(REF ? __fmul2_rn(dq, iv[i]) : __ffma2_rn(dq, iv[i], nw[i]));
+        }
+        if (active) {
+          uint4* dst = reinterpret_cast<uint4*>(op + (size_t)(a0 + a) * slot_elems + base);
+          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          dst[8] = make_uint4(o[4], o[5], o[6], o[7]);  // 64 channels further on
+        }
+      }
     }
   }
 }
 
+template <typename WT, bool REF>
+cudaError_t launch_fakequant_t(const WT* W, int64_t N, int64_t K, const float* s, const float* inv_s,
+                               const awq_config& cfg, uint16_t* op, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(fakequant_kernel<WT, REF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kFqSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int nstrips = (int)((K + kFqCols - 1) / kFqCols);
+  // one wave: at most kFqBlocksPerSm blocks per SM in total
+  int64_t rblocks = (int64_t)sms * kFqBlocksPerSm / nstrips;
+  if (rblocks < 1) rblocks = 1;
+  if (rblocks > N) rblocks = N;
+  const int rows_per_block = (int)((N + rblocks - 1) / rblocks);
+  rblocks = (N + rows_per_block - 1) / rows_per_block;
+  const float qmax = (float)((1 << cfg.w_bit) - 1);
+  fakequant_kernel<WT, REF><<<(unsigned)(rblocks * nstrips), kFqWarps * 32, kFqSmem, st>>>(
+      W, (int)N, (int)K, cfg.n_grid, s, inv_s, qmax, cfg.delta_floor, op, N * K, nstrips, rows_per_block);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,
                              const float* inv_s, const awq_config& cfg, uint16_t* op, cudaStream_t st) {
-  const int64_t ngroups = N * K / 128;
-  const unsigned blocks = (unsigned)((ngroups * 8 + 255) / 256);
-  const float qmax = (float)((1 << cfg.w_bit) - 1);
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
-  const int64_t slot = N * K;
-  const int k = (int)K, g = cfg.n_grid;
-  const float fl = cfg.delta_floor;
   if (w_dtype == AWQ_BF16) {
-    if (ref)
-      fakequant_kernel<uint16_t, true><<<blocks, 256, 0, st>>>((const uint16_t*)W, ngroups, k, g, s, inv_s, qmax,
-                                                               fl, op, slot);
-    else
-      fakequant_kernel<uint16_t, false><<<blocks, 256, 0, st>>>((const uint16_t*)W, ngroups, k, g, s, inv_s, qmax,
-                                                                fl, op, slot);
-  } else {
-    if (ref)
-      fakequant_kernel<float, true><<<blocks, 256, 0, st>>>((const float*)W, ngroups, k, g, s, inv_s, qmax, fl,
-                                                            op, slot);
-    else
-      fakequant_kernel<float, false><<<blocks, 256, 0, st>>>((const float*)W, ngroups, k, g, s, inv_s, qmax, fl,
-                                                             op, slot);
+    const uint16_t* w = (const uint16_t*)W;
+    return ref ? launch_fakequant_t<uint16_t, true>(w, N, K, s, inv_s, cfg, op, st)
+               : launch_fakequant_t<uint16_t, false>(w, N, K, s, inv_s, cfg, op, st);
   }
-  return cudaGetLastError();
+  const float* w = (const float*)W;
+  return ref ? launch_fakequant_t<float, true>(w, N, K, s, inv_s, cfg, op, st)
+             : launch_fakequant_t<float, false>(w, N, K, s, inv_s, cfg, op, st);
 }
 
 // ============================================================== pack
@@ -382,14 +483,16 @@ __global__ void __launch_bounds__(256) pack_kernel(const WT* __restrict__ W, int
   const int64_t off = (valid ? gid : 0) * 128 + sub * 16;
   const int col = (int)(off % K);
   float v[16], sv[16];
-  load16w<WT>(W + off, v);
-  load16f(s + col, sv);
+  WLoad<WT>::load8(W + off, v);
+  WLoad<WT>::load8(W + off + 8, v + 8);
+  load8f(s + col, sv);
+  load8f(s + col + 8, sv + 8);
 #pragma unroll
   for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(v[e], sv[e]);
   float mn, mx;
   group_minmax16(v, mn, mx);
   const GroupFast g = group_fast(mn, mx, qmax, floor_);
-  const float z = -g.lo;
+  const float z = g.z;
   float k[16];
   quant_codes_minus_z<16>(v, g, k);
   uint32_t w0 = 0, w1 = 0;
