@@ -17,7 +17,6 @@ constexpr int kStatsRows = 128;  // tokens per statistics chunk
 constexpr int kTileM = 128;  // tokens per tile (tensor-memory lanes)
 constexpr int kTileN = 256;  // output rows per tile (tensor-memory columns)
 constexpr int kTileK = 64;   // input channels per pipeline stage (128 B of bf16)
-constexpr int kDefaultClusterM = 2;  // CTAs per cluster sharing an operand tile (RESIDUAL form)
 
 inline int stats_chunks(int64_t n_tok) { return (int)((n_tok + kStatsRows - 1) / kStatsRows); }
 
@@ -39,5 +38,7 @@ cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, 
 cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
                                const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
                                float* dump = nullptr, int withhold_first_fill = 0, int cluster_m = 0);
+// cluster_m: 0 = default kernel (CTA pairs, cta_group::2, for the RESIDUAL
+// form); 1, 2 or 4 = the single-CTA kernel with clusters of that size.
 
 }  // namespace awq

@@ -318,6 +318,215 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- CTA-pair form
+//
+// RESIDUAL form on CTA pairs (cta_group::2), the default search product.
+// A cluster of two CTAs on neighbouring SMs computes 256 x 256 output tiles
+// (two token tiles of 128 against one operand tile of 256 rows): each CTA
+// loads its 128 token rows of X and its half (128 rows) of the operand tile
+// into its own shared memory, and one thread of the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), which reads A and B
+// from both CTAs and accumulates each CTA's 128 rows in that CTA's tensor
+// memory. Per stage each SM therefore receives 32 KiB for a 128 x 256 x 64
+// product (48 KiB in the single-CTA form), so the ring holds kPairStages
+// stages in the same shared memory.
+//   full[s]   (even CTA) : both CTAs' copies of stage s landed (64 KiB);
+//                          the odd CTA's copies report to it across the pair
+//   empty[s]  (each CTA) : the pair's MMAs released stage s (commit multicast)
+//   tfull[b]  (each CTA) : accumulator b is complete (commit multicast)
+//   tempty[b] (even CTA) : all 8 epilogue warps of the pair read accumulator b
+// Waits are bounded as in the single-CTA form; the final cluster barrier
+// keeps each CTA alive until its peer no longer touches its shared memory or
+// barriers.
+
+constexpr int kPairStages = 6;
+constexpr int PA_BYTES = BM * BK * 2;          // 16 KiB: this CTA's token rows
+constexpr int PB_BYTES = (BN / 2) * BK * 2;    // 16 KiB: this CTA's half of the operand rows
+constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr int PAIR_SMEM_BYTES = kPairStages * PSTAGE_BYTES + 1024 + BAR_BYTES;
+constexpr uint32_t PAIR_IDESC = umma_idesc_bf16_f32(2 * BM, BN);
+static_assert(PAIR_SMEM_BYTES <= 232448, "shared memory per CTA");
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    search_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
+                            const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (base_u32 & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kPairStages * PA_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kPairStages * PB_BYTES);
+  uint64_t* full = bars;                     // [kPairStages]
+  uint64_t* empty = bars + kPairStages;      // [kPairStages]
+  uint64_t* tfull = bars + 2 * kPairStages;  // [2]
+  uint64_t* tempty = tfull + 2;              // [2]
+  uint64_t* drain = tempty + 2;              // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank() & 1u;
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  constexpr uint16_t kPairMask = 3;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the even CTA's barriers exist before its peer reports to them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer (both CTAs)
+      uint32_t stage = 0, phase = 0;
+      uint32_t used = 0, last_par = 0;
+      bool ok = true;
+      for (int it = pair; it < p.items && ok; it += npairs) {
+        const int a = it / (p.mtg * p.nt);
+        const int t = it - a * p.mtg * p.nt;
+        int mg, nb;
+        decode_tile(t, p.mtg, p.nt, GROUP_M / 2, mg, nb);
+        const int mb = mg * 2 + (int)rank;
+        for (int kb = 0; kb < p.kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fbar = mapa_shared(&full[stage], 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PSTAGE_BYTES);
+          tma_load_2d_pair(sA + stage * PA_BYTES, &tmX, fbar, kb * BK, mb * BM);
+          tma_load_3d_pair(sB + stage * PB_BYTES, &tmB, fbar, kb * BK, nb * BN + (int)rank * (BN / 2), a);
+          used |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every copy issued by the pair reports to the even CTA's barriers: it
+      // waits for all of them before the final cluster barrier.
+      if (leader)
+        for (int s = 0; s < kPairStages; ++s)
+          if (used & (1u << s)) mbar_wait(&full[s], (last_par >> s) & 1u, p.timeout_ns, nullptr, p.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ MMA issuer (even CTA)
+      uint32_t stage = 0, phase = 0;
+      uint32_t ph = 0;
+      uint32_t local = 0;
+      bool ok = true;
+      for (int it = pair; it < p.items && ok; it += npairs, ++local) {
+        const int buf = (int)(local & 1u);
+        if (!mbar_wait(&tempty[buf], ((ph >> buf) & 1u) ^ 1u, p.timeout_ns, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < p.kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = umma_desc_k_sw128(smem_u32(sA + stage * PA_BYTES));
+          const uint64_t bdesc = umma_desc_k_sw128(smem_u32(sB + stage * PB_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16_pair(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), PAIR_IDESC,
+                           (kb > 0 || k > 0) ? 1u : 0u);
+          umma_commit_pair_multicast(&empty[stage], kPairMask);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_multicast(&tfull[buf], kPairMask);
+        ph ^= 1u << buf;
+      }
+      umma_commit_pair(drain);
+      mbar_wait(drain, 0u, p.timeout_ns, nullptr, p.status);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t ph = 0;
+    uint32_t local = 0;
+    for (int it = pair; it < p.items; it += npairs, ++local) {
+      const int a = it / (p.mtg * p.nt);
+      const int t = it - a * p.mtg * p.nt;
+      int mg, nb;
+      decode_tile(t, p.mtg, p.nt, GROUP_M / 2, mg, nb);
+      const int mb = mg * 2 + (int)rank;
+      const int buf = (int)(local & 1u);
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], (ph >> buf) & 1u, p.timeout_ns, abort_flag, p.status)))
+        break;
+      tc_fence_after();
+      const uint32_t acc_addr = tmem_base + lane_base + (uint32_t)(buf * BN);
+      float ss = 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(acc_addr + (uint32_t)(c * 32), v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float d = __uint_as_float(v[i]);
+          ss = fmaf(d, d, ss);
+        }
+        if (p.dump != nullptr) {
+          const int row = mb * BM + q * 32 + lane;
+          const int col0 = nb * BN + c * 32;
+          if (row < p.n_tok)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col0 + i < p.N) p.dump[((size_t)a * p.n_tok + row) * p.N + col0 + i] = __uint_as_float(v[i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(&tempty[buf], 0));
+      ph ^= 1u << buf;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0 && mb < p.mt) p.partials[((((size_t)a * p.mt + mb) * p.nt + nb) << 2) + q] = ss;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer no longer copies into, reports to or arrives on this CTA
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -380,6 +589,32 @@ cudaError_t launch_residual(const CUtensorMap& tmX, const CUtensorMap& tmB, Para
   return cudaLaunchKernelEx(&lc, search_gemm_kernel<false, CM>, tmX, tmB, p);
 }
 
+cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmB, Params p, int sms, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(search_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PAIR_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.blockDim = dim3(NUM_THREADS);
+  lc.dynamicSmemBytes = PAIR_SMEM_BYTES;
+  lc.stream = st;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int pairs = sms / 2;
+  lc.gridDim = dim3(2 * pairs);
+  int active = 0;
+  e = cudaOccupancyMaxActiveClusters(&active, search_gemm_pair_kernel, &lc);
+  if (e != cudaSuccess) return e;
+  if (active > 0 && active < pairs) pairs = active;
+  if (pairs > p.items) pairs = p.items;
+  lc.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&lc, search_gemm_pair_kernel, tmX, tmB, p);
+}
+
 }  // namespace
 
 cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
@@ -388,7 +623,10 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
   const int G = cfg.n_grid;
   const int slots = ref ? G + 1 : G;
-  int CM = cluster_m > 0 ? cluster_m : kDefaultClusterM;
+  // cluster_m 0: the default (CTA pairs for RESIDUAL, single CTAs for
+  // REFERENCE); 1, 2 or 4: the single-CTA kernel with that cluster size.
+  const bool pair = !ref && !withhold_first_fill && cluster_m == 0;
+  int CM = pair ? 2 : (cluster_m > 0 ? cluster_m : 1);
   if (ref || withhold_first_fill) CM = 1;
   if (CM != 1 && CM != 2 && CM != 4) return cudaErrorInvalidValue;
   CUtensorMap tmX, tmB;
@@ -428,7 +666,8 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
     search_gemm_kernel<true, 1><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);
     return cudaGetLastError();
   }
-  if (CM == 1) e = launch_residual<1>(tmX, tmB, p, sms, st);
+  if (pair) e = launch_pair(tmX, tmB, p, sms, st);
+  else if (CM == 1) e = launch_residual<1>(tmX, tmB, p, sms, st);
   else if (CM == 2) e = launch_residual<2>(tmX, tmB, p, sms, st);
   else e = launch_residual<4>(tmX, tmB, p, sms, st);
   if (e != cudaSuccess) return e;
