@@ -129,7 +129,8 @@ AWQ_API awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_
 
 /* mean_abs[j] = (1/n_tok) sum_t |X[t, j]|  (fp32 out; fp32 partial sums over
    blocks of 128 tokens, a compensated fp32 sum across blocks, fixed order:
-   deterministic).
+   deterministic). One kernel, preceded by a small memset of the scratch's
+   ticket counters on `stream`.
    X: device bf16 [n_tok][in] (x_dtype must be AWQ_BF16). in % 8 == 0.
    mean_abs: device fp32 [in]. ws: device scratch of at least the queried
    size. Source: "AWQ: How Activation-Aware Quantization Saves 4-bit LLMs",
@@ -139,7 +140,7 @@ AWQ_API awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, 
                          float* mean_abs, void* ws, size_t ws_bytes, awq_stream_t stream);
 
 /* Largest ceil(n_tok / 128) * in that awq_act_stats_noalloc accepts (its
-   fixed scratch: 4 MiB of fp32 partial sums). */
+   fixed scratch: 4 MiB of fp32 partial sums, plus 16 KiB of counters). */
 #define AWQ_NOALLOC_STATS_MAX_FLOATS (1u << 20)
 
 /* awq_act_stats for callers that cannot allocate device memory or pass a
@@ -148,8 +149,9 @@ AWQ_API awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, 
    cudaMalloc, which may synchronise the device, is not allowed). The pages
    have no counterpart: this is an interface variant of step 1, not part of
    the method. Same arguments and result as awq_act_stats without ws/ws_bytes.
-   The partial sums live in a library-owned 4 MiB device array that every GPU
-   loading the library keeps until exit. Its address is looked up on the first
+   The partial sums live in a library-owned device array (4 MiB + 16 KiB)
+   that every GPU loading the library keeps until exit; each call clears the
+   array's counters with a memset on `stream` before its kernel. Its address is looked up on the first
    call made on each device (with that device current); make that first call
    before any stream capture. All calls share the array, so calls that
    overlap on the GPU race: serialise them. Calls allocate nothing.

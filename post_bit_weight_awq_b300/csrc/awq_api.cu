@@ -107,9 +107,14 @@ const char* awq_status_string(int status) {
   }
 }
 
+// Statistics scratch: fp32 partial sums [chunks][in], then the per-strip tickets.
+size_t stats_ticket_offset(int64_t n_tok, int64_t in) {
+  return align_up((size_t)stats_chunks(n_tok) * (size_t)in * 4, kAlign);
+}
+
 awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_t* bytes) {
   if (bytes == nullptr || n_tok < 1 || in < 1 || n_tok > kMaxDim || in > kMaxDim) return AWQ_ERR_INVALID_ARG;
-  *bytes = align_up((size_t)stats_chunks(n_tok) * (size_t)in * 4, kAlign);
+  *bytes = stats_ticket_offset(n_tok, in) + align_up((size_t)stats_strips(in) * 4, kAlign);
   return AWQ_OK;
 }
 
@@ -123,7 +128,8 @@ awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, int64_t 
   size_t need = 0;
   awq_act_stats_workspace_size(n_tok, in, &need);
   if (ws_bytes < need) return AWQ_ERR_WORKSPACE;
-  return from_cuda(launch_stats((const uint16_t*)X, n_tok, in, (float*)ws, mean_abs, (cudaStream_t)stream));
+  uint32_t* tickets = (uint32_t*)((uint8_t*)ws + stats_ticket_offset(n_tok, in));
+  return from_cuda(launch_stats((const uint16_t*)X, n_tok, in, (float*)ws, tickets, mean_abs, (cudaStream_t)stream));
 }
 
 awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, const awq_config* cfg, size_t* bytes) {

@@ -18,11 +18,14 @@ namespace awq {
 // LLMs", "How does AWQ decide which weights to protect?"; "AWQ > Summary",
 // "Salient weight identification").
 //
-// Block = 32 x 8 threads over a strip of 256 channels and a chunk of
-// kStatsRows tokens. Each thread reads 8 channels (16 B) of every 8th row of
-// the chunk, so a warp reads 512 contiguous bytes per row. The 8 row phases
-// are added in fixed order in shared memory; the finalize kernel adds the
-// chunks with a compensated fp32 sum in fixed order. Deterministic.
+// One launch. Block = 32 x 8 threads over a strip of 256 channels and a
+// chunk of kStatsRows tokens. Each thread reads 8 channels (16 B) of every
+// 8th row of the chunk, so a warp reads 512 contiguous bytes per row. The 8
+// row phases are added in fixed order in shared memory and the chunk's
+// partial sums go to scratch. The block that finishes last on a strip (a
+// ticket counter per strip, zeroed before the launch) adds that strip's
+// chunks with a compensated fp32 sum in chunk order and writes the mean:
+// the result does not depend on which block finishes last. Deterministic.
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;
@@ -43,9 +46,11 @@ __device__ __forceinline__ void acc_abs_bf16x8(float (&a)[8], const uint4& v) {
   a[7] += fabsf(bf16_hi(v.w));
 }
 
-__global__ void __launch_bounds__(256) stats_partial_kernel(const uint16_t* __restrict__ X, int n, int K,
-                                                            float* __restrict__ partials) {
+__global__ void __launch_bounds__(256) stats_kernel(const uint16_t* __restrict__ X, int n, int K,
+                                                    float* __restrict__ partials, uint32_t* __restrict__ tickets,
+                                                    float* __restrict__ mean_abs) {
   __shared__ float red[8][256 + 8];
+  __shared__ bool last;
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int col = (blockIdx.x * 32 + tx) * 8;
   const int r0 = blockIdx.y * kStatsRows;
@@ -71,30 +76,33 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const uint16_t* __re
   for (int y = 0; y < 8; ++y) sum += red[y][t];
   const int c = blockIdx.x * 256 + t;
   if (c < K) partials[(size_t)blockIdx.y * K + c] = sum;
-}
-
-__global__ void __launch_bounds__(256) stats_finalize_kernel(const float* __restrict__ partials, int chunks,
-                                                             int n, int K, float* __restrict__ mean_abs) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= K) return;
-  // compensated (Neumaier) fp32 sum over the chunks, fixed order
-  float sum = 0.0f, comp = 0.0f;
-  for (int i = 0; i < chunks; ++i) {
-    const float x = partials[(size_t)i * K + c];
-    const float t = __fadd_rn(sum, x);
-    comp = __fadd_rn(comp, fabsf(sum) >= fabsf(x) ? __fadd_rn(__fsub_rn(sum, t), x) : __fadd_rn(__fsub_rn(x, t), sum));
-    sum = t;
+  // publish this chunk, then find out whether it was the strip's last one
+  __threadfence();
+  __syncthreads();
+  if (t == 0) last = atomicAdd(&tickets[blockIdx.x], 1u) == gridDim.y - 1;
+  __syncthreads();
+  if (!last || c >= K) return;
+  __threadfence();
+  // compensated (Neumaier) fp32 sum over the chunks, fixed order; the other
+  // blocks' partials are read past L1
+  float s = 0.0f, comp = 0.0f;
+  for (int i = 0; i < (int)gridDim.y; ++i) {
+    const float x = __ldcg(partials + (size_t)i * K + c);
+    const float u = __fadd_rn(s, x);
+    comp = __fadd_rn(comp, fabsf(s) >= fabsf(x) ? __fadd_rn(__fsub_rn(s, u), x) : __fadd_rn(__fsub_rn(x, u), s));
+    s = u;
   }
-  mean_abs[c] = (float)(((double)sum + (double)comp) / (double)n);
+  mean_abs[c] = (float)(((double)s + (double)comp) / (double)n);
 }
 
-cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partials, float* mean_abs,
-                         cudaStream_t st) {
+cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partials, uint32_t* tickets,
+                         float* mean_abs, cudaStream_t st) {
   const int chunks = stats_chunks(n);
-  dim3 grid((unsigned)((K + 255) / 256), (unsigned)chunks);
-  stats_partial_kernel<<<grid, dim3(32, 8), 0, st>>>(X, (int)n, (int)K, partials);
-  stats_finalize_kernel<<<(unsigned)((K + 255) / 256), 256, 0, st>>>(partials, chunks, (int)n, (int)K,
-                                                                      mean_abs);
+  const unsigned strips = (unsigned)((K + 255) / 256);
+  cudaError_t e = cudaMemsetAsync(tickets, 0, strips * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  stats_kernel<<<dim3(strips, (unsigned)chunks), dim3(32, 8), 0, st>>>(X, (int)n, (int)K, partials, tickets,
+                                                                       mean_abs);
   return cudaGetLastError();
 }
 
@@ -109,21 +117,28 @@ cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partial
 // a direct pow by at most ~n_grid fp64 ulps, which changes the fp32-rounded
 // scale only when it lies that close to an fp32 rounding boundary). x^alpha
 // is non-decreasing in x, so max(s_i) and min(s_i) are the powers of the
-// largest and smallest clamped statistic; each block finds those two with a
-// fixed-order reduction and forms 1 / sqrt(max * min) per alpha.
-// One thread per channel; alpha = 0 gives s = 1 exactly.
+// largest and smallest clamped statistic; every block finds those two (16-byte
+// loads of the whole vector, a fixed-order reduction) and its first n_grid
+// threads form 1 / sqrt(max * min) per alpha while the others start on their
+// channel's powers. One thread per channel, 64 channels per block so that
+// the fp64 work spreads over many SMs; alpha = 0 gives s = 1 exactly.
 
-__global__ void __launch_bounds__(128) alpha_scales_kernel(const float* __restrict__ mean_abs, int K, int G,
-                                                           double clamp_min, int normalize,
-                                                           float* __restrict__ s_out,
-                                                           float* __restrict__ inv_out) {
-  __shared__ float smax[4], smin[4];
+constexpr int kAlphaThreads = 64;
+
+__global__ void __launch_bounds__(kAlphaThreads) alpha_scales_kernel(const float* __restrict__ mean_abs, int K, int G,
+                                                                     double clamp_min, int normalize,
+                                                                     float* __restrict__ s_out,
+                                                                     float* __restrict__ inv_out) {
+  __shared__ float smax[kAlphaThreads / 32], smin[kAlphaThreads / 32];
   __shared__ double inv_norm[kMaxGrid];
   float mx = -INFINITY, mn = INFINITY;
-  for (int j = threadIdx.x; j < K; j += blockDim.x) {
-    const float v = mean_abs[j];
-    mx = fmaxf(mx, v);
-    mn = fminf(mn, v);
+  const float4* m4 = reinterpret_cast<const float4*>(mean_abs);
+  const int K4 = K >> 2;  // K is a multiple of 128
+#pragma unroll 4
+  for (int j = threadIdx.x; j < K4; j += kAlphaThreads) {
+    const float4 v = m4[j];
+    mx = fmax3f(mx, fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    mn = fmin3f(mn, fminf(v.x, v.y), fminf(v.z, v.w));
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -141,7 +156,7 @@ __global__ void __launch_bounds__(128) alpha_scales_kernel(const float* __restri
     double c = 1.0;
     if (normalize) {
       float bmx = smax[0], bmn = smin[0];
-      for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+      for (int w = 1; w < kAlphaThreads / 32; ++w) {
         bmx = fmaxf(bmx, smax[w]);
         bmn = fminf(bmn, smin[w]);
       }
@@ -150,11 +165,11 @@ __global__ void __launch_bounds__(128) alpha_scales_kernel(const float* __restri
     }
     inv_norm[i] = 1.0 / c;
   }
+  const int j = blockIdx.x * kAlphaThreads + threadIdx.x;
+  double root = 1.0;
+  if (j < K) root = pow(fmax((double)mean_abs[j], clamp_min), 1.0 / (double)G);
   __syncthreads();
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= K) return;
-  const double b = fmax((double)mean_abs[j], clamp_min);
-  const double root = pow(b, 1.0 / (double)G);
   double p = 1.0;  // b^(i/G)
   for (int i = 0; i < G; ++i) {
     const float s32 = (float)(p * inv_norm[i]);
@@ -166,8 +181,8 @@ __global__ void __launch_bounds__(128) alpha_scales_kernel(const float* __restri
 
 cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_config& cfg, float* s,
                                 float* inv_s, cudaStream_t st) {
-  alpha_scales_kernel<<<(unsigned)((K + 127) / 128), 128, 0, st>>>(mean_abs, (int)K, cfg.n_grid,
-                                                                   (double)cfg.sx_clamp_min, cfg.normalize, s, inv_s);
+  alpha_scales_kernel<<<(unsigned)((K + kAlphaThreads - 1) / kAlphaThreads), kAlphaThreads, 0, st>>>(
+      mean_abs, (int)K, cfg.n_grid, (double)cfg.sx_clamp_min, cfg.normalize, s, inv_s);
   return cudaGetLastError();
 }
 
@@ -467,64 +482,105 @@ cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, c
 // Final codes of W * diag(s) with the same quantiser, 8 codes per int32
 // ("What is AWQ Quantization? ...", "INT4 Weight Packing & Export"), one fp16
 // scale ("AWQ (Activation-Aware Weight Quantization) - AI Glossary", memory
-// example) and one fp16 zero per group. A group is held by 8 lanes with 16
-// weights (two words) each; even lanes collect their neighbour's two words
-// and write four words with one 128-bit store.
+// example) and one fp16 zero per group. Same layout as the fake-quant
+// kernel: a block owns a 512-channel strip and a row range, a warp one row at
+// a time, 8 lanes per group with channels [8l, 8l+8) and [64+8l, 64+8l+8),
+// so lane l's two code words are words l and 8+l of its group and every
+// 4-byte store instruction of a warp fills four whole 32-byte sectors. The
+// lane's 16 scales are loaded once per block; the next row's weights load
+// while the current row is quantised.
+
+constexpr int kPackWarps = 8;
+// resident blocks per SM: the fp32-weight variant needs more registers
+template <typename WT>
+constexpr int pack_blocks_per_sm() { return sizeof(WT) == 2 ? 3 : 2; }
 
 template <typename WT>
-__global__ void __launch_bounds__(256) pack_kernel(const WT* __restrict__ W, int64_t ngroups, int K,
-                                                   const float* __restrict__ s, float qmax, float floor_,
-                                                   int32_t* __restrict__ qweight, uint16_t* __restrict__ scales,
-                                                   uint16_t* __restrict__ zeros) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t gid = t >> 3;
-  const int sub = (int)(t & 7);
-  const bool valid = gid < ngroups;
-  const int64_t off = (valid ? gid : 0) * 128 + sub * 16;
-  const int col = (int)(off % K);
-  float v[16], sv[16];
-  WLoad<WT>::load8(W + off, v);
-  WLoad<WT>::load8(W + off + 8, v + 8);
-  load8f(s + col, sv);
-  load8f(s + col + 8, sv + 8);
+__global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT>())
+    pack_kernel(const WT* __restrict__ W, int N, int K, const float* __restrict__ s, float qmax, float floor_,
+                int32_t* __restrict__ qweight, uint16_t* __restrict__ scales, uint16_t* __restrict__ zeros,
+                int nstrips, int rows_per_block) {
+  const int strip = blockIdx.x % nstrips;
+  const int col0 = strip * kFqCols;
+  const int ncols = min(kFqCols, K - col0);
+  const int r_begin = (blockIdx.x / nstrips) * rows_per_block;
+  const int r_end = min(N, r_begin + rows_per_block);
+  if (r_begin >= r_end) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane >> 3, sub = lane & 7;
+  const bool active = grp * 128 < ncols;  // groups past a partial strip repeat group 0 and store nothing
+  const int c_lo = (active ? grp * 128 : 0) + sub * 8;
+  float2 sv[8];
+  {
+    float t[16];
+    load8f(s + col0 + c_lo, t);
+    load8f(s + col0 + c_lo + 64, t + 8);
 #pragma unroll
-  for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(v[e], sv[e]);
-  float mn, mx;
-  group_minmax16(v, mn, mx);
-  const GroupFast g = group_fast(mn, mx, qmax, floor_);
-  const float z = g.z;
-  float k[16];
-  quant_codes_minus_z<16>(v, g, k);
-  uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    w0 |= (uint32_t)__fadd_rn(k[e], z) << (4 * e);
-    w1 |= (uint32_t)__fadd_rn(k[8 + e], z) << (4 * e);
+    for (int i = 0; i < 8; ++i) sv[i] = make_float2(t[2 * i], t[2 * i + 1]);
   }
-  const uint32_t w2 = __shfl_down_sync(0xffffffffu, w0, 1);
-  const uint32_t w3 = __shfl_down_sync(0xffffffffu, w1, 1);
-  if (valid) {
-    if ((sub & 1) == 0)
-      *reinterpret_cast<uint4*>(qweight + gid * 16 + sub * 2) = make_uint4(w0, w1, w2, w3);
-    if (sub == 0) {
-      scales[gid] = __half_as_ushort(__float2half_rn(g.delta));
-      zeros[gid] = __half_as_ushort(__float2half_rn(z));
+  const int kw = K >> 3, kg = K >> 7;
+  int row = r_begin + warp;
+  RowRegs<WT> nxt;
+  if (row < r_end) nxt.load(W + (size_t)row * K + col0 + c_lo);
+  for (; row < r_end; row += kPackWarps) {
+    float2 w[8];
+    nxt.unpack(w);
+    if (row + kPackWarps < r_end) nxt.load(W + (size_t)(row + kPackWarps) * K + col0 + c_lo);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 p = __fmul2_rn(w[i], sv[i]);
+      v[2 * i] = p.x;
+      v[2 * i + 1] = p.y;
+    }
+    float mn, mx;
+    group_minmax16(v, mn, mx);
+    const GroupFast g = group_fast(mn, mx, qmax, floor_);
+    float k[16];
+    quant_codes_minus_z<16>(v, g, k);
+    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      w0 |= (uint32_t)__fadd_rn(k[e], g.z) << (4 * e);
+      w1 |= (uint32_t)__fadd_rn(k[8 + e], g.z) << (4 * e);
+    }
+    if (active) {
+      int32_t* q = qweight + (size_t)row * kw + ((col0 + c_lo) >> 3);
+      q[0] = (int32_t)w0;
+      q[8] = (int32_t)w1;  // 64 channels further on
+      if (sub == 0) {
+        const size_t gi = (size_t)row * kg + ((col0 + grp * 128) >> 7);
+        scales[gi] = __half_as_ushort(__float2half_rn(g.delta));
+        zeros[gi] = __half_as_ushort(__float2half_rn(g.z));
+      }
     }
   }
 }
 
+template <typename WT>
+cudaError_t launch_pack_t(const WT* W, int64_t N, int64_t K, const float* s, const awq_config& cfg,
+                          int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int nstrips = (int)((K + kFqCols - 1) / kFqCols);
+  int64_t rblocks = (int64_t)sms * pack_blocks_per_sm<WT>() / nstrips;
+  if (rblocks < 1) rblocks = 1;
+  if (rblocks > N) rblocks = N;
+  const int rows_per_block = (int)((N + rblocks - 1) / rblocks);
+  rblocks = (N + rows_per_block - 1) / rows_per_block;
+  const float qmax = (float)((1 << cfg.w_bit) - 1);
+  pack_kernel<WT><<<(unsigned)(rblocks * nstrips), kPackWarps * 32, 0, st>>>(
+      W, (int)N, (int)K, s, qmax, cfg.delta_floor, qweight, scales, zeros, nstrips, rows_per_block);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pack(const void* W, int w_dtype, int64_t N, int64_t K, const float* s, const awq_config& cfg,
                         int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
-  const int64_t ngroups = N * K / 128;
-  const unsigned blocks = (unsigned)((ngroups * 8 + 255) / 256);
-  const float qmax = (float)((1 << cfg.w_bit) - 1);
   if (w_dtype == AWQ_BF16)
-    pack_kernel<uint16_t><<<blocks, 256, 0, st>>>((const uint16_t*)W, ngroups, (int)K, s, qmax, cfg.delta_floor,
-                                                  qweight, scales, zeros);
-  else
-    pack_kernel<float><<<blocks, 256, 0, st>>>((const float*)W, ngroups, (int)K, s, qmax, cfg.delta_floor,
-                                               qweight, scales, zeros);
-  return cudaGetLastError();
+    return launch_pack_t<uint16_t>((const uint16_t*)W, N, K, s, cfg, qweight, scales, zeros, st);
+  return launch_pack_t<float>((const float*)W, N, K, s, cfg, qweight, scales, zeros, st);
 }
 
 // ============================================================== loss + argmin

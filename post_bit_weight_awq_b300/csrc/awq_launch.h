@@ -19,9 +19,11 @@ constexpr int kTileN = 256;  // output rows per tile (tensor-memory columns)
 constexpr int kTileK = 64;   // input channels per pipeline stage (128 B of bf16)
 
 inline int stats_chunks(int64_t n_tok) { return (int)((n_tok + kStatsRows - 1) / kStatsRows); }
+inline int stats_strips(int64_t in) { return (int)((in + 255) / 256); }
 
-cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partials, float* mean_abs,
-                         cudaStream_t st);
+// partials: fp32 [stats_chunks(n)][K]; tickets: uint32 [stats_strips(K)] (zeroed by the launch).
+cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partials, uint32_t* tickets,
+                         float* mean_abs, cudaStream_t st);
 cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_config& cfg, float* s,
                                 float* inv_s, cudaStream_t st);
 cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,

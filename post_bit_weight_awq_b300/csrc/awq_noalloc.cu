@@ -9,14 +9,16 @@
 // this library's own device memory instead of a caller workspace.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
-// library holds it (4 MiB) until the process exits. In host code its name is
-// only a host-side stand-in, so its device address is looked up once per
-// device with cudaGetSymbolAddress, with that device current, on the first
-// call made on that device; that first call should come before any stream
-// capture. All calls share the array and it keeps the last call's contents;
-// the kernels write every partial they later read, so nothing needs clearing
-// between calls. Calls whose work overlaps on the GPU (two streams, or two
-// host threads) race on the array: serialise them.
+// library holds it (4 MiB + 16 KiB) until the process exits. In host code
+// its name is only a host-side stand-in, so its device address is looked up
+// once per device with cudaGetSymbolAddress, with that device current, on
+// the first call made on that device; that first call should come before
+// any stream capture. All calls share the array and it keeps the last
+// call's contents; the kernel writes every partial it later reads, and each
+// call clears the strips' ticket counters (the part that must start at
+// zero) with a memset on its stream before the kernel runs. Calls whose work
+// overlaps on the GPU (two streams, or two host threads) race on the array:
+// serialise them.
 #include <mutex>
 
 #include "awq.h"
@@ -25,7 +27,10 @@
 namespace {
 
 constexpr size_t kScratchFloats = AWQ_NOALLOC_STATS_MAX_FLOATS;
-static __device__ __align__(256) float g_stats_scratch[kScratchFloats];
+// ceil(n_tok/128) * in <= kScratchFloats implies in <= kScratchFloats, so at
+// most kScratchFloats / 256 strips of 256 channels need a ticket counter.
+constexpr size_t kTicketWords = kScratchFloats / 256;
+static __device__ __align__(256) float g_stats_scratch[kScratchFloats + kTicketWords];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -60,7 +65,8 @@ extern "C" awq_status awq_act_stats_noalloc(const void* X, int32_t x_dtype, int6
   float* scratch = nullptr;
   const awq_status st = scratch_on_current_device(&scratch);
   if (st != AWQ_OK) return st;
-  const cudaError_t e =
-      awq::launch_stats(static_cast<const uint16_t*>(X), n_tok, in, scratch, mean_abs, (cudaStream_t)stream);
+  uint32_t* tickets = reinterpret_cast<uint32_t*>(scratch + kScratchFloats);
+  const cudaError_t e = awq::launch_stats(static_cast<const uint16_t*>(X), n_tok, in, scratch, tickets, mean_abs,
+                                          (cudaStream_t)stream);
   return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA;
 }

@@ -46,11 +46,11 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
+constexpr int kRasterTokenTiles = 16;  // token tiles per raster band
 constexpr int NUM_THREADS = 192;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
 constexpr uint32_t IDESC = umma_idesc_bf16_f32(BM, BN);
-constexpr int GROUP_M = 16;  // output-tile raster: 16 token tiles per column sweep
 
 struct Params {
   int mt, nt;         // token tiles, output-row tiles
@@ -58,6 +58,8 @@ struct Params {
   int G;              // alphas
   int mtg;            // token-tile groups of the cluster size: ceil(mt / CM)
   int items;          // work items (RESIDUAL: G*mtg*nt; REFERENCE: mt*nt)
+  int raster_group;   // tiles of the stationary operand per raster sweep
+  int raster_n;       // 1: operand tiles stay, token tiles sweep; 0: the reverse
   uint64_t timeout_ns;
   float* partials;    // [G][mt][nt][4]
   uint32_t* status;
@@ -66,16 +68,23 @@ struct Params {
   int withhold_first_fill;  // test aid: leave out each CTA's first operand fill
 };
 
-// Tile t of an m_tiles x nt grid, rastered in groups of `group` token tiles
-// so that concurrently running CTAs share operand panels in L2.
-__device__ __forceinline__ void decode_tile(int t, int m_tiles, int nt, int group, int& mb, int& nb) {
-  const int span = group * nt;
-  const int grp = t / span;
-  const int first_m = grp * group;
-  const int gm = min(group, m_tiles - first_m);
-  const int r = t - grp * span;
-  mb = first_m + r % gm;
-  nb = r / gm;
+// Tile t of an m_tiles x nt grid in raster order. Tiles are taken in bands
+// of `group` tiles of the stationary operand (operand-row tiles if raster_n,
+// else token tiles): within a band the other operand sweeps its whole range,
+// so the band's panels of the stationary operand stay in L2 while each panel
+// of the swept operand is read once per band.
+__device__ __forceinline__ void decode_tile(int t, int m_tiles, int nt, int group, int raster_n, int& mb, int& nb) {
+  const int n_stat = raster_n ? nt : m_tiles;   // stationary dimension
+  const int n_sweep = raster_n ? m_tiles : nt;  // swept dimension
+  const int span = group * n_sweep;
+  const int band = t / span;
+  const int first = band * group;
+  const int gsz = min(group, n_stat - first);
+  const int r = t - band * span;
+  const int i_stat = first + r % gsz;
+  const int i_sweep = r / gsz;
+  mb = raster_n ? i_sweep : i_stat;
+  nb = raster_n ? i_stat : i_sweep;
 }
 
 template <bool REF, int CM>
@@ -147,7 +156,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           t = it - a * p.mtg * p.nt;
         }
         int mg, nb;
-        decode_tile(t, p.mtg, p.nt, GROUP_M / CM, mg, nb);
+        decode_tile(t, p.mtg, p.nt, p.raster_group, p.raster_n, mg, nb);
         const int mb = mg * CM + rank;
         for (int pass = 0; pass < passes && ok; ++pass) {
           const int slot = REF ? (pass == 0 ? p.G : pass - 1) : a;
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         t = it - a * p.mtg * p.nt;
       }
       int mg, nb;
-      decode_tile(t, p.mtg, p.nt, GROUP_M / CM, mg, nb);
+      decode_tile(t, p.mtg, p.nt, p.raster_group, p.raster_n, mg, nb);
       const int mb = mg * CM + rank;
       if (REF) {
         // All lanes wait; the warp goes on only if every lane saw the phase
@@ -409,7 +418,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int a = it / (p.mtg * p.nt);
         const int t = it - a * p.mtg * p.nt;
         int mg, nb;
-        decode_tile(t, p.mtg, p.nt, GROUP_M / 2, mg, nb);
+        decode_tile(t, p.mtg, p.nt, p.raster_group, p.raster_n, mg, nb);
         const int mb = mg * 2 + (int)rank;
         for (int kb = 0; kb < p.kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status)) {
@@ -481,7 +490,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int a = it / (p.mtg * p.nt);
       const int t = it - a * p.mtg * p.nt;
       int mg, nb;
-      decode_tile(t, p.mtg, p.nt, GROUP_M / 2, mg, nb);
+      decode_tile(t, p.mtg, p.nt, p.raster_group, p.raster_n, mg, nb);
       const int mb = mg * 2 + (int)rank;
       const int buf = (int)(local & 1u);
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], (ph >> buf) & 1u, p.timeout_ns, abort_flag, p.status)))
@@ -649,6 +658,12 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
   p.kb = (int)(K / BK);
   p.G = G;
   p.items = ref ? p.mt * p.nt : G * p.mtg * p.nt;
+  // L2 raster: bands of kRasterTokenTiles token tiles stay in L2 while the
+  // operand tiles sweep past them (measured best among band sizes and
+  // orientations on the layer shapes of the benchmark suite).
+  p.raster_n = 0;
+  p.raster_group = (kRasterTokenTiles + CM - 1) / CM;
+  if (p.raster_group > p.mtg) p.raster_group = p.mtg;
   const uint32_t ms = cfg.wait_timeout_ms ? cfg.wait_timeout_ms : 2000u;
   p.timeout_ns = (uint64_t)ms * 1000000ull;
   p.partials = partials;
