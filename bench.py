@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "ms per layer AWQ search+pack (20-pt α grid); % BF16 TC peak and % HBM BW"
 DEFAULT_WORKLOAD = "llama7b_q_proj"
-KERNELS_PER_STEP = 7  # stats, alpha scales, fake-quant, search product, loss reduce + select, pack
+KERNELS_PER_STEP = 6  # stats, alpha scales, fused fake-quant + search product, loss reduce + select, pack
 RUN_AHEAD_CYCLES = 4_000_000  # GPU spin before each timed step so the host enqueues the whole step first
 FLUSH_BYTES = 512 << 20
 
@@ -51,13 +51,15 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-GEMM_SOURCES = ["post_bit_weight_awq_b300/csrc/awq_search_gemm.cu", "post_bit_weight_awq_b300/csrc/awq_device.cuh"]
+GEMM_SOURCES = ["post_bit_weight_awq_b300/csrc/awq_search_gemm.cu", "post_bit_weight_awq_b300/csrc/awq_device.cuh",
+                "post_bit_weight_awq_b300/csrc/awq_quant.cuh"]
 
 
 def profiled_traffic(workload):
-    """DRAM bytes per launch of the search kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "search_gemm_kernel.md")
+    """DRAM bytes per launch of the fused search kernel from the committed ncu
+    summary of this workload, if it was taken on the current kernel source;
+    else None."""
+    path = os.path.join(ROOT, "profiles", f"search_fused_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -223,6 +225,7 @@ def gpu_arm(args, rank, world, local_rank):
     op = torch.empty(G, N, K, dtype=torch.bfloat16, device=dev)
     mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
     parts = torch.empty(G, mt, nt, 4, dtype=f32, device=dev)
+    ready = torch.zeros(G * (nt + 1) + 1, dtype=i32, device=dev)
     status = torch.zeros(4, dtype=i32, device=dev)
     losses = torch.empty(G, dtype=f32, device=dev)
     best = torch.empty(1, dtype=i32, device=dev)
@@ -245,19 +248,25 @@ def gpu_arm(args, rank, world, local_rank):
         capi.awq_alpha_scales(mean_abs, cfg, s, inv, st)
         if ev:
             ev[2].record(st)
-        capi.awq_fakequant(Wd, s, inv, cfg, op, st)
+        capi.awq_search_fused(Wd, Xd, s, inv, cfg, op, parts, ready, status, st)
         if ev:
             ev[3].record(st)
-        capi.awq_search_gemm(Xd, op, cfg, parts, status, st, n_tok=n, in_features=K, out_features=N)
-        if ev:
-            ev[4].record(st)
         capi.awq_loss_select(parts, s, cfg, losses, best, s_best, status, st, n_tok=n, out_features=N,
                              in_features=K)
         if ev:
-            ev[5].record(st)
+            ev[4].record(st)
         capi.awq_quantize_pack(Wd, s_best, cfg, qw, sc, zr, st)
         if ev:
-            ev[6].record(st)
+            ev[5].record(st)
+
+    def unfused(ev):
+        # the fake-quant and the search product as separate launches (what the fused kernel overlaps)
+        st = torch.cuda.current_stream(dev)
+        ev[0].record(st)
+        capi.awq_fakequant(Wd, s, inv, cfg, op, st)
+        ev[1].record(st)
+        capi.awq_search_gemm(Xd, op, cfg, parts, status, st, n_tok=n, in_features=K, out_features=N)
+        ev[2].record(st)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -281,7 +290,8 @@ def gpu_arm(args, rank, world, local_rank):
     if not torch.equal(losses, losses_eager):
         raise RuntimeError("graph replay does not reproduce the eager step")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    uevents = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     if dist:
@@ -309,12 +319,21 @@ def gpu_arm(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if int(status[0]) != 0:
         raise RuntimeError("device status " + capi.status_string(int(status[0])))
+    for k in range(args.steps):
+        flush.zero_()
+        torch.cuda._sleep(RUN_AHEAD_CYCLES)
+        unfused(uevents[k])
+    torch.cuda.synchronize()
+    if int(status[0]) != 0:
+        raise RuntimeError("device status " + capi.status_string(int(status[0])))
 
-    stage_names = ["stats", "alpha_scales", "fakequant", "search_gemm", "loss_select", "pack"]
+    stage_names = ["stats", "alpha_scales", "search", "loss_select", "pack"]
     per_stage = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in events) for i, nm in enumerate(stage_names)}
+    alone = {"fakequant": statistics.mean(e[0].elapsed_time(e[1]) for e in uevents),
+             "search_gemm": statistics.mean(e[1].elapsed_time(e[2]) for e in uevents)}
     step_ms = [a.elapsed_time(b) for a, b in gev]
     ms_step = statistics.mean(step_ms)
-    ms_step_eager = statistics.mean(e[0].elapsed_time(e[6]) for e in events)
+    ms_step_eager = statistics.mean(e[0].elapsed_time(e[5]) for e in events)
     t_total = sum(step_ms)
     if dist:
         t_total = multi.max_over_ranks(t_total, device=dev)
@@ -384,8 +403,8 @@ def gpu_arm(args, rank, world, local_rank):
 
     pk = peaks()
     flops = G * 2.0 * n * K * N
-    gemm_ms = per_stage["search_gemm"]
-    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    search_ms = per_stage["search"]
+    achieved = flops / (search_ms * 1e-3) / 1e12
     traffic = profiled_traffic(args.workload)
     wbytes = 2 if L["w_dtype"] == "bf16" else 4
     hbm_bytes = {
@@ -393,17 +412,30 @@ def gpu_arm(args, rank, world, local_rank):
         "fakequant": wbytes * N * K + G * 2.0 * N * K,
         "pack": wbytes * N * K + N * K / 2 + 4.0 * N * K / 128,
     }
+
+    def tensor_fracs(tf):
+        d = {"tflops": round(tf, 1), "frac_bf16_burst": round(tf / pk["bf16_tflops"], 3)}
+        if pk.get("bf16_tflops_sustained"):
+            d["frac_bf16_sustained"] = round(tf / pk["bf16_tflops_sustained"], 3)
+        return d
+
+    def hbm_fracs(nm, ms):
+        gbs = hbm_bytes[nm] / (ms * 1e-3) / 1e9
+        return {"gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)}
+
     stages = {}
     for nm, ms in per_stage.items():
         d = {"ms": round(ms, 4)}
         if nm in hbm_bytes:
-            gbs = hbm_bytes[nm] / (ms * 1e-3) / 1e9
-            d.update({"gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)})
-        if nm == "search_gemm":
-            d.update({"tflops": round(achieved, 1), "frac_bf16_burst": round(achieved / pk["bf16_tflops"], 3)})
-            if pk.get("bf16_tflops_sustained"):
-                d["frac_bf16_sustained"] = round(achieved / pk["bf16_tflops_sustained"], 3)
+            d.update(hbm_fracs(nm, ms))
+        if nm == "search":
+            d["kernel"] = "search_gemm_pair_kernel<fused> (fake-quant warps + tcgen05 pair products)"
+            d.update(tensor_fracs(achieved))
         stages[nm] = d
+    # the two halves of the fused stage launched separately, for the per-kernel rooflines
+    separate = {"fakequant": {"ms": round(alone["fakequant"], 4), **hbm_fracs("fakequant", alone["fakequant"])},
+                "search_gemm": {"ms": round(alone["search_gemm"], 4),
+                                **tensor_fracs(flops / (alone["search_gemm"] * 1e-3) / 1e12)}}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -421,11 +453,12 @@ def gpu_arm(args, rank, world, local_rank):
                    "launch": "whole step replayed as one CUDA graph",
                    "l2": "flushed between steps (512 MiB write outside the timed events)"},
         "ms_per_step_eager": round(ms_step_eager, 4),
-        "roofline": {"bound": "tensor", "kernel": "search_gemm_pair_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": "search_gemm_pair_kernel<fused>", "achieved": round(achieved, 1),
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 3),
                      "traffic": traffic, "peak_source": f"{pk['source']} bf16 burst",
                      "algorithmic_flops_per_launch": flops},
         "stages": stages,
+        "stages_unfused": separate,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clocks,

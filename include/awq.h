@@ -165,7 +165,7 @@ AWQ_API awq_status awq_act_stats_noalloc(const void* X, int32_t x_dtype, int64_t
 /* Device bytes of scratch that awq_search_layer needs. Host-only. It holds a
    status word, s and 1/s for every alpha ([n_grid][in] fp32 each), the bf16
    search operand for every alpha ([n_grid (+1 in REFERENCE form)][out][in]),
-   and the per-tile partial sums. */
+   the per-tile partial sums and the operand-tile ready counters. */
 AWQ_API awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, const awq_config* cfg,
                               size_t* bytes);
 
@@ -180,7 +180,9 @@ AWQ_API awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, co
    ws/ws_bytes: scratch, at least awq_workspace_size(); its first 4 bytes are
    the device status word read by awq_get_device_status.
    The products run on bf16 tensor cores with fp32 accumulation; the step-2
-   output matrix never leaves the chip. */
+   output matrix never leaves the chip. In the RESIDUAL form the fake-quant
+   runs inside the search kernel (awq_search_fused); the REFERENCE form runs
+   awq_fakequant and awq_search_gemm one after the other. */
 AWQ_API awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t in,
                             const void* X, int32_t x_dtype, int64_t n_tok, const float* mean_abs,
                             const awq_config* cfg, float* losses, int32_t* best_idx,
@@ -210,8 +212,10 @@ AWQ_API size_t awq_packed_bytes(int64_t out, int64_t in, const awq_config* cfg);
 AWQ_API awq_status awq_get_device_status(const void* ws, awq_stream_t stream, awq_status* status);
 
 /* ------------------------------------------- stages of step 2, one by one
-   awq_search_layer runs exactly these four in this order on its workspace.
-   They are exported so that each kernel can be timed and checked alone. */
+   awq_search_layer runs awq_alpha_scales, then awq_search_fused (RESIDUAL
+   form) or awq_fakequant and awq_search_gemm (REFERENCE form), then
+   awq_loss_select, on its workspace. They are exported so that each kernel
+   can be timed and checked alone. */
 
 /* s[i][j] and inv_s[i][j] = 1/s[i][j] for every alpha_i (device fp32
    [n_grid][in]); the scale law of the search_scale listing and "AWQ >
@@ -245,9 +249,34 @@ AWQ_API awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, con
                            int64_t out, const awq_config* cfg, float* partials, uint32_t* status,
                            awq_stream_t stream);
 
-/* Test aid: awq_search_gemm in RESIDUAL form with a chosen cluster size
-   (cluster_m CTAs share each operand tile through TMA multicast: 1, 2 or 4;
-   0 = the size awq_search_gemm uses). If `dump` is not NULL the kernel also
+/* awq_fakequant followed by awq_search_gemm (RESIDUAL form only), in one
+   kernel: besides the search roles, every CTA of the CTA-pair search kernel
+   runs quantiser warps that write op (bit for bit what awq_fakequant writes)
+   in the order the products consume it, one 256-row operand tile and
+   512-channel strip at a time, and publish each tile in ready[i][nt]; the
+   search waits (bounded) for a tile's counter before loading it, so the
+   fake-quant overlaps the products instead of preceding them.
+   W: device [out][in] (AWQ_BF16 or AWQ_FP32). s, inv_s: as written by
+   awq_alpha_scales. op: device bf16 bits [n_grid][out][in] (scratch, fully
+   written). partials, status: as awq_search_gemm. ready: device uint32
+   scratch of n_grid * (n_tiles + 1) + 1 words (n_tiles from
+   awq_search_tiles): per-tile and per-alpha counters and a progress word
+   (the highest alpha started, plus one); zeroed by the call.
+   Returns AWQ_ERR_UNSUPPORTED for the REFERENCE form. The quantiser warps of
+   one CTA serve tiles consumed by others, so all CTAs of the launch must be
+   resident together, as they are when the GPU runs nothing else (the grid is
+   sized to the SM count); otherwise a wait runs out and *status reports
+   AWQ_ERR_TIMEOUT. */
+AWQ_API awq_status awq_search_fused(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X,
+                                    int64_t n_tok, const float* s, const float* inv_s, const awq_config* cfg,
+                                    uint16_t* op, float* partials, uint32_t* ready, uint32_t* status,
+                                    awq_stream_t stream);
+
+/* Test aid: awq_search_gemm in RESIDUAL form with a chosen kernel:
+   cluster_m 0 = the CTA-pair kernel awq_search_gemm uses (cta_group::2, two
+   CTAs share each 256x256 tile); 1, 2 or 4 = the single-CTA kernel with
+   that many CTAs per cluster sharing each operand tile through TMA
+   multicast. If `dump` is not NULL the kernel also
    stores the raw fp32 products D[i][t][r] = (X op_i^T)[t][r] there (device
    fp32 [n_grid][n_tok][out]), so the tensor-core data path can be checked
    element by element against a plain matrix product on small shapes; those

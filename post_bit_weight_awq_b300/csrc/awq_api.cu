@@ -51,7 +51,7 @@ awq_status check_xdtype(int32_t x_dtype) {
 awq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
 
 struct SearchLayout {
-  size_t status, s, inv_s, op, partials, total;
+  size_t status, s, inv_s, op, partials, ready, total;
   int64_t mt, nt;
 };
 
@@ -72,6 +72,8 @@ SearchLayout search_layout(int64_t n_tok, int64_t out, int64_t in, const awq_con
   off = align_up(off + (size_t)slots * out * in * 2, kAlign);
   L.partials = off;
   off = align_up(off + (size_t)G * L.mt * L.nt * 4 * 4, kAlign);
+  L.ready = off;
+  off = align_up(off + fused_ready_words(G, L.nt) * 4, kAlign);
   L.total = off;
   return L;
 }
@@ -190,6 +192,26 @@ awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, const uint1
                                       (cudaStream_t)stream));
 }
 
+awq_status awq_search_fused(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X, int64_t n_tok,
+                            const float* s, const float* inv_s, const awq_config* cfg, uint16_t* op, float* partials,
+                            uint32_t* ready, uint32_t* status, awq_stream_t stream) {
+  if (W == nullptr || X == nullptr || s == nullptr || inv_s == nullptr || op == nullptr || partials == nullptr ||
+      ready == nullptr || status == nullptr)
+    return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (cfg->loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
+  st = check_wdtype(w_dtype);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(W) || !aligned16(X) || !aligned16(s) || !aligned16(inv_s) || !aligned16(op) ||
+      !aligned16(partials) || !aligned16(ready) || !aligned16(status))
+    return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, s, inv_s, out, *cfg, op, partials,
+                                       ready, status, (cudaStream_t)stream));
+}
+
 awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op, int64_t out,
                                 const awq_config* cfg, float* partials, uint32_t* status, float* dump,
                                 int32_t cluster_m, awq_stream_t stream) {
@@ -263,10 +285,19 @@ awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t
   uint16_t* op = (uint16_t*)(base + L.op);
   float* partials = (float*)(base + L.partials);
 
+  uint32_t* ready = (uint32_t*)(base + L.ready);
+
   cudaError_t e = cudaMemsetAsync(status, 0, 4, s);
   if (e == cudaSuccess) e = launch_alpha_scales(mean_abs, in, *cfg, sc, inv, s);
-  if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
-  if (e == cudaSuccess) e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s);
+  if (cfg->loss_form == AWQ_LOSS_RESIDUAL) {
+    // fake-quant runs inside the search kernel, ahead of the products that consume it
+    if (e == cudaSuccess)
+      e = launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, sc, inv, out, *cfg, op, partials, ready,
+                              status, s);
+  } else {
+    if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
+    if (e == cudaSuccess) e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s);
+  }
   if (e == cudaSuccess)
     e = launch_loss_select(partials, cfg->n_grid, L.mt * L.nt * 4, n_tok, out, sc, in, losses, best_idx, s_best,
                            status, s);

@@ -328,6 +328,15 @@ __device__ __forceinline__ void lds_lane16(const float4* row, int lane, float2 (
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
 
+// Scales of one alpha for fq_lane16, from the lane-ordered shared-memory rows.
+struct SmemLane {
+  const float4* s;
+  const float4* inv;
+  int lane;
+  __device__ __forceinline__ void load_s(float2 (&v)[8]) const { lds_lane16(s, lane, v); }
+  __device__ __forceinline__ void load_inv(float2 (&v)[8]) const { lds_lane16(inv, lane, v); }
+};
+
 template <typename WT, bool REF>
 __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
     fakequant_kernel(const WT* __restrict__ W, int N, int K, int G, const float* __restrict__ s,
@@ -383,54 +392,8 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
       for (int i = 0; i < 8; ++i) nw[i] = make_float2(-w[i].x, -w[i].y);
 #pragma unroll 1
       for (int a = 0; a < gc; ++a) {
-        float2 v[8];
-        {
-          float2 sv[8];
-          lds_lane16(ss + a * 128, slane, sv);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = __fmul2_rn(w[i], sv[i]);
-        }
-        float mn = fminf(v[0].x, v[0].y), mx = fmaxf(v[0].x, v[0].y);
-#pragma unroll
-        for (int i = 1; i < 8; ++i) {
-          mn = fmin3f(mn, v[i].x, v[i].y);
-          mx = fmax3f(mx, v[i].x, v[i].y);
-        }
-#pragma unroll
-        for (int o = 4; o; o >>= 1) {
-          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        }
-        const GroupFast g = group_fast(mn, mx, qmax, floor_);
-        // q - z for the lane's 16 values (see quant_codes_minus_z), as pairs
-        float2 k[8];
-        float dmax = 0.0f;
-        const float2 r2 = make_float2(g.r, g.r);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float2 t = __fmul2_rn(v[i], r2);
-          k[i] = make_float2(rintf(t.x), rintf(t.y));
-          const float2 d = __fadd2_rn(t, make_float2(-k[i].x, -k[i].y));
-          dmax = fmax3f(dmax, fabsf(d.x), fabsf(d.y));
-        }
-        if (!(dmax < g.edge)) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            k[i] = make_float2(rintf(__fdiv_rn(v[i].x, g.delta)), rintf(__fdiv_rn(v[i].y, g.delta)));
-        }
-        if (g.clamp) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) k[i] = make_float2(fminf(k[i].x, g.hi), fminf(k[i].y, g.hi));
-        }
-        float2 iv[8];
-        lds_lane16(si + a * 128, slane, iv);
-        const float2 d2 = make_float2(g.delta, g.delta);
         uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float2 dq = __fmul2_rn(k[i], d2);  // dequantised, scaled space
-          o[i] = pack_bf16x2(REF ? __fmul2_rn(dq, iv[i]) : __ffma2_rn(dq, iv[i], nw[i]));
-        }
+        fq_lane16<REF>(w, nw, SmemLane{ss + a * 128, si + a * 128, slane}, qmax, floor_, o);
         if (active) {
           uint4* dst = reinterpret_cast<uint4*>(op + (size_t)(a0 + a) * slot_elems + base);
           dst[0] = make_uint4(o[0], o[1], o[2], o[3]);

@@ -43,4 +43,17 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
 // cluster_m: 0 = default kernel (CTA pairs, cta_group::2, for the RESIDUAL
 // form); 1, 2 or 4 = the single-CTA kernel with clusters of that size.
 
+// Words of the fused search's synchronisation scratch: a counter per operand
+// tile and per alpha, and one progress word.
+inline size_t fused_ready_words(int64_t G, int64_t n_tiles) { return (size_t)(G * (n_tiles + 1) + 1); }
+
+// RESIDUAL form with the fake-quant fused in: quantiser warps in every CTA of
+// the CTA-pair search kernel write op (as launch_fakequant does) while the
+// search consumes it. ready: uint32 [fused_ready_words(n_grid, ceil(N/256))],
+// zeroed by the call.
+cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, int64_t n_tok, int64_t K,
+                                const float* s, const float* inv_s, int64_t N, const awq_config& cfg, uint16_t* op,
+                                float* partials, uint32_t* ready, uint32_t* status, cudaStream_t st,
+                                float* dump = nullptr);
+
 }  // namespace awq

@@ -36,6 +36,7 @@
 // and MMAs land, frees tensor memory and returns.
 #include "awq_device.cuh"
 #include "awq_launch.h"
+#include "awq_quant.cuh"
 
 namespace awq {
 namespace {
@@ -66,6 +67,17 @@ struct Params {
   float* dump;        // optional raw products [G][n_tok][N] (RESIDUAL, test aid)
   int n_tok, N;
   int withhold_first_fill;  // test aid: leave out each CTA's first operand fill
+  // fused fake-quant (pair kernel with quantiser warps)
+  const void* W;            // [N][K] bf16 bits or fp32
+  int w_bf16;
+  int K;
+  int nstrips;              // 512-channel strips of K
+  const float* s;           // [G][K]
+  const float* inv_s;       // [G][K]
+  uint16_t* op;             // [G][N][K] bf16, written by the quantiser warps
+  uint32_t* ready;          // [G][nt] quantiser-warp arrivals per operand tile, then [G] per alpha,
+                            // then the search progress word (see quantise_units)
+  float qmax, floor_;
 };
 
 // Tile t of an m_tiles x nt grid in raster order. Tiles are taken in bands
@@ -349,6 +361,134 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // barriers.
 
 constexpr int kPairStages = 6;
+constexpr int kFqWarpsFused = 8;                                 // quantiser warps per CTA (fused form)
+constexpr int kFusedThreads = NUM_THREADS + 32 * kFqWarpsFused;  // 448
+constexpr int kFqStrip = 512;                                    // channels per quantiser unit
+
+// Wait until *ctr >= need (acquire at GPU scope), bounded like mbar_wait.
+__device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t need, uint64_t timeout_ns,
+                                             volatile int* abort_flag, uint32_t* status) {
+  if (ld_acquire_gpu(ctr) >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(ctr) >= need) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) break;
+    }
+  }
+  set_status(status, AWQ_ERR_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+// The lane's 16 scales and reciprocals, held in registers for a unit.
+struct RegLane {
+  const float2 (&s)[8];
+  const float2 (&inv)[8];
+  __device__ __forceinline__ void load_s(float2 (&v)[8]) const {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = s[i];
+  }
+  __device__ __forceinline__ void load_inv(float2 (&v)[8]) const {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = inv[i];
+  }
+};
+
+__device__ __forceinline__ void ldg_lane16(const float* p, float2 (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  const float4 c = *reinterpret_cast<const float4*>(p + 64);
+  const float4 d = *reinterpret_cast<const float4*>(p + 68);
+  v[0] = make_float2(a.x, a.y);
+  v[1] = make_float2(a.z, a.w);
+  v[2] = make_float2(b.x, b.y);
+  v[3] = make_float2(b.z, b.w);
+  v[4] = make_float2(c.x, c.y);
+  v[5] = make_float2(c.z, c.w);
+  v[6] = make_float2(d.x, d.y);
+  v[7] = make_float2(d.z, d.w);
+}
+
+// 16 weights of a lane: channels [c, c+8) and [c+64, c+72) of a row.
+__device__ __forceinline__ void ldg_w16(const void* W, int w_bf16, size_t off, float2 (&w)[8]) {
+  if (w_bf16) {
+    const uint16_t* p = static_cast<const uint16_t*>(W) + off;
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    const uint4 b = *reinterpret_cast<const uint4*>(p + 64);
+    const uint32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = make_float2(bf16_lo(x[i]), bf16_hi(x[i]));
+  } else {
+    ldg_lane16(static_cast<const float*>(W) + off, w);
+  }
+}
+
+// Quantiser warps of the fused form. The search operand of alpha a is cut
+// into units (a, operand-row tile nb, 512-channel strip), numbered a-major
+// then nb then strip, i.e. in the order the search consumes them, and dealt
+// to the CTAs round-robin. The CTA's 8 quantiser warps take 32 rows of the
+// unit's 256 each (lane layout and arithmetic as in the fake-quant kernel,
+// with the lane's scales held in registers for the unit), then each warp
+// publishes its rows: every lane fences (generic -> async proxy, then GPU
+// scope), and lane 0 adds 1 to ready[a][nb] and to the alpha's counter with
+// release semantics. A tile is complete when its counter reaches
+// nstrips * 8, an alpha when its counter reaches nt * nstrips * 8. The
+// quantisers never wait, so every unit is finished as long as all CTAs of
+// the launch are resident, which the grid size ensures on a GPU that runs
+// nothing else. (Holding the quantisers a fixed number of alphas ahead of
+// the products, so that each operand is written just before it is read,
+// measured no faster on the benchmark layers.)
+__device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane) {
+  const int grp = lane >> 3, sub = lane & 7;
+  const int per_a = p.nt * p.nstrips;
+  const int units = p.G * per_a;
+  const size_t slot = (size_t)p.N * p.K;
+  uint32_t* ready_alpha = p.ready + (size_t)p.G * p.nt;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int a = u / per_a;
+    const int rem = u - a * per_a;
+    const int nb = rem / p.nstrips;
+    const int col0 = (rem - nb * p.nstrips) * kFqStrip;
+    const int ncols = min(kFqStrip, p.K - col0);
+    const bool active = grp * 128 < ncols;  // groups past a partial strip repeat group 0, store nothing
+    const int c = col0 + (active ? grp * 128 : 0) + sub * 8;
+    const int r0 = nb * BN + fw * 32;
+    const int r1 = min(r0 + 32, p.N);
+    if (r0 < r1) {
+      float2 sv[8], iv[8];
+      ldg_lane16(p.s + (size_t)a * p.K + c, sv);
+      ldg_lane16(p.inv_s + (size_t)a * p.K + c, iv);
+      float2 wn[8];
+      ldg_w16(p.W, p.w_bf16, (size_t)r0 * p.K + c, wn);
+      for (int r = r0; r < r1; ++r) {
+        float2 w[8], nw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          w[i] = wn[i];
+          nw[i] = make_float2(-w[i].x, -w[i].y);
+        }
+        if (r + 1 < r1) ldg_w16(p.W, p.w_bf16, (size_t)(r + 1) * p.K + c, wn);
+        uint32_t o[8];
+        fq_lane16<false>(w, nw, RegLane{sv, iv}, p.qmax, p.floor_, o);
+        if (active) {
+          uint4* dst = reinterpret_cast<uint4*>(p.op + (size_t)a * slot + (size_t)r * p.K + c);
+          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          dst[8] = make_uint4(o[4], o[5], o[6], o[7]);  // 64 channels further on
+        }
+      }
+    }
+    fence_proxy_async_global();
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      red_release_gpu_add(&p.ready[(size_t)a * p.nt + nb], 1u);
+      red_release_gpu_add(&ready_alpha[a], 1u);
+    }
+  }
+}
 constexpr int PA_BYTES = BM * BK * 2;          // 16 KiB: this CTA's token rows
 constexpr int PB_BYTES = (BN / 2) * BK * 2;    // 16 KiB: this CTA's half of the operand rows
 constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
@@ -356,7 +496,8 @@ constexpr int PAIR_SMEM_BYTES = kPairStages * PSTAGE_BYTES + 1024 + BAR_BYTES;
 constexpr uint32_t PAIR_IDESC = umma_idesc_bf16_f32(2 * BM, BN);
 static_assert(PAIR_SMEM_BYTES <= 232448, "shared memory per CTA");
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <bool FUSED>
+__global__ void __launch_bounds__(FUSED ? kFusedThreads : NUM_THREADS, 1)
     search_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                             const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -414,12 +555,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t used = 0, last_par = 0;
       bool ok = true;
+      int started = -1, verified = -1;  // fused form: newest alpha started / known fully quantised
       for (int it = pair; it < p.items && ok; it += npairs) {
         const int a = it / (p.mtg * p.nt);
         const int t = it - a * p.mtg * p.nt;
         int mg, nb;
         decode_tile(t, p.mtg, p.nt, p.raster_group, p.raster_n, mg, nb);
         const int mb = mg * 2 + (int)rank;
+        if (FUSED) {
+          if (a > started) {
+            started = a;
+            atomicMax(p.ready + (size_t)p.G * p.nt + p.G, (uint32_t)(a + 1));  // progress word (diagnostic)
+          }
+          if (a != verified) {
+            // the quantiser warps of every CTA have written this operand tile
+            // (or the whole alpha, after which no further check is needed)
+            const uint32_t* alpha_ctr = p.ready + (size_t)p.G * p.nt + a;
+            if (ld_acquire_gpu(alpha_ctr) >= (uint32_t)(p.nt * p.nstrips * kFqWarpsFused)) {
+              verified = a;
+            } else if (!wait_counter(&p.ready[(size_t)a * p.nt + nb], (uint32_t)(p.nstrips * kFqWarpsFused),
+                                     p.timeout_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_global();  // order the TMA reads after the quantisers' generic-proxy writes
+          }
+        }
         for (int kb = 0; kb < p.kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status)) {
             ok = false;
@@ -480,7 +641,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       umma_commit_pair(drain);
       mbar_wait(drain, 0u, p.timeout_ns, nullptr, p.status);
     }
-  } else {
+  } else if (warp < 6) {
     // -------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -524,6 +685,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (lane == 0 && mb < p.mt) p.partials[((((size_t)a * p.mt + mb) * p.nt + nb) << 2) + q] = ss;
     }
+  } else if (FUSED) {
+    // -------------------------------------------------------------- quantiser warps (both CTAs)
+    quantise_units(p, warp - 6, lane);
   }
 
   tc_fence_before();
@@ -598,8 +762,10 @@ cudaError_t launch_residual(const CUtensorMap& tmX, const CUtensorMap& tmB, Para
   return cudaLaunchKernelEx(&lc, search_gemm_kernel<false, CM>, tmX, tmB, p);
 }
 
-cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmB, Params p, int sms, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(search_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <bool FUSED>
+cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmB, const Params& p, int sms, cudaStream_t st) {
+  constexpr int threads = FUSED ? kFusedThreads : NUM_THREADS;
+  cudaError_t e = cudaFuncSetAttribute(search_gemm_pair_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        PAIR_SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
@@ -608,7 +774,7 @@ cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmB, Params p
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  lc.blockDim = dim3(NUM_THREADS);
+  lc.blockDim = dim3(threads);
   lc.dynamicSmemBytes = PAIR_SMEM_BYTES;
   lc.stream = st;
   lc.attrs = attr;
@@ -616,42 +782,36 @@ cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmB, Params p
   int pairs = sms / 2;
   lc.gridDim = dim3(2 * pairs);
   int active = 0;
-  e = cudaOccupancyMaxActiveClusters(&active, search_gemm_pair_kernel, &lc);
+  e = cudaOccupancyMaxActiveClusters(&active, search_gemm_pair_kernel<FUSED>, &lc);
   if (e != cudaSuccess) return e;
   if (active > 0 && active < pairs) pairs = active;
-  if (pairs > p.items) pairs = p.items;
+  // The fused form keeps every pair even without search items of its own:
+  // its quantiser warps serve the operand tiles of other pairs.
+  if (!FUSED && pairs > p.items) pairs = p.items;
   lc.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&lc, search_gemm_pair_kernel, tmX, tmB, p);
+  return cudaLaunchKernelEx(&lc, search_gemm_pair_kernel<FUSED>, tmX, tmB, p);
 }
 
-}  // namespace
-
-cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
-                               const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
-                               float* dump, int withhold_first_fill, int cluster_m) {
+// Tensor maps and tiling of a search launch. CM: CTAs per cluster sharing an
+// operand tile (2 for the CTA-pair kernels).
+cudaError_t setup_search(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
+                         const awq_config& cfg, int CM, CUtensorMap* tmX, CUtensorMap* tmB, Params* pp, int* sms) {
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
   const int G = cfg.n_grid;
   const int slots = ref ? G + 1 : G;
-  // cluster_m 0: the default (CTA pairs for RESIDUAL, single CTAs for
-  // REFERENCE); 1, 2 or 4: the single-CTA kernel with that cluster size.
-  const bool pair = !ref && !withhold_first_fill && cluster_m == 0;
-  int CM = pair ? 2 : (cluster_m > 0 ? cluster_m : 1);
-  if (ref || withhold_first_fill) CM = 1;
-  if (CM != 1 && CM != 2 && CM != 4) return cudaErrorInvalidValue;
-  CUtensorMap tmX, tmB;
   const cuuint64_t xd[2] = {(cuuint64_t)K, (cuuint64_t)n_tok};
   const cuuint32_t xb[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
   const cuuint64_t bd[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)slots};
   const cuuint32_t bb[3] = {(cuuint32_t)BK, (cuuint32_t)(BN / CM), 1u};
-  if (!make_map(&tmX, X, 2, xd, xb) || !make_map(&tmB, op, 3, bd, bb)) return cudaErrorInvalidValue;
+  if (!make_map(tmX, X, 2, xd, xb) || !make_map(tmB, op, 3, bd, bb)) return cudaErrorInvalidValue;
 
-  int dev = 0, sms = 0;
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
 
-  Params p;
+  Params p = {};
   p.mt = (int)((n_tok + BM - 1) / BM);
   p.nt = (int)((N + BN - 1) / BN);
   p.mtg = (p.mt + CM - 1) / CM;
@@ -666,11 +826,33 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
   if (p.raster_group > p.mtg) p.raster_group = p.mtg;
   const uint32_t ms = cfg.wait_timeout_ms ? cfg.wait_timeout_ms : 2000u;
   p.timeout_ns = (uint64_t)ms * 1000000ull;
+  p.n_tok = (int)n_tok;
+  p.N = (int)N;
+  p.K = (int)K;
+  *pp = p;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
+                               const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
+                               float* dump, int withhold_first_fill, int cluster_m) {
+  const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
+  // cluster_m 0: the default (CTA pairs for RESIDUAL, single CTAs for
+  // REFERENCE); 1, 2 or 4: the single-CTA kernel with that cluster size.
+  const bool pair = !ref && !withhold_first_fill && cluster_m == 0;
+  int CM = pair ? 2 : (cluster_m > 0 ? cluster_m : 1);
+  if (ref || withhold_first_fill) CM = 1;
+  if (CM != 1 && CM != 2 && CM != 4) return cudaErrorInvalidValue;
+  CUtensorMap tmX, tmB;
+  Params p;
+  int sms = 0;
+  cudaError_t e = setup_search(X, n_tok, K, op, N, cfg, CM, &tmX, &tmB, &p, &sms);
+  if (e != cudaSuccess) return e;
   p.partials = partials;
   p.status = status;
   p.dump = ref ? nullptr : dump;
-  p.n_tok = (int)n_tok;
-  p.N = (int)N;
   p.withhold_first_fill = withhold_first_fill;
 
   if (ref) {
@@ -681,10 +863,38 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
     search_gemm_kernel<true, 1><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);
     return cudaGetLastError();
   }
-  if (pair) e = launch_pair(tmX, tmB, p, sms, st);
+  if (pair) e = launch_pair<false>(tmX, tmB, p, sms, st);
   else if (CM == 1) e = launch_residual<1>(tmX, tmB, p, sms, st);
   else if (CM == 2) e = launch_residual<2>(tmX, tmB, p, sms, st);
   else e = launch_residual<4>(tmX, tmB, p, sms, st);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, int64_t n_tok, int64_t K,
+                                const float* s, const float* inv_s, int64_t N, const awq_config& cfg, uint16_t* op,
+                                float* partials, uint32_t* ready, uint32_t* status, cudaStream_t st, float* dump) {
+  if (cfg.loss_form != AWQ_LOSS_RESIDUAL) return cudaErrorInvalidValue;
+  CUtensorMap tmX, tmB;
+  Params p;
+  int sms = 0;
+  cudaError_t e = setup_search(X, n_tok, K, op, N, cfg, 2, &tmX, &tmB, &p, &sms);
+  if (e != cudaSuccess) return e;
+  p.partials = partials;
+  p.status = status;
+  p.dump = dump;
+  p.W = W;
+  p.w_bf16 = w_dtype == AWQ_BF16 ? 1 : 0;
+  p.nstrips = (int)((K + kFqStrip - 1) / kFqStrip);
+  p.s = s;
+  p.inv_s = inv_s;
+  p.op = op;
+  p.ready = ready;
+  p.qmax = (float)((1 << cfg.w_bit) - 1);
+  p.floor_ = cfg.delta_floor;
+  e = cudaMemsetAsync(ready, 0, fused_ready_words(p.G, p.nt) * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  e = launch_pair<true>(tmX, tmB, p, sms, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

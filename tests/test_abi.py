@@ -37,9 +37,8 @@ def test_library_exports_every_declared_symbol(lib):
     assert exported == header_functions()
 
 
-def test_library_is_built_for_sm_103a(lib):
-    out = os.popen(f"cuobjdump --list-elf {capi.LIB_PATH} 2>&1").read()
-    assert "sm_103a" in out
+def test_library_is_built_for_sm_103a_only():
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
 def test_config_default(lib):
@@ -121,3 +120,15 @@ def test_host_validation_of_search_and_pack(lib):
     assert _status_of(p, A, B, cfg, C, D + 1, D, 0, **pkw) == capi.AWQ_ERR_MISALIGNED
     assert _status_of(p, A, B, capi.config(w_bit=8), C, D, D, 0, **pkw) == capi.AWQ_ERR_UNSUPPORTED
     assert _status_of(p, A, B, cfg, C, D, D, 0, **{**pkw, "w_dtype": 3}) == capi.AWQ_ERR_INVALID_ARG
+
+
+def test_host_validation_of_fused_search(lib):
+    A, B, C, D = 0x1000, 0x2000, 0x3000, 0x4000
+    f = capi.awq_search_fused
+    kw = dict(out_features=256, in_features=256, n_tok=128, w_dtype=capi.AWQ_BF16)
+    cfg = capi.config()
+    assert _status_of(f, A, B, C, C, capi.config(loss_form=capi.AWQ_LOSS_REFERENCE), D, D, D, D, 0, **kw) == \
+        capi.AWQ_ERR_UNSUPPORTED
+    assert _status_of(f, A, B, C, C, cfg, D, D, 0, D, 0, **kw) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A, B, C, C, cfg, D, D, D + 4, D, 0, **kw) == capi.AWQ_ERR_MISALIGNED
+    assert _status_of(f, A, B, C, C, cfg, D, D, D, D, 0, **{**kw, "w_dtype": 9}) == capi.AWQ_ERR_INVALID_ARG

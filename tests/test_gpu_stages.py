@@ -160,6 +160,48 @@ def test_search_gemm_products_and_partials(n, N, K, G, cluster_m):
         np.testing.assert_allclose(partials2.cpu().numpy(), partials.cpu().numpy(), rtol=1e-5, atol=1e-6)
 
 
+# ------------------------------------------------------------------ fused fake-quant + search product
+
+
+@pytest.mark.parametrize("layer,kw", [("tiny", {}),
+                                      ("llama7b_q_proj", dict(out_features=300, in_features=640, n_tok=257)),
+                                      ("llama7b_q_proj", dict(out_features=1024, in_features=1024, n_tok=512)),
+                                      ("70b_mlp", dict(out_features=520, in_features=8192, n_tok=130))])
+def test_fused_search_matches_separate_stages(layer, kw):
+    """The quantiser warps of the fused kernel write exactly the operand that
+    awq_fakequant writes, and the products consume it only once it is
+    complete: op and the partial sums equal the two-launch path bit for bit
+    (ragged operand tiles, a partial channel strip, fp32 weights included)."""
+    L = workloads.make_layer(layer, **kw)
+    N, K = L["W"].shape
+    n = L["X"].shape[0]
+    W, X = dev_weight(L), dev_bf16(L["X"])
+    cfg = capi.config()
+    G = cfg.n_grid
+    s = torch.empty(G, K, dtype=torch.float32, device="cuda")
+    inv = torch.empty_like(s)
+    capi.awq_alpha_scales(dev_f32(O.f32(O.channel_importance(L["X"]))), cfg, s, inv)
+    op_ref = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
+    capi.awq_fakequant(W, s, inv, cfg, op_ref)
+    mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
+    p_ref = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    capi.awq_search_gemm(X, op_ref, cfg, p_ref, status, n_tok=n, in_features=K, out_features=N)
+    op = torch.full_like(op_ref, float("nan"))
+    parts = torch.full_like(p_ref, float("nan"))
+    ready = torch.full((G * (nt + 1) + 1,), 7, dtype=torch.int32, device="cuda")  # the call zeroes it
+    for _ in range(2):  # twice: ready counters and op are reset / rewritten by each call
+        capi.awq_search_fused(W, X, s, inv, cfg, op, parts, ready, status)
+        torch.cuda.synchronize()
+        assert int(status[0]) == 0
+        assert torch.equal(op.view(torch.int16), op_ref.view(torch.int16))
+        assert torch.equal(parts, p_ref)
+        strips8 = ((K + 511) // 512) * 8
+        assert torch.all(ready[:G * nt] == strips8)  # every tile, every strip, every quantiser warp
+        assert torch.all(ready[G * nt:G * (nt + 1)] == nt * strips8)
+        assert int(ready[-1]) == G  # the search started every alpha
+
+
 # ------------------------------------------------------------------ loss + argmin
 
 
