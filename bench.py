@@ -384,6 +384,47 @@ def gpu_arm(args, rank, world, local_rank):
         e2e_ms = multi.max_over_ranks(e2e_ms, device=dev) / world
     assert capi.awq_get_device_status(search_ws, stream) == capi.AWQ_OK
 
+    # ---------------------------------------------------------- the packed layer in use (w4a16 decode product)
+    # copies of the packed layer, more bytes than L2, applied one after another to one token (a decode step
+    # running through layers): HBM bandwidth of awq_w4a16_gemv
+    gemv = None
+    if K * 4 <= 50 * 1024:
+        layer_bytes = N * K // 2 + 2 * 2 * N * (K // 128)
+        copies = max(4, int((256 << 20) // layer_bytes) + 1)
+        packs = [(qw.clone(), sc.clone(), zr.clone()) for _ in range(copies)]
+        xg = torch.randn(1, K, device=dev).to(torch.bfloat16)
+        yg = torch.empty(1, N, dtype=f32, device=dev)
+        gcfg = capi.config()
+
+        def gemv_pass():
+            st = torch.cuda.current_stream(dev)
+            for q_, s_, z_ in packs:
+                capi.awq_w4a16_gemv(xg, q_, s_, z_, gcfg, yg, st)
+
+        gemv_pass()
+        gg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gg):
+            gemv_pass()
+        for _ in range(3):
+            gg.replay()
+        torch.cuda.synchronize()
+        gt = []
+        for _ in range(max(3, args.steps // 2)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            gg.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            gt.append(a.elapsed_time(b) / copies)
+        ms_g = statistics.median(gt)
+        gbytes = layer_bytes + K * 2 + N * 4
+        gemv = {"kernel": "w4a16_gemv_kernel<1>", "tokens": 1, "layer": [N, K], "ms_per_layer": round(ms_g, 5),
+                "bytes_per_layer": gbytes, "gbs": round(gbytes / (ms_g * 1e-3) / 1e9, 1),
+                "frac_hbm": round(gbytes / (ms_g * 1e-3) / 1e9 / peaks()["hbm_gbs"], 3),
+                "timing": f"{copies} distinct copies per CUDA graph (> L2), L2 flushed before each graph"}
+        del packs
+
     # ---------------------------------------------------------- parity spot check vs stored oracle losses
     parity = None
     gpath = os.path.join(ROOT, "tests", "golden", "oracle_losses.json")
@@ -459,6 +500,7 @@ def gpu_arm(args, rank, world, local_rank):
                      "algorithmic_flops_per_launch": flops},
         "stages": stages,
         "stages_unfused": separate,
+        "w4a16_gemv": gemv,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clocks,

@@ -203,6 +203,30 @@ AWQ_API awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out
                              const float* s, const awq_config* cfg, int32_t* qweight,
                              uint16_t* scales_f16, uint16_t* zeros_f16, awq_stream_t stream);
 
+/* ---------------------------------------------------------------- using the packed layer */
+
+/* Largest token count, and token count times `in`, that awq_w4a16_gemv
+   accepts (the tokens' activations are staged in shared memory as fp32). */
+#define AWQ_W4A16_MAX_TOKENS 8
+#define AWQ_W4A16_MAX_TOKEN_CHANNELS (50 * 1024)
+
+/* The packed layer applied to a few tokens (w4a16, the decode case):
+   y[t][r] = sum_k x[t][k] * (q[r][k] - z[r][g]) * scale[r][g], g = k / group,
+   with q, scale, z as written by awq_quantize_pack ("AWQ: How
+   Activation-Aware Quantization Saves 4-bit LLMs", "What do you actually
+   deploy" and the decode remark after it: decoding is memory-bound and reads
+   a quarter of the fp16 weight bytes). The codes quantise W * diag(s_best),
+   so x is the layer input already divided by s_best (folded into its
+   producer). x: device bf16 [n_tok][in] (x_dtype AWQ_BF16), 1 <= n_tok <=
+   AWQ_W4A16_MAX_TOKENS and n_tok * in <= AWQ_W4A16_MAX_TOKEN_CHANNELS,
+   else AWQ_ERR_UNSUPPORTED. qweight/scales_f16/zeros_f16: as
+   awq_quantize_pack (qweight 16-byte aligned). y: device fp32 [n_tok][out].
+   Each code is read once from memory; products and sums in fp32 (exact
+   dequantised weights, fp32 fused multiply-adds in a fixed order). */
+AWQ_API awq_status awq_w4a16_gemv(const void* x, int32_t x_dtype, int64_t n_tok, int64_t in,
+                                  const int32_t* qweight, const uint16_t* scales_f16, const uint16_t* zeros_f16,
+                                  int64_t out, const awq_config* cfg, float* y, awq_stream_t stream);
+
 /* Bytes of the packed layer (codes + scales + zeros), host-only; 0 for
    invalid arguments. */
 AWQ_API size_t awq_packed_bytes(int64_t out, int64_t in, const awq_config* cfg);

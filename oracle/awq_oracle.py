@@ -23,6 +23,9 @@ Sources (web pages on AWQ, cited by title and section):
   INT32 containers).
 * [AWQ-Ref]    "AWQ (Activation-Aware Weight Quantization) - AI Glossary",
   "Example: Where 4-bit memory saving comes from" (13e9-weight arithmetic).
+* [AWQ-devto] "What do you actually deploy" (w4a16: 4-bit weights, 16-bit
+  activations) and the decode remark after it (token-by-token decoding is
+  memory-bound, so reading a quarter of the weight bytes is the payoff).
 
 Readings taken where the pages are silent or disagree (each also listed in
 the design notes):
@@ -72,6 +75,7 @@ __all__ = [
     "unpack_words",
     "quantize_pack",
     "packed_bytes",
+    "w4a16_linear",
 ]
 
 
@@ -317,3 +321,25 @@ def packed_bytes(out_features: int, in_features: int, group: int = 128, w_bit: i
     scales = (n // group) * 2
     zeros = (n // group) * 2 if zero_point else 0
     return {"codes": codes, "scales": scales, "zeros": zeros, "total": codes + scales + zeros}
+
+
+def w4a16_linear(x, qweight, scales_f16, zeros_f16, group: int = 128) -> np.ndarray:
+    """y = x @ W_hat^T for a packed layer: W_hat[r, k] = (q[r, k] - z[r, g]) * scale[r, g].
+
+    [AWQ-devto, "What do you actually deploy": 4-bit weights with 16-bit
+    activations; the decode remark: decoding reads the packed weights.]
+    The layer is the output of ``quantize_pack``: codes of W * diag(s), so the
+    caller passes activations already divided by s (the fold into the
+    preceding norm described in "AWQ > Salient Weight Preservation").
+    x: [M, in]; qweight int32 [out, in/8]; scales/zeros fp16 [out, in/group].
+    fp64 arithmetic on the stored fp16 values. Returns fp64 [M, out].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out_f = np.asarray(qweight).shape[0]
+    K = np.asarray(qweight).shape[1] * 8
+    q = unpack_words(qweight, K).astype(np.float64)
+    sc = np.asarray(scales_f16, dtype=np.float16).astype(np.float64)
+    z = np.asarray(zeros_f16, dtype=np.float16).astype(np.float64)
+    W_hat = dequantize_groups(q, sc, z, group)
+    assert W_hat.shape == (out_f, K)
+    return x @ W_hat.T

@@ -38,6 +38,7 @@ EXPORTED = (
     "awq_workspace_size",
     "awq_search_layer",
     "awq_quantize_pack",
+    "awq_w4a16_gemv",
     "awq_packed_bytes",
     "awq_get_device_status",
     "awq_alpha_scales",
@@ -97,6 +98,7 @@ def lib() -> ctypes.CDLL:
         "awq_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _CFG, ctypes.POINTER(_SZ)]),
         "awq_search_layer": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _I64, _P, _CFG, _P, _P, _P, _P, _SZ, _P]),
         "awq_quantize_pack": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _CFG, _P, _P, _P, _P]),
+        "awq_w4a16_gemv": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _I64, _CFG, _P, _P]),
         "awq_packed_bytes": (_SZ, [_I64, _I64, _CFG]),
         "awq_get_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
         "awq_alpha_scales": (ctypes.c_int, [_P, _I64, _CFG, _P, _P, _P]),
@@ -244,6 +246,16 @@ def awq_quantize_pack(W, s, cfg: AwqConfig, qweight, scales, zeros, stream=None,
     wd = _dtype_code(W) if w_dtype is None else w_dtype
     _check(lib().awq_quantize_pack(_ptr(W), wd, N, K, _ptr(s), ctypes.byref(cfg), _ptr(qweight), _ptr(scales),
                                    _ptr(zeros), _stream(stream)), "awq_quantize_pack")
+
+
+def awq_w4a16_gemv(x, qweight, scales, zeros, cfg: AwqConfig, y, stream=None, *, n_tok=None, in_features=None,
+                   out_features=None, x_dtype=None) -> None:
+    n = x.shape[0] if n_tok is None else n_tok
+    K = x.shape[1] if in_features is None else in_features
+    N = qweight.shape[0] if out_features is None else out_features
+    xd = _dtype_code(x) if x_dtype is None else x_dtype
+    _check(lib().awq_w4a16_gemv(_ptr(x), xd, n, K, _ptr(qweight), _ptr(scales), _ptr(zeros), N, ctypes.byref(cfg),
+                                _ptr(y), _stream(stream)), "awq_w4a16_gemv")
 
 
 def awq_get_device_status(ws, stream=None) -> int:

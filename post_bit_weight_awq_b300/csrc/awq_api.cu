@@ -322,6 +322,25 @@ awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out, int64_
                                (cudaStream_t)stream));
 }
 
+awq_status awq_w4a16_gemv(const void* x, int32_t x_dtype, int64_t n_tok, int64_t in, const int32_t* qweight,
+                          const uint16_t* scales_f16, const uint16_t* zeros_f16, int64_t out, const awq_config* cfg,
+                          float* y, awq_stream_t stream) {
+  if (x == nullptr || qweight == nullptr || scales_f16 == nullptr || zeros_f16 == nullptr || y == nullptr)
+    return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_xdtype(x_dtype);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  if (n_tok > AWQ_W4A16_MAX_TOKENS || n_tok * in > AWQ_W4A16_MAX_TOKEN_CHANNELS) return AWQ_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(qweight) || (reinterpret_cast<uintptr_t>(scales_f16) & 1u) ||
+      (reinterpret_cast<uintptr_t>(zeros_f16) & 1u) || (reinterpret_cast<uintptr_t>(y) & 3u))
+    return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_w4a16_gemv((const uint16_t*)x, n_tok, in, qweight, scales_f16, zeros_f16, out, y,
+                                     (cudaStream_t)stream));
+}
+
 size_t awq_packed_bytes(int64_t out, int64_t in, const awq_config* cfg) {
   if (check_cfg(cfg) != AWQ_OK || out < 1 || in < 1 || in % cfg->group != 0) return 0;
   const size_t n = (size_t)out * (size_t)in;

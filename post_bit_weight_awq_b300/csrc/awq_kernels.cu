@@ -85,12 +85,21 @@ __global__ void __launch_bounds__(256) stats_kernel(const uint16_t* __restrict__
   __threadfence();
   // compensated (Neumaier) fp32 sum over the chunks, fixed order; the other
   // blocks' partials are read past L1
+  // (loads issued 8 chunks at a time, so the L2 round trips overlap)
+  const int chunks = (int)gridDim.y;
   float s = 0.0f, comp = 0.0f;
-  for (int i = 0; i < (int)gridDim.y; ++i) {
-    const float x = __ldcg(partials + (size_t)i * K + c);
-    const float u = __fadd_rn(s, x);
-    comp = __fadd_rn(comp, fabsf(s) >= fabsf(x) ? __fadd_rn(__fsub_rn(s, u), x) : __fadd_rn(__fsub_rn(x, u), s));
-    s = u;
+  for (int i0 = 0; i0 < chunks; i0 += 8) {
+    float xb[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) xb[u] = i0 + u < chunks ? __ldcg(partials + (size_t)(i0 + u) * K + c) : 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (i0 + u >= chunks) break;
+      const float x = xb[u];
+      const float v = __fadd_rn(s, x);
+      comp = __fadd_rn(comp, fabsf(s) >= fabsf(x) ? __fadd_rn(__fsub_rn(s, v), x) : __fadd_rn(__fsub_rn(x, v), s));
+      s = v;
+    }
   }
   mean_abs[c] = (float)(((double)s + (double)comp) / (double)n);
 }
@@ -113,29 +122,32 @@ cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partial
 // formula"), alpha_i = i / n_grid, then optionally s_i /= sqrt(max(s_i) *
 // min(s_i)). The scale decides the codes, so it is formed in fp64 and rounded
 // to fp32 once. Since alpha_i = i / n_grid, b^alpha_i = (b^(1/n_grid))^i: one
-// pow per channel, then one fp64 product per alpha (the products drift from
-// a direct pow by at most ~n_grid fp64 ulps, which changes the fp32-rounded
-// scale only when it lies that close to an fp32 rounding boundary). x^alpha
-// is non-decreasing in x, so max(s_i) and min(s_i) are the powers of the
-// largest and smallest clamped statistic; every block finds those two (16-byte
-// loads of the whole vector, a fixed-order reduction) and its first n_grid
-// threads form 1 / sqrt(max * min) per alpha while the others start on their
-// channel's powers. One thread per channel, 64 channels per block so that
-// the fp64 work spreads over many SMs; alpha = 0 gives s = 1 exactly.
+// pow per channel, then fp64 products (the products drift from a direct pow
+// by at most ~n_grid fp64 ulps, which changes the fp32-rounded scale only
+// when it lies that close to an fp32 rounding boundary). x^alpha is
+// non-decreasing in x, so max(s_i) and min(s_i) are the powers of the
+// largest and smallest clamped statistic.
+// fp64 runs at 1/64 of the fp32 rate on this GPU, so the kernel is a chain of
+// fp64 latencies; it keeps the chains short and parallel: 32 channels per
+// block of two warps. Both warps find the statistic's max/min (16-byte loads,
+// fixed-order reduction); then warp 0 forms 1 / sqrt(max * min) per alpha
+// while warp 1 forms each channel's root b^(1/n_grid); then warp w writes the
+// alphas of parity w for the 32 channels, stepping by root^2. alpha = 0 gives
+// s = 1 exactly.
 
-constexpr int kAlphaThreads = 64;
+constexpr int kAlphaChannels = 32;
 
-__global__ void __launch_bounds__(kAlphaThreads) alpha_scales_kernel(const float* __restrict__ mean_abs, int K, int G,
-                                                                     double clamp_min, int normalize,
-                                                                     float* __restrict__ s_out,
-                                                                     float* __restrict__ inv_out) {
-  __shared__ float smax[kAlphaThreads / 32], smin[kAlphaThreads / 32];
+__global__ void __launch_bounds__(64) alpha_scales_kernel(const float* __restrict__ mean_abs, int K, int G,
+                                                          double clamp_min, int normalize,
+                                                          float* __restrict__ s_out, float* __restrict__ inv_out) {
+  __shared__ float smax[2], smin[2];
   __shared__ double inv_norm[kMaxGrid];
+  __shared__ double root_sh[kAlphaChannels];
   float mx = -INFINITY, mn = INFINITY;
   const float4* m4 = reinterpret_cast<const float4*>(mean_abs);
   const int K4 = K >> 2;  // K is a multiple of 128
 #pragma unroll 4
-  for (int j = threadIdx.x; j < K4; j += kAlphaThreads) {
+  for (int j = threadIdx.x; j < K4; j += 64) {
     const float4 v = m4[j];
     mx = fmax3f(mx, fmaxf(v.x, v.y), fmaxf(v.z, v.w));
     mn = fmin3f(mn, fminf(v.x, v.y), fminf(v.z, v.w));
@@ -151,37 +163,37 @@ __global__ void __launch_bounds__(kAlphaThreads) alpha_scales_kernel(const float
     smin[warp] = mn;
   }
   __syncthreads();
-  if ((int)threadIdx.x < G) {
-    const int i = threadIdx.x;
-    double c = 1.0;
-    if (normalize) {
-      float bmx = smax[0], bmn = smin[0];
-      for (int w = 1; w < kAlphaThreads / 32; ++w) {
-        bmx = fmaxf(bmx, smax[w]);
-        bmn = fminf(bmn, smin[w]);
+  const int j = blockIdx.x * kAlphaChannels + lane;
+  if (warp == 0) {
+    const double lo = fmax((double)fminf(smin[0], smin[1]), clamp_min);
+    const double hi = fmax((double)fmaxf(smax[0], smax[1]), clamp_min);
+    for (int i = lane; i < G; i += 32) {
+      double c = 1.0;
+      if (normalize) {
+        const double alpha = (double)i / (double)G;
+        c = sqrt(pow(hi, alpha) * pow(lo, alpha));
       }
-      const double alpha = (double)i / (double)G;
-      c = sqrt(pow(fmax((double)bmx, clamp_min), alpha) * pow(fmax((double)bmn, clamp_min), alpha));
+      inv_norm[i] = 1.0 / c;
     }
-    inv_norm[i] = 1.0 / c;
+  } else {
+    root_sh[lane] = j < K ? pow(fmax((double)mean_abs[j], clamp_min), 1.0 / (double)G) : 1.0;
   }
-  const int j = blockIdx.x * kAlphaThreads + threadIdx.x;
-  double root = 1.0;
-  if (j < K) root = pow(fmax((double)mean_abs[j], clamp_min), 1.0 / (double)G);
   __syncthreads();
   if (j >= K) return;
-  double p = 1.0;  // b^(i/G)
-  for (int i = 0; i < G; ++i) {
+  const double root = root_sh[lane];
+  const double step = root * root;
+  double p = warp == 0 ? 1.0 : root;  // b^(i/G) for i = warp, warp + 2, ...
+  for (int i = warp; i < G; i += 2) {
     const float s32 = (float)(p * inv_norm[i]);
     s_out[(size_t)i * K + j] = s32;
     inv_out[(size_t)i * K + j] = __fdiv_rn(1.0f, s32);
-    p *= root;
+    p *= step;
   }
 }
 
 cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_config& cfg, float* s,
                                 float* inv_s, cudaStream_t st) {
-  alpha_scales_kernel<<<(unsigned)((K + kAlphaThreads - 1) / kAlphaThreads), kAlphaThreads, 0, st>>>(
+  alpha_scales_kernel<<<(unsigned)((K + kAlphaChannels - 1) / kAlphaChannels), 64, 0, st>>>(
       mean_abs, (int)K, cfg.n_grid, (double)cfg.sx_clamp_min, cfg.normalize, s, inv_s);
   return cudaGetLastError();
 }

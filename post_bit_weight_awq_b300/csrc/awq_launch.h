@@ -56,4 +56,9 @@ cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, i
                                 float* partials, uint32_t* ready, uint32_t* status, cudaStream_t st,
                                 float* dump = nullptr);
 
+// y[m][r] = sum_k x[m][k] * (q[r][k] - z[r][g]) * scale[r][g] for m < M <= 8,
+// x bf16 [M][K] (staged as fp32 in shared memory: M * K * 4 bytes).
+cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int32_t* qweight, const uint16_t* scales,
+                              const uint16_t* zeros, int64_t N, float* y, cudaStream_t st);
+
 }  // namespace awq

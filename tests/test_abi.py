@@ -132,3 +132,18 @@ def test_host_validation_of_fused_search(lib):
     assert _status_of(f, A, B, C, C, cfg, D, D, 0, D, 0, **kw) == capi.AWQ_ERR_INVALID_ARG
     assert _status_of(f, A, B, C, C, cfg, D, D, D + 4, D, 0, **kw) == capi.AWQ_ERR_MISALIGNED
     assert _status_of(f, A, B, C, C, cfg, D, D, D, D, 0, **{**kw, "w_dtype": 9}) == capi.AWQ_ERR_INVALID_ARG
+
+
+def test_host_validation_of_w4a16(lib):
+    f = capi.awq_w4a16_gemv
+    A, B, C, D, E = 0x1000, 0x2000, 0x3000, 0x4000, 0x5000
+    kw = dict(n_tok=2, in_features=256, out_features=4, x_dtype=capi.AWQ_BF16)
+    cfg = capi.config()
+    assert _status_of(f, A, B, C, D, cfg, E, 0, **{**kw, "n_tok": 9}) == capi.AWQ_ERR_UNSUPPORTED
+    assert _status_of(f, A, B, C, D, cfg, E, 0, **{**kw, "n_tok": 8, "in_features": 8192}) == \
+        capi.AWQ_ERR_UNSUPPORTED
+    assert _status_of(f, A, B, C, D, cfg, 0, 0, **kw) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A, B + 4, C, D, cfg, E, 0, **kw) == capi.AWQ_ERR_MISALIGNED
+    assert _status_of(f, A, B, C + 1, D, cfg, E, 0, **kw) == capi.AWQ_ERR_MISALIGNED
+    assert _status_of(f, A, B, C, D, cfg, E, 0, **{**kw, "in_features": 200}) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A, B, C, D, capi.config(group=64), E, 0, **kw) == capi.AWQ_ERR_UNSUPPORTED

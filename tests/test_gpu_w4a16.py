@@ -1,0 +1,84 @@
+"""The packed layer applied to a few tokens (awq_w4a16_gemv) against the CPU
+oracle: element by element, within the bound of its fp32 arithmetic, on
+ragged and full-size shapes, and end to end from a layer packed on the GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads
+from gpu_util import dev_bf16, dev_f32, dev_weight
+from post_bit_weight_awq_b300 import build, capi
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    build.build()
+    capi.lib()
+
+
+def _bound(x, W_hat):
+    # exact products (bf16 x times small integers), fp32 pair sums over 16
+    # terms, one pair add, one fused scale per 32 columns, at most K/1024
+    # chunk sums per lane and a 5-level lane tree: under 64 roundings of 2^-24
+    # of sum |x| |w|
+    return 64 * 2.0**-24 * (np.abs(x) @ np.abs(W_hat).T) + 1e-30
+
+
+def _random_packed(rng, N, K):
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float64)
+    s = O.f32(rng.uniform(0.5, 2.0, K))
+    return O.quantize_pack(W, s)
+
+
+def _run(x32, pk):
+    M, K = x32.shape
+    N = pk["qweight"].shape[0]
+    y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    capi.awq_w4a16_gemv(dev_bf16(x32), torch.from_numpy(pk["qweight"]).cuda(),
+                        torch.from_numpy(pk["scales"].view(np.int16)).cuda(),
+                        torch.from_numpy(pk["zeros"].view(np.int16)).cuda(), capi.config(), y)
+    torch.cuda.synchronize()
+    return y.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 7, 128), (3, 300, 1024), (8, 130, 4096), (4, 1000, 11008), (2, 4096, 4096),
+                                   (1, 4096, 4096), (6, 520, 8192), (5, 2, 640)])
+def test_w4a16_matches_oracle(M, N, K):
+    rng = np.random.default_rng(M * 1000 + N + K)
+    pk = _random_packed(rng, N, K)
+    x = workloads.round_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32)).astype(np.float64)
+    got = _run(x.astype(np.float32), pk)
+    ref = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"])
+    W_hat = O.dequantize_groups(O.unpack_words(pk["qweight"], K), pk["scales"].astype(np.float64),
+                                pk["zeros"].astype(np.float64))
+    bad = np.abs(got - ref) > _bound(x, W_hat)
+    assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got - ref).max():.3e}"
+
+
+def test_layer_packed_on_gpu_reproduces_the_searched_weight():
+    """Search-side weight and inference-side packed layer agree: the GPU pack
+    of W * diag(s) applied to x / s equals x W_hat^T of the fake-quant, up to
+    the fp16 storage of each group's step (2^-11) and the fp32 sums."""
+    L = workloads.make_layer("llama7b_q_proj", n_tok=64, out_features=384, in_features=2048)
+    W, X = L["W"].astype(np.float64), L["X"]
+    N, K = W.shape
+    s32 = O.f32(O.awq_scales(O.channel_importance(X), 0.4))
+    qw = torch.empty(N, K // 8, dtype=torch.int32, device="cuda")
+    sc = torch.empty(N, K // 128, dtype=torch.float16, device="cuda")
+    zr = torch.empty(N, K // 128, dtype=torch.float16, device="cuda")
+    capi.awq_quantize_pack(dev_weight(L), dev_f32(s32), capi.config(), qw, sc, zr)
+    x = workloads.round_to_bf16((X[:4] / s32[None, :]).astype(np.float32)).astype(np.float64)
+    y = torch.empty(4, N, dtype=torch.float32, device="cuda")
+    capi.awq_w4a16_gemv(dev_bf16(x.astype(np.float32)), qw, sc, zr, capi.config(), y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    W_hat = O.fake_quantize(W, s32)
+    ref = x @ (W_hat * s32[None, :]).T  # x already carries 1/s
+    bound = 2.0**-11 * (np.abs(x) @ np.abs(W_hat * s32[None, :]).T) + _bound(x, W_hat * s32[None, :])
+    assert np.all(np.abs(got - ref) <= bound)

@@ -326,3 +326,43 @@ def test_generator_is_deterministic():
     assert len(a["outlier_channels"]) == 3
     # bf16-exact activations
     workloads.bf16_bits(a["X"])
+
+
+# ---------------------------------------------------------------- packed-layer product (w4a16)
+
+
+def test_w4a16_linear_brute_force_from_words():
+    # codes read straight from the words with integer shifts, sums by loops
+    rng = np.random.default_rng(11)
+    M, N, K = 2, 3, 256
+    words = rng.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    sc = rng.uniform(0.001, 0.02, size=(N, K // 128)).astype(np.float16)
+    zr = rng.integers(0, 16, size=(N, K // 128)).astype(np.float16)
+    x = rng.standard_normal((M, K))
+    got = O.w4a16_linear(x, words, sc, zr)
+    for m in range(M):
+        for r in range(N):
+            acc = 0.0
+            for k in range(K):
+                word = int(words[r, k // 8]) & 0xFFFFFFFF
+                q = (word >> (4 * (k % 8))) & 0xF
+                acc += x[m, k] * (q - float(zr[r, k // 128])) * float(sc[r, k // 128])
+            assert got[m, r] == pytest.approx(acc, rel=1e-12, abs=1e-12)
+
+
+def test_w4a16_linear_matches_the_searched_weight():
+    # the packed layer applied to x / s reproduces x @ W_hat^T of the search's
+    # fake-quant (scaling equation), up to the fp16 storage of each step:
+    # |fp16(delta) - delta| <= 2^-11 delta, so every product term moves by at
+    # most 2^-11 of its size
+    W, X = _small_layer(out=16, K=512, n=8)
+    sx = O.channel_importance(X)
+    s = O.f32(O.awq_scales(sx, 0.55))
+    pk = O.quantize_pack(W, s)
+    got = O.w4a16_linear(X / s[None, :], pk["qweight"], pk["scales"], pk["zeros"])
+    W_hat = O.fake_quantize(W, s)
+    ref = X @ W_hat.T
+    bound = 2.0**-11 * (np.abs(X) @ np.abs(W_hat).T) + 1e-12
+    assert np.all(np.abs(got - ref) <= bound)
+    # and it is not trivially close: the quantisation error itself is much larger
+    assert np.max(np.abs(X @ W.T - ref)) > 50 * np.max(np.abs(got - ref))
