@@ -188,6 +188,33 @@ AWQ_API awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out,
                             const awq_config* cfg, float* losses, int32_t* best_idx,
                             float* s_best, void* ws, size_t ws_bytes, awq_stream_t stream);
 
+/* Several linears that read the same input X (the q/k/v projections behind
+   one RMSNorm, or gate/up behind another) must share one s, because 1/s is
+   folded into that one producer of X ("AWQ > Salient Weight Preservation":
+   the inverse scale is absorbed into the preceding LayerNorm/RMSNorm). The
+   block search scores each alpha by the output MSE of all the linears
+   together, i.e. the search of the layer whose weight is their rows one
+   after another: L_i = sum_j sum (X W_hat_ij^T - X W_j^T)^2 / (n_tok *
+   sum_j out_j). At most AWQ_BLOCK_MAX_LINEARS linears. */
+#define AWQ_BLOCK_MAX_LINEARS 16
+
+/* Device bytes of scratch awq_search_block needs: awq_workspace_size for
+   sum_j outs[j] rows plus room for those rows of W. Host-only; outs is a
+   host array of `count` output sizes. */
+AWQ_API awq_status awq_search_block_workspace_size(int64_t n_tok, const int64_t* outs, int32_t count, int64_t in,
+                                                   int32_t w_dtype, const awq_config* cfg, size_t* bytes);
+
+/* awq_search_layer over a block of linears sharing X. W_list: HOST array of
+   `count` device pointers, W_list[j] of [outs[j]][in] (same dtype, 16-byte
+   aligned); outs: HOST array. The rows are copied one after another into the
+   workspace (device-to-device copies on `stream`), then searched as one
+   layer. Outputs as awq_search_layer; pack each linear afterwards with
+   awq_quantize_pack and the same s_best. */
+AWQ_API awq_status awq_search_block(const void* const* W_list, int32_t w_dtype, const int64_t* outs, int32_t count,
+                                    int64_t in, const void* X, int32_t x_dtype, int64_t n_tok,
+                                    const float* mean_abs, const awq_config* cfg, float* losses, int32_t* best_idx,
+                                    float* s_best, void* ws, size_t ws_bytes, awq_stream_t stream);
+
 /* ---------------------------------------------------------------- step 3 */
 
 /* Final INT4 codes of W * diag(s) with the quantiser above, bit-exact with
@@ -206,9 +233,10 @@ AWQ_API awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out
 /* ---------------------------------------------------------------- using the packed layer */
 
 /* Largest token count, and token count times `in`, that awq_w4a16_gemv
-   accepts (the tokens' activations are staged in shared memory as fp32). */
+   accepts (the tokens' activations are staged in shared memory as fp32,
+   4.5 bytes per value with the bank padding). */
 #define AWQ_W4A16_MAX_TOKENS 8
-#define AWQ_W4A16_MAX_TOKEN_CHANNELS (50 * 1024)
+#define AWQ_W4A16_MAX_TOKEN_CHANNELS (44 * 1024)
 
 /* The packed layer applied to a few tokens (w4a16, the decode case):
    y[t][r] = sum_k x[t][k] * (q[r][k] - z[r][g]) * scale[r][g], g = k / group,

@@ -71,6 +71,7 @@ __all__ = [
     "output_mse",
     "output_sq_err_sum",
     "search_scale",
+    "search_scale_block",
     "pack_words",
     "unpack_words",
     "quantize_pack",
@@ -252,6 +253,17 @@ def search_scale(
         "s_best": scales[best_i],
         "scales": np.stack(scales),
     }
+
+
+def search_scale_block(W_list, X, sx, **kw) -> Dict[str, object]:
+    """One scale for several linears that read the same X.
+
+    [AWQ-SWP: the inverse scale is folded into the preceding LayerNorm /
+    RMSNorm, so all linears fed by that norm (q/k/v, or gate/up) must share
+    s.] The search scores each alpha by the output MSE of all of them
+    together: the search of the layer whose weight is their rows stacked.
+    """
+    return search_scale(np.concatenate([np.asarray(W, dtype=np.float64) for W in W_list], axis=0), X, sx, **kw)
 
 
 def pack_words(q) -> np.ndarray:

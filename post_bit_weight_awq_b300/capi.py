@@ -37,6 +37,8 @@ EXPORTED = (
     "awq_act_stats_noalloc",
     "awq_workspace_size",
     "awq_search_layer",
+    "awq_search_block_workspace_size",
+    "awq_search_block",
     "awq_quantize_pack",
     "awq_w4a16_gemv",
     "awq_packed_bytes",
@@ -97,6 +99,9 @@ def lib() -> ctypes.CDLL:
         "awq_act_stats_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P]),
         "awq_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _CFG, ctypes.POINTER(_SZ)]),
         "awq_search_layer": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _I64, _P, _CFG, _P, _P, _P, _P, _SZ, _P]),
+        "awq_search_block_workspace_size": (ctypes.c_int, [_I64, _P, _I32, _I64, _I32, _CFG, ctypes.POINTER(_SZ)]),
+        "awq_search_block": (ctypes.c_int, [_P, _I32, _P, _I32, _I64, _P, _I32, _I64, _P, _CFG, _P, _P, _P, _P, _SZ,
+                                            _P]),
         "awq_quantize_pack": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _CFG, _P, _P, _P, _P]),
         "awq_w4a16_gemv": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _I64, _CFG, _P, _P]),
         "awq_packed_bytes": (_SZ, [_I64, _I64, _CFG]),
@@ -237,6 +242,30 @@ def awq_search_layer(W, X, mean_abs, cfg: AwqConfig, losses, best_idx, s_best, w
     _check(lib().awq_search_layer(_ptr(W), wd, N, K, _ptr(X), xd, n, _ptr(mean_abs), ctypes.byref(cfg),
                                   _ptr(losses), _ptr(best_idx), _ptr(s_best), _ptr(ws), wb, _stream(stream)),
            "awq_search_layer")
+
+
+def awq_search_block_workspace_size(n_tok: int, outs, in_features: int, cfg: AwqConfig, w_dtype: int = AWQ_BF16) -> int:
+    arr = (ctypes.c_int64 * len(outs))(*outs)
+    b = _SZ(0)
+    _check(lib().awq_search_block_workspace_size(n_tok, ctypes.cast(arr, _P), len(outs), in_features, w_dtype,
+                                                 ctypes.byref(cfg), ctypes.byref(b)), "awq_search_block_workspace_size")
+    return b.value
+
+
+def awq_search_block(Ws, X, mean_abs, cfg: AwqConfig, losses, best_idx, s_best, ws, stream=None, *, outs=None,
+                     in_features=None, n_tok=None, w_dtype=None, x_dtype=None, ws_bytes=None) -> None:
+    """Ws: sequence of device weight tensors [out_j, in] (or raw pointers with ``outs``)."""
+    outs = [W.shape[0] for W in Ws] if outs is None else list(outs)
+    K = Ws[0].shape[1] if in_features is None else in_features
+    n = X.shape[0] if n_tok is None else n_tok
+    wd = _dtype_code(Ws[0]) if w_dtype is None else w_dtype
+    xd = _dtype_code(X) if x_dtype is None else x_dtype
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    ptrs = (ctypes.c_void_p * len(Ws))(*[_ptr(W) for W in Ws])
+    arr = (ctypes.c_int64 * len(outs))(*outs)
+    _check(lib().awq_search_block(ctypes.cast(ptrs, _P), wd, ctypes.cast(arr, _P), len(outs), K, _ptr(X), xd, n,
+                                  _ptr(mean_abs), ctypes.byref(cfg), _ptr(losses), _ptr(best_idx), _ptr(s_best),
+                                  _ptr(ws), wb, _stream(stream)), "awq_search_block")
 
 
 def awq_quantize_pack(W, s, cfg: AwqConfig, qweight, scales, zeros, stream=None, *, out_features=None,

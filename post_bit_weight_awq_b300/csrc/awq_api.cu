@@ -78,6 +78,10 @@ SearchLayout search_layout(int64_t n_tok, int64_t out, int64_t in, const awq_con
   return L;
 }
 
+awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X, int64_t n_tok,
+                      const float* mean_abs, const awq_config& c, float* losses, int32_t* best_idx, float* s_best,
+                      uint8_t* base, const SearchLayout& L, cudaStream_t s);
+
 }  // namespace
 
 extern "C" {
@@ -277,8 +281,72 @@ awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t
   const SearchLayout L = search_layout(n_tok, out, in, *cfg);
   if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
 
-  cudaStream_t s = (cudaStream_t)stream;
+  return run_search(W, w_dtype, out, in, X, n_tok, mean_abs, *cfg, losses, best_idx, s_best, (uint8_t*)ws, L,
+                    (cudaStream_t)stream);
+}
+
+awq_status awq_search_block_workspace_size(int64_t n_tok, const int64_t* outs, int32_t count, int64_t in,
+                                           int32_t w_dtype, const awq_config* cfg, size_t* bytes) {
+  if (bytes == nullptr || outs == nullptr || count < 1 || count > AWQ_BLOCK_MAX_LINEARS) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_wdtype(w_dtype);
+  if (st != AWQ_OK) return st;
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    if (outs[i] < 1) return AWQ_ERR_INVALID_ARG;
+    total += outs[i];
+  }
+  st = check_dims(n_tok, total, in);
+  if (st != AWQ_OK) return st;
+  const size_t wbytes = w_dtype == AWQ_BF16 ? 2 : 4;
+  *bytes = search_layout(n_tok, total, in, *cfg).total + align_up((size_t)total * in * wbytes, kAlign);
+  return AWQ_OK;
+}
+
+awq_status awq_search_block(const void* const* W_list, int32_t w_dtype, const int64_t* outs, int32_t count,
+                            int64_t in, const void* X, int32_t x_dtype, int64_t n_tok, const float* mean_abs,
+                            const awq_config* cfg, float* losses, int32_t* best_idx, float* s_best, void* ws,
+                            size_t ws_bytes, awq_stream_t stream) {
+  if (W_list == nullptr || X == nullptr || mean_abs == nullptr || losses == nullptr || best_idx == nullptr ||
+      s_best == nullptr || ws == nullptr)
+    return AWQ_ERR_INVALID_ARG;
+  size_t need = 0;
+  awq_status st = awq_search_block_workspace_size(n_tok, outs, count, in, w_dtype, cfg, &need);
+  if (st != AWQ_OK) return st;
+  st = check_xdtype(x_dtype);
+  if (st != AWQ_OK) return st;
+  for (int i = 0; i < count; ++i) {
+    if (W_list[i] == nullptr) return AWQ_ERR_INVALID_ARG;
+    if (!aligned16(W_list[i])) return AWQ_ERR_MISALIGNED;
+  }
+  if (!aligned16(X) || !aligned16(mean_abs) || !aligned16(s_best) || !aligned16(ws)) return AWQ_ERR_MISALIGNED;
+  if (ws_bytes < need) return AWQ_ERR_WORKSPACE;
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) total += outs[i];
+  const SearchLayout L = search_layout(n_tok, total, in, *cfg);
+  // the linears' rows, one after another, behind the search's own scratch
   uint8_t* base = (uint8_t*)ws;
+  uint8_t* wcat = base + L.total;
+  const size_t wbytes = w_dtype == AWQ_BF16 ? 2 : 4;
+  cudaStream_t s = (cudaStream_t)stream;
+  size_t off = 0;
+  for (int i = 0; i < count; ++i) {
+    const size_t b = (size_t)outs[i] * in * wbytes;
+    if (cudaMemcpyAsync(wcat + off, W_list[i], b, cudaMemcpyDeviceToDevice, s) != cudaSuccess) return AWQ_ERR_CUDA;
+    off += b;
+  }
+  return run_search(wcat, w_dtype, total, in, X, n_tok, mean_abs, *cfg, losses, best_idx, s_best, base, L, s);
+}
+
+}  // extern "C"
+
+namespace {
+
+awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X, int64_t n_tok,
+                      const float* mean_abs, const awq_config& c, float* losses, int32_t* best_idx, float* s_best,
+                      uint8_t* base, const SearchLayout& L, cudaStream_t s) {
+  const awq_config* cfg = &c;
   uint32_t* status = (uint32_t*)(base + L.status);
   float* sc = (float*)(base + L.s);
   float* inv = (float*)(base + L.inv_s);
@@ -303,6 +371,10 @@ awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t
                            status, s);
   return from_cuda(e);
 }
+
+}  // namespace
+
+extern "C" {
 
 awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out, int64_t in, const float* s,
                              const awq_config* cfg, int32_t* qweight, uint16_t* scales_f16, uint16_t* zeros_f16,

@@ -419,12 +419,10 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
 template <typename WT, bool REF>
 cudaError_t launch_fakequant_t(const WT* W, int64_t N, int64_t K, const float* s, const float* inv_s,
                                const awq_config& cfg, uint16_t* op, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(fakequant_kernel<WT, REF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kFqSmem);
+  cudaError_t e = ensure_dynamic_smem((const void*)fakequant_kernel<WT, REF>, kFqSmem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   const int nstrips = (int)((K + kFqCols - 1) / kFqCols);
   // one wave: at most kFqBlocksPerSm blocks per SM in total
@@ -535,9 +533,8 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT>())
 template <typename WT>
 cudaError_t launch_pack_t(const WT* W, int64_t N, int64_t K, const float* s, const awq_config& cfg,
                           int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   const int nstrips = (int)((K + kFqCols - 1) / kFqCols);
   int64_t rblocks = (int64_t)sms * pack_blocks_per_sm<WT>() / nstrips;

@@ -18,6 +18,12 @@ constexpr int kTileM = 128;  // tokens per tile (tensor-memory lanes)
 constexpr int kTileN = 256;  // output rows per tile (tensor-memory columns)
 constexpr int kTileK = 64;   // input channels per pipeline stage (128 B of bf16)
 
+// SM count of the current device, queried once per device.
+cudaError_t sm_count(int* sms);
+// Allow `bytes` of dynamic shared memory for kernel `func` on the current
+// device (the attribute is set once per kernel, device and size increase).
+cudaError_t ensure_dynamic_smem(const void* func, int bytes);
+
 inline int stats_chunks(int64_t n_tok) { return (int)((n_tok + kStatsRows - 1) / kStatsRows); }
 inline int stats_strips(int64_t in) { return (int)((in + 255) / 256); }
 

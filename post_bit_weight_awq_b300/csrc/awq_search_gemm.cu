@@ -735,8 +735,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 template <int CM>
 cudaError_t launch_residual(const CUtensorMap& tmX, const CUtensorMap& tmB, Params p, int sms, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(search_gemm_kernel<false, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
+  cudaError_t e = ensure_dynamic_smem((const void*)search_gemm_kernel<false, CM>, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[1];
@@ -765,8 +764,7 @@ cudaError_t launch_residual(const CUtensorMap& tmX, const CUtensorMap& tmB, Para
 template <bool FUSED>
 cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmB, const Params& p, int sms, cudaStream_t st) {
   constexpr int threads = FUSED ? kFusedThreads : NUM_THREADS;
-  cudaError_t e = cudaFuncSetAttribute(search_gemm_pair_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PAIR_SMEM_BYTES);
+  cudaError_t e = ensure_dynamic_smem((const void*)search_gemm_pair_kernel<FUSED>, PAIR_SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[1];
@@ -805,10 +803,7 @@ cudaError_t setup_search(const uint16_t* X, int64_t n_tok, int64_t K, const uint
   const cuuint32_t bb[3] = {(cuuint32_t)BK, (cuuint32_t)(BN / CM), 1u};
   if (!make_map(tmX, X, 2, xd, xb) || !make_map(tmB, op, 3, bd, bb)) return cudaErrorInvalidValue;
 
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = sm_count(sms);
   if (e != cudaSuccess) return e;
 
   Params p = {};
@@ -856,8 +851,7 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
   p.withhold_first_fill = withhold_first_fill;
 
   if (ref) {
-    e = cudaFuncSetAttribute(search_gemm_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
+    e = ensure_dynamic_smem((const void*)search_gemm_kernel<true, 1>, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int grid = p.items < sms ? p.items : sms;
     search_gemm_kernel<true, 1><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);

@@ -5,10 +5,11 @@
 // reads the 4-bit codes, a quarter of the bytes of fp16 weights).
 //
 // The packed layer is streamed from HBM once; x (at most 8 tokens) is
-// converted to fp32 and staged in shared memory. One CTA of 16 or 32 warps
-// per SM; each warp owns one output row at a time and each lane 32
-// consecutive codes (one 16-byte load, inside one group of 128) per step,
-// four steps' loads issued before any is used. Codes become floats without conversion
+// converted to fp32 and staged in shared memory. One CTA of 16 warps per SM;
+// each warp owns R output rows at a time (R = 4 for one token, fewer for
+// more) and each lane one chunk of 32 consecutive codes of each (16-byte
+// loads, inside one group of 128) per step, with the next step's loads in
+// flight while the current one is computed. Codes become floats without conversion
 // instructions: a byte permute places a nibble under the exponent bits of
 // 2^23 (0x4B00_00qq = 2^23 + q exactly), and one packed subtraction of
 // 2^23 + z gives (q - z, q' - z) for two neighbouring columns, exactly. The
@@ -23,11 +24,9 @@
 namespace awq {
 namespace {
 
-// threads per CTA: more warps (more loads in flight) while the registers of
-// the M token accumulators still fit without spilling
-template <int M>
-__host__ __device__ constexpr int w4_threads() { return M <= 2 ? 1024 : 512; }
-constexpr int kW4Unroll = 4;  // 16-byte code loads in flight per lane
+constexpr int kW4Threads = 512;
+constexpr int kW4Warps = kW4Threads / 32;
+constexpr int kW4Pad = 36;    // shared-memory floats per 32 channels of x
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 r;
@@ -42,102 +41,162 @@ __device__ __forceinline__ float nib_f(uint32_t v, int b) {
   return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440u + (uint32_t)b));
 }
 
+// Rows a warp works on together (R): the lane's 32 values of x per token are
+// read from shared memory once per chunk and used for all of them, which
+// divides the shared-memory traffic (4 bytes of x per 4-bit code) by R. The
+// launcher takes the largest R the registers allow (4 for one token, 2 for
+// two, else 1) that still gives every SM at least one CTA.
 template <int M>
-__global__ void __launch_bounds__(w4_threads<M>(), 1)
+__host__ __device__ constexpr int w4_max_rows() { return M == 1 ? 4 : (M == 2 ? 2 : 1); }
+
+// The loads of one step of a warp: chunk cbase + lane (32 codes) of R rows,
+// with each chunk's group step and zero.
+template <int R>
+struct W4Step {
+  uint4 q[R];
+  uint16_t s[R], z[R];
+};
+
+template <int R>
+__device__ __forceinline__ void w4_load(W4Step<R>& st, const int32_t* __restrict__ qweight,
+                                        const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros,
+                                        int r0, int N, int c, int chunks, int kw, int kg) {
+  if (c >= chunks) return;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int r = r0 + i;
+    if (r < N) {
+      st.q[i] = ld_stream_v4(qweight + (size_t)r * kw + 4 * c);
+      st.s[i] = scales[(size_t)r * kg + (c >> 2)];
+      st.z[i] = zeros[(size_t)r * kg + (c >> 2)];
+    }
+  }
+}
+
+template <int M, int R>
+__global__ void __launch_bounds__(kW4Threads, 1)
     w4a16_gemv_kernel(const uint16_t* __restrict__ x, int K, const int32_t* __restrict__ qweight,
                       const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros, int N,
                       float* __restrict__ y) {
   extern __shared__ float4 w4_smem[];
-  float* xs = reinterpret_cast<float*>(w4_smem);  // [M][K] fp32
-  constexpr int kThreads = w4_threads<M>(), kWarps = kThreads / 32;
-  for (int i = threadIdx.x; i < M * K / 8; i += kThreads) {
-    const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * 8);
-    float4 a, b;
-    a.x = bf16_lo(v.x);
-    a.y = bf16_hi(v.x);
-    a.z = bf16_lo(v.y);
-    a.w = bf16_hi(v.y);
-    b.x = bf16_lo(v.z);
-    b.y = bf16_hi(v.z);
-    b.z = bf16_lo(v.w);
-    b.w = bf16_hi(v.w);
-    w4_smem[2 * i] = a;
-    w4_smem[2 * i + 1] = b;
-  }
-  __syncthreads();
-
+  // x as fp32, each run of 32 channels followed by 4 floats of padding: lane
+  // l reads the run of chunk 32u + l, and the padding puts the 32 lanes'
+  // 16-byte reads at the same offset into 8 distinct bank groups
+  float* xs = reinterpret_cast<float*>(w4_smem);  // [M][K / 32][36]
+  const int kp = (K >> 5) * kW4Pad;                // padded floats per token
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunks = K >> 5;  // 32-code chunks per row
   const int kw = K >> 3, kg = K >> 7;
-  for (int r = blockIdx.x * kWarps + warp; r < N; r += gridDim.x * kWarps) {
-    const int32_t* qrow = qweight + (size_t)r * kw;
-    float acc[M];
+  const int steps_per_group = (chunks + 31) / 32;
+  const int gstride = gridDim.x * kW4Warps * R;
+
+  // The warp's steps run through (group of R rows, chunk step); the loads of
+  // the next step are issued before the current one is computed. The first
+  // step's loads go out before x is staged, so their latency overlaps it.
+  int r0 = (blockIdx.x * kW4Warps + warp) * R, k = 0;
+  W4Step<R> cur, nxt;
+  if (r0 < N) w4_load<R>(cur, qweight, scales, zeros, r0, N, lane, chunks, kw, kg);
+
+  for (int i = threadIdx.x; i < M * K / 8; i += kW4Threads) {
+    const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * 8);
+    const int m = (i * 8) / K, kk = i * 8 - m * K;
+    float* d = xs + (size_t)m * kp + (kk >> 5) * kW4Pad + (kk & 31);
+    reinterpret_cast<float4*>(d)[0] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+    reinterpret_cast<float4*>(d)[1] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+  }
+  __syncthreads();
+
+  float acc[R][M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) acc[m] = 0.0f;
-    for (int c0 = lane; c0 < chunks; c0 += 32 * kW4Unroll) {
-      uint4 q[kW4Unroll];
+  for (int i = 0; i < R; ++i)
 #pragma unroll
-      for (int u = 0; u < kW4Unroll; ++u)
-        if (c0 + 32 * u < chunks) q[u] = ld_stream_v4(qrow + 4 * (c0 + 32 * u));
+    for (int m = 0; m < M; ++m) acc[i][m] = 0.0f;
+  while (r0 < N) {
+    int nr = r0, nk = k + 1;
+    if (nk == steps_per_group) {
+      nr = r0 + gstride;
+      nk = 0;
+    }
+    if (nr < N) w4_load<R>(nxt, qweight, scales, zeros, nr, N, nk * 32 + lane, chunks, kw, kg);
+    const int c = k * 32 + lane;
+    if (c < chunks) {
+      // the lane's 32 x values per token, as pairs
+      float2 xv[M][16];
 #pragma unroll
-      for (int u = 0; u < kW4Unroll; ++u) {
-        const int c = c0 + 32 * u;
-        if (c >= chunks) break;
-        const int k0 = c << 5;
-        const int g = k0 >> 7;
-        const float sc = __half2float(__ushort_as_half(scales[(size_t)r * kg + g]));
-        const float zoff = 8388608.0f + __half2float(__ushort_as_half(zeros[(size_t)r * kg + g]));
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float4 f = *reinterpret_cast<const float4*>(xs + (size_t)m * kp + c * kW4Pad + 4 * t);
+          xv[m][2 * t] = make_float2(f.x, f.y);
+          xv[m][2 * t + 1] = make_float2(f.z, f.w);
+        }
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        if (r0 + i >= N) break;
+        const float sc = __half2float(__ushort_as_half(cur.s[i]));
+        const float zoff = 8388608.0f + __half2float(__ushort_as_half(cur.z[i]));
         const float2 nz = make_float2(-zoff, -zoff);
         float2 part[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) part[m] = make_float2(0.0f, 0.0f);
-        const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+        const uint32_t wd[4] = {cur.q[i].x, cur.q[i].y, cur.q[i].z, cur.q[i].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t lo = wd[j] & 0x0F0F0F0Fu;         // nibbles 0, 2, 4, 6: even columns
           const uint32_t hi = (wd[j] >> 4) & 0x0F0F0F0Fu;  // nibbles 1, 3, 5, 7: odd columns
 #pragma unroll
-          for (int b = 0; b < 4; b += 2) {
-            // columns k0 + 8j + 2b .. + 3
-            const float2 w01 = __fadd2_rn(make_float2(nib_f(lo, b), nib_f(hi, b)), nz);
-            const float2 w23 = __fadd2_rn(make_float2(nib_f(lo, b + 1), nib_f(hi, b + 1)), nz);
+          for (int b = 0; b < 4; ++b) {
+            // columns 32c + 8j + 2b, + 1
+            const float2 w = __fadd2_rn(make_float2(nib_f(lo, b), nib_f(hi, b)), nz);
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-              const float4 xv = *reinterpret_cast<const float4*>(xs + (size_t)m * K + k0 + 8 * j + 2 * b);
-              part[m] = __ffma2_rn(w01, make_float2(xv.x, xv.y), part[m]);
-              part[m] = __ffma2_rn(w23, make_float2(xv.z, xv.w), part[m]);
-            }
+            for (int m = 0; m < M; ++m) part[m] = __ffma2_rn(w, xv[m][4 * j + b], part[m]);
           }
         }
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[m] = fmaf(sc, part[m].x + part[m].y, acc[m]);
+        for (int m = 0; m < M; ++m) acc[i][m] = fmaf(sc, part[m].x + part[m].y, acc[i][m]);
       }
     }
+    if (nk == 0) {  // rows r0 .. r0 + R - 1 are complete
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-      float v = acc[m];
+      for (int i = 0; i < R; ++i)
 #pragma unroll
-      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == m) y[(size_t)m * N + r] = v;
+        for (int m = 0; m < M; ++m) {
+          float v = acc[i][m];
+#pragma unroll
+          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == m && r0 + i < N) y[(size_t)m * N + r0 + i] = v;
+          acc[i][m] = 0.0f;
+        }
     }
+    cur = nxt;
+    r0 = nr;
+    k = nk;
   }
+}
+
+template <int M, int R>
+cudaError_t launch_w4_r(const uint16_t* x, int64_t K, const int32_t* qweight, const uint16_t* scales,
+                        const uint16_t* zeros, int64_t N, float* y, int sms, cudaStream_t st) {
+  const int smem = (int)(M * (K / 32) * kW4Pad * 4);
+  cudaError_t e = ensure_dynamic_smem((const void*)w4a16_gemv_kernel<M, R>, smem);
+  if (e != cudaSuccess) return e;
+  int64_t grid = (N + kW4Warps * R - 1) / (kW4Warps * R);
+  if (grid > sms) grid = sms;
+  w4a16_gemv_kernel<M, R><<<(unsigned)grid, kW4Threads, smem, st>>>(x, (int)K, qweight, scales, zeros, (int)N, y);
+  return cudaGetLastError();
 }
 
 template <int M>
 cudaError_t launch_w4_t(const uint16_t* x, int64_t K, const int32_t* qweight, const uint16_t* scales,
                         const uint16_t* zeros, int64_t N, float* y, cudaStream_t st) {
-  const int smem = (int)(M * K * 4);
-  cudaError_t e = cudaFuncSetAttribute(w4a16_gemv_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  constexpr int kThreads = w4_threads<M>();
-  int64_t grid = (N + kThreads / 32 - 1) / (kThreads / 32);
-  if (grid > sms) grid = sms;
-  w4a16_gemv_kernel<M><<<(unsigned)grid, kThreads, smem, st>>>(x, (int)K, qweight, scales, zeros, (int)N, y);
-  return cudaGetLastError();
+  int R = w4_max_rows<M>();
+  while (R > 1 && N < (int64_t)sms * kW4Warps * R) R >>= 1;
+  if (R == 4) return launch_w4_r<M, (w4_max_rows<M>() >= 4 ? 4 : 1)>(x, K, qweight, scales, zeros, N, y, sms, st);
+  if (R == 2) return launch_w4_r<M, (w4_max_rows<M>() >= 2 ? 2 : 1)>(x, K, qweight, scales, zeros, N, y, sms, st);
+  return launch_w4_r<M, 1>(x, K, qweight, scales, zeros, N, y, sms, st);
 }
 
 }  // namespace

@@ -147,3 +147,24 @@ def test_host_validation_of_w4a16(lib):
     assert _status_of(f, A, B, C + 1, D, cfg, E, 0, **kw) == capi.AWQ_ERR_MISALIGNED
     assert _status_of(f, A, B, C, D, cfg, E, 0, **{**kw, "in_features": 200}) == capi.AWQ_ERR_INVALID_ARG
     assert _status_of(f, A, B, C, D, capi.config(group=64), E, 0, **kw) == capi.AWQ_ERR_UNSUPPORTED
+
+
+def test_host_validation_of_block_search(lib):
+    cfg = capi.config()
+    with pytest.raises(capi.AwqError) as e:
+        capi.awq_search_block_workspace_size(128, [], 256, cfg)
+    assert e.value.status == capi.AWQ_ERR_INVALID_ARG
+    with pytest.raises(capi.AwqError) as e:
+        capi.awq_search_block_workspace_size(128, [8] * 17, 256, cfg)
+    assert e.value.status == capi.AWQ_ERR_INVALID_ARG
+    one = capi.awq_search_block_workspace_size(128, [512], 256, cfg)
+    three = capi.awq_search_block_workspace_size(128, [256, 128, 128], 256, cfg)
+    assert three == one == capi.awq_workspace_size(128, 512, 256, cfg) + 512 * 256 * 2
+    f = capi.awq_search_block
+    A, B, C, D = 0x1000, 0x2000, 0x3000, 0x4000
+    kw = dict(outs=[64, 64], in_features=256, n_tok=128, w_dtype=capi.AWQ_BF16, x_dtype=capi.AWQ_BF16,
+              ws_bytes=1 << 30)
+    assert _status_of(f, [A, 0], B, C, cfg, D, D, D, D, 0, **kw) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, [A, A + 8], B, C, cfg, D, D, D, D, 0, **kw) == capi.AWQ_ERR_MISALIGNED
+    assert _status_of(f, [A, A], B, C, cfg, D, D, D, D, 0, **{**kw, "ws_bytes": 1024}) == capi.AWQ_ERR_WORKSPACE
+    assert _status_of(f, [A, A], B, C, cfg, D, D, D, D, 0, **{**kw, "outs": [64, 0]}) == capi.AWQ_ERR_INVALID_ARG

@@ -259,3 +259,29 @@ def test_full_size_layer(name):
     s_best = O.f32(O.awq_scales(sx, O.alpha_grid(G)[g["best_idx"]]))
     rows = np.unique(np.concatenate([np.arange(4), np.arange(N - 4, N), rng.integers(0, N, 120)]))
     _check_pack(L, s_best, rows)
+
+
+def test_block_search_shared_input():
+    """Linears behind one norm (GQA-like q/k/v: 512, 128, 128 outputs) share
+    one scale; the block search matches the oracle's block search at levels
+    2 and 3, and each linear packs bit-exactly with the oracle's s_best."""
+    rng = np.random.default_rng(9)
+    K, n = 1024, 256
+    base = workloads.make_layer("llama7b_q_proj", n_tok=n, out_features=768, in_features=K, seed=5)
+    X = base["X"]
+    Ws32 = [workloads.round_to_bf16(base["W"][a:b]) for a, b in ((0, 512), (512, 640), (640, 768))]
+    sx32 = O.f32(O.channel_importance(X))
+    res = O.search_scale_block([W.astype(np.float64) for W in Ws32], X.astype(np.float64), sx32)
+    cfg = capi.config()
+    Wd = [dev_bf16(W) for W in Ws32]
+    outs = [W.shape[0] for W in Ws32]
+    ws = torch.empty(capi.awq_search_block_workspace_size(n, outs, K, cfg), dtype=torch.uint8, device="cuda")
+    losses = torch.empty(cfg.n_grid, dtype=torch.float32, device="cuda")
+    best = torch.empty(1, dtype=torch.int32, device="cuda")
+    s_best = torch.empty(K, dtype=torch.float32, device="cuda")
+    capi.awq_search_block(Wd, dev_bf16(X), dev_f32(sx32), cfg, losses, best, s_best, ws)
+    assert capi.awq_get_device_status(ws) == capi.AWQ_OK
+    _check_levels(losses.cpu().numpy(), int(best[0]), res["losses"])
+    s32 = O.f32(res["s_best"])
+    for W in Ws32:
+        _check_pack({"W": W, "w_dtype": "bf16"}, s32)

@@ -48,7 +48,7 @@ def _run(x32, pk):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 7, 128), (3, 300, 1024), (8, 130, 4096), (4, 1000, 11008), (2, 4096, 4096),
-                                   (1, 4096, 4096), (6, 520, 8192), (5, 2, 640)])
+                                   (1, 4096, 4096), (5, 520, 8192), (5, 2, 640)])
 def test_w4a16_matches_oracle(M, N, K):
     rng = np.random.default_rng(M * 1000 + N + K)
     pk = _random_packed(rng, N, K)

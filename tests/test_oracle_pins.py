@@ -366,3 +366,21 @@ def test_w4a16_linear_matches_the_searched_weight():
     assert np.all(np.abs(got - ref) <= bound)
     # and it is not trivially close: the quantisation error itself is much larger
     assert np.max(np.abs(X @ W.T - ref)) > 50 * np.max(np.abs(got - ref))
+
+
+def test_block_search_is_the_output_weighted_mean_of_the_linears():
+    # three linears sharing X, searched separately with the same statistic:
+    # the block loss of each alpha is their losses weighted by output count
+    rng = np.random.default_rng(21)
+    K, n = 256, 48
+    Ws = [(rng.standard_normal((r, K)) * 0.02) for r in (24, 8, 8)]
+    X = rng.standard_normal((n, K))
+    X[:, 17] *= 30.0
+    X = workloads.round_to_bf16(X.astype(np.float32)).astype(np.float64)
+    sx = O.channel_importance(X)
+    blk = O.search_scale_block(Ws, X, sx)
+    parts = [O.search_scale(W, X, sx)["losses"] for W in Ws]
+    outs = np.array([W.shape[0] for W in Ws], dtype=np.float64)
+    ref = sum(o * l for o, l in zip(outs, parts)) / outs.sum()
+    np.testing.assert_allclose(blk["losses"], ref, rtol=1e-12)
+    assert blk["best_idx"] == int(np.argmin(ref))
