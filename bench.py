@@ -425,6 +425,11 @@ def gpu_arm(args, rank, world, local_rank):
                 "timing": f"{copies} distinct copies per CUDA graph (> L2), L2 flushed before each graph"}
         del packs
 
+    # ---------------------------------------------------------- bandwidth kernels on the largest layer
+    # the statistics, fake-quant and pack kernels move 33-700 MB on the benchmark layer, a few microseconds of
+    # work beside a few microseconds of launch and ramp; on the 70B-class MLP layer they move 0.27-9.9 GB
+    large = None if args.no_large else large_layer_rates(dev, flush, peaks()["hbm_gbs"])
+
     # ---------------------------------------------------------- parity spot check vs stored oracle losses
     parity = None
     gpath = os.path.join(ROOT, "tests", "golden", "oracle_losses.json")
@@ -501,6 +506,7 @@ def gpu_arm(args, rank, world, local_rank):
         "stages": stages,
         "stages_unfused": separate,
         "w4a16_gemv": gemv,
+        "bandwidth_kernels_70b_layer": large,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clocks,
@@ -509,6 +515,54 @@ def gpu_arm(args, rank, world, local_rank):
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
+
+
+def large_layer_rates(dev, flush, hbm_gbs):
+    """Time the statistics, fake-quant and pack kernels alone on the 70B-class MLP shape (W 28672 x 8192
+    bf16, X 16384 x 8192 bf16, 20 alphas; random data, timing only), L2 flushed before each launch."""
+    import torch
+
+    from post_bit_weight_awq_b300 import capi
+
+    n, N, K = 16384, 28672, 8192
+    cfg = capi.config()
+    G = cfg.n_grid
+    X = torch.randn(n, K, device=dev).to(torch.bfloat16)
+    W = (torch.randn(N, K, device=dev) * 0.01).to(torch.bfloat16)
+    mean = torch.empty(K, dtype=torch.float32, device=dev)
+    sws = torch.empty(capi.awq_act_stats_workspace_size(n, K), dtype=torch.uint8, device=dev)
+    s = torch.empty(G, K, dtype=torch.float32, device=dev)
+    inv = torch.empty_like(s)
+    op = torch.empty(G, N, K, dtype=torch.bfloat16, device=dev)
+    qw = torch.empty(N, K // 8, dtype=torch.int32, device=dev)
+    sc = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+    zr = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+    capi.awq_act_stats(X, mean, sws)
+    capi.awq_alpha_scales(mean, cfg, s, inv)
+    calls = {
+        "stats": (lambda: capi.awq_act_stats(X, mean, sws), 2.0 * n * K),
+        "fakequant": (lambda: capi.awq_fakequant(W, s, inv, cfg, op), 2.0 * N * K + G * 2.0 * N * K),
+        "pack": (lambda: capi.awq_quantize_pack(W, s[7], cfg, qw, sc, zr), 2.0 * N * K + N * K / 2 + 4.0 * N * K / 128),
+    }
+    out = {"layer": {"W": [N, K], "X": [n, K], "n_grid": G}, "data": "random, timing only"}
+    for name, (fn, nbytes) in calls.items():
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(5):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 3)}
+    del op, X, W
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -520,6 +574,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--oracle-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-large", action="store_true", help="skip the 70B-class bandwidth-kernel timings")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

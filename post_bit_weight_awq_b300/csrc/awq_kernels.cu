@@ -511,11 +511,16 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT>())
     const GroupFast g = group_fast(mn, mx, qmax, floor_);
     float k[16];
     quant_codes_minus_z<16>(v, g, k);
+    // q = (q - z) + z in [0, 15]; 2^23 + q carries q in its low mantissa bits,
+    // which avoids a float-to-integer conversion per code
+    const float2 zb = make_float2(8388608.0f + g.z, 8388608.0f + g.z);
     uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      w0 |= (uint32_t)__fadd_rn(k[e], g.z) << (4 * e);
-      w1 |= (uint32_t)__fadd_rn(k[8 + e], g.z) << (4 * e);
+    for (int e = 0; e < 8; e += 2) {
+      const float2 a = __fadd2_rn(make_float2(k[e], k[e + 1]), zb);
+      const float2 b = __fadd2_rn(make_float2(k[8 + e], k[9 + e]), zb);
+      w0 |= ((__float_as_uint(a.x) & 0xFu) << (4 * e)) | ((__float_as_uint(a.y) & 0xFu) << (4 * e + 4));
+      w1 |= ((__float_as_uint(b.x) & 0xFu) << (4 * e)) | ((__float_as_uint(b.y) & 0xFu) << (4 * e + 4));
     }
     if (active) {
       int32_t* q = qweight + (size_t)row * kw + ((col0 + c_lo) >> 3);
