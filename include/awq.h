@@ -18,7 +18,11 @@
  * `group` weights): delta = max((vmax - vmin) / (2^w_bit - 1), delta_floor),
  * z = rne(-vmin / delta), q = clamp(rne(v / delta) + z, 0, 2^w_bit - 1),
  * dequantised value (q - z) * delta. Codes are decided in fp32 with correctly
- * rounded operations in exactly that order; rne is round-half-to-even.
+ * rounded operations in exactly that order; rne is round-half-to-even. With
+ * zero_point = 0 Q is the symmetric round-to-nearest of "Why does naive
+ * 4-bit quantization wreck LLM accuracy?" on the first page:
+ * delta = max(max|v| / 2^(w_bit-1), delta_floor), z = 2^(w_bit-1) fixed,
+ * same q and dequantisation (the top code clamps at 2^(w_bit-1) - 1 steps).
  *
  * Sources (web pages on AWQ, by title and section):
  *   - "AWQ: How Activation-Aware Quantization Saves 4-bit LLMs":
@@ -53,7 +57,7 @@
  *     non-finite loss) are written to a device status word; read it with
  *     awq_get_device_status, which synchronises the stream.
  *   - Shapes: in % group == 0, group % 8 == 0 (group == 128 in this build),
- *     w_bit == 4, zero_point == 1, 1 <= n_grid <= 64. n_tok and out are
+ *     w_bit == 4, zero_point 0 or 1, 1 <= n_grid <= 64. n_tok and out are
  *     arbitrary (>= 1); the loss divides by the true n_tok * out.
  *   - The codes quantise W * diag(s): the caller folds 1/s into whatever
  *     produces X (for a transformer, the preceding LayerNorm/RMSNorm weight,
@@ -107,7 +111,8 @@ typedef struct {
   int32_t w_bit;            /* 4 */
   int32_t group;            /* 128: weights per scale/zero along `in` */
   int32_t n_grid;           /* 20: alpha_i = i / n_grid, i < n_grid */
-  int32_t zero_point;       /* 1: asymmetric with zero point (only mode built) */
+  int32_t zero_point;       /* 1: asymmetric with zero point; 0: symmetric, delta = max|v| / 2^(w_bit-1),
+                               codes stored with the fixed zero point 2^(w_bit-1) */
   int32_t normalize;        /* 1: divide s by sqrt(max(s) * min(s)) */
   float sx_clamp_min;       /* 1e-4: sx is clamped from below before the power */
   float delta_floor;        /* 1e-5: lower bound of a group's step */

@@ -126,13 +126,22 @@ def quantize_groups(
     delta_floor: float = 1e-5,
     pinned: bool = True,
     round_fn: Callable[[np.ndarray], np.ndarray] = np.rint,
+    zero_point: bool = True,
 ):
-    """Group-wise asymmetric min/max quantisation of V [rows, in] along ``in``.
+    """Group-wise min/max quantisation of V [rows, in] along ``in``.
 
-    [AWQ-SWP, step-size equation: delta = (v_max - v_min) / (2^b - 1);
-    AWQ-devto quant_config: zero point on, groups of 128 along the input.]
-    Per group: delta = max((vmax - vmin) / (2^b - 1), delta_floor),
+    Asymmetric, with a zero point (the default) [AWQ-SWP, step-size equation:
+    delta = (v_max - v_min) / (2^b - 1); AWQ-devto quant_config: zero point
+    on, groups of 128 along the input]. Per group:
+    delta = max((vmax - vmin) / (2^b - 1), delta_floor),
     z = round(-vmin / delta), q = clamp(round(v / delta) + z, 0, 2^b - 1).
+    Symmetric, ``zero_point=False`` [AWQ-devto, "Why does naive 4-bit
+    quantization wreck LLM accuracy?": delta = max|w| / 2^(N-1),
+    Q(w) = delta * round(w / delta)]: delta = max(max|v| / 2^(b-1),
+    delta_floor); the rounded value lies in [-2^(b-1), 2^(b-1)] and is stored
+    in b bits as q = clamp(round(v / delta) + 2^(b-1), 0, 2^b - 1), i.e. with
+    the fixed zero point z = 2^(b-1) (the largest positive weight of a group
+    clamps to 2^(b-1) - 1 steps).
     ``pinned`` rounds every step to fp32 (the precision the kernels decide
     codes in); ``pinned=False`` is the same formula in fp64. ``round_fn`` is
     round-half-to-even; a test may pass the identity to remove rounding.
@@ -147,9 +156,15 @@ def quantize_groups(
     Vg = V.reshape(rows, K // group, group)
     vmax = Vg.max(axis=2)
     vmin = Vg.min(axis=2)
-    delta = r(r(vmax - vmin) / qmax)
-    delta = np.maximum(delta, r(np.float64(delta_floor)))
-    z = round_fn(r(-vmin / delta))
+    if zero_point:
+        delta = r(r(vmax - vmin) / qmax)
+        delta = np.maximum(delta, r(np.float64(delta_floor)))
+        z = round_fn(r(-vmin / delta))
+    else:
+        half = float(2 ** (w_bit - 1))
+        delta = r(np.maximum(-vmin, vmax) / half)  # max |v| / 2^(b-1)
+        delta = np.maximum(delta, r(np.float64(delta_floor)))
+        z = np.full_like(delta, half)
     q = np.clip(round_fn(r(Vg / delta[:, :, None])) + z[:, :, None], 0.0, qmax)
     return q.reshape(rows, K), delta, z
 
@@ -170,6 +185,7 @@ def fake_quantize(
     delta_floor: float = 1e-5,
     pinned: bool = True,
     round_fn: Callable[[np.ndarray], np.ndarray] = np.rint,
+    zero_point: bool = True,
 ) -> np.ndarray:
     """W_hat = Q(W * s) / s: scale columns up, quantise, fold the scale back.
 
@@ -186,7 +202,7 @@ def fake_quantize(
         V = f32(W * s[None, :])
     else:
         V = W * s[None, :]
-    q, delta, z = quantize_groups(V, w_bit, group, delta_floor, pinned, round_fn)
+    q, delta, z = quantize_groups(V, w_bit, group, delta_floor, pinned, round_fn, zero_point)
     return dequantize_groups(q, delta, z, group) / s[None, :]
 
 
@@ -227,6 +243,7 @@ def search_scale(
     delta_floor: float = 1e-5,
     pinned: bool = True,
     loss: Optional[Callable] = None,
+    zero_point: bool = True,
 ) -> Dict[str, object]:
     """Grid search over alpha for the scale with the lowest output MSE.
 
@@ -240,7 +257,7 @@ def search_scale(
     losses, scales = [], []
     for i, alpha in enumerate(alpha_grid(n_grid)):
         s = awq_scales(sx, alpha, clamp_min, normalize)
-        W_hat = fake_quantize(W, s, w_bit, group, delta_floor, pinned)
+        W_hat = fake_quantize(W, s, w_bit, group, delta_floor, pinned, zero_point=zero_point)
         err = loss(X, W, W_hat)
         losses.append(err)
         scales.append(s)
@@ -295,7 +312,7 @@ def unpack_words(words, in_features: int) -> np.ndarray:
     return out.reshape(rows, in_features)
 
 
-def quantize_pack(W, s, w_bit: int = 4, group: int = 128, delta_floor: float = 1e-5):
+def quantize_pack(W, s, w_bit: int = 4, group: int = 128, delta_floor: float = 1e-5, zero_point: bool = True):
     """Final codes of W * diag(s), packed, with fp16 group scales and zeros.
 
     [AWQ-Gloss, "INT4 Weight Packing & Export"; AWQ-Ref, memory example: one
@@ -310,7 +327,7 @@ def quantize_pack(W, s, w_bit: int = 4, group: int = 128, delta_floor: float = 1
     W = np.asarray(W, dtype=np.float64)
     s32 = f32(np.asarray(s, dtype=np.float64))
     V = f32(W * s32[None, :])
-    q, delta, z = quantize_groups(V, w_bit, group, delta_floor, pinned=True)
+    q, delta, z = quantize_groups(V, w_bit, group, delta_floor, pinned=True, zero_point=zero_point)
     return {
         "qweight": pack_words(q),
         "scales": delta.astype(np.float32).astype(np.float16),

@@ -25,7 +25,8 @@ awq_status check_cfg(const awq_config* cfg) {
   if (cfg->group <= 0 || cfg->w_bit <= 0) return AWQ_ERR_INVALID_ARG;
   if (!(cfg->sx_clamp_min > 0.0f) || !(cfg->delta_floor > 0.0f)) return AWQ_ERR_INVALID_ARG;
   if (cfg->loss_form != AWQ_LOSS_RESIDUAL && cfg->loss_form != AWQ_LOSS_REFERENCE) return AWQ_ERR_INVALID_ARG;
-  if (cfg->w_bit != 4 || cfg->group != kGroup || cfg->zero_point != 1) return AWQ_ERR_UNSUPPORTED;
+  if (cfg->zero_point != 0 && cfg->zero_point != 1) return AWQ_ERR_INVALID_ARG;
+  if (cfg->w_bit != 4 || cfg->group != kGroup) return AWQ_ERR_UNSUPPORTED;
   return AWQ_OK;
 }
 

@@ -20,7 +20,8 @@ namespace awq {
 //
 // One launch. Block = 32 x 8 threads over a strip of 256 channels and a
 // chunk of kStatsRows tokens. Each thread reads 8 channels (16 B) of every
-// 8th row of the chunk, so a warp reads 512 contiguous bytes per row. The 8
+// 8th row of the chunk, eight rows' loads in flight at a time, so a warp
+// reads 512 contiguous bytes per row. The 8
 // row phases are added in fixed order in shared memory and the chunk's
 // partial sums go to scratch. The block that finishes last on a strip (a
 // ticket counter per strip, zeroed before the launch) adds that strip's
@@ -58,12 +59,12 @@ __global__ void __launch_bounds__(256) stats_kernel(const uint16_t* __restrict__
   float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (col < K) {
     int r = r0 + ty;
-    for (; r + 24 < r1; r += 32) {
-      uint4 v[4];
+    for (; r + 56 < r1; r += 64) {  // 8 rows' loads in flight per thread
+      uint4 v[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = ld_nc_v4(X + (size_t)(r + 8 * u) * K + col);
+      for (int u = 0; u < 8; ++u) v[u] = ld_nc_v4(X + (size_t)(r + 8 * u) * K + col);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc_abs_bf16x8(a, v[u]);
+      for (int u = 0; u < 8; ++u) acc_abs_bf16x8(a, v[u]);
     }
     for (; r < r1; r += 8) acc_abs_bf16x8(a, ld_nc_v4(X + (size_t)r * K + col));
   }
@@ -352,8 +353,8 @@ struct SmemLane {
 template <typename WT, bool REF>
 __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
     fakequant_kernel(const WT* __restrict__ W, int N, int K, int G, const float* __restrict__ s,
-                     const float* __restrict__ inv_s, float qmax, float floor_, uint16_t* __restrict__ op,
-                     int64_t slot_elems, int nstrips, int rows_per_block) {
+                     const float* __restrict__ inv_s, float qmax, float floor_, int symmetric,
+                     uint16_t* __restrict__ op, int64_t slot_elems, int nstrips, int rows_per_block) {
   extern __shared__ float4 fq_smem[];
   float4* ss = fq_smem;                          // [chunk][4][32] float4
   float4* si = fq_smem + kFqAlphaChunk * 128;    // same for 1/s
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
 #pragma unroll 1
       for (int a = 0; a < gc; ++a) {
         uint32_t o[8];
-        fq_lane16<REF>(w, nw, SmemLane{ss + a * 128, si + a * 128, slane}, qmax, floor_, o);
+        fq_lane16<REF>(w, nw, SmemLane{ss + a * 128, si + a * 128, slane}, qmax, floor_, symmetric != 0, o);
         if (active) {
           uint4* dst = reinterpret_cast<uint4*>(op + (size_t)(a0 + a) * slot_elems + base);
           dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -433,7 +434,8 @@ cudaError_t launch_fakequant_t(const WT* W, int64_t N, int64_t K, const float* s
   rblocks = (N + rows_per_block - 1) / rows_per_block;
   const float qmax = (float)((1 << cfg.w_bit) - 1);
   fakequant_kernel<WT, REF><<<(unsigned)(rblocks * nstrips), kFqWarps * 32, kFqSmem, st>>>(
-      W, (int)N, (int)K, cfg.n_grid, s, inv_s, qmax, cfg.delta_floor, op, N * K, nstrips, rows_per_block);
+      W, (int)N, (int)K, cfg.n_grid, s, inv_s, qmax, cfg.delta_floor, cfg.zero_point == 0 ? 1 : 0, op, N * K,
+      nstrips, rows_per_block);
   return cudaGetLastError();
 }
 
@@ -471,8 +473,8 @@ constexpr int pack_blocks_per_sm() { return sizeof(WT) == 2 ? 3 : 2; }
 template <typename WT>
 __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT>())
     pack_kernel(const WT* __restrict__ W, int N, int K, const float* __restrict__ s, float qmax, float floor_,
-                int32_t* __restrict__ qweight, uint16_t* __restrict__ scales, uint16_t* __restrict__ zeros,
-                int nstrips, int rows_per_block) {
+                int symmetric, int32_t* __restrict__ qweight, uint16_t* __restrict__ scales,
+                uint16_t* __restrict__ zeros, int nstrips, int rows_per_block) {
   const int strip = blockIdx.x % nstrips;
   const int col0 = strip * kFqCols;
   const int ncols = min(kFqCols, K - col0);
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT>())
     }
     float mn, mx;
     group_minmax16(v, mn, mx);
-    const GroupFast g = group_fast(mn, mx, qmax, floor_);
+    const GroupFast g = group_fast(mn, mx, qmax, floor_, symmetric != 0);
     float k[16];
     quant_codes_minus_z<16>(v, g, k);
     // q = (q - z) + z in [0, 15]; 2^23 + q carries q in its low mantissa bits,
@@ -549,7 +551,8 @@ cudaError_t launch_pack_t(const WT* W, int64_t N, int64_t K, const float* s, con
   rblocks = (N + rows_per_block - 1) / rows_per_block;
   const float qmax = (float)((1 << cfg.w_bit) - 1);
   pack_kernel<WT><<<(unsigned)(rblocks * nstrips), kPackWarps * 32, 0, st>>>(
-      W, (int)N, (int)K, s, qmax, cfg.delta_floor, qweight, scales, zeros, nstrips, rows_per_block);
+      W, (int)N, (int)K, s, qmax, cfg.delta_floor, cfg.zero_point == 0 ? 1 : 0, qweight, scales, zeros, nstrips,
+      rows_per_block);
   return cudaGetLastError();
 }
 

@@ -78,6 +78,7 @@ struct Params {
   uint32_t* ready;          // [G][nt] quantiser-warp arrivals per operand tile, then [G] per alpha,
                             // then the search progress word (see quantise_units)
   float qmax, floor_;
+  int symmetric;            // zero point off (fixed z = 2^(b-1))
 };
 
 // Tile t of an m_tiles x nt grid in raster order. Tiles are taken in bands
@@ -472,7 +473,7 @@ __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane
         }
         if (r + 1 < r1) ldg_w16(p.W, p.w_bf16, (size_t)(r + 1) * p.K + c, wn);
         uint32_t o[8];
-        fq_lane16<false>(w, nw, RegLane{sv, iv}, p.qmax, p.floor_, o);
+        fq_lane16<false>(w, nw, RegLane{sv, iv}, p.qmax, p.floor_, p.symmetric != 0, o);
         if (active) {
           uint4* dst = reinterpret_cast<uint4*>(p.op + (size_t)a * slot + (size_t)r * p.K + c);
           dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -886,6 +887,7 @@ cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, i
   p.ready = ready;
   p.qmax = (float)((1 << cfg.w_bit) - 1);
   p.floor_ = cfg.delta_floor;
+  p.symmetric = cfg.zero_point == 0 ? 1 : 0;
   e = cudaMemsetAsync(ready, 0, fused_ready_words(p.G, p.nt) * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   e = launch_pair<true>(tmX, tmB, p, sms, st);

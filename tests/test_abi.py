@@ -108,6 +108,8 @@ def test_host_validation_of_search_and_pack(lib):
         capi.AWQ_ERR_UNSUPPORTED
     assert _status_of(s, A, B, C, capi.config(n_grid=65), D, D, D, D, 0, ws_bytes=need, **kw) == \
         capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(s, A, B, C, capi.config(zero_point=2), D, D, D, D, 0, ws_bytes=need, **kw) == \
+        capi.AWQ_ERR_INVALID_ARG
     assert _status_of(s, A, B, C, capi.config(loss_form=5), D, D, D, D, 0, ws_bytes=need, **kw) == \
         capi.AWQ_ERR_INVALID_ARG
     assert _status_of(s, A, B, C, cfg, D, D, D, D + 4, 0, ws_bytes=need, **kw) == capi.AWQ_ERR_MISALIGNED

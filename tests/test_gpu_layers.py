@@ -285,3 +285,13 @@ def test_block_search_shared_input():
     s32 = O.f32(res["s_best"])
     for W in Ws32:
         _check_pack({"W": W, "w_dtype": "bf16"}, s32)
+
+
+def test_symmetric_search_layer_levels():
+    """The whole search with the zero point off (fused kernel path), levels
+    2 and 3 against the oracle with the same quantiser."""
+    L = workloads.make_layer("llama7b_q_proj", n_tok=512, out_features=640, in_features=1024, seed=3)
+    sx32 = O.f32(O.channel_importance(L["X"]))
+    res = _oracle_losses(L["W"], L["X"], sx=sx32, zero_point=False)
+    losses, best, s_best = _search_with_statistic(L, sx32, capi.config(zero_point=0))
+    _check_levels(losses, best, res["losses"])

@@ -277,3 +277,39 @@ def test_pack_hand_built_groups():
     np.testing.assert_array_equal(qw.cpu().numpy(), ref["qweight"])
     np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint16), ref["scales"].view(np.uint16))
     np.testing.assert_array_equal(zr.cpu().numpy().view(np.uint16), ref["zeros"].view(np.uint16))
+
+
+# ------------------------------------------------------------------ symmetric quantiser (zero point off)
+
+
+@pytest.mark.parametrize("layer,kw", [("tiny", {}), ("llama7b_q_proj", dict(out_features=200, in_features=1024,
+                                                                          n_tok=64))])
+def test_symmetric_pack_and_fakequant_bit_exact(layer, kw):
+    L = workloads.make_layer(layer, **kw)
+    W, X = L["W"], L["X"]
+    N, K = W.shape
+    cfg = capi.config(zero_point=0)
+    sx = O.channel_importance(X)
+    for alpha in (0.0, 0.45, 0.9):
+        s32 = O.f32(O.awq_scales(sx, alpha))
+        ref = O.quantize_pack(W.astype(np.float64), s32, zero_point=False)
+        qw = torch.empty(N, K // 8, dtype=torch.int32, device="cuda")
+        sc = torch.empty(N, K // 128, dtype=torch.float16, device="cuda")
+        zr = torch.empty(N, K // 128, dtype=torch.float16, device="cuda")
+        capi.awq_quantize_pack(dev_weight(L), dev_f32(s32), cfg, qw, sc, zr)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(qw.cpu().numpy(), ref["qweight"])
+        np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint16), ref["scales"].view(np.uint16))
+        assert np.all(zr.cpu().numpy() == 8.0)
+    # the search operand of every alpha, as in test_fakequant_codes_and_values
+    G = cfg.n_grid
+    s32, inv32 = _oracle_scales32(sx, G)
+    op = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
+    capi.awq_fakequant(dev_weight(L), dev_f32(s32), dev_f32(inv32), cfg, op)
+    got = host_bf16_to_f64(op)
+    W64 = W.astype(np.float64)
+    for i in range(G):
+        W_hat = O.fake_quantize(W64, s32[i], zero_point=False)
+        ref = W_hat - W64
+        tol = 2.0**-8 * np.abs(ref) + 1e-6 * (np.abs(W64) + np.abs(W_hat)) + 1e-30
+        assert not (np.abs(got[i] - ref) > tol).any(), f"alpha {i}"

@@ -384,3 +384,37 @@ def test_block_search_is_the_output_weighted_mean_of_the_linears():
     ref = sum(o * l for o, l in zip(outs, parts)) / outs.sum()
     np.testing.assert_allclose(blk["losses"], ref, rtol=1e-12)
     assert blk["best_idx"] == int(np.argmin(ref))
+
+
+# ---------------------------------------------------------------- symmetric quantiser (zero point off)
+
+
+def test_symmetric_quantizer_matches_native_fp32_restatement():
+    # "Why does naive 4-bit quantization wreck LLM accuracy?": delta = max|w| / 2^(N-1),
+    # Q(w) = delta * round(w / delta); 4-bit storage clamps the rounded value to [-8, 7]
+    rng = np.random.default_rng(13)
+    V = (rng.standard_normal((6, 256)) * 0.05).astype(np.float32)
+    V[2, :128] = np.abs(V[2, :128])  # one-sign group
+    V[3, 128:] = -np.abs(V[3, 128:])
+    q, delta, z = O.quantize_groups(V.astype(np.float64), zero_point=False)
+    assert np.all(z == 8.0)
+    for r in range(V.shape[0]):
+        for g in range(2):
+            grp = V[r, 128 * g:128 * g + 128]
+            amax = np.float32(np.max(np.abs(grp)))
+            d = np.float32(amax / np.float32(8.0))
+            assert delta[r, g] == float(d)
+            codes = np.clip(np.rint(grp / d), -8, 7)  # fp32 division, ties to even
+            np.testing.assert_array_equal(q[r, 128 * g:128 * g + 128] - 8.0, codes.astype(np.float64))
+
+
+def test_symmetric_error_bound_and_range():
+    rng = np.random.default_rng(14)
+    V = rng.standard_normal((5, 384)) * 0.02
+    q, delta, z = O.quantize_groups(V, zero_point=False)
+    assert q.min() >= 0 and q.max() <= 15
+    err = np.abs(V - O.dequantize_groups(q, delta, z))
+    d = np.repeat(delta, 128, axis=1)
+    top = q == 15  # the positive maximum may clamp from +8 to +7 steps: error up to one step
+    assert np.all(err[~top] <= d[~top] / 2 * (1 + 1e-6))
+    assert np.all(err[top] <= d[top] * (1 + 1e-6))
