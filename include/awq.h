@@ -354,6 +354,18 @@ AWQ_API awq_status awq_search_gemm_withhold_fill(const void* X, int64_t n_tok, i
                                                  const uint16_t* op, int64_t out, const awq_config* cfg,
                                                  float* partials, uint32_t* status, awq_stream_t stream);
 
+/* Test aid for the cross-CTA waits of awq_search_fused: the quantiser warps
+   leave out their first unit (alpha 0, operand tile 0, channel strip 0), so
+   that tile's ready counter never completes and the TMA producers that need
+   it wait in vain. Each wait gives up after cfg->wait_timeout_ms; the kernel
+   then writes AWQ_ERR_TIMEOUT to *status, stops all its roles, lets what it
+   issued finish, frees its tensor memory and returns. Same arguments as
+   awq_search_fused; partials and op are not meaningful. */
+AWQ_API awq_status awq_search_fused_withhold_unit(const void* W, int32_t w_dtype, int64_t out, int64_t in,
+                                                  const void* X, int64_t n_tok, const float* s, const float* inv_s,
+                                                  const awq_config* cfg, uint16_t* op, float* partials,
+                                                  uint32_t* ready, uint32_t* status, awq_stream_t stream);
+
 /* losses[i] = (sum of partials[i]) / (n_tok * out): fp32 sums per thread
    over a fixed stride, fp64 across threads in a fixed tree (deterministic);
    best_idx = first i with the smallest fp32 loss; s_best = s[best_idx]. A

@@ -50,6 +50,7 @@ EXPORTED = (
     "awq_search_fused",
     "awq_search_gemm_dump",
     "awq_search_gemm_withhold_fill",
+    "awq_search_fused_withhold_unit",
     "awq_loss_select",
 )
 
@@ -114,6 +115,8 @@ def lib() -> ctypes.CDLL:
         "awq_search_fused": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I64, _P, _P, _CFG, _P, _P, _P, _P, _P]),
         "awq_search_gemm_dump": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P, _I32, _P]),
         "awq_search_gemm_withhold_fill": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
+        "awq_search_fused_withhold_unit": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I64, _P, _P, _CFG, _P, _P, _P,
+                                                          _P, _P]),
         "awq_loss_select": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _CFG, _P, _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
@@ -325,6 +328,17 @@ def awq_search_fused(W, X, s, inv_s, cfg: AwqConfig, op, partials, ready, status
     wd = _dtype_code(W) if w_dtype is None else w_dtype
     _check(lib().awq_search_fused(_ptr(W), wd, N, K, _ptr(X), n, _ptr(s), _ptr(inv_s), ctypes.byref(cfg), _ptr(op),
                                   _ptr(partials), _ptr(ready), _ptr(status), _stream(stream)), "awq_search_fused")
+
+
+def awq_search_fused_withhold_unit(W, X, s, inv_s, cfg: AwqConfig, op, partials, ready, status, stream=None, *,
+                                   out_features=None, in_features=None, n_tok=None, w_dtype=None) -> None:
+    N = W.shape[0] if out_features is None else out_features
+    K = W.shape[1] if in_features is None else in_features
+    n = X.shape[0] if n_tok is None else n_tok
+    wd = _dtype_code(W) if w_dtype is None else w_dtype
+    _check(lib().awq_search_fused_withhold_unit(_ptr(W), wd, N, K, _ptr(X), n, _ptr(s), _ptr(inv_s),
+                                                ctypes.byref(cfg), _ptr(op), _ptr(partials), _ptr(ready),
+                                                _ptr(status), _stream(stream)), "awq_search_fused_withhold_unit")
 
 
 def awq_search_gemm_dump(X, op, cfg: AwqConfig, partials, status, dump, stream=None, *, n_tok=None,

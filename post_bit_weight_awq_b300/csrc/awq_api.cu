@@ -217,6 +217,27 @@ awq_status awq_search_fused(const void* W, int32_t w_dtype, int64_t out, int64_t
                                        ready, status, (cudaStream_t)stream));
 }
 
+awq_status awq_search_fused_withhold_unit(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X,
+                                          int64_t n_tok, const float* s, const float* inv_s, const awq_config* cfg,
+                                          uint16_t* op, float* partials, uint32_t* ready, uint32_t* status,
+                                          awq_stream_t stream) {
+  if (W == nullptr || X == nullptr || s == nullptr || inv_s == nullptr || op == nullptr || partials == nullptr ||
+      ready == nullptr || status == nullptr)
+    return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  if (cfg->loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
+  st = check_wdtype(w_dtype);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(W) || !aligned16(X) || !aligned16(s) || !aligned16(inv_s) || !aligned16(op) ||
+      !aligned16(partials) || !aligned16(ready) || !aligned16(status))
+    return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, s, inv_s, out, *cfg, op, partials,
+                                       ready, status, (cudaStream_t)stream, nullptr, 0));
+}
+
 awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op, int64_t out,
                                 const awq_config* cfg, float* partials, uint32_t* status, float* dump,
                                 int32_t cluster_m, awq_stream_t stream) {

@@ -60,7 +60,7 @@ inline size_t fused_ready_words(int64_t G, int64_t n_tiles) { return (size_t)(G 
 cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, int64_t n_tok, int64_t K,
                                 const float* s, const float* inv_s, int64_t N, const awq_config& cfg, uint16_t* op,
                                 float* partials, uint32_t* ready, uint32_t* status, cudaStream_t st,
-                                float* dump = nullptr);
+                                float* dump = nullptr, int skip_unit = -1);
 
 // y[m][r] = sum_k x[m][k] * (q[r][k] - z[r][g]) * scale[r][g] for m < M <= 8,
 // x bf16 [M][K] (staged as fp32 in shared memory: M * K * 4 bytes).

@@ -79,6 +79,7 @@ struct Params {
                             // then the search progress word (see quantise_units)
   float qmax, floor_;
   int symmetric;            // zero point off (fixed z = 2^(b-1))
+  int skip_unit;            // test aid: quantiser unit never written or published (-1: none)
 };
 
 // Tile t of an m_tiles x nt grid in raster order. Tiles are taken in bands
@@ -449,6 +450,7 @@ __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane
   const size_t slot = (size_t)p.N * p.K;
   uint32_t* ready_alpha = p.ready + (size_t)p.G * p.nt;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    if (u == p.skip_unit) continue;  // test aid: the tile of this unit never becomes ready
     const int a = u / per_a;
     const int rem = u - a * per_a;
     const int nb = rem / p.nstrips;
@@ -825,6 +827,7 @@ cudaError_t setup_search(const uint16_t* X, int64_t n_tok, int64_t K, const uint
   p.n_tok = (int)n_tok;
   p.N = (int)N;
   p.K = (int)K;
+  p.skip_unit = -1;
   *pp = p;
   return cudaSuccess;
 }
@@ -868,7 +871,8 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
 
 cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, int64_t n_tok, int64_t K,
                                 const float* s, const float* inv_s, int64_t N, const awq_config& cfg, uint16_t* op,
-                                float* partials, uint32_t* ready, uint32_t* status, cudaStream_t st, float* dump) {
+                                float* partials, uint32_t* ready, uint32_t* status, cudaStream_t st, float* dump,
+                                int skip_unit) {
   if (cfg.loss_form != AWQ_LOSS_RESIDUAL) return cudaErrorInvalidValue;
   CUtensorMap tmX, tmB;
   Params p;
@@ -888,6 +892,7 @@ cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, i
   p.qmax = (float)((1 << cfg.w_bit) - 1);
   p.floor_ = cfg.delta_floor;
   p.symmetric = cfg.zero_point == 0 ? 1 : 0;
+  p.skip_unit = skip_unit;
   e = cudaMemsetAsync(ready, 0, fused_ready_words(p.G, p.nt) * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   e = launch_pair<true>(tmX, tmB, p, sms, st);

@@ -51,3 +51,42 @@ def test_stuck_wait_ends_with_timeout_status_and_device_stays_usable():
     for i in range(G):
         ref = ((A.astype(np.float64) @ B[i].astype(np.float64).T) ** 2).sum()
         assert P[i] == pytest.approx(ref, rel=1e-4)
+
+
+def test_fused_search_stuck_tile_ends_with_timeout_and_device_stays_usable():
+    """The cross-CTA wait of the fused search: one quantiser unit is never
+    published, so the producers needing its tile wait until the limit; the
+    kernel reports AWQ_ERR_TIMEOUT and the next launch is correct."""
+    n, N, K = 512, 1024, 512
+    rng = np.random.default_rng(4)
+    X = dev_bf16(workloads.round_to_bf16(rng.standard_normal((n, K)).astype(np.float32)))
+    W = dev_bf16(workloads.round_to_bf16((rng.standard_normal((N, K)) * 0.02).astype(np.float32)))
+    cfg = capi.config(n_grid=3, wait_timeout_ms=100)
+    G = cfg.n_grid
+    s = torch.empty(G, K, dtype=torch.float32, device="cuda")
+    inv = torch.empty_like(s)
+    mean = X.float().abs().mean(0).contiguous()
+    capi.awq_alpha_scales(mean, cfg, s, inv)
+    mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
+    op = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
+    parts = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device="cuda")
+    ready = torch.zeros(G * (nt + 1) + 1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    capi.awq_search_fused_withhold_unit(W, X, s, inv, cfg, op, parts, ready, status)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status[0]) == capi.AWQ_ERR_TIMEOUT
+    assert elapsed < 5.0
+    # the next launch on the same device is correct: it equals the two separate launches
+    status.zero_()
+    capi.awq_search_fused(W, X, s, inv, cfg, op, parts, ready, status)
+    op_ref = torch.empty_like(op)
+    p_ref = torch.zeros_like(parts)
+    capi.awq_fakequant(W, s, inv, cfg, op_ref)
+    capi.awq_search_gemm(X, op_ref, cfg, p_ref, status, n_tok=n, in_features=K, out_features=N)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    assert torch.equal(op.view(torch.int16), op_ref.view(torch.int16))
+    assert torch.equal(parts, p_ref)
