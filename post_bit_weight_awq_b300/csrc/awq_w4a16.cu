@@ -6,10 +6,10 @@
 //
 // The packed layer is streamed from HBM once; x (at most 8 tokens) is
 // converted to fp32 and staged in shared memory. One CTA of 16 warps per SM;
-// each warp owns R output rows at a time (R = 4 for one token, fewer for
-// more) and each lane one chunk of 32 consecutive codes of each (16-byte
-// loads, inside one group of 128) per step, with the next step's loads in
-// flight while the current one is computed. Codes become floats without conversion
+// each warp owns R output rows at a time and each lane 4 / R chunks of 32
+// consecutive codes of each (16-byte loads, each inside one group of 128)
+// per step, with the next step's loads in flight while the current one is
+// computed. Codes become floats without conversion
 // instructions: a byte permute places a nibble under the exponent bits of
 // 2^23 (0x4B00_00qq = 2^23 + q exactly), and one packed subtraction of
 // 2^23 + z gives (q - z, q' - z) for two neighbouring columns, exactly. The
@@ -41,34 +41,64 @@ __device__ __forceinline__ float nib_f(uint32_t v, int b) {
   return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440u + (uint32_t)b));
 }
 
-// Rows a warp works on together (R): the lane's 32 values of x per token are
-// read from shared memory once per chunk and used for all of them, which
-// divides the shared-memory traffic (4 bytes of x per 4-bit code) by R. The
-// launcher takes the largest R the registers allow (4 for one token, 2 for
-// two, else 1) that still gives every SM at least one CTA.
+// A step of a warp covers R rows and U chunks of 32 codes per lane (lane l
+// takes chunks base + l + 32u of each of the R rows): R * U = 4 16-byte code
+// loads per lane, and the next step's loads are in flight while the current
+// one is computed. The lane's x values of a chunk (32 per token) are read
+// from shared memory once and used for all R rows, which divides the
+// shared-memory traffic (4 bytes of x per 4-bit code) by R. The launcher
+// takes, among the R the registers allow (up to 4 for one token, 2 for two,
+// else 1), the one that leaves the fewest warps idle in the last round of
+// row groups; U = 4 / R (2 for more than four tokens).
 template <int M>
 __host__ __device__ constexpr int w4_max_rows() { return M == 1 ? 4 : (M == 2 ? 2 : 1); }
 
-// The loads of one step of a warp: chunk cbase + lane (32 codes) of R rows,
-// with each chunk's group step and zero.
-template <int R>
+template <int R, int U>
 struct W4Step {
-  uint4 q[R];
-  uint16_t s[R], z[R];
+  uint4 q[R][U];
+  uint16_t s[R][U], z[R][U];
 };
 
-template <int R>
-__device__ __forceinline__ void w4_load(W4Step<R>& st, const int32_t* __restrict__ qweight,
+template <int R, int U>
+__device__ __forceinline__ void w4_load(W4Step<R, U>& st, const int32_t* __restrict__ qweight,
                                         const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros,
-                                        int r0, int N, int c, int chunks, int kw, int kg) {
-  if (c >= chunks) return;
+                                        int r0, int N, int cbase, int chunks, int kw, int kg) {
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int r = r0 + i;
-    if (r < N) {
-      st.q[i] = ld_stream_v4(qweight + (size_t)r * kw + 4 * c);
-      st.s[i] = scales[(size_t)r * kg + (c >> 2)];
-      st.z[i] = zeros[(size_t)r * kg + (c >> 2)];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = cbase + 32 * u;
+      if (r < N && c < chunks) {
+        st.q[i][u] = ld_stream_v4(qweight + (size_t)r * kw + 4 * c);
+        st.s[i][u] = scales[(size_t)r * kg + (c >> 2)];
+        st.z[i][u] = zeros[(size_t)r * kg + (c >> 2)];
+      }
+    }
+  }
+}
+
+// x * (q - z) over the lane's 32 codes of one chunk: fp32 pairs, two columns at a time.
+template <int M>
+__device__ __forceinline__ void w4_chunk(const uint4 q, float zf, const float* __restrict__ xc, int kp, float2 (&part)[M]) {
+  const float zoff = 8388608.0f + zf;
+  const float2 nz = make_float2(-zoff, -zoff);
+  const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo = wd[j] & 0x0F0F0F0Fu;         // nibbles 0, 2, 4, 6: even columns
+    const uint32_t hi = (wd[j] >> 4) & 0x0F0F0F0Fu;  // nibbles 1, 3, 5, 7: odd columns
+#pragma unroll
+    for (int b = 0; b < 4; b += 2) {
+      // columns 8j + 2b .. + 3 of the chunk
+      const float2 w01 = __fadd2_rn(make_float2(nib_f(lo, b), nib_f(hi, b)), nz);
+      const float2 w23 = __fadd2_rn(make_float2(nib_f(lo, b + 1), nib_f(hi, b + 1)), nz);
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const float4 xv = *reinterpret_cast<const float4*>(xc + (size_t)m * kp + 8 * j + 2 * b);
+        part[m] = __ffma2_rn(w01, make_float2(xv.x, xv.y), part[m]);
+        part[m] = __ffma2_rn(w23, make_float2(xv.z, xv.w), part[m]);
+      }
     }
   }
 }
@@ -78,6 +108,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     w4a16_gemv_kernel(const uint16_t* __restrict__ x, int K, const int32_t* __restrict__ qweight,
                       const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros, int N,
                       float* __restrict__ y) {
+  constexpr int U = M > 4 ? 2 : 4 / R;  // fewer chunks in flight when many token accumulators need registers
   extern __shared__ float4 w4_smem[];
   // x as fp32, each run of 32 channels followed by 4 floats of padding: lane
   // l reads the run of chunk 32u + l, and the padding puts the 32 lanes'
@@ -87,15 +118,14 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunks = K >> 5;  // 32-code chunks per row
   const int kw = K >> 3, kg = K >> 7;
-  const int steps_per_group = (chunks + 31) / 32;
+  const int steps_per_group = (chunks + 32 * U - 1) / (32 * U);
   const int gstride = gridDim.x * kW4Warps * R;
 
-  // The warp's steps run through (group of R rows, chunk step); the loads of
-  // the next step are issued before the current one is computed. The first
-  // step's loads go out before x is staged, so their latency overlaps it.
+  // The warp's steps run through (group of R rows, step of U chunks); the
+  // first step's loads go out before x is staged, so their latency overlaps it.
   int r0 = (blockIdx.x * kW4Warps + warp) * R, k = 0;
-  W4Step<R> cur, nxt;
-  if (r0 < N) w4_load<R>(cur, qweight, scales, zeros, r0, N, lane, chunks, kw, kg);
+  W4Step<R, U> cur, nxt;
+  if (r0 < N) w4_load<R, U>(cur, qweight, scales, zeros, r0, N, lane, chunks, kw, kg);
 
   for (int i = threadIdx.x; i < M * K / 8; i += kW4Threads) {
     const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * 8);
@@ -117,41 +147,20 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       nr = r0 + gstride;
       nk = 0;
     }
-    if (nr < N) w4_load<R>(nxt, qweight, scales, zeros, nr, N, nk * 32 + lane, chunks, kw, kg);
-    const int c = k * 32 + lane;
-    if (c < chunks) {
-      // the lane's 32 x values per token, as pairs
-      float2 xv[M][16];
+    if (nr < N) w4_load<R, U>(nxt, qweight, scales, zeros, nr, N, nk * 32 * U + lane, chunks, kw, kg);
 #pragma unroll
-      for (int m = 0; m < M; ++m)
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float4 f = *reinterpret_cast<const float4*>(xs + (size_t)m * kp + c * kW4Pad + 4 * t);
-          xv[m][2 * t] = make_float2(f.x, f.y);
-          xv[m][2 * t + 1] = make_float2(f.z, f.w);
-        }
+    for (int u = 0; u < U; ++u) {
+      const int c = k * 32 * U + lane + 32 * u;
+      if (c >= chunks) break;
+      const float* xc = xs + c * kW4Pad;
 #pragma unroll
       for (int i = 0; i < R; ++i) {
         if (r0 + i >= N) break;
-        const float sc = __half2float(__ushort_as_half(cur.s[i]));
-        const float zoff = 8388608.0f + __half2float(__ushort_as_half(cur.z[i]));
-        const float2 nz = make_float2(-zoff, -zoff);
         float2 part[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) part[m] = make_float2(0.0f, 0.0f);
-        const uint32_t wd[4] = {cur.q[i].x, cur.q[i].y, cur.q[i].z, cur.q[i].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t lo = wd[j] & 0x0F0F0F0Fu;         // nibbles 0, 2, 4, 6: even columns
-          const uint32_t hi = (wd[j] >> 4) & 0x0F0F0F0Fu;  // nibbles 1, 3, 5, 7: odd columns
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            // columns 32c + 8j + 2b, + 1
-            const float2 w = __fadd2_rn(make_float2(nib_f(lo, b), nib_f(hi, b)), nz);
-#pragma unroll
-            for (int m = 0; m < M; ++m) part[m] = __ffma2_rn(w, xv[m][4 * j + b], part[m]);
-          }
-        }
+        w4_chunk<M>(cur.q[i][u], __half2float(__ushort_as_half(cur.z[i][u])), xc, kp, part);
+        const float sc = __half2float(__ushort_as_half(cur.s[i][u]));
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[i][m] = fmaf(sc, part[m].x + part[m].y, acc[i][m]);
       }
@@ -192,8 +201,20 @@ cudaError_t launch_w4_t(const uint16_t* x, int64_t K, const int32_t* qweight, co
   int sms = 0;
   cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
-  int R = w4_max_rows<M>();
-  while (R > 1 && N < (int64_t)sms * kW4Warps * R) R >>= 1;
+  // rows per warp: the candidate whose last round of row groups leaves the
+  // fewest warps idle, unless a larger R (more reuse of x) is within 0.1 of it
+  const int64_t warps = (int64_t)sms * kW4Warps;
+  int R = 1;
+  double best = -1.0;
+  for (int r = w4_max_rows<M>(); r >= 1; r >>= 1) {
+    const int64_t groups = (N + r - 1) / r;
+    const int64_t rounds = (groups + warps - 1) / warps;
+    const double busy = (double)groups / (double)(rounds * warps);
+    if (busy > best + 0.1) {
+      best = busy;
+      R = r;
+    }
+  }
   if (R == 4) return launch_w4_r<M, (w4_max_rows<M>() >= 4 ? 4 : 1)>(x, K, qweight, scales, zeros, N, y, sms, st);
   if (R == 2) return launch_w4_r<M, (w4_max_rows<M>() >= 2 ? 2 : 1)>(x, K, qweight, scales, zeros, N, y, sms, st);
   return launch_w4_r<M, 1>(x, K, qweight, scales, zeros, N, y, sms, st);
