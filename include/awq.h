@@ -186,7 +186,11 @@ AWQ_API awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, co
    the device status word read by awq_get_device_status.
    The products run on bf16 tensor cores with fp32 accumulation; the step-2
    output matrix never leaves the chip. In the RESIDUAL form the fake-quant
-   runs inside the search kernel (awq_search_fused); the REFERENCE form runs
+   runs inside the search kernel (awq_search_fused) for searches below 2e13
+   flops (2 * n_grid * n_tok * out * in); larger ones, which run long enough
+   to settle at the GPU's power cap, run awq_fakequant and then the
+   single-CTA products with 2-CTA operand multicast (awq_search_gemm_dump
+   with cluster_m 2), which do more work per joule. The REFERENCE form runs
    awq_fakequant and awq_search_gemm one after the other. */
 AWQ_API awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t in,
                             const void* X, int32_t x_dtype, int64_t n_tok, const float* mean_abs,

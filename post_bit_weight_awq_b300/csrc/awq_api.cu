@@ -12,6 +12,13 @@ namespace {
 
 constexpr size_t kAlign = 1024;
 
+// Search size (flops of the alpha products) from which awq_search_layer
+// uses the single-CTA products instead of the fused CTA-pair kernel: below
+// it a search fits in the GPU's burst power budget, above it the run settles
+// at the power cap (measured: 13B-class 33 ms vs 38 ms, 70B-class 115 ms vs
+// 138 ms per search; Llama-7B q_proj and MLP within 3% either way).
+constexpr double kLargeSearchFlops = 2e13;
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -379,11 +386,18 @@ awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, c
 
   cudaError_t e = cudaMemsetAsync(status, 0, 4, s);
   if (e == cudaSuccess) e = launch_alpha_scales(mean_abs, in, *cfg, sc, inv, s);
-  if (cfg->loss_form == AWQ_LOSS_RESIDUAL) {
+  const double flops = 2.0 * cfg->n_grid * (double)n_tok * (double)out * (double)in;
+  if (cfg->loss_form == AWQ_LOSS_RESIDUAL && flops < kLargeSearchFlops) {
     // fake-quant runs inside the search kernel, ahead of the products that consume it
     if (e == cudaSuccess)
       e = launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, sc, inv, out, *cfg, op, partials, ready,
                               status, s);
+  } else if (cfg->loss_form == AWQ_LOSS_RESIDUAL) {
+    // searches that run for tens of milliseconds and more settle at the power cap, where the single-CTA
+    // products with 2-CTA operand multicast do more work per joule than the CTA-pair products
+    if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
+    if (e == cudaSuccess)
+      e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 2);
   } else {
     if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
     if (e == cudaSuccess) e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s);
