@@ -419,7 +419,7 @@ def gpu_arm(args, rank, world, local_rank):
             gt.append(a.elapsed_time(b) / copies)
         ms_g = statistics.median(gt)
         gbytes = layer_bytes + K * 2 + N * 4
-        gemv = {"kernel": "w4a16_gemv_kernel<1>", "tokens": 1, "layer": [N, K], "ms_per_layer": round(ms_g, 5),
+        gemv = {"kernel": "w4a16_gemv_kernel<1, R> (R rows per warp, chosen by the launcher)", "tokens": 1, "layer": [N, K], "ms_per_layer": round(ms_g, 5),
                 "bytes_per_layer": gbytes, "gbs": round(gbytes / (ms_g * 1e-3) / 1e9, 1),
                 "frac_hbm": round(gbytes / (ms_g * 1e-3) / 1e9 / peaks()["hbm_gbs"], 3),
                 "timing": f"{copies} distinct copies per CUDA graph (> L2), L2 flushed before each graph"}

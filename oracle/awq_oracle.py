@@ -328,10 +328,14 @@ def quantize_pack(W, s, w_bit: int = 4, group: int = 128, delta_floor: float = 1
     s32 = f32(np.asarray(s, dtype=np.float64))
     V = f32(W * s32[None, :])
     q, delta, z = quantize_groups(V, w_bit, group, delta_floor, pinned=True, zero_point=zero_point)
+    # a zero point beyond the fp16 range (a near-constant group far from 0, step at the floor) rounds to inf,
+    # as an IEEE round-to-nearest conversion does; that is the stored value, not an error
+    with np.errstate(over="ignore"):
+        zeros16 = z.astype(np.float32).astype(np.float16)
     return {
         "qweight": pack_words(q),
         "scales": delta.astype(np.float32).astype(np.float16),
-        "zeros": z.astype(np.float32).astype(np.float16),
+        "zeros": zeros16,
         "codes": q.astype(np.int64),
         "delta": delta,
         "z": z,
