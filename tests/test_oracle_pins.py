@@ -91,18 +91,19 @@ def test_scale_clamp_and_power_closed_form():
 # ---------------------------------------------------------------- quantiser
 
 
-def _native_fp32_rtn_group(vals, floor=np.float32(1e-5)):
-    """Independent per-group asymmetric RTN in native fp32 scalar arithmetic."""
+def _native_fp32_rtn_group(vals, floor=np.float32(1e-5), levels=15):
+    """Independent per-group asymmetric RTN in native fp32 scalar arithmetic
+    (`levels` = 2^b - 1 steps across the group's range)."""
     v = [np.float32(x) for x in vals]
     hi, lo = max(v), min(v)
-    d = np.float32(np.float32(hi - lo) / np.float32(15.0))
+    d = np.float32(np.float32(hi - lo) / np.float32(levels))
     if d < floor:
         d = floor
     z = np.float32(np.rint(np.float32(-lo / d)))
     codes = []
     for x in v:
         c = np.float32(np.rint(np.float32(x / d))) + z
-        codes.append(min(max(float(c), 0.0), 15.0))
+        codes.append(min(max(float(c), 0.0), float(levels)))
     return codes, float(d), float(z)
 
 
@@ -418,3 +419,104 @@ def test_symmetric_error_bound_and_range():
     top = q == 15  # the positive maximum may clamp from +8 to +7 steps: error up to one step
     assert np.all(err[~top] <= d[~top] / 2 * (1 + 1e-6))
     assert np.all(err[top] <= d[top] * (1 + 1e-6))
+
+
+# ---------------------------------------------------------------- group sizes and code widths (the quantiser's knobs)
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("w_bit", [2, 3, 4, 8])
+def test_group_size_and_width_match_native_fp32(group, w_bit):
+    # "AWQ > Salient Weight Preservation", step-size equation: the range over 2^b - 1 levels, for any b;
+    # the first page's deployment notes: finer groups carry their own step. Checked group by group
+    # against the scalar fp32 restatement, which walks the row in slices of `group`.
+    rng = np.random.default_rng(100 * group + w_bit)
+    W = O.f32(rng.standard_normal((4, 256)) * 0.02)  # fp32 weights, as the kernels read them
+    s32 = O.f32(rng.uniform(0.3, 3.0, 256))
+    V = O.f32(W * s32[None, :])
+    q, d, z = O.quantize_groups(V, w_bit=w_bit, group=group)
+    assert d.shape == (4, 256 // group)
+    for r in range(4):
+        for g in range(256 // group):
+            vals = [np.float32(W[r, k]) * np.float32(s32[k]) for k in range(g * group, (g + 1) * group)]
+            codes, dn, zn = _native_fp32_rtn_group(vals, levels=2**w_bit - 1)
+            assert d[r, g] == dn and z[r, g] == zn, (r, g)
+            np.testing.assert_array_equal(q[r, g * group:(g + 1) * group], codes)
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("w_bit", [2, 3, 4, 8])
+def test_symmetric_group_size_and_width_match_native_fp32(group, w_bit):
+    # "Why does naive 4-bit quantization wreck LLM accuracy?": delta = max|w| / 2^(N-1); b bits hold
+    # -2^(b-1) .. 2^(b-1) - 1 steps
+    rng = np.random.default_rng(200 * group + w_bit)
+    V = (rng.standard_normal((3, 256)) * 0.05).astype(np.float32)
+    half = np.float32(2 ** (w_bit - 1))
+    q, delta, z = O.quantize_groups(V.astype(np.float64), w_bit=w_bit, group=group, zero_point=False)
+    assert np.all(z == float(half))
+    for r in range(3):
+        for g in range(256 // group):
+            grp = V[r, g * group:(g + 1) * group]
+            d = np.float32(np.float32(np.max(np.abs(grp))) / half)
+            assert delta[r, g] == float(d)
+            codes = np.clip(np.rint(grp / d), -half, half - 1)
+            np.testing.assert_array_equal(q[r, g * group:(g + 1) * group] - float(half), codes.astype(np.float64))
+
+
+@pytest.mark.parametrize("w_bit", [2, 3, 4, 5, 8])
+def test_group_of_exact_levels_is_reproduced(w_bit):
+    """Closed form: a group whose values are 2^b evenly spaced levels (power-of-two spacing, the zero at
+    level z0) has step = the spacing, zero point z0 and codes = the level indices, and dequantises
+    exactly. A wrong level count (2^b or 2^b - 2) or a wrong zero point breaks it."""
+    levels = 2**w_bit
+    group = 128
+    rng = np.random.default_rng(w_bit)
+    for z0 in (0, 1, levels // 2, levels - 1):
+        spacing = 2.0**-7
+        idx = np.concatenate([[0, levels - 1], rng.integers(0, levels, group - 2)])
+        vals = (idx - z0) * spacing
+        q, d, z = O.quantize_groups(vals[None, :], w_bit=w_bit, group=group)
+        assert d[0, 0] == spacing and z[0, 0] == z0
+        np.testing.assert_array_equal(q[0], idx)
+        np.testing.assert_array_equal(O.dequantize_groups(q, d, z, group)[0], vals)
+
+
+def test_finer_groups_never_widen_the_step():
+    """A group of g weights inside a group of 2g has a range no wider than the larger group's, so its
+    step is at most the larger group's step (the pages' accuracy/overhead trade-off of finer groups):
+    the step of group j at size g is bounded by that of group j // 2 at size 2g."""
+    rng = np.random.default_rng(21)
+    V = O.f32(rng.standard_normal((8, 512)) * 0.03)
+    V[:, 7] = 2.0  # an outlier column widens only the groups that hold it
+    steps = {g: O.quantize_groups(V, group=g)[1] for g in (32, 64, 128)}
+    for g in (32, 64):
+        fine, coarse = steps[g], steps[2 * g]
+        assert np.all(fine <= np.repeat(coarse, 2, axis=1))
+    # the outlier's 32-group step is far above the others', and only its own groups carry it
+    assert steps[32][:, 0].min() > 10 * steps[32][:, 1:].max()
+    assert np.all(steps[64][:, 1:] < steps[64][:, :1])
+
+
+@pytest.mark.parametrize("group", [32, 64])
+def test_pack_and_w4a16_with_finer_groups(group):
+    """Packed layer with groups of 32 or 64: one fp16 scale and zero per group, codes unchanged by the
+    storage, and the product over the words equals the dequantised weight's (brute force)."""
+    rng = np.random.default_rng(group)
+    W = rng.standard_normal((6, 256)) * 0.02
+    s = O.f32(rng.uniform(0.5, 2.0, 256))
+    pk = O.quantize_pack(W, s, group=group)
+    assert pk["scales"].shape == (6, 256 // group) and pk["zeros"].shape == (6, 256 // group)
+    np.testing.assert_array_equal(O.unpack_words(pk["qweight"], 256), pk["codes"])
+    x = rng.standard_normal((3, 256))
+    y = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"], group=group)
+    ref = np.zeros((3, 6))
+    for t in range(3):
+        for r in range(6):
+            acc = 0.0
+            for k in range(256):
+                word = int(pk["qweight"][r, k // 8]) & 0xFFFFFFFF
+                code = (word >> (4 * (k % 8))) & 0xF
+                gi = k // group
+                acc += x[t, k] * (code - float(pk["zeros"][r, gi])) * float(pk["scales"][r, gi])
+            ref[t, r] = acc
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-15)
