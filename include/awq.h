@@ -56,9 +56,14 @@
  *     Conditions found on the device (a bounded wait that ran out, a
  *     non-finite loss) are written to a device status word; read it with
  *     awq_get_device_status, which synchronises the stream.
- *   - Shapes: in % group == 0, group % 8 == 0 (group == 128 in this build),
- *     w_bit == 4, zero_point 0 or 1, 1 <= n_grid <= 64. n_tok and out are
- *     arbitrary (>= 1); the loss divides by the true n_tok * out.
+ *   - Shapes: group 32, 64 or 128 ("AWQ: How Activation-Aware Quantization
+ *     Saves 4-bit LLMs", deployment notes: finer groups, more scales), in a
+ *     multiple of 128 whatever the group (the kernels hold 128-channel
+ *     blocks in 8 lanes), w_bit 2..8 for the search and 4 for the packed
+ *     layer (awq_quantize_pack, awq_w4a16_gemv), zero_point 0 or 1,
+ *     1 <= n_grid <= 64. Other group sizes and widths return
+ *     AWQ_ERR_UNSUPPORTED. n_tok and out are arbitrary (>= 1); the loss
+ *     divides by the true n_tok * out.
  *   - The codes quantise W * diag(s): the caller folds 1/s into whatever
  *     produces X (for a transformer, the preceding LayerNorm/RMSNorm weight,
  *     as "AWQ > Salient Weight Preservation" describes). s_best is returned
@@ -87,7 +92,7 @@ typedef struct CUstream_st* awq_stream_t;
 typedef enum {
   AWQ_OK = 0,
   AWQ_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad config */
-  AWQ_ERR_UNSUPPORTED = 2, /* valid but not built: w_bit != 4, group != 128 ... */
+  AWQ_ERR_UNSUPPORTED = 2, /* valid but not built: group not 32/64/128, w_bit outside 2..8 (4 to pack) ... */
   AWQ_ERR_MISALIGNED = 3,  /* a device pointer is not 16-byte aligned */
   AWQ_ERR_WORKSPACE = 4,   /* ws_bytes below the size the query returns */
   AWQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
@@ -108,8 +113,8 @@ typedef enum { AWQ_BF16 = 0, AWQ_FP32 = 1 } awq_dtype;
 typedef enum { AWQ_LOSS_RESIDUAL = 0, AWQ_LOSS_REFERENCE = 1 } awq_loss_form;
 
 typedef struct {
-  int32_t w_bit;            /* 4 */
-  int32_t group;            /* 128: weights per scale/zero along `in` */
+  int32_t w_bit;            /* 4: bits per code (2..8 in the search, 4 in the packed layer) */
+  int32_t group;            /* 128: weights per scale/zero along `in` (32, 64 or 128) */
   int32_t n_grid;           /* 20: alpha_i = i / n_grid, i < n_grid */
   int32_t zero_point;       /* 1: asymmetric with zero point; 0: symmetric, delta = max|v| / 2^(w_bit-1),
                                codes stored with the fixed zero point 2^(w_bit-1) */
@@ -234,7 +239,8 @@ AWQ_API awq_status awq_search_block(const void* const* W_list, int32_t w_dtype, 
    qweight: device int32 [out][in/8]; the code of column 8j+k sits in bits
    [4k, 4k+4) of word j. scales_f16 / zeros_f16: device fp16 bit patterns
    [out][in/group] holding fp16(delta) and fp16(z), round-to-nearest-even.
-   Needs no scratch. */
+   cfg->w_bit must be 4 (the pages pack 4-bit codes into INT32 containers;
+   other widths return AWQ_ERR_UNSUPPORTED). Needs no scratch. */
 AWQ_API awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out, int64_t in,
                              const float* s, const awq_config* cfg, int32_t* qweight,
                              uint16_t* scales_f16, uint16_t* zeros_f16, awq_stream_t stream);

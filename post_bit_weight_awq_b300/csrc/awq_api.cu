@@ -33,14 +33,25 @@ awq_status check_cfg(const awq_config* cfg) {
   if (!(cfg->sx_clamp_min > 0.0f) || !(cfg->delta_floor > 0.0f)) return AWQ_ERR_INVALID_ARG;
   if (cfg->loss_form != AWQ_LOSS_RESIDUAL && cfg->loss_form != AWQ_LOSS_REFERENCE) return AWQ_ERR_INVALID_ARG;
   if (cfg->zero_point != 0 && cfg->zero_point != 1) return AWQ_ERR_INVALID_ARG;
-  if (cfg->w_bit != 4 || cfg->group != kGroup) return AWQ_ERR_UNSUPPORTED;
+  // groups of 32, 64 or 128 weights (one or two groups per lane run of the
+  // quantiser kernels); 2 to 8 bits per code in the search, whose codes are
+  // never stored
+  if (cfg->group != 32 && cfg->group != 64 && cfg->group != 128) return AWQ_ERR_UNSUPPORTED;
+  if (cfg->w_bit < 2 || cfg->w_bit > 8) return AWQ_ERR_UNSUPPORTED;
   return AWQ_OK;
+}
+
+// The packed format holds 4-bit codes, 8 to an int32.
+awq_status check_packed_cfg(const awq_config* cfg) {
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  return cfg->w_bit == 4 ? AWQ_OK : AWQ_ERR_UNSUPPORTED;
 }
 
 awq_status check_dims(int64_t n_tok, int64_t out, int64_t in) {
   if (n_tok < 1 || out < 1 || in < 1) return AWQ_ERR_INVALID_ARG;
   if (n_tok > kMaxDim || out > kMaxDim || in > kMaxDim) return AWQ_ERR_INVALID_ARG;
-  if (in % kGroup != 0) return AWQ_ERR_INVALID_ARG;
+  if (in % kBlockCols != 0) return AWQ_ERR_INVALID_ARG;
   if (out * in > ((int64_t)1 << 40)) return AWQ_ERR_INVALID_ARG;
   return AWQ_OK;
 }
@@ -174,7 +185,7 @@ awq_status awq_alpha_scales(const float* mean_abs, int64_t in, const awq_config*
   if (mean_abs == nullptr || s == nullptr || inv_s == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
-  if (in < 1 || in > kMaxDim || in % kGroup != 0) return AWQ_ERR_INVALID_ARG;
+  if (in < 1 || in > kMaxDim || in % kBlockCols != 0) return AWQ_ERR_INVALID_ARG;
   if (!aligned16(mean_abs) || !aligned16(s) || !aligned16(inv_s)) return AWQ_ERR_MISALIGNED;
   return from_cuda(launch_alpha_scales(mean_abs, in, *cfg, s, inv_s, (cudaStream_t)stream));
 }
@@ -417,7 +428,7 @@ awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out, int64_
                              awq_stream_t stream) {
   if (W == nullptr || s == nullptr || qweight == nullptr || scales_f16 == nullptr || zeros_f16 == nullptr)
     return AWQ_ERR_INVALID_ARG;
-  awq_status st = check_cfg(cfg);
+  awq_status st = check_packed_cfg(cfg);
   if (st != AWQ_OK) return st;
   st = check_wdtype(w_dtype);
   if (st != AWQ_OK) return st;
@@ -435,7 +446,7 @@ awq_status awq_w4a16_gemv(const void* x, int32_t x_dtype, int64_t n_tok, int64_t
                           float* y, awq_stream_t stream) {
   if (x == nullptr || qweight == nullptr || scales_f16 == nullptr || zeros_f16 == nullptr || y == nullptr)
     return AWQ_ERR_INVALID_ARG;
-  awq_status st = check_cfg(cfg);
+  awq_status st = check_packed_cfg(cfg);
   if (st != AWQ_OK) return st;
   st = check_xdtype(x_dtype);
   if (st != AWQ_OK) return st;
@@ -445,8 +456,8 @@ awq_status awq_w4a16_gemv(const void* x, int32_t x_dtype, int64_t n_tok, int64_t
   if (!aligned16(x) || !aligned16(qweight) || (reinterpret_cast<uintptr_t>(scales_f16) & 1u) ||
       (reinterpret_cast<uintptr_t>(zeros_f16) & 1u) || (reinterpret_cast<uintptr_t>(y) & 3u))
     return AWQ_ERR_MISALIGNED;
-  return from_cuda(launch_w4a16_gemv((const uint16_t*)x, n_tok, in, qweight, scales_f16, zeros_f16, out, y,
-                                     (cudaStream_t)stream));
+  return from_cuda(launch_w4a16_gemv((const uint16_t*)x, n_tok, in, qweight, scales_f16, zeros_f16, out,
+                                     cfg->group, y, (cudaStream_t)stream));
 }
 
 size_t awq_packed_bytes(int64_t out, int64_t in, const awq_config* cfg) {

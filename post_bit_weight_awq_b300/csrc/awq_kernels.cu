@@ -248,17 +248,6 @@ __device__ __forceinline__ void load8f(const float* p, float* v) {
   v[7] = b.w;
 }
 
-// Group minimum and maximum of 16 values per lane over the 8 lanes of a group
-// (lanes 8j .. 8j+7 of the warp).
-__device__ __forceinline__ void group_minmax16(const float (&v)[16], float& mn, float& mx) {
-  minmax_n<16>(v, mn, mx);
-#pragma unroll
-  for (int o = 4; o; o >>= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-}
-
 __device__ __forceinline__ uint4 pack_bf16x8(const float* r) {
   uint4 o;
   o.x = pack_bf16x2(r[0], r[1]);
@@ -350,7 +339,7 @@ struct SmemLane {
   __device__ __forceinline__ void load_inv(float2 (&v)[8]) const { lds_lane16(inv, lane, v); }
 };
 
-template <typename WT, bool REF>
+template <typename WT, bool REF, int GROUP>
 __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
     fakequant_kernel(const WT* __restrict__ W, int N, int K, int G, const float* __restrict__ s,
                      const float* __restrict__ inv_s, float qmax, float floor_, int symmetric,
@@ -406,7 +395,7 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
 #pragma unroll 1
       for (int a = 0; a < gc; ++a) {
         uint32_t o[8];
-        fq_lane16<REF>(w, nw, SmemLane{ss + a * 128, si + a * 128, slane}, qmax, floor_, symmetric != 0, o);
+        fq_lane16<REF, GROUP>(w, nw, SmemLane{ss + a * 128, si + a * 128, slane}, qmax, floor_, symmetric != 0, o);
         if (active) {
           uint4* dst = reinterpret_cast<uint4*>(op + (size_t)(a0 + a) * slot_elems + base);
           dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -417,10 +406,10 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
   }
 }
 
-template <typename WT, bool REF>
+template <typename WT, bool REF, int GROUP>
 cudaError_t launch_fakequant_t(const WT* W, int64_t N, int64_t K, const float* s, const float* inv_s,
                                const awq_config& cfg, uint16_t* op, cudaStream_t st) {
-  cudaError_t e = ensure_dynamic_smem((const void*)fakequant_kernel<WT, REF>, kFqSmem);
+  cudaError_t e = ensure_dynamic_smem((const void*)fakequant_kernel<WT, REF, GROUP>, kFqSmem);
   if (e != cudaSuccess) return e;
   int sms = 0;
   e = sm_count(&sms);
@@ -433,23 +422,34 @@ cudaError_t launch_fakequant_t(const WT* W, int64_t N, int64_t K, const float* s
   const int rows_per_block = (int)((N + rblocks - 1) / rblocks);
   rblocks = (N + rows_per_block - 1) / rows_per_block;
   const float qmax = (float)((1 << cfg.w_bit) - 1);
-  fakequant_kernel<WT, REF><<<(unsigned)(rblocks * nstrips), kFqWarps * 32, kFqSmem, st>>>(
+  fakequant_kernel<WT, REF, GROUP><<<(unsigned)(rblocks * nstrips), kFqWarps * 32, kFqSmem, st>>>(
       W, (int)N, (int)K, cfg.n_grid, s, inv_s, qmax, cfg.delta_floor, cfg.zero_point == 0 ? 1 : 0, op, N * K,
       nstrips, rows_per_block);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,
-                             const float* inv_s, const awq_config& cfg, uint16_t* op, cudaStream_t st) {
+template <int GROUP>
+cudaError_t launch_fakequant_g(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,
+                               const float* inv_s, const awq_config& cfg, uint16_t* op, cudaStream_t st) {
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
   if (w_dtype == AWQ_BF16) {
     const uint16_t* w = (const uint16_t*)W;
-    return ref ? launch_fakequant_t<uint16_t, true>(w, N, K, s, inv_s, cfg, op, st)
-               : launch_fakequant_t<uint16_t, false>(w, N, K, s, inv_s, cfg, op, st);
+    return ref ? launch_fakequant_t<uint16_t, true, GROUP>(w, N, K, s, inv_s, cfg, op, st)
+               : launch_fakequant_t<uint16_t, false, GROUP>(w, N, K, s, inv_s, cfg, op, st);
   }
   const float* w = (const float*)W;
-  return ref ? launch_fakequant_t<float, true>(w, N, K, s, inv_s, cfg, op, st)
-             : launch_fakequant_t<float, false>(w, N, K, s, inv_s, cfg, op, st);
+  return ref ? launch_fakequant_t<float, true, GROUP>(w, N, K, s, inv_s, cfg, op, st)
+             : launch_fakequant_t<float, false, GROUP>(w, N, K, s, inv_s, cfg, op, st);
+}
+
+cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,
+                             const float* inv_s, const awq_config& cfg, uint16_t* op, cudaStream_t st) {
+  switch (cfg.group) {
+    case 32: return launch_fakequant_g<32>(W, w_dtype, N, K, s, inv_s, cfg, op, st);
+    case 64: return launch_fakequant_g<64>(W, w_dtype, N, K, s, inv_s, cfg, op, st);
+    case 128: return launch_fakequant_g<128>(W, w_dtype, N, K, s, inv_s, cfg, op, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // ============================================================== pack
@@ -466,12 +466,13 @@ cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, c
 // while the current row is quantised.
 
 constexpr int kPackWarps = 8;
-// resident blocks per SM: the fp32-weight variant needs more registers
-template <typename WT>
-constexpr int pack_blocks_per_sm() { return sizeof(WT) == 2 ? 3 : 2; }
+// resident blocks per SM: fp32 weights, and two groups per lane, need more
+// registers than the 80 of three blocks
+template <typename WT, int GROUP>
+constexpr int pack_blocks_per_sm() { return (sizeof(WT) == 2 && GROUP == 128) ? 3 : 2; }
 
-template <typename WT>
-__global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT>())
+template <typename WT, int GROUP>
+__global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>())
     pack_kernel(const WT* __restrict__ W, int N, int K, const float* __restrict__ s, float qmax, float floor_,
                 int symmetric, int32_t* __restrict__ qweight, uint16_t* __restrict__ scales,
                 uint16_t* __restrict__ zeros, int nstrips, int rows_per_block) {
@@ -483,8 +484,12 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT>())
   if (r_begin >= r_end) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane >> 3, sub = lane & 7;
-  const bool active = grp * 128 < ncols;  // groups past a partial strip repeat group 0 and store nothing
+  const bool active = grp * 128 < ncols;  // blocks past a partial strip repeat block 0 and store nothing
   const int c_lo = (active ? grp * 128 : 0) + sub * 8;
+  // the lane stores the scale and zero of each group whose first channel it
+  // holds: run A's group when its run starts one, and (for groups under 128)
+  // run B's group, 64 channels further on
+  const bool lead = (sub % (GROUP / 8 < 8 ? GROUP / 8 : 8)) == 0;
   float2 sv[8];
   {
     float t[16];
@@ -493,7 +498,7 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT>())
 #pragma unroll
     for (int i = 0; i < 8; ++i) sv[i] = make_float2(t[2 * i], t[2 * i + 1]);
   }
-  const int kw = K >> 3, kg = K >> 7;
+  const int kw = K >> 3, kg = K / GROUP;
   int row = r_begin + warp;
   RowRegs<WT> nxt;
   if (row < r_end) nxt.load(W + (size_t)row * K + col0 + c_lo);
@@ -501,66 +506,77 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT>())
     float2 w[8];
     nxt.unpack(w);
     if (row + kPackWarps < r_end) nxt.load(W + (size_t)(row + kPackWarps) * K + col0 + c_lo);
-    float v[16];
+    float2 v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float2 p = __fmul2_rn(w[i], sv[i]);
-      v[2 * i] = p.x;
-      v[2 * i + 1] = p.y;
-    }
-    float mn, mx;
-    group_minmax16(v, mn, mx);
-    const GroupFast g = group_fast(mn, mx, qmax, floor_, symmetric != 0);
-    float k[16];
-    quant_codes_minus_z<16>(v, g, k);
+    for (int i = 0; i < 8; ++i) v[i] = __fmul2_rn(w[i], sv[i]);
+    GroupFast ga, gb;
+    lane_groups<GROUP>(v, qmax, floor_, symmetric != 0, ga, gb);
+    float2 k[8];
+    lane_codes_minus_z<GROUP>(v, ga, gb, k);
     // q = (q - z) + z in [0, 15]; 2^23 + q carries q in its low mantissa bits,
     // which avoids a float-to-integer conversion per code
-    const float2 zb = make_float2(8388608.0f + g.z, 8388608.0f + g.z);
+    const float2 za = make_float2(8388608.0f + ga.z, 8388608.0f + ga.z);
+    const float2 zb = make_float2(8388608.0f + gb.z, 8388608.0f + gb.z);
     uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const float2 a = __fadd2_rn(make_float2(k[e], k[e + 1]), zb);
-      const float2 b = __fadd2_rn(make_float2(k[8 + e], k[9 + e]), zb);
-      w0 |= ((__float_as_uint(a.x) & 0xFu) << (4 * e)) | ((__float_as_uint(a.y) & 0xFu) << (4 * e + 4));
-      w1 |= ((__float_as_uint(b.x) & 0xFu) << (4 * e)) | ((__float_as_uint(b.y) & 0xFu) << (4 * e + 4));
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = __fadd2_rn(k[i], za);
+      const float2 b = __fadd2_rn(k[4 + i], zb);
+      w0 |= ((__float_as_uint(a.x) & 0xFu) << (8 * i)) | ((__float_as_uint(a.y) & 0xFu) << (8 * i + 4));
+      w1 |= ((__float_as_uint(b.x) & 0xFu) << (8 * i)) | ((__float_as_uint(b.y) & 0xFu) << (8 * i + 4));
     }
     if (active) {
       int32_t* q = qweight + (size_t)row * kw + ((col0 + c_lo) >> 3);
       q[0] = (int32_t)w0;
       q[8] = (int32_t)w1;  // 64 channels further on
-      if (sub == 0) {
-        const size_t gi = (size_t)row * kg + ((col0 + grp * 128) >> 7);
-        scales[gi] = __half_as_ushort(__float2half_rn(g.delta));
-        zeros[gi] = __half_as_ushort(__float2half_rn(g.z));
+      if (lead) {
+        const size_t gi = (size_t)row * kg + (col0 + c_lo) / GROUP;
+        scales[gi] = __half_as_ushort(__float2half_rn(ga.delta));
+        zeros[gi] = __half_as_ushort(__float2half_rn(ga.z));
+        if (GROUP < 128) {
+          scales[gi + 64 / GROUP] = __half_as_ushort(__float2half_rn(gb.delta));
+          zeros[gi + 64 / GROUP] = __half_as_ushort(__float2half_rn(gb.z));
+        }
       }
     }
   }
 }
 
-template <typename WT>
+template <typename WT, int GROUP>
 cudaError_t launch_pack_t(const WT* W, int64_t N, int64_t K, const float* s, const awq_config& cfg,
                           int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
   int sms = 0;
   cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   const int nstrips = (int)((K + kFqCols - 1) / kFqCols);
-  int64_t rblocks = (int64_t)sms * pack_blocks_per_sm<WT>() / nstrips;
+  int64_t rblocks = (int64_t)sms * pack_blocks_per_sm<WT, GROUP>() / nstrips;
   if (rblocks < 1) rblocks = 1;
   if (rblocks > N) rblocks = N;
   const int rows_per_block = (int)((N + rblocks - 1) / rblocks);
   rblocks = (N + rows_per_block - 1) / rows_per_block;
   const float qmax = (float)((1 << cfg.w_bit) - 1);
-  pack_kernel<WT><<<(unsigned)(rblocks * nstrips), kPackWarps * 32, 0, st>>>(
+  pack_kernel<WT, GROUP><<<(unsigned)(rblocks * nstrips), kPackWarps * 32, 0, st>>>(
       W, (int)N, (int)K, s, qmax, cfg.delta_floor, cfg.zero_point == 0 ? 1 : 0, qweight, scales, zeros, nstrips,
       rows_per_block);
   return cudaGetLastError();
 }
 
+template <int GROUP>
+cudaError_t launch_pack_g(const void* W, int w_dtype, int64_t N, int64_t K, const float* s, const awq_config& cfg,
+                          int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
+  if (w_dtype == AWQ_BF16)
+    return launch_pack_t<uint16_t, GROUP>((const uint16_t*)W, N, K, s, cfg, qweight, scales, zeros, st);
+  return launch_pack_t<float, GROUP>((const float*)W, N, K, s, cfg, qweight, scales, zeros, st);
+}
+
 cudaError_t launch_pack(const void* W, int w_dtype, int64_t N, int64_t K, const float* s, const awq_config& cfg,
                         int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
-  if (w_dtype == AWQ_BF16)
-    return launch_pack_t<uint16_t>((const uint16_t*)W, N, K, s, cfg, qweight, scales, zeros, st);
-  return launch_pack_t<float>((const float*)W, N, K, s, cfg, qweight, scales, zeros, st);
+  switch (cfg.group) {
+    case 32: return launch_pack_g<32>(W, w_dtype, N, K, s, cfg, qweight, scales, zeros, st);
+    case 64: return launch_pack_g<64>(W, w_dtype, N, K, s, cfg, qweight, scales, zeros, st);
+    case 128: return launch_pack_g<128>(W, w_dtype, N, K, s, cfg, qweight, scales, zeros, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // ============================================================== loss + argmin

@@ -9,7 +9,7 @@
 
 namespace awq {
 
-constexpr int kGroup = 128;      // weights per quantisation group (only size built)
+constexpr int kBlockCols = 128;  // input channels of one 8-lane block of the quantiser kernels; `in` is a multiple
 constexpr int kMaxGrid = 64;     // largest alpha grid
 constexpr int kStatsRows = 128;  // tokens per statistics chunk
 
@@ -63,8 +63,9 @@ cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, i
                                 float* dump = nullptr, int skip_unit = -1);
 
 // y[m][r] = sum_k x[m][k] * (q[r][k] - z[r][g]) * scale[r][g] for m < M <= 8,
-// x bf16 [M][K] (staged as fp32 in shared memory: M * K * 4 bytes).
+// g = k / group (group 32, 64 or 128), x bf16 [M][K] (staged as fp32 in
+// shared memory: M * K * 4 bytes).
 cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int32_t* qweight, const uint16_t* scales,
-                              const uint16_t* zeros, int64_t N, float* y, cudaStream_t st);
+                              const uint16_t* zeros, int64_t N, int group, float* y, cudaStream_t st);
 
 }  // namespace awq

@@ -443,6 +443,7 @@ __device__ __forceinline__ void ldg_w16(const void* W, int w_bf16, size_t off, f
 // nothing else. (Holding the quantisers a fixed number of alphas ahead of
 // the products, so that each operand is written just before it is read,
 // measured no faster on the benchmark layers.)
+template <int GROUP>
 __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane) {
   const int grp = lane >> 3, sub = lane & 7;
   const int per_a = p.nt * p.nstrips;
@@ -475,7 +476,7 @@ __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane
         }
         if (r + 1 < r1) ldg_w16(p.W, p.w_bf16, (size_t)(r + 1) * p.K + c, wn);
         uint32_t o[8];
-        fq_lane16<false>(w, nw, RegLane{sv, iv}, p.qmax, p.floor_, p.symmetric != 0, o);
+        fq_lane16<false, GROUP>(w, nw, RegLane{sv, iv}, p.qmax, p.floor_, p.symmetric != 0, o);
         if (active) {
           uint4* dst = reinterpret_cast<uint4*>(p.op + (size_t)a * slot + (size_t)r * p.K + c);
           dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -499,7 +500,7 @@ constexpr int PAIR_SMEM_BYTES = kPairStages * PSTAGE_BYTES + 1024 + BAR_BYTES;
 constexpr uint32_t PAIR_IDESC = umma_idesc_bf16_f32(2 * BM, BN);
 static_assert(PAIR_SMEM_BYTES <= 232448, "shared memory per CTA");
 
-template <bool FUSED>
+template <bool FUSED, int GROUP = 128>
 __global__ void __launch_bounds__(FUSED ? kFusedThreads : NUM_THREADS, 1)
     search_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                             const Params p) {
@@ -690,7 +691,7 @@ __global__ void __launch_bounds__(FUSED ? kFusedThreads : NUM_THREADS, 1)
     }
   } else if (FUSED) {
     // -------------------------------------------------------------- quantiser warps (both CTAs)
-    quantise_units(p, warp - 6, lane);
+    quantise_units<GROUP>(p, warp - 6, lane);
   }
 
   tc_fence_before();
@@ -764,10 +765,10 @@ cudaError_t launch_residual(const CUtensorMap& tmX, const CUtensorMap& tmB, Para
   return cudaLaunchKernelEx(&lc, search_gemm_kernel<false, CM>, tmX, tmB, p);
 }
 
-template <bool FUSED>
+template <bool FUSED, int GROUP = 128>
 cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmB, const Params& p, int sms, cudaStream_t st) {
   constexpr int threads = FUSED ? kFusedThreads : NUM_THREADS;
-  cudaError_t e = ensure_dynamic_smem((const void*)search_gemm_pair_kernel<FUSED>, PAIR_SMEM_BYTES);
+  cudaError_t e = ensure_dynamic_smem((const void*)search_gemm_pair_kernel<FUSED, GROUP>, PAIR_SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[1];
@@ -783,14 +784,14 @@ cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmB, const Pa
   int pairs = sms / 2;
   lc.gridDim = dim3(2 * pairs);
   int active = 0;
-  e = cudaOccupancyMaxActiveClusters(&active, search_gemm_pair_kernel<FUSED>, &lc);
+  e = cudaOccupancyMaxActiveClusters(&active, search_gemm_pair_kernel<FUSED, GROUP>, &lc);
   if (e != cudaSuccess) return e;
   if (active > 0 && active < pairs) pairs = active;
   // The fused form keeps every pair even without search items of its own:
   // its quantiser warps serve the operand tiles of other pairs.
   if (!FUSED && pairs > p.items) pairs = p.items;
   lc.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&lc, search_gemm_pair_kernel<FUSED>, tmX, tmB, p);
+  return cudaLaunchKernelEx(&lc, search_gemm_pair_kernel<FUSED, GROUP>, tmX, tmB, p);
 }
 
 // Tensor maps and tiling of a search launch. CM: CTAs per cluster sharing an
@@ -895,7 +896,12 @@ cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, i
   p.skip_unit = skip_unit;
   e = cudaMemsetAsync(ready, 0, fused_ready_words(p.G, p.nt) * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  e = launch_pair<true>(tmX, tmB, p, sms, st);
+  switch (cfg.group) {
+    case 32: e = launch_pair<true, 32>(tmX, tmB, p, sms, st); break;
+    case 64: e = launch_pair<true, 64>(tmX, tmB, p, sms, st); break;
+    case 128: e = launch_pair<true, 128>(tmX, tmB, p, sms, st); break;
+    default: return cudaErrorInvalidValue;
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

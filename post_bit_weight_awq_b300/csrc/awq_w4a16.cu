@@ -7,7 +7,7 @@
 // The packed layer is streamed from HBM once; x (at most 8 tokens) is
 // converted to fp32 and staged in shared memory. One CTA of 16 warps per SM;
 // each warp owns R output rows at a time and each lane 4 / R chunks of 32
-// consecutive codes of each (16-byte loads, each inside one group of 128)
+// consecutive codes of each (16-byte loads, each inside one group)
 // per step, with the next step's loads in flight while the current one is
 // computed. Codes become floats without conversion
 // instructions: a byte permute places a nibble under the exponent bits of
@@ -62,7 +62,7 @@ struct W4Step {
 template <int R, int U>
 __device__ __forceinline__ void w4_load(W4Step<R, U>& st, const int32_t* __restrict__ qweight,
                                         const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros,
-                                        int r0, int N, int cbase, int chunks, int kw, int kg) {
+                                        int r0, int N, int cbase, int chunks, int kw, int kg, int gsh) {
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int r = r0 + i;
@@ -71,8 +71,8 @@ __device__ __forceinline__ void w4_load(W4Step<R, U>& st, const int32_t* __restr
       const int c = cbase + 32 * u;
       if (r < N && c < chunks) {
         st.q[i][u] = ld_stream_v4(qweight + (size_t)r * kw + 4 * c);
-        st.s[i][u] = scales[(size_t)r * kg + (c >> 2)];
-        st.z[i][u] = zeros[(size_t)r * kg + (c >> 2)];
+        st.s[i][u] = scales[(size_t)r * kg + (c >> gsh)];  // a chunk lies inside one group
+        st.z[i][u] = zeros[(size_t)r * kg + (c >> gsh)];
       }
     }
   }
@@ -106,7 +106,7 @@ __device__ __forceinline__ void w4_chunk(const uint4 q, float zf, const float* _
 template <int M, int R>
 __global__ void __launch_bounds__(kW4Threads, 1)
     w4a16_gemv_kernel(const uint16_t* __restrict__ x, int K, const int32_t* __restrict__ qweight,
-                      const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros, int N,
+                      const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros, int N, int gsh,
                       float* __restrict__ y) {
   constexpr int U = M > 4 ? 2 : 4 / R;  // fewer chunks in flight when many token accumulators need registers
   extern __shared__ float4 w4_smem[];
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   const int kp = (K >> 5) * kW4Pad;                // padded floats per token
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunks = K >> 5;  // 32-code chunks per row
-  const int kw = K >> 3, kg = K >> 7;
+  const int kw = K >> 3, kg = K >> (5 + gsh);  // groups of 32 << gsh codes
   const int steps_per_group = (chunks + 32 * U - 1) / (32 * U);
   const int gstride = gridDim.x * kW4Warps * R;
 
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   // first step's loads go out before x is staged, so their latency overlaps it.
   int r0 = (blockIdx.x * kW4Warps + warp) * R, k = 0;
   W4Step<R, U> cur, nxt;
-  if (r0 < N) w4_load<R, U>(cur, qweight, scales, zeros, r0, N, lane, chunks, kw, kg);
+  if (r0 < N) w4_load<R, U>(cur, qweight, scales, zeros, r0, N, lane, chunks, kw, kg, gsh);
 
   for (int i = threadIdx.x; i < M * K / 8; i += kW4Threads) {
     const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * 8);
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       nr = r0 + gstride;
       nk = 0;
     }
-    if (nr < N) w4_load<R, U>(nxt, qweight, scales, zeros, nr, N, nk * 32 * U + lane, chunks, kw, kg);
+    if (nr < N) w4_load<R, U>(nxt, qweight, scales, zeros, nr, N, nk * 32 * U + lane, chunks, kw, kg, gsh);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = k * 32 * U + lane + 32 * u;
@@ -185,19 +185,20 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 
 template <int M, int R>
 cudaError_t launch_w4_r(const uint16_t* x, int64_t K, const int32_t* qweight, const uint16_t* scales,
-                        const uint16_t* zeros, int64_t N, float* y, int sms, cudaStream_t st) {
+                        const uint16_t* zeros, int64_t N, int gsh, float* y, int sms, cudaStream_t st) {
   const int smem = (int)(M * (K / 32) * kW4Pad * 4);
   cudaError_t e = ensure_dynamic_smem((const void*)w4a16_gemv_kernel<M, R>, smem);
   if (e != cudaSuccess) return e;
   int64_t grid = (N + kW4Warps * R - 1) / (kW4Warps * R);
   if (grid > sms) grid = sms;
-  w4a16_gemv_kernel<M, R><<<(unsigned)grid, kW4Threads, smem, st>>>(x, (int)K, qweight, scales, zeros, (int)N, y);
+  w4a16_gemv_kernel<M, R><<<(unsigned)grid, kW4Threads, smem, st>>>(x, (int)K, qweight, scales, zeros, (int)N, gsh,
+                                                                    y);
   return cudaGetLastError();
 }
 
 template <int M>
 cudaError_t launch_w4_t(const uint16_t* x, int64_t K, const int32_t* qweight, const uint16_t* scales,
-                        const uint16_t* zeros, int64_t N, float* y, cudaStream_t st) {
+                        const uint16_t* zeros, int64_t N, int gsh, float* y, cudaStream_t st) {
   int sms = 0;
   cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
@@ -215,24 +216,28 @@ cudaError_t launch_w4_t(const uint16_t* x, int64_t K, const int32_t* qweight, co
       R = r;
     }
   }
-  if (R == 4) return launch_w4_r<M, (w4_max_rows<M>() >= 4 ? 4 : 1)>(x, K, qweight, scales, zeros, N, y, sms, st);
-  if (R == 2) return launch_w4_r<M, (w4_max_rows<M>() >= 2 ? 2 : 1)>(x, K, qweight, scales, zeros, N, y, sms, st);
-  return launch_w4_r<M, 1>(x, K, qweight, scales, zeros, N, y, sms, st);
+  if (R == 4)
+    return launch_w4_r<M, (w4_max_rows<M>() >= 4 ? 4 : 1)>(x, K, qweight, scales, zeros, N, gsh, y, sms, st);
+  if (R == 2)
+    return launch_w4_r<M, (w4_max_rows<M>() >= 2 ? 2 : 1)>(x, K, qweight, scales, zeros, N, gsh, y, sms, st);
+  return launch_w4_r<M, 1>(x, K, qweight, scales, zeros, N, gsh, y, sms, st);
 }
 
 }  // namespace
 
 cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int32_t* qweight, const uint16_t* scales,
-                              const uint16_t* zeros, int64_t N, float* y, cudaStream_t st) {
+                              const uint16_t* zeros, int64_t N, int group, float* y, cudaStream_t st) {
+  const int gsh = group == 32 ? 0 : (group == 64 ? 1 : (group == 128 ? 2 : -1));
+  if (gsh < 0) return cudaErrorInvalidValue;
   switch (M) {
-    case 1: return launch_w4_t<1>(x, K, qweight, scales, zeros, N, y, st);
-    case 2: return launch_w4_t<2>(x, K, qweight, scales, zeros, N, y, st);
-    case 3: return launch_w4_t<3>(x, K, qweight, scales, zeros, N, y, st);
-    case 4: return launch_w4_t<4>(x, K, qweight, scales, zeros, N, y, st);
-    case 5: return launch_w4_t<5>(x, K, qweight, scales, zeros, N, y, st);
-    case 6: return launch_w4_t<6>(x, K, qweight, scales, zeros, N, y, st);
-    case 7: return launch_w4_t<7>(x, K, qweight, scales, zeros, N, y, st);
-    case 8: return launch_w4_t<8>(x, K, qweight, scales, zeros, N, y, st);
+    case 1: return launch_w4_t<1>(x, K, qweight, scales, zeros, N, gsh, y, st);
+    case 2: return launch_w4_t<2>(x, K, qweight, scales, zeros, N, gsh, y, st);
+    case 3: return launch_w4_t<3>(x, K, qweight, scales, zeros, N, gsh, y, st);
+    case 4: return launch_w4_t<4>(x, K, qweight, scales, zeros, N, gsh, y, st);
+    case 5: return launch_w4_t<5>(x, K, qweight, scales, zeros, N, gsh, y, st);
+    case 6: return launch_w4_t<6>(x, K, qweight, scales, zeros, N, gsh, y, st);
+    case 7: return launch_w4_t<7>(x, K, qweight, scales, zeros, N, gsh, y, st);
+    case 8: return launch_w4_t<8>(x, K, qweight, scales, zeros, N, gsh, y, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -104,8 +104,12 @@ def test_host_validation_of_search_and_pack(lib):
     s = capi.awq_search_layer
     assert _status_of(s, A, B, C, cfg, D, D, D, 0, 0, ws_bytes=need, **kw) == capi.AWQ_ERR_INVALID_ARG
     assert _status_of(s, A, B, C, cfg, D, D, D, D, 0, ws_bytes=need - 1, **kw) == capi.AWQ_ERR_WORKSPACE
-    assert _status_of(s, A, B, C, capi.config(group=64), D, D, D, D, 0, ws_bytes=need, **kw) == \
-        capi.AWQ_ERR_UNSUPPORTED
+    # groups of 32, 64 and 128 and codes of 2 to 8 bits are built; others are refused before any launch
+    for bad in (dict(group=256), dict(group=16), dict(group=96), dict(w_bit=9), dict(w_bit=1)):
+        assert _status_of(s, A, B, C, capi.config(**bad), D, D, D, D, 0, ws_bytes=need, **kw) == \
+            capi.AWQ_ERR_UNSUPPORTED, bad
+    assert _status_of(s, A, B, C, capi.config(w_bit=0), D, D, D, D, 0, ws_bytes=need, **kw) == \
+        capi.AWQ_ERR_INVALID_ARG
     assert _status_of(s, A, B, C, capi.config(n_grid=65), D, D, D, D, 0, ws_bytes=need, **kw) == \
         capi.AWQ_ERR_INVALID_ARG
     assert _status_of(s, A, B, C, capi.config(zero_point=2), D, D, D, D, 0, ws_bytes=need, **kw) == \
@@ -120,7 +124,9 @@ def test_host_validation_of_search_and_pack(lib):
     assert _status_of(p, A, B, cfg, C, D, 0, 0, **pkw) == capi.AWQ_ERR_INVALID_ARG
     assert _status_of(p, A, B, cfg, C + 4, D, D, 0, **pkw) == capi.AWQ_ERR_MISALIGNED
     assert _status_of(p, A, B, cfg, C, D + 1, D, 0, **pkw) == capi.AWQ_ERR_MISALIGNED
-    assert _status_of(p, A, B, capi.config(w_bit=8), C, D, D, 0, **pkw) == capi.AWQ_ERR_UNSUPPORTED
+    # the packed format holds 4-bit codes only, at any of the built group sizes
+    for bad in (dict(w_bit=8), dict(w_bit=3), dict(w_bit=3, group=32), dict(group=256)):
+        assert _status_of(p, A, B, capi.config(**bad), C, D, D, 0, **pkw) == capi.AWQ_ERR_UNSUPPORTED, bad
     assert _status_of(p, A, B, cfg, C, D, D, 0, **{**pkw, "w_dtype": 3}) == capi.AWQ_ERR_INVALID_ARG
 
 
@@ -148,7 +154,8 @@ def test_host_validation_of_w4a16(lib):
     assert _status_of(f, A, B + 4, C, D, cfg, E, 0, **kw) == capi.AWQ_ERR_MISALIGNED
     assert _status_of(f, A, B, C + 1, D, cfg, E, 0, **kw) == capi.AWQ_ERR_MISALIGNED
     assert _status_of(f, A, B, C, D, cfg, E, 0, **{**kw, "in_features": 200}) == capi.AWQ_ERR_INVALID_ARG
-    assert _status_of(f, A, B, C, D, capi.config(group=64), E, 0, **kw) == capi.AWQ_ERR_UNSUPPORTED
+    for bad in (dict(group=256), dict(w_bit=2), dict(w_bit=8, group=64)):
+        assert _status_of(f, A, B, C, D, capi.config(**bad), E, 0, **kw) == capi.AWQ_ERR_UNSUPPORTED, bad
 
 
 def test_host_validation_of_block_search(lib):

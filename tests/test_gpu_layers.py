@@ -295,3 +295,27 @@ def test_symmetric_search_layer_levels():
     res = _oracle_losses(L["W"], L["X"], sx=sx32, zero_point=False)
     losses, best, s_best = _search_with_statistic(L, sx32, capi.config(zero_point=0))
     _check_levels(losses, best, res["losses"])
+
+
+@pytest.mark.parametrize("group,w_bit", [(64, 4), (32, 4), (128, 3), (64, 2)])
+def test_group_and_width_search_layer_levels(group, w_bit):
+    """The whole search with groups of 32/64 and 2- or 3-bit codes (fused kernel path), levels 2 and 3
+    against the oracle with the same quantiser; level 1 (the pack) for the 4-bit cases."""
+    L = workloads.make_layer("llama7b_q_proj", n_tok=512, out_features=640, in_features=1024, seed=group + w_bit)
+    sx32 = O.f32(O.channel_importance(L["X"]))
+    res = _oracle_losses(L["W"], L["X"], sx=sx32, group=group, w_bit=w_bit)
+    losses, best, s_best = _search_with_statistic(L, sx32, capi.config(group=group, w_bit=w_bit))
+    _check_levels(losses, best, res["losses"])
+    if w_bit == 4:
+        W = L["W"]
+        N, K = W.shape
+        s32 = O.f32(res["s_best"])
+        qw = torch.empty(N, K // 8, dtype=torch.int32, device="cuda")
+        sc = torch.empty(N, K // group, dtype=torch.float16, device="cuda")
+        zr = torch.empty(N, K // group, dtype=torch.float16, device="cuda")
+        capi.awq_quantize_pack(dev_weight(L), dev_f32(s32), capi.config(group=group), qw, sc, zr)
+        torch.cuda.synchronize()
+        ref = O.quantize_pack(W.astype(np.float64), s32, group=group)
+        np.testing.assert_array_equal(qw.cpu().numpy(), ref["qweight"])
+        np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint16), ref["scales"].view(np.uint16))
+        np.testing.assert_array_equal(zr.cpu().numpy().view(np.uint16), ref["zeros"].view(np.uint16))

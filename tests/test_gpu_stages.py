@@ -313,3 +313,82 @@ def test_symmetric_pack_and_fakequant_bit_exact(layer, kw):
         ref = W_hat - W64
         tol = 2.0**-8 * np.abs(ref) + 1e-6 * (np.abs(W64) + np.abs(W_hat)) + 1e-30
         assert not (np.abs(got[i] - ref) > tol).any(), f"alpha {i}"
+
+
+# ------------------------------------------------------------------ group sizes and code widths
+
+
+@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("zero_point", [1, 0])
+@pytest.mark.parametrize("w_dtype_layer,kw", [("tiny", {}),
+                                              ("llama7b_q_proj", dict(out_features=130, in_features=640, n_tok=64))])
+def test_finer_groups_pack_bit_exact(group, zero_point, w_dtype_layer, kw):
+    """Groups of 32 and 64: codes, fp16 scales and zeros equal the oracle's bit for bit (fp32 and bf16
+    weights, a partial 512-channel strip at in = 640)."""
+    L = workloads.make_layer(w_dtype_layer, **kw)
+    W, X = L["W"], L["X"]
+    N, K = W.shape
+    cfg = capi.config(group=group, zero_point=zero_point)
+    sx = O.channel_importance(X)
+    for alpha in (0.0, 0.5, 0.95):
+        s32 = O.f32(O.awq_scales(sx, alpha))
+        ref = O.quantize_pack(W.astype(np.float64), s32, group=group, zero_point=bool(zero_point))
+        qw = torch.empty(N, K // 8, dtype=torch.int32, device="cuda")
+        sc = torch.full((N, K // group), float("nan"), dtype=torch.float16, device="cuda")
+        zr = torch.full((N, K // group), float("nan"), dtype=torch.float16, device="cuda")
+        capi.awq_quantize_pack(dev_weight(L), dev_f32(s32), cfg, qw, sc, zr)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(qw.cpu().numpy(), ref["qweight"])
+        np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint16), ref["scales"].view(np.uint16))
+        np.testing.assert_array_equal(zr.cpu().numpy().view(np.uint16), ref["zeros"].view(np.uint16))
+
+
+@pytest.mark.parametrize("group,w_bit,zero_point", [(32, 4, 1), (64, 4, 1), (128, 3, 1), (64, 2, 1), (32, 8, 1),
+                                                    (128, 8, 0), (32, 3, 0)])
+def test_group_and_width_fakequant_values(group, w_bit, zero_point):
+    """The search operand for other group sizes and code widths, every alpha, against the oracle's
+    fake-quant with the same knobs (the tolerance of test_fakequant_codes_and_values)."""
+    L = workloads.make_layer("llama7b_q_proj", out_features=96, in_features=640, n_tok=128, seed=group + w_bit)
+    W, X = L["W"].astype(np.float64), L["X"]
+    N, K = W.shape
+    cfg = capi.config(group=group, w_bit=w_bit, zero_point=zero_point)
+    G = cfg.n_grid
+    s32, inv32 = _oracle_scales32(O.channel_importance(X), G)
+    op = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
+    capi.awq_fakequant(dev_weight(L), dev_f32(s32), dev_f32(inv32), cfg, op)
+    got = host_bf16_to_f64(op)
+    for i in range(G):
+        W_hat = O.fake_quantize(W, s32[i], w_bit=w_bit, group=group, zero_point=bool(zero_point))
+        ref = W_hat - W
+        tol = 2.0**-8 * np.abs(ref) + 1e-6 * (np.abs(W) + np.abs(W_hat)) + 1e-30
+        bad = np.abs(got[i] - ref) > tol
+        assert not bad.any(), f"alpha {i}: {bad.sum()} elements off"
+
+
+@pytest.mark.parametrize("group,w_bit,zero_point", [(32, 4, 1), (64, 3, 1), (64, 4, 0)])
+def test_fused_search_matches_separate_stages_other_quantisers(group, w_bit, zero_point):
+    """The fused kernel's quantiser warps with other group sizes and widths write the operand the
+    fake-quant kernel writes, bit for bit, and the partial sums are identical."""
+    L = workloads.make_layer("llama7b_q_proj", out_features=300, in_features=640, n_tok=257)
+    N, K = L["W"].shape
+    n = L["X"].shape[0]
+    W, X = dev_weight(L), dev_bf16(L["X"])
+    cfg = capi.config(group=group, w_bit=w_bit, zero_point=zero_point)
+    G = cfg.n_grid
+    s = torch.empty(G, K, dtype=torch.float32, device="cuda")
+    inv = torch.empty_like(s)
+    capi.awq_alpha_scales(dev_f32(O.f32(O.channel_importance(L["X"]))), cfg, s, inv)
+    op_ref = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
+    capi.awq_fakequant(W, s, inv, cfg, op_ref)
+    mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
+    p_ref = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    capi.awq_search_gemm(X, op_ref, cfg, p_ref, status, n_tok=n, in_features=K, out_features=N)
+    op = torch.full_like(op_ref, float("nan"))
+    parts = torch.full_like(p_ref, float("nan"))
+    ready = torch.zeros((G * (nt + 1) + 1,), dtype=torch.int32, device="cuda")
+    capi.awq_search_fused(W, X, s, inv, cfg, op, parts, ready, status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    assert torch.equal(op.view(torch.int16), op_ref.view(torch.int16))
+    assert torch.equal(parts, p_ref)

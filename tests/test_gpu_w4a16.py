@@ -30,19 +30,19 @@ def _bound(x, W_hat):
     return 64 * 2.0**-24 * (np.abs(x) @ np.abs(W_hat).T) + 1e-30
 
 
-def _random_packed(rng, N, K):
+def _random_packed(rng, N, K, group=128):
     W = (rng.standard_normal((N, K)) * 0.02).astype(np.float64)
     s = O.f32(rng.uniform(0.5, 2.0, K))
-    return O.quantize_pack(W, s)
+    return O.quantize_pack(W, s, group=group)
 
 
-def _run(x32, pk):
+def _run(x32, pk, group=128):
     M, K = x32.shape
     N = pk["qweight"].shape[0]
     y = torch.empty(M, N, dtype=torch.float32, device="cuda")
     capi.awq_w4a16_gemv(dev_bf16(x32), torch.from_numpy(pk["qweight"]).cuda(),
                         torch.from_numpy(pk["scales"].view(np.int16)).cuda(),
-                        torch.from_numpy(pk["zeros"].view(np.int16)).cuda(), capi.config(), y)
+                        torch.from_numpy(pk["zeros"].view(np.int16)).cuda(), capi.config(group=group), y)
     torch.cuda.synchronize()
     return y.cpu().numpy().astype(np.float64)
 
@@ -57,6 +57,21 @@ def test_w4a16_matches_oracle(M, N, K):
     ref = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"])
     W_hat = O.dequantize_groups(O.unpack_words(pk["qweight"], K), pk["scales"].astype(np.float64),
                                 pk["zeros"].astype(np.float64))
+    bad = np.abs(got - ref) > _bound(x, W_hat)
+    assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got - ref).max():.3e}"
+
+
+@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1024), (4, 130, 640), (8, 520, 4096), (1, 4096, 4096)])
+def test_w4a16_finer_groups_match_oracle(group, M, N, K):
+    """Groups of 32 and 64: one stored step and zero per 32 or 64 columns."""
+    rng = np.random.default_rng(group * 7 + M * 1000 + N + K)
+    pk = _random_packed(rng, N, K, group)
+    x = workloads.round_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32)).astype(np.float64)
+    got = _run(x.astype(np.float32), pk, group)
+    ref = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"], group=group)
+    W_hat = O.dequantize_groups(O.unpack_words(pk["qweight"], K), pk["scales"].astype(np.float64),
+                                pk["zeros"].astype(np.float64), group)
     bad = np.abs(got - ref) > _bound(x, W_hat)
     assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got - ref).max():.3e}"
 
