@@ -245,6 +245,46 @@ AWQ_API awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out
                              const float* s, const awq_config* cfg, int32_t* qweight,
                              uint16_t* scales_f16, uint16_t* zeros_f16, awq_stream_t stream);
 
+/* ---------------------------------------------------------------- layers from host memory */
+
+/* One layer of awq_quantize_layers. Pointers may be host or device memory
+   (unified addressing); host buffers should be pinned (cudaHostAlloc or
+   cudaHostRegister) for the copies to overlap the computation. */
+typedef struct {
+  const void* W;        /* [out][in], of the call's w_dtype */
+  const void* X;        /* bf16 [n_tok][in]: the layer's calibration activations */
+  int64_t n_tok, out, in;
+  int32_t* qweight;     /* out: [out][in/8], as awq_quantize_pack */
+  uint16_t* scales_f16; /* out: [out][in/group] */
+  uint16_t* zeros_f16;  /* out: [out][in/group] */
+  float* losses;        /* out: [n_grid] */
+  int32_t* best_idx;    /* out: [1] */
+  float* s_best;        /* out: [in] */
+  float* mean_abs;      /* out: [in], or NULL when not wanted */
+} awq_layer_io;
+
+/* Device bytes of the workspace awq_quantize_layers needs for layers of at
+   most these sizes. Host-only. */
+AWQ_API awq_status awq_pipeline_workspace_size(int64_t max_n_tok, int64_t max_out, int64_t max_in,
+                                               int32_t w_dtype, const awq_config* cfg, size_t* bytes);
+
+/* The whole method (statistics, alpha search, pack) for `count` layers
+   whose inputs and outputs are in host memory, the way a model is quantised
+   layer by layer. The workspace holds two slots of inputs and outputs: the
+   search of layer i runs on `stream` while layer i+1's W and X are copied in
+   and layer i-1's outputs are copied out on two library-owned copy streams,
+   so the host link and the GPU work overlap. Results are the same as those
+   of awq_act_stats, awq_search_layer and awq_quantize_pack called one layer
+   at a time. Asynchronous: the outputs are in place once `stream` has
+   passed this call (work queued on `stream` afterwards waits for the last
+   copy). cfg->w_bit must be 4. ws: device, awq_pipeline_workspace_size()
+   bytes for the largest layer dimensions; its first 4 bytes are the status
+   word, which keeps the first device-side error of any layer (read it with
+   awq_get_device_status). Calls from several host threads are serialised
+   while they enqueue. */
+AWQ_API awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_t w_dtype,
+                                       const awq_config* cfg, void* ws, size_t ws_bytes, awq_stream_t stream);
+
 /* ---------------------------------------------------------------- using the packed layer */
 
 /* Largest token count, and token count times `in`, that awq_w4a16_gemv

@@ -41,6 +41,8 @@ EXPORTED = (
     "awq_search_block",
     "awq_quantize_pack",
     "awq_w4a16_gemv",
+    "awq_pipeline_workspace_size",
+    "awq_quantize_layers",
     "awq_packed_bytes",
     "awq_get_device_status",
     "awq_alpha_scales",
@@ -66,6 +68,24 @@ class AwqConfig(ctypes.Structure):
         ("delta_floor", ctypes.c_float),
         ("loss_form", ctypes.c_int32),
         ("wait_timeout_ms", ctypes.c_uint32),
+    ]
+
+
+class AwqLayerIO(ctypes.Structure):
+    """One layer of awq_quantize_layers (host or device pointers)."""
+    _fields_ = [
+        ("W", ctypes.c_void_p),
+        ("X", ctypes.c_void_p),
+        ("n_tok", ctypes.c_int64),
+        ("out", ctypes.c_int64),
+        ("in_", ctypes.c_int64),
+        ("qweight", ctypes.c_void_p),
+        ("scales_f16", ctypes.c_void_p),
+        ("zeros_f16", ctypes.c_void_p),
+        ("losses", ctypes.c_void_p),
+        ("best_idx", ctypes.c_void_p),
+        ("s_best", ctypes.c_void_p),
+        ("mean_abs", ctypes.c_void_p),
     ]
 
 
@@ -105,6 +125,8 @@ def lib() -> ctypes.CDLL:
                                             _P]),
         "awq_quantize_pack": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _CFG, _P, _P, _P, _P]),
         "awq_w4a16_gemv": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _I64, _CFG, _P, _P]),
+        "awq_pipeline_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _I32, _CFG, ctypes.POINTER(_SZ)]),
+        "awq_quantize_layers": (ctypes.c_int, [_P, _I32, _I32, _CFG, _P, _SZ, _P]),
         "awq_packed_bytes": (_SZ, [_I64, _I64, _CFG]),
         "awq_get_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
         "awq_alpha_scales": (ctypes.c_int, [_P, _I64, _CFG, _P, _P, _P]),
@@ -269,6 +291,29 @@ def awq_search_block(Ws, X, mean_abs, cfg: AwqConfig, losses, best_idx, s_best, 
     _check(lib().awq_search_block(ctypes.cast(ptrs, _P), wd, ctypes.cast(arr, _P), len(outs), K, _ptr(X), xd, n,
                                   _ptr(mean_abs), ctypes.byref(cfg), _ptr(losses), _ptr(best_idx), _ptr(s_best),
                                   _ptr(ws), wb, _stream(stream)), "awq_search_block")
+
+
+def awq_pipeline_workspace_size(max_n_tok: int, max_out: int, max_in: int, w_dtype: int, cfg: AwqConfig) -> int:
+    n = _SZ(0)
+    _check(lib().awq_pipeline_workspace_size(max_n_tok, max_out, max_in, w_dtype, ctypes.byref(cfg),
+                                             ctypes.byref(n)), "awq_pipeline_workspace_size")
+    return n.value
+
+
+def layer_io(W, X, qweight, scales, zeros, losses, best_idx, s_best, mean_abs=None, *, n_tok=None, out=None,
+             in_features=None) -> AwqLayerIO:
+    """An AwqLayerIO from tensors (host or device) or raw pointers with the sizes given."""
+    return AwqLayerIO(_ptr(W), _ptr(X), X.shape[0] if n_tok is None else n_tok, W.shape[0] if out is None else out,
+                      W.shape[1] if in_features is None else in_features, _ptr(qweight), _ptr(scales), _ptr(zeros),
+                      _ptr(losses), _ptr(best_idx), _ptr(s_best), _ptr(mean_abs))
+
+
+def awq_quantize_layers(layers, w_dtype: int, cfg: AwqConfig, ws, stream=None, *, ws_bytes=None) -> None:
+    """layers: sequence of AwqLayerIO (see ``layer_io``)."""
+    arr = (AwqLayerIO * len(layers))(*layers)
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check(lib().awq_quantize_layers(ctypes.cast(arr, _P), len(layers), w_dtype, ctypes.byref(cfg), _ptr(ws), wb,
+                                     _stream(stream)), "awq_quantize_layers")
 
 
 def awq_quantize_pack(W, s, cfg: AwqConfig, qweight, scales, zeros, stream=None, *, out_features=None,

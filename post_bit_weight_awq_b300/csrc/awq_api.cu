@@ -3,6 +3,8 @@
 // carving, and the launch sequence of each step.
 #include <string.h>
 
+#include <mutex>
+
 #include "awq.h"
 #include "awq_launch.h"
 
@@ -99,7 +101,101 @@ SearchLayout search_layout(int64_t n_tok, int64_t out, int64_t in, const awq_con
 
 awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X, int64_t n_tok,
                       const float* mean_abs, const awq_config& c, float* losses, int32_t* best_idx, float* s_best,
-                      uint8_t* base, const SearchLayout& L, cudaStream_t s);
+                      uint8_t* base, const SearchLayout& L, cudaStream_t s, bool clear_status = true);
+
+
+// ------------------------------------------------------------- host-buffer layer pipeline
+//
+// Layers whose weights and activations sit in host memory go through two
+// device slots: layer i's statistics, search and pack run on the caller's
+// stream in slot i % 2 while layer i+1's inputs are copied into the other
+// slot on a copy-in stream and layer i-1's outputs are copied out of it on
+// a copy-out stream (the link is full duplex). Events order each slot's
+// copy-in after the previous copy-out of that slot (which follows its
+// compute), the compute after the copy-in, and the copy-out after the
+// compute. The search workspace and the statistics scratch are shared by
+// all layers, which run one after another on the caller's stream.
+
+struct PipeLayout {
+  size_t search, stats;  // offsets: search workspace (status word first), statistics scratch
+  size_t slot[2];        // offsets of the two slots
+  size_t W, X, mean_abs, qweight, scales, zeros, losses, best, s_best;  // offsets inside a slot
+  size_t total;
+};
+
+PipeLayout pipe_layout(int64_t n_tok, int64_t out, int64_t in, int32_t w_dtype, const awq_config& cfg) {
+  PipeLayout P;
+  const size_t wbytes = w_dtype == AWQ_BF16 ? 2 : 4;
+  size_t off = 0;
+  P.search = off;
+  off = align_up(off + search_layout(n_tok, out, in, cfg).total, kAlign);
+  P.stats = off;
+  size_t stats_bytes = 0;
+  awq_act_stats_workspace_size(n_tok, in, &stats_bytes);
+  off = align_up(off + stats_bytes, kAlign);
+  size_t o = 0;
+  P.W = o;
+  o = align_up(o + (size_t)out * in * wbytes, kAlign);
+  P.X = o;
+  o = align_up(o + (size_t)n_tok * in * 2, kAlign);
+  P.mean_abs = o;
+  o = align_up(o + (size_t)in * 4, kAlign);
+  P.qweight = o;
+  o = align_up(o + (size_t)out * in / 2, kAlign);
+  P.scales = o;
+  o = align_up(o + (size_t)out * (in / cfg.group) * 2, kAlign);
+  P.zeros = o;
+  o = align_up(o + (size_t)out * (in / cfg.group) * 2, kAlign);
+  P.losses = o;
+  o = align_up(o + (size_t)cfg.n_grid * 4, kAlign);
+  P.best = o;
+  o = align_up(o + 4, kAlign);
+  P.s_best = o;
+  o = align_up(o + (size_t)in * 4, kAlign);
+  P.slot[0] = off;
+  P.slot[1] = off + o;
+  P.total = off + 2 * o;
+  return P;
+}
+
+// Copy streams and events of the pipeline, created once per device. The
+// mutex is held while a call enqueues its work, so two host threads never
+// interleave their event records on the shared streams.
+struct PipeRes {
+  bool ready = false;
+  cudaStream_t in_s = nullptr, out_s = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t in_ev[2] = {}, comp_ev[2] = {}, out_ev[2] = {};
+};
+constexpr int kPipeDevices = 64;
+std::mutex g_pipe_mu;
+PipeRes g_pipe[kPipeDevices];
+
+cudaError_t pipe_resources(int dev, PipeRes** out) {
+  if (dev < 0 || dev >= kPipeDevices) return cudaErrorInvalidDevice;
+  PipeRes& r = g_pipe[dev];
+  if (!r.ready) {
+    cudaError_t e = cudaStreamCreateWithFlags(&r.in_s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&r.out_s, cudaStreamNonBlocking);
+    cudaEvent_t* evs[8] = {&r.start, &r.done, &r.in_ev[0], &r.in_ev[1], &r.comp_ev[0], &r.comp_ev[1],
+                           &r.out_ev[0], &r.out_ev[1]};
+    for (int i = 0; i < 8 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+    r.ready = true;
+  }
+  *out = &r;
+  return cudaSuccess;
+}
+
+awq_status check_layer_io(const awq_layer_io& L, const awq_config& cfg) {
+  if (L.W == nullptr || L.X == nullptr || L.qweight == nullptr || L.scales_f16 == nullptr ||
+      L.zeros_f16 == nullptr || L.losses == nullptr || L.best_idx == nullptr || L.s_best == nullptr)
+    return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_dims(L.n_tok, L.out, L.in);
+  if (st != AWQ_OK) return st;
+  if (L.in % cfg.group != 0) return AWQ_ERR_INVALID_ARG;
+  return AWQ_OK;
+}
 
 }  // namespace
 
@@ -385,7 +481,7 @@ namespace {
 
 awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X, int64_t n_tok,
                       const float* mean_abs, const awq_config& c, float* losses, int32_t* best_idx, float* s_best,
-                      uint8_t* base, const SearchLayout& L, cudaStream_t s) {
+                      uint8_t* base, const SearchLayout& L, cudaStream_t s, bool clear_status) {
   const awq_config* cfg = &c;
   uint32_t* status = (uint32_t*)(base + L.status);
   float* sc = (float*)(base + L.s);
@@ -395,7 +491,7 @@ awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, c
 
   uint32_t* ready = (uint32_t*)(base + L.ready);
 
-  cudaError_t e = cudaMemsetAsync(status, 0, 4, s);
+  cudaError_t e = clear_status ? cudaMemsetAsync(status, 0, 4, s) : cudaSuccess;
   if (e == cudaSuccess) e = launch_alpha_scales(mean_abs, in, *cfg, sc, inv, s);
   const double flops = 2.0 * cfg->n_grid * (double)n_tok * (double)out * (double)in;
   if (cfg->loss_form == AWQ_LOSS_RESIDUAL && flops < kLargeSearchFlops) {
@@ -479,6 +575,110 @@ awq_status awq_get_device_status(const void* ws, awq_stream_t stream, awq_status
   if (e != cudaSuccess) return AWQ_ERR_CUDA;
   *status = (awq_status)word;
   return AWQ_OK;
+}
+
+awq_status awq_pipeline_workspace_size(int64_t max_n_tok, int64_t max_out, int64_t max_in, int32_t w_dtype,
+                                       const awq_config* cfg, size_t* bytes) {
+  if (bytes == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_packed_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_wdtype(w_dtype);
+  if (st != AWQ_OK) return st;
+  st = check_dims(max_n_tok, max_out, max_in);
+  if (st != AWQ_OK) return st;
+  *bytes = pipe_layout(max_n_tok, max_out, max_in, w_dtype, *cfg).total;
+  return AWQ_OK;
+}
+
+awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_t w_dtype, const awq_config* cfg,
+                               void* ws, size_t ws_bytes, awq_stream_t stream) {
+  if (layers == nullptr || count < 1 || ws == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_packed_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_wdtype(w_dtype);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(ws)) return AWQ_ERR_MISALIGNED;
+  int64_t n_max = 1, out_max = 1, in_max = 1;
+  for (int32_t i = 0; i < count; ++i) {
+    st = check_layer_io(layers[i], *cfg);
+    if (st != AWQ_OK) return st;
+    n_max = layers[i].n_tok > n_max ? layers[i].n_tok : n_max;
+    out_max = layers[i].out > out_max ? layers[i].out : out_max;
+    in_max = layers[i].in > in_max ? layers[i].in : in_max;
+  }
+  // every region of the layout grows with each dimension, so the layout of
+  // the largest dimensions holds every layer at the same offsets
+  const PipeLayout P = pipe_layout(n_max, out_max, in_max, w_dtype, *cfg);
+  if (ws_bytes < P.total) return AWQ_ERR_WORKSPACE;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AWQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  PipeRes* R = nullptr;
+  if (pipe_resources(dev, &R) != cudaSuccess) return AWQ_ERR_CUDA;
+  const cudaStream_t cs = (cudaStream_t)stream;
+  uint8_t* base = (uint8_t*)ws;
+  const size_t wbytes = w_dtype == AWQ_BF16 ? 2 : 4;
+  // the copy streams start after the work already queued on the caller's
+  // stream (which may still use this workspace); the status word is
+  // cleared once, so it keeps the first error of any layer
+  cudaError_t e = cudaMemsetAsync(base + P.search, 0, 4, cs);
+  if (e == cudaSuccess) e = cudaEventRecord(R->start, cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(R->in_s, R->start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(R->out_s, R->start, 0);
+  for (int32_t i = 0; i < count && e == cudaSuccess; ++i) {
+    const awq_layer_io& L = layers[i];
+    const int b = i & 1;
+    uint8_t* slot = base + P.slot[b];
+    const size_t gcols = (size_t)(L.in / cfg->group);
+    // copy-in: after the previous copy-out of this slot (two layers back)
+    if (i >= 2) e = cudaStreamWaitEvent(R->in_s, R->out_ev[b], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(slot + P.W, L.W, (size_t)L.out * L.in * wbytes, cudaMemcpyDefault, R->in_s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(slot + P.X, L.X, (size_t)L.n_tok * L.in * 2, cudaMemcpyDefault, R->in_s);
+    if (e == cudaSuccess) e = cudaEventRecord(R->in_ev[b], R->in_s);
+    // compute on the caller's stream
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, R->in_ev[b], 0);
+    float* mean_abs = (float*)(slot + P.mean_abs);
+    float* s_best = (float*)(slot + P.s_best);
+    if (e == cudaSuccess) {
+      uint8_t* sws = base + P.stats;
+      e = launch_stats((const uint16_t*)(slot + P.X), L.n_tok, L.in, (float*)sws,
+                       (uint32_t*)(sws + stats_ticket_offset(L.n_tok, L.in)), mean_abs, cs);
+    }
+    if (e == cudaSuccess) {
+      const SearchLayout SL = search_layout(L.n_tok, L.out, L.in, *cfg);
+      st = run_search(slot + P.W, w_dtype, L.out, L.in, slot + P.X, L.n_tok, mean_abs, *cfg,
+                      (float*)(slot + P.losses), (int32_t*)(slot + P.best), s_best, base + P.search, SL, cs,
+                      /*clear_status=*/false);
+      if (st != AWQ_OK) return st;
+    }
+    if (e == cudaSuccess)
+      e = launch_pack(slot + P.W, w_dtype, L.out, L.in, s_best, *cfg, (int32_t*)(slot + P.qweight),
+                      (uint16_t*)(slot + P.scales), (uint16_t*)(slot + P.zeros), cs);
+    if (e == cudaSuccess) e = cudaEventRecord(R->comp_ev[b], cs);
+    // copy-out
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(R->out_s, R->comp_ev[b], 0);
+    const struct {
+      void* dst;
+      size_t off, bytes;
+    } outs[6] = {{L.qweight, P.qweight, (size_t)L.out * L.in / 2},
+                 {L.scales_f16, P.scales, (size_t)L.out * gcols * 2},
+                 {L.zeros_f16, P.zeros, (size_t)L.out * gcols * 2},
+                 {L.losses, P.losses, (size_t)cfg->n_grid * 4},
+                 {L.best_idx, P.best, 4},
+                 {L.s_best, P.s_best, (size_t)L.in * 4}};
+    for (int k = 0; k < 6 && e == cudaSuccess; ++k)
+      e = cudaMemcpyAsync(outs[k].dst, slot + outs[k].off, outs[k].bytes, cudaMemcpyDefault, R->out_s);
+    if (e == cudaSuccess && L.mean_abs != nullptr)
+      e = cudaMemcpyAsync(L.mean_abs, mean_abs, (size_t)L.in * 4, cudaMemcpyDefault, R->out_s);
+    if (e == cudaSuccess) e = cudaEventRecord(R->out_ev[b], R->out_s);
+  }
+  // the caller's stream continues once the last outputs have arrived
+  if (e == cudaSuccess) e = cudaEventRecord(R->done, R->out_s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, R->done, 0);
+  return from_cuda(e);
 }
 
 }  // extern "C"

@@ -177,3 +177,37 @@ def test_host_validation_of_block_search(lib):
     assert _status_of(f, [A, A + 8], B, C, cfg, D, D, D, D, 0, **kw) == capi.AWQ_ERR_MISALIGNED
     assert _status_of(f, [A, A], B, C, cfg, D, D, D, D, 0, **{**kw, "ws_bytes": 1024}) == capi.AWQ_ERR_WORKSPACE
     assert _status_of(f, [A, A], B, C, cfg, D, D, D, D, 0, **{**kw, "outs": [64, 0]}) == capi.AWQ_ERR_INVALID_ARG
+
+
+def test_host_validation_of_layer_pipeline(lib):
+    cfg = capi.config()
+    need = capi.awq_pipeline_workspace_size(128, 256, 512, capi.AWQ_BF16, cfg)
+    # two slots of inputs and outputs on top of the search workspace and the statistics scratch
+    slot = 256 * 512 * 2 + 128 * 512 * 2 + 256 * 512 // 2 + 2 * 256 * 4 * 2 + 2 * 512 * 4
+    assert need >= capi.awq_workspace_size(128, 256, 512, cfg) + 2 * slot
+    assert capi.awq_pipeline_workspace_size(128, 256, 512, capi.AWQ_FP32, cfg) > need
+    with pytest.raises(capi.AwqError) as e:
+        capi.awq_pipeline_workspace_size(128, 256, 512, capi.AWQ_BF16, capi.config(w_bit=3))
+    assert e.value.status == capi.AWQ_ERR_UNSUPPORTED
+    A = 0x10000
+    io = capi.AwqLayerIO(A, A, 128, 256, 512, A, A, A, A, A, A, 0)
+    f = capi.lib().awq_quantize_layers
+
+    def call(layers, count, w_dtype=capi.AWQ_BF16, c=cfg, ws=0x100000, ws_bytes=need):
+        arr = (capi.AwqLayerIO * max(1, len(layers)))(*layers)
+        return f(ctypes.cast(arr, ctypes.c_void_p) if layers else None, count, w_dtype, ctypes.byref(c), ws,
+                 ws_bytes, None)
+
+    assert call([], 0) == capi.AWQ_ERR_INVALID_ARG
+    assert call([io], 0) == capi.AWQ_ERR_INVALID_ARG
+    assert call([io], 1, ws=0) == capi.AWQ_ERR_INVALID_ARG
+    assert call([io], 1, ws=0x100004) == capi.AWQ_ERR_MISALIGNED
+    assert call([io], 1, ws_bytes=need - 1) == capi.AWQ_ERR_WORKSPACE
+    assert call([io], 1, c=capi.config(w_bit=8)) == capi.AWQ_ERR_UNSUPPORTED
+    assert call([io], 1, w_dtype=7) == capi.AWQ_ERR_INVALID_ARG
+    bad = capi.AwqLayerIO(A, A, 128, 256, 200, A, A, A, A, A, A, 0)  # in not a multiple of 128
+    assert call([io, bad], 2) == capi.AWQ_ERR_INVALID_ARG
+    null = capi.AwqLayerIO(A, A, 128, 256, 512, 0, A, A, A, A, A, 0)
+    assert call([io, null], 2) == capi.AWQ_ERR_INVALID_ARG
+    big = capi.AwqLayerIO(A, A, 129, 256, 512, A, A, A, A, A, A, 0)  # more tokens than the workspace was sized for
+    assert call([io, big], 2) == capi.AWQ_ERR_WORKSPACE
