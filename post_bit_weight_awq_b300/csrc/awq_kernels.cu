@@ -47,7 +47,7 @@ __device__ __forceinline__ void acc_abs_bf16x8(float (&a)[8], const uint4& v) {
   a[7] += fabsf(bf16_hi(v.w));
 }
 
-__global__ void __launch_bounds__(256) stats_kernel(const uint16_t* __restrict__ X, int n, int K,
+__global__ void __launch_bounds__(256, 4) stats_kernel(const uint16_t* __restrict__ X, int n, int K,
                                                     float* __restrict__ partials, uint32_t* __restrict__ tickets,
                                                     float* __restrict__ mean_abs) {
   __shared__ float red[8][256 + 8];
@@ -85,16 +85,16 @@ __global__ void __launch_bounds__(256) stats_kernel(const uint16_t* __restrict__
   if (!last || c >= K) return;
   __threadfence();
   // compensated (Neumaier) fp32 sum over the chunks, fixed order; the other
-  // blocks' partials are read past L1
-  // (loads issued 8 chunks at a time, so the L2 round trips overlap)
+  // blocks' partials are read past L1, 32 chunks' loads in flight at a time
+  // (one L2 round trip for up to 4096 tokens)
   const int chunks = (int)gridDim.y;
   float s = 0.0f, comp = 0.0f;
-  for (int i0 = 0; i0 < chunks; i0 += 8) {
-    float xb[8];
+  for (int i0 = 0; i0 < chunks; i0 += 32) {
+    float xb[32];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) xb[u] = i0 + u < chunks ? __ldcg(partials + (size_t)(i0 + u) * K + c) : 0.0f;
+    for (int u = 0; u < 32; ++u) xb[u] = i0 + u < chunks ? __ldcg(partials + (size_t)(i0 + u) * K + c) : 0.0f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 32; ++u) {
       if (i0 + u >= chunks) break;
       const float x = xb[u];
       const float v = __fadd_rn(s, x);
@@ -122,79 +122,75 @@ cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partial
 // Saves 4-bit LLMs", search_scale listing; "AWQ > Summary", "The scaling
 // formula"), alpha_i = i / n_grid, then optionally s_i /= sqrt(max(s_i) *
 // min(s_i)). The scale decides the codes, so it is formed in fp64 and rounded
-// to fp32 once. Since alpha_i = i / n_grid, b^alpha_i = (b^(1/n_grid))^i: one
-// pow per channel, then fp64 products (the products drift from a direct pow
-// by at most ~n_grid fp64 ulps, which changes the fp32-rounded scale only
-// when it lies that close to an fp32 rounding boundary). x^alpha is
-// non-decreasing in x, so max(s_i) and min(s_i) are the powers of the
-// largest and smallest clamped statistic.
+// to fp32 once. x^alpha is non-decreasing in x, so max(s_i) and min(s_i) are
+// the powers of the largest and smallest clamped statistic, hi and lo, and
+//   s_i = b^(i/G) / (hi^(i/G) lo^(i/G))^(1/2) = (b / sqrt(hi lo))^(i/G):
+// one fp64 pow per channel gives the root r = (b / sqrt(hi lo))^(1/G), and
+// s_i = r^i follows by fp64 products (they drift from a direct pow by at most
+// ~n_grid fp64 ulps, which changes the fp32-rounded scale only when it lies
+// that close to an fp32 rounding boundary). alpha = 0 gives s = 1 exactly.
 // fp64 runs at 1/64 of the fp32 rate on this GPU, so the kernel is a chain of
-// fp64 latencies; it keeps the chains short and parallel: 32 channels per
-// block of two warps. Both warps find the statistic's max/min (16-byte loads,
-// fixed-order reduction); then warp 0 forms 1 / sqrt(max * min) per alpha
-// while warp 1 forms each channel's root b^(1/n_grid); then warp w writes the
-// alphas of parity w for the 32 channels, stepping by root^2. alpha = 0 gives
-// s = 1 exactly.
+// fp64 latencies kept short: 64 channels per block, one thread per channel.
+// Every block finds the statistic's max/min itself (16-byte loads, fixed
+// order), which costs one 4-byte read per channel from L2.
 
-constexpr int kAlphaChannels = 32;
+constexpr int kAlphaChannels = 64;
 
-__global__ void __launch_bounds__(64) alpha_scales_kernel(const float* __restrict__ mean_abs, int K, int G,
-                                                          double clamp_min, int normalize,
-                                                          float* __restrict__ s_out, float* __restrict__ inv_out) {
+__global__ void __launch_bounds__(kAlphaChannels) alpha_scales_kernel(const float* __restrict__ mean_abs, int K,
+                                                                      int G, double clamp_min, int normalize,
+                                                                      float* __restrict__ s_out,
+                                                                      float* __restrict__ inv_out) {
   __shared__ float smax[2], smin[2];
-  __shared__ double inv_norm[kMaxGrid];
-  __shared__ double root_sh[kAlphaChannels];
+  const int j = blockIdx.x * kAlphaChannels + threadIdx.x;
+  const float bj = j < K ? mean_abs[j] : 1.0f;  // in flight during the reduction
   float mx = -INFINITY, mn = INFINITY;
-  const float4* m4 = reinterpret_cast<const float4*>(mean_abs);
-  const int K4 = K >> 2;  // K is a multiple of 128
+  if (normalize) {
+    const float4* m4 = reinterpret_cast<const float4*>(mean_abs);
+    const int K4 = K >> 2;  // K is a multiple of 128
 #pragma unroll 4
-  for (int j = threadIdx.x; j < K4; j += 64) {
-    const float4 v = m4[j];
-    mx = fmax3f(mx, fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-    mn = fmin3f(mn, fminf(v.x, v.y), fminf(v.z, v.w));
-  }
+    for (int q = threadIdx.x; q < K4; q += kAlphaChannels) {
+      const float4 v = m4[q];
+      mx = fmax3f(mx, fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+      mn = fmin3f(mn, fminf(v.x, v.y), fminf(v.z, v.w));
+    }
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    for (int o = 16; o; o >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+      smax[warp] = mx;
+      smin[warp] = mn;
+    }
+    __syncthreads();
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    smax[warp] = mx;
-    smin[warp] = mn;
-  }
-  __syncthreads();
-  const int j = blockIdx.x * kAlphaChannels + lane;
-  if (warp == 0) {
+  if (j >= K) return;
+  double base = fmax((double)bj, clamp_min);
+  if (normalize) {
     const double lo = fmax((double)fminf(smin[0], smin[1]), clamp_min);
     const double hi = fmax((double)fmaxf(smax[0], smax[1]), clamp_min);
-    for (int i = lane; i < G; i += 32) {
-      double c = 1.0;
-      if (normalize) {
-        const double alpha = (double)i / (double)G;
-        c = sqrt(pow(hi, alpha) * pow(lo, alpha));
-      }
-      inv_norm[i] = 1.0 / c;
-    }
-  } else {
-    root_sh[lane] = j < K ? pow(fmax((double)mean_abs[j], clamp_min), 1.0 / (double)G) : 1.0;
+    base /= sqrt(hi * lo);
   }
-  __syncthreads();
-  if (j >= K) return;
-  const double root = root_sh[lane];
+  const double root = pow(base, 1.0 / (double)G);
   const double step = root * root;
-  double p = warp == 0 ? 1.0 : root;  // b^(i/G) for i = warp, warp + 2, ...
-  for (int i = warp; i < G; i += 2) {
-    const float s32 = (float)(p * inv_norm[i]);
-    s_out[(size_t)i * K + j] = s32;
-    inv_out[(size_t)i * K + j] = __fdiv_rn(1.0f, s32);
-    p *= step;
+  double p[2] = {1.0, root};  // root^i for the even and the odd i: two independent product chains
+  for (int i = 0; i < G; i += 2) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (i + u < G) {
+        const float s32 = (float)p[u];
+        s_out[(size_t)(i + u) * K + j] = s32;
+        inv_out[(size_t)(i + u) * K + j] = __fdiv_rn(1.0f, s32);
+      }
+      p[u] *= step;
+    }
   }
 }
 
 cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_config& cfg, float* s,
                                 float* inv_s, cudaStream_t st) {
-  alpha_scales_kernel<<<(unsigned)((K + kAlphaChannels - 1) / kAlphaChannels), 64, 0, st>>>(
+  alpha_scales_kernel<<<(unsigned)((K + kAlphaChannels - 1) / kAlphaChannels), kAlphaChannels, 0, st>>>(
       mean_abs, (int)K, cfg.n_grid, (double)cfg.sx_clamp_min, cfg.normalize, s, inv_s);
   return cudaGetLastError();
 }
