@@ -285,6 +285,24 @@ AWQ_API awq_status awq_pipeline_workspace_size(int64_t max_n_tok, int64_t max_ou
 AWQ_API awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_t w_dtype,
                                        const awq_config* cfg, void* ws, size_t ws_bytes, awq_stream_t stream);
 
+/* ---------------------------------------------------------------- checked builds */
+
+/* The library can be built with every global-memory access of its bandwidth
+   kernels, quantiser warps, search epilogue and decode product preceded by a
+   bounds check against the buffer's extent as the call's shapes define it
+   (python -m post_bit_weight_awq_b300.build --checked, which writes
+   libawq_checked.so next to libawq.so). A failed check is counted and its
+   access skipped, so an indexing error shows up as a count instead of a
+   memory fault. awq_bounds_report returns the number of failed checks since
+   the previous report and, for the first recorded one, the source unit
+   (1 awq_kernels.cu, 2 awq_search_gemm.cu, 3 awq_w4a16.cu; 0 if none), line
+   and element offset, then clears the records; it synchronises the device.
+   awq_bounds_selftest launches one check that fails by construction (the
+   element one past `buf[0..n)`; nothing is written). Both return
+   AWQ_ERR_UNSUPPORTED from the release library. */
+AWQ_API awq_status awq_bounds_report(uint64_t* failures, int32_t* unit, uint64_t* line, uint64_t* offset);
+AWQ_API awq_status awq_bounds_selftest(float* buf, int32_t n, awq_stream_t stream);
+
 /* ---------------------------------------------------------------- using the packed layer */
 
 /* Largest token count, and token count times `in`, that awq_w4a16_gemv

@@ -1,9 +1,12 @@
 """Build libawq.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-Usage: python -m post_bit_weight_awq_b300.build [--force] [--verbose]
+Usage: python -m post_bit_weight_awq_b300.build [--force] [--verbose] [--checked]
 
 The library links the CUDA runtime statically, so it loads on a machine with
-no GPU (symbol checks) and needs only the driver at run time.
+no GPU (symbol checks) and needs only the driver at run time. --checked builds
+libawq_checked.so instead: the same sources with AWQ_CHECKED defined, which
+puts a bounds check in front of the kernels' global-memory accesses (a failed
+check is counted and the access skipped; awq_bounds_report reads the count).
 """
 from __future__ import annotations
 
@@ -20,6 +23,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libawq.so")
 BUILD_DIR = os.path.join(PKG, "_build")
+CHECKED_LIB = os.path.join(PKG, "libawq_checked.so")
+CHECKED_BUILD_DIR = os.path.join(PKG, "_build_checked")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [
@@ -50,34 +55,38 @@ def headers():
                   + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in sources() + headers() + [__file__])
 
 
-def build(force: bool = False, verbose: bool = False, extra=None) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=None, checked: bool = False) -> str:
+    lib = CHECKED_LIB if checked else LIB
+    build_dir = CHECKED_BUILD_DIR if checked else BUILD_DIR
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        if checked:
+            cmd[1:1] = ["-DAWQ_CHECKED"]
         if extra:
             cmd[1:1] = list(extra)
         if verbose:
             print(" ".join(cmd), flush=True)
         subprocess.run(cmd, check=True)
         objs.append(obj)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None):
@@ -85,9 +94,10 @@ def main(argv=None):
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-info", action="store_true", help="print registers/spills per kernel")
+    ap.add_argument("--checked", action="store_true", help="build libawq_checked.so (bounds-checked kernels)")
     a = ap.parse_args(argv)
     extra = ["-Xptxas", "-v"] if a.ptxas_info else None
-    path = build(force=a.force or a.ptxas_info, verbose=a.verbose, extra=extra)
+    path = build(force=a.force or a.ptxas_info, verbose=a.verbose, extra=extra, checked=a.checked)
     print(path)
 
 

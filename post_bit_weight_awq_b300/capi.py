@@ -11,7 +11,8 @@ import ctypes
 import os
 from typing import Optional
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libawq.so")
+# AWQ_LIBRARY selects another build of the library (libawq_checked.so, the bounds-checked kernels).
+LIB_PATH = os.environ.get("AWQ_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "libawq.so")
 
 AWQ_OK = 0
 AWQ_ERR_INVALID_ARG = 1
@@ -44,6 +45,8 @@ EXPORTED = (
     "awq_pipeline_workspace_size",
     "awq_quantize_layers",
     "awq_packed_bytes",
+    "awq_bounds_report",
+    "awq_bounds_selftest",
     "awq_get_device_status",
     "awq_alpha_scales",
     "awq_fakequant",
@@ -128,6 +131,9 @@ def lib() -> ctypes.CDLL:
         "awq_pipeline_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _I32, _CFG, ctypes.POINTER(_SZ)]),
         "awq_quantize_layers": (ctypes.c_int, [_P, _I32, _I32, _CFG, _P, _SZ, _P]),
         "awq_packed_bytes": (_SZ, [_I64, _I64, _CFG]),
+        "awq_bounds_report": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_I32),
+                                             ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
+        "awq_bounds_selftest": (ctypes.c_int, [_P, _I32, _P]),
         "awq_get_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
         "awq_alpha_scales": (ctypes.c_int, [_P, _I64, _CFG, _P, _P, _P]),
         "awq_fakequant": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _CFG, _P, _P]),
@@ -291,6 +297,19 @@ def awq_search_block(Ws, X, mean_abs, cfg: AwqConfig, losses, best_idx, s_best, 
     _check(lib().awq_search_block(ctypes.cast(ptrs, _P), wd, ctypes.cast(arr, _P), len(outs), K, _ptr(X), xd, n,
                                   _ptr(mean_abs), ctypes.byref(cfg), _ptr(losses), _ptr(best_idx), _ptr(s_best),
                                   _ptr(ws), wb, _stream(stream)), "awq_search_block")
+
+
+def awq_bounds_report():
+    """(failed checks, source unit, line, offset) of a checked build; raises AwqError from a release build."""
+    f, u, ln, off = ctypes.c_uint64(0), _I32(0), ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(lib().awq_bounds_report(ctypes.byref(f), ctypes.byref(u), ctypes.byref(ln), ctypes.byref(off)),
+           "awq_bounds_report")
+    return f.value, u.value, ln.value, off.value
+
+
+def awq_bounds_selftest(buf, stream=None, *, n=None) -> None:
+    _check(lib().awq_bounds_selftest(_ptr(buf), buf.numel() if n is None else n, _stream(stream)),
+           "awq_bounds_selftest")
 
 
 def awq_pipeline_workspace_size(max_n_tok: int, max_out: int, max_in: int, w_dtype: int, cfg: AwqConfig) -> int:

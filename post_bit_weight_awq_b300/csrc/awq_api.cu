@@ -7,6 +7,7 @@
 
 #include "awq.h"
 #include "awq_launch.h"
+#include "awq_trace.h"
 
 using namespace awq;
 
@@ -241,6 +242,7 @@ awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_t* bytes
 
 awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, int64_t in, float* mean_abs, void* ws,
                          size_t ws_bytes, awq_stream_t stream) {
+  AWQ_TRACE("awq_act_stats");
   if (X == nullptr || mean_abs == nullptr || ws == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_xdtype(x_dtype);
   if (st != AWQ_OK) return st;
@@ -278,6 +280,7 @@ awq_status awq_search_tiles(int64_t n_tok, int64_t out, const awq_config* cfg, i
 
 awq_status awq_alpha_scales(const float* mean_abs, int64_t in, const awq_config* cfg, float* s, float* inv_s,
                             awq_stream_t stream) {
+  AWQ_TRACE("awq_alpha_scales");
   if (mean_abs == nullptr || s == nullptr || inv_s == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
@@ -288,6 +291,7 @@ awq_status awq_alpha_scales(const float* mean_abs, int64_t in, const awq_config*
 
 awq_status awq_fakequant(const void* W, int32_t w_dtype, int64_t out, int64_t in, const float* s,
                          const float* inv_s, const awq_config* cfg, uint16_t* op, awq_stream_t stream) {
+  AWQ_TRACE("awq_fakequant");
   if (W == nullptr || s == nullptr || inv_s == nullptr || op == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
@@ -301,6 +305,7 @@ awq_status awq_fakequant(const void* W, int32_t w_dtype, int64_t out, int64_t in
 
 awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, const uint16_t* op, int64_t out,
                            const awq_config* cfg, float* partials, uint32_t* status, awq_stream_t stream) {
+  AWQ_TRACE("awq_search_gemm");
   if (X == nullptr || op == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
@@ -314,6 +319,7 @@ awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, const uint1
 awq_status awq_search_fused(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X, int64_t n_tok,
                             const float* s, const float* inv_s, const awq_config* cfg, uint16_t* op, float* partials,
                             uint32_t* ready, uint32_t* status, awq_stream_t stream) {
+  AWQ_TRACE("awq_search_fused");
   if (W == nullptr || X == nullptr || s == nullptr || inv_s == nullptr || op == nullptr || partials == nullptr ||
       ready == nullptr || status == nullptr)
     return AWQ_ERR_INVALID_ARG;
@@ -335,6 +341,7 @@ awq_status awq_search_fused_withhold_unit(const void* W, int32_t w_dtype, int64_
                                           int64_t n_tok, const float* s, const float* inv_s, const awq_config* cfg,
                                           uint16_t* op, float* partials, uint32_t* ready, uint32_t* status,
                                           awq_stream_t stream) {
+  AWQ_TRACE("awq_search_fused_withhold_unit");
   if (W == nullptr || X == nullptr || s == nullptr || inv_s == nullptr || op == nullptr || partials == nullptr ||
       ready == nullptr || status == nullptr)
     return AWQ_ERR_INVALID_ARG;
@@ -355,6 +362,7 @@ awq_status awq_search_fused_withhold_unit(const void* W, int32_t w_dtype, int64_
 awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op, int64_t out,
                                 const awq_config* cfg, float* partials, uint32_t* status, float* dump,
                                 int32_t cluster_m, awq_stream_t stream) {
+  AWQ_TRACE("awq_search_gemm_dump");
   if (cluster_m != 0 && cluster_m != 1 && cluster_m != 2 && cluster_m != 4) return AWQ_ERR_INVALID_ARG;
   if (cfg != nullptr && cfg->loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
   if (X == nullptr || op == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
@@ -371,6 +379,7 @@ awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const 
 awq_status awq_search_gemm_withhold_fill(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
                                          int64_t out, const awq_config* cfg, float* partials, uint32_t* status,
                                          awq_stream_t stream) {
+  AWQ_TRACE("awq_search_gemm_withhold_fill");
   if (X == nullptr || op == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
@@ -384,6 +393,7 @@ awq_status awq_search_gemm_withhold_fill(const void* X, int64_t n_tok, int64_t i
 awq_status awq_loss_select(const float* partials, int64_t n_tok, int64_t out, int64_t in, const float* s,
                            const awq_config* cfg, float* losses, int32_t* best_idx, float* s_best,
                            uint32_t* status, awq_stream_t stream) {
+  AWQ_TRACE("awq_loss_select");
   if (partials == nullptr || s == nullptr || losses == nullptr || best_idx == nullptr || s_best == nullptr ||
       status == nullptr)
     return AWQ_ERR_INVALID_ARG;
@@ -401,6 +411,7 @@ awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t
                             int32_t x_dtype, int64_t n_tok, const float* mean_abs, const awq_config* cfg,
                             float* losses, int32_t* best_idx, float* s_best, void* ws, size_t ws_bytes,
                             awq_stream_t stream) {
+  AWQ_TRACE("awq_search_layer");
   if (W == nullptr || X == nullptr || mean_abs == nullptr || losses == nullptr || best_idx == nullptr ||
       s_best == nullptr || ws == nullptr)
     return AWQ_ERR_INVALID_ARG;
@@ -444,6 +455,7 @@ awq_status awq_search_block(const void* const* W_list, int32_t w_dtype, const in
                             int64_t in, const void* X, int32_t x_dtype, int64_t n_tok, const float* mean_abs,
                             const awq_config* cfg, float* losses, int32_t* best_idx, float* s_best, void* ws,
                             size_t ws_bytes, awq_stream_t stream) {
+  AWQ_TRACE("awq_search_block");
   if (W_list == nullptr || X == nullptr || mean_abs == nullptr || losses == nullptr || best_idx == nullptr ||
       s_best == nullptr || ws == nullptr)
     return AWQ_ERR_INVALID_ARG;
@@ -522,6 +534,7 @@ extern "C" {
 awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out, int64_t in, const float* s,
                              const awq_config* cfg, int32_t* qweight, uint16_t* scales_f16, uint16_t* zeros_f16,
                              awq_stream_t stream) {
+  AWQ_TRACE("awq_quantize_pack");
   if (W == nullptr || s == nullptr || qweight == nullptr || scales_f16 == nullptr || zeros_f16 == nullptr)
     return AWQ_ERR_INVALID_ARG;
   awq_status st = check_packed_cfg(cfg);
@@ -540,6 +553,7 @@ awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out, int64_
 awq_status awq_w4a16_gemv(const void* x, int32_t x_dtype, int64_t n_tok, int64_t in, const int32_t* qweight,
                           const uint16_t* scales_f16, const uint16_t* zeros_f16, int64_t out, const awq_config* cfg,
                           float* y, awq_stream_t stream) {
+  AWQ_TRACE("awq_w4a16_gemv");
   if (x == nullptr || qweight == nullptr || scales_f16 == nullptr || zeros_f16 == nullptr || y == nullptr)
     return AWQ_ERR_INVALID_ARG;
   awq_status st = check_packed_cfg(cfg);
@@ -592,6 +606,7 @@ awq_status awq_pipeline_workspace_size(int64_t max_n_tok, int64_t max_out, int64
 
 awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_t w_dtype, const awq_config* cfg,
                                void* ws, size_t ws_bytes, awq_stream_t stream) {
+  AWQ_TRACE("awq_quantize_layers");
   if (layers == nullptr || count < 1 || ws == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_packed_cfg(cfg);
   if (st != AWQ_OK) return st;
@@ -679,6 +694,40 @@ awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_
   if (e == cudaSuccess) e = cudaEventRecord(R->done, R->out_s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, R->done, 0);
   return from_cuda(e);
+}
+
+awq_status awq_bounds_report(uint64_t* failures, int32_t* unit, uint64_t* line, uint64_t* offset) {
+  if (failures == nullptr || unit == nullptr || line == nullptr || offset == nullptr) return AWQ_ERR_INVALID_ARG;
+#ifdef AWQ_CHECKED
+  cudaError_t (*const take[3])(unsigned long long*) = {take_oob_kernels, take_oob_search, take_oob_w4a16};
+  *failures = 0;
+  *unit = 0;
+  *line = 0;
+  *offset = 0;
+  for (int u = 0; u < 3; ++u) {
+    unsigned long long rec[3] = {0, 0, 0};
+    if (take[u](rec) != cudaSuccess) return AWQ_ERR_CUDA;
+    if (rec[0] != 0 && *unit == 0) {
+      *unit = u + 1;
+      *line = rec[1];
+      *offset = rec[2];
+    }
+    *failures += rec[0];
+  }
+  return AWQ_OK;
+#else
+  return AWQ_ERR_UNSUPPORTED;
+#endif
+}
+
+awq_status awq_bounds_selftest(float* buf, int32_t n, awq_stream_t stream) {
+  if (buf == nullptr || n < 1) return AWQ_ERR_INVALID_ARG;
+#ifdef AWQ_CHECKED
+  return from_cuda(launch_bounds_selftest(buf, n, (cudaStream_t)stream));
+#else
+  (void)stream;
+  return AWQ_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // extern "C"

@@ -25,6 +25,48 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// ----------------------------------------------------------------- checked builds
+//
+// With AWQ_CHECKED defined (the library built by build.py --checked as
+// libawq_checked.so), every global-memory access of the bandwidth kernels,
+// the quantiser warps, the search epilogue and the decode product is
+// preceded by a check that the accessed elements [off, off + len) lie inside
+// the buffer's logical extent n (taken from the call's shapes). A failed
+// check counts itself, keeps the source line and offset of the first
+// failure, and skips the access: an index bug shows up as a count, not as a
+// fault. The records live per translation unit; awq_bounds_report collects
+// them. Release builds compile every check to `true`.
+#ifdef AWQ_CHECKED
+namespace {
+__device__ unsigned long long g_oob_count;
+__device__ unsigned long long g_oob_first;  // source line << 40 | offset (low 40 bits)
+
+__device__ __noinline__ bool checked_in_bounds(size_t off, size_t len, size_t n, int line) {
+  if (off <= n && len <= n - off) return true;
+  if (atomicAdd(&g_oob_count, 1ull) == 0ull)
+    atomicExch(&g_oob_first, ((unsigned long long)line << 40) | (off & ((1ull << 40) - 1)));
+  return false;
+}
+}  // namespace
+#define AWQ_IN(off, len, n) ::awq::checked_in_bounds((size_t)(off), (size_t)(len), (size_t)(n), __LINE__)
+
+// This translation unit's record (count, first line, first offset), then zeroed.
+static inline cudaError_t take_oob_record(unsigned long long* out) {
+  unsigned long long c = 0, f = 0, zero = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&c, g_oob_count, sizeof(c));
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&f, g_oob_first, sizeof(f));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_oob_count, &zero, sizeof(zero));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_oob_first, &zero, sizeof(zero));
+  out[0] = c;
+  out[1] = f >> 40;
+  out[2] = f & ((1ull << 40) - 1);
+  return e;
+}
+#else
+#define AWQ_IN(off, len, n) true
+#endif
+
 // ----------------------------------------------------------------- status
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t code) {

@@ -62,11 +62,15 @@ __global__ void __launch_bounds__(256, 4) stats_kernel(const uint16_t* __restric
     for (; r + 56 < r1; r += 64) {  // 8 rows' loads in flight per thread
       uint4 v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = ld_nc_v4(X + (size_t)(r + 8 * u) * K + col);
+      for (int u = 0; u < 8; ++u) {
+        const size_t off = (size_t)(r + 8 * u) * K + col;
+        v[u] = AWQ_IN(off, 8, (size_t)n * K) ? ld_nc_v4(X + off) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
       for (int u = 0; u < 8; ++u) acc_abs_bf16x8(a, v[u]);
     }
-    for (; r < r1; r += 8) acc_abs_bf16x8(a, ld_nc_v4(X + (size_t)r * K + col));
+    for (; r < r1; r += 8)
+      if (AWQ_IN((size_t)r * K + col, 8, (size_t)n * K)) acc_abs_bf16x8(a, ld_nc_v4(X + (size_t)r * K + col));
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) red[ty][tx * 8 + i] = a[i];
@@ -76,7 +80,7 @@ __global__ void __launch_bounds__(256, 4) stats_kernel(const uint16_t* __restric
 #pragma unroll
   for (int y = 0; y < 8; ++y) sum += red[y][t];
   const int c = blockIdx.x * 256 + t;
-  if (c < K) partials[(size_t)blockIdx.y * K + c] = sum;
+  if (c < K && AWQ_IN((size_t)blockIdx.y * K + c, 1, (size_t)gridDim.y * K)) partials[(size_t)blockIdx.y * K + c] = sum;
   // publish this chunk, then find out whether it was the strip's last one
   __threadfence();
   __syncthreads();
@@ -92,7 +96,10 @@ __global__ void __launch_bounds__(256, 4) stats_kernel(const uint16_t* __restric
   for (int i0 = 0; i0 < chunks; i0 += 32) {
     float xb[32];
 #pragma unroll
-    for (int u = 0; u < 32; ++u) xb[u] = i0 + u < chunks ? __ldcg(partials + (size_t)(i0 + u) * K + c) : 0.0f;
+    for (int u = 0; u < 32; ++u)
+      xb[u] = i0 + u < chunks && AWQ_IN((size_t)(i0 + u) * K + c, 1, (size_t)chunks * K)
+                  ? __ldcg(partials + (size_t)(i0 + u) * K + c)
+                  : 0.0f;
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       if (i0 + u >= chunks) break;
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(256, 4) stats_kernel(const uint16_t* __restric
       s = v;
     }
   }
-  mean_abs[c] = (float)(((double)s + (double)comp) / (double)n);
+  if (AWQ_IN(c, 1, K)) mean_abs[c] = (float)(((double)s + (double)comp) / (double)n);
 }
 
 cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partials, uint32_t* tickets,
@@ -142,14 +149,14 @@ __global__ void __launch_bounds__(kAlphaChannels) alpha_scales_kernel(const floa
                                                                       float* __restrict__ inv_out) {
   __shared__ float smax[2], smin[2];
   const int j = blockIdx.x * kAlphaChannels + threadIdx.x;
-  const float bj = j < K ? mean_abs[j] : 1.0f;  // in flight during the reduction
+  const float bj = j < K && AWQ_IN(j, 1, K) ? mean_abs[j] : 1.0f;  // in flight during the reduction
   float mx = -INFINITY, mn = INFINITY;
   if (normalize) {
     const float4* m4 = reinterpret_cast<const float4*>(mean_abs);
     const int K4 = K >> 2;  // K is a multiple of 128
 #pragma unroll 4
     for (int q = threadIdx.x; q < K4; q += kAlphaChannels) {
-      const float4 v = m4[q];
+      const float4 v = AWQ_IN(4 * (size_t)q, 4, K) ? m4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
       mx = fmax3f(mx, fmaxf(v.x, v.y), fmaxf(v.z, v.w));
       mn = fmin3f(mn, fminf(v.x, v.y), fminf(v.z, v.w));
     }
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(kAlphaChannels) alpha_scales_kernel(const floa
   for (int i = 0; i < G; i += 2) {
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      if (i + u < G) {
+      if (i + u < G && AWQ_IN((size_t)(i + u) * K + j, 1, (size_t)G * K)) {
         const float s32 = (float)p[u];
         s_out[(size_t)(i + u) * K + j] = s32;
         inv_out[(size_t)(i + u) * K + j] = __fdiv_rn(1.0f, s32);
@@ -367,20 +374,23 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
       const int ln = (c >> 7) * 8 + (h >> 3);
       const int q = (e >> 6) * 2 + ((h & 7) >> 2);
       const size_t g = (size_t)(a0 + a) * K + col0 + c;
-      ss[(a * 4 + q) * 32 + ln] = *reinterpret_cast<const float4*>(s + g);
-      si[(a * 4 + q) * 32 + ln] = *reinterpret_cast<const float4*>(inv_s + g);
+      const bool ok = AWQ_IN(g, 4, (size_t)G * K);
+      ss[(a * 4 + q) * 32 + ln] = ok ? *reinterpret_cast<const float4*>(s + g) : make_float4(1.f, 1.f, 1.f, 1.f);
+      si[(a * 4 + q) * 32 + ln] = ok ? *reinterpret_cast<const float4*>(inv_s + g) : make_float4(1.f, 1.f, 1.f, 1.f);
     }
     __syncthreads();
 
     int row = r_begin + warp;
-    RowRegs<WT> nxt;
-    if (row < r_end) nxt.load(W + (size_t)row * K + col0 + c_lo);
+    RowRegs<WT> nxt{};
+    const size_t wn = (size_t)N * K;  // elements of W and of one operand slot
+    if (row < r_end && AWQ_IN((size_t)row * K + col0 + c_lo, 72, wn)) nxt.load(W + (size_t)row * K + col0 + c_lo);
     for (; row < r_end; row += kFqWarps) {
       float2 w[8];
       nxt.unpack(w);
       const size_t base = (size_t)row * K + col0 + c_lo;
-      if (row + kFqWarps < r_end) nxt.load(W + base + (size_t)kFqWarps * K);
-      if (REF && a0 == 0 && active) {
+      if (row + kFqWarps < r_end && AWQ_IN(base + (size_t)kFqWarps * K, 72, wn))
+        nxt.load(W + base + (size_t)kFqWarps * K);
+      if (REF && a0 == 0 && active && AWQ_IN((size_t)G * slot_elems + base, 72, (size_t)(G + 1) * wn)) {
         uint4* dst = reinterpret_cast<uint4*>(op + (size_t)G * slot_elems + base);
         dst[0] = make_uint4(pack_bf16x2(w[0]), pack_bf16x2(w[1]), pack_bf16x2(w[2]), pack_bf16x2(w[3]));
         dst[8] = make_uint4(pack_bf16x2(w[4]), pack_bf16x2(w[5]), pack_bf16x2(w[6]), pack_bf16x2(w[7]));
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
       for (int a = 0; a < gc; ++a) {
         uint32_t o[8];
         fq_lane16<REF, GROUP>(w, nw, SmemLane{ss + a * 128, si + a * 128, slane}, qmax, floor_, symmetric != 0, o);
-        if (active) {
+        if (active && AWQ_IN((size_t)(a0 + a) * slot_elems + base, 72, (size_t)(REF ? G + 1 : G) * wn)) {
           uint4* dst = reinterpret_cast<uint4*>(op + (size_t)(a0 + a) * slot_elems + base);
           dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
           dst[8] = make_uint4(o[4], o[5], o[6], o[7]);  // 64 channels further on
@@ -488,20 +498,24 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>
   const bool lead = (sub % (GROUP / 8 < 8 ? GROUP / 8 : 8)) == 0;
   float2 sv[8];
   {
-    float t[16];
-    load8f(s + col0 + c_lo, t);
-    load8f(s + col0 + c_lo + 64, t + 8);
+    float t[16] = {};
+    if (AWQ_IN(col0 + c_lo, 72, K)) {
+      load8f(s + col0 + c_lo, t);
+      load8f(s + col0 + c_lo + 64, t + 8);
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) sv[i] = make_float2(t[2 * i], t[2 * i + 1]);
   }
   const int kw = K >> 3, kg = K / GROUP;
+  const size_t wn = (size_t)N * K;
   int row = r_begin + warp;
-  RowRegs<WT> nxt;
-  if (row < r_end) nxt.load(W + (size_t)row * K + col0 + c_lo);
+  RowRegs<WT> nxt{};
+  if (row < r_end && AWQ_IN((size_t)row * K + col0 + c_lo, 72, wn)) nxt.load(W + (size_t)row * K + col0 + c_lo);
   for (; row < r_end; row += kPackWarps) {
     float2 w[8];
     nxt.unpack(w);
-    if (row + kPackWarps < r_end) nxt.load(W + (size_t)(row + kPackWarps) * K + col0 + c_lo);
+    if (row + kPackWarps < r_end && AWQ_IN((size_t)(row + kPackWarps) * K + col0 + c_lo, 72, wn))
+      nxt.load(W + (size_t)(row + kPackWarps) * K + col0 + c_lo);
     float2 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = __fmul2_rn(w[i], sv[i]);
@@ -521,12 +535,12 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>
       w0 |= ((__float_as_uint(a.x) & 0xFu) << (8 * i)) | ((__float_as_uint(a.y) & 0xFu) << (8 * i + 4));
       w1 |= ((__float_as_uint(b.x) & 0xFu) << (8 * i)) | ((__float_as_uint(b.y) & 0xFu) << (8 * i + 4));
     }
-    if (active) {
+    if (active && AWQ_IN((size_t)row * kw + ((col0 + c_lo) >> 3), 9, (size_t)N * kw)) {
       int32_t* q = qweight + (size_t)row * kw + ((col0 + c_lo) >> 3);
       q[0] = (int32_t)w0;
       q[8] = (int32_t)w1;  // 64 channels further on
-      if (lead) {
-        const size_t gi = (size_t)row * kg + (col0 + c_lo) / GROUP;
+      const size_t gi = (size_t)row * kg + (col0 + c_lo) / GROUP;
+      if (lead && AWQ_IN(gi, GROUP < 128 ? 64 / GROUP + 1 : 1, (size_t)N * kg)) {
         scales[gi] = __half_as_ushort(__float2half_rn(ga.delta));
         zeros[gi] = __half_as_ushort(__float2half_rn(ga.z));
         if (GROUP < 128) {
@@ -591,7 +605,8 @@ __global__ void __launch_bounds__(256) loss_reduce_kernel(const float* __restric
   const int a = blockIdx.x;
   const float* p = partials + (size_t)a * per_alpha;
   float acc = 0.0f;
-  for (int64_t t = threadIdx.x; t < per_alpha; t += blockDim.x) acc += p[t];
+  for (int64_t t = threadIdx.x; t < per_alpha; t += blockDim.x)
+    if (AWQ_IN((size_t)a * per_alpha + t, 1, (size_t)gridDim.x * per_alpha)) acc += p[t];
   double d = (double)acc;
 #pragma unroll
   for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
@@ -626,7 +641,7 @@ __global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ l
   }
   __syncthreads();
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j < K) s_best[j] = s[(size_t)best_sh * K + j];
+  if (j < K && AWQ_IN((size_t)best_sh * K + j, 1, (size_t)G * K)) s_best[j] = s[(size_t)best_sh * K + j];
 }
 
 cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, int64_t n_tok, int64_t N,
@@ -636,5 +651,20 @@ cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, 
   select_kernel<<<(unsigned)((K + 255) / 256), 256, 0, st>>>(losses, G, s, (int)K, best_idx, s_best);
   return cudaGetLastError();
 }
+
+#ifdef AWQ_CHECKED
+cudaError_t take_oob_kernels(unsigned long long* out) { return take_oob_record(out); }
+
+// One check that fails by construction, the offset one past an n-element
+// buffer: it is counted and the write is skipped (the buffer stays intact).
+__global__ void bounds_selftest_kernel(float* buf, int n) {
+  if (threadIdx.x == 0 && AWQ_IN(n, 1, n)) buf[n] = 1.0f;
+}
+
+cudaError_t launch_bounds_selftest(float* buf, int n, cudaStream_t st) {
+  bounds_selftest_kernel<<<1, 32, 0, st>>>(buf, n);
+  return cudaGetLastError();
+}
+#endif
 
 }  // namespace awq

@@ -68,4 +68,13 @@ cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, i
 cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int32_t* qweight, const uint16_t* scales,
                               const uint16_t* zeros, int64_t N, int group, float* y, cudaStream_t st);
 
+#ifdef AWQ_CHECKED
+// Checked builds: each kernel translation unit's record of failed bounds
+// checks (count, first source line, first offset), read and zeroed.
+cudaError_t take_oob_kernels(unsigned long long* out);
+cudaError_t take_oob_search(unsigned long long* out);
+cudaError_t take_oob_w4a16(unsigned long long* out);
+cudaError_t launch_bounds_selftest(float* buf, int n, cudaStream_t st);
+#endif
+
 }  // namespace awq

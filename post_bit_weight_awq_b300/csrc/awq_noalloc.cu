@@ -23,6 +23,7 @@
 
 #include "awq.h"
 #include "awq_launch.h"
+#include "awq_trace.h"
 
 namespace {
 
@@ -54,6 +55,7 @@ awq_status scratch_on_current_device(float** out) {
 
 extern "C" awq_status awq_act_stats_noalloc(const void* X, int32_t x_dtype, int64_t n_tok, int64_t in,
                                             float* mean_abs, awq_stream_t stream) {
+  AWQ_TRACE("awq_act_stats_noalloc");
   if (X == nullptr || mean_abs == nullptr) return AWQ_ERR_INVALID_ARG;
   if (x_dtype == AWQ_FP32) return AWQ_ERR_UNSUPPORTED;
   if (x_dtype != AWQ_BF16) return AWQ_ERR_INVALID_ARG;

@@ -308,7 +308,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (row < p.n_tok)
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                  if (col0 + i < p.N)
+                  if (col0 + i < p.N &&
+                      AWQ_IN(((size_t)a * p.n_tok + row) * p.N + col0 + i, 1, (size_t)p.G * p.n_tok * p.N))
                     p.dump[((size_t)a * p.n_tok + row) * p.N + col0 + i] = __uint_as_float(v[i]);
             }
           }
@@ -320,7 +321,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         const int alpha = REF ? pass - 1 : a;
-        if (lane == 0 && mb < p.mt) p.partials[((((size_t)alpha * p.mt + mb) * p.nt + nb) << 2) + q] = ss;
+        if (lane == 0 && mb < p.mt &&
+            AWQ_IN((((size_t)alpha * p.mt + mb) * p.nt + nb) * 4 + q, 1, (size_t)p.G * p.mt * p.nt * 4))
+          p.partials[((((size_t)alpha * p.mt + mb) * p.nt + nb) << 2) + q] = ss;
       }
       if (REF && ok) {
         tc_fence_before();
@@ -462,11 +465,14 @@ __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane
     const int r0 = nb * BN + fw * 32;
     const int r1 = min(r0 + 32, p.N);
     if (r0 < r1) {
-      float2 sv[8], iv[8];
-      ldg_lane16(p.s + (size_t)a * p.K + c, sv);
-      ldg_lane16(p.inv_s + (size_t)a * p.K + c, iv);
-      float2 wn[8];
-      ldg_w16(p.W, p.w_bf16, (size_t)r0 * p.K + c, wn);
+      float2 sv[8] = {}, iv[8] = {};
+      if (AWQ_IN((size_t)a * p.K + c, 72, (size_t)p.G * p.K)) {
+        ldg_lane16(p.s + (size_t)a * p.K + c, sv);
+        ldg_lane16(p.inv_s + (size_t)a * p.K + c, iv);
+      }
+      const size_t wn_elems = (size_t)p.N * p.K;
+      float2 wn[8] = {};
+      if (AWQ_IN((size_t)r0 * p.K + c, 72, wn_elems)) ldg_w16(p.W, p.w_bf16, (size_t)r0 * p.K + c, wn);
       for (int r = r0; r < r1; ++r) {
         float2 w[8], nw[8];
 #pragma unroll
@@ -474,10 +480,11 @@ __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane
           w[i] = wn[i];
           nw[i] = make_float2(-w[i].x, -w[i].y);
         }
-        if (r + 1 < r1) ldg_w16(p.W, p.w_bf16, (size_t)(r + 1) * p.K + c, wn);
+        if (r + 1 < r1 && AWQ_IN((size_t)(r + 1) * p.K + c, 72, wn_elems))
+          ldg_w16(p.W, p.w_bf16, (size_t)(r + 1) * p.K + c, wn);
         uint32_t o[8];
         fq_lane16<false, GROUP>(w, nw, RegLane{sv, iv}, p.qmax, p.floor_, p.symmetric != 0, o);
-        if (active) {
+        if (active && AWQ_IN((size_t)a * slot + (size_t)r * p.K + c, 72, (size_t)p.G * slot)) {
           uint4* dst = reinterpret_cast<uint4*>(p.op + (size_t)a * slot + (size_t)r * p.K + c);
           dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
           dst[8] = make_uint4(o[4], o[5], o[6], o[7]);  // 64 channels further on
@@ -488,8 +495,8 @@ __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane
     __threadfence();
     __syncwarp();
     if (lane == 0) {
-      red_release_gpu_add(&p.ready[(size_t)a * p.nt + nb], 1u);
-      red_release_gpu_add(&ready_alpha[a], 1u);
+      if (AWQ_IN((size_t)a * p.nt + nb, 1, (size_t)p.G * p.nt)) red_release_gpu_add(&p.ready[(size_t)a * p.nt + nb], 1u);
+      if (AWQ_IN(a, 1, p.G)) red_release_gpu_add(&ready_alpha[a], 1u);
     }
   }
 }
@@ -678,7 +685,9 @@ __global__ void __launch_bounds__(FUSED ? kFusedThreads : NUM_THREADS, 1)
           if (row < p.n_tok)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (col0 + i < p.N) p.dump[((size_t)a * p.n_tok + row) * p.N + col0 + i] = __uint_as_float(v[i]);
+              if (col0 + i < p.N &&
+                  AWQ_IN(((size_t)a * p.n_tok + row) * p.N + col0 + i, 1, (size_t)p.G * p.n_tok * p.N))
+                p.dump[((size_t)a * p.n_tok + row) * p.N + col0 + i] = __uint_as_float(v[i]);
         }
       }
       tc_fence_before();
@@ -687,7 +696,9 @@ __global__ void __launch_bounds__(FUSED ? kFusedThreads : NUM_THREADS, 1)
       ph ^= 1u << buf;
 #pragma unroll
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0 && mb < p.mt) p.partials[((((size_t)a * p.mt + mb) * p.nt + nb) << 2) + q] = ss;
+      if (lane == 0 && mb < p.mt &&
+          AWQ_IN((((size_t)a * p.mt + mb) * p.nt + nb) * 4 + q, 1, (size_t)p.G * p.mt * p.nt * 4))
+        p.partials[((((size_t)a * p.mt + mb) * p.nt + nb) << 2) + q] = ss;
     }
   } else if (FUSED) {
     // -------------------------------------------------------------- quantiser warps (both CTAs)
@@ -905,5 +916,9 @@ cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, i
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+
+#ifdef AWQ_CHECKED
+cudaError_t take_oob_search(unsigned long long* out) { return take_oob_record(out); }
+#endif
 
 }  // namespace awq

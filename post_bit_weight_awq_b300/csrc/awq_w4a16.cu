@@ -69,7 +69,8 @@ __device__ __forceinline__ void w4_load(W4Step<R, U>& st, const int32_t* __restr
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = cbase + 32 * u;
-      if (r < N && c < chunks) {
+      if (r < N && c < chunks && AWQ_IN((size_t)r * kw + 4 * c, 4, (size_t)N * kw) &&
+          AWQ_IN((size_t)r * kg + (c >> gsh), 1, (size_t)N * kg)) {
         st.q[i][u] = ld_stream_v4(qweight + (size_t)r * kw + 4 * c);
         st.s[i][u] = scales[(size_t)r * kg + (c >> gsh)];  // a chunk lies inside one group
         st.z[i][u] = zeros[(size_t)r * kg + (c >> gsh)];
@@ -128,7 +129,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   if (r0 < N) w4_load<R, U>(cur, qweight, scales, zeros, r0, N, lane, chunks, kw, kg, gsh);
 
   for (int i = threadIdx.x; i < M * K / 8; i += kW4Threads) {
-    const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)i * 8);
+    const uint4 v = AWQ_IN((size_t)i * 8, 8, (size_t)M * K) ? *reinterpret_cast<const uint4*>(x + (size_t)i * 8)
+                                                              : make_uint4(0u, 0u, 0u, 0u);
     const int m = (i * 8) / K, kk = i * 8 - m * K;
     float* d = xs + (size_t)m * kp + (kk >> 5) * kW4Pad + (kk & 31);
     reinterpret_cast<float4*>(d)[0] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           float v = acc[i][m];
 #pragma unroll
           for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == m && r0 + i < N) y[(size_t)m * N + r0 + i] = v;
+          if (lane == m && r0 + i < N && AWQ_IN((size_t)m * N + r0 + i, 1, (size_t)M * N)) y[(size_t)m * N + r0 + i] = v;
           acc[i][m] = 0.0f;
         }
     }
@@ -241,5 +243,9 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int
     default: return cudaErrorInvalidValue;
   }
 }
+
+#ifdef AWQ_CHECKED
+cudaError_t take_oob_w4a16(unsigned long long* out) { return take_oob_record(out); }
+#endif
 
 }  // namespace awq

@@ -9,3 +9,16 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With AWQ_BOUNDS_REPORT set (a run against the bounds-checked library), write the library's record of
+    failed bounds checks to that file when the session ends."""
+    path = os.environ.get("AWQ_BOUNDS_REPORT")
+    if not path:
+        return
+    from post_bit_weight_awq_b300 import capi
+
+    failures, unit, line, offset = capi.awq_bounds_report()
+    with open(path, "w") as f:
+        f.write(f"{failures} {unit} {line} {offset}\n")

@@ -211,3 +211,19 @@ def test_host_validation_of_layer_pipeline(lib):
     assert call([io, null], 2) == capi.AWQ_ERR_INVALID_ARG
     big = capi.AwqLayerIO(A, A, 129, 256, 512, A, A, A, A, A, A, 0)  # more tokens than the workspace was sized for
     assert call([io, big], 2) == capi.AWQ_ERR_WORKSPACE
+
+
+def test_bounds_checks_are_absent_from_the_release_library(lib):
+    f, u, ln, off = ctypes.c_uint64(), ctypes.c_int32(), ctypes.c_uint64(), ctypes.c_uint64()
+    assert lib.awq_bounds_report(ctypes.byref(f), ctypes.byref(u), ctypes.byref(ln), ctypes.byref(off)) == \
+        capi.AWQ_ERR_UNSUPPORTED
+    assert lib.awq_bounds_selftest(ctypes.c_void_p(0x1000), 4, None) == capi.AWQ_ERR_UNSUPPORTED
+    assert lib.awq_bounds_report(None, ctypes.byref(u), ctypes.byref(ln), ctypes.byref(off)) == \
+        capi.AWQ_ERR_INVALID_ARG
+
+
+def test_checked_library_builds_and_exports_the_same_calls():
+    path = build.build(checked=True)
+    checked = ctypes.CDLL(path)
+    for name in capi.EXPORTED:
+        assert hasattr(checked, name), name
