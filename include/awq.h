@@ -187,6 +187,10 @@ AWQ_API awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, co
    losses: device fp32 [n_grid], the mean squared output error per alpha.
    best_idx: device int32 [1], first index of the smallest loss.
    s_best: device fp32 [in], s of that alpha (fold 1/s_best into X's producer).
+   row_losses: NULL, or device fp32 [n_grid][out]: each output row's share of
+   the loss, sum over tokens of the squared error of that row divided by
+   n_tok * out (so a row of row_losses sums to the loss up to rounding); the
+   search epilogue adds them up in fp64 as it goes, at some extra cost.
    ws/ws_bytes: scratch, at least awq_workspace_size(); its first 4 bytes are
    the device status word read by awq_get_device_status.
    The products run on bf16 tensor cores with fp32 accumulation; the step-2
@@ -200,7 +204,8 @@ AWQ_API awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, co
 AWQ_API awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t in,
                             const void* X, int32_t x_dtype, int64_t n_tok, const float* mean_abs,
                             const awq_config* cfg, float* losses, int32_t* best_idx,
-                            float* s_best, void* ws, size_t ws_bytes, awq_stream_t stream);
+                            float* s_best, float* row_losses, void* ws, size_t ws_bytes,
+                            awq_stream_t stream);
 
 /* Several linears that read the same input X (the q/k/v projections behind
    one RMSNorm, or gate/up behind another) must share one s, because 1/s is

@@ -122,7 +122,8 @@ def lib() -> ctypes.CDLL:
         "awq_act_stats": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _SZ, _P]),
         "awq_act_stats_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P]),
         "awq_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _CFG, ctypes.POINTER(_SZ)]),
-        "awq_search_layer": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _I64, _P, _CFG, _P, _P, _P, _P, _SZ, _P]),
+        "awq_search_layer": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _I64, _P, _CFG, _P, _P, _P, _P, _P, _SZ,
+                                            _P]),
         "awq_search_block_workspace_size": (ctypes.c_int, [_I64, _P, _I32, _I64, _I32, _CFG, ctypes.POINTER(_SZ)]),
         "awq_search_block": (ctypes.c_int, [_P, _I32, _P, _I32, _I64, _P, _I32, _I64, _P, _CFG, _P, _P, _P, _P, _SZ,
                                             _P]),
@@ -263,7 +264,7 @@ def awq_act_stats_noalloc(X, mean_abs, stream=None, *, n_tok=None, in_features=N
 
 def awq_search_layer(W, X, mean_abs, cfg: AwqConfig, losses, best_idx, s_best, ws, stream=None, *,
                      out_features=None, in_features=None, n_tok=None, w_dtype=None, x_dtype=None,
-                     ws_bytes=None) -> None:
+                     ws_bytes=None, row_losses=None) -> None:
     N = W.shape[0] if out_features is None else out_features
     K = W.shape[1] if in_features is None else in_features
     n = X.shape[0] if n_tok is None else n_tok
@@ -271,7 +272,8 @@ def awq_search_layer(W, X, mean_abs, cfg: AwqConfig, losses, best_idx, s_best, w
     xd = _dtype_code(X) if x_dtype is None else x_dtype
     wb = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check(lib().awq_search_layer(_ptr(W), wd, N, K, _ptr(X), xd, n, _ptr(mean_abs), ctypes.byref(cfg),
-                                  _ptr(losses), _ptr(best_idx), _ptr(s_best), _ptr(ws), wb, _stream(stream)),
+                                  _ptr(losses), _ptr(best_idx), _ptr(s_best), _ptr(row_losses), _ptr(ws), wb,
+                                  _stream(stream)),
            "awq_search_layer")
 
 

@@ -73,7 +73,7 @@ awq_status check_xdtype(int32_t x_dtype) {
 awq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
 
 struct SearchLayout {
-  size_t status, s, inv_s, op, partials, ready, total;
+  size_t status, s, inv_s, op, partials, ready, row_acc, total;
   int64_t mt, nt;
 };
 
@@ -96,13 +96,16 @@ SearchLayout search_layout(int64_t n_tok, int64_t out, int64_t in, const awq_con
   off = align_up(off + (size_t)G * L.mt * L.nt * 4 * 4, kAlign);
   L.ready = off;
   off = align_up(off + fused_ready_words(G, L.nt) * 4, kAlign);
+  L.row_acc = off;  // fp64 [G][out], used when per-row losses are asked for
+  off = align_up(off + (size_t)G * out * 8, kAlign);
   L.total = off;
   return L;
 }
 
 awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X, int64_t n_tok,
                       const float* mean_abs, const awq_config& c, float* losses, int32_t* best_idx, float* s_best,
-                      uint8_t* base, const SearchLayout& L, cudaStream_t s, bool clear_status = true);
+                      uint8_t* base, const SearchLayout& L, cudaStream_t s, bool clear_status = true,
+                      float* row_losses = nullptr);
 
 
 // ------------------------------------------------------------- host-buffer layer pipeline
@@ -409,8 +412,8 @@ awq_status awq_loss_select(const float* partials, int64_t n_tok, int64_t out, in
 
 awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X,
                             int32_t x_dtype, int64_t n_tok, const float* mean_abs, const awq_config* cfg,
-                            float* losses, int32_t* best_idx, float* s_best, void* ws, size_t ws_bytes,
-                            awq_stream_t stream) {
+                            float* losses, int32_t* best_idx, float* s_best, float* row_losses, void* ws,
+                            size_t ws_bytes, awq_stream_t stream) {
   AWQ_TRACE("awq_search_layer");
   if (W == nullptr || X == nullptr || mean_abs == nullptr || losses == nullptr || best_idx == nullptr ||
       s_best == nullptr || ws == nullptr)
@@ -428,8 +431,9 @@ awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t
   const SearchLayout L = search_layout(n_tok, out, in, *cfg);
   if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
 
+  if (row_losses != nullptr && (reinterpret_cast<uintptr_t>(row_losses) & 3u)) return AWQ_ERR_MISALIGNED;
   return run_search(W, w_dtype, out, in, X, n_tok, mean_abs, *cfg, losses, best_idx, s_best, (uint8_t*)ws, L,
-                    (cudaStream_t)stream);
+                    (cudaStream_t)stream, true, row_losses);
 }
 
 awq_status awq_search_block_workspace_size(int64_t n_tok, const int64_t* outs, int32_t count, int64_t in,
@@ -493,7 +497,8 @@ namespace {
 
 awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X, int64_t n_tok,
                       const float* mean_abs, const awq_config& c, float* losses, int32_t* best_idx, float* s_best,
-                      uint8_t* base, const SearchLayout& L, cudaStream_t s, bool clear_status) {
+                      uint8_t* base, const SearchLayout& L, cudaStream_t s, bool clear_status,
+                      float* row_losses) {
   const awq_config* cfg = &c;
   uint32_t* status = (uint32_t*)(base + L.status);
   float* sc = (float*)(base + L.s);
@@ -502,28 +507,32 @@ awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, c
   float* partials = (float*)(base + L.partials);
 
   uint32_t* ready = (uint32_t*)(base + L.ready);
+  double* row_acc = row_losses != nullptr ? (double*)(base + L.row_acc) : nullptr;
 
   cudaError_t e = clear_status ? cudaMemsetAsync(status, 0, 4, s) : cudaSuccess;
+  if (e == cudaSuccess && row_acc != nullptr) e = cudaMemsetAsync(row_acc, 0, (size_t)cfg->n_grid * out * 8, s);
   if (e == cudaSuccess) e = launch_alpha_scales(mean_abs, in, *cfg, sc, inv, s);
   const double flops = 2.0 * cfg->n_grid * (double)n_tok * (double)out * (double)in;
   if (cfg->loss_form == AWQ_LOSS_RESIDUAL && flops < kLargeSearchFlops) {
     // fake-quant runs inside the search kernel, ahead of the products that consume it
     if (e == cudaSuccess)
       e = launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, sc, inv, out, *cfg, op, partials, ready,
-                              status, s);
+                              status, s, nullptr, -1, row_acc);
   } else if (cfg->loss_form == AWQ_LOSS_RESIDUAL) {
     // searches that run for tens of milliseconds and more settle at the power cap, where the single-CTA
     // products with 2-CTA operand multicast do more work per joule than the CTA-pair products
     if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
     if (e == cudaSuccess)
-      e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 2);
+      e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 2, row_acc);
   } else {
     if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
-    if (e == cudaSuccess) e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s);
+    if (e == cudaSuccess)
+      e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 0, row_acc);
   }
   if (e == cudaSuccess)
     e = launch_loss_select(partials, cfg->n_grid, L.mt * L.nt * 4, n_tok, out, sc, in, losses, best_idx, s_best,
                            status, s);
+  if (e == cudaSuccess && row_acc != nullptr) e = launch_row_losses(row_acc, cfg->n_grid, out, n_tok, row_losses, s);
   return from_cuda(e);
 }
 

@@ -644,6 +644,24 @@ __global__ void __launch_bounds__(256) select_kernel(const float* __restrict__ l
   if (j < K && AWQ_IN((size_t)best_sh * K + j, 1, (size_t)G * K)) s_best[j] = s[(size_t)best_sh * K + j];
 }
 
+__global__ void __launch_bounds__(256) row_losses_kernel(const double* __restrict__ row_acc, size_t total,
+                                                         double denom, float* __restrict__ row_losses) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x)
+    row_losses[i] = (float)(row_acc[i] / denom);
+}
+
+cudaError_t launch_row_losses(const double* row_acc, int G, int64_t N, int64_t n_tok, float* row_losses,
+                              cudaStream_t st) {
+  const size_t total = (size_t)G * (size_t)N;
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  size_t blocks = (total + 255) / 256;
+  if (blocks > (size_t)sms * 8) blocks = (size_t)sms * 8;
+  row_losses_kernel<<<(unsigned)blocks, 256, 0, st>>>(row_acc, total, (double)n_tok * (double)N, row_losses);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, int64_t n_tok, int64_t N,
                                const float* s, int64_t K, float* losses, int32_t* best_idx, float* s_best,
                                uint32_t* status, cudaStream_t st) {

@@ -37,6 +37,10 @@ cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, c
 cudaError_t launch_pack(const void* W, int w_dtype, int64_t N, int64_t K, const float* s,
                         const awq_config& cfg, int32_t* qweight, uint16_t* scales, uint16_t* zeros,
                         cudaStream_t st);
+// row_losses[i][r] = row_acc[i][r] / (n_tok * N) as fp32.
+cudaError_t launch_row_losses(const double* row_acc, int G, int64_t N, int64_t n_tok, float* row_losses,
+                              cudaStream_t st);
+
 cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, int64_t n_tok, int64_t N,
                                const float* s, int64_t K, float* losses, int32_t* best_idx, float* s_best,
                                uint32_t* status, cudaStream_t st);
@@ -45,9 +49,12 @@ cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, 
 // be encoded.
 cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
                                const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
-                               float* dump = nullptr, int withhold_first_fill = 0, int cluster_m = 0);
+                               float* dump = nullptr, int withhold_first_fill = 0, int cluster_m = 0,
+                               double* row_acc = nullptr);
 // cluster_m: 0 = default kernel (CTA pairs, cta_group::2, for the RESIDUAL
 // form); 1, 2 or 4 = the single-CTA kernel with clusters of that size.
+// row_acc: if not null, fp64 [n_grid][N] to which each output row's sum of
+// squared errors over the tokens is added (the caller zeroes it).
 
 // Words of the fused search's synchronisation scratch: a counter per operand
 // tile and per alpha, and one progress word.
@@ -60,7 +67,7 @@ inline size_t fused_ready_words(int64_t G, int64_t n_tiles) { return (size_t)(G 
 cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, int64_t n_tok, int64_t K,
                                 const float* s, const float* inv_s, int64_t N, const awq_config& cfg, uint16_t* op,
                                 float* partials, uint32_t* ready, uint32_t* status, cudaStream_t st,
-                                float* dump = nullptr, int skip_unit = -1);
+                                float* dump = nullptr, int skip_unit = -1, double* row_acc = nullptr);
 
 // y[m][r] = sum_k x[m][k] * (q[r][k] - z[r][g]) * scale[r][g] for m < M <= 8,
 // g = k / group (group 32, 64 or 128), x bf16 [M][K] (staged as fp32 in

@@ -65,6 +65,7 @@ struct Params {
   float* partials;    // [G][mt][nt][4]
   uint32_t* status;
   float* dump;        // optional raw products [G][n_tok][N] (RESIDUAL, test aid)
+  double* row_acc;    // optional per-output-row sums of squared errors [G][N] (added to; nullptr: off)
   int n_tok, N;
   int withhold_first_fill;  // test aid: leave out each CTA's first operand fill
   // fused fake-quant (pair kernel with quantiser warps)
@@ -87,6 +88,34 @@ struct Params {
 // else token tiles): within a band the other operand sweeps its whole range,
 // so the band's panels of the stationary operand stay in L2 while each panel
 // of the swept operand is read once per band.
+// Per-column sums over the warp of the squares of 32 values per lane (lane =
+// token row, value i = column i of a 32-column chunk): five exchange steps
+// halve the columns each lane holds while summing over the lane pairs, so
+// that lane l ends with column l summed over all 32 lanes (31 shuffles).
+template <int N>
+__device__ __forceinline__ void column_sum_step(float (&a)[32], int lane) {
+  const bool upper = (lane & N) != 0;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float send = upper ? a[i] : a[i + N];
+    const float keep = upper ? a[i + N] : a[i];
+    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, N);
+  }
+}
+
+// Adds the warp's per-column sums of d^2 for the chunk's 32 columns to
+// row_acc[alpha][col0 + lane] (columns past N are padding and are skipped).
+__device__ __forceinline__ void add_row_sums(float (&sq)[32], int lane, double* row_acc, int alpha, int col0, int N,
+                                             int G) {
+  column_sum_step<16>(sq, lane);
+  column_sum_step<8>(sq, lane);
+  column_sum_step<4>(sq, lane);
+  column_sum_step<2>(sq, lane);
+  column_sum_step<1>(sq, lane);
+  const int col = col0 + lane;
+  if (col < N && AWQ_IN((size_t)alpha * N + col, 1, (size_t)G * N)) atomicAdd(&row_acc[(size_t)alpha * N + col], (double)sq[0]);
+}
+
 __device__ __forceinline__ void decode_tile(int t, int m_tiles, int nt, int group, int raster_n, int& mb, int& nb) {
   const int n_stat = raster_n ? nt : m_tiles;   // stationary dimension
   const int n_sweep = raster_n ? m_tiles : nt;  // swept dimension
@@ -288,6 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(acc_addr + (uint32_t)(c * 32), v);
+          float sq[32];
           if (REF) {
             uint32_t y[32];
             tmem_ld_32x32b_x32(tmem_base + lane_base + (uint32_t)(BN + c * 32), y);
@@ -295,13 +325,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < 32; ++i) {
               const float d = __fsub_rn(__uint_as_float(v[i]), __uint_as_float(y[i]));
               ss = fmaf(d, d, ss);
+              sq[i] = d * d;
             }
+            if (p.row_acc != nullptr) add_row_sums(sq, lane, p.row_acc, pass - 1, nb * BN + c * 32, p.N, p.G);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float d = __uint_as_float(v[i]);
               ss = fmaf(d, d, ss);
+              sq[i] = d * d;
             }
+            if (p.row_acc != nullptr) add_row_sums(sq, lane, p.row_acc, a, nb * BN + c * 32, p.N, p.G);
             if (p.dump != nullptr) {
               const int row = mb * BM + q * 32 + lane;
               const int col0 = nb * BN + c * 32;
@@ -674,11 +708,14 @@ __global__ void __launch_bounds__(FUSED ? kFusedThreads : NUM_THREADS, 1)
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(acc_addr + (uint32_t)(c * 32), v);
+        float sq[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float d = __uint_as_float(v[i]);
           ss = fmaf(d, d, ss);
+          sq[i] = d * d;
         }
+        if (p.row_acc != nullptr) add_row_sums(sq, lane, p.row_acc, a, nb * BN + c * 32, p.N, p.G);
         if (p.dump != nullptr) {
           const int row = mb * BM + q * 32 + lane;
           const int col0 = nb * BN + c * 32;
@@ -848,7 +885,7 @@ cudaError_t setup_search(const uint16_t* X, int64_t n_tok, int64_t K, const uint
 
 cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
                                const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
-                               float* dump, int withhold_first_fill, int cluster_m) {
+                               float* dump, int withhold_first_fill, int cluster_m, double* row_acc) {
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
   // cluster_m 0: the default (CTA pairs for RESIDUAL, single CTAs for
   // REFERENCE); 1, 2 or 4: the single-CTA kernel with that cluster size.
@@ -864,6 +901,7 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
   p.partials = partials;
   p.status = status;
   p.dump = ref ? nullptr : dump;
+  p.row_acc = row_acc;
   p.withhold_first_fill = withhold_first_fill;
 
   if (ref) {
@@ -884,7 +922,7 @@ cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, cons
 cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, int64_t n_tok, int64_t K,
                                 const float* s, const float* inv_s, int64_t N, const awq_config& cfg, uint16_t* op,
                                 float* partials, uint32_t* ready, uint32_t* status, cudaStream_t st, float* dump,
-                                int skip_unit) {
+                                int skip_unit, double* row_acc) {
   if (cfg.loss_form != AWQ_LOSS_RESIDUAL) return cudaErrorInvalidValue;
   CUtensorMap tmX, tmB;
   Params p;
@@ -894,6 +932,7 @@ cudaError_t launch_search_fused(const void* W, int w_dtype, const uint16_t* X, i
   p.partials = partials;
   p.status = status;
   p.dump = dump;
+  p.row_acc = row_acc;
   p.W = W;
   p.w_bf16 = w_dtype == AWQ_BF16 ? 1 : 0;
   p.nstrips = (int)((K + kFqStrip - 1) / kFqStrip);

@@ -24,6 +24,7 @@ class QuantizedLayer:
     qweight: torch.Tensor  # int32 [out, in/8]
     scales: torch.Tensor  # fp16 [out, in/group]
     zeros: torch.Tensor  # fp16 [out, in/group]
+    row_losses: Optional[torch.Tensor] = None  # fp32 [n_grid, out] when asked for: each row's share of the loss
 
 
 class Workspace:
@@ -53,8 +54,9 @@ def _check_inputs(W: torch.Tensor, X: torch.Tensor) -> None:
 
 
 def quantize_layer(W: torch.Tensor, X: torch.Tensor, cfg: Optional[capi.AwqConfig] = None,
-                   workspace: Optional[Workspace] = None, stream=None) -> QuantizedLayer:
-    """AWQ search + INT4 pack of one layer (asynchronous on ``stream``)."""
+                   workspace: Optional[Workspace] = None, stream=None, row_losses: bool = False) -> QuantizedLayer:
+    """AWQ search + INT4 pack of one layer (asynchronous on ``stream``); with ``row_losses`` the search
+    also returns each output row's share of every alpha's loss."""
     _check_inputs(W, X)
     cfg = capi.config() if cfg is None else cfg
     N, K = W.shape
@@ -71,8 +73,10 @@ def quantize_layer(W: torch.Tensor, X: torch.Tensor, cfg: Optional[capi.AwqConfi
         qweight=torch.empty(N, K // 8, dtype=torch.int32, device=dev),
         scales=torch.empty(N, K // cfg.group, dtype=torch.float16, device=dev),
         zeros=torch.empty(N, K // cfg.group, dtype=torch.float16, device=dev),
+        row_losses=torch.empty(cfg.n_grid, N, dtype=torch.float32, device=dev) if row_losses else None,
     )
     capi.awq_act_stats(X, out.mean_abs, buf, stream)
-    capi.awq_search_layer(W, X, out.mean_abs, cfg, out.losses, out.best_idx, out.s_best, buf, stream)
+    capi.awq_search_layer(W, X, out.mean_abs, cfg, out.losses, out.best_idx, out.s_best, buf, stream,
+                          row_losses=out.row_losses)
     capi.awq_quantize_pack(W, out.s_best, cfg, out.qweight, out.scales, out.zeros, stream)
     return out

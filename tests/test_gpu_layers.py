@@ -225,11 +225,26 @@ def test_full_size_layer(name):
     G = cfg.n_grid
 
     # level 2 and 3: the library's one-call path
-    q = _run_layer(L, cfg)
+    q = layer.quantize_layer(dev_weight(L), dev_bf16(X), cfg, row_losses=True)
+    torch.cuda.synchronize()
     sx = O.channel_importance(X)
     np.testing.assert_allclose(q.mean_abs.cpu().numpy(), sx, rtol=1e-5)
     rel = _check_levels(q.losses.cpu().numpy(), int(q.best_idx[0]), g["losses"])
     print(f"{name}: max rel loss err {rel:.2e}, gpu best {int(q.best_idx[0])}, oracle best {g['best_idx']}")
+
+    # level 2 on sampled output rows: the oracle's exact per-row loss against the search's row losses
+    # (the loss is a sum over rows and s depends only on X, so a row subset is exact)
+    rl = q.row_losses.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(rl.sum(axis=1), q.losses.cpu().numpy().astype(np.float64), rtol=1e-4)
+    rrng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, N - 1], rrng.integers(0, N, 4)]))
+    X64 = X.astype(np.float64)
+    for i in sorted({0, 7, G - 1, g["best_idx"]}):
+        s32 = O.f32(O.awq_scales(sx, O.alpha_grid(G)[i]))
+        Wr = W[rows].astype(np.float64)
+        D = X64 @ (O.fake_quantize(Wr, s32) - Wr).T
+        ref_rows = (D * D).sum(axis=0) / (n * N)
+        np.testing.assert_allclose(rl[i, rows], ref_rows, rtol=LOSS_RTOL)
 
     # sampled output tiles of the same launch configuration, alpha by alpha
     Wd, Xd = dev_weight(L), dev_bf16(X)
@@ -319,3 +334,45 @@ def test_group_and_width_search_layer_levels(group, w_bit):
         np.testing.assert_array_equal(qw.cpu().numpy(), ref["qweight"])
         np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint16), ref["scales"].view(np.uint16))
         np.testing.assert_array_equal(zr.cpu().numpy().view(np.uint16), ref["zeros"].view(np.uint16))
+
+
+@pytest.mark.parametrize("form", [capi.AWQ_LOSS_RESIDUAL, capi.AWQ_LOSS_REFERENCE])
+def test_row_losses_match_the_oracle_rows(form):
+    """Each output row's share of the loss, every alpha, both loss forms (ragged tiles): it sums to the
+    per-alpha loss and matches the oracle row by row within 1e-2, or within the bound of the kernels'
+    arithmetic where that is larger (the REFERENCE form subtracts two rounded products)."""
+    L = workloads.make_layer("llama7b_q_proj", n_tok=300, out_features=520, in_features=1024, seed=5)
+    n, K = L["X"].shape
+    N = L["W"].shape[0]
+    sx32 = O.f32(O.channel_importance(L["X"]))
+    cfg = capi.config(loss_form=form)
+    G = cfg.n_grid
+    ws = torch.empty(capi.awq_workspace_size(n, N, K, cfg), dtype=torch.uint8, device="cuda")
+    losses = torch.empty(G, dtype=torch.float32, device="cuda")
+    best = torch.empty(1, dtype=torch.int32, device="cuda")
+    s_best = torch.empty(K, dtype=torch.float32, device="cuda")
+    rl = torch.full((G, N), float("nan"), dtype=torch.float32, device="cuda")
+    capi.awq_search_layer(dev_weight(L), dev_bf16(L["X"]), dev_f32(sx32), cfg, losses, best, s_best, ws,
+                          row_losses=rl)
+    assert capi.awq_get_device_status(ws) == capi.AWQ_OK
+    rl = rl.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(rl.sum(axis=1), losses.cpu().numpy().astype(np.float64), rtol=1e-4)
+    W = L["W"].astype(np.float64)
+    X = L["X"].astype(np.float64)
+    ax = np.abs(X)
+    for i, a in enumerate(O.alpha_grid(G)):
+        s32 = O.f32(O.awq_scales(sx32, a))
+        Wh = O.fake_quantize(W, s32)
+        E = Wh - W
+        y = X @ E.T
+        ref = (y * y).sum(axis=0) / (n * N)
+        if form == capi.AWQ_LOSS_RESIDUAL:
+            rnd = 2.0**-8 * np.abs(E) + 2.0**-20 * (np.abs(W) + np.abs(Wh))
+            mag = np.abs(E)
+        else:
+            rnd = 2.0**-8 * np.abs(Wh)
+            mag = np.abs(Wh) + np.abs(W)
+        b = ax @ rnd.T + K * 2.0**-24 * (ax @ mag.T)
+        bound = (2.0 * np.abs(y) * b + b * b).sum(axis=0) / (n * N)
+        tol = np.maximum(LOSS_RTOL * ref, bound)
+        assert np.all(np.abs(rl[i] - ref) <= tol), f"alpha {i}: max rel {np.max(np.abs(rl[i] - ref) / ref):.3e}"
