@@ -29,6 +29,11 @@ AWQ_FP32 = 1
 AWQ_LOSS_RESIDUAL = 0
 AWQ_LOSS_REFERENCE = 1
 
+# limits of include/awq.h
+AWQ_W4A16_MAX_TOKENS = 8
+AWQ_W4A16_MAX_TOKEN_CHANNELS = 44 * 1024
+AWQ_BLOCK_MAX_LINEARS = 16
+
 # Every function that include/awq.h declares.
 EXPORTED = (
     "awq_config_default",

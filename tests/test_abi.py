@@ -227,3 +227,11 @@ def test_checked_library_builds_and_exports_the_same_calls():
     checked = ctypes.CDLL(path)
     for name in capi.EXPORTED:
         assert hasattr(checked, name), name
+
+
+def test_binding_constants_match_the_header():
+    text = open(HEADER).read()
+    for name in ("AWQ_W4A16_MAX_TOKENS", "AWQ_W4A16_MAX_TOKEN_CHANNELS", "AWQ_BLOCK_MAX_LINEARS"):
+        m = re.search(r"#define\s+" + name + r"\s+(.+)", text)
+        assert m, name
+        assert eval(m.group(1).split("/*")[0].strip()) == getattr(capi, name), name

@@ -376,3 +376,19 @@ def test_row_losses_match_the_oracle_rows(form):
         bound = (2.0 * np.abs(y) * b + b * b).sum(axis=0) / (n * N)
         tol = np.maximum(LOSS_RTOL * ref, bound)
         assert np.all(np.abs(rl[i] - ref) <= tol), f"alpha {i}: max rel {np.max(np.abs(rl[i] - ref) / ref):.3e}"
+
+
+@pytest.mark.parametrize("n_grid", [1, 2, 64])
+@pytest.mark.parametrize("form", [capi.AWQ_LOSS_RESIDUAL, capi.AWQ_LOSS_REFERENCE])
+def test_grid_sizes_at_the_limits(n_grid, form):
+    """The smallest grids (alpha = 0 alone, which is plain RTN and must pick index 0; two points) and the
+    largest one the library accepts (64 alphas: the fused kernel's per-alpha counters, the partials and the
+    alpha-scale products at their longest), levels 2 and 3 against the oracle."""
+    L = workloads.make_layer("llama7b_q_proj", n_tok=256, out_features=384, in_features=640, seed=n_grid)
+    sx32 = O.f32(O.channel_importance(L["X"]))
+    res = _oracle_losses(L["W"], L["X"], sx=sx32, n_grid=n_grid)
+    losses, best, s_best = _search_with_statistic(L, sx32, capi.config(n_grid=n_grid, loss_form=form))
+    assert losses.shape == (n_grid,)
+    _check_levels(losses, best, res["losses"])
+    if n_grid == 1:
+        assert best == 0 and np.all(s_best == 1.0)

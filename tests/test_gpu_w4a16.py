@@ -76,6 +76,21 @@ def test_w4a16_finer_groups_match_oracle(group, M, N, K):
     assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got - ref).max():.3e}"
 
 
+@pytest.mark.parametrize("M,K", [(1, 45056), (8, 5632), (2, 22528)])
+def test_w4a16_at_the_largest_token_channel_count(M, K):
+    """n_tok * in at AWQ_W4A16_MAX_TOKEN_CHANNELS (the activations fill the kernel's shared memory)."""
+    assert M * K == capi.AWQ_W4A16_MAX_TOKEN_CHANNELS
+    rng = np.random.default_rng(K + M)
+    N = 130
+    pk = _random_packed(rng, N, K)
+    x = workloads.round_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32)).astype(np.float64)
+    got = _run(x.astype(np.float32), pk)
+    ref = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"])
+    W_hat = O.dequantize_groups(O.unpack_words(pk["qweight"], K), pk["scales"].astype(np.float64),
+                                pk["zeros"].astype(np.float64))
+    assert not (np.abs(got - ref) > _bound(x, W_hat)).any()
+
+
 def test_layer_packed_on_gpu_reproduces_the_searched_weight():
     """Search-side weight and inference-side packed layer agree: the GPU pack
     of W * diag(s) applied to x / s equals x W_hat^T of the fake-quant, up to
