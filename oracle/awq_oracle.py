@@ -62,6 +62,8 @@ import numpy as np
 __all__ = [
     "CLAMP_MIN",
     "f32",
+    "bf16",
+    "w4a16_expand_bf16",
     "channel_importance",
     "alpha_grid",
     "awq_scales",
@@ -376,3 +378,31 @@ def w4a16_linear(x, qweight, scales_f16, zeros_f16, group: int = 128) -> np.ndar
     W_hat = dequantize_groups(q, sc, z, group)
     assert W_hat.shape == (out_f, K)
     return x @ W_hat.T
+
+
+def bf16(x) -> np.ndarray:
+    """Round to the nearest bfloat16 (ties to even), via fp32, returned as fp64.
+
+    The value is first rounded to fp32 (exact for the products below), then
+    the low 16 bits of the fp32 pattern are rounded away half-to-even.
+    """
+    x32 = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+    b = x32.view(np.uint32).astype(np.uint64)
+    lsb = (b >> 16) & 1
+    r = ((b + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def w4a16_expand_bf16(qweight, scales_f16, zeros_f16, group: int = 128) -> np.ndarray:
+    """The packed layer as the bf16 weight the prefill product multiplies:
+    W_hat[r, k] = bf16((q[r, k] - z[r, g]) * scale[r, g]), fp64 [out, in].
+
+    [AWQ-devto, "What do you actually deploy": 4-bit weights used with 16-bit
+    activations.] The product (q - z) * scale is exact in fp64 (and in fp32
+    while |q - z| < 2^13); bf16 rounding is the only approximation.
+    """
+    K = np.asarray(qweight).shape[1] * 8
+    q = unpack_words(qweight, K).astype(np.float64)
+    sc = np.asarray(scales_f16, dtype=np.float16).astype(np.float64)
+    z = np.asarray(zeros_f16, dtype=np.float16).astype(np.float64)
+    return bf16(dequantize_groups(q, sc, z, group))

@@ -520,3 +520,43 @@ def test_pack_and_w4a16_with_finer_groups(group):
                 acc += x[t, k] * (code - float(pk["zeros"][r, gi])) * float(pk["scales"][r, gi])
             ref[t, r] = acc
     np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------- bf16 weight of the prefill product
+
+
+def test_bf16_rounding_matches_torch_conversion():
+    """The oracle's own bf16 rounding against torch's float32 -> bfloat16 conversion (a library routine),
+    on random values, exact ties (both directions), signed zeros and values near the bf16 limits."""
+    import torch
+
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-20, 20, 20000),
+        # fp32 values exactly halfway between two bf16 values: low 16 bits 0x8000, odd and even bf16 lsb
+        (np.arange(1, 2001, dtype=np.uint32) * 0x20000 + 0x3F808000).view(np.float32),
+        (np.arange(1, 2001, dtype=np.uint32) * 0x20000 + 0x3F818000).view(np.float32),
+        np.array([0.0, -0.0, 1e-38, -1e-38, 3.3e38, -3.3e38], dtype=np.float32),
+    ]).astype(np.float32)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.bf16(vals.astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+    assert np.array_equal(np.signbit(got), np.signbit(ref))
+
+
+def test_expanded_weight_is_the_rounded_dequantised_weight():
+    """w4a16_expand_bf16 equals bf16 of (q - z) * scale computed element by element from the words."""
+    rng = np.random.default_rng(8)
+    W = rng.standard_normal((5, 256)) * 0.02
+    pk = O.quantize_pack(W, O.f32(rng.uniform(0.5, 2.0, 256)), group=64)
+    Wb = O.w4a16_expand_bf16(pk["qweight"], pk["scales"], pk["zeros"], group=64)
+    for r in range(5):
+        for k in range(0, 256, 7):
+            code = (int(pk["qweight"][r, k // 8]) & 0xFFFFFFFF) >> (4 * (k % 8)) & 0xF
+            v = (code - float(pk["zeros"][r, k // 64])) * float(pk["scales"][r, k // 64])
+            assert Wb[r, k] == O.bf16(np.array([v]))[0]
+    # and it is within half a bf16 step (8 significant bits: 2^-8 relative) of the exact dequantised weight
+    exact = O.dequantize_groups(O.unpack_words(pk["qweight"], 256), pk["scales"].astype(np.float64),
+                                pk["zeros"].astype(np.float64), 64)
+    assert np.all(np.abs(Wb - exact) <= 2.0**-8 * np.abs(exact))
+    assert np.any(np.abs(Wb - exact) > 2.0**-9 * np.abs(exact))  # and the bound is not loose by a factor 2
