@@ -414,6 +414,34 @@ def gpu_arm(args, rank, world, local_rank):
                 "timing": f"{copies} distinct copies per CUDA graph (> L2), L2 flushed before each graph"}
         del packs
 
+    # ---------------------------------------------------------- the packed layer in a prefill (2048 prompt tokens)
+    # expand to bf16 in the workspace, then the tensor-core product (awq_w4a16_gemm); L2 flushed before each run
+    gemm = None
+    Mp = 2048
+    xp = torch.randn(Mp, K, device=dev).to(torch.bfloat16)
+    yp = torch.empty(Mp, N, dtype=f32, device=dev)
+    gws = torch.empty(capi.awq_w4a16_gemm_workspace_size(Mp, K, N, cfg), dtype=u8, device=dev)
+    for _ in range(3):
+        capi.awq_w4a16_gemm(xp, qw, sc, zr, cfg, yp, gws, stream)
+    torch.cuda.synchronize()
+    pt = []
+    for _ in range(max(3, args.steps // 2)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        capi.awq_w4a16_gemm(xp, qw, sc, zr, cfg, yp, gws, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        pt.append(a.elapsed_time(b))
+    assert capi.awq_get_device_status(gws, stream) == capi.AWQ_OK
+    ms_p = statistics.median(pt)
+    pflops = 2.0 * Mp * N * K
+    gemm = {"call": "awq_w4a16_gemm (bf16 expansion of the packed layer + tcgen05 CTA-pair product)", "tokens": Mp,
+            "layer": [N, K], "ms": round(ms_p, 5), "tflops": round(pflops / (ms_p * 1e-3) / 1e12, 1),
+            "frac_bf16_burst": round(pflops / (ms_p * 1e-3) / 1e12 / peaks()["bf16_tflops"], 3),
+            "timing": "median of CUDA-event timed calls, L2 flushed before each"}
+    del gws, xp, yp
+
     # ---------------------------------------------------------- bandwidth kernels on the largest layer
     # the statistics, fake-quant and pack kernels move 33-700 MB on the benchmark layer, a few microseconds of
     # work beside a few microseconds of launch and ramp; on the 70B-class MLP layer they move 0.27-9.9 GB
@@ -495,6 +523,7 @@ def gpu_arm(args, rank, world, local_rank):
         "stages": stages,
         "stages_unfused": separate,
         "w4a16_gemv": gemv,
+        "w4a16_gemm_prefill": gemm,
         "bandwidth_kernels_70b_layer": large,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "awq_quantize_layers: steps layers in one call, each layer's W and X copied in from pinned "

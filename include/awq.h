@@ -250,6 +250,23 @@ AWQ_API awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out
                              const float* s, const awq_config* cfg, int32_t* qweight,
                              uint16_t* scales_f16, uint16_t* zeros_f16, awq_stream_t stream);
 
+/* The packed layer applied to any number of tokens (the prefill case; for
+   up to AWQ_W4A16_MAX_TOKENS tokens awq_w4a16_gemv reads the codes
+   directly). The layer is expanded once into the workspace as
+   W_hat[r][k] = bf16((q - z[r][g]) * scale[r][g]) (the fp32 product is
+   exact while |q - z| < 2^13, so bf16 rounding is its only approximation:
+   at most 2^-8 relative per weight), then y = x W_hat^T runs on the tensor
+   cores with fp32 accumulation (the search's CTA-pair product with one
+   operand). x: device bf16 [n_tok][in]; y: device fp32 [n_tok][out],
+   16-byte aligned; ws: awq_w4a16_gemm_workspace_size() bytes, its first 4
+   bytes a status word (awq_get_device_status). cfg->w_bit must be 4. */
+AWQ_API awq_status awq_w4a16_gemm_workspace_size(int64_t n_tok, int64_t in, int64_t out, const awq_config* cfg,
+                                                 size_t* bytes);
+AWQ_API awq_status awq_w4a16_gemm(const void* x, int32_t x_dtype, int64_t n_tok, int64_t in,
+                                  const int32_t* qweight, const uint16_t* scales_f16, const uint16_t* zeros_f16,
+                                  int64_t out, const awq_config* cfg, float* y, void* ws, size_t ws_bytes,
+                                  awq_stream_t stream);
+
 /* ---------------------------------------------------------------- layers from host memory */
 
 /* One layer of awq_quantize_layers. Pointers may be host or device memory

@@ -47,6 +47,8 @@ EXPORTED = (
     "awq_search_block",
     "awq_quantize_pack",
     "awq_w4a16_gemv",
+    "awq_w4a16_gemm_workspace_size",
+    "awq_w4a16_gemm",
     "awq_pipeline_workspace_size",
     "awq_quantize_layers",
     "awq_packed_bytes",
@@ -134,6 +136,8 @@ def lib() -> ctypes.CDLL:
                                             _P]),
         "awq_quantize_pack": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _CFG, _P, _P, _P, _P]),
         "awq_w4a16_gemv": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _I64, _CFG, _P, _P]),
+        "awq_w4a16_gemm_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _CFG, ctypes.POINTER(_SZ)]),
+        "awq_w4a16_gemm": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _I64, _CFG, _P, _P, _SZ, _P]),
         "awq_pipeline_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _I32, _CFG, ctypes.POINTER(_SZ)]),
         "awq_quantize_layers": (ctypes.c_int, [_P, _I32, _I32, _CFG, _P, _SZ, _P]),
         "awq_packed_bytes": (_SZ, [_I64, _I64, _CFG]),
@@ -349,6 +353,25 @@ def awq_quantize_pack(W, s, cfg: AwqConfig, qweight, scales, zeros, stream=None,
     wd = _dtype_code(W) if w_dtype is None else w_dtype
     _check(lib().awq_quantize_pack(_ptr(W), wd, N, K, _ptr(s), ctypes.byref(cfg), _ptr(qweight), _ptr(scales),
                                    _ptr(zeros), _stream(stream)), "awq_quantize_pack")
+
+
+def awq_w4a16_gemm_workspace_size(n_tok: int, in_features: int, out_features: int, cfg: AwqConfig) -> int:
+    n = _SZ(0)
+    _check(lib().awq_w4a16_gemm_workspace_size(n_tok, in_features, out_features, ctypes.byref(cfg), ctypes.byref(n)),
+           "awq_w4a16_gemm_workspace_size")
+    return n.value
+
+
+def awq_w4a16_gemm(x, qweight, scales, zeros, cfg: AwqConfig, y, ws, stream=None, *, n_tok=None, in_features=None,
+                   out_features=None, x_dtype=None, ws_bytes=None) -> None:
+    """y [n_tok, out] fp32 = x [n_tok, in] bf16 times the packed layer's bf16 weight (prefill product)."""
+    n = x.shape[0] if n_tok is None else n_tok
+    K = x.shape[1] if in_features is None else in_features
+    N = qweight.shape[0] if out_features is None else out_features
+    xd = _dtype_code(x) if x_dtype is None else x_dtype
+    wb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check(lib().awq_w4a16_gemm(_ptr(x), xd, n, K, _ptr(qweight), _ptr(scales), _ptr(zeros), N, ctypes.byref(cfg),
+                                _ptr(y), _ptr(ws), wb, _stream(stream)), "awq_w4a16_gemm")
 
 
 def awq_w4a16_gemv(x, qweight, scales, zeros, cfg: AwqConfig, y, stream=None, *, n_tok=None, in_features=None,

@@ -579,6 +579,64 @@ awq_status awq_w4a16_gemv(const void* x, int32_t x_dtype, int64_t n_tok, int64_t
                                      cfg->group, y, (cudaStream_t)stream));
 }
 
+// Prefill product scratch: status word, the product's tile partials, then the bf16 weight.
+struct GemmLayout {
+  size_t status, partials, w_hat, total;
+};
+
+GemmLayout gemm_layout(int64_t n_tok, int64_t out, int64_t in) {
+  GemmLayout L;
+  const int64_t mt = (n_tok + kTileM - 1) / kTileM, nt = (out + kTileN - 1) / kTileN;
+  L.status = 0;
+  L.partials = kAlign;
+  L.w_hat = align_up(L.partials + (size_t)mt * nt * 4 * 4, kAlign);
+  L.total = align_up(L.w_hat + (size_t)out * in * 2, kAlign);
+  return L;
+}
+
+awq_status awq_w4a16_gemm_workspace_size(int64_t n_tok, int64_t in, int64_t out, const awq_config* cfg,
+                                         size_t* bytes) {
+  if (bytes == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_packed_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  *bytes = gemm_layout(n_tok, out, in).total;
+  return AWQ_OK;
+}
+
+awq_status awq_w4a16_gemm(const void* x, int32_t x_dtype, int64_t n_tok, int64_t in, const int32_t* qweight,
+                          const uint16_t* scales_f16, const uint16_t* zeros_f16, int64_t out, const awq_config* cfg,
+                          float* y, void* ws, size_t ws_bytes, awq_stream_t stream) {
+  AWQ_TRACE("awq_w4a16_gemm");
+  if (x == nullptr || qweight == nullptr || scales_f16 == nullptr || zeros_f16 == nullptr || y == nullptr ||
+      ws == nullptr)
+    return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_packed_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_xdtype(x_dtype);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(x) || !aligned16(qweight) || !aligned16(y) || !aligned16(ws) ||
+      (reinterpret_cast<uintptr_t>(scales_f16) & 1u) || (reinterpret_cast<uintptr_t>(zeros_f16) & 1u))
+    return AWQ_ERR_MISALIGNED;
+  const GemmLayout L = gemm_layout(n_tok, out, in);
+  if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
+  uint8_t* base = (uint8_t*)ws;
+  uint16_t* w_hat = (uint16_t*)(base + L.w_hat);
+  uint32_t* status = (uint32_t*)(base + L.status);
+  const cudaStream_t s = (cudaStream_t)stream;
+  awq_config one = *cfg;  // the product of one operand: the search kernels with a grid of one alpha
+  one.n_grid = 1;
+  one.loss_form = AWQ_LOSS_RESIDUAL;
+  cudaError_t e = cudaMemsetAsync(status, 0, 4, s);
+  if (e == cudaSuccess) e = launch_w4_expand(qweight, scales_f16, zeros_f16, out, in, cfg->group, w_hat, s);
+  if (e == cudaSuccess)
+    e = launch_search_gemm((const uint16_t*)x, n_tok, in, w_hat, out, one, (float*)(base + L.partials), status, s, y);
+  return from_cuda(e);
+}
+
 size_t awq_packed_bytes(int64_t out, int64_t in, const awq_config* cfg) {
   if (check_cfg(cfg) != AWQ_OK || out < 1 || in < 1 || in % cfg->group != 0) return 0;
   const size_t n = (size_t)out * (size_t)in;

@@ -84,4 +84,9 @@ cudaError_t take_oob_w4a16(unsigned long long* out);
 cudaError_t launch_bounds_selftest(float* buf, int n, cudaStream_t st);
 #endif
 
+// W_hat[r][k] = bf16((q[r][k] - z[r][g]) * scale[r][g]) for the whole packed
+// layer (bf16 [N][K]), the operand of the prefill product.
+cudaError_t launch_w4_expand(const int32_t* qweight, const uint16_t* scales, const uint16_t* zeros, int64_t N,
+                             int64_t K, int group, uint16_t* w_hat, cudaStream_t st);
+
 }  // namespace awq

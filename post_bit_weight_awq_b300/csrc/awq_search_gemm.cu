@@ -64,7 +64,7 @@ struct Params {
   uint64_t timeout_ns;
   float* partials;    // [G][mt][nt][4]
   uint32_t* status;
-  float* dump;        // optional raw products [G][n_tok][N] (RESIDUAL, test aid)
+  float* dump;        // optional raw products [G][n_tok][N] (RESIDUAL): the W4A16 product's output, and a test aid
   double* row_acc;    // optional per-output-row sums of squared errors [G][N] (added to; nullptr: off)
   int n_tok, N;
   int withhold_first_fill;  // test aid: leave out each CTA's first operand fill
@@ -88,6 +88,26 @@ struct Params {
 // else token tiles): within a band the other operand sweeps its whole range,
 // so the band's panels of the stationary operand stay in L2 while each panel
 // of the swept operand is read once per band.
+// Raw products of one lane's token row, columns col0 .. col0 + 31 of alpha a,
+// to dump[a][row][col]: 16-byte stores when the chunk is whole and rows are
+// 16-byte aligned (N a multiple of 4), else one value at a time.
+__device__ __forceinline__ void store_products(const Params& p, int a, int row, int col0, const uint32_t (&v)[32]) {
+  const size_t base = ((size_t)a * p.n_tok + row) * p.N + col0;
+  const size_t total = (size_t)p.G * p.n_tok * p.N;
+  if (col0 + 32 <= p.N && (p.N & 3) == 0) {
+    if (!AWQ_IN(base, 32, total)) return;
+    float4* d = reinterpret_cast<float4*>(p.dump + base);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      d[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                         __uint_as_float(v[4 * i + 3]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < p.N && AWQ_IN(base + i, 1, total)) p.dump[base + i] = __uint_as_float(v[i]);
+  }
+}
+
 // Per-column sums over the warp of the squares of 32 values per lane (lane =
 // token row, value i = column i of a 32-column chunk): five exchange steps
 // halve the columns each lane holds while summing over the lane pairs, so
@@ -339,12 +359,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (p.dump != nullptr) {
               const int row = mb * BM + q * 32 + lane;
               const int col0 = nb * BN + c * 32;
-              if (row < p.n_tok)
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (col0 + i < p.N &&
-                      AWQ_IN(((size_t)a * p.n_tok + row) * p.N + col0 + i, 1, (size_t)p.G * p.n_tok * p.N))
-                    p.dump[((size_t)a * p.n_tok + row) * p.N + col0 + i] = __uint_as_float(v[i]);
+              if (row < p.n_tok) store_products(p, a, row, col0, v);
             }
           }
         }
@@ -719,12 +734,7 @@ __global__ void __launch_bounds__(FUSED ? kFusedThreads : NUM_THREADS, 1)
         if (p.dump != nullptr) {
           const int row = mb * BM + q * 32 + lane;
           const int col0 = nb * BN + c * 32;
-          if (row < p.n_tok)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col0 + i < p.N &&
-                  AWQ_IN(((size_t)a * p.n_tok + row) * p.N + col0 + i, 1, (size_t)p.G * p.n_tok * p.N))
-                p.dump[((size_t)a * p.n_tok + row) * p.N + col0 + i] = __uint_as_float(v[i]);
+          if (row < p.n_tok) store_products(p, a, row, col0, v);
         }
       }
       tc_fence_before();

@@ -185,6 +185,38 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   }
 }
 
+// ------------------------------------------------------------ prefill: expand, then the tensor-core product
+//
+// For token counts past the decode kernel's, the packed layer is expanded
+// once to W_hat = bf16((q - z) * scale) (the fp32 product is exact: q - z is
+// a small integer and the fp16 step has 11 significant bits) and multiplied
+// with x on the tensor cores by the search kernels' CTA-pair product with
+// G = 1 and its raw-product output. One thread expands one 32-bit word (8
+// codes of one group) into 16 bytes.
+__global__ void __launch_bounds__(256) w4_expand_kernel(const int32_t* __restrict__ qweight,
+                                                        const uint16_t* __restrict__ scales,
+                                                        const uint16_t* __restrict__ zeros, int64_t words, int kw,
+                                                        int kg, int gsh, uint16_t* __restrict__ w_hat) {
+  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words; w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = w / kw;
+    const int c = (int)(w - r * kw);               // word within the row: codes 8c .. 8c + 7
+    const size_t gi = (size_t)r * kg + (c >> (gsh + 2));  // 8c / (32 << gsh)
+    if (!AWQ_IN(w, 1, words) || !AWQ_IN(gi, 1, (size_t)(words / kw) * kg)) continue;
+    const uint32_t q = (uint32_t)qweight[w];
+    const float sc = __half2float(__ushort_as_half(scales[gi]));
+    const float z = __half2float(__ushort_as_half(zeros[gi]));
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = __fmul_rn(__fsub_rn((float)((q >> (8 * j)) & 0xFu), z), sc);
+      const float b = __fmul_rn(__fsub_rn((float)((q >> (8 * j + 4)) & 0xFu), z), sc);
+      o[j] = pack_bf16x2(a, b);
+    }
+    if (AWQ_IN((size_t)w * 8, 8, (size_t)words * 8))
+      *reinterpret_cast<uint4*>(w_hat + (size_t)w * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 template <int M, int R>
 cudaError_t launch_w4_r(const uint16_t* x, int64_t K, const int32_t* qweight, const uint16_t* scales,
                         const uint16_t* zeros, int64_t N, int gsh, float* y, int sms, cudaStream_t st) {
@@ -226,6 +258,21 @@ cudaError_t launch_w4_t(const uint16_t* x, int64_t K, const int32_t* qweight, co
 }
 
 }  // namespace
+
+cudaError_t launch_w4_expand(const int32_t* qweight, const uint16_t* scales, const uint16_t* zeros, int64_t N,
+                             int64_t K, int group, uint16_t* w_hat, cudaStream_t st) {
+  const int gsh = group == 32 ? 0 : (group == 64 ? 1 : (group == 128 ? 2 : -1));
+  if (gsh < 0) return cudaErrorInvalidValue;
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  const int64_t words = N * (K / 8);
+  int64_t blocks = (words + 255) / 256;
+  if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+  w4_expand_kernel<<<(unsigned)blocks, 256, 0, st>>>(qweight, scales, zeros, words, (int)(K / 8), (int)(K / group),
+                                                      gsh, w_hat);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int32_t* qweight, const uint16_t* scales,
                               const uint16_t* zeros, int64_t N, int group, float* y, cudaStream_t st) {

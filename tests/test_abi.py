@@ -235,3 +235,18 @@ def test_binding_constants_match_the_header():
         m = re.search(r"#define\s+" + name + r"\s+(.+)", text)
         assert m, name
         assert eval(m.group(1).split("/*")[0].strip()) == getattr(capi, name), name
+
+
+def test_host_validation_of_w4a16_gemm(lib):
+    f = capi.awq_w4a16_gemm
+    A, B, C, D, E, F = 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000
+    cfg = capi.config()
+    need = capi.awq_w4a16_gemm_workspace_size(64, 256, 128, cfg)
+    assert need >= 128 * 256 * 2  # the bf16 weight
+    kw = dict(n_tok=64, in_features=256, out_features=128, x_dtype=capi.AWQ_BF16, ws_bytes=need)
+    assert _status_of(f, A, B, C, D, cfg, 0, F, 0, **kw) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A, B, C, D, cfg, E + 4, F, 0, **kw) == capi.AWQ_ERR_MISALIGNED
+    assert _status_of(f, A, B, C, D, cfg, E, F, 0, **{**kw, "ws_bytes": need - 1}) == capi.AWQ_ERR_WORKSPACE
+    assert _status_of(f, A, B, C, D, capi.config(w_bit=3), E, F, 0, **kw) == capi.AWQ_ERR_UNSUPPORTED
+    assert _status_of(f, A, B, C, D, cfg, E, F, 0, **{**kw, "in_features": 200}) == capi.AWQ_ERR_INVALID_ARG
+    assert _status_of(f, A, B, C, D, cfg, E, F, 0, **{**kw, "x_dtype": capi.AWQ_FP32}) == capi.AWQ_ERR_UNSUPPORTED

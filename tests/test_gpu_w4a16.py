@@ -112,3 +112,38 @@ def test_layer_packed_on_gpu_reproduces_the_searched_weight():
     ref = x @ (W_hat * s32[None, :]).T  # x already carries 1/s
     bound = 2.0**-11 * (np.abs(x) @ np.abs(W_hat * s32[None, :]).T) + _bound(x, W_hat * s32[None, :])
     assert np.all(np.abs(got - ref) <= bound)
+
+
+# ------------------------------------------------------------------ prefill: expanded weight on the tensor cores
+
+
+def _run_gemm(x32, pk, group=128):
+    M, K = x32.shape
+    N = pk["qweight"].shape[0]
+    cfg = capi.config(group=group)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(capi.awq_w4a16_gemm_workspace_size(M, K, N, cfg), dtype=torch.uint8, device="cuda")
+    capi.awq_w4a16_gemm(dev_bf16(x32), torch.from_numpy(pk["qweight"]).cuda(),
+                        torch.from_numpy(pk["scales"].view(np.int16)).cuda(),
+                        torch.from_numpy(pk["zeros"].view(np.int16)).cuda(), cfg, y, ws)
+    assert capi.awq_get_device_status(ws) == capi.AWQ_OK
+    torch.cuda.synchronize()
+    return y.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("M,N,K,group", [(16, 300, 1024, 128), (129, 520, 640, 64), (1000, 4096, 4096, 128),
+                                         (300, 130, 8192, 32), (9, 7, 128, 128)])
+def test_w4a16_gemm_matches_oracle(M, N, K, group):
+    """The prefill product: against x times the oracle's bf16 weight within the fp32 accumulation bound,
+    and against the exact packed layer within the bf16 rounding of the weight."""
+    rng = np.random.default_rng(M + N + K + group)
+    pk = _random_packed(rng, N, K, group)
+    x = workloads.round_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32)).astype(np.float64)
+    got = _run_gemm(x.astype(np.float32), pk, group)
+    Wb = O.w4a16_expand_bf16(pk["qweight"], pk["scales"], pk["zeros"], group)
+    ref = x @ Wb.T
+    mag = np.abs(x) @ np.abs(Wb).T
+    bad = np.abs(got - ref) > K * 2.0**-24 * mag + 1e-30
+    assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got - ref).max():.3e}"
+    exact = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"], group=group)
+    assert np.all(np.abs(got - exact) <= (2.0**-8 + K * 2.0**-24) * mag + 1e-30)
