@@ -269,11 +269,13 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* r) {
 // RESIDUAL writes bf16(W_hat_i - W); REFERENCE writes bf16(W_hat_i) and, in
 // slot G, bf16(W).
 //
-// A block owns a strip of 512 input channels (four groups) and a range of
-// output rows; each warp takes one row of the strip at a time, 8 lanes per
-// group and 16 weights per lane: lane l of a group holds channels
-// [8l, 8l+8) and [64+8l, 64+8l+8), so each 16-byte load or store of the warp
-// covers four whole 128-byte segments. The strip's s and 1/s for a chunk of
+// A block owns a strip of 512 input channels (four 128-channel blocks) and a
+// range of output rows; each warp takes one row of the strip at a time, 8
+// lanes per 128-channel block and 16 weights per lane: lane l of a block
+// holds channels [8l, 8l+8) and [64+8l, 64+8l+8), so each 16-byte load or
+// store of the warp covers four whole 128-byte segments. A group of 128 is
+// one block; groups of 64 or 32 are one run of 8 or 4 lanes (the quantiser
+// reduces each run separately). The strip's s and 1/s for a chunk of
 // alphas are staged in shared memory once per block, in lane order (float4 q
 // of lane l at [q][l]) so that every 16-byte shared load of a warp reads 512
 // contiguous bytes without bank conflicts, and reused by every row. W is read
@@ -281,7 +283,7 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* r) {
 // its alphas). Products, differences and the dequantisation run as packed
 // fp32 pairs (one instruction, two correctly rounded results).
 
-constexpr int kFqCols = 512;        // input channels per strip (4 groups)
+constexpr int kFqCols = 512;        // input channels per strip (four 128-channel blocks)
 constexpr int kFqWarps = 8;         // rows in flight per block
 constexpr int kFqAlphaChunk = 20;   // alphas staged in shared memory at once
 constexpr int kFqSmem = 2 * kFqAlphaChunk * kFqCols * 4;  // s and 1/s: 80 KiB
@@ -465,9 +467,10 @@ cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, c
 // scale ("AWQ (Activation-Aware Weight Quantization) - AI Glossary", memory
 // example) and one fp16 zero per group. Same layout as the fake-quant
 // kernel: a block owns a 512-channel strip and a row range, a warp one row at
-// a time, 8 lanes per group with channels [8l, 8l+8) and [64+8l, 64+8l+8),
-// so lane l's two code words are words l and 8+l of its group and every
-// 4-byte store instruction of a warp fills four whole 32-byte sectors. The
+// a time, 8 lanes per 128-channel block with channels [8l, 8l+8) and
+// [64+8l, 64+8l+8), so lane l's two code words are words l and 8+l of its
+// block and every 4-byte store instruction of a warp fills four whole 32-byte
+// sectors. The
 // lane's 16 scales are loaded once per block; the next row's weights load
 // while the current row is quantised.
 
