@@ -137,25 +137,28 @@ cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partial
 // ~n_grid fp64 ulps, which changes the fp32-rounded scale only when it lies
 // that close to an fp32 rounding boundary). alpha = 0 gives s = 1 exactly.
 // fp64 runs at 1/64 of the fp32 rate on this GPU, so the kernel is a chain of
-// fp64 latencies kept short: 64 channels per block, one thread per channel.
-// Every block finds the statistic's max/min itself (16-byte loads, fixed
-// order), which costs one 4-byte read per channel from L2.
+// latencies kept short: 64 channels per block of 256 threads. All threads
+// find the statistic's max/min (16-byte loads, one round of them for
+// in <= 4096, fixed-order reduction); the first two warps form the 64
+// channels' roots (one pow each); then a quad of threads per channel, thread
+// p of the quad writing the alphas i = p (mod 4), stepping by root^4.
 
 constexpr int kAlphaChannels = 64;
+constexpr int kAlphaThreads = 4 * kAlphaChannels;
 
-__global__ void __launch_bounds__(kAlphaChannels) alpha_scales_kernel(const float* __restrict__ mean_abs, int K,
-                                                                      int G, double clamp_min, int normalize,
-                                                                      float* __restrict__ s_out,
-                                                                      float* __restrict__ inv_out) {
-  __shared__ float smax[2], smin[2];
-  const int j = blockIdx.x * kAlphaChannels + threadIdx.x;
-  const float bj = j < K && AWQ_IN(j, 1, K) ? mean_abs[j] : 1.0f;  // in flight during the reduction
-  float mx = -INFINITY, mn = INFINITY;
+__global__ void __launch_bounds__(kAlphaThreads) alpha_scales_kernel(const float* __restrict__ mean_abs, int K,
+                                                                     int G, double clamp_min, int normalize,
+                                                                     float* __restrict__ s_out,
+                                                                     float* __restrict__ inv_out) {
+  __shared__ float smax[kAlphaThreads / 32], smin[kAlphaThreads / 32];
+  const int phase = threadIdx.x & 3;
+  const int j = blockIdx.x * kAlphaChannels + (threadIdx.x >> 2);
   if (normalize) {
+    float mx = -INFINITY, mn = INFINITY;
     const float4* m4 = reinterpret_cast<const float4*>(mean_abs);
     const int K4 = K >> 2;  // K is a multiple of 128
 #pragma unroll 4
-    for (int q = threadIdx.x; q < K4; q += kAlphaChannels) {
+    for (int q = threadIdx.x; q < K4; q += kAlphaThreads) {
       const float4 v = AWQ_IN(4 * (size_t)q, 4, K) ? m4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
       mx = fmax3f(mx, fmaxf(v.x, v.y), fmaxf(v.z, v.w));
       mn = fmin3f(mn, fminf(v.x, v.y), fminf(v.z, v.w));
@@ -165,39 +168,47 @@ __global__ void __launch_bounds__(kAlphaChannels) alpha_scales_kernel(const floa
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     }
-    const int warp = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) {
-      smax[warp] = mx;
-      smin[warp] = mn;
+      smax[threadIdx.x >> 5] = mx;
+      smin[threadIdx.x >> 5] = mn;
     }
     __syncthreads();
   }
-  if (j >= K) return;
-  double base = fmax((double)bj, clamp_min);
-  if (normalize) {
-    const double lo = fmax((double)fminf(smin[0], smin[1]), clamp_min);
-    const double hi = fmax((double)fmaxf(smax[0], smax[1]), clamp_min);
-    base /= sqrt(hi * lo);
-  }
-  const double root = pow(base, 1.0 / (double)G);
-  const double step = root * root;
-  double p[2] = {1.0, root};  // root^i for the even and the odd i: two independent product chains
-  for (int i = 0; i < G; i += 2) {
+  // the first two warps form the block's 64 roots with every lane active (an
+  // fp64 instruction costs a warp the same whatever its active lanes)
+  __shared__ double root_sh[kAlphaChannels];
+  if (threadIdx.x < kAlphaChannels) {
+    const int jc = blockIdx.x * kAlphaChannels + threadIdx.x;
+    double base = fmax(jc < K && AWQ_IN(jc, 1, K) ? (double)mean_abs[jc] : 1.0, clamp_min);
+    if (normalize) {
+      float hi32 = smax[0], lo32 = smin[0];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (i + u < G && AWQ_IN((size_t)(i + u) * K + j, 1, (size_t)G * K)) {
-        const float s32 = (float)p[u];
-        s_out[(size_t)(i + u) * K + j] = s32;
-        inv_out[(size_t)(i + u) * K + j] = __fdiv_rn(1.0f, s32);
+      for (int w = 1; w < kAlphaThreads / 32; ++w) {
+        hi32 = fmaxf(hi32, smax[w]);
+        lo32 = fminf(lo32, smin[w]);
       }
-      p[u] *= step;
+      base /= sqrt(fmax((double)hi32, clamp_min) * fmax((double)lo32, clamp_min));
     }
+    root_sh[threadIdx.x] = pow(base, 1.0 / (double)G);
+  }
+  __syncthreads();
+  const double root = root_sh[threadIdx.x >> 2];
+  if (j >= K) return;
+  const double r2 = root * root, step = r2 * r2;
+  double p = phase == 0 ? 1.0 : (phase == 1 ? root : (phase == 2 ? r2 : r2 * root));  // root^phase
+  for (int i = phase; i < G; i += 4) {
+    if (AWQ_IN((size_t)i * K + j, 1, (size_t)G * K)) {
+      const float s32 = (float)p;
+      s_out[(size_t)i * K + j] = s32;
+      inv_out[(size_t)i * K + j] = __fdiv_rn(1.0f, s32);
+    }
+    p *= step;
   }
 }
 
 cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_config& cfg, float* s,
                                 float* inv_s, cudaStream_t st) {
-  alpha_scales_kernel<<<(unsigned)((K + kAlphaChannels - 1) / kAlphaChannels), kAlphaChannels, 0, st>>>(
+  alpha_scales_kernel<<<(unsigned)((K + kAlphaChannels - 1) / kAlphaChannels), kAlphaThreads, 0, st>>>(
       mean_abs, (int)K, cfg.n_grid, (double)cfg.sx_clamp_min, cfg.normalize, s, inv_s);
   return cudaGetLastError();
 }

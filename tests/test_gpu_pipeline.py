@@ -128,3 +128,16 @@ def test_error_in_one_layer_stays_in_the_status_word():
     assert status == capi.AWQ_ERR_NONFINITE
     for i in (0, 2):
         _assert_same(outs[i], _device_path(Ls[i], cfg))
+
+
+@pytest.mark.parametrize("kw", [dict(loss_form=capi.AWQ_LOSS_REFERENCE), dict(zero_point=0, group=32)])
+def test_layers_from_host_with_other_configurations(kw):
+    """The REFERENCE loss form, and the symmetric quantiser with groups of 32, through the pipeline: the
+    same outputs as the one-layer device path."""
+    Ls = [workloads.make_layer("llama7b_q_proj", n_tok=n, out_features=N, in_features=K, seed=40 + i)
+          for i, (n, N, K) in enumerate([(200, 300, 512), (129, 130, 768), (64, 260, 512)])]
+    cfg = capi.config(**kw)
+    outs, status = _run_pipeline(Ls, cfg, capi.AWQ_BF16)
+    assert status == capi.AWQ_OK
+    for L, o in zip(Ls, outs):
+        _assert_same(o, _device_path(L, cfg))
