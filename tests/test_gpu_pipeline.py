@@ -141,3 +141,62 @@ def test_layers_from_host_with_other_configurations(kw):
     assert status == capi.AWQ_OK
     for L, o in zip(Ls, outs):
         _assert_same(o, _device_path(L, cfg))
+
+
+def test_layers_from_pageable_host_memory():
+    """Unpinned host buffers: the copies lose their overlap but not their correctness."""
+    Ls = [workloads.make_layer("llama7b_q_proj", n_tok=128, out_features=256, in_features=512, seed=s)
+          for s in (51, 52, 53)]
+    cfg = capi.config()
+    ins = []
+    outs = []
+    for L in Ls:
+        Wh = torch.from_numpy(np.ascontiguousarray(workloads.bf16_bits(L["W"]).view(np.int16)))
+        Xh = torch.from_numpy(np.ascontiguousarray(workloads.bf16_bits(L["X"]).view(np.int16)))
+        ins.append((Wh, Xh))
+        N, K = L["W"].shape
+        outs.append(dict(qweight=torch.zeros(N, K // 8, dtype=torch.int32),
+                         scales=torch.zeros(N, K // 128, dtype=torch.int16),
+                         zeros=torch.zeros(N, K // 128, dtype=torch.int16),
+                         losses=torch.zeros(cfg.n_grid), best=torch.zeros(1, dtype=torch.int32),
+                         s_best=torch.zeros(K), mean=torch.zeros(K)))
+    ios = [capi.layer_io(Wh, Xh, o["qweight"], o["scales"], o["zeros"], o["losses"], o["best"], o["s_best"], o["mean"],
+                         n_tok=128, out=256, in_features=512) for (Wh, Xh), o in zip(ins, outs)]
+    ws = torch.empty(capi.awq_pipeline_workspace_size(128, 256, 512, capi.AWQ_BF16, cfg), dtype=torch.uint8,
+                     device="cuda")
+    capi.awq_quantize_layers(ios, capi.AWQ_BF16, cfg, ws, torch.cuda.current_stream())
+    assert capi.awq_get_device_status(ws) == capi.AWQ_OK
+    torch.cuda.synchronize()
+    for L, o in zip(Ls, outs):
+        _assert_same(o, _device_path(L, cfg))
+
+
+def test_two_host_threads_enqueue_pipelines_at_once():
+    """Two threads run the pipeline on their own streams and workspaces at the same time; the shared copy
+    streams and events are taken in turn, and both threads get exactly the device path's outputs."""
+    import threading
+
+    cfg = capi.config()
+    sets = [[workloads.make_layer("llama7b_q_proj", n_tok=128, out_features=256, in_features=512, seed=60 + 10 * t + i)
+             for i in range(3)] for t in range(2)]
+    results = [None, None]
+    errors = []
+
+    def work(t):
+        try:
+            with torch.cuda.stream(torch.cuda.Stream()):
+                results[t] = _run_pipeline(sets[t], cfg, capi.AWQ_BF16)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for t in range(2):
+        outs, status = results[t]
+        assert status == capi.AWQ_OK
+        for L, o in zip(sets[t], outs):
+            _assert_same(o, _device_path(L, cfg))
