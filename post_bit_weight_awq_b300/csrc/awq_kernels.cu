@@ -1,9 +1,11 @@
-// Bandwidth-bound kernels of the AWQ per-layer search and pack (sm_103a):
-//   stats_partial / stats_finalize : mean |x| per input channel
-//   alpha_scales                   : s_i = max(sx, clamp)^alpha_i, normalised
-//   fakequant                      : the search operand for every alpha
-//   pack                           : final INT4 codes, fp16 scales and zeros
-//   loss_select                    : per-alpha loss, first argmin, s_best
+// Bandwidth- and latency-bound kernels of the AWQ per-layer search and pack
+// (sm_103a):
+//   stats        : mean |x| per input channel (chunk partials, last block adds)
+//   alpha_scales : s_i = max(sx, clamp)^alpha_i, normalised
+//   fakequant    : the search operand for every alpha
+//   pack         : final INT4 codes, fp16 scales and zeros
+//   row_losses   : each output row's share of the loss, from the search's sums
+//   loss_select  : per-alpha loss, first argmin, s_best
 #include <math.h>
 
 #include "awq_device.cuh"
@@ -213,41 +215,7 @@ cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_conf
   return cudaGetLastError();
 }
 
-// ============================================================== weight loads
-
-template <typename WT>
-struct WLoad;
-
-template <>
-struct WLoad<uint16_t> {  // bf16 bits
-  static __device__ __forceinline__ void load8(const uint16_t* p, float* w) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    w[0] = bf16_lo(v.x);
-    w[1] = bf16_hi(v.x);
-    w[2] = bf16_lo(v.y);
-    w[3] = bf16_hi(v.y);
-    w[4] = bf16_lo(v.z);
-    w[5] = bf16_hi(v.z);
-    w[6] = bf16_lo(v.w);
-    w[7] = bf16_hi(v.w);
-  }
-};
-
-template <>
-struct WLoad<float> {
-  static __device__ __forceinline__ void load8(const float* p, float* w) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
-    w[0] = a.x;
-    w[1] = a.y;
-    w[2] = a.z;
-    w[3] = a.w;
-    w[4] = b.x;
-    w[5] = b.y;
-    w[6] = b.z;
-    w[7] = b.w;
-  }
-};
+// ============================================================== loads
 
 __device__ __forceinline__ void load8f(const float* p, float* v) {
   const float4 a = *reinterpret_cast<const float4*>(p);
@@ -260,15 +228,6 @@ __device__ __forceinline__ void load8f(const float* p, float* v) {
   v[5] = b.y;
   v[6] = b.z;
   v[7] = b.w;
-}
-
-__device__ __forceinline__ uint4 pack_bf16x8(const float* r) {
-  uint4 o;
-  o.x = pack_bf16x2(r[0], r[1]);
-  o.y = pack_bf16x2(r[2], r[3]);
-  o.z = pack_bf16x2(r[4], r[5]);
-  o.w = pack_bf16x2(r[6], r[7]);
-  return o;
 }
 
 // ============================================================== fake-quant
