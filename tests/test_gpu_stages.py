@@ -392,3 +392,41 @@ def test_fused_search_matches_separate_stages_other_quantisers(group, w_bit, zer
     assert int(status[0]) == 0
     assert torch.equal(op.view(torch.int16), op_ref.view(torch.int16))
     assert torch.equal(parts, p_ref)
+
+
+# ------------------------------------------------------------------ near-tie code decisions
+
+
+def _near_tie_rows(step, rows=8, K=512, seed=0):
+    """fp32 rows whose groups of 128 span [0, 15 * step] and otherwise hold values a few ulps either side of
+    the exact ties (k + 1/2) * step, where the fast code decision must hand over to the IEEE division."""
+    rng = np.random.default_rng(seed)
+    W = np.zeros((rows, K), dtype=np.float32)
+    for r in range(rows):
+        for g in range(K // 128):
+            vals = np.empty(128, dtype=np.float32)
+            vals[0], vals[1] = np.float32(0.0), np.float32(15.0 * step)
+            for i in range(2, 128):
+                k = rng.integers(0, 15)
+                tie = np.float32((k + 0.5) * step)
+                vals[i] = tie + np.float32(rng.integers(-3, 4)) * np.spacing(tie)
+            W[r, g * 128:(g + 1) * 128] = rng.permutation(vals)
+    return W
+
+
+@pytest.mark.parametrize("step", [1.0, 1.0 / 15.0, 0.013, 3.3e-3])
+@pytest.mark.parametrize("zero_point", [1, 0])
+def test_pack_decides_near_ties_exactly(step, zero_point):
+    W = _near_tie_rows(step, seed=int(step * 1e6) + zero_point)
+    rows, K = W.shape
+    cfg = capi.config(zero_point=zero_point)
+    for s32 in (np.ones(K, dtype=np.float32), np.full(K, 1.5, dtype=np.float32)):
+        ref = O.quantize_pack(W.astype(np.float64), s32.astype(np.float64), zero_point=bool(zero_point))
+        qw = torch.empty(rows, K // 8, dtype=torch.int32, device="cuda")
+        sc = torch.empty(rows, K // 128, dtype=torch.float16, device="cuda")
+        zr = torch.empty(rows, K // 128, dtype=torch.float16, device="cuda")
+        capi.awq_quantize_pack(dev_f32(W), dev_f32(s32), cfg, qw, sc, zr)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(qw.cpu().numpy(), ref["qweight"])
+        np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint16), ref["scales"].view(np.uint16))
+        np.testing.assert_array_equal(zr.cpu().numpy().view(np.uint16), ref["zeros"].view(np.uint16))

@@ -560,3 +560,36 @@ def test_expanded_weight_is_the_rounded_dequantised_weight():
                                 pk["zeros"].astype(np.float64), 64)
     assert np.all(np.abs(Wb - exact) <= 2.0**-8 * np.abs(exact))
     assert np.any(np.abs(Wb - exact) > 2.0**-9 * np.abs(exact))  # and the bound is not loose by a factor 2
+
+
+# ---------------------------------------------------------------- randomised pin of the quantiser
+
+
+def test_quantizer_against_scalar_restatement_randomised():
+    """Many random groups (sizes 32/64/128, 2-8 bits, normal, heavy-tailed, one-sign, near-constant and
+    tie-laden values) against the scalar fp32 restatement, group by group."""
+    rng = np.random.default_rng(99)
+    for trial in range(60):
+        group = int(rng.choice([32, 64, 128]))
+        w_bit = int(rng.integers(2, 9))
+        kind = trial % 5
+        n = group * 2
+        if kind == 0:
+            v = rng.standard_normal(n) * 0.05
+        elif kind == 1:
+            v = rng.standard_t(2, n) * 0.01
+        elif kind == 2:
+            v = np.abs(rng.standard_normal(n)) + 3.0
+        elif kind == 3:
+            v = 0.7 + rng.standard_normal(n) * 1e-6
+        else:
+            levels = 2**w_bit - 1
+            v = (rng.integers(0, levels, n) + 0.5) / levels  # exact-tie candidates on a unit range
+            v[0], v[1] = 0.0, 1.0
+        V = O.f32(v)[None, :]
+        q, d, z = O.quantize_groups(V, w_bit=w_bit, group=group)
+        for g in range(2):
+            vals = V[0, g * group:(g + 1) * group]
+            codes, dn, zn = _native_fp32_rtn_group(vals, levels=2**w_bit - 1)
+            assert d[0, g] == dn and z[0, g] == zn, (trial, g)
+            np.testing.assert_array_equal(q[0, g * group:(g + 1) * group], codes)
