@@ -285,32 +285,37 @@ def search_scale_block(W_list, X, sx, **kw) -> Dict[str, object]:
     return search_scale(np.concatenate([np.asarray(W, dtype=np.float64) for W in W_list], axis=0), X, sx, **kw)
 
 
-def pack_words(q) -> np.ndarray:
-    """Pack codes [rows, in] (0..15) into int32 words [rows, in/8].
+def pack_words(q, w_bit: int = 4) -> np.ndarray:
+    """Pack b-bit codes [rows, in] into int32 words [rows, in * b / 32].
 
     [AWQ-Gloss, "INT4 Weight Packing & Export": 4-bit codes in INT32
-    containers.] Code of column 8j+k goes to bits [4k, 4k+4) of word j.
+    containers.] Code of column (32/b)*j + k goes to bits [b*k, b*k + b) of
+    word j (for b = 4: column 8j+k in bits [4k, 4k+4)). b divides 32: 2, 4 or 8.
     """
+    if w_bit not in (2, 4, 8):
+        raise ValueError("codes are packed for 2, 4 or 8 bits")
+    per = 32 // w_bit
     q = np.asarray(q)
     rows, K = q.shape
-    if K % 8:
-        raise ValueError("in_features must be a multiple of 8")
-    qi = q.astype(np.int64).reshape(rows, K // 8, 8)
-    if qi.min(initial=0) < 0 or qi.max(initial=0) > 15:
-        raise ValueError("codes outside [0, 15]")
-    words = np.zeros((rows, K // 8), dtype=np.int64)
-    for k in range(8):
-        words += qi[:, :, k] << (4 * k)
+    if K % per:
+        raise ValueError("in_features must be a multiple of the codes per word")
+    qi = q.astype(np.int64).reshape(rows, K // per, per)
+    if qi.min(initial=0) < 0 or qi.max(initial=0) > 2**w_bit - 1:
+        raise ValueError("codes outside the range of the width")
+    words = np.zeros((rows, K // per), dtype=np.int64)
+    for k in range(per):
+        words += qi[:, :, k] << (w_bit * k)
     return words.astype(np.uint32).view(np.int32)
 
 
-def unpack_words(words, in_features: int) -> np.ndarray:
-    """Inverse of ``pack_words``: int32 [rows, in/8] -> codes int64 [rows, in]."""
+def unpack_words(words, in_features: int, w_bit: int = 4) -> np.ndarray:
+    """Inverse of ``pack_words``: int32 [rows, in*b/32] -> codes int64 [rows, in]."""
+    per = 32 // w_bit
     w = np.asarray(words).view(np.uint32).astype(np.int64)
     rows = w.shape[0]
-    out = np.zeros((rows, in_features // 8, 8), dtype=np.int64)
-    for k in range(8):
-        out[:, :, k] = (w >> (4 * k)) & 0xF
+    out = np.zeros((rows, in_features // per, per), dtype=np.int64)
+    for k in range(per):
+        out[:, :, k] = (w >> (w_bit * k)) & (2**w_bit - 1)
     return out.reshape(rows, in_features)
 
 
@@ -321,11 +326,13 @@ def quantize_pack(W, s, w_bit: int = 4, group: int = 128, delta_floor: float = 1
     16-bit scale per group of 128; AWQ-devto quant_config: zero point on.]
     Codes use the pinned fp32 quantiser on fl32(W * fl32(s)); the stored scale
     is fp16(delta) and the stored zero fp16(z).
-    Returns dict(qweight int32 [out, in/8], scales fp16, zeros fp16, codes,
+    Codes of 2 or 8 bits pack the same way, 16 or 4 to a word (3-bit codes do
+    not fill a 32-bit word evenly and are not packed).
+    Returns dict(qweight int32 [out, in*b/32], scales fp16, zeros fp16, codes,
     delta fp32-valued fp64, z).
     """
-    if w_bit != 4:
-        raise ValueError("only 4-bit codes are packed")
+    if w_bit not in (2, 4, 8):
+        raise ValueError("codes are packed for 2, 4 or 8 bits")
     W = np.asarray(W, dtype=np.float64)
     s32 = f32(np.asarray(s, dtype=np.float64))
     V = f32(W * s32[None, :])
@@ -335,7 +342,7 @@ def quantize_pack(W, s, w_bit: int = 4, group: int = 128, delta_floor: float = 1
     with np.errstate(over="ignore"):
         zeros16 = z.astype(np.float32).astype(np.float16)
     return {
-        "qweight": pack_words(q),
+        "qweight": pack_words(q, w_bit),
         "scales": delta.astype(np.float32).astype(np.float16),
         "zeros": zeros16,
         "codes": q.astype(np.int64),

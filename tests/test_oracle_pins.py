@@ -593,3 +593,34 @@ def test_quantizer_against_scalar_restatement_randomised():
             codes, dn, zn = _native_fp32_rtn_group(vals, levels=2**w_bit - 1)
             assert d[0, g] == dn and z[0, g] == zn, (trial, g)
             np.testing.assert_array_equal(q[0, g * group:(g + 1) * group], codes)
+
+
+# ---------------------------------------------------------------- 2- and 8-bit packing
+
+
+@pytest.mark.parametrize("w_bit", [2, 8])
+def test_pack_order_for_other_widths(w_bit):
+    """Hand-written words: column (32/b)*j + k sits in bits [b*k, b*k + b) of word j."""
+    per = 32 // w_bit
+    q = np.zeros((1, 2 * per), dtype=np.int64)
+    q[0, 0] = 1                 # lowest bits of word 0
+    q[0, per - 1] = 2**w_bit - 1  # highest bits of word 0
+    q[0, per + 1] = 2           # second code of word 1
+    words = O.pack_words(q, w_bit).view(np.uint32)
+    assert int(words[0, 0]) == 1 | ((2**w_bit - 1) << (32 - w_bit))
+    assert int(words[0, 1]) == 2 << w_bit
+    np.testing.assert_array_equal(O.unpack_words(O.pack_words(q, w_bit), 2 * per, w_bit), q)
+
+
+@pytest.mark.parametrize("w_bit", [2, 8])
+def test_quantize_pack_other_widths_round_trip(w_bit):
+    rng = np.random.default_rng(w_bit)
+    W = rng.standard_normal((5, 256)) * 0.02
+    s = O.f32(rng.uniform(0.5, 2.0, 256))
+    pk = O.quantize_pack(W, s, w_bit=w_bit, group=64)
+    assert pk["qweight"].shape == (5, 256 * w_bit // 32)
+    np.testing.assert_array_equal(O.unpack_words(pk["qweight"], 256, w_bit), pk["codes"])
+    q, d, z = O.quantize_groups(O.f32(W * s[None, :]), w_bit=w_bit, group=64)
+    np.testing.assert_array_equal(pk["codes"], q)
+    with pytest.raises(ValueError):
+        O.quantize_pack(W, s, w_bit=3)
