@@ -59,8 +59,9 @@
  *   - Shapes: group 32, 64 or 128 ("AWQ: How Activation-Aware Quantization
  *     Saves 4-bit LLMs", deployment notes: finer groups, more scales), in a
  *     multiple of 128 whatever the group (the kernels hold 128-channel
- *     blocks in 8 lanes), w_bit 2..8 for the search and 4 for the packed
- *     layer (awq_quantize_pack, awq_w4a16_gemv), zero_point 0 or 1,
+ *     blocks in 8 lanes), w_bit 2..8 for the search, 2, 4 or 8 for
+ *     awq_quantize_pack and 4 for the products over the packed layer
+ *     (awq_w4a16_gemv, awq_w4a16_gemm), zero_point 0 or 1,
  *     1 <= n_grid <= 64. Other group sizes and widths return
  *     AWQ_ERR_UNSUPPORTED. n_tok and out are arbitrary (>= 1); the loss
  *     divides by the true n_tok * out.
@@ -92,7 +93,7 @@ typedef struct CUstream_st* awq_stream_t;
 typedef enum {
   AWQ_OK = 0,
   AWQ_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad config */
-  AWQ_ERR_UNSUPPORTED = 2, /* valid but not built: group not 32/64/128, w_bit outside 2..8 (4 to pack) ... */
+  AWQ_ERR_UNSUPPORTED = 2, /* valid but not built: group not 32/64/128, w_bit outside 2..8 (2/4/8 to pack) ... */
   AWQ_ERR_MISALIGNED = 3,  /* a device pointer is not 16-byte aligned */
   AWQ_ERR_WORKSPACE = 4,   /* ws_bytes below the size the query returns */
   AWQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
@@ -113,7 +114,7 @@ typedef enum { AWQ_BF16 = 0, AWQ_FP32 = 1 } awq_dtype;
 typedef enum { AWQ_LOSS_RESIDUAL = 0, AWQ_LOSS_REFERENCE = 1 } awq_loss_form;
 
 typedef struct {
-  int32_t w_bit;            /* 4: bits per code (2..8 in the search, 4 in the packed layer) */
+  int32_t w_bit;            /* 4: bits per code (2..8 in the search; 2, 4 or 8 packed; 4 in the products) */
   int32_t group;            /* 128: weights per scale/zero along `in` (32, 64 or 128) */
   int32_t n_grid;           /* 20: alpha_i = i / n_grid, i < n_grid */
   int32_t zero_point;       /* 1: asymmetric with zero point; 0: symmetric, delta = max|v| / 2^(w_bit-1),
@@ -244,8 +245,11 @@ AWQ_API awq_status awq_search_block(const void* const* W_list, int32_t w_dtype, 
    qweight: device int32 [out][in/8]; the code of column 8j+k sits in bits
    [4k, 4k+4) of word j. scales_f16 / zeros_f16: device fp16 bit patterns
    [out][in/group] holding fp16(delta) and fp16(z), round-to-nearest-even.
-   cfg->w_bit must be 4 (the pages pack 4-bit codes into INT32 containers;
-   other widths return AWQ_ERR_UNSUPPORTED). Needs no scratch. */
+   cfg->w_bit 4 is the pages' format (4-bit codes in INT32 containers); 2 and
+   8 pack the same way, 16 or 4 codes to a word: qweight is then int32
+   [out][in * w_bit / 32], column (32/w_bit) j + k in bits
+   [w_bit k, w_bit k + w_bit) of word j. Other widths (3, 5, 6, 7 do not fill
+   a 32-bit word evenly) return AWQ_ERR_UNSUPPORTED. Needs no scratch. */
 AWQ_API awq_status awq_quantize_pack(const void* W, int32_t w_dtype, int64_t out, int64_t in,
                              const float* s, const awq_config* cfg, int32_t* qweight,
                              uint16_t* scales_f16, uint16_t* zeros_f16, awq_stream_t stream);
@@ -276,7 +280,7 @@ typedef struct {
   const void* W;        /* [out][in], of the call's w_dtype */
   const void* X;        /* bf16 [n_tok][in]: the layer's calibration activations */
   int64_t n_tok, out, in;
-  int32_t* qweight;     /* out: [out][in/8], as awq_quantize_pack */
+  int32_t* qweight;     /* out: [out][in * w_bit / 32], as awq_quantize_pack */
   uint16_t* scales_f16; /* out: [out][in/group] */
   uint16_t* zeros_f16;  /* out: [out][in/group] */
   float* losses;        /* out: [n_grid] */

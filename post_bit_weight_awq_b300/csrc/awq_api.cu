@@ -44,8 +44,15 @@ awq_status check_cfg(const awq_config* cfg) {
   return AWQ_OK;
 }
 
-// The packed format holds 4-bit codes, 8 to an int32.
+// The packed format holds codes of 2, 4 or 8 bits, 32/b to an int32.
 awq_status check_packed_cfg(const awq_config* cfg) {
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  return (cfg->w_bit == 2 || cfg->w_bit == 4 || cfg->w_bit == 8) ? AWQ_OK : AWQ_ERR_UNSUPPORTED;
+}
+
+// The products over the packed layer read 4-bit codes.
+awq_status check_product_cfg(const awq_config* cfg) {
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
   return cfg->w_bit == 4 ? AWQ_OK : AWQ_ERR_UNSUPPORTED;
@@ -145,7 +152,7 @@ PipeLayout pipe_layout(int64_t n_tok, int64_t out, int64_t in, int32_t w_dtype, 
   P.mean_abs = o;
   o = align_up(o + (size_t)in * 4, kAlign);
   P.qweight = o;
-  o = align_up(o + (size_t)out * in / 2, kAlign);
+  o = align_up(o + (size_t)out * in * cfg.w_bit / 8, kAlign);
   P.scales = o;
   o = align_up(o + (size_t)out * (in / cfg.group) * 2, kAlign);
   P.zeros = o;
@@ -565,7 +572,7 @@ awq_status awq_w4a16_gemv(const void* x, int32_t x_dtype, int64_t n_tok, int64_t
   AWQ_TRACE("awq_w4a16_gemv");
   if (x == nullptr || qweight == nullptr || scales_f16 == nullptr || zeros_f16 == nullptr || y == nullptr)
     return AWQ_ERR_INVALID_ARG;
-  awq_status st = check_packed_cfg(cfg);
+  awq_status st = check_product_cfg(cfg);
   if (st != AWQ_OK) return st;
   st = check_xdtype(x_dtype);
   if (st != AWQ_OK) return st;
@@ -597,7 +604,7 @@ GemmLayout gemm_layout(int64_t n_tok, int64_t out, int64_t in) {
 awq_status awq_w4a16_gemm_workspace_size(int64_t n_tok, int64_t in, int64_t out, const awq_config* cfg,
                                          size_t* bytes) {
   if (bytes == nullptr) return AWQ_ERR_INVALID_ARG;
-  awq_status st = check_packed_cfg(cfg);
+  awq_status st = check_product_cfg(cfg);
   if (st != AWQ_OK) return st;
   st = check_dims(n_tok, out, in);
   if (st != AWQ_OK) return st;
@@ -612,7 +619,7 @@ awq_status awq_w4a16_gemm(const void* x, int32_t x_dtype, int64_t n_tok, int64_t
   if (x == nullptr || qweight == nullptr || scales_f16 == nullptr || zeros_f16 == nullptr || y == nullptr ||
       ws == nullptr)
     return AWQ_ERR_INVALID_ARG;
-  awq_status st = check_packed_cfg(cfg);
+  awq_status st = check_product_cfg(cfg);
   if (st != AWQ_OK) return st;
   st = check_xdtype(x_dtype);
   if (st != AWQ_OK) return st;
@@ -745,7 +752,7 @@ awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_
     const struct {
       void* dst;
       size_t off, bytes;
-    } outs[6] = {{L.qweight, P.qweight, (size_t)L.out * L.in / 2},
+    } outs[6] = {{L.qweight, P.qweight, (size_t)L.out * L.in * cfg->w_bit / 8},
                  {L.scales_f16, P.scales, (size_t)L.out * gcols * 2},
                  {L.zeros_f16, P.zeros, (size_t)L.out * gcols * 2},
                  {L.losses, P.losses, (size_t)cfg->n_grid * 4},

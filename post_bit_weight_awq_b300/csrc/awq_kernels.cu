@@ -450,7 +450,7 @@ constexpr int kPackWarps = 8;
 template <typename WT, int GROUP>
 constexpr int pack_blocks_per_sm() { return (sizeof(WT) == 2 && GROUP == 128) ? 3 : 2; }
 
-template <typename WT, int GROUP>
+template <typename WT, int GROUP, int BITS>
 __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>())
     pack_kernel(const WT* __restrict__ W, int N, int K, const float* __restrict__ s, float qmax, float floor_,
                 int symmetric, int32_t* __restrict__ qweight, uint16_t* __restrict__ scales,
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>
 #pragma unroll
     for (int i = 0; i < 8; ++i) sv[i] = make_float2(t[2 * i], t[2 * i + 1]);
   }
-  const int kw = K >> 3, kg = K / GROUP;
+  const int kw = K * BITS / 32, kg = K / GROUP;  // code words and groups per row
   const size_t wn = (size_t)N * K;
   int row = r_begin + warp;
   RowRegs<WT> nxt{};
@@ -496,22 +496,48 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>
     lane_groups<GROUP>(v, qmax, floor_, symmetric != 0, ga, gb);
     float2 k[8];
     lane_codes_minus_z<GROUP>(v, ga, gb, k);
-    // q = (q - z) + z in [0, 15]; 2^23 + q carries q in its low mantissa bits,
-    // which avoids a float-to-integer conversion per code
+    // q = (q - z) + z in [0, 2^b - 1]; 2^23 + q carries q in its low mantissa
+    // bits, which avoids a float-to-integer conversion per code
     const float2 za = make_float2(8388608.0f + ga.z, 8388608.0f + ga.z);
     const float2 zb = make_float2(8388608.0f + gb.z, 8388608.0f + gb.z);
-    uint32_t w0 = 0, w1 = 0;
+    constexpr uint32_t kMask = (1u << BITS) - 1u;
+    uint32_t qa[8], qb[8];  // the codes of run A and run B
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 a = __fadd2_rn(k[i], za);
       const float2 b = __fadd2_rn(k[4 + i], zb);
-      w0 |= ((__float_as_uint(a.x) & 0xFu) << (8 * i)) | ((__float_as_uint(a.y) & 0xFu) << (8 * i + 4));
-      w1 |= ((__float_as_uint(b.x) & 0xFu) << (8 * i)) | ((__float_as_uint(b.y) & 0xFu) << (8 * i + 4));
+      qa[2 * i] = __float_as_uint(a.x) & kMask;
+      qa[2 * i + 1] = __float_as_uint(a.y) & kMask;
+      qb[2 * i] = __float_as_uint(b.x) & kMask;
+      qb[2 * i + 1] = __float_as_uint(b.y) & kMask;
     }
-    if (active && AWQ_IN((size_t)row * kw + ((col0 + c_lo) >> 3), 9, (size_t)N * kw)) {
-      int32_t* q = qweight + (size_t)row * kw + ((col0 + c_lo) >> 3);
-      q[0] = (int32_t)w0;
-      q[8] = (int32_t)w1;  // 64 channels further on
+    // words of 32 / BITS codes, column (32/b) j + k in bits [b k, b k + b) of word j: a run of 8 codes is
+    // one word (4 bits), two words (8 bits) or half a word (2 bits, joined with the next lane's half)
+    uint32_t wa[2] = {0u, 0u}, wb[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int word = (e * BITS) >> 5, bit = (e * BITS) & 31;
+      wa[word] |= qa[e] << bit;
+      wb[word] |= qb[e] << bit;
+    }
+    if (BITS == 2) {  // the odd lane's 16 bits go above the even lane's (8 channels further on)
+      wa[0] |= __shfl_down_sync(0xffffffffu, wa[0], 1) << 16;
+      wb[0] |= __shfl_down_sync(0xffffffffu, wb[0], 1) << 16;
+    }
+    const size_t w_at = (size_t)row * kw + (size_t)(col0 + c_lo) * BITS / 32;  // run A's first word
+    constexpr int kRunB = 64 * BITS / 32;                                      // words from run A to run B
+    if (active && AWQ_IN(w_at, kRunB + (BITS == 8 ? 2 : 1), (size_t)N * kw)) {
+      int32_t* q = qweight + w_at;
+      if (BITS == 4) {
+        q[0] = (int32_t)wa[0];
+        q[kRunB] = (int32_t)wb[0];
+      } else if (BITS == 8) {
+        *reinterpret_cast<int2*>(q) = make_int2((int)wa[0], (int)wa[1]);
+        *reinterpret_cast<int2*>(q + kRunB) = make_int2((int)wb[0], (int)wb[1]);
+      } else if ((sub & 1) == 0) {
+        q[0] = (int32_t)wa[0];
+        q[kRunB] = (int32_t)wb[0];
+      }
       const size_t gi = (size_t)row * kg + (col0 + c_lo) / GROUP;
       if (lead && AWQ_IN(gi, GROUP < 128 ? 64 / GROUP + 1 : 1, (size_t)N * kg)) {
         scales[gi] = __half_as_ushort(__float2half_rn(ga.delta));
@@ -525,7 +551,7 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>
   }
 }
 
-template <typename WT, int GROUP>
+template <typename WT, int GROUP, int BITS>
 cudaError_t launch_pack_t(const WT* W, int64_t N, int64_t K, const float* s, const awq_config& cfg,
                           int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
   int sms = 0;
@@ -538,18 +564,29 @@ cudaError_t launch_pack_t(const WT* W, int64_t N, int64_t K, const float* s, con
   const int rows_per_block = (int)((N + rblocks - 1) / rblocks);
   rblocks = (N + rows_per_block - 1) / rows_per_block;
   const float qmax = (float)((1 << cfg.w_bit) - 1);
-  pack_kernel<WT, GROUP><<<(unsigned)(rblocks * nstrips), kPackWarps * 32, 0, st>>>(
+  pack_kernel<WT, GROUP, BITS><<<(unsigned)(rblocks * nstrips), kPackWarps * 32, 0, st>>>(
       W, (int)N, (int)K, s, qmax, cfg.delta_floor, cfg.zero_point == 0 ? 1 : 0, qweight, scales, zeros, nstrips,
       rows_per_block);
   return cudaGetLastError();
 }
 
+template <int GROUP, int BITS>
+cudaError_t launch_pack_b(const void* W, int w_dtype, int64_t N, int64_t K, const float* s, const awq_config& cfg,
+                          int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
+  if (w_dtype == AWQ_BF16)
+    return launch_pack_t<uint16_t, GROUP, BITS>((const uint16_t*)W, N, K, s, cfg, qweight, scales, zeros, st);
+  return launch_pack_t<float, GROUP, BITS>((const float*)W, N, K, s, cfg, qweight, scales, zeros, st);
+}
+
 template <int GROUP>
 cudaError_t launch_pack_g(const void* W, int w_dtype, int64_t N, int64_t K, const float* s, const awq_config& cfg,
                           int32_t* qweight, uint16_t* scales, uint16_t* zeros, cudaStream_t st) {
-  if (w_dtype == AWQ_BF16)
-    return launch_pack_t<uint16_t, GROUP>((const uint16_t*)W, N, K, s, cfg, qweight, scales, zeros, st);
-  return launch_pack_t<float, GROUP>((const float*)W, N, K, s, cfg, qweight, scales, zeros, st);
+  switch (cfg.w_bit) {
+    case 2: return launch_pack_b<GROUP, 2>(W, w_dtype, N, K, s, cfg, qweight, scales, zeros, st);
+    case 4: return launch_pack_b<GROUP, 4>(W, w_dtype, N, K, s, cfg, qweight, scales, zeros, st);
+    case 8: return launch_pack_b<GROUP, 8>(W, w_dtype, N, K, s, cfg, qweight, scales, zeros, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_pack(const void* W, int w_dtype, int64_t N, int64_t K, const float* s, const awq_config& cfg,

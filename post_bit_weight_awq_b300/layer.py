@@ -21,7 +21,7 @@ class QuantizedLayer:
     losses: torch.Tensor  # fp32 [n_grid]
     best_idx: torch.Tensor  # int32 [1]
     s_best: torch.Tensor  # fp32 [in]; fold 1/s_best into the producer of X
-    qweight: torch.Tensor  # int32 [out, in/8]
+    qweight: torch.Tensor  # int32 [out, in * w_bit / 32]
     scales: torch.Tensor  # fp16 [out, in/group]
     zeros: torch.Tensor  # fp16 [out, in/group]
     row_losses: Optional[torch.Tensor] = None  # fp32 [n_grid, out] when asked for: each row's share of the loss
@@ -70,7 +70,7 @@ def quantize_layer(W: torch.Tensor, X: torch.Tensor, cfg: Optional[capi.AwqConfi
         losses=torch.empty(cfg.n_grid, dtype=torch.float32, device=dev),
         best_idx=torch.empty(1, dtype=torch.int32, device=dev),
         s_best=torch.empty(K, dtype=torch.float32, device=dev),
-        qweight=torch.empty(N, K // 8, dtype=torch.int32, device=dev),
+        qweight=torch.empty(N, K * cfg.w_bit // 32, dtype=torch.int32, device=dev),
         scales=torch.empty(N, K // cfg.group, dtype=torch.float16, device=dev),
         zeros=torch.empty(N, K // cfg.group, dtype=torch.float16, device=dev),
         row_losses=torch.empty(cfg.n_grid, N, dtype=torch.float32, device=dev) if row_losses else None,

@@ -124,8 +124,8 @@ def test_host_validation_of_search_and_pack(lib):
     assert _status_of(p, A, B, cfg, C, D, 0, 0, **pkw) == capi.AWQ_ERR_INVALID_ARG
     assert _status_of(p, A, B, cfg, C + 4, D, D, 0, **pkw) == capi.AWQ_ERR_MISALIGNED
     assert _status_of(p, A, B, cfg, C, D + 1, D, 0, **pkw) == capi.AWQ_ERR_MISALIGNED
-    # the packed format holds 4-bit codes only, at any of the built group sizes
-    for bad in (dict(w_bit=8), dict(w_bit=3), dict(w_bit=3, group=32), dict(group=256)):
+    # codes are packed for 2, 4 and 8 bits (widths that divide a 32-bit word), at any built group size
+    for bad in (dict(w_bit=3), dict(w_bit=6), dict(w_bit=3, group=32), dict(group=256)):
         assert _status_of(p, A, B, capi.config(**bad), C, D, D, 0, **pkw) == capi.AWQ_ERR_UNSUPPORTED, bad
     assert _status_of(p, A, B, cfg, C, D, D, 0, **{**pkw, "w_dtype": 3}) == capi.AWQ_ERR_INVALID_ARG
 
@@ -203,7 +203,7 @@ def test_host_validation_of_layer_pipeline(lib):
     assert call([io], 1, ws=0) == capi.AWQ_ERR_INVALID_ARG
     assert call([io], 1, ws=0x100004) == capi.AWQ_ERR_MISALIGNED
     assert call([io], 1, ws_bytes=need - 1) == capi.AWQ_ERR_WORKSPACE
-    assert call([io], 1, c=capi.config(w_bit=8)) == capi.AWQ_ERR_UNSUPPORTED
+    assert call([io], 1, c=capi.config(w_bit=3)) == capi.AWQ_ERR_UNSUPPORTED  # 3-bit codes are not packed
     assert call([io], 1, w_dtype=7) == capi.AWQ_ERR_INVALID_ARG
     bad = capi.AwqLayerIO(A, A, 128, 256, 200, A, A, A, A, A, A, 0)  # in not a multiple of 128
     assert call([io, bad], 2) == capi.AWQ_ERR_INVALID_ARG

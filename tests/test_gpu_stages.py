@@ -430,3 +430,27 @@ def test_pack_decides_near_ties_exactly(step, zero_point):
         np.testing.assert_array_equal(qw.cpu().numpy(), ref["qweight"])
         np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint16), ref["scales"].view(np.uint16))
         np.testing.assert_array_equal(zr.cpu().numpy().view(np.uint16), ref["zeros"].view(np.uint16))
+
+
+@pytest.mark.parametrize("w_bit", [2, 8])
+@pytest.mark.parametrize("group,zero_point", [(128, 1), (64, 0), (32, 1)])
+@pytest.mark.parametrize("layer,kw", [("tiny", {}),
+                                      ("llama7b_q_proj", dict(out_features=130, in_features=640, n_tok=64))])
+def test_pack_other_widths_bit_exact(w_bit, group, zero_point, layer, kw):
+    """2-bit (16 per word) and 8-bit (4 per word) packing: words, scales and zeros equal the oracle's."""
+    L = workloads.make_layer(layer, **kw)
+    W, X = L["W"], L["X"]
+    N, K = W.shape
+    cfg = capi.config(w_bit=w_bit, group=group, zero_point=zero_point)
+    sx = O.channel_importance(X)
+    for alpha in (0.0, 0.6):
+        s32 = O.f32(O.awq_scales(sx, alpha))
+        ref = O.quantize_pack(W.astype(np.float64), s32, w_bit=w_bit, group=group, zero_point=bool(zero_point))
+        qw = torch.full((N, K * w_bit // 32), -1, dtype=torch.int32, device="cuda")
+        sc = torch.empty(N, K // group, dtype=torch.float16, device="cuda")
+        zr = torch.empty(N, K // group, dtype=torch.float16, device="cuda")
+        capi.awq_quantize_pack(dev_weight(L), dev_f32(s32), cfg, qw, sc, zr)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(qw.cpu().numpy(), ref["qweight"])
+        np.testing.assert_array_equal(sc.cpu().numpy().view(np.uint16), ref["scales"].view(np.uint16))
+        np.testing.assert_array_equal(zr.cpu().numpy().view(np.uint16), ref["zeros"].view(np.uint16))
