@@ -11,8 +11,13 @@
  *        W_hat_i = Q(W * diag(s_i)) * diag(1 / s_i)
  *        L_i     = mean over (t, r) of (X W_hat_i^T - X W^T)[t, r]^2
  *      best = first i with the smallest L_i                     (awq_search_layer)
- *   3. codes of W * diag(s_best) packed 8 per int32, fp16 group scales and
- *      fp16 zero points                                         (awq_quantize_pack)
+ *   3. codes of W * diag(s_best) packed 8 per int32 (32/w_bit for 2 or 8
+ *      bits), fp16 group scales and fp16 zero points           (awq_quantize_pack)
+ *   4. the packed layer applied to activations: a few tokens   (awq_w4a16_gemv)
+ *      or any number of tokens                                  (awq_w4a16_gemm)
+ * Steps 1-3 for a sequence of layers held in host memory, with the copies
+ * overlapping the work: awq_quantize_layers. Several linears that read one X
+ * and must share one s: awq_search_block.
  *
  * Q is group-wise asymmetric min/max quantisation along `in` (groups of
  * `group` weights): delta = max((vmax - vmin) / (2^w_bit - 1), delta_floor),
