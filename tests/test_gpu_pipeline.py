@@ -32,7 +32,7 @@ def _host_inputs(L):
 
 def _host_outputs(N, K, cfg):
     pin = dict(pin_memory=True)
-    return dict(qweight=torch.zeros(N, K // 8, dtype=torch.int32, **pin),
+    return dict(qweight=torch.zeros(N, K * cfg.w_bit // 32, dtype=torch.int32, **pin),
                 scales=torch.zeros(N, K // cfg.group, dtype=torch.int16, **pin),
                 zeros=torch.zeros(N, K // cfg.group, dtype=torch.int16, **pin),
                 losses=torch.zeros(cfg.n_grid, dtype=torch.float32, **pin),
@@ -130,7 +130,8 @@ def test_error_in_one_layer_stays_in_the_status_word():
         _assert_same(outs[i], _device_path(Ls[i], cfg))
 
 
-@pytest.mark.parametrize("kw", [dict(loss_form=capi.AWQ_LOSS_REFERENCE), dict(zero_point=0, group=32)])
+@pytest.mark.parametrize("kw", [dict(loss_form=capi.AWQ_LOSS_REFERENCE), dict(zero_point=0, group=32),
+                                dict(w_bit=8, group=64)])
 def test_layers_from_host_with_other_configurations(kw):
     """The REFERENCE loss form, and the symmetric quantiser with groups of 32, through the pipeline: the
     same outputs as the one-layer device path."""
