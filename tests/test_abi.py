@@ -8,6 +8,7 @@ import re
 
 import pytest
 
+import oracle as O
 from post_bit_weight_awq_b300 import build, capi
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -250,3 +251,32 @@ def test_host_validation_of_w4a16_gemm(lib):
     assert _status_of(f, A, B, C, D, capi.config(w_bit=3), E, F, 0, **kw) == capi.AWQ_ERR_UNSUPPORTED
     assert _status_of(f, A, B, C, D, cfg, E, F, 0, **{**kw, "in_features": 200}) == capi.AWQ_ERR_INVALID_ARG
     assert _status_of(f, A, B, C, D, cfg, E, F, 0, **{**kw, "x_dtype": capi.AWQ_FP32}) == capi.AWQ_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("w_bit", [2, 4, 8])
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("zero_point", [0, 1])
+def test_packed_bytes_matches_the_oracle_for_every_layout(lib, w_bit, group, zero_point):
+    cfg = capi.config(w_bit=w_bit, group=group, zero_point=zero_point)
+    for out, inf in ((4096, 4096), (28672, 8192), (7, 128)):
+        ref = O.packed_bytes(out, inf, group=group, w_bit=w_bit, zero_point=bool(zero_point))
+        assert capi.awq_packed_bytes(out, inf, cfg) == ref["total"]
+
+
+def test_workspace_sizes_grow_with_every_dimension(lib):
+    cfg = capi.config()
+    base = (1024, 1024, 1024)
+    for fn in (lambda n, N, K: capi.awq_workspace_size(n, N, K, cfg),
+               lambda n, N, K: capi.awq_pipeline_workspace_size(n, N, K, capi.AWQ_BF16, cfg),
+               lambda n, N, K: capi.awq_w4a16_gemm_workspace_size(n, K, N, cfg)):
+        b = fn(*base)
+        for i in range(3):
+            dims = list(base)
+            dims[i] *= 2
+            assert fn(*dims) >= b
+    # the search workspace holds the G operand copies; the prefill scratch holds the bf16 weight
+    assert capi.awq_workspace_size(1024, 1024, 1024, cfg) >= 20 * 1024 * 1024 * 2
+    assert capi.awq_w4a16_gemm_workspace_size(1024, 1024, 1024, cfg) >= 1024 * 1024 * 2
+    # more alphas, more operand copies
+    assert capi.awq_workspace_size(256, 256, 256, capi.config(n_grid=64)) > \
+        capi.awq_workspace_size(256, 256, 256, capi.config(n_grid=20))
