@@ -280,3 +280,22 @@ def test_workspace_sizes_grow_with_every_dimension(lib):
     # more alphas, more operand copies
     assert capi.awq_workspace_size(256, 256, 256, capi.config(n_grid=64)) > \
         capi.awq_workspace_size(256, 256, 256, capi.config(n_grid=20))
+
+
+def test_every_status_has_its_own_message(lib):
+    codes = [capi.AWQ_OK, capi.AWQ_ERR_INVALID_ARG, capi.AWQ_ERR_UNSUPPORTED, capi.AWQ_ERR_MISALIGNED,
+             capi.AWQ_ERR_WORKSPACE, capi.AWQ_ERR_CUDA, capi.AWQ_ERR_TIMEOUT, capi.AWQ_ERR_NONFINITE]
+    msgs = [capi.status_string(c) for c in codes]
+    assert len(set(msgs)) == len(codes)
+    assert "unknown" in capi.status_string(99)
+
+
+def test_layer_api_rejects_bad_inputs_before_the_library():
+    import torch
+
+    from post_bit_weight_awq_b300 import layer
+
+    W = torch.zeros(4, 128, dtype=torch.bfloat16)
+    X = torch.zeros(8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        layer.quantize_layer(W, X)  # host tensors
