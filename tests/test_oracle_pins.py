@@ -624,3 +624,16 @@ def test_quantize_pack_other_widths_round_trip(w_bit):
     np.testing.assert_array_equal(pk["codes"], q)
     with pytest.raises(ValueError):
         O.quantize_pack(W, s, w_bit=3)
+
+
+def test_memory_arithmetic_70b_golden():
+    """The 70B deployment figure: 140 GB of fp16 weights, 35 GB of 4-bit codes; with one fp16 scale and
+    one fp16 zero per 128 weights the reduction lies between the page's 72% and the codes' 75%."""
+    g = json.load(open(os.path.join(GOLDEN, "memory_70b.json")))
+    rows, cols = 175000, 400000  # 7e10 weights, rows of whole groups of 128 (the counts are per weight)
+    assert rows * cols == g["weights"] and cols % 128 == 0
+    b = O.packed_bytes(rows, cols, group=128)
+    assert rows * cols * 2 == g["fp16_bytes"]
+    assert b["codes"] == g["int4_bytes"]
+    reduction = 1.0 - b["total"] / g["fp16_bytes"]
+    assert g["stated_reduction"] <= reduction <= 0.75
