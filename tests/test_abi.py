@@ -299,3 +299,21 @@ def test_layer_api_rejects_bad_inputs_before_the_library():
     X = torch.zeros(8, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         layer.quantize_layer(W, X)  # host tensors
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/awq.h compiles as C99 with warnings as errors, and a C program linked against libawq.so runs
+    the host-only entry points."""
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = os.path.join(os.path.dirname(__file__), "c_abi_check.c")
+    exe = str(tmp_path / "c_abi_check")
+    libdir = os.path.dirname(capi.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), src,
+                    "-o", exe, "-L", libdir, "-lawq", "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert "c abi ok" in r.stdout
