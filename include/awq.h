@@ -308,7 +308,7 @@ AWQ_API awq_status awq_pipeline_workspace_size(int64_t max_n_tok, int64_t max_ou
    of awq_act_stats, awq_search_layer and awq_quantize_pack called one layer
    at a time. Asynchronous: the outputs are in place once `stream` has
    passed this call (work queued on `stream` afterwards waits for the last
-   copy). cfg->w_bit must be 4. ws: device, awq_pipeline_workspace_size()
+   copy). cfg->w_bit 2, 4 or 8 (packed as by awq_quantize_pack). ws: device, awq_pipeline_workspace_size()
    bytes for the largest layer dimensions; its first 4 bytes are the status
    word, which keeps the first device-side error of any layer (read it with
    awq_get_device_status). Calls from several host threads are serialised
