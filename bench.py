@@ -1,10 +1,14 @@
 """Benchmark: AWQ per-layer search + INT4 pack on B300, one JSON line.
 
-A step is one pass of the whole path over one synthetic layer, through the C
-ABI: activation statistics, the 20-point alpha search (scales, fake-quant,
-tcgen05 search product with fused squared-error epilogue, loss + argmin) and
-the final pack. Inputs are resident in HBM when the timed region starts; L2
-is flushed (a 512 MiB write) between steps, outside the timed events.
+A step is one pass of the whole path over one synthetic layer through the
+library's public calls: awq_act_stats (activation statistics),
+awq_search_layer (alpha scales, fake-quant, tcgen05 search product with the
+squared-error epilogue, loss + argmin) and awq_quantize_pack (final codes).
+The headline layer is the 70B-class MLP projection (W 28672 x 8192 bf16,
+X 16384 x 8192 bf16, 20 alphas), the largest workload of the suite. Inputs
+are resident in HBM when the timed region starts; they are larger than L2,
+and L2 is flushed (a 512 MiB write) between steps anyway, outside the timed
+events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle, bounded sample
@@ -29,8 +33,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "ms per layer AWQ search+pack (20-pt α grid); % BF16 TC peak and % HBM BW"
-DEFAULT_WORKLOAD = "llama7b_q_proj"
-KERNELS_PER_STEP = 6  # stats, alpha scales, fused fake-quant + search product, loss reduce + select, pack
+DEFAULT_WORKLOAD = "70b_mlp"
+# the other workloads of the suite, each timed through the same calls (one entry per layer, not the headline)
+SIDE_WORKLOADS = ("tiny", "llama7b_q_proj", "llama7b_mlp", "13b_up_proj")
 RUN_AHEAD_CYCLES = 4_000_000  # GPU spin before each timed step so the host enqueues the whole step first
 FLUSH_BYTES = 512 << 20
 
@@ -55,11 +60,11 @@ GEMM_SOURCES = ["post_bit_weight_awq_b300/csrc/awq_search_gemm.cu", "post_bit_we
                 "post_bit_weight_awq_b300/csrc/awq_quant.cuh"]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per launch of the fused search kernel from the committed ncu
-    summary of this workload, if it was taken on the current kernel source;
-    else None."""
-    path = os.path.join(ROOT, "profiles", f"search_fused_{workload}.md")
+def profiled_traffic(kernel_tag, workload):
+    """DRAM bytes per launch of the search kernel from the committed ncu summary
+    profiles/search_<kernel_tag>_<workload>.md, if it was taken on the current
+    kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"search_{kernel_tag}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -115,39 +120,38 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+                "reasons": reasons, "samples": len(rows), "power_w_median": statistics.median(pw) if pw else None,
+                "power_w_max": max(pw, default=None)}
 
 
 # ------------------------------------------------------------------ oracle arm
 
 
-def oracle_layer(workload):
-    import workloads
-
-    return workloads.make_layer(workloads.WORKLOADS[workload][0])
-
-
-def oracle_sample(L, rows):
-    """Run the oracle's statistics, search and pack on the first ``rows``
-    output rows of layer ``L`` (all tokens, all input channels). Returns the
-    seconds taken and the factor that scales the sample to the whole layer."""
+def oracle_sample(L, rows, X64=None):
+    """Run the oracle's statistics over all of X, then its search and pack on
+    the first ``rows`` output rows of layer ``L`` (all tokens, all input
+    channels). The loss is a sum over output rows and s depends only on X, so
+    the sample is the oracle's exact work for those rows. Returns the seconds
+    of the statistics, the seconds of the row sample and the factor out/rows
+    that scales the row sample to the whole layer."""
     import numpy as np
 
     import oracle as O
 
     W = L["W"][:rows].astype(np.float64)
-    X = L["X"].astype(np.float64)
+    X = L["X"].astype(np.float64) if X64 is None else X64
     N = L["W"].shape[0]
     t0 = time.perf_counter()
     sx = O.channel_importance(X)
+    t1 = time.perf_counter()
     res = O.search_scale(W, X, sx)
     O.quantize_pack(W, O.f32(res["s_best"]))
-    dt = time.perf_counter() - t0
-    return dt, N / rows
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1, N / rows
 
 
 def blas_threads():
@@ -160,31 +164,306 @@ def blas_threads():
 
 
 def reference_arm(args, rank):
+    """The CPU oracle as it stands on this host's cores, on a bounded row sample of the same layer per step."""
     if rank != 0:
         return
-    rows = args.oracle_rows
-    L = oracle_layer(args.workload)
+    import numpy as np
+
+    import workloads
+
+    name = workloads.WORKLOADS[args.workload][0]
+    L = workloads.make_layer(name)
+    X64 = L["X"].astype(np.float64)
+    rows = args.reference_rows
     for _ in range(args.warmup):
-        oracle_sample(L, rows)
-    times = []
+        oracle_sample(L, rows, X64)
+    stats_s, rows_s = [], []
     scale = 1.0
+    t_run = time.perf_counter()
     for _ in range(args.steps):
-        dt, scale = oracle_sample(L, rows)
-        times.append(dt * scale * 1e3)
-    ms = statistics.mean(times)
+        ts, tr, scale = oracle_sample(L, rows, X64)
+        stats_s.append(ts)
+        rows_s.append(tr)
+    wall = time.perf_counter() - t_run
+    sample_ms = (statistics.mean(stats_s) + statistics.mean(rows_s)) * 1e3
+    ms = (statistics.mean(stats_s) + statistics.mean(rows_s) * scale) * 1e3
     cores = blas_threads()
-    sample = (f"oracle statistics+search+pack on output rows [0,{rows}) of the layer (all tokens), "
-              f"time scaled by out/rows = {scale:g} to one layer")
-    line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "n_grid": 20, "group": 128},
-            "cpu_baseline": {"value": ms, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample},
-            "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    sample = (f"oracle statistics over all {L['X'].shape[0]} tokens ({statistics.mean(stats_s):.2f} s) + search and "
+              f"pack of output rows [0,{rows}) of the {name} layer ({statistics.mean(rows_s):.2f} s) per step; "
+              f"value = statistics + rows time x out/rows = {scale:g}, one layer")
+    line = {"impl": "reference", "metric": METRIC, "value": round(ms, 1), "unit": "ms", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sample_ms, 1),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "layer": name, "W": list(L["W"].shape), "X": list(L["X"].shape),
+                       "n_grid": 20, "group": 128},
+            "cpu_baseline": {"value": round(ms, 1), "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(ms, 1), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s_timed_steps": round(wall, 2)}
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ GPU arm
+
+
+def timed(fn, flush, reps):
+    """Median CUDA-event time (ms) of fn() over reps runs, L2 flushed before each."""
+    import torch
+
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def hbm_bytes(n, N, K, G, wbytes):
+    """Algorithmic bytes of the bandwidth kernels: the statistics read X once; the fake-quant reads W once and
+    writes G bf16 operands; the pack reads W and writes the codes, fp16 scales and zeros."""
+    return {"stats": 2.0 * n * K, "fakequant": wbytes * N * K + G * 2.0 * N * K,
+            "pack": wbytes * N * K + N * K / 2 + 4.0 * N * K / 128}
+
+
+class LayerRun:
+    """One layer resident on the device with the buffers of the three public calls."""
+
+    def __init__(self, name, dev, cfg):
+        import numpy as np
+        import torch
+
+        import workloads
+        from post_bit_weight_awq_b300 import capi
+
+        self.name = name
+        L = workloads.make_layer(name)
+        self.L = L
+        W32, X32 = L["W"], L["X"]
+        self.N, self.K = W32.shape
+        self.n = X32.shape[0]
+        self.cfg = cfg
+        self.G = cfg.n_grid
+        self.wbytes = 2 if L["w_dtype"] == "bf16" else 4
+
+        def to_dev_bf16(a):
+            return torch.from_numpy(workloads.bf16_bits(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        self.W = to_dev_bf16(W32) if L["w_dtype"] == "bf16" else torch.from_numpy(W32).to(dev)
+        self.X = to_dev_bf16(X32)
+        n, N, K, G = self.n, self.N, self.K, self.G
+        f32 = torch.float32
+        self.mean_abs = torch.empty(K, dtype=f32, device=dev)
+        self.ws = torch.empty(max(capi.awq_workspace_size(n, N, K, cfg), capi.awq_act_stats_workspace_size(n, K)),
+                              dtype=torch.uint8, device=dev)
+        self.losses = torch.empty(G, dtype=f32, device=dev)
+        self.best = torch.empty(1, dtype=torch.int32, device=dev)
+        self.s_best = torch.empty(K, dtype=f32, device=dev)
+        self.qw = torch.empty(N, K // 8, dtype=torch.int32, device=dev)
+        self.sc = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+        self.zr = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+        self.flops = 2.0 * G * n * N * K
+
+    def step(self, ev=None):
+        """awq_act_stats, awq_search_layer, awq_quantize_pack on the current stream (events between the calls)."""
+        import torch
+
+        from post_bit_weight_awq_b300 import capi
+
+        st = torch.cuda.current_stream()
+        if ev:
+            ev[0].record(st)
+        capi.awq_act_stats(self.X, self.mean_abs, self.ws, st)
+        if ev:
+            ev[1].record(st)
+        capi.awq_search_layer(self.W, self.X, self.mean_abs, self.cfg, self.losses, self.best, self.s_best, self.ws,
+                              st)
+        if ev:
+            ev[2].record(st)
+        capi.awq_quantize_pack(self.W, self.s_best, self.cfg, self.qw, self.sc, self.zr, st)
+        if ev:
+            ev[3].record(st)
+
+    def parity(self):
+        """Per-alpha losses of the last step against the stored oracle losses of this layer."""
+        import numpy as np
+
+        gpath = os.path.join(ROOT, "tests", "golden", "oracle_losses.json")
+        if not os.path.exists(gpath):
+            return None
+        g = json.load(open(gpath)).get(self.name)
+        if not g:
+            return None
+        lo = np.array(g["losses"])
+        lg = self.losses.cpu().numpy().astype(np.float64)
+        b = int(self.best[0])
+        return {"max_rel_loss_err": float(np.max(np.abs(lg - lo) / lo)), "gpu_best_idx": b,
+                "oracle_best_idx": g["best_idx"], "oracle_loss_at_gpu_best_over_min": float(lo[b] / lo.min())}
+
+
+def stage_kernels(R, flush, reps):
+    """Each kernel awq_search_layer may run, launched alone through the stage calls, plus the statistics and
+    pack calls: median CUDA-event ms per launch, L2 flushed before each."""
+    import torch
+
+    from post_bit_weight_awq_b300 import capi, capi_testing
+
+    dev = R.W.device
+    G, N, K, n = R.G, R.N, R.K, R.n
+    s = torch.empty(G, K, dtype=torch.float32, device=dev)
+    inv = torch.empty_like(s)
+    op = torch.empty(G, N, K, dtype=torch.bfloat16, device=dev)
+    mt, nt, _, _ = capi_testing.awq_search_tiles(n, N, R.cfg)
+    parts = torch.empty(G, mt, nt, 4, dtype=torch.float32, device=dev)
+    ready = torch.zeros(G * (nt + 1) + 1, dtype=torch.int32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    losses = torch.empty(G, dtype=torch.float32, device=dev)
+    best = torch.empty(1, dtype=torch.int32, device=dev)
+    s_best = torch.empty(K, dtype=torch.float32, device=dev)
+    capi_testing.awq_alpha_scales(R.mean_abs, R.cfg, s, inv)
+    calls = {
+        "stats": lambda: capi.awq_act_stats(R.X, R.mean_abs, R.ws),
+        "alpha_scales": lambda: capi_testing.awq_alpha_scales(R.mean_abs, R.cfg, s, inv),
+        "fused_search": lambda: capi_testing.awq_search_fused(R.W, R.X, s, inv, R.cfg, op, parts, ready, status),
+        "fakequant": lambda: capi_testing.awq_fakequant(R.W, s, inv, R.cfg, op),
+        "search_gemm": lambda: capi_testing.awq_search_gemm(R.X, op, R.cfg, parts, status, n_tok=n, in_features=K,
+                                                            out_features=N),
+        "loss_select": lambda: capi_testing.awq_loss_select(parts, s, R.cfg, losses, best, s_best, status, n_tok=n,
+                                                            out_features=N, in_features=K),
+        "pack": lambda: capi.awq_quantize_pack(R.W, R.s_best, R.cfg, R.qw, R.sc, R.zr),
+    }
+    out = {}
+    for nm, fn in calls.items():
+        fn()
+        torch.cuda.synchronize()
+        out[nm] = timed(fn, flush, reps)
+    if int(status[0]) != 0:
+        raise RuntimeError("device status " + capi.status_string(int(status[0])))
+    del op
+    return out
+
+
+def fractions(R, ms, pk):
+    """Per-kernel achieved rates and fractions of the measured peaks."""
+    hb = hbm_bytes(R.n, R.N, R.K, R.G, R.wbytes)
+    d = {}
+    for nm, t in ms.items():
+        e = {"ms": round(t, 4)}
+        if nm in hb:
+            gbs = hb[nm] / (t * 1e-3) / 1e9
+            e.update({"bytes": hb[nm], "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)})
+        if nm in ("fused_search", "search_gemm"):
+            tf = R.flops / (t * 1e-3) / 1e12
+            e.update({"tflops": round(tf, 1), "frac_bf16_burst": round(tf / pk["bf16_tflops"], 3)})
+            if pk.get("bf16_tflops_sustained"):
+                e["frac_bf16_sustained"] = round(tf / pk["bf16_tflops_sustained"], 3)
+        d[nm] = e
+    return d
+
+
+def side_workload(name, dev, flush, pk, reps):
+    """Statistics, search and pack of each layer of a smaller workload through the public calls (eager, L2
+    flushed before each step), with the search's fraction of the tensor peak and the oracle parity."""
+    import torch
+
+    import workloads
+    from post_bit_weight_awq_b300 import capi, capi_testing
+
+    out = []
+    for layer in workloads.WORKLOADS[name]:
+        R = LayerRun(layer, dev, capi.config())
+        for _ in range(2):
+            R.step()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(reps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            R.step(ev)
+            evs.append(ev)
+        torch.cuda.synchronize()
+        assert capi.awq_get_device_status(R.ws) == capi.AWQ_OK
+        st = [statistics.median(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(3)]
+        hb = hbm_bytes(R.n, R.N, R.K, R.G, R.wbytes)
+        tf = R.flops / (st[1] * 1e-3) / 1e12
+        out.append({
+            "layer": layer, "W": [R.N, R.K], "X": [R.n, R.K], "ms_per_layer": round(sum(st), 4),
+            "stats_ms": round(st[0], 4), "stats_frac_hbm": round(hb["stats"] / (st[0] * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+            "search_ms": round(st[1], 4), "search_tflops": round(tf, 1),
+            "search_frac_bf16_burst": round(tf / pk["bf16_tflops"], 3),
+            "search_path": ("fused" if R.flops < capi_testing.AWQ_SEARCH_FUSED_MAX_FLOPS
+                            else "fake-quant launch + pair products"),
+            "pack_ms": round(st[2], 4), "pack_frac_hbm": round(hb["pack"] / (st[2] * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+            "parity_vs_oracle": R.parity()})
+        del R
+        torch.cuda.empty_cache()
+    return out
+
+
+def decode_line(R, dev, flush, pk, reps):
+    """awq_w4a16_gemv on the packed layer of the step, one token: enough copies of the layer to exceed L2,
+    applied one after another (a decode step running through layers), L2 flushed before each pass."""
+    import torch
+
+    from post_bit_weight_awq_b300 import capi
+
+    N, K = R.N, R.K
+    if K > capi.AWQ_W4A16_MAX_TOKEN_CHANNELS:
+        return None
+    layer_bytes = N * K // 2 + 2 * 2 * N * (K // 128)
+    copies = max(3, int((256 << 20) // layer_bytes) + 1)
+    packs = [(R.qw.clone(), R.sc.clone(), R.zr.clone()) for _ in range(copies)]
+    xg = torch.randn(1, K, device=dev).to(torch.bfloat16)
+    yg = torch.empty(1, N, dtype=torch.float32, device=dev)
+
+    def one_pass():
+        for q_, s_, z_ in packs:
+            capi.awq_w4a16_gemv(xg, q_, s_, z_, R.cfg, yg)
+
+    one_pass()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        one_pass()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ms = timed(g.replay, flush, reps) / copies
+    gbytes = layer_bytes + K * 2 + N * 4
+    del packs
+    return {"kernel": "w4a16_gemv_kernel<1, R>", "tokens": 1, "layer": [N, K], "ms_per_layer": round(ms, 5),
+            "bytes_per_layer": gbytes, "gbs": round(gbytes / (ms * 1e-3) / 1e9, 1),
+            "frac_hbm": round(gbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+            "timing": f"{copies} distinct copies per CUDA graph (> L2), L2 flushed before each graph"}
+
+
+def prefill_line(R, dev, flush, pk, reps):
+    """awq_w4a16_gemm on the packed layer of the step, 2048 prompt tokens (expansion + tensor-core product)."""
+    import torch
+
+    from post_bit_weight_awq_b300 import capi
+
+    N, K = R.N, R.K
+    Mp = 2048
+    xp = torch.randn(Mp, K, device=dev).to(torch.bfloat16)
+    yp = torch.empty(Mp, N, dtype=torch.float32, device=dev)
+    gws = torch.empty(capi.awq_w4a16_gemm_workspace_size(Mp, K, N, R.cfg), dtype=torch.uint8, device=dev)
+
+    def call():
+        capi.awq_w4a16_gemm(xp, R.qw, R.sc, R.zr, R.cfg, yp, gws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ms = timed(call, flush, reps)
+    assert capi.awq_get_device_status(gws) == capi.AWQ_OK
+    pflops = 2.0 * Mp * N * K
+    del gws, xp, yp
+    return {"call": "awq_w4a16_gemm (bf16 expansion of the packed layer + tcgen05 CTA-pair product)", "tokens": Mp,
+            "layer": [N, K], "ms": round(ms, 5), "tflops": round(pflops / (ms * 1e-3) / 1e12, 1),
+            "frac_bf16_burst": round(pflops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"], 3),
+            "timing": "median of CUDA-event timed calls, L2 flushed before each"}
 
 
 def gpu_arm(args, rank, world, local_rank):
@@ -192,7 +471,7 @@ def gpu_arm(args, rank, world, local_rank):
     import torch
 
     import workloads
-    from post_bit_weight_awq_b300 import build, capi, multi
+    from post_bit_weight_awq_b300 import build, capi, capi_testing, multi
 
     build.build()
     capi.lib()
@@ -204,94 +483,37 @@ def gpu_arm(args, rank, world, local_rank):
 
         dist.init_process_group("nccl", device_id=dev)
 
+    pk = peaks()
     name = workloads.WORKLOADS[args.workload][0]
-    L = workloads.make_layer(name)
-    W32, X32 = L["W"], L["X"]
-    N, K = W32.shape
-    n = X32.shape[0]
     cfg = capi.config()
-    G = cfg.n_grid
-
-    def to_dev_bf16(a):
-        return torch.from_numpy(workloads.bf16_bits(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    Wd = to_dev_bf16(W32) if L["w_dtype"] == "bf16" else torch.from_numpy(W32).to(dev)
-    Xd = to_dev_bf16(X32)
-    f32, i32, u8 = torch.float32, torch.int32, torch.uint8
-    mean_abs = torch.empty(K, dtype=f32, device=dev)
-    stats_ws = torch.empty(capi.awq_act_stats_workspace_size(n, K), dtype=u8, device=dev)
-    s = torch.empty(G, K, dtype=f32, device=dev)
-    inv = torch.empty_like(s)
-    op = torch.empty(G, N, K, dtype=torch.bfloat16, device=dev)
-    mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
-    parts = torch.empty(G, mt, nt, 4, dtype=f32, device=dev)
-    ready = torch.zeros(G * (nt + 1) + 1, dtype=i32, device=dev)
-    status = torch.zeros(4, dtype=i32, device=dev)
-    losses = torch.empty(G, dtype=f32, device=dev)
-    best = torch.empty(1, dtype=i32, device=dev)
-    s_best = torch.empty(K, dtype=f32, device=dev)
-    qw = torch.empty(N, K // 8, dtype=i32, device=dev)
-    sc = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
-    zr = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=u8, device=dev)
+    R = LayerRun(name, dev, cfg)
+    n, N, K, G = R.n, R.N, R.K, R.G
+    flops = R.flops
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step(ev=None):
-        # the same kernels, in the same order, as awq_act_stats + awq_search_layer + awq_quantize_pack;
-        # launched on the current stream (the capture stream while a CUDA graph is recorded)
-        st = torch.cuda.current_stream(dev)
-        if ev:
-            ev[0].record(st)
-        capi.awq_act_stats(Xd, mean_abs, stats_ws, st)
-        if ev:
-            ev[1].record(st)
-        capi.awq_alpha_scales(mean_abs, cfg, s, inv, st)
-        if ev:
-            ev[2].record(st)
-        capi.awq_search_fused(Wd, Xd, s, inv, cfg, op, parts, ready, status, st)
-        if ev:
-            ev[3].record(st)
-        capi.awq_loss_select(parts, s, cfg, losses, best, s_best, status, st, n_tok=n, out_features=N,
-                             in_features=K)
-        if ev:
-            ev[4].record(st)
-        capi.awq_quantize_pack(Wd, s_best, cfg, qw, sc, zr, st)
-        if ev:
-            ev[5].record(st)
-
-    def unfused(ev):
-        # the fake-quant and the search product as separate launches (what the fused kernel overlaps)
-        st = torch.cuda.current_stream(dev)
-        ev[0].record(st)
-        capi.awq_fakequant(Wd, s, inv, cfg, op, st)
-        ev[1].record(st)
-        capi.awq_search_gemm(Xd, op, cfg, parts, status, st, n_tok=n, in_features=K, out_features=N)
-        ev[2].record(st)
 
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        R.step()
     torch.cuda.synchronize()
-    assert int(status[0]) == 0, capi.status_string(int(status[0]))
+    assert capi.awq_get_device_status(R.ws, stream) == capi.AWQ_OK
 
     # the whole step as one CUDA graph (no host launch gaps between kernels)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        step()
+        R.step()
     for _ in range(args.warmup):
         flush.zero_()
         graph.replay()
     torch.cuda.synchronize()
     # the replayed graph must reproduce the eager step's results
-    losses_eager = losses.clone()
-    losses.zero_()
+    losses_eager = R.losses.clone()
+    R.losses.zero_()
     graph.replay()
     torch.cuda.synchronize()
-    if not torch.equal(losses, losses_eager):
+    if not torch.equal(R.losses, losses_eager):
         raise RuntimeError("graph replay does not reproduce the eager step")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    uevents = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     if dist:
@@ -311,54 +533,58 @@ def gpu_arm(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    # per-stage device times: the same step launched eagerly, host run ahead of the GPU
-    for k in range(args.steps):
-        flush.zero_()
-        torch.cuda._sleep(RUN_AHEAD_CYCLES)
-        step(events[k])
-    torch.cuda.synchronize()
-    if int(status[0]) != 0:
-        raise RuntimeError("device status " + capi.status_string(int(status[0])))
-    for k in range(args.steps):
-        flush.zero_()
-        torch.cuda._sleep(RUN_AHEAD_CYCLES)
-        unfused(uevents[k])
-    torch.cuda.synchronize()
-    if int(status[0]) != 0:
-        raise RuntimeError("device status " + capi.status_string(int(status[0])))
-
-    stage_names = ["stats", "alpha_scales", "search", "loss_select", "pack"]
-    per_stage = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in events) for i, nm in enumerate(stage_names)}
-    alone = {"fakequant": statistics.mean(e[0].elapsed_time(e[1]) for e in uevents),
-             "search_gemm": statistics.mean(e[1].elapsed_time(e[2]) for e in uevents)}
+    assert capi.awq_get_device_status(R.ws, stream) == capi.AWQ_OK
     step_ms = [a.elapsed_time(b) for a, b in gev]
     ms_step = statistics.mean(step_ms)
-    ms_step_eager = statistics.mean(e[0].elapsed_time(e[5]) for e in events)
     t_total = sum(step_ms)
     if dist:
         t_total = multi.max_over_ranks(t_total, device=dev)
-    layers = args.steps * world
-    value = t_total / layers
+    value = t_total / (args.steps * world)
+    parity = R.parity()
+
+    # the three public calls of the step, timed one by one (eager, events between the calls)
+    evs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda._sleep(RUN_AHEAD_CYCLES)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        R.step(ev)
+        evs.append(ev)
+    torch.cuda.synchronize()
+    calls_ms = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, nm in enumerate(("awq_act_stats", "awq_search_layer", "awq_quantize_pack"))}
+
+    # each kernel alone (stage calls), for the per-kernel rooflines
+    kern = fractions(R, stage_kernels(R, flush, max(3, args.steps // 4)), pk)
+    fused_path = flops < capi_testing.AWQ_SEARCH_FUSED_MAX_FLOPS
+    search_kernel = "fused_search" if fused_path else "search_gemm"
+    search_ms = kern[search_kernel]["ms"]
+    achieved = flops / (search_ms * 1e-3) / 1e12
+    long_step = ms_step > 100.0  # a timed region of seconds settles at the power cap
+    sustained = pk.get("bf16_tflops_sustained")
+    peak, peak_kind = (sustained, "sustained") if (long_step and sustained) else (pk["bf16_tflops"], "burst")
 
     # ---------------------------------------------------------- end to end (host buffers)
     # the public layer pipeline (awq_quantize_layers): K layers whose W and X sit in pinned host memory, each
     # copied in, searched, packed and copied out; the copies of one layer overlap the search of the next
+    L = R.L
     pin = dict(pin_memory=True)
-    Wh = (torch.from_numpy(workloads.bf16_bits(W32).view(np.int16)).view(torch.bfloat16) if L["w_dtype"] == "bf16"
-          else torch.from_numpy(W32)).clone().pin_memory()
-    Xh = torch.from_numpy(workloads.bf16_bits(X32).view(np.int16)).view(torch.bfloat16).clone().pin_memory()
-    outs_h = {"qweight": torch.empty(N, K // 8, dtype=i32, **pin), "scales": torch.empty(N, K // 128,
-                                                                                      dtype=torch.float16, **pin),
-              "zeros": torch.empty(N, K // 128, dtype=torch.float16, **pin), "losses": torch.empty(G, dtype=f32, **pin),
-              "best_idx": torch.empty(1, dtype=i32, **pin), "s_best": torch.empty(K, dtype=f32, **pin)}
-    del op
+    Wh = (torch.from_numpy(workloads.bf16_bits(L["W"]).view(np.int16)).view(torch.bfloat16) if L["w_dtype"] == "bf16"
+          else torch.from_numpy(L["W"])).pin_memory()
+    Xh = torch.from_numpy(workloads.bf16_bits(L["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    outs_h = {"qweight": torch.empty(N, K // 8, dtype=torch.int32, **pin),
+              "scales": torch.empty(N, K // 128, dtype=torch.float16, **pin),
+              "zeros": torch.empty(N, K // 128, dtype=torch.float16, **pin),
+              "losses": torch.empty(G, dtype=torch.float32, **pin),
+              "best_idx": torch.empty(1, dtype=torch.int32, **pin),
+              "s_best": torch.empty(K, dtype=torch.float32, **pin)}
     wcode = capi.AWQ_BF16 if L["w_dtype"] == "bf16" else capi.AWQ_FP32
-    pipe_ws = torch.empty(capi.awq_pipeline_workspace_size(n, N, K, wcode, cfg), dtype=u8, device=dev)
+    pipe_ws = torch.empty(capi.awq_pipeline_workspace_size(n, N, K, wcode, cfg), dtype=torch.uint8, device=dev)
     h2d = Wh.numel() * Wh.element_size() + Xh.numel() * Xh.element_size()
     d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
     io = capi.layer_io(Wh, Xh, outs_h["qweight"], outs_h["scales"], outs_h["zeros"], outs_h["losses"],
                        outs_h["best_idx"], outs_h["s_best"])
-    capi.awq_quantize_layers([io] * max(3, args.warmup), wcode, cfg, pipe_ws, stream)
+    capi.awq_quantize_layers([io] * 3, wcode, cfg, pipe_ws, stream)
     torch.cuda.synchronize()
     ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     flush.zero_()
@@ -370,220 +596,66 @@ def gpu_arm(args, rank, world, local_rank):
     if dist:
         e2e_ms = multi.max_over_ranks(e2e_ms, device=dev) / world
     assert capi.awq_get_device_status(pipe_ws, stream) == capi.AWQ_OK
-    assert int(outs_h["best_idx"][0]) == int(best[0])  # the streamed layer chose what the device path chose
-    del pipe_ws
+    assert int(outs_h["best_idx"][0]) == int(R.best[0])  # the streamed layer chose what the device path chose
+    assert torch.equal(outs_h["qweight"], R.qw.cpu())  # and packed the same codes
+    del pipe_ws, Wh, Xh
 
-    # ---------------------------------------------------------- the packed layer in use (w4a16 decode product)
-    # copies of the packed layer, more bytes than L2, applied one after another to one token (a decode step
-    # running through layers): HBM bandwidth of awq_w4a16_gemv
-    gemv = None
-    if K * 4 <= 50 * 1024:
-        layer_bytes = N * K // 2 + 2 * 2 * N * (K // 128)
-        copies = max(4, int((256 << 20) // layer_bytes) + 1)
-        packs = [(qw.clone(), sc.clone(), zr.clone()) for _ in range(copies)]
-        xg = torch.randn(1, K, device=dev).to(torch.bfloat16)
-        yg = torch.empty(1, N, dtype=f32, device=dev)
-        gcfg = capi.config()
+    # ---------------------------------------------------------- the packed layer in use
+    gemv = decode_line(R, dev, flush, pk, max(3, args.steps // 2))
+    gemm = prefill_line(R, dev, flush, pk, max(3, args.steps // 2))
 
-        def gemv_pass():
-            st = torch.cuda.current_stream(dev)
-            for q_, s_, z_ in packs:
-                capi.awq_w4a16_gemv(xg, q_, s_, z_, gcfg, yg, st)
-
-        gemv_pass()
-        gg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gg):
-            gemv_pass()
-        for _ in range(3):
-            gg.replay()
-        torch.cuda.synchronize()
-        gt = []
-        for _ in range(max(3, args.steps // 2)):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            gg.replay()
-            b.record(stream)
-            torch.cuda.synchronize()
-            gt.append(a.elapsed_time(b) / copies)
-        ms_g = statistics.median(gt)
-        gbytes = layer_bytes + K * 2 + N * 4
-        gemv = {"kernel": "w4a16_gemv_kernel<1, R> (R rows per warp, chosen by the launcher)", "tokens": 1, "layer": [N, K], "ms_per_layer": round(ms_g, 5),
-                "bytes_per_layer": gbytes, "gbs": round(gbytes / (ms_g * 1e-3) / 1e9, 1),
-                "frac_hbm": round(gbytes / (ms_g * 1e-3) / 1e9 / peaks()["hbm_gbs"], 3),
-                "timing": f"{copies} distinct copies per CUDA graph (> L2), L2 flushed before each graph"}
-        del packs
-
-    # ---------------------------------------------------------- the packed layer in a prefill (2048 prompt tokens)
-    # expand to bf16 in the workspace, then the tensor-core product (awq_w4a16_gemm); L2 flushed before each run
-    gemm = None
-    Mp = 2048
-    xp = torch.randn(Mp, K, device=dev).to(torch.bfloat16)
-    yp = torch.empty(Mp, N, dtype=f32, device=dev)
-    gws = torch.empty(capi.awq_w4a16_gemm_workspace_size(Mp, K, N, cfg), dtype=u8, device=dev)
-    for _ in range(3):
-        capi.awq_w4a16_gemm(xp, qw, sc, zr, cfg, yp, gws, stream)
-    torch.cuda.synchronize()
-    pt = []
-    for _ in range(max(3, args.steps // 2)):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        capi.awq_w4a16_gemm(xp, qw, sc, zr, cfg, yp, gws, stream)
-        b.record(stream)
-        torch.cuda.synchronize()
-        pt.append(a.elapsed_time(b))
-    assert capi.awq_get_device_status(gws, stream) == capi.AWQ_OK
-    ms_p = statistics.median(pt)
-    pflops = 2.0 * Mp * N * K
-    gemm = {"call": "awq_w4a16_gemm (bf16 expansion of the packed layer + tcgen05 CTA-pair product)", "tokens": Mp,
-            "layer": [N, K], "ms": round(ms_p, 5), "tflops": round(pflops / (ms_p * 1e-3) / 1e12, 1),
-            "frac_bf16_burst": round(pflops / (ms_p * 1e-3) / 1e12 / peaks()["bf16_tflops"], 3),
-            "timing": "median of CUDA-event timed calls, L2 flushed before each"}
-    del gws, xp, yp
-
-    # ---------------------------------------------------------- bandwidth kernels on the largest layer
-    # the statistics, fake-quant and pack kernels move 33-700 MB on the benchmark layer, a few microseconds of
-    # work beside a few microseconds of launch and ramp; on the 70B-class MLP layer they move 0.27-9.9 GB
-    large = None if args.no_large else large_layer_rates(dev, flush, peaks()["hbm_gbs"])
-
-    # ---------------------------------------------------------- parity spot check vs stored oracle losses
-    parity = None
-    gpath = os.path.join(ROOT, "tests", "golden", "oracle_losses.json")
-    if os.path.exists(gpath):
-        g = json.load(open(gpath)).get(name)
-        if g:
-            lo = np.array(g["losses"])
-            lg = outs_h["losses"].numpy().astype(np.float64)
-            parity = {"max_rel_loss_err": float(np.max(np.abs(lg - lo) / lo)),
-                      "gpu_best_idx": int(outs_h["best_idx"][0]), "oracle_best_idx": g["best_idx"],
-                      "oracle_loss_at_gpu_best_over_min": float(lo[int(outs_h["best_idx"][0])] / lo.min())}
+    # ---------------------------------------------------------- the other workloads, one entry per layer
+    side = None
+    del R, graph
+    torch.cuda.empty_cache()
+    if not args.no_side and world == 1:
+        side = {w: side_workload(w, dev, flush, pk, 5) for w in SIDE_WORKLOADS}
 
     if dist:
         dist.destroy_process_group()
     if rank != 0:
         return
 
-    pk = peaks()
-    flops = G * 2.0 * n * K * N
-    search_ms = per_stage["search"]
-    achieved = flops / (search_ms * 1e-3) / 1e12
-    traffic = profiled_traffic(args.workload)
-    wbytes = 2 if L["w_dtype"] == "bf16" else 4
-    hbm_bytes = {
-        "stats": 2.0 * n * K,
-        "fakequant": wbytes * N * K + G * 2.0 * N * K,
-        "pack": wbytes * N * K + N * K / 2 + 4.0 * N * K / 128,
-    }
-
-    def tensor_fracs(tf):
-        d = {"tflops": round(tf, 1), "frac_bf16_burst": round(tf / pk["bf16_tflops"], 3)}
-        if pk.get("bf16_tflops_sustained"):
-            d["frac_bf16_sustained"] = round(tf / pk["bf16_tflops_sustained"], 3)
-        return d
-
-    def hbm_fracs(nm, ms):
-        gbs = hbm_bytes[nm] / (ms * 1e-3) / 1e9
-        return {"gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)}
-
-    stages = {}
-    for nm, ms in per_stage.items():
-        d = {"ms": round(ms, 4)}
-        if nm in hbm_bytes:
-            d.update(hbm_fracs(nm, ms))
-        if nm == "search":
-            d["kernel"] = "search_gemm_pair_kernel<fused> (fake-quant warps + tcgen05 pair products)"
-            d.update(tensor_fracs(achieved))
-        stages[nm] = d
-    # the two halves of the fused stage launched separately, for the per-kernel rooflines
-    separate = {"fakequant": {"ms": round(alone["fakequant"], 4), **hbm_fracs("fakequant", alone["fakequant"])},
-                "search_gemm": {"ms": round(alone["search_gemm"], 4),
-                                **tensor_fracs(flops / (alone["search_gemm"] * 1e-3) / 1e12)}}
-
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        dt, scale = oracle_sample(L, args.oracle_rows)
-        cpu = {"value": dt * scale * 1e3, "unit": "ms", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"oracle search+pack on output rows [0,{args.oracle_rows}) of the layer (all tokens), "
-                         f"{dt:.1f} s, scaled by out/rows = {scale:g} to one layer"}
+        ts, tr, scale = oracle_sample(L, args.oracle_rows)
+        cpu = {"value": round((ts + tr * scale) * 1e3, 1), "unit": "ms", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"oracle statistics over all {n} tokens ({ts:.1f} s) + search and pack of output rows "
+                         f"[0,{args.oracle_rows}) ({tr:.1f} s), the rows scaled by out/rows = {scale:g} to one layer"}
 
+    kernel_names = {"fused_search": "search_gemm_pair_kernel<fused> (quantiser warps + tcgen05 pair products)",
+                    "search_gemm": "search_gemm_pair_kernel (tcgen05 pair products; fake-quant launched before it)"}
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "layer": name, "W": [N, K], "X": [n, K], "w_dtype": L["w_dtype"],
                    "n_grid": G, "group": 128, "loss_form": "residual", "parallelism": f"replicas{world}",
-                   "launch": "whole step replayed as one CUDA graph",
-                   "l2": "flushed between steps (512 MiB write outside the timed events)"},
-        "ms_per_step_eager": round(ms_step_eager, 4),
-        "roofline": {"bound": "tensor", "kernel": "search_gemm_pair_kernel<fused>", "achieved": round(achieved, 1),
-                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 3),
-                     "traffic": traffic, "peak_source": f"{pk['source']} bf16 burst",
-                     "algorithmic_flops_per_launch": flops},
-        "stages": stages,
-        "stages_unfused": separate,
-        "w4a16_gemv": gemv,
-        "w4a16_gemm_prefill": gemm,
-        "bandwidth_kernels_70b_layer": large,
+                   "calls": "awq_act_stats + awq_search_layer + awq_quantize_pack",
+                   "launch": "the three calls captured as one CUDA graph and replayed",
+                   "l2": "inputs larger than L2, and L2 flushed between steps (512 MiB write outside the timed events)"},
+        "roofline": {"bound": "tensor", "kernel": kernel_names[search_kernel], "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
+                     "traffic": profiled_traffic("fused" if fused_path else "pair", args.workload),
+                     "peak_source": f"{pk['source']} bf16 {peak_kind}", "algorithmic_flops_per_launch": flops,
+                     "launch_ms": search_ms},
+        "calls": {k: round(v, 4) for k, v in calls_ms.items()},
+        "kernels": kern,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "awq_quantize_layers: steps layers in one call, each layer's W and X copied in from pinned "
                        "host memory and its packed outputs, losses and s_best copied out, copies overlapping the "
                        "previous layer's search (no L2 flush inside the call)"},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        # stats, alpha scales, [fake-quant,] search product, loss reduce, select, pack
+        "gpu_launches": (6 if fused_path else 7) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
         "parity_vs_oracle": parity,
+        "w4a16_gemv": gemv,
+        "w4a16_gemm_prefill": gemm,
+        "other_workloads": side,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
-
-
-def large_layer_rates(dev, flush, hbm_gbs):
-    """Time the statistics, fake-quant and pack kernels alone on the 70B-class MLP shape (W 28672 x 8192
-    bf16, X 16384 x 8192 bf16, 20 alphas; random data, timing only), L2 flushed before each launch."""
-    import torch
-
-    from post_bit_weight_awq_b300 import capi
-
-    n, N, K = 16384, 28672, 8192
-    cfg = capi.config()
-    G = cfg.n_grid
-    X = torch.randn(n, K, device=dev).to(torch.bfloat16)
-    W = (torch.randn(N, K, device=dev) * 0.01).to(torch.bfloat16)
-    mean = torch.empty(K, dtype=torch.float32, device=dev)
-    sws = torch.empty(capi.awq_act_stats_workspace_size(n, K), dtype=torch.uint8, device=dev)
-    s = torch.empty(G, K, dtype=torch.float32, device=dev)
-    inv = torch.empty_like(s)
-    op = torch.empty(G, N, K, dtype=torch.bfloat16, device=dev)
-    qw = torch.empty(N, K // 8, dtype=torch.int32, device=dev)
-    sc = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
-    zr = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
-    capi.awq_act_stats(X, mean, sws)
-    capi.awq_alpha_scales(mean, cfg, s, inv)
-    calls = {
-        "stats": (lambda: capi.awq_act_stats(X, mean, sws), 2.0 * n * K),
-        "fakequant": (lambda: capi.awq_fakequant(W, s, inv, cfg, op), 2.0 * N * K + G * 2.0 * N * K),
-        "pack": (lambda: capi.awq_quantize_pack(W, s[7], cfg, qw, sc, zr), 2.0 * N * K + N * K / 2 + 4.0 * N * K / 128),
-    }
-    out = {"layer": {"W": [N, K], "X": [n, K], "n_grid": G}, "data": "random, timing only"}
-    for name, (fn, nbytes) in calls.items():
-        fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(5):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        ms = statistics.median(ts)
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        out[name] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 3)}
-    del op, X, W
-    torch.cuda.empty_cache()
-    return out
 
 
 def main():
@@ -593,9 +665,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--oracle-rows", type=int, default=256)
+    ap.add_argument("--oracle-rows", type=int, default=128, help="output rows of the cpu_baseline sample")
+    ap.add_argument("--reference-rows", type=int, default=64, help="output rows per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-large", action="store_true", help="skip the 70B-class bandwidth-kernel timings")
+    ap.add_argument("--no-side", action="store_true", help="skip the entries of the other workloads")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

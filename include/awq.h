@@ -144,9 +144,9 @@ AWQ_API const char* awq_status_string(int status);
 AWQ_API awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_t* bytes);
 
 /* mean_abs[j] = (1/n_tok) sum_t |X[t, j]|  (fp32 out; fp32 partial sums over
-   blocks of 128 tokens, a compensated fp32 sum across blocks, fixed order:
-   deterministic). One kernel, preceded by a small memset of the scratch's
-   ticket counters on `stream`.
+   chunks of tokens whose length depends only on n_tok and in, a compensated
+   fp32 sum across chunks, fixed order: deterministic). One kernel, preceded
+   by a small memset of the scratch's ticket counters on `stream`.
    X: device bf16 [n_tok][in] (x_dtype must be AWQ_BF16). in % 8 == 0.
    mean_abs: device fp32 [in]. ws: device scratch of at least the queried
    size. Source: "AWQ: How Activation-Aware Quantization Saves 4-bit LLMs",
@@ -155,8 +155,11 @@ AWQ_API awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_
 AWQ_API awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, int64_t in,
                          float* mean_abs, void* ws, size_t ws_bytes, awq_stream_t stream);
 
-/* Largest ceil(n_tok / 128) * in that awq_act_stats_noalloc accepts (its
-   fixed scratch: 4 MiB of fp32 partial sums, plus 16 KiB of counters). */
+/* Largest number of fp32 partial sums (awq_act_stats_workspace_size less
+   its counters, i.e. chunks * in with at most 592 / ceil(in / 256) + 1
+   chunks of tokens) that awq_act_stats_noalloc accepts: its fixed scratch
+   holds 4 MiB of partial sums plus 16 KiB of counters. Every n_tok is
+   accepted for in up to 896768 channels. */
 #define AWQ_NOALLOC_STATS_MAX_FLOATS (1u << 20)
 
 /* awq_act_stats for callers that cannot allocate device memory or pass a
@@ -167,12 +170,13 @@ AWQ_API awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, 
    the method. Same arguments and result as awq_act_stats without ws/ws_bytes.
    The partial sums live in a library-owned device array (4 MiB + 16 KiB)
    that every GPU loading the library keeps until exit; each call clears the
-   array's counters with a memset on `stream` before its kernel. Its address is looked up on the first
-   call made on each device (with that device current); make that first call
-   before any stream capture. All calls share the array, so calls that
-   overlap on the GPU race: serialise them. Calls allocate nothing.
-   Returns AWQ_ERR_WORKSPACE if ceil(n_tok/128) * in exceeds
-   AWQ_NOALLOC_STATS_MAX_FLOATS (e.g. n_tok = 16384 allows in <= 8192). */
+   array's counters with a memset on `stream` before its kernel. Its address
+   is looked up on the first call made in each context of a device (with that
+   device current), so after a cudaDeviceReset the next call looks it up
+   again; make the first call on a device before any stream capture. All
+   calls share the array, so calls that overlap on the GPU race: serialise
+   them. Calls allocate nothing. Returns AWQ_ERR_WORKSPACE if the partial
+   sums exceed AWQ_NOALLOC_STATS_MAX_FLOATS. */
 AWQ_API awq_status awq_act_stats_noalloc(const void* X, int32_t x_dtype, int64_t n_tok, int64_t in,
                                          float* mean_abs, awq_stream_t stream);
 
@@ -200,13 +204,8 @@ AWQ_API awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, co
    ws/ws_bytes: scratch, at least awq_workspace_size(); its first 4 bytes are
    the device status word read by awq_get_device_status.
    The products run on bf16 tensor cores with fp32 accumulation; the step-2
-   output matrix never leaves the chip. In the RESIDUAL form the fake-quant
-   runs inside the search kernel (awq_search_fused) for searches below 2e13
-   flops (2 * n_grid * n_tok * out * in); larger ones, which run long enough
-   to settle at the GPU's power cap, run awq_fakequant and then the
-   single-CTA products with 2-CTA operand multicast (awq_search_gemm_dump
-   with cluster_m 2), which do more work per joule. The REFERENCE form runs
-   awq_fakequant and awq_search_gemm one after the other. */
+   output matrix never leaves the chip. The kernels it runs, each also
+   callable alone, are declared in awq_stages.h. */
 AWQ_API awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t in,
                             const void* X, int32_t x_dtype, int64_t n_tok, const float* mean_abs,
                             const awq_config* cfg, float* losses, int32_t* best_idx,
@@ -316,24 +315,6 @@ AWQ_API awq_status awq_pipeline_workspace_size(int64_t max_n_tok, int64_t max_ou
 AWQ_API awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_t w_dtype,
                                        const awq_config* cfg, void* ws, size_t ws_bytes, awq_stream_t stream);
 
-/* ---------------------------------------------------------------- checked builds */
-
-/* The library can be built with every global-memory access of its bandwidth
-   kernels, quantiser warps, search epilogue and decode product preceded by a
-   bounds check against the buffer's extent as the call's shapes define it
-   (python -m post_bit_weight_awq_b300.build --checked, which writes
-   libawq_checked.so next to libawq.so). A failed check is counted and its
-   access skipped, so an indexing error shows up as a count instead of a
-   memory fault. awq_bounds_report returns the number of failed checks since
-   the previous report and, for the first recorded one, the source unit
-   (1 awq_kernels.cu, 2 awq_search_gemm.cu, 3 awq_w4a16.cu; 0 if none), line
-   and element offset, then clears the records; it synchronises the device.
-   awq_bounds_selftest launches one check that fails by construction (the
-   element one past `buf[0..n)`; nothing is written). Both return
-   AWQ_ERR_UNSUPPORTED from the release library. */
-AWQ_API awq_status awq_bounds_report(uint64_t* failures, int32_t* unit, uint64_t* line, uint64_t* offset);
-AWQ_API awq_status awq_bounds_selftest(float* buf, int32_t n, awq_stream_t stream);
-
 /* ---------------------------------------------------------------- using the packed layer */
 
 /* Largest token count, and token count times `in`, that awq_w4a16_gemv
@@ -366,113 +347,6 @@ AWQ_API size_t awq_packed_bytes(int64_t out, int64_t in, const awq_config* cfg);
 /* Synchronise `stream`, read the status word at the start of `ws` (device)
    into *status (host) and clear it. Returns AWQ_ERR_CUDA if the copy fails. */
 AWQ_API awq_status awq_get_device_status(const void* ws, awq_stream_t stream, awq_status* status);
-
-/* ------------------------------------------- stages of step 2, one by one
-   awq_search_layer runs awq_alpha_scales, then awq_search_fused (RESIDUAL
-   form) or awq_fakequant and awq_search_gemm (REFERENCE form), then
-   awq_loss_select, on its workspace. They are exported so that each kernel
-   can be timed and checked alone. */
-
-/* s[i][j] and inv_s[i][j] = 1/s[i][j] for every alpha_i (device fp32
-   [n_grid][in]); the scale law of the search_scale listing and "AWQ >
-   Summary", "The scaling formula". s is formed in fp64 (b^(i/n_grid) as the
-   i-th power of b^(1/n_grid), times the fp64 reciprocal normaliser) and
-   rounded to fp32 once; inv_s is the correctly rounded fp32 reciprocal of
-   that value. */
-AWQ_API awq_status awq_alpha_scales(const float* mean_abs, int64_t in, const awq_config* cfg, float* s,
-                            float* inv_s, awq_stream_t stream);
-
-/* For every alpha_i: W_hat_i = Q(W * s_i) * inv_s_i. RESIDUAL form writes
-   bf16(W_hat_i - W) to op[i]; REFERENCE form writes bf16(W_hat_i) to op[i]
-   and bf16(W) to op[n_grid]. op: device bf16 bits [n_slots][out][in]. */
-AWQ_API awq_status awq_fakequant(const void* W, int32_t w_dtype, int64_t out, int64_t in, const float* s,
-                         const float* inv_s, const awq_config* cfg, uint16_t* op,
-                         awq_stream_t stream);
-
-/* Tile grid of the search product: the n_tok x out output of one alpha is
-   cut into m_tiles x n_tiles tiles of tile_m x tile_n. Host-only. */
-AWQ_API awq_status awq_search_tiles(int64_t n_tok, int64_t out, const awq_config* cfg, int64_t* m_tiles,
-                            int64_t* n_tiles, int32_t* tile_m, int32_t* tile_n);
-
-/* partials[i][mt][nt][q] = sum over the 32 tokens of lane quarter q of tile
-   (mt, nt) and over the tile's outputs of (X op_i^T)^2 (RESIDUAL) or of
-   (X op_i^T - X op_G^T)^2 (REFERENCE). X: device bf16 [n_tok][in]. op: as
-   written by awq_fakequant. partials: device fp32 [n_grid][m_tiles][n_tiles][4].
-   status: device uint32, set to AWQ_ERR_TIMEOUT if a wait ran out.
-   tcgen05 tensor cores (bf16 in, fp32 accumulate in tensor memory), operands
-   staged by TMA. */
-AWQ_API awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
-                           int64_t out, const awq_config* cfg, float* partials, uint32_t* status,
-                           awq_stream_t stream);
-
-/* awq_fakequant followed by awq_search_gemm (RESIDUAL form only), in one
-   kernel: besides the search roles, every CTA of the CTA-pair search kernel
-   runs quantiser warps that write op (bit for bit what awq_fakequant writes)
-   in the order the products consume it, one 256-row operand tile and
-   512-channel strip at a time, and publish each tile in ready[i][nt]; the
-   search waits (bounded) for a tile's counter before loading it, so the
-   fake-quant overlaps the products instead of preceding them.
-   W: device [out][in] (AWQ_BF16 or AWQ_FP32). s, inv_s: as written by
-   awq_alpha_scales. op: device bf16 bits [n_grid][out][in] (scratch, fully
-   written). partials, status: as awq_search_gemm. ready: device uint32
-   scratch of n_grid * (n_tiles + 1) + 1 words (n_tiles from
-   awq_search_tiles): per-tile and per-alpha counters and a progress word
-   (the highest alpha started, plus one); zeroed by the call.
-   Returns AWQ_ERR_UNSUPPORTED for the REFERENCE form. The quantiser warps of
-   one CTA serve tiles consumed by others, so all CTAs of the launch must be
-   resident together, as they are when the GPU runs nothing else (the grid is
-   sized to the SM count); otherwise a wait runs out and *status reports
-   AWQ_ERR_TIMEOUT. */
-AWQ_API awq_status awq_search_fused(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X,
-                                    int64_t n_tok, const float* s, const float* inv_s, const awq_config* cfg,
-                                    uint16_t* op, float* partials, uint32_t* ready, uint32_t* status,
-                                    awq_stream_t stream);
-
-/* Test aid: awq_search_gemm in RESIDUAL form with a chosen kernel:
-   cluster_m 0 = the CTA-pair kernel awq_search_gemm uses (cta_group::2, two
-   CTAs share each 256x256 tile); 1, 2 or 4 = the single-CTA kernel with
-   that many CTAs per cluster sharing each operand tile through TMA
-   multicast. If `dump` is not NULL the kernel also
-   stores the raw fp32 products D[i][t][r] = (X op_i^T)[t][r] there (device
-   fp32 [n_grid][n_tok][out]), so the tensor-core data path can be checked
-   element by element against a plain matrix product on small shapes; those
-   stores cost n_grid * n_tok * out * 4 bytes of traffic. Not for production
-   use. */
-AWQ_API awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
-                                        int64_t out, const awq_config* cfg, float* partials,
-                                        uint32_t* status, float* dump, int32_t cluster_m,
-                                        awq_stream_t stream);
-
-/* Test aid for the bounded waits: awq_search_gemm with the first operand
-   fill of every CTA left out, so the MMA issuer's wait on that pipeline stage
-   can never complete. Each wait gives up after cfg->wait_timeout_ms; the
-   kernel then writes AWQ_ERR_TIMEOUT to *status, stops all its roles, lets
-   the copies and MMAs it did issue finish, frees its tensor memory and
-   returns, leaving the device usable. partials are not meaningful. */
-AWQ_API awq_status awq_search_gemm_withhold_fill(const void* X, int64_t n_tok, int64_t in,
-                                                 const uint16_t* op, int64_t out, const awq_config* cfg,
-                                                 float* partials, uint32_t* status, awq_stream_t stream);
-
-/* Test aid for the cross-CTA waits of awq_search_fused: the quantiser warps
-   leave out their first unit (alpha 0, operand tile 0, channel strip 0), so
-   that tile's ready counter never completes and the TMA producers that need
-   it wait in vain. Each wait gives up after cfg->wait_timeout_ms; the kernel
-   then writes AWQ_ERR_TIMEOUT to *status, stops all its roles, lets what it
-   issued finish, frees its tensor memory and returns. Same arguments as
-   awq_search_fused; partials and op are not meaningful. */
-AWQ_API awq_status awq_search_fused_withhold_unit(const void* W, int32_t w_dtype, int64_t out, int64_t in,
-                                                  const void* X, int64_t n_tok, const float* s, const float* inv_s,
-                                                  const awq_config* cfg, uint16_t* op, float* partials,
-                                                  uint32_t* ready, uint32_t* status, awq_stream_t stream);
-
-/* losses[i] = (sum of partials[i]) / (n_tok * out): fp32 sums per thread
-   over a fixed stride, fp64 across threads in a fixed tree (deterministic);
-   best_idx = first i with the smallest fp32 loss; s_best = s[best_idx]. A
-   non-finite loss sets *status to AWQ_ERR_NONFINITE. */
-AWQ_API awq_status awq_loss_select(const float* partials, int64_t n_tok, int64_t out, int64_t in,
-                           const float* s, const awq_config* cfg, float* losses,
-                           int32_t* best_idx, float* s_best, uint32_t* status,
-                           awq_stream_t stream);
 
 #ifdef __cplusplus
 }

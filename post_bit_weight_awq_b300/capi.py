@@ -34,7 +34,7 @@ AWQ_W4A16_MAX_TOKENS = 8
 AWQ_W4A16_MAX_TOKEN_CHANNELS = 44 * 1024
 AWQ_BLOCK_MAX_LINEARS = 16
 
-# Every function that include/awq.h declares.
+# Every function that include/awq.h (the product interface) declares.
 EXPORTED = (
     "awq_config_default",
     "awq_status_string",
@@ -52,18 +52,7 @@ EXPORTED = (
     "awq_pipeline_workspace_size",
     "awq_quantize_layers",
     "awq_packed_bytes",
-    "awq_bounds_report",
-    "awq_bounds_selftest",
     "awq_get_device_status",
-    "awq_alpha_scales",
-    "awq_fakequant",
-    "awq_search_tiles",
-    "awq_search_gemm",
-    "awq_search_fused",
-    "awq_search_gemm_dump",
-    "awq_search_gemm_withhold_fill",
-    "awq_search_fused_withhold_unit",
-    "awq_loss_select",
 )
 
 
@@ -141,21 +130,7 @@ def lib() -> ctypes.CDLL:
         "awq_pipeline_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _I32, _CFG, ctypes.POINTER(_SZ)]),
         "awq_quantize_layers": (ctypes.c_int, [_P, _I32, _I32, _CFG, _P, _SZ, _P]),
         "awq_packed_bytes": (_SZ, [_I64, _I64, _CFG]),
-        "awq_bounds_report": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_I32),
-                                             ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
-        "awq_bounds_selftest": (ctypes.c_int, [_P, _I32, _P]),
         "awq_get_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
-        "awq_alpha_scales": (ctypes.c_int, [_P, _I64, _CFG, _P, _P, _P]),
-        "awq_fakequant": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _CFG, _P, _P]),
-        "awq_search_tiles": (ctypes.c_int, [_I64, _I64, _CFG, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
-                                            ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
-        "awq_search_gemm": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
-        "awq_search_fused": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I64, _P, _P, _CFG, _P, _P, _P, _P, _P]),
-        "awq_search_gemm_dump": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P, _I32, _P]),
-        "awq_search_gemm_withhold_fill": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
-        "awq_search_fused_withhold_unit": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I64, _P, _P, _CFG, _P, _P, _P,
-                                                          _P, _P]),
-        "awq_loss_select": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _CFG, _P, _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -238,11 +213,6 @@ def awq_workspace_size(n_tok: int, out_features: int, in_features: int, cfg: Awq
     return b.value
 
 
-def awq_search_tiles(n_tok: int, out_features: int, cfg: AwqConfig):
-    mt, nt, tm, tn = _I64(0), _I64(0), _I32(0), _I32(0)
-    _check(lib().awq_search_tiles(n_tok, out_features, ctypes.byref(cfg), ctypes.byref(mt), ctypes.byref(nt),
-                                  ctypes.byref(tm), ctypes.byref(tn)), "awq_search_tiles")
-    return mt.value, nt.value, tm.value, tn.value
 
 
 def awq_packed_bytes(out_features: int, in_features: int, cfg: AwqConfig) -> int:
@@ -310,17 +280,8 @@ def awq_search_block(Ws, X, mean_abs, cfg: AwqConfig, losses, best_idx, s_best, 
                                   _ptr(ws), wb, _stream(stream)), "awq_search_block")
 
 
-def awq_bounds_report():
-    """(failed checks, source unit, line, offset) of a checked build; raises AwqError from a release build."""
-    f, u, ln, off = ctypes.c_uint64(0), _I32(0), ctypes.c_uint64(0), ctypes.c_uint64(0)
-    _check(lib().awq_bounds_report(ctypes.byref(f), ctypes.byref(u), ctypes.byref(ln), ctypes.byref(off)),
-           "awq_bounds_report")
-    return f.value, u.value, ln.value, off.value
 
 
-def awq_bounds_selftest(buf, stream=None, *, n=None) -> None:
-    _check(lib().awq_bounds_selftest(_ptr(buf), buf.numel() if n is None else n, _stream(stream)),
-           "awq_bounds_selftest")
 
 
 def awq_pipeline_workspace_size(max_n_tok: int, max_out: int, max_in: int, w_dtype: int, cfg: AwqConfig) -> int:
@@ -388,73 +349,3 @@ def awq_get_device_status(ws, stream=None) -> int:
     st = ctypes.c_int(0)
     _check(lib().awq_get_device_status(_ptr(ws), _stream(stream), ctypes.byref(st)), "awq_get_device_status")
     return st.value
-
-
-def awq_alpha_scales(mean_abs, cfg: AwqConfig, s, inv_s, stream=None, *, in_features=None) -> None:
-    K = mean_abs.shape[0] if in_features is None else in_features
-    _check(lib().awq_alpha_scales(_ptr(mean_abs), K, ctypes.byref(cfg), _ptr(s), _ptr(inv_s), _stream(stream)),
-           "awq_alpha_scales")
-
-
-def awq_fakequant(W, s, inv_s, cfg: AwqConfig, op, stream=None, *, out_features=None, in_features=None,
-                  w_dtype=None) -> None:
-    N = W.shape[0] if out_features is None else out_features
-    K = W.shape[1] if in_features is None else in_features
-    wd = _dtype_code(W) if w_dtype is None else w_dtype
-    _check(lib().awq_fakequant(_ptr(W), wd, N, K, _ptr(s), _ptr(inv_s), ctypes.byref(cfg), _ptr(op),
-                               _stream(stream)), "awq_fakequant")
-
-
-def awq_search_gemm(X, op, cfg: AwqConfig, partials, status, stream=None, *, n_tok=None, in_features=None,
-                    out_features=None) -> None:
-    n = X.shape[0] if n_tok is None else n_tok
-    K = X.shape[1] if in_features is None else in_features
-    N = op.shape[-2] if out_features is None else out_features
-    _check(lib().awq_search_gemm(_ptr(X), n, K, _ptr(op), N, ctypes.byref(cfg), _ptr(partials), _ptr(status),
-                                 _stream(stream)), "awq_search_gemm")
-
-
-def awq_search_fused(W, X, s, inv_s, cfg: AwqConfig, op, partials, ready, status, stream=None, *, out_features=None,
-                     in_features=None, n_tok=None, w_dtype=None) -> None:
-    N = W.shape[0] if out_features is None else out_features
-    K = W.shape[1] if in_features is None else in_features
-    n = X.shape[0] if n_tok is None else n_tok
-    wd = _dtype_code(W) if w_dtype is None else w_dtype
-    _check(lib().awq_search_fused(_ptr(W), wd, N, K, _ptr(X), n, _ptr(s), _ptr(inv_s), ctypes.byref(cfg), _ptr(op),
-                                  _ptr(partials), _ptr(ready), _ptr(status), _stream(stream)), "awq_search_fused")
-
-
-def awq_search_fused_withhold_unit(W, X, s, inv_s, cfg: AwqConfig, op, partials, ready, status, stream=None, *,
-                                   out_features=None, in_features=None, n_tok=None, w_dtype=None) -> None:
-    N = W.shape[0] if out_features is None else out_features
-    K = W.shape[1] if in_features is None else in_features
-    n = X.shape[0] if n_tok is None else n_tok
-    wd = _dtype_code(W) if w_dtype is None else w_dtype
-    _check(lib().awq_search_fused_withhold_unit(_ptr(W), wd, N, K, _ptr(X), n, _ptr(s), _ptr(inv_s),
-                                                ctypes.byref(cfg), _ptr(op), _ptr(partials), _ptr(ready),
-                                                _ptr(status), _stream(stream)), "awq_search_fused_withhold_unit")
-
-
-def awq_search_gemm_dump(X, op, cfg: AwqConfig, partials, status, dump, stream=None, *, n_tok=None,
-                         in_features=None, out_features=None, cluster_m=0) -> None:
-    n = X.shape[0] if n_tok is None else n_tok
-    K = X.shape[1] if in_features is None else in_features
-    N = op.shape[-2] if out_features is None else out_features
-    _check(lib().awq_search_gemm_dump(_ptr(X), n, K, _ptr(op), N, ctypes.byref(cfg), _ptr(partials), _ptr(status),
-                                      _ptr(dump), cluster_m, _stream(stream)), "awq_search_gemm_dump")
-
-
-def awq_search_gemm_withhold_fill(X, op, cfg: AwqConfig, partials, status, stream=None, *, n_tok=None,
-                                  in_features=None, out_features=None) -> None:
-    n = X.shape[0] if n_tok is None else n_tok
-    K = X.shape[1] if in_features is None else in_features
-    N = op.shape[-2] if out_features is None else out_features
-    _check(lib().awq_search_gemm_withhold_fill(_ptr(X), n, K, _ptr(op), N, ctypes.byref(cfg), _ptr(partials),
-                                               _ptr(status), _stream(stream)), "awq_search_gemm_withhold_fill")
-
-
-def awq_loss_select(partials, s, cfg: AwqConfig, losses, best_idx, s_best, status, stream=None, *, n_tok,
-                    out_features, in_features) -> None:
-    _check(lib().awq_loss_select(_ptr(partials), n_tok, out_features, in_features, _ptr(s), ctypes.byref(cfg),
-                                 _ptr(losses), _ptr(best_idx), _ptr(s_best), _ptr(status), _stream(stream)),
-           "awq_loss_select")

@@ -1,4 +1,5 @@
-// C ABI of the AWQ per-layer search and pack (declared in include/awq.h).
+// C ABI of the AWQ per-layer search and pack (declared in include/awq.h,
+// include/awq_stages.h and include/awq_testing.h).
 // Host code only: argument checks (all before any CUDA call), workspace
 // carving, and the launch sequence of each step.
 #include <string.h>
@@ -7,6 +8,8 @@
 
 #include "awq.h"
 #include "awq_launch.h"
+#include "awq_stages.h"
+#include "awq_testing.h"
 #include "awq_trace.h"
 
 using namespace awq;
@@ -16,11 +19,9 @@ namespace {
 constexpr size_t kAlign = 1024;
 
 // Search size (flops of the alpha products) from which awq_search_layer
-// uses the single-CTA products instead of the fused CTA-pair kernel: below
-// it a search fits in the GPU's burst power budget, above it the run settles
-// at the power cap (measured: 13B-class 33 ms vs 38 ms, 70B-class 115 ms vs
-// 138 ms per search; Llama-7B q_proj and MLP within 3% either way).
-constexpr double kLargeSearchFlops = 2e13;
+// runs the fake-quant as its own launch ahead of the CTA-pair products
+// instead of inside them.
+constexpr double kLargeSearchFlops = AWQ_SEARCH_FUSED_MAX_FLOPS;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -241,7 +242,7 @@ const char* awq_status_string(int status) {
 
 // Statistics scratch: fp32 partial sums [chunks][in], then the per-strip tickets.
 size_t stats_ticket_offset(int64_t n_tok, int64_t in) {
-  return align_up((size_t)stats_chunks(n_tok) * (size_t)in * 4, kAlign);
+  return align_up((size_t)stats_chunks(n_tok, in) * (size_t)in * 4, kAlign);
 }
 
 awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_t* bytes) {
@@ -371,9 +372,9 @@ awq_status awq_search_fused_withhold_unit(const void* W, int32_t w_dtype, int64_
 
 awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const uint16_t* op, int64_t out,
                                 const awq_config* cfg, float* partials, uint32_t* status, float* dump,
-                                int32_t cluster_m, awq_stream_t stream) {
+                                int32_t single_cta, awq_stream_t stream) {
   AWQ_TRACE("awq_search_gemm_dump");
-  if (cluster_m != 0 && cluster_m != 1 && cluster_m != 2 && cluster_m != 4) return AWQ_ERR_INVALID_ARG;
+  if (single_cta != 0 && single_cta != 1) return AWQ_ERR_INVALID_ARG;
   if (cfg != nullptr && cfg->loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
   if (X == nullptr || op == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
@@ -383,7 +384,7 @@ awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const 
   if (!aligned16(X) || !aligned16(op) || !aligned16(partials) || !aligned16(status) || !aligned16(dump))
     return AWQ_ERR_MISALIGNED;
   return from_cuda(launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status,
-                                      (cudaStream_t)stream, dump, 0, cluster_m));
+                                      (cudaStream_t)stream, dump, 0, single_cta));
 }
 
 awq_status awq_search_gemm_withhold_fill(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
@@ -526,15 +527,14 @@ awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, c
       e = launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, sc, inv, out, *cfg, op, partials, ready,
                               status, s, nullptr, -1, row_acc);
   } else if (cfg->loss_form == AWQ_LOSS_RESIDUAL) {
-    // searches that run for tens of milliseconds and more settle at the power cap, where the single-CTA
-    // products with 2-CTA operand multicast do more work per joule than the CTA-pair products
-    if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
-    if (e == cudaSuccess)
-      e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 2, row_acc);
-  } else {
+    // the fake-quant launch, then the CTA-pair products
     if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
     if (e == cudaSuccess)
       e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 0, row_acc);
+  } else {
+    if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
+    if (e == cudaSuccess)
+      e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 1, row_acc);
   }
   if (e == cudaSuccess)
     e = launch_loss_select(partials, cfg->n_grid, L.mt * L.nt * 4, n_tok, out, sc, in, losses, best_idx, s_best,

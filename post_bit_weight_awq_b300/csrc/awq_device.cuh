@@ -179,18 +179,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Same 3D load, written to the same shared-memory offset in every CTA of the
-// cluster named in `mask`; each destination CTA's mbarrier at `bar`'s offset
-// receives the byte count of its copy.
-__device__ __forceinline__ void tma_load_3d_multicast(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                                      int y, int z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(mask)
-      : "memory");
-}
-
 // As tma_load_2d / tma_load_3d, for a CTA pair: the copy lands in this CTA's
 // shared memory and its byte count is reported to the mbarrier at `bar_cluster`,
 // a shared::cluster address that may lie in either CTA of the pair.
@@ -346,16 +334,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
-}
-
-// As umma_commit, but the arrival is delivered to the mbarrier at the same
-// shared-memory offset in every CTA of the cluster named in `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
 }
 
 // Each lane of the warp reads 32 consecutive 32-bit columns of its own

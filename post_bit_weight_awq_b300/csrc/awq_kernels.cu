@@ -20,15 +20,19 @@ namespace awq {
 // LLMs", "How does AWQ decide which weights to protect?"; "AWQ > Summary",
 // "Salient weight identification").
 //
-// One launch. Block = 32 x 8 threads over a strip of 256 channels and a
-// chunk of kStatsRows tokens. Each thread reads 8 channels (16 B) of every
-// 8th row of the chunk, eight rows' loads in flight at a time, so a warp
-// reads 512 contiguous bytes per row. The 8
-// row phases are added in fixed order in shared memory and the chunk's
-// partial sums go to scratch. The block that finishes last on a strip (a
-// ticket counter per strip, zeroed before the launch) adds that strip's
-// chunks with a compensated fp32 sum in chunk order and writes the mean:
-// the result does not depend on which block finishes last. Deterministic.
+// One launch, one wave. Block = 32 x 8 threads over a strip of 256 channels
+// and a chunk of tokens (stats_chunk_rows: about kStatsTargetBlocks blocks
+// in all, so every block streams a long run of rows instead of the grid
+// running many short waves). Each thread reads 8 channels (16 B) of every
+// 8th row of the chunk, so a warp reads 512 contiguous bytes per row; loads
+// go in batches of 4 rows, the next batch issued before the current one is
+// added, so 4 to 8 loads per thread stay in flight. The 8 row phases are
+// added in fixed order in shared memory and the chunk's partial sums go to
+// scratch. The block that finishes last on a strip (a ticket counter per
+// strip, zeroed before the launch) adds that strip's chunks with a
+// compensated fp32 sum in chunk order and writes the mean: the result does
+// not depend on which block finishes last, and the chunking depends only on
+// the shape. Deterministic.
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;
@@ -49,30 +53,41 @@ __device__ __forceinline__ void acc_abs_bf16x8(float (&a)[8], const uint4& v) {
   a[7] += fabsf(bf16_hi(v.w));
 }
 
-__global__ void __launch_bounds__(256, 4) stats_kernel(const uint16_t* __restrict__ X, int n, int K,
+constexpr int kStatsBatch = 4;  // rows per load batch of a thread
+
+// Rows r, r + 8, r + 16, r + 24 of the thread's phase (zeros past the chunk).
+__device__ __forceinline__ void stats_load_batch(const uint16_t* __restrict__ X, int r, int r1, int K, int col,
+                                                 size_t total, uint4 (&v)[kStatsBatch]) {
+#pragma unroll
+  for (int u = 0; u < kStatsBatch; ++u) {
+    const int row = r + 8 * u;
+    const size_t off = (size_t)row * K + col;
+    v[u] = row < r1 && AWQ_IN(off, 8, total) ? ld_nc_v4(X + off) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__global__ void __launch_bounds__(256, 4) stats_kernel(const uint16_t* __restrict__ X, int n, int K, int chunk_rows,
                                                     float* __restrict__ partials, uint32_t* __restrict__ tickets,
                                                     float* __restrict__ mean_abs) {
   __shared__ float red[8][256 + 8];
   __shared__ bool last;
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int col = (blockIdx.x * 32 + tx) * 8;
-  const int r0 = blockIdx.y * kStatsRows;
-  const int r1 = min(r0 + kStatsRows, n);
+  const int r0 = blockIdx.y * chunk_rows;
+  const int r1 = min(r0 + chunk_rows, n);
+  const size_t total = (size_t)n * K;
   float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (col < K) {
+    uint4 cur[kStatsBatch], nxt[kStatsBatch];
     int r = r0 + ty;
-    for (; r + 56 < r1; r += 64) {  // 8 rows' loads in flight per thread
-      uint4 v[8];
+    stats_load_batch(X, r, r1, K, col, total, cur);
+    for (; r < r1; r += 8 * kStatsBatch) {
+      stats_load_batch(X, r + 8 * kStatsBatch, r1, K, col, total, nxt);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const size_t off = (size_t)(r + 8 * u) * K + col;
-        v[u] = AWQ_IN(off, 8, (size_t)n * K) ? ld_nc_v4(X + off) : make_uint4(0u, 0u, 0u, 0u);
-      }
+      for (int u = 0; u < kStatsBatch; ++u) acc_abs_bf16x8(a, cur[u]);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc_abs_bf16x8(a, v[u]);
+      for (int u = 0; u < kStatsBatch; ++u) cur[u] = nxt[u];
     }
-    for (; r < r1; r += 8)
-      if (AWQ_IN((size_t)r * K + col, 8, (size_t)n * K)) acc_abs_bf16x8(a, ld_nc_v4(X + (size_t)r * K + col));
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) red[ty][tx * 8 + i] = a[i];
@@ -92,7 +107,6 @@ __global__ void __launch_bounds__(256, 4) stats_kernel(const uint16_t* __restric
   __threadfence();
   // compensated (Neumaier) fp32 sum over the chunks, fixed order; the other
   // blocks' partials are read past L1, 32 chunks' loads in flight at a time
-  // (one L2 round trip for up to 4096 tokens)
   const int chunks = (int)gridDim.y;
   float s = 0.0f, comp = 0.0f;
   for (int i0 = 0; i0 < chunks; i0 += 32) {
@@ -116,12 +130,12 @@ __global__ void __launch_bounds__(256, 4) stats_kernel(const uint16_t* __restric
 
 cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partials, uint32_t* tickets,
                          float* mean_abs, cudaStream_t st) {
-  const int chunks = stats_chunks(n);
-  const unsigned strips = (unsigned)((K + 255) / 256);
+  const int chunks = stats_chunks(n, K);
+  const unsigned strips = (unsigned)stats_strips(K);
   cudaError_t e = cudaMemsetAsync(tickets, 0, strips * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  stats_kernel<<<dim3(strips, (unsigned)chunks), dim3(32, 8), 0, st>>>(X, (int)n, (int)K, partials, tickets,
-                                                                       mean_abs);
+  stats_kernel<<<dim3(strips, (unsigned)chunks), dim3(32, 8), 0, st>>>(X, (int)n, (int)K, (int)stats_chunk_rows(n, K),
+                                                                       partials, tickets, mean_abs);
   return cudaGetLastError();
 }
 

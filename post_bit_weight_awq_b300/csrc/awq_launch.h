@@ -11,7 +11,12 @@ namespace awq {
 
 constexpr int kBlockCols = 128;  // input channels of one 8-lane block of the quantiser kernels; `in` is a multiple
 constexpr int kMaxGrid = 64;     // largest alpha grid
-constexpr int kStatsRows = 128;  // tokens per statistics chunk
+// Statistics: a block reads a strip of 256 channels over a chunk of tokens;
+// the chunk length depends on the shape only (results do not depend on the
+// GPU) and is chosen so that about kStatsTargetBlocks blocks cover X: one
+// wave of 4 resident blocks on each SM of a 148-SM B300.
+constexpr int kStatsTargetBlocks = 592;
+constexpr int kStatsRowQuantum = 32;  // chunk lengths are multiples of 8 row phases x 4 rows per batch
 
 // Search-product tiling (one CTA per SM, persistent).
 constexpr int kTileM = 128;  // tokens per tile (tensor-memory lanes)
@@ -24,10 +29,21 @@ cudaError_t sm_count(int* sms);
 // device (the attribute is set once per kernel, device and size increase).
 cudaError_t ensure_dynamic_smem(const void* func, int bytes);
 
-inline int stats_chunks(int64_t n_tok) { return (int)((n_tok + kStatsRows - 1) / kStatsRows); }
 inline int stats_strips(int64_t in) { return (int)((in + 255) / 256); }
+// Tokens per statistics chunk: n_tok * strips / kStatsTargetBlocks, rounded
+// up to a multiple of kStatsRowQuantum (at least one quantum).
+inline int64_t stats_chunk_rows(int64_t n_tok, int64_t in) {
+  const int64_t per = (n_tok * stats_strips(in) + kStatsTargetBlocks - 1) / kStatsTargetBlocks;
+  const int64_t q = (per + kStatsRowQuantum - 1) / kStatsRowQuantum * kStatsRowQuantum;
+  return q < kStatsRowQuantum ? kStatsRowQuantum : q;
+}
+// Chunks of the token range: at most kStatsTargetBlocks / strips + 1.
+inline int stats_chunks(int64_t n_tok, int64_t in) {
+  const int64_t r = stats_chunk_rows(n_tok, in);
+  return (int)((n_tok + r - 1) / r);
+}
 
-// partials: fp32 [stats_chunks(n)][K]; tickets: uint32 [stats_strips(K)] (zeroed by the launch).
+// partials: fp32 [stats_chunks(n, K)][K]; tickets: uint32 [stats_strips(K)] (zeroed by the launch).
 cudaError_t launch_stats(const uint16_t* X, int64_t n, int64_t K, float* partials, uint32_t* tickets,
                          float* mean_abs, cudaStream_t st);
 cudaError_t launch_alpha_scales(const float* mean_abs, int64_t K, const awq_config& cfg, float* s,
@@ -49,10 +65,11 @@ cudaError_t launch_loss_select(const float* partials, int G, int64_t per_alpha, 
 // be encoded.
 cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
                                const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
-                               float* dump = nullptr, int withhold_first_fill = 0, int cluster_m = 0,
+                               float* dump = nullptr, int withhold_first_fill = 0, int single_cta = 0,
                                double* row_acc = nullptr);
-// cluster_m: 0 = default kernel (CTA pairs, cta_group::2, for the RESIDUAL
-// form); 1, 2 or 4 = the single-CTA kernel with clusters of that size.
+// single_cta: 0 = the default kernel (CTA pairs, cta_group::2, for the
+// RESIDUAL form); 1 = the single-CTA kernel (always used for the REFERENCE
+// form and the withheld-fill test aid).
 // row_acc: if not null, fp64 [n_grid][N] to which each output row's sum of
 // squared errors over the tokens is added (the caller zeroes it).
 

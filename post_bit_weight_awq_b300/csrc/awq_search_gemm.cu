@@ -11,17 +11,10 @@
 //                   memory and stays resident; for each alpha, D_i = X W_hat_i^T
 //                   and partial_i = sum (D_i - Y)^2.
 //
-// Structure (one CTA per SM, persistent over tiles, 192 threads):
+// Structure of the single-CTA form (one CTA per SM, persistent over tiles,
+// 192 threads; used for the REFERENCE form and the bounded-wait test aid):
 //   warp 0, lane 0 : TMA producer. X tile [128 x 64] and operand tile
 //                    [256 x 64] per stage, 128-byte swizzle, 4-stage ring.
-//                    With a cluster of CM CTAs along the token dimension
-//                    (RESIDUAL form), the CM CTAs work on CM token tiles of
-//                    the same output-row block: each loads its own X tile
-//                    and one 1/CM slice of the shared operand tile, which
-//                    TMA multicasts into every CTA of the cluster, so L2
-//                    serves (16 + 32/CM) KiB per CTA per stage instead of
-//                    48 KiB. A stage is refilled only after the MMAs of
-//                    every CTA in the cluster have released it.
 //   warp 1         : allocates 512 tensor-memory columns; lane 0 issues
 //                    tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) and
 //                    commits completions to mbarriers.
@@ -31,6 +24,7 @@
 // Tensor memory: two 256-column fp32 accumulators. RESIDUAL double-buffers
 // them so the epilogue of a tile overlaps the next tile's MMAs; REFERENCE
 // keeps Y in the second and accumulates X W_hat_i^T in the first.
+// The default RESIDUAL product is the CTA-pair form further down.
 // Every wait is bounded (wall time and iteration count): on a timeout the
 // kernel records AWQ_ERR_TIMEOUT, stops all roles, lets its in-flight copies
 // and MMAs land, frees tensor memory and returns.
@@ -57,7 +51,7 @@ struct Params {
   int mt, nt;         // token tiles, output-row tiles
   int kb;             // K blocks of 64
   int G;              // alphas
-  int mtg;            // token-tile groups of the cluster size: ceil(mt / CM)
+  int mtg;            // token-tile groups: ceil(mt / 2) for the CTA-pair form, mt for the single-CTA form
   int items;          // work items (RESIDUAL: G*mtg*nt; REFERENCE: mt*nt)
   int raster_group;   // tiles of the stationary operand per raster sweep
   int raster_n;       // 1: operand tiles stay, token tiles sweep; 0: the reverse
@@ -150,7 +144,7 @@ __device__ __forceinline__ void decode_tile(int t, int m_tiles, int nt, int grou
   nb = raster_n ? i_stat : i_sweep;
 }
 
-template <bool REF, int CM>
+template <bool REF>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     search_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                        const Params p) {
@@ -170,17 +164,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  static_assert(!REF || CM == 1, "the REFERENCE form runs without clusters");
-  constexpr uint16_t kMask = (uint16_t)((1u << CM) - 1u);
-  constexpr int kSliceRows = BN / CM;
-  const int rank = CM > 1 ? (int)cluster_ctarank() : 0;
-  const int cluster = blockIdx.x / CM;
-  const int nclusters = gridDim.x / CM;
+  const int cta = blockIdx.x;
+  const int ncta = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CM);  // released by the MMAs of every CTA in the cluster
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -200,7 +190,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) cluster_sync_all();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int passes = REF ? p.G + 1 : 1;
@@ -212,7 +201,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t used = 0, last_par = 0;  // per-stage bit: stage used; parity of its last fill
       bool ok = true;
       bool withhold = p.withhold_first_fill != 0;
-      for (int it = cluster; it < p.items && ok; it += nclusters) {
+      for (int it = cta; it < p.items && ok; it += ncta) {
         int a = 0, t = it;
         if (!REF) {
           a = it / (p.mtg * p.nt);
@@ -220,7 +209,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         int mg, nb;
         decode_tile(t, p.mtg, p.nt, p.raster_group, p.raster_n, mg, nb);
-        const int mb = mg * CM + rank;
+        const int mb = mg;
         for (int pass = 0; pass < passes && ok; ++pass) {
           const int slot = REF ? (pass == 0 ? p.G : pass - 1) : a;
           for (int kb = 0; kb < p.kb; ++kb) {
@@ -234,11 +223,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
               mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
               tma_load_2d(sA + stage * A_BYTES, &tmX, &full[stage], kb * BK, mb * BM);
-              if (CM == 1)
-                tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nb * BN, slot);
-              else
-                tma_load_3d_multicast(sB + stage * B_BYTES + rank * (kSliceRows * BK * 2), &tmB, &full[stage],
-                                      kb * BK, nb * BN + rank * kSliceRows, slot, kMask);
+              tma_load_3d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nb * BN, slot);
               used |= 1u << stage;
               last_par = (last_par & ~(1u << stage)) | (phase << stage);
             }
@@ -260,7 +245,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t ph = 0;  // bit b: parity of accumulator buffer b
       uint32_t local = 0;
       bool ok = true;
-      for (int it = cluster; it < p.items && ok; it += nclusters, ++local) {
+      for (int it = cta; it < p.items && ok; it += ncta, ++local) {
         for (int pass = 0; pass < passes && ok; ++pass) {
           // RESIDUAL: alternate buffers per tile. REFERENCE: Y -> buffer 1, D_i -> buffer 0.
           const int buf = REF ? (pass == 0 ? 1 : 0) : (int)(local & 1u);
@@ -282,10 +267,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int k = 0; k < BK / 16; ++k)
               umma_bf16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), IDESC,
                         (kb > 0 || k > 0) ? 1u : 0u);
-            if (CM == 1)
-              umma_commit(&empty[stage]);
-            else
-              umma_commit_multicast(&empty[stage], kMask);
+            umma_commit(&empty[stage]);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -307,7 +289,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t ph = 0;  // bit b: parity of accumulator buffer b
     uint32_t local = 0;
     bool ok = true;
-    for (int it = cluster; it < p.items && ok; it += nclusters, ++local) {
+    for (int it = cta; it < p.items && ok; it += ncta, ++local) {
       int a = 0, t = it;
       if (!REF) {
         a = it / (p.mtg * p.nt);
@@ -315,7 +297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       int mg, nb;
       decode_tile(t, p.mtg, p.nt, p.raster_group, p.raster_n, mg, nb);
-      const int mb = mg * CM + rank;
+      const int mb = mg;
       if (REF) {
         // All lanes wait; the warp goes on only if every lane saw the phase
         // complete, so the warp-collective tensor-memory loads stay converged.
@@ -385,7 +367,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) cluster_sync_all();  // no peer still multicasts into this CTA or arrives on its barriers
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -795,32 +776,14 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
-template <int CM>
-cudaError_t launch_residual(const CUtensorMap& tmX, const CUtensorMap& tmB, Params p, int sms, cudaStream_t st) {
-  cudaError_t e = ensure_dynamic_smem((const void*)search_gemm_kernel<false, CM>, SMEM_BYTES);
+// Single-CTA launch: one persistent CTA per SM (fewer if there are fewer items).
+template <bool REF>
+cudaError_t launch_single(const CUtensorMap& tmX, const CUtensorMap& tmB, const Params& p, int sms, cudaStream_t st) {
+  cudaError_t e = ensure_dynamic_smem((const void*)search_gemm_kernel<REF>, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CM;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  lc.blockDim = dim3(NUM_THREADS);
-  lc.dynamicSmemBytes = SMEM_BYTES;
-  lc.stream = st;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  int clusters = sms / CM;
-  if (CM > 1) {
-    lc.gridDim = dim3(CM * clusters);
-    int active = 0;
-    e = cudaOccupancyMaxActiveClusters(&active, search_gemm_kernel<false, CM>, &lc);
-    if (e != cudaSuccess) return e;
-    if (active > 0 && active < clusters) clusters = active;
-  }
-  if (clusters > p.items) clusters = p.items;
-  lc.gridDim = dim3(CM * clusters);
-  return cudaLaunchKernelEx(&lc, search_gemm_kernel<false, CM>, tmX, tmB, p);
+  const int grid = p.items < sms ? p.items : sms;
+  search_gemm_kernel<REF><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);
+  return cudaGetLastError();
 }
 
 template <bool FUSED, int GROUP = 128>
@@ -852,8 +815,9 @@ cudaError_t launch_pair(const CUtensorMap& tmX, const CUtensorMap& tmB, const Pa
   return cudaLaunchKernelEx(&lc, search_gemm_pair_kernel<FUSED, GROUP>, tmX, tmB, p);
 }
 
-// Tensor maps and tiling of a search launch. CM: CTAs per cluster sharing an
-// operand tile (2 for the CTA-pair kernels).
+// Tensor maps and tiling of a search launch. CM: CTAs that split one 256-row
+// operand tile (2 for the CTA-pair kernels, each loading its 128-row half;
+// 1 for the single-CTA kernel).
 cudaError_t setup_search(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
                          const awq_config& cfg, int CM, CUtensorMap* tmX, CUtensorMap* tmB, Params* pp, int* sms) {
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
@@ -895,36 +859,24 @@ cudaError_t setup_search(const uint16_t* X, int64_t n_tok, int64_t K, const uint
 
 cudaError_t launch_search_gemm(const uint16_t* X, int64_t n_tok, int64_t K, const uint16_t* op, int64_t N,
                                const awq_config& cfg, float* partials, uint32_t* status, cudaStream_t st,
-                               float* dump, int withhold_first_fill, int cluster_m, double* row_acc) {
+                               float* dump, int withhold_first_fill, int single_cta, double* row_acc) {
   const bool ref = cfg.loss_form == AWQ_LOSS_REFERENCE;
-  // cluster_m 0: the default (CTA pairs for RESIDUAL, single CTAs for
-  // REFERENCE); 1, 2 or 4: the single-CTA kernel with that cluster size.
-  const bool pair = !ref && !withhold_first_fill && cluster_m == 0;
-  int CM = pair ? 2 : (cluster_m > 0 ? cluster_m : 1);
-  if (ref || withhold_first_fill) CM = 1;
-  if (CM != 1 && CM != 2 && CM != 4) return cudaErrorInvalidValue;
+  // the CTA-pair kernel for the RESIDUAL form; the single-CTA kernel for the
+  // REFERENCE form, the withheld-fill test aid, or when asked for
+  const bool pair = !ref && !withhold_first_fill && !single_cta;
   CUtensorMap tmX, tmB;
   Params p;
   int sms = 0;
-  cudaError_t e = setup_search(X, n_tok, K, op, N, cfg, CM, &tmX, &tmB, &p, &sms);
+  cudaError_t e = setup_search(X, n_tok, K, op, N, cfg, pair ? 2 : 1, &tmX, &tmB, &p, &sms);
   if (e != cudaSuccess) return e;
   p.partials = partials;
   p.status = status;
   p.dump = ref ? nullptr : dump;
   p.row_acc = row_acc;
   p.withhold_first_fill = withhold_first_fill;
-
-  if (ref) {
-    e = ensure_dynamic_smem((const void*)search_gemm_kernel<true, 1>, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    const int grid = p.items < sms ? p.items : sms;
-    search_gemm_kernel<true, 1><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmB, p);
-    return cudaGetLastError();
-  }
-  if (pair) e = launch_pair<false>(tmX, tmB, p, sms, st);
-  else if (CM == 1) e = launch_residual<1>(tmX, tmB, p, sms, st);
-  else if (CM == 2) e = launch_residual<2>(tmX, tmB, p, sms, st);
-  else e = launch_residual<4>(tmX, tmB, p, sms, st);
+  if (ref) e = launch_single<true>(tmX, tmB, p, sms, st);
+  else if (pair) e = launch_pair<false>(tmX, tmB, p, sms, st);
+  else e = launch_single<false>(tmX, tmB, p, sms, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -17,8 +17,8 @@ def pytest_sessionfinish(session, exitstatus):
     path = os.environ.get("AWQ_BOUNDS_REPORT")
     if not path:
         return
-    from post_bit_weight_awq_b300 import capi
+    from post_bit_weight_awq_b300 import capi_testing
 
-    failures, unit, line, offset = capi.awq_bounds_report()
+    failures, unit, line, offset = capi_testing.awq_bounds_report()
     with open(path, "w") as f:
         f.write(f"{failures} {unit} {line} {offset}\n")

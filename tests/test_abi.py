@@ -9,33 +9,50 @@ import re
 import pytest
 
 import oracle as O
-from post_bit_weight_awq_b300 import build, capi
+from post_bit_weight_awq_b300 import build, capi, capi_testing
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "awq.h")
+STAGES_HEADER = os.path.join(ROOT, "include", "awq_stages.h")
+TESTING_HEADER = os.path.join(ROOT, "include", "awq_testing.h")
 
 
 @pytest.fixture(scope="module")
 def lib():
     build.build()
-    return capi.lib()
+    return capi_testing.lib()
 
 
-def header_functions():
-    text = open(HEADER).read()
+def header_functions(path=HEADER):
+    text = open(path).read()
     return sorted(set(re.findall(r"^AWQ_API\s+[\w\s\*]+?\b(awq_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_binding_list():
+    """The product header declares exactly the product binding; the stage calls and the test aids live in
+    their own headers and their own binding module."""
     assert header_functions() == sorted(capi.EXPORTED)
+    assert header_functions(STAGES_HEADER) == sorted(capi_testing.STAGE_EXPORTED)
+    assert header_functions(TESTING_HEADER) == sorted(capi_testing.TESTING_EXPORTED)
+    assert not set(capi.EXPORTED) & set(capi_testing.STAGE_EXPORTED + capi_testing.TESTING_EXPORTED)
 
 
 def test_library_exports_every_declared_symbol(lib):
-    for name in header_functions():
+    declared = header_functions() + header_functions(STAGES_HEADER) + header_functions(TESTING_HEADER)
+    for name in declared:
         assert hasattr(lib, name), name
     out = os.popen(f"nm -D --defined-only {capi.LIB_PATH}").read()
     exported = sorted(set(re.findall(r"\bT (awq_\w+)", out)))
-    assert exported == header_functions()
+    assert exported == sorted(declared)
+
+
+def test_product_binding_loads_without_the_test_aids():
+    """The product binding sets the signatures of the product calls only."""
+    import inspect
+
+    src = inspect.getsource(capi)
+    for name in capi_testing.STAGE_EXPORTED + capi_testing.TESTING_EXPORTED:
+        assert f'"{name}"' not in src, name
 
 
 def test_library_is_built_for_sm_103a_only():
@@ -71,7 +88,7 @@ def test_workspace_sizes(lib):
     ref = capi.awq_workspace_size(n, N, K, capi.config(loss_form=capi.AWQ_LOSS_REFERENCE))
     assert ref >= ws + N * K * 2
     assert capi.awq_act_stats_workspace_size(n, K) >= (n // 128) * K * 4
-    mt, nt, tm, tn = capi.awq_search_tiles(n, N, cfg)
+    mt, nt, tm, tn = capi_testing.awq_search_tiles(n, N, cfg)
     assert (mt, nt) == ((n + tm - 1) // tm, (N + tn - 1) // tn)
 
 
@@ -133,7 +150,7 @@ def test_host_validation_of_search_and_pack(lib):
 
 def test_host_validation_of_fused_search(lib):
     A, B, C, D = 0x1000, 0x2000, 0x3000, 0x4000
-    f = capi.awq_search_fused
+    f = capi_testing.awq_search_fused
     kw = dict(out_features=256, in_features=256, n_tok=128, w_dtype=capi.AWQ_BF16)
     cfg = capi.config()
     assert _status_of(f, A, B, C, C, capi.config(loss_form=capi.AWQ_LOSS_REFERENCE), D, D, D, D, 0, **kw) == \
@@ -226,16 +243,19 @@ def test_bounds_checks_are_absent_from_the_release_library(lib):
 def test_checked_library_builds_and_exports_the_same_calls():
     path = build.build(checked=True)
     checked = ctypes.CDLL(path)
-    for name in capi.EXPORTED:
+    for name in capi.EXPORTED + capi_testing.STAGE_EXPORTED + capi_testing.TESTING_EXPORTED:
         assert hasattr(checked, name), name
 
 
 def test_binding_constants_match_the_header():
-    text = open(HEADER).read()
-    for name in ("AWQ_W4A16_MAX_TOKENS", "AWQ_W4A16_MAX_TOKEN_CHANNELS", "AWQ_BLOCK_MAX_LINEARS"):
-        m = re.search(r"#define\s+" + name + r"\s+(.+)", text)
-        assert m, name
-        assert eval(m.group(1).split("/*")[0].strip()) == getattr(capi, name), name
+    for path, mod, names in ((HEADER, capi, ("AWQ_W4A16_MAX_TOKENS", "AWQ_W4A16_MAX_TOKEN_CHANNELS",
+                                             "AWQ_BLOCK_MAX_LINEARS")),
+                             (STAGES_HEADER, capi_testing, ("AWQ_SEARCH_FUSED_MAX_FLOPS",))):
+        text = open(path).read()
+        for name in names:
+            m = re.search(r"#define\s+" + name + r"\s+(.+)", text)
+            assert m, name
+            assert eval(m.group(1).split("/*")[0].strip()) == getattr(mod, name), name
 
 
 def test_host_validation_of_w4a16_gemm(lib):

@@ -18,14 +18,14 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 SELFTEST = r"""
 import torch
-from post_bit_weight_awq_b300 import capi
+from post_bit_weight_awq_b300 import capi, capi_testing
 buf = torch.full((64,), 7.0, device="cuda")
-assert capi.awq_bounds_report()[0] == 0
-capi.awq_bounds_selftest(buf)
-failures, unit, line, offset = capi.awq_bounds_report()
+assert capi_testing.awq_bounds_report()[0] == 0
+capi_testing.awq_bounds_selftest(buf)
+failures, unit, line, offset = capi_testing.awq_bounds_report()
 assert failures == 1 and unit == 1 and line > 0 and offset == 64, (failures, unit, line, offset)
 assert bool(torch.all(buf == 7.0))
-assert capi.awq_bounds_report()[0] == 0  # the report clears the record
+assert capi_testing.awq_bounds_report()[0] == 0  # the report clears the record
 print("selftest ok")
 """
 

@@ -12,7 +12,7 @@ import torch
 
 import workloads
 from gpu_util import dev_bf16
-from post_bit_weight_awq_b300 import build, capi
+from post_bit_weight_awq_b300 import build, capi, capi_testing
 
 pytestmark = pytest.mark.gpu
 
@@ -32,19 +32,19 @@ def test_stuck_wait_ends_with_timeout_status_and_device_stays_usable():
     B = workloads.round_to_bf16((rng.standard_normal((G, N, K)) * 0.05).astype(np.float32))
     Ad, Bd = dev_bf16(A), dev_bf16(B.reshape(G * N, K))
     cfg = capi.config(n_grid=G, wait_timeout_ms=100)
-    mt, nt, tm, tn = capi.awq_search_tiles(n, N, cfg)
+    mt, nt, tm, tn = capi_testing.awq_search_tiles(n, N, cfg)
     partials = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    capi.awq_search_gemm_withhold_fill(Ad, Bd, cfg, partials, status, n_tok=n, in_features=K, out_features=N)
+    capi_testing.awq_search_gemm_withhold_fill(Ad, Bd, cfg, partials, status, n_tok=n, in_features=K, out_features=N)
     torch.cuda.synchronize()
     elapsed = time.perf_counter() - t0
     assert int(status[0]) == capi.AWQ_ERR_TIMEOUT
     assert elapsed < 5.0
     # the next launch on the same device is correct
     status.zero_()
-    capi.awq_search_gemm(Ad, Bd, cfg, partials, status, n_tok=n, in_features=K, out_features=N)
+    capi_testing.awq_search_gemm(Ad, Bd, cfg, partials, status, n_tok=n, in_features=K, out_features=N)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     P = partials.cpu().numpy().astype(np.float64).sum(axis=(1, 2, 3))
@@ -66,26 +66,26 @@ def test_fused_search_stuck_tile_ends_with_timeout_and_device_stays_usable():
     s = torch.empty(G, K, dtype=torch.float32, device="cuda")
     inv = torch.empty_like(s)
     mean = X.float().abs().mean(0).contiguous()
-    capi.awq_alpha_scales(mean, cfg, s, inv)
-    mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
+    capi_testing.awq_alpha_scales(mean, cfg, s, inv)
+    mt, nt, _, _ = capi_testing.awq_search_tiles(n, N, cfg)
     op = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
     parts = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device="cuda")
     ready = torch.zeros(G * (nt + 1) + 1, dtype=torch.int32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    capi.awq_search_fused_withhold_unit(W, X, s, inv, cfg, op, parts, ready, status)
+    capi_testing.awq_search_fused_withhold_unit(W, X, s, inv, cfg, op, parts, ready, status)
     torch.cuda.synchronize()
     elapsed = time.perf_counter() - t0
     assert int(status[0]) == capi.AWQ_ERR_TIMEOUT
     assert elapsed < 5.0
     # the next launch on the same device is correct: it equals the two separate launches
     status.zero_()
-    capi.awq_search_fused(W, X, s, inv, cfg, op, parts, ready, status)
+    capi_testing.awq_search_fused(W, X, s, inv, cfg, op, parts, ready, status)
     op_ref = torch.empty_like(op)
     p_ref = torch.zeros_like(parts)
-    capi.awq_fakequant(W, s, inv, cfg, op_ref)
-    capi.awq_search_gemm(X, op_ref, cfg, p_ref, status, n_tok=n, in_features=K, out_features=N)
+    capi_testing.awq_fakequant(W, s, inv, cfg, op_ref)
+    capi_testing.awq_search_gemm(X, op_ref, cfg, p_ref, status, n_tok=n, in_features=K, out_features=N)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     assert torch.equal(op.view(torch.int16), op_ref.view(torch.int16))

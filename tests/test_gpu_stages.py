@@ -10,7 +10,7 @@ import torch
 import oracle as O
 import workloads
 from gpu_util import dev_bf16, dev_f32, dev_weight, host_bf16_to_f64, save_debug
-from post_bit_weight_awq_b300 import build, capi
+from post_bit_weight_awq_b300 import build, capi, capi_testing
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,7 @@ def test_alpha_scales_match_oracle(normalize):
     G = cfg.n_grid
     s = torch.empty(G, K, dtype=torch.float32, device="cuda")
     inv = torch.empty_like(s)
-    capi.awq_alpha_scales(dev_f32(sx32), cfg, s, inv)
+    capi_testing.awq_alpha_scales(dev_f32(sx32), cfg, s, inv)
     s_h, inv_h = s.cpu().numpy().astype(np.float64), inv.cpu().numpy().astype(np.float64)
     assert np.all(s_h[0] == 1.0) and np.all(inv_h[0] == 1.0)
     for i, a in enumerate(O.alpha_grid(G)):
@@ -96,7 +96,7 @@ def test_fakequant_codes_and_values(layer, rows, form):
     s32, inv32 = _oracle_scales32(O.channel_importance(X), G)
     slots = G + 1 if form == capi.AWQ_LOSS_REFERENCE else G
     op = torch.empty(slots, N, K, dtype=torch.bfloat16, device="cuda")
-    capi.awq_fakequant(dev_weight(L), dev_f32(s32), dev_f32(inv32), cfg, op)
+    capi_testing.awq_fakequant(dev_weight(L), dev_f32(s32), dev_f32(inv32), cfg, op)
     got = host_bf16_to_f64(op)
     for i in range(G):
         W_hat = O.fake_quantize(W, s32[i])
@@ -114,20 +114,20 @@ def test_fakequant_codes_and_values(layer, rows, form):
 # ------------------------------------------------------------------ search product
 
 
-@pytest.mark.parametrize("cluster_m", [0, 1, 2, 4])  # 0: the default CTA-pair kernel
+@pytest.mark.parametrize("single_cta", [0, 1])  # 0: the default CTA-pair kernel
 @pytest.mark.parametrize("n,N,K,G", [(128, 256, 128, 1), (300, 520, 384, 3), (1, 7, 128, 2), (257, 130, 256, 2),
                                      (512, 1024, 1024, 2)])
-def test_search_gemm_products_and_partials(n, N, K, G, cluster_m):
+def test_search_gemm_products_and_partials(n, N, K, G, single_cta):
     rng = np.random.default_rng(n + 31 * N + 7 * K + G)
     A = _rand_bf16(rng, (n, K))
     B = _rand_bf16(rng, (G, N, K), 0.05)
     cfg = capi.config(n_grid=G)
-    mt, nt, tm, tn = capi.awq_search_tiles(n, N, cfg)
+    mt, nt, tm, tn = capi_testing.awq_search_tiles(n, N, cfg)
     partials = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device="cuda")
     dump = torch.zeros(G, n, N, dtype=torch.float32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
-    capi.awq_search_gemm_dump(dev_bf16(A), dev_bf16(B.reshape(G * N, K)), cfg, partials, status, dump,
-                              n_tok=n, in_features=K, out_features=N, cluster_m=cluster_m)
+    capi_testing.awq_search_gemm_dump(dev_bf16(A), dev_bf16(B.reshape(G * N, K)), cfg, partials, status, dump,
+                              n_tok=n, in_features=K, out_features=N, single_cta=single_cta)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     D = dump.cpu().numpy().astype(np.float64)
@@ -138,7 +138,7 @@ def test_search_gemm_products_and_partials(n, N, K, G, cluster_m):
         scale = np.sqrt(K) * 0.05
         ok = np.allclose(D[i], ref, rtol=1e-5, atol=1e-5 * scale)
         if not ok:
-            save_debug(f"gemm_{n}_{N}_{K}_{G}_{i}_c{cluster_m}", got=D[i], ref=ref, A=A, B=B[i])
+            save_debug(f"gemm_{n}_{N}_{K}_{G}_{i}_c{single_cta}", got=D[i], ref=ref, A=A, B=B[i])
         assert ok, f"product of alpha {i} differs: max err {np.abs(D[i] - ref).max()}"
         sq = ref * ref
         for mb in range(mt):
@@ -150,11 +150,11 @@ def test_search_gemm_products_and_partials(n, N, K, G, cluster_m):
                     assert P[i, mb, nb, q] == pytest.approx(expect, rel=1e-4, abs=1e-6)
     # the production entry point (the CTA-pair kernel) gives the same partials
     partials2 = torch.zeros_like(partials)
-    capi.awq_search_gemm(dev_bf16(A), dev_bf16(B.reshape(G * N, K)), cfg, partials2, status, n_tok=n,
+    capi_testing.awq_search_gemm(dev_bf16(A), dev_bf16(B.reshape(G * N, K)), cfg, partials2, status, n_tok=n,
                          in_features=K, out_features=N)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
-    if cluster_m == 0:
+    if single_cta == 0:
         assert torch.equal(partials, partials2)
     else:
         np.testing.assert_allclose(partials2.cpu().numpy(), partials.cpu().numpy(), rtol=1e-5, atol=1e-6)
@@ -180,18 +180,18 @@ def test_fused_search_matches_separate_stages(layer, kw):
     G = cfg.n_grid
     s = torch.empty(G, K, dtype=torch.float32, device="cuda")
     inv = torch.empty_like(s)
-    capi.awq_alpha_scales(dev_f32(O.f32(O.channel_importance(L["X"]))), cfg, s, inv)
+    capi_testing.awq_alpha_scales(dev_f32(O.f32(O.channel_importance(L["X"]))), cfg, s, inv)
     op_ref = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
-    capi.awq_fakequant(W, s, inv, cfg, op_ref)
-    mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
+    capi_testing.awq_fakequant(W, s, inv, cfg, op_ref)
+    mt, nt, _, _ = capi_testing.awq_search_tiles(n, N, cfg)
     p_ref = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
-    capi.awq_search_gemm(X, op_ref, cfg, p_ref, status, n_tok=n, in_features=K, out_features=N)
+    capi_testing.awq_search_gemm(X, op_ref, cfg, p_ref, status, n_tok=n, in_features=K, out_features=N)
     op = torch.full_like(op_ref, float("nan"))
     parts = torch.full_like(p_ref, float("nan"))
     ready = torch.full((G * (nt + 1) + 1,), 7, dtype=torch.int32, device="cuda")  # the call zeroes it
     for _ in range(2):  # twice: ready counters and op are reset / rewritten by each call
-        capi.awq_search_fused(W, X, s, inv, cfg, op, parts, ready, status)
+        capi_testing.awq_search_fused(W, X, s, inv, cfg, op, parts, ready, status)
         torch.cuda.synchronize()
         assert int(status[0]) == 0
         assert torch.equal(op.view(torch.int16), op_ref.view(torch.int16))
@@ -209,7 +209,7 @@ def test_loss_select_sums_argmin_and_copy():
     rng = np.random.default_rng(5)
     n, N, K, G = 300, 520, 256, 6
     cfg = capi.config(n_grid=G)
-    mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
+    mt, nt, _, _ = capi_testing.awq_search_tiles(n, N, cfg)
     parts = rng.uniform(0.0, 1.0, (G, mt, nt, 4)).astype(np.float32)
     parts[3] *= 0.25  # alpha 3 smallest
     parts[4] = parts[3]  # tie with 3: the first one wins
@@ -218,7 +218,7 @@ def test_loss_select_sums_argmin_and_copy():
     best = torch.empty(1, dtype=torch.int32, device="cuda")
     s_best = torch.empty(K, dtype=torch.float32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
-    capi.awq_loss_select(dev_f32(parts), dev_f32(s), cfg, losses, best, s_best, status, n_tok=n, out_features=N,
+    capi_testing.awq_loss_select(dev_f32(parts), dev_f32(s), cfg, losses, best, s_best, status, n_tok=n, out_features=N,
                          in_features=K)
     torch.cuda.synchronize()
     ref = parts.astype(np.float64).reshape(G, -1).sum(axis=1) / (n * N)
@@ -227,7 +227,7 @@ def test_loss_select_sums_argmin_and_copy():
     np.testing.assert_array_equal(s_best.cpu().numpy(), s[3])
     assert int(status[0]) == 0
     parts[1, 0, 0, 0] = np.nan
-    capi.awq_loss_select(dev_f32(parts), dev_f32(s), cfg, losses, best, s_best, status, n_tok=n, out_features=N,
+    capi_testing.awq_loss_select(dev_f32(parts), dev_f32(s), cfg, losses, best, s_best, status, n_tok=n, out_features=N,
                          in_features=K)
     torch.cuda.synchronize()
     assert int(status[0]) == capi.AWQ_ERR_NONFINITE
@@ -305,7 +305,7 @@ def test_symmetric_pack_and_fakequant_bit_exact(layer, kw):
     G = cfg.n_grid
     s32, inv32 = _oracle_scales32(sx, G)
     op = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
-    capi.awq_fakequant(dev_weight(L), dev_f32(s32), dev_f32(inv32), cfg, op)
+    capi_testing.awq_fakequant(dev_weight(L), dev_f32(s32), dev_f32(inv32), cfg, op)
     got = host_bf16_to_f64(op)
     W64 = W.astype(np.float64)
     for i in range(G):
@@ -355,7 +355,7 @@ def test_group_and_width_fakequant_values(group, w_bit, zero_point):
     G = cfg.n_grid
     s32, inv32 = _oracle_scales32(O.channel_importance(X), G)
     op = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
-    capi.awq_fakequant(dev_weight(L), dev_f32(s32), dev_f32(inv32), cfg, op)
+    capi_testing.awq_fakequant(dev_weight(L), dev_f32(s32), dev_f32(inv32), cfg, op)
     got = host_bf16_to_f64(op)
     for i in range(G):
         W_hat = O.fake_quantize(W, s32[i], w_bit=w_bit, group=group, zero_point=bool(zero_point))
@@ -377,17 +377,17 @@ def test_fused_search_matches_separate_stages_other_quantisers(group, w_bit, zer
     G = cfg.n_grid
     s = torch.empty(G, K, dtype=torch.float32, device="cuda")
     inv = torch.empty_like(s)
-    capi.awq_alpha_scales(dev_f32(O.f32(O.channel_importance(L["X"]))), cfg, s, inv)
+    capi_testing.awq_alpha_scales(dev_f32(O.f32(O.channel_importance(L["X"]))), cfg, s, inv)
     op_ref = torch.empty(G, N, K, dtype=torch.bfloat16, device="cuda")
-    capi.awq_fakequant(W, s, inv, cfg, op_ref)
-    mt, nt, _, _ = capi.awq_search_tiles(n, N, cfg)
+    capi_testing.awq_fakequant(W, s, inv, cfg, op_ref)
+    mt, nt, _, _ = capi_testing.awq_search_tiles(n, N, cfg)
     p_ref = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
-    capi.awq_search_gemm(X, op_ref, cfg, p_ref, status, n_tok=n, in_features=K, out_features=N)
+    capi_testing.awq_search_gemm(X, op_ref, cfg, p_ref, status, n_tok=n, in_features=K, out_features=N)
     op = torch.full_like(op_ref, float("nan"))
     parts = torch.full_like(p_ref, float("nan"))
     ready = torch.zeros((G * (nt + 1) + 1,), dtype=torch.int32, device="cuda")
-    capi.awq_search_fused(W, X, s, inv, cfg, op, parts, ready, status)
+    capi_testing.awq_search_fused(W, X, s, inv, cfg, op, parts, ready, status)
     torch.cuda.synchronize()
     assert int(status[0]) == 0
     assert torch.equal(op.view(torch.int16), op_ref.view(torch.int16))

@@ -637,3 +637,94 @@ def test_memory_arithmetic_70b_golden():
     assert b["codes"] == g["int4_bytes"]
     reduction = 1.0 - b["total"] / g["fp16_bytes"]
     assert g["stated_reduction"] <= reduction <= 0.75
+
+
+# ---------------------------------------------------------------- the composed search, restated independently
+
+
+def _torch_group_rtn(V, group=128, qmax=15.0, floor=1e-5):
+    """Asymmetric min/max group quantise-dequantise in torch float64, written
+    from the step-size equation of "AWQ > Salient Weight Preservation" and the
+    zero point of the deployment quant_config, independently of the oracle:
+    step = max((max - min) / (2^b - 1), floor), zero = round(-min / step),
+    code = clamp(round(v / step) + zero, 0, 2^b - 1), value = (code - zero) * step
+    (torch.round rounds half to even)."""
+    import torch
+
+    rows, K = V.shape
+    g = V.reshape(rows, K // group, group)
+    hi = g.amax(dim=2, keepdim=True)
+    lo = g.amin(dim=2, keepdim=True)
+    step = torch.clamp((hi - lo) / qmax, min=floor)
+    zero = torch.round(-lo / step)
+    code = torch.clamp(torch.round(g / step) + zero, 0.0, qmax)
+    return ((code - zero) * step).reshape(rows, K)
+
+
+def _torch_search(W, X, n_grid=20):
+    """The per-layer grid search of "AWQ: How Activation-Aware Quantization
+    Saves 4-bit LLMs" ("How does AWQ protect channels without mixed
+    precision?"), step by step in torch float64: the statistic is the mean
+    |x| per input channel; for alpha = i / n_grid the scale is the clamped
+    statistic to the power alpha; the weight's columns are multiplied by it,
+    quantised with the group quantiser, and divided by it again; the error is
+    the mean of the squared difference between the quantised layer's output
+    and the unquantised layer's output; a later alpha replaces the best only if
+    its error is strictly lower."""
+    import torch
+
+    Wt = torch.from_numpy(np.asarray(W, dtype=np.float64))
+    Xt = torch.from_numpy(np.asarray(X, dtype=np.float64))
+    sx = Xt.abs().mean(dim=0)
+    y_ref = Xt @ Wt.T
+    errs, best, best_err, best_s = [], -1, float("inf"), None
+    for i in range(n_grid):
+        s = sx.clamp(min=1e-4) ** (i / n_grid)
+        w_q = _torch_group_rtn(Wt * s) / s
+        err = float(((Xt @ w_q.T - y_ref) ** 2).mean())
+        errs.append(err)
+        if err < best_err:
+            best, best_err, best_s = i, err, s
+    return np.array(errs), best, best_s.numpy()
+
+
+@pytest.mark.parametrize("layer", ["tiny", "square1024"])
+def test_search_matches_an_independent_restatement(layer):
+    """The oracle's composed search (fp64 quantiser, no normalisation, as the
+    pages' search is written) equals an independent torch float64 statement
+    of the same steps: every per-alpha loss to 1e-12 relative, the same first
+    minimum and the same scale. With the normalisation on, the losses move by
+    rounding only (the normaliser cancels in exact arithmetic)."""
+    if layer == "tiny":
+        L = workloads.make_layer("tiny")
+    else:
+        L = workloads.make_layer("llama7b_q_proj", n_tok=256, out_features=1024, in_features=1024, seed=11)
+    W, X = L["W"].astype(np.float64), L["X"].astype(np.float64)
+    sx = O.channel_importance(X)
+    assert sx.min() > 1e-4  # the clamp constant (1e-4 here, its fp32 value in the oracle) never binds
+    ref_losses, ref_best, ref_s = _torch_search(W, X)
+    res = O.search_scale(W, X, sx, normalize=False, pinned=False)
+    np.testing.assert_allclose(res["losses"], ref_losses, rtol=1e-12)
+    assert res["best_idx"] == ref_best
+    np.testing.assert_allclose(res["s_best"], ref_s, rtol=1e-14)
+    norm = O.search_scale(W, X, sx, normalize=True, pinned=False)
+    np.testing.assert_allclose(norm["losses"], ref_losses, rtol=1e-10)
+    assert norm["best_idx"] == ref_best
+
+
+@pytest.mark.parametrize("layer", ["tiny", "square1024"])
+def test_fp32_decided_search_tracks_the_fp64_search(layer):
+    """The search whose codes are decided in fp32 (the precision the kernels
+    decide them in) against the same search in fp64: per-alpha losses within
+    1e-3 relative, and the same chosen alpha. A code can differ only where
+    v / step lies within an fp32 rounding of a half-integer."""
+    if layer == "tiny":
+        L = workloads.make_layer("tiny")
+    else:
+        L = workloads.make_layer("llama7b_q_proj", n_tok=256, out_features=1024, in_features=1024, seed=11)
+    W, X = L["W"].astype(np.float64), L["X"].astype(np.float64)
+    sx = O.channel_importance(X)
+    a = O.search_scale(W, X, sx, pinned=True)
+    b = O.search_scale(W, X, sx, pinned=False)
+    np.testing.assert_allclose(a["losses"], b["losses"], rtol=1e-3)
+    assert a["best_idx"] == b["best_idx"]
