@@ -16,10 +16,12 @@
 extern "C" {
 #endif
 
-/* awq_search_layer (RESIDUAL form) runs the fake-quant inside the search
-   kernel (awq_search_fused) when the search's products take fewer than this
-   many flops, 2 * n_grid * n_tok * out * in, and as a launch of its own
-   ahead of the products (awq_fakequant, then awq_search_gemm) otherwise. */
+/* awq_search_layer (RESIDUAL form) runs the fake-quant inside the CTA-pair
+   search kernel (awq_search_fused) when the search's products take fewer
+   than this many flops, 2 * n_grid * n_tok * out * in. Larger searches run
+   long enough to settle at the GPU's power limit, where the single-CTA
+   products draw less energy per flop: they run awq_fakequant, then
+   awq_search_gemm, whose products are the single-CTA kernel at that size. */
 #define AWQ_SEARCH_FUSED_MAX_FLOPS 2e13
 
 /* s[i][j] and inv_s[i][j] = 1/s[i][j] for every alpha_i (device fp32
@@ -50,7 +52,9 @@ AWQ_API awq_status awq_search_tiles(int64_t n_tok, int64_t out, const awq_config
    written by awq_fakequant. partials: device fp32 [n_grid][m_tiles][n_tiles][4].
    status: device uint32, set to AWQ_ERR_TIMEOUT if a wait ran out.
    tcgen05 tensor cores (bf16 in, fp32 accumulate in tensor memory), operands
-   staged by TMA; the RESIDUAL form runs on CTA pairs (cta_group::2). */
+   staged by TMA. The RESIDUAL form runs the products awq_search_layer runs
+   for this size: CTA pairs (cta_group::2) below AWQ_SEARCH_FUSED_MAX_FLOPS,
+   single CTAs from there on; the REFERENCE form runs on single CTAs. */
 AWQ_API awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, const uint16_t* op, int64_t out,
                                    const awq_config* cfg, float* partials, uint32_t* status, awq_stream_t stream);
 

@@ -19,11 +19,19 @@ namespace {
 constexpr size_t kAlign = 1024;
 
 // Search size (flops of the alpha products) from which awq_search_layer
-// runs the fake-quant as its own launch ahead of the CTA-pair products
-// instead of inside them.
+// runs the fake-quant as its own launch, followed by the single-CTA
+// products, instead of the fused CTA-pair kernel. A search this long runs at
+// the GPU's power limit, where the single-CTA products draw less energy per
+// flop (70B-class layer, same box, back to back: 108 ms at 1.26 GHz and
+// 0.85 kW against 135 ms at 0.95 GHz and 0.95 kW for the pair products).
 constexpr double kLargeSearchFlops = AWQ_SEARCH_FUSED_MAX_FLOPS;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Flops of a search's alpha products: 2 * n_grid * n_tok * out * in.
+inline double search_flops(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg) {
+  return 2.0 * cfg.n_grid * (double)n_tok * (double)out * (double)in;
+}
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Largest sizes accepted: every index the kernels form stays below 2^31 per
@@ -323,8 +331,10 @@ awq_status awq_search_gemm(const void* X, int64_t n_tok, int64_t in, const uint1
   st = check_dims(n_tok, out, in);
   if (st != AWQ_OK) return st;
   if (!aligned16(X) || !aligned16(op) || !aligned16(partials) || !aligned16(status)) return AWQ_ERR_MISALIGNED;
+  // the products awq_search_layer runs for a search of this size
+  const int single_cta = search_flops(n_tok, out, in, *cfg) >= kLargeSearchFlops ? 1 : 0;
   return from_cuda(launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status,
-                                      (cudaStream_t)stream));
+                                      (cudaStream_t)stream, nullptr, 0, single_cta));
 }
 
 awq_status awq_search_fused(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X, int64_t n_tok,
@@ -520,17 +530,17 @@ awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, c
   cudaError_t e = clear_status ? cudaMemsetAsync(status, 0, 4, s) : cudaSuccess;
   if (e == cudaSuccess && row_acc != nullptr) e = cudaMemsetAsync(row_acc, 0, (size_t)cfg->n_grid * out * 8, s);
   if (e == cudaSuccess) e = launch_alpha_scales(mean_abs, in, *cfg, sc, inv, s);
-  const double flops = 2.0 * cfg->n_grid * (double)n_tok * (double)out * (double)in;
+  const double flops = search_flops(n_tok, out, in, *cfg);
   if (cfg->loss_form == AWQ_LOSS_RESIDUAL && flops < kLargeSearchFlops) {
     // fake-quant runs inside the search kernel, ahead of the products that consume it
     if (e == cudaSuccess)
       e = launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, sc, inv, out, *cfg, op, partials, ready,
                               status, s, nullptr, -1, row_acc);
   } else if (cfg->loss_form == AWQ_LOSS_RESIDUAL) {
-    // the fake-quant launch, then the CTA-pair products
+    // the fake-quant launch, then the single-CTA products
     if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
     if (e == cudaSuccess)
-      e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 0, row_acc);
+      e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 1, row_acc);
   } else {
     if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
     if (e == cudaSuccess)

@@ -267,11 +267,18 @@ __device__ __forceinline__ void load8f(const float* p, float* v) {
 // its alphas). Products, differences and the dequantisation run as packed
 // fp32 pairs (one instruction, two correctly rounded results).
 
-constexpr int kFqCols = 512;        // input channels per strip (four 128-channel blocks)
-constexpr int kFqWarps = 8;         // rows in flight per block
-constexpr int kFqAlphaChunk = 20;   // alphas staged in shared memory at once
-constexpr int kFqSmem = 2 * kFqAlphaChunk * kFqCols * 4;  // s and 1/s: 80 KiB
-constexpr int kFqBlocksPerSm = 2;
+// Occupancy of the fake-quant kernel (build-time tunables, defaults measured best).
+#ifndef AWQ_FQ_ALPHA_CHUNK
+#define AWQ_FQ_ALPHA_CHUNK 20
+#endif
+#ifndef AWQ_FQ_BLOCKS_PER_SM
+#define AWQ_FQ_BLOCKS_PER_SM 2
+#endif
+constexpr int kFqCols = 512;                       // input channels per strip (four 128-channel blocks)
+constexpr int kFqWarps = 8;                        // rows in flight per block
+constexpr int kFqAlphaChunk = AWQ_FQ_ALPHA_CHUNK;  // alphas staged in shared memory at once
+constexpr int kFqSmem = 2 * kFqAlphaChunk * kFqCols * 4;  // s and 1/s: 80 KiB for 20 alphas
+constexpr int kFqBlocksPerSm = AWQ_FQ_BLOCKS_PER_SM;
 
 template <typename WT>
 struct RowRegs;
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
 
     int row = r_begin + warp;
     RowRegs<WT> nxt{};
-    const size_t wn = (size_t)N * K;  // elements of W and of one operand slot
+    [[maybe_unused]] const size_t wn = (size_t)N * K;  // elements of W and of one operand slot (bounds checks)
     if (row < r_end && AWQ_IN((size_t)row * K + col0 + c_lo, 72, wn)) nxt.load(W + (size_t)row * K + col0 + c_lo);
     for (; row < r_end; row += kFqWarps) {
       float2 w[8];
@@ -494,7 +501,7 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>
     for (int i = 0; i < 8; ++i) sv[i] = make_float2(t[2 * i], t[2 * i + 1]);
   }
   const int kw = K * BITS / 32, kg = K / GROUP;  // code words and groups per row
-  const size_t wn = (size_t)N * K;
+  [[maybe_unused]] const size_t wn = (size_t)N * K;  // elements of W (bounds checks)
   int row = r_begin + warp;
   RowRegs<WT> nxt{};
   if (row < r_end && AWQ_IN((size_t)row * K + col0 + c_lo, 72, wn)) nxt.load(W + (size_t)row * K + col0 + c_lo);
@@ -510,33 +517,56 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>
     lane_groups<GROUP>(v, qmax, floor_, symmetric != 0, ga, gb);
     float2 k[8];
     lane_codes_minus_z<GROUP>(v, ga, gb, k);
-    // q = (q - z) + z in [0, 2^b - 1]; 2^23 + q carries q in its low mantissa
-    // bits, which avoids a float-to-integer conversion per code
-    const float2 za = make_float2(8388608.0f + ga.z, 8388608.0f + ga.z);
-    const float2 zb = make_float2(8388608.0f + gb.z, 8388608.0f + gb.z);
-    constexpr uint32_t kMask = (1u << BITS) - 1u;
-    uint32_t qa[8], qb[8];  // the codes of run A and run B
+    uint32_t wa[2] = {0u, 0u}, wb[2] = {0u, 0u};  // run A's and run B's words
+    if constexpr (BITS == 4) {
+      // q = (q - z) + z, exact integers in [0, 15]. A run of 8 codes is one word q_0 + 16 q_1 + ... + 16^7 q_7
+      // (column order), built as two 16-bit halves h = (q_0 + 256 q_2) + 16 (q_1 + 256 q_3): every step is
+      // exact in fp32 (h < 2^16), and 2^23 + h carries h in its low mantissa bits, so one byte permute joins
+      // the two halves without a float-to-integer conversion or a shift per code
+      const float2 za = make_float2(ga.z, ga.z), zb = make_float2(gb.z, gb.z);
+      const float2 c256 = make_float2(256.0f, 256.0f);
+      float2 qa4[4], qb4[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 a = __fadd2_rn(k[i], za);
-      const float2 b = __fadd2_rn(k[4 + i], zb);
-      qa[2 * i] = __float_as_uint(a.x) & kMask;
-      qa[2 * i + 1] = __float_as_uint(a.y) & kMask;
-      qb[2 * i] = __float_as_uint(b.x) & kMask;
-      qb[2 * i + 1] = __float_as_uint(b.y) & kMask;
-    }
-    // words of 32 / BITS codes, column (32/b) j + k in bits [b k, b k + b) of word j: a run of 8 codes is
-    // one word (4 bits), two words (8 bits) or half a word (2 bits, joined with the next lane's half)
-    uint32_t wa[2] = {0u, 0u}, wb[2] = {0u, 0u};
+      for (int i = 0; i < 4; ++i) {
+        qa4[i] = __fadd2_rn(k[i], za);
+        qb4[i] = __fadd2_rn(k[4 + i], zb);
+      }
+      const float2 pa0 = __ffma2_rn(qa4[1], c256, qa4[0]), pa1 = __ffma2_rn(qa4[3], c256, qa4[2]);
+      const float2 pb0 = __ffma2_rn(qb4[1], c256, qb4[0]), pb1 = __ffma2_rn(qb4[3], c256, qb4[2]);
+      const float ha0 = __fmaf_rn(pa0.y, 16.0f, __fadd_rn(pa0.x, 8388608.0f));
+      const float ha1 = __fmaf_rn(pa1.y, 16.0f, __fadd_rn(pa1.x, 8388608.0f));
+      const float hb0 = __fmaf_rn(pb0.y, 16.0f, __fadd_rn(pb0.x, 8388608.0f));
+      const float hb1 = __fmaf_rn(pb1.y, 16.0f, __fadd_rn(pb1.x, 8388608.0f));
+      wa[0] = __byte_perm(__float_as_uint(ha0), __float_as_uint(ha1), 0x5410);
+      wb[0] = __byte_perm(__float_as_uint(hb0), __float_as_uint(hb1), 0x5410);
+    } else {
+      // q = (q - z) + z in [0, 2^b - 1]; 2^23 + q carries q in its low mantissa
+      // bits, which avoids a float-to-integer conversion per code
+      const float2 za = make_float2(8388608.0f + ga.z, 8388608.0f + ga.z);
+      const float2 zb = make_float2(8388608.0f + gb.z, 8388608.0f + gb.z);
+      constexpr uint32_t kMask = (1u << BITS) - 1u;
+      uint32_t qa[8], qb[8];  // the codes of run A and run B
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int word = (e * BITS) >> 5, bit = (e * BITS) & 31;
-      wa[word] |= qa[e] << bit;
-      wb[word] |= qb[e] << bit;
-    }
-    if (BITS == 2) {  // the odd lane's 16 bits go above the even lane's (8 channels further on)
-      wa[0] |= __shfl_down_sync(0xffffffffu, wa[0], 1) << 16;
-      wb[0] |= __shfl_down_sync(0xffffffffu, wb[0], 1) << 16;
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = __fadd2_rn(k[i], za);
+        const float2 b = __fadd2_rn(k[4 + i], zb);
+        qa[2 * i] = __float_as_uint(a.x) & kMask;
+        qa[2 * i + 1] = __float_as_uint(a.y) & kMask;
+        qb[2 * i] = __float_as_uint(b.x) & kMask;
+        qb[2 * i + 1] = __float_as_uint(b.y) & kMask;
+      }
+      // words of 32 / BITS codes, column (32/b) j + k in bits [b k, b k + b) of word j: a run of 8 codes is
+      // two words (8 bits) or half a word (2 bits, joined with the next lane's half)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int word = (e * BITS) >> 5, bit = (e * BITS) & 31;
+        wa[word] |= qa[e] << bit;
+        wb[word] |= qb[e] << bit;
+      }
+      if (BITS == 2) {  // the odd lane's 16 bits go above the even lane's (8 channels further on)
+        wa[0] |= __shfl_down_sync(0xffffffffu, wa[0], 1) << 16;
+        wb[0] |= __shfl_down_sync(0xffffffffu, wb[0], 1) << 16;
+      }
     }
     const size_t w_at = (size_t)row * kw + (size_t)(col0 + c_lo) * BITS / 32;  // run A's first word
     constexpr int kRunB = 64 * BITS / 32;                                      // words from run A to run B

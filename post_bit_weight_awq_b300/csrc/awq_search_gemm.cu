@@ -87,7 +87,7 @@ struct Params {
 // 16-byte aligned (N a multiple of 4), else one value at a time.
 __device__ __forceinline__ void store_products(const Params& p, int a, int row, int col0, const uint32_t (&v)[32]) {
   const size_t base = ((size_t)a * p.n_tok + row) * p.N + col0;
-  const size_t total = (size_t)p.G * p.n_tok * p.N;
+  [[maybe_unused]] const size_t total = (size_t)p.G * p.n_tok * p.N;  // (bounds checks)
   if (col0 + 32 <= p.N && (p.N & 3) == 0) {
     if (!AWQ_IN(base, 32, total)) return;
     float4* d = reinterpret_cast<float4*>(p.dump + base);
@@ -500,7 +500,7 @@ __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane
         ldg_lane16(p.s + (size_t)a * p.K + c, sv);
         ldg_lane16(p.inv_s + (size_t)a * p.K + c, iv);
       }
-      const size_t wn_elems = (size_t)p.N * p.K;
+      [[maybe_unused]] const size_t wn_elems = (size_t)p.N * p.K;  // (bounds checks)
       float2 wn[8] = {};
       if (AWQ_IN((size_t)r0 * p.K + c, 72, wn_elems)) ldg_w16(p.W, p.w_bf16, (size_t)r0 * p.K + c, wn);
       for (int r = r0; r < r1; ++r) {
