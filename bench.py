@@ -231,7 +231,7 @@ def hbm_bytes(n, N, K, G, wbytes):
 class LayerRun:
     """One layer resident on the device with the buffers of the three public calls."""
 
-    def __init__(self, name, dev, cfg):
+    def __init__(self, name, dev, cfg, rows=None):
         import numpy as np
         import torch
 
@@ -239,7 +239,7 @@ class LayerRun:
         from post_bit_weight_awq_b300 import capi
 
         self.name = name
-        L = workloads.make_layer(name)
+        L = workloads.make_layer(name, out_features=rows)
         self.L = L
         W32, X32 = L["W"], L["X"]
         self.N, self.K = W32.shape
@@ -294,7 +294,7 @@ class LayerRun:
         if not os.path.exists(gpath):
             return None
         g = json.load(open(gpath)).get(self.name)
-        if not g:
+        if not g or g["out_features"] != self.N:
             return None
         lo = np.array(g["losses"])
         lg = self.losses.cpu().numpy().astype(np.float64)
@@ -472,7 +472,6 @@ def prefill_line(R, dev, flush, pk, reps):
 
 
 def gpu_arm(args, rank, world, local_rank):
-    import numpy as np
     import torch
 
     import workloads
@@ -491,7 +490,7 @@ def gpu_arm(args, rank, world, local_rank):
     pk = peaks()
     name = workloads.WORKLOADS[args.workload][0]
     cfg = capi.config()
-    R = LayerRun(name, dev, cfg)
+    R = LayerRun(name, dev, cfg, rows=args.rows)
     n, N, K, G = R.n, R.N, R.K, R.G
     flops = R.flops
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -569,48 +568,12 @@ def gpu_arm(args, rank, world, local_rank):
     sustained = pk.get("bf16_tflops_sustained")
     peak, peak_kind = (sustained, "sustained") if (long_step and sustained) else (pk["bf16_tflops"], "burst")
 
-    # ---------------------------------------------------------- end to end (host buffers)
-    # the public layer pipeline (awq_quantize_layers): K layers whose W and X sit in pinned host memory, each
-    # copied in, searched, packed and copied out; the copies of one layer overlap the search of the next
     L = R.L
-    pin = dict(pin_memory=True)
-    Wh = (torch.from_numpy(workloads.bf16_bits(L["W"]).view(np.int16)).view(torch.bfloat16) if L["w_dtype"] == "bf16"
-          else torch.from_numpy(L["W"])).pin_memory()
-    Xh = torch.from_numpy(workloads.bf16_bits(L["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    outs_h = {"qweight": torch.empty(N, K // 8, dtype=torch.int32, **pin),
-              "scales": torch.empty(N, K // 128, dtype=torch.float16, **pin),
-              "zeros": torch.empty(N, K // 128, dtype=torch.float16, **pin),
-              "losses": torch.empty(G, dtype=torch.float32, **pin),
-              "best_idx": torch.empty(1, dtype=torch.int32, **pin),
-              "s_best": torch.empty(K, dtype=torch.float32, **pin)}
-    wcode = capi.AWQ_BF16 if L["w_dtype"] == "bf16" else capi.AWQ_FP32
-    pipe_ws = torch.empty(capi.awq_pipeline_workspace_size(n, N, K, wcode, cfg), dtype=torch.uint8, device=dev)
-    h2d = Wh.numel() * Wh.element_size() + Xh.numel() * Xh.element_size()
-    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
-    io = capi.layer_io(Wh, Xh, outs_h["qweight"], outs_h["scales"], outs_h["zeros"], outs_h["losses"],
-                       outs_h["best_idx"], outs_h["s_best"])
-    capi.awq_quantize_layers([io] * 3, wcode, cfg, pipe_ws, stream)
-    torch.cuda.synchronize()
-    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush.zero_()
-    ea.record(stream)
-    capi.awq_quantize_layers([io] * args.steps, wcode, cfg, pipe_ws, stream)
-    eb.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = ea.elapsed_time(eb) / args.steps
-    if dist:
-        e2e_ms = multi.max_over_ranks(e2e_ms, device=dev) / world
-    assert capi.awq_get_device_status(pipe_ws, stream) == capi.AWQ_OK
-    assert int(outs_h["best_idx"][0]) == int(R.best[0])  # the streamed layer chose what the device path chose
-    assert torch.equal(outs_h["qweight"], R.qw.cpu())  # and packed the same codes
-    del pipe_ws, Wh, Xh
-
-    # ---------------------------------------------------------- the packed layer in use
-    gemv = decode_line(R, dev, flush, pk, max(3, args.steps // 2))
-    gemm = prefill_line(R, dev, flush, pk, max(3, args.steps // 2))
-
-    # ---------------------------------------------------------- the other workloads, one entry per layer
-    side = None
+    e2e, gemv, gemm, side = None, None, None, None
+    if not args.no_extras:
+        e2e = end_to_end(R, args, cfg, dev, flush, stream, world, dist)
+        gemv = decode_line(R, dev, flush, pk, max(3, args.steps // 2))
+        gemm = prefill_line(R, dev, flush, pk, max(3, args.steps // 2))
     del R, graph
     torch.cuda.empty_cache()
     if not args.no_side and world == 1:
@@ -646,10 +609,7 @@ def gpu_arm(args, rank, world, local_rank):
                      "launch_ms": search_ms},
         "calls": {k: round(v, 4) for k, v in calls_ms.items()},
         "kernels": kern,
-        "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "awq_quantize_layers: steps layers in one call, each layer's W and X copied in from pinned "
-                       "host memory and its packed outputs, losses and s_best copied out, copies overlapping the "
-                       "previous layer's search (no L2 flush inside the call)"},
+        "e2e": e2e,
         # stats, alpha scales, [fake-quant,] search product, loss reduce, select, pack
         "gpu_launches": (6 if fused_path else 7) * args.steps,
         "clocks": clocks,
@@ -663,6 +623,54 @@ def gpu_arm(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def end_to_end(R, args, cfg, dev, flush, stream, world, dist):
+    """The public layer pipeline (awq_quantize_layers): K layers whose W and X sit in pinned host memory, each
+    copied in, searched, packed and copied out; the copies of one layer overlap the search of the next."""
+    import numpy as np
+    import torch
+
+    import workloads
+    from post_bit_weight_awq_b300 import capi, multi
+
+    L = R.L
+    n, N, K, G = R.n, R.N, R.K, R.G
+    pin = dict(pin_memory=True)
+    Wh = (torch.from_numpy(workloads.bf16_bits(L["W"]).view(np.int16)).view(torch.bfloat16) if L["w_dtype"] == "bf16"
+          else torch.from_numpy(L["W"])).pin_memory()
+    Xh = torch.from_numpy(workloads.bf16_bits(L["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    outs_h = {"qweight": torch.empty(N, K // 8, dtype=torch.int32, **pin),
+              "scales": torch.empty(N, K // 128, dtype=torch.float16, **pin),
+              "zeros": torch.empty(N, K // 128, dtype=torch.float16, **pin),
+              "losses": torch.empty(G, dtype=torch.float32, **pin),
+              "best_idx": torch.empty(1, dtype=torch.int32, **pin),
+              "s_best": torch.empty(K, dtype=torch.float32, **pin)}
+    wcode = capi.AWQ_BF16 if L["w_dtype"] == "bf16" else capi.AWQ_FP32
+    pipe_ws = torch.empty(capi.awq_pipeline_workspace_size(n, N, K, wcode, cfg), dtype=torch.uint8, device=dev)
+    h2d = Wh.numel() * Wh.element_size() + Xh.numel() * Xh.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+    io = capi.layer_io(Wh, Xh, outs_h["qweight"], outs_h["scales"], outs_h["zeros"], outs_h["losses"],
+                       outs_h["best_idx"], outs_h["s_best"])
+    capi.awq_quantize_layers([io] * 3, wcode, cfg, pipe_ws, stream)
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush.zero_()
+    ea.record(stream)
+    capi.awq_quantize_layers([io] * args.steps, wcode, cfg, pipe_ws, stream)
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / args.steps
+    if dist:
+        e2e_ms = multi.max_over_ranks(e2e_ms, device=dev) / world
+    assert capi.awq_get_device_status(pipe_ws, stream) == capi.AWQ_OK
+    assert int(outs_h["best_idx"][0]) == int(R.best[0])  # the streamed layer chose what the device path chose
+    assert torch.equal(outs_h["qweight"], R.qw.cpu())  # and packed the same codes
+    del pipe_ws, Wh, Xh
+    return {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "awq_quantize_layers: steps layers in one call, each layer's W and X copied in from pinned host "
+                   "memory and its packed outputs, losses and s_best copied out, copies overlapping the previous "
+                   "layer's search (no L2 flush inside the call)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -674,6 +682,9 @@ def main():
     ap.add_argument("--reference-rows", type=int, default=64, help="output rows per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side", action="store_true", help="skip the entries of the other workloads")
+    ap.add_argument("--no-extras", action="store_true", help="skip the end-to-end, decode and prefill timings")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="output rows of the layer (default: the workload's); a smaller case for profiler captures")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -155,11 +155,11 @@ AWQ_API awq_status awq_act_stats_workspace_size(int64_t n_tok, int64_t in, size_
 AWQ_API awq_status awq_act_stats(const void* X, int32_t x_dtype, int64_t n_tok, int64_t in,
                          float* mean_abs, void* ws, size_t ws_bytes, awq_stream_t stream);
 
-/* Largest number of fp32 partial sums (awq_act_stats_workspace_size less
-   its counters, i.e. chunks * in with at most 592 / ceil(in / 256) + 1
-   chunks of tokens) that awq_act_stats_noalloc accepts: its fixed scratch
-   holds 4 MiB of partial sums plus 16 KiB of counters. Every n_tok is
-   accepted for in up to 896768 channels. */
+/* Largest number of fp32 partial sums (chunks * in, with
+   max(1, 592 / ceil(in / 256)) chunks of tokens at most) that
+   awq_act_stats_noalloc accepts: its fixed scratch holds 4 MiB of partial
+   sums plus 16 KiB of counters. Every n_tok is accepted for in up to 2^20
+   channels. */
 #define AWQ_NOALLOC_STATS_MAX_FLOATS (1u << 20)
 
 /* awq_act_stats for callers that cannot allocate device memory or pass a

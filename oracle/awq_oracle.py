@@ -27,8 +27,7 @@ Sources (web pages on AWQ, cited by title and section):
   activations) and the decode remark after it (token-by-token decoding is
   memory-bound, so reading a quarter of the weight bytes is the payoff).
 
-Readings taken where the pages are silent or disagree (each also listed in
-the design notes):
+Readings taken where the pages are silent or disagree:
 
 * Quantiser: asymmetric min/max with a zero point [AWQ-SWP step-size equation;
   AWQ-devto quant_config], not the symmetric max|w| form of [AWQ-devto, "Why

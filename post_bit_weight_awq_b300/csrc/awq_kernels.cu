@@ -254,18 +254,16 @@ __device__ __forceinline__ void load8f(const float* p, float* v) {
 // slot G, bf16(W).
 //
 // A block owns a strip of 512 input channels (four 128-channel blocks) and a
-// range of output rows; each warp takes one row of the strip at a time, 8
-// lanes per 128-channel block and 16 weights per lane: lane l of a block
-// holds channels [8l, 8l+8) and [64+8l, 64+8l+8), so each 16-byte load or
-// store of the warp covers four whole 128-byte segments. A group of 128 is
-// one block; groups of 64 or 32 are one run of 8 or 4 lanes (the quantiser
-// reduces each run separately). The strip's s and 1/s for a chunk of
-// alphas are staged in shared memory once per block, in lane order (float4 q
-// of lane l at [q][l]) so that every 16-byte shared load of a warp reads 512
-// contiguous bytes without bank conflicts, and reused by every row. W is read
-// once (the next row's weights are loaded while the current row runs through
-// its alphas). Products, differences and the dequantisation run as packed
-// fp32 pairs (one instruction, two correctly rounded results).
+// range of output rows; each warp takes two rows of the strip at a time, one
+// per half-warp, in the quad layout of awq_quant.cuh: the 4 lanes of a quad
+// share a 128-channel block, lane quarter p holding the runs of 8 channels at
+// 32 j + 8 p (j = 0..3), 32 weights per lane. Every 16-byte load or store of
+// a warp then covers 64 contiguous bytes of each of the 8 (row, block)
+// pairs. The strip's s and 1/s for a chunk of alphas are staged in shared
+// memory once per block, in the order the lanes read them (the 16 lanes of a
+// half-warp read 256 contiguous bytes per 16-byte load, the two halves the
+// same addresses), and reused by every row. W is read once: the next row
+// pair's weights load while the current pair runs through its alphas.
 
 // Occupancy of the fake-quant kernel (build-time tunables, defaults measured best).
 #ifndef AWQ_FQ_ALPHA_CHUNK
@@ -275,64 +273,88 @@ __device__ __forceinline__ void load8f(const float* p, float* v) {
 #define AWQ_FQ_BLOCKS_PER_SM 2
 #endif
 constexpr int kFqCols = 512;                       // input channels per strip (four 128-channel blocks)
-constexpr int kFqWarps = 8;                        // rows in flight per block
+constexpr int kFqWarps = 8;                        // row pairs in flight per block
 constexpr int kFqAlphaChunk = AWQ_FQ_ALPHA_CHUNK;  // alphas staged in shared memory at once
-constexpr int kFqSmem = 2 * kFqAlphaChunk * kFqCols * 4;  // s and 1/s: 80 KiB for 20 alphas
+constexpr int kFqQuadF4 = 128;                     // float4 of s (or 1/s) per alpha per strip
+constexpr int kFqSmem = 2 * kFqAlphaChunk * kFqQuadF4 * 16;  // s and 1/s: 80 KiB for 20 alphas
 constexpr int kFqBlocksPerSm = AWQ_FQ_BLOCKS_PER_SM;
 
+// A lane's 32 weights of one row in the quad layout (runs at c, c+32, c+64, c+96).
 template <typename WT>
-struct RowRegs;
+struct QuadRow;
 template <>
-struct RowRegs<uint16_t> {
-  uint4 a, b;
+struct QuadRow<uint16_t> {
+  uint4 r[4];
   __device__ __forceinline__ void load(const uint16_t* p) {
-    a = *reinterpret_cast<const uint4*>(p);
-    b = *reinterpret_cast<const uint4*>(p + 64);
-  }
-  __device__ __forceinline__ void unpack(float2 (&w)[8]) const {
-    const uint32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = make_float2(bf16_lo(x[i]), bf16_hi(x[i]));
+    for (int j = 0; j < 4; ++j) r[j] = *reinterpret_cast<const uint4*>(p + 32 * j);
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r[j] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __device__ __forceinline__ void unpack_run(int j, float2 (&w)[4]) const {
+    const uint32_t x[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = make_float2(bf16_lo(x[i]), bf16_hi(x[i]));
+  }
+  __device__ __forceinline__ void unpack(float2 (&w)[16]) const {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 w4[4];
+      unpack_run(j, w4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[4 * j + i] = w4[i];
+    }
   }
 };
 template <>
-struct RowRegs<float> {
-  float4 a0, a1, b0, b1;
+struct QuadRow<float> {
+  float4 r[8];
   __device__ __forceinline__ void load(const float* p) {
-    a0 = *reinterpret_cast<const float4*>(p);
-    a1 = *reinterpret_cast<const float4*>(p + 4);
-    b0 = *reinterpret_cast<const float4*>(p + 64);
-    b1 = *reinterpret_cast<const float4*>(p + 68);
-  }
-  __device__ __forceinline__ void unpack(float2 (&w)[8]) const {
-    const float4 x[4] = {a0, a1, b0, b1};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      w[2 * i] = make_float2(x[i].x, x[i].y);
-      w[2 * i + 1] = make_float2(x[i].z, x[i].w);
+    for (int j = 0; j < 4; ++j) {
+      r[2 * j] = *reinterpret_cast<const float4*>(p + 32 * j);
+      r[2 * j + 1] = *reinterpret_cast<const float4*>(p + 32 * j + 4);
+    }
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) r[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __device__ __forceinline__ void unpack_run(int j, float2 (&w)[4]) const {
+    w[0] = make_float2(r[2 * j].x, r[2 * j].y);
+    w[1] = make_float2(r[2 * j].z, r[2 * j].w);
+    w[2] = make_float2(r[2 * j + 1].x, r[2 * j + 1].y);
+    w[3] = make_float2(r[2 * j + 1].z, r[2 * j + 1].w);
+  }
+  __device__ __forceinline__ void unpack(float2 (&w)[16]) const {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      w[2 * j] = make_float2(r[j].x, r[j].y);
+      w[2 * j + 1] = make_float2(r[j].z, r[j].w);
     }
   }
 };
 
-// The 16 values of one lane from a lane-ordered shared-memory row [4][32] of float4.
-__device__ __forceinline__ void lds_lane16(const float4* row, int lane, float2 (&v)[8]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 x = row[q * 32 + lane];
-    v[2 * q] = make_float2(x.x, x.y);
-    v[2 * q + 1] = make_float2(x.z, x.w);
-  }
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
 
-// Scales of one alpha for fq_lane16, from the lane-ordered shared-memory rows.
-struct SmemLane {
+// Scales of one alpha for fq_quad, from the staged shared-memory rows
+// [4 runs][2 halves of a run][16 quad slots] of float4.
+struct SmemQuad {
   const float4* s;
   const float4* inv;
-  int lane;
-  __device__ __forceinline__ void load_s(float2 (&v)[8]) const { lds_lane16(s, lane, v); }
-  __device__ __forceinline__ void load_inv(float2 (&v)[8]) const { lds_lane16(inv, lane, v); }
+  int slot;  // 4 * block + quarter
+  __device__ __forceinline__ static void get(const float4* base, int slot, int j, float2 (&v)[4]) {
+    const float4 a = base[(2 * j) * 16 + slot];
+    const float4 b = base[(2 * j + 1) * 16 + slot];
+    v[0] = make_float2(a.x, a.y);
+    v[1] = make_float2(a.z, a.w);
+    v[2] = make_float2(b.x, b.y);
+    v[3] = make_float2(b.z, b.w);
+  }
+  __device__ __forceinline__ void load_s(int j, float2 (&v)[4]) const { get(s, slot, j, v); }
+  __device__ __forceinline__ void load_inv(int j, float2 (&v)[4]) const { get(inv, slot, j, v); }
 };
 
 template <typename WT, bool REF, int GROUP>
@@ -341,8 +363,8 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
                      const float* __restrict__ inv_s, float qmax, float floor_, int symmetric,
                      uint16_t* __restrict__ op, int64_t slot_elems, int nstrips, int rows_per_block) {
   extern __shared__ float4 fq_smem[];
-  float4* ss = fq_smem;                          // [chunk][4][32] float4
-  float4* si = fq_smem + kFqAlphaChunk * 128;    // same for 1/s
+  float4* ss = fq_smem;                            // [chunk][4][2][16] float4
+  float4* si = fq_smem + kFqAlphaChunk * kFqQuadF4;  // same for 1/s
   const int strip = blockIdx.x % nstrips;
   const int col0 = strip * kFqCols;
   const int ncols = min(kFqCols, K - col0);  // a multiple of 128
@@ -350,56 +372,56 @@ __global__ void __launch_bounds__(kFqWarps * 32, kFqBlocksPerSm)
   const int r_end = min(N, r_begin + rows_per_block);
   if (r_begin >= r_end) return;  // uniform over the block
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = lane >> 3, sub = lane & 7;
-  // Groups past a partial strip repeat group 0's work and store nothing.
-  const bool active = grp * 128 < ncols;
-  const int slane = active ? lane : sub;
-  const int c_lo = (active ? grp * 128 : 0) + sub * 8;  // channels c_lo + [0,8) and c_lo + 64 + [0,8)
+  const int hw = lane >> 4, blk = (lane >> 2) & 3, quarter = lane & 3;
+  // Blocks past a partial strip repeat block 0's work and store nothing.
+  const bool active = blk * 128 < ncols;
+  const int slot = (active ? blk : 0) * 4 + quarter;
+  const int c_lo = (active ? blk * 128 : 0) + 8 * quarter;  // runs at c_lo + 32 j within the strip
+  const QuantSpec q = make_quant_spec(qmax, floor_, symmetric != 0);
+  [[maybe_unused]] const size_t wn = (size_t)N * K;  // elements of W and of one operand slot (bounds checks)
+  const int pair_step = 2 * kFqWarps;
 
   for (int a0 = 0; a0 < G; a0 += kFqAlphaChunk) {
     const int gc = min(kFqAlphaChunk, G - a0);
     __syncthreads();  // the previous chunk's scales are no longer read
-    const int c4n = ncols >> 2;
-    for (int i = threadIdx.x; i < gc * c4n; i += blockDim.x) {
-      const int a = i / c4n, c4 = i - a * c4n;
-      const int c = 4 * c4;  // channel within the strip -> (lane, float4 index q)
-      const int e = c & 127, h = e & 63;
-      const int ln = (c >> 7) * 8 + (h >> 3);
-      const int q = (e >> 6) * 2 + ((h & 7) >> 2);
+    for (int i = threadIdx.x; i < gc * kFqQuadF4; i += blockDim.x) {
+      const int a = i / kFqQuadF4, c = 4 * (i - a * kFqQuadF4);  // channel within the strip
+      const int b = c >> 7, e = c & 127;
+      const int idx = ((a * 4 + (e >> 5)) * 2 + ((e & 7) >> 2)) * 16 + b * 4 + ((e & 31) >> 3);
       const size_t g = (size_t)(a0 + a) * K + col0 + c;
-      const bool ok = AWQ_IN(g, 4, (size_t)G * K);
-      ss[(a * 4 + q) * 32 + ln] = ok ? *reinterpret_cast<const float4*>(s + g) : make_float4(1.f, 1.f, 1.f, 1.f);
-      si[(a * 4 + q) * 32 + ln] = ok ? *reinterpret_cast<const float4*>(inv_s + g) : make_float4(1.f, 1.f, 1.f, 1.f);
+      const bool ok = c < ncols && AWQ_IN(g, 4, (size_t)G * K);
+      ss[idx] = ok ? *reinterpret_cast<const float4*>(s + g) : make_float4(1.f, 1.f, 1.f, 1.f);
+      si[idx] = ok ? *reinterpret_cast<const float4*>(inv_s + g) : make_float4(1.f, 1.f, 1.f, 1.f);
     }
     __syncthreads();
 
-    int row = r_begin + warp;
-    RowRegs<WT> nxt{};
-    [[maybe_unused]] const size_t wn = (size_t)N * K;  // elements of W and of one operand slot (bounds checks)
-    if (row < r_end && AWQ_IN((size_t)row * K + col0 + c_lo, 72, wn)) nxt.load(W + (size_t)row * K + col0 + c_lo);
-    for (; row < r_end; row += kFqWarps) {
-      float2 w[8];
-      nxt.unpack(w);
+    // row pairs: this half-warp's row is first + hw; the loop condition is the pair's, uniform over the warp.
+    // A pair's weights are loaded as it starts: its alpha loop is long, and the other warps of the SM issue
+    // while this one waits, so a prefetch buffer would only cost registers.
+    for (int first = r_begin + 2 * warp; first < r_end; first += pair_step) {
+      const int row = first + hw;
+      const bool live = row < r_end;
       const size_t base = (size_t)row * K + col0 + c_lo;
-      if (row + kFqWarps < r_end && AWQ_IN(base + (size_t)kFqWarps * K, 72, wn))
-        nxt.load(W + base + (size_t)kFqWarps * K);
-      if (REF && a0 == 0 && active && AWQ_IN((size_t)G * slot_elems + base, 72, (size_t)(G + 1) * wn)) {
-        uint4* dst = reinterpret_cast<uint4*>(op + (size_t)G * slot_elems + base);
-        dst[0] = make_uint4(pack_bf16x2(w[0]), pack_bf16x2(w[1]), pack_bf16x2(w[2]), pack_bf16x2(w[3]));
-        dst[8] = make_uint4(pack_bf16x2(w[4]), pack_bf16x2(w[5]), pack_bf16x2(w[6]), pack_bf16x2(w[7]));
+      float2 w[16];
+      {
+        QuadRow<WT> cur;
+        cur.zero();
+        if (live && AWQ_IN(base, 104, wn)) cur.load(W + base);
+        cur.unpack(w);
       }
-      float2 nw[8];  // -w
+      if (REF && a0 == 0 && live && active && AWQ_IN((size_t)G * slot_elems + base, 104, (size_t)(G + 1) * wn)) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) nw[i] = make_float2(-w[i].x, -w[i].y);
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(op + (size_t)G * slot_elems + base + 32 * j) =
+              make_uint4(pack_bf16x2(w[4 * j]), pack_bf16x2(w[4 * j + 1]), pack_bf16x2(w[4 * j + 2]),
+                         pack_bf16x2(w[4 * j + 3]));
+      }
 #pragma unroll 1
       for (int a = 0; a < gc; ++a) {
-        uint32_t o[8];
-        fq_lane16<REF, GROUP>(w, nw, SmemLane{ss + a * 128, si + a * 128, slane}, qmax, floor_, symmetric != 0, o);
-        if (active && AWQ_IN((size_t)(a0 + a) * slot_elems + base, 72, (size_t)(REF ? G + 1 : G) * wn)) {
-          uint4* dst = reinterpret_cast<uint4*>(op + (size_t)(a0 + a) * slot_elems + base);
-          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-          dst[8] = make_uint4(o[4], o[5], o[6], o[7]);  // 64 channels further on
-        }
+        const bool store =
+            live && active && AWQ_IN((size_t)(a0 + a) * slot_elems + base, 104, (size_t)(REF ? G + 1 : G) * wn);
+        fq_quad<REF, GROUP>(w, SmemQuad{ss + a * kFqQuadF4, si + a * kFqQuadF4, slot}, q,
+                            op + (size_t)(a0 + a) * slot_elems + base, store);
       }
     }
   }
@@ -457,25 +479,82 @@ cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, c
 // ("What is AWQ Quantization? ...", "INT4 Weight Packing & Export"), one fp16
 // scale ("AWQ (Activation-Aware Weight Quantization) - AI Glossary", memory
 // example) and one fp16 zero per group. Same layout as the fake-quant
-// kernel: a block owns a 512-channel strip and a row range, a warp one row at
-// a time, 8 lanes per 128-channel block with channels [8l, 8l+8) and
-// [64+8l, 64+8l+8), so lane l's two code words are words l and 8+l of its
-// block and every 4-byte store instruction of a warp fills four whole 32-byte
-// sectors. The
-// lane's 16 scales are loaded once per block; the next row's weights load
-// while the current row is quantised.
+// kernel: a block owns a 512-channel strip and a row range, a warp two rows
+// at a time (one per half-warp) in the quad layout, so a lane's run j of 8
+// channels is one 4-bit code word (words 16 block + 4 j + quarter of the
+// strip's row) and the 4 lanes of a quad write 16 contiguous bytes per
+// store instruction. The lane's 32 scales are loaded once per block; the
+// next row pair's weights load while the current pair is quantised.
 
 constexpr int kPackWarps = 8;
-// resident blocks per SM: fp32 weights, and two groups per lane, need more
-// registers than the 80 of three blocks
+// resident blocks per SM for bf16 weights in groups of 128 (build-time tunable); fp32 weights, and several
+// groups per lane, need more registers and run 2
+#ifndef AWQ_PACK_BLOCKS_PER_SM
+#define AWQ_PACK_BLOCKS_PER_SM 3
+#endif
 template <typename WT, int GROUP>
-constexpr int pack_blocks_per_sm() { return (sizeof(WT) == 2 && GROUP == 128) ? 3 : 2; }
+constexpr int pack_blocks_per_sm() { return (sizeof(WT) == 2 && GROUP == 128) ? AWQ_PACK_BLOCKS_PER_SM : 2; }
+
+// Code word(s) of one run of 8 codes k + z (k = q - z as fp32 pairs, exact small integers).
+// BITS 4: one word, q_0 + 16 q_1 + ... + 16^7 q_7, built as two 16-bit halves
+// (q_0 + 256 q_2) + 16 (q_1 + 256 q_3): every step is exact in fp32 (each half
+// < 2^16), and 2^23 + half carries the half in its low mantissa bits, so one
+// byte permute joins the halves without a float-to-integer conversion or a
+// shift per code. BITS 8: two words of 4 codes; BITS 2: the low 16 bits of a
+// word (the run's 8 codes), joined with the next run's by the caller.
+template <int BITS>
+__device__ __forceinline__ void run_words(const float2 (&k)[4], float z, uint32_t (&wd)[2]) {
+  const float2 zz = make_float2(z, z);
+  float2 qf[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) qf[i] = __fadd2_rn(k[i], zz);
+  if constexpr (BITS == 4) {
+    const float2 c256 = make_float2(256.0f, 256.0f);
+    const float2 p0 = __ffma2_rn(qf[1], c256, qf[0]), p1 = __ffma2_rn(qf[3], c256, qf[2]);
+    const float h0 = __fmaf_rn(p0.y, 16.0f, __fadd_rn(p0.x, 8388608.0f));
+    const float h1 = __fmaf_rn(p1.y, 16.0f, __fadd_rn(p1.x, 8388608.0f));
+    wd[0] = __byte_perm(__float_as_uint(h0), __float_as_uint(h1), 0x5410);
+    wd[1] = 0u;
+  } else {
+    // 2^23 + q carries q in its low mantissa bits
+    constexpr uint32_t kMask = (1u << BITS) - 1u;
+    wd[0] = 0u;
+    wd[1] = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = __fadd2_rn(qf[i], make_float2(8388608.0f, 8388608.0f));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = 2 * i + h;
+        const uint32_t code = __float_as_uint(h ? a.y : a.x) & kMask;
+        wd[(e * BITS) >> 5] |= code << ((e * BITS) & 31);
+      }
+    }
+  }
+}
+
+// The 8 weights of one run as fp32 pairs (bf16 or fp32 storage).
+__device__ __forceinline__ void load_run(const uint16_t* p, float2 (&w)[4]) {
+  const uint4 r = *reinterpret_cast<const uint4*>(p);
+  const uint32_t x[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = make_float2(bf16_lo(x[i]), bf16_hi(x[i]));
+}
+__device__ __forceinline__ void load_run(const float* p, float2 (&w)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  w[0] = make_float2(a.x, a.y);
+  w[1] = make_float2(a.z, a.w);
+  w[2] = make_float2(b.x, b.y);
+  w[3] = make_float2(b.z, b.w);
+}
 
 template <typename WT, int GROUP, int BITS>
 __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>())
     pack_kernel(const WT* __restrict__ W, int N, int K, const float* __restrict__ s, float qmax, float floor_,
                 int symmetric, int32_t* __restrict__ qweight, uint16_t* __restrict__ scales,
                 uint16_t* __restrict__ zeros, int nstrips, int rows_per_block) {
+  constexpr int NG = quad_groups<GROUP>(), RUNS = 4 / NG;  // groups per lane, runs per group
   const int strip = blockIdx.x % nstrips;
   const int col0 = strip * kFqCols;
   const int ncols = min(kFqCols, K - col0);
@@ -483,112 +562,85 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>
   const int r_end = min(N, r_begin + rows_per_block);
   if (r_begin >= r_end) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = lane >> 3, sub = lane & 7;
-  const bool active = grp * 128 < ncols;  // blocks past a partial strip repeat block 0 and store nothing
-  const int c_lo = (active ? grp * 128 : 0) + sub * 8;
-  // the lane stores the scale and zero of each group whose first channel it
-  // holds: run A's group when its run starts one, and (for groups under 128)
-  // run B's group, 64 channels further on
-  const bool lead = (sub % (GROUP / 8 < 8 ? GROUP / 8 : 8)) == 0;
-  float2 sv[8];
-  {
-    float t[16] = {};
-    if (AWQ_IN(col0 + c_lo, 72, K)) {
-      load8f(s + col0 + c_lo, t);
-      load8f(s + col0 + c_lo + 64, t + 8);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sv[i] = make_float2(t[2 * i], t[2 * i + 1]);
+  const int hw = lane >> 4, blk = (lane >> 2) & 3, quarter = lane & 3;
+  const bool active = blk * 128 < ncols;  // blocks past a partial strip repeat block 0 and store nothing
+  const int c_lo = (active ? blk * 128 : 0) + 8 * quarter;  // runs at c_lo + 32 j within the strip
+  const QuantSpec q = make_quant_spec(qmax, floor_, symmetric != 0);
+  // the strip's scales in shared memory, in the order the lanes read them (as the fake-quant kernel stages
+  // one alpha); registers hold the weights in flight instead
+  __shared__ float4 s_sm[kFqQuadF4];
+  for (int i = threadIdx.x; i < kFqQuadF4; i += blockDim.x) {
+    const int c = 4 * i, b = c >> 7, e = c & 127;
+    const int idx = ((e >> 5) * 2 + ((e & 7) >> 2)) * 16 + b * 4 + ((e & 31) >> 3);
+    s_sm[idx] = c < ncols && AWQ_IN(col0 + c, 4, K) ? *reinterpret_cast<const float4*>(s + col0 + c)
+                                                    : make_float4(1.f, 1.f, 1.f, 1.f);
   }
+  __syncthreads();
+  const int slot = (active ? blk : 0) * 4 + quarter;
   const int kw = K * BITS / 32, kg = K / GROUP;  // code words and groups per row
   [[maybe_unused]] const size_t wn = (size_t)N * K;  // elements of W (bounds checks)
-  int row = r_begin + warp;
-  RowRegs<WT> nxt{};
-  if (row < r_end && AWQ_IN((size_t)row * K + col0 + c_lo, 72, wn)) nxt.load(W + (size_t)row * K + col0 + c_lo);
-  for (; row < r_end; row += kPackWarps) {
-    float2 w[8];
-    nxt.unpack(w);
-    if (row + kPackWarps < r_end && AWQ_IN((size_t)(row + kPackWarps) * K + col0 + c_lo, 72, wn))
-      nxt.load(W + (size_t)(row + kPackWarps) * K + col0 + c_lo);
-    float2 v[8];
+  const int pair_step = 2 * kPackWarps;
+  int first = r_begin + 2 * warp;
+  QuadRow<WT> nxt;
+  nxt.zero();
+  if (first + hw < r_end && AWQ_IN((size_t)(first + hw) * K + col0 + c_lo, 104, wn))
+    nxt.load(W + (size_t)(first + hw) * K + col0 + c_lo);
+  for (; first < r_end; first += pair_step) {
+    const int row = first + hw;
+    const bool live = row < r_end && active;
+    float2 v[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __fmul2_rn(w[i], sv[i]);
-    GroupFast ga, gb;
-    lane_groups<GROUP>(v, qmax, floor_, symmetric != 0, ga, gb);
-    float2 k[8];
-    lane_codes_minus_z<GROUP>(v, ga, gb, k);
-    uint32_t wa[2] = {0u, 0u}, wb[2] = {0u, 0u};  // run A's and run B's words
-    if constexpr (BITS == 4) {
-      // q = (q - z) + z, exact integers in [0, 15]. A run of 8 codes is one word q_0 + 16 q_1 + ... + 16^7 q_7
-      // (column order), built as two 16-bit halves h = (q_0 + 256 q_2) + 16 (q_1 + 256 q_3): every step is
-      // exact in fp32 (h < 2^16), and 2^23 + h carries h in its low mantissa bits, so one byte permute joins
-      // the two halves without a float-to-integer conversion or a shift per code
-      const float2 za = make_float2(ga.z, ga.z), zb = make_float2(gb.z, gb.z);
-      const float2 c256 = make_float2(256.0f, 256.0f);
-      float2 qa4[4], qb4[4];
+    for (int j = 0; j < 4; ++j) {
+      float2 w4[4], sv[4];
+      nxt.unpack_run(j, w4);
+      SmemQuad::get(s_sm, slot, j, sv);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        qa4[i] = __fadd2_rn(k[i], za);
-        qb4[i] = __fadd2_rn(k[4 + i], zb);
-      }
-      const float2 pa0 = __ffma2_rn(qa4[1], c256, qa4[0]), pa1 = __ffma2_rn(qa4[3], c256, qa4[2]);
-      const float2 pb0 = __ffma2_rn(qb4[1], c256, qb4[0]), pb1 = __ffma2_rn(qb4[3], c256, qb4[2]);
-      const float ha0 = __fmaf_rn(pa0.y, 16.0f, __fadd_rn(pa0.x, 8388608.0f));
-      const float ha1 = __fmaf_rn(pa1.y, 16.0f, __fadd_rn(pa1.x, 8388608.0f));
-      const float hb0 = __fmaf_rn(pb0.y, 16.0f, __fadd_rn(pb0.x, 8388608.0f));
-      const float hb1 = __fmaf_rn(pb1.y, 16.0f, __fadd_rn(pb1.x, 8388608.0f));
-      wa[0] = __byte_perm(__float_as_uint(ha0), __float_as_uint(ha1), 0x5410);
-      wb[0] = __byte_perm(__float_as_uint(hb0), __float_as_uint(hb1), 0x5410);
-    } else {
-      // q = (q - z) + z in [0, 2^b - 1]; 2^23 + q carries q in its low mantissa
-      // bits, which avoids a float-to-integer conversion per code
-      const float2 za = make_float2(8388608.0f + ga.z, 8388608.0f + ga.z);
-      const float2 zb = make_float2(8388608.0f + gb.z, 8388608.0f + gb.z);
-      constexpr uint32_t kMask = (1u << BITS) - 1u;
-      uint32_t qa[8], qb[8];  // the codes of run A and run B
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 a = __fadd2_rn(k[i], za);
-        const float2 b = __fadd2_rn(k[4 + i], zb);
-        qa[2 * i] = __float_as_uint(a.x) & kMask;
-        qa[2 * i + 1] = __float_as_uint(a.y) & kMask;
-        qb[2 * i] = __float_as_uint(b.x) & kMask;
-        qb[2 * i + 1] = __float_as_uint(b.y) & kMask;
-      }
-      // words of 32 / BITS codes, column (32/b) j + k in bits [b k, b k + b) of word j: a run of 8 codes is
-      // two words (8 bits) or half a word (2 bits, joined with the next lane's half)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int word = (e * BITS) >> 5, bit = (e * BITS) & 31;
-        wa[word] |= qa[e] << bit;
-        wb[word] |= qb[e] << bit;
-      }
-      if (BITS == 2) {  // the odd lane's 16 bits go above the even lane's (8 channels further on)
-        wa[0] |= __shfl_down_sync(0xffffffffu, wa[0], 1) << 16;
-        wb[0] |= __shfl_down_sync(0xffffffffu, wb[0], 1) << 16;
-      }
+      for (int i = 0; i < 4; ++i) v[4 * j + i] = __fmul2_rn(w4[i], sv[i]);
     }
-    const size_t w_at = (size_t)row * kw + (size_t)(col0 + c_lo) * BITS / 32;  // run A's first word
-    constexpr int kRunB = 64 * BITS / 32;                                      // words from run A to run B
-    if (active && AWQ_IN(w_at, kRunB + (BITS == 8 ? 2 : 1), (size_t)N * kw)) {
-      int32_t* q = qweight + w_at;
-      if (BITS == 4) {
-        q[0] = (int32_t)wa[0];
-        q[kRunB] = (int32_t)wb[0];
-      } else if (BITS == 8) {
-        *reinterpret_cast<int2*>(q) = make_int2((int)wa[0], (int)wa[1]);
-        *reinterpret_cast<int2*>(q + kRunB) = make_int2((int)wb[0], (int)wb[1]);
-      } else if ((sub & 1) == 0) {
-        q[0] = (int32_t)wa[0];
-        q[kRunB] = (int32_t)wb[0];
+    if (row + pair_step < r_end && AWQ_IN((size_t)(row + pair_step) * K + col0 + c_lo, 104, wn))
+      nxt.load(W + (size_t)(row + pair_step) * K + col0 + c_lo);
+    GroupFast g[NG];
+    quad_group_params<GROUP>(v, q, g);
+    // codes in place; a group redone by division reads its weights again (rare). A half-warp past the last
+    // row (an odd row count) computes on stale values and stores nothing; it re-reads a valid row.
+    const WT* wrow = W + (size_t)(row < r_end ? row : r_begin) * K + col0 + c_lo;
+    quad_codes<GROUP>(v, g, [&](int j, float2 (&v4)[4]) {
+      float2 w8[4] = {}, sv[4];
+      if (AWQ_IN((wrow - W) + 32 * j, 8, wn)) load_run(wrow + 32 * j, w8);
+      SmemQuad::get(s_sm, slot, j, sv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v4[i] = __fmul2_rn(w8[i], sv[i]);
+    });
+    uint32_t words[4][2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 k4[4] = {v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]};
+      run_words<BITS>(k4, g[j / RUNS].z, words[j]);
+    }
+    if (BITS == 2) {  // the odd quarter's 16 bits go above the even quarter's (8 channels further on)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) words[j][0] |= __shfl_down_sync(0xffffffffu, words[j][0], 1) << 16;
+    }
+    if (live) {
+      const size_t w_row = (size_t)row * kw + (size_t)(col0 + c_lo) * BITS / 32;  // run 0's first word
+      constexpr int kRunWords = 32 * BITS / 32;                                   // words from run j to j + 1
+      if (AWQ_IN(w_row, 3 * kRunWords + (BITS == 8 ? 2 : 1), (size_t)N * kw)) {
+        int32_t* dst = qweight + w_row;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (BITS == 8)
+            *reinterpret_cast<int2*>(dst + j * kRunWords) = make_int2((int)words[j][0], (int)words[j][1]);
+          else if (BITS == 4 || (quarter & 1) == 0)
+            dst[j * kRunWords] = (int32_t)words[j][0];
+        }
       }
-      const size_t gi = (size_t)row * kg + (col0 + c_lo) / GROUP;
-      if (lead && AWQ_IN(gi, GROUP < 128 ? 64 / GROUP + 1 : 1, (size_t)N * kg)) {
-        scales[gi] = __half_as_ushort(__float2half_rn(ga.delta));
-        zeros[gi] = __half_as_ushort(__float2half_rn(ga.z));
-        if (GROUP < 128) {
-          scales[gi + 64 / GROUP] = __half_as_ushort(__float2half_rn(gb.delta));
-          zeros[gi + 64 / GROUP] = __half_as_ushort(__float2half_rn(gb.z));
+      // the quarter holding each group's first channel stores its fp16 step and zero
+      const size_t gi0 = (size_t)row * kg + (col0 + c_lo) / GROUP;
+      if (quarter == 0 && AWQ_IN(gi0, NG, (size_t)N * kg)) {
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+          scales[gi0 + gi] = __half_as_ushort(__float2half_rn(g[gi].delta));
+          zeros[gi0 + gi] = __half_as_ushort(__float2half_rn(g[gi].z));
         }
       }
     }

@@ -30,14 +30,18 @@ cudaError_t sm_count(int* sms);
 cudaError_t ensure_dynamic_smem(const void* func, int bytes);
 
 inline int stats_strips(int64_t in) { return (int)((in + 255) / 256); }
-// Tokens per statistics chunk: n_tok * strips / kStatsTargetBlocks, rounded
-// up to a multiple of kStatsRowQuantum (at least one quantum).
+// Tokens per statistics chunk: the token range split into
+// kStatsTargetBlocks / strips chunks (at least one), each rounded up to a
+// multiple of kStatsRowQuantum, so that strips x chunks stays within
+// kStatsTargetBlocks whenever there are fewer strips than that.
 inline int64_t stats_chunk_rows(int64_t n_tok, int64_t in) {
-  const int64_t per = (n_tok * stats_strips(in) + kStatsTargetBlocks - 1) / kStatsTargetBlocks;
+  const int64_t strips = stats_strips(in);
+  const int64_t target = strips < kStatsTargetBlocks ? kStatsTargetBlocks / strips : 1;
+  const int64_t per = (n_tok + target - 1) / target;
   const int64_t q = (per + kStatsRowQuantum - 1) / kStatsRowQuantum * kStatsRowQuantum;
   return q < kStatsRowQuantum ? kStatsRowQuantum : q;
 }
-// Chunks of the token range: at most kStatsTargetBlocks / strips + 1.
+// Chunks of the token range: at most max(1, kStatsTargetBlocks / strips).
 inline int stats_chunks(int64_t n_tok, int64_t in) {
   const int64_t r = stats_chunk_rows(n_tok, in);
   return (int)((n_tok + r - 1) / r);

@@ -41,7 +41,17 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
-constexpr int kRasterTokenTiles = 16;  // token tiles per raster band
+// Token tiles per raster band (build-time tunables): the CTA-pair kernels
+// (burst-length searches) and the single-CTA kernel (searches long enough to
+// run at the power limit, where every DRAM byte costs energy).
+#ifndef AWQ_RASTER_TILES_PAIR
+#define AWQ_RASTER_TILES_PAIR 16
+#endif
+#ifndef AWQ_RASTER_TILES_SINGLE
+#define AWQ_RASTER_TILES_SINGLE 16
+#endif
+constexpr int kRasterTokenTilesPair = AWQ_RASTER_TILES_PAIR;
+constexpr int kRasterTokenTilesSingle = AWQ_RASTER_TILES_SINGLE;
 constexpr int NUM_THREADS = 192;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
@@ -479,6 +489,7 @@ __device__ __forceinline__ void ldg_w16(const void* W, int w_bf16, size_t off, f
 template <int GROUP>
 __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane) {
   const int grp = lane >> 3, sub = lane & 7;
+  const QuantSpec qs = make_quant_spec(p.qmax, p.floor_, p.symmetric != 0);
   const int per_a = p.nt * p.nstrips;
   const int units = p.G * per_a;
   const size_t slot = (size_t)p.N * p.K;
@@ -513,7 +524,7 @@ __device__ __forceinline__ void quantise_units(const Params& p, int fw, int lane
         if (r + 1 < r1 && AWQ_IN((size_t)(r + 1) * p.K + c, 72, wn_elems))
           ldg_w16(p.W, p.w_bf16, (size_t)(r + 1) * p.K + c, wn);
         uint32_t o[8];
-        fq_lane16<false, GROUP>(w, nw, RegLane{sv, iv}, p.qmax, p.floor_, p.symmetric != 0, o);
+        fq_lane16<false, GROUP>(w, nw, RegLane{sv, iv}, qs, o);
         if (active && AWQ_IN((size_t)a * slot + (size_t)r * p.K + c, 72, (size_t)p.G * slot)) {
           uint4* dst = reinterpret_cast<uint4*>(p.op + (size_t)a * slot + (size_t)r * p.K + c);
           dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -839,11 +850,11 @@ cudaError_t setup_search(const uint16_t* X, int64_t n_tok, int64_t K, const uint
   p.kb = (int)(K / BK);
   p.G = G;
   p.items = ref ? p.mt * p.nt : G * p.mtg * p.nt;
-  // L2 raster: bands of kRasterTokenTiles token tiles stay in L2 while the
-  // operand tiles sweep past them (measured best among band sizes and
-  // orientations on the layer shapes of the benchmark suite).
+  // L2 raster: bands of token tiles stay in L2 while the operand tiles sweep
+  // past them, so each operand tile is read from DRAM once per band.
   p.raster_n = 0;
-  p.raster_group = (kRasterTokenTiles + CM - 1) / CM;
+  const int band = CM == 2 ? kRasterTokenTilesPair : kRasterTokenTilesSingle;
+  p.raster_group = (band + CM - 1) / CM;
   if (p.raster_group > p.mtg) p.raster_group = p.mtg;
   const uint32_t ms = cfg.wait_timeout_ms ? cfg.wait_timeout_ms : 2000u;
   p.timeout_ns = (uint64_t)ms * 1000000ull;
