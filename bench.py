@@ -205,10 +205,12 @@ def reference_arm(args, rank):
 # ------------------------------------------------------------------ GPU arm
 
 
-def timed(fn, flush, reps):
-    """Median CUDA-event time (ms) of fn() over reps runs, L2 flushed before each."""
+def timed(fn, flush, reps, warm=0):
+    """Median CUDA-event time (ms) of fn() over reps runs, L2 flushed before each, after `warm` untimed runs."""
     import torch
 
+    for _ in range(warm):
+        fn()
     ts = []
     for _ in range(reps):
         flush.zero_()
@@ -343,7 +345,9 @@ def stage_kernels(R, flush, reps):
     for nm, fn in calls.items():
         fn()
         torch.cuda.synchronize()
-        out[nm] = timed(fn, flush, reps)
+        short = nm not in ("search_gemm", "fused_search")
+        # the short kernels: a few untimed launches bring the clock up from idle, then the median of many
+        out[nm] = timed(fn, flush, max(reps, 15) if short else reps, warm=5 if short else 0)
     if int(status[0]) != 0:
         raise RuntimeError("device status " + capi.status_string(int(status[0])))
     del op

@@ -483,10 +483,22 @@ cudaError_t launch_fakequant(const void* W, int w_dtype, int64_t N, int64_t K, c
 // at a time (one per half-warp) in the quad layout, so a lane's run j of 8
 // channels is one 4-bit code word (words 16 block + 4 j + quarter of the
 // strip's row) and the 4 lanes of a quad write 16 contiguous bytes per
-// store instruction. The lane's 32 scales are loaded once per block; the
-// next row pair's weights load while the current pair is quantised.
+// store instruction. The strip's scales are staged in shared memory once
+// per block. The weights go through a per-warp ring of kPackStages row pairs
+// in shared memory, filled by per-thread asynchronous copies: each lane
+// copies the 4 runs it will read, so no lane waits on another, and two row
+// pairs are in flight while the third is quantised (the arithmetic takes
+// about a third of the issue slots, so the bytes in flight set the speed).
 
 constexpr int kPackWarps = 8;
+#ifndef AWQ_PACK_STAGES
+#define AWQ_PACK_STAGES 3
+#endif
+constexpr int kPackStages = AWQ_PACK_STAGES;  // row pairs per warp in the shared-memory ring (build-time tunable)
+template <typename WT>
+constexpr int pack_pieces() { return 4 * (int)sizeof(WT) / 2; }  // 16-byte pieces of a lane's 32 weights
+template <typename WT>
+constexpr int pack_ring_bytes() { return kPackWarps * kPackStages * pack_pieces<WT>() * 32 * 16; }
 // resident blocks per SM for bf16 weights in groups of 128 (build-time tunable); fp32 weights, and several
 // groups per lane, need more registers and run 2
 #ifndef AWQ_PACK_BLOCKS_PER_SM
@@ -580,36 +592,68 @@ __global__ void __launch_bounds__(kPackWarps * 32, pack_blocks_per_sm<WT, GROUP>
   const int kw = K * BITS / 32, kg = K / GROUP;  // code words and groups per row
   [[maybe_unused]] const size_t wn = (size_t)N * K;  // elements of W (bounds checks)
   const int pair_step = 2 * kPackWarps;
-  int first = r_begin + 2 * warp;
-  QuadRow<WT> nxt;
-  nxt.zero();
-  if (first + hw < r_end && AWQ_IN((size_t)(first + hw) * K + col0 + c_lo, 104, wn))
-    nxt.load(W + (size_t)(first + hw) * K + col0 + c_lo);
-  for (; first < r_end; first += pair_step) {
-    const int row = first + hw;
+  // the warp's ring (dynamic shared memory): [stage][16-byte piece][lane] (a lane's 4 runs are 4 pieces of
+  // bf16, 8 of fp32)
+  constexpr int kPieces = pack_pieces<WT>();
+  extern __shared__ uint4 pack_ring[];
+  uint4* ring = pack_ring + (size_t)warp * kPackStages * kPieces * 32 + lane;
+  // copy the lane's runs of row pair `it` into its stage (zeros past the last row)
+  auto fetch = [&](int it) {
+    const int row = r_begin + 2 * warp + it * pair_step + hw;
+    uint4* dst = ring + (it % kPackStages) * kPieces * 32;
+    if (row < r_end && AWQ_IN((size_t)row * K + col0 + c_lo, 104, wn)) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(W + (size_t)row * K + col0 + c_lo);
+#pragma unroll
+      for (int pc = 0; pc < kPieces; ++pc)
+        cp_async16(dst + pc * 32, src + (pc / (kPieces / 4)) * 32 * sizeof(WT) + (pc % (kPieces / 4)) * 16);
+    } else {
+#pragma unroll
+      for (int pc = 0; pc < kPieces; ++pc) dst[pc * 32] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_commit();
+  };
+  // run j's 4 pairs of weights from the stage of row pair `it`
+  auto run_of = [&](int it, int j, float2 (&w4)[4]) {
+    const uint4* src = ring + (it % kPackStages) * kPieces * 32;
+    if constexpr (sizeof(WT) == 2) {
+      const uint4 r = src[j * 32];
+      const uint32_t x[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w4[i] = make_float2(bf16_lo(x[i]), bf16_hi(x[i]));
+    } else {
+      const uint4 a = src[(2 * j) * 32], b = src[(2 * j + 1) * 32];
+      w4[0] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
+      w4[1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
+      w4[2] = make_float2(__uint_as_float(b.x), __uint_as_float(b.y));
+      w4[3] = make_float2(__uint_as_float(b.z), __uint_as_float(b.w));
+    }
+  };
+  const int npairs = (r_end - r_begin - 2 * warp + pair_step - 1) / pair_step;  // this warp's row pairs
+#pragma unroll
+  for (int it = 0; it < kPackStages - 1; ++it) fetch(it);
+  for (int it = 0; it < npairs; ++it) {
+    cp_async_wait<kPackStages - 2>();  // row pair `it` has landed (this lane's copies)
+    fetch(it + kPackStages - 1);       // into the stage row pair it - 1 used
+    const int row = r_begin + 2 * warp + it * pair_step + hw;
     const bool live = row < r_end && active;
     float2 v[16];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float2 w4[4], sv[4];
-      nxt.unpack_run(j, w4);
+      run_of(it, j, w4);
       SmemQuad::get(s_sm, slot, j, sv);
 #pragma unroll
       for (int i = 0; i < 4; ++i) v[4 * j + i] = __fmul2_rn(w4[i], sv[i]);
     }
-    if (row + pair_step < r_end && AWQ_IN((size_t)(row + pair_step) * K + col0 + c_lo, 104, wn))
-      nxt.load(W + (size_t)(row + pair_step) * K + col0 + c_lo);
     GroupFast g[NG];
     quad_group_params<GROUP>(v, q, g);
-    // codes in place; a group redone by division reads its weights again (rare). A half-warp past the last
-    // row (an odd row count) computes on stale values and stores nothing; it re-reads a valid row.
-    const WT* wrow = W + (size_t)(row < r_end ? row : r_begin) * K + col0 + c_lo;
+    // codes in place; a group redone by division (rare) forms its values again from the stage
     quad_codes<GROUP>(v, g, [&](int j, float2 (&v4)[4]) {
-      float2 w8[4] = {}, sv[4];
-      if (AWQ_IN((wrow - W) + 32 * j, 8, wn)) load_run(wrow + 32 * j, w8);
+      float2 w4[4], sv[4];
+      run_of(it, j, w4);
       SmemQuad::get(s_sm, slot, j, sv);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v4[i] = __fmul2_rn(w8[i], sv[i]);
+      for (int i = 0; i < 4; ++i) v4[i] = __fmul2_rn(w4[i], sv[i]);
     });
     uint32_t words[4][2];
 #pragma unroll
@@ -660,7 +704,9 @@ cudaError_t launch_pack_t(const WT* W, int64_t N, int64_t K, const float* s, con
   const int rows_per_block = (int)((N + rblocks - 1) / rblocks);
   rblocks = (N + rows_per_block - 1) / rows_per_block;
   const float qmax = (float)((1 << cfg.w_bit) - 1);
-  pack_kernel<WT, GROUP, BITS><<<(unsigned)(rblocks * nstrips), kPackWarps * 32, 0, st>>>(
+  e = ensure_dynamic_smem((const void*)pack_kernel<WT, GROUP, BITS>, pack_ring_bytes<WT>());
+  if (e != cudaSuccess) return e;
+  pack_kernel<WT, GROUP, BITS><<<(unsigned)(rblocks * nstrips), kPackWarps * 32, pack_ring_bytes<WT>(), st>>>(
       W, (int)N, (int)K, s, qmax, cfg.delta_floor, cfg.zero_point == 0 ? 1 : 0, qweight, scales, zeros, nstrips,
       rows_per_block);
   return cudaGetLastError();
