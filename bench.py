@@ -412,39 +412,46 @@ def side_workload(name, dev, flush, pk, reps):
 
 
 def decode_line(R, dev, flush, pk, reps):
-    """awq_w4a16_gemv on the packed layer of the step, one token: enough copies of the layer to exceed L2,
-    applied one after another (a decode step running through layers), L2 flushed before each pass."""
+    """awq_w4a16_gemv on the packed layer of the step, for one and for four tokens: enough copies of the layer
+    to exceed L2, applied one after another (a decode step running through layers), L2 flushed before each
+    pass."""
     import torch
 
     from post_bit_weight_awq_b300 import capi
 
     N, K = R.N, R.K
-    if K > capi.AWQ_W4A16_MAX_TOKEN_CHANNELS:
-        return None
     layer_bytes = N * K // 2 + 2 * 2 * N * (K // 128)
     copies = max(3, int((256 << 20) // layer_bytes) + 1)
     packs = [(R.qw.clone(), R.sc.clone(), R.zr.clone()) for _ in range(copies)]
-    xg = torch.randn(1, K, device=dev).to(torch.bfloat16)
-    yg = torch.empty(1, N, dtype=torch.float32, device=dev)
+    out = {"layer": [N, K], "tokens": {},
+           "timing": f"{copies} distinct copies per CUDA graph (> L2), L2 flushed before each graph"}
+    for M in (1, 4):
+        if M * K > capi.AWQ_W4A16_MAX_TOKEN_CHANNELS:
+            continue
+        xg = torch.randn(M, K, device=dev).to(torch.bfloat16)
+        yg = torch.empty(M, N, dtype=torch.float32, device=dev)
 
-    def one_pass():
-        for q_, s_, z_ in packs:
-            capi.awq_w4a16_gemv(xg, q_, s_, z_, R.cfg, yg)
+        def one_pass():
+            for q_, s_, z_ in packs:
+                capi.awq_w4a16_gemv(xg, q_, s_, z_, R.cfg, yg)
 
-    one_pass()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
         one_pass()
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
-    ms = timed(g.replay, flush, reps) / copies
-    gbytes = layer_bytes + K * 2 + N * 4
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            one_pass()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ms = timed(g.replay, flush, reps) / copies
+        gbytes = layer_bytes + 2 * M * K + 4 * M * N
+        # groups of 128: the tensor-core kernel for two or more tokens and for one token on 2^27 weights or more
+        kernel = "w4a16_mma_kernel" if (M >= 2 or N * K >= 1 << 27) else f"w4a16_gemv_kernel<{M}, R>"
+        out["tokens"][str(M)] = {"kernel": kernel, "ms_per_layer": round(ms, 5), "bytes_per_layer": gbytes,
+                                 "gbs": round(gbytes / (ms * 1e-3) / 1e9, 1),
+                                 "frac_hbm": round(gbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3)}
+        del g
     del packs
-    return {"kernel": "w4a16_gemv_kernel<1, R>", "tokens": 1, "layer": [N, K], "ms_per_layer": round(ms, 5),
-            "bytes_per_layer": gbytes, "gbs": round(gbytes / (ms * 1e-3) / 1e9, 1),
-            "frac_hbm": round(gbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
-            "timing": f"{copies} distinct copies per CUDA graph (> L2), L2 flushed before each graph"}
+    return out if out["tokens"] else None
 
 
 def prefill_line(R, dev, flush, pk, reps):

@@ -318,8 +318,9 @@ AWQ_API awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count
 /* ---------------------------------------------------------------- using the packed layer */
 
 /* Largest token count, and token count times `in`, that awq_w4a16_gemv
-   accepts (the tokens' activations are staged in shared memory as fp32,
-   4.5 bytes per value with the bank padding). */
+   accepts (the tokens' activations are staged in one block's shared memory:
+   as fp32 for groups of 32 and 64, 4.5 bytes per value with the bank
+   padding; as bf16 pairs for groups of 128, 2.5 bytes per value). */
 #define AWQ_W4A16_MAX_TOKENS 8
 #define AWQ_W4A16_MAX_TOKEN_CHANNELS (44 * 1024)
 
@@ -334,8 +335,14 @@ AWQ_API awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count
    AWQ_W4A16_MAX_TOKENS and n_tok * in <= AWQ_W4A16_MAX_TOKEN_CHANNELS,
    else AWQ_ERR_UNSUPPORTED. qweight/scales_f16/zeros_f16: as
    awq_quantize_pack (qweight 16-byte aligned). y: device fp32 [n_tok][out].
-   Each code is read once from memory; products and sums in fp32 (exact
-   dequantised weights, fp32 fused multiply-adds in a fixed order). */
+   Each code is read once from memory, and every (q - z) is exact. Groups of
+   32 and 64: fp32 products and fused multiply-adds in a fixed order. Groups
+   of 128: tensor-core products of bf16 x with the exact (q - z), summed in
+   fp32 per group, then scaled by the group's step in fp32 (for two or more
+   tokens, and for one token on a layer of at least 2^27 weights; smaller
+   single-token layers take the fp32 path). The order of every sum is fixed
+   by the shapes and the device's SM count: repeated calls give the same
+   bits. */
 AWQ_API awq_status awq_w4a16_gemv(const void* x, int32_t x_dtype, int64_t n_tok, int64_t in,
                                   const int32_t* qweight, const uint16_t* scales_f16, const uint16_t* zeros_f16,
                                   int64_t out, const awq_config* cfg, float* y, awq_stream_t stream);

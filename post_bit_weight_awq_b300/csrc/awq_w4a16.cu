@@ -18,6 +18,7 @@
 // row.
 #include <cuda_fp16.h>
 
+#include "awq.h"
 #include "awq_device.cuh"
 #include "awq_launch.h"
 
@@ -185,6 +186,313 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   }
 }
 
+// ------------------------------------------------------------ decode on the tensor cores (groups of 128)
+//
+// The same product for groups of 128 with mma.sync (bf16 in, fp32
+// accumulate; m16n8k16): a warp computes 16 output rows for all M <= 8
+// tokens (the 8 columns of the MMA). Inside each group of 128 channels the
+// order of k is permuted, the same way for the weights (A) and the
+// activations (B), which leaves the dot product unchanged: thread quarter c
+// of the MMA takes the group's channels 32 c .. 32 c + 31, i.e. 16 bytes of
+// each of its two rows, and step kb = 2 m + h of the group pairs the codes
+// (n_2h, n_2h+4) and (n_2h+1, n_2h+5) of word m. So
+// (w >> 4j) & 0x000F000F | 0x43004300 is the bf16 pair (128 + n_j,
+// 128 + n_j+4) in one mask-and-or, and one packed bf16 subtraction of
+// 128 + z gives (q - z) exactly (small integers are exact in bf16). x is
+// staged in shared memory once per block in the matching order: word j of
+// each 8 consecutive channels holds channels j and j + 4, so one 16-byte load
+// of x gives one 16-byte chunk of the staged words. Each (group, quarter) row
+// of 16 words is padded to 20, so the four quarters' reads of one token fall
+// in distinct banks. The MMA
+// adds exact products in fp32; after the group's 8 steps the partial is
+// scaled by the group's fp16 step and added to one of four running sums
+// (group index mod 4), which are added at the end: every operation on the
+// way keeps the error within a few dozen fp32 roundings of sum |x| |w|.
+// A zero point outside [-128, 127] (never produced for groups that contain
+// both signs) is split as z = z_lo + 256 k, and the group takes one more MMA
+// with the constant -256 k.
+//
+// The codes stream through a per-warp ring of kMmaStages groups in shared
+// memory, filled by per-thread asynchronous copies (each thread copies the
+// 16 bytes of each of its two rows that it reads itself, so no thread waits
+// on another). Rows past the layer's end are not copied: their sums land in
+// output rows that are never stored. Each lane of a quad also loads one of
+// its rows' steps or zeros for the same group, turns it into what the MMA
+// side needs (the step as fp32, the zero as the bf16 pair 128 + z_lo) and
+// shares it within the quad by shuffles.
+//
+// Work split: one block per SM owns a contiguous run of row tiles, and its
+// (tile, group) steps are cut into kMmaWarps equal contiguous ranges, one per
+// warp, so every SM and every warp has the same number of groups to within
+// one tile per block. A tile that lies inside one warp's range is written
+// directly; a tile cut between warps leaves partial sums in shared memory,
+// and the warp holding the tile's first group adds the later warps' partials
+// in warp order, so the result does not depend on timing.
+
+// Ring depth and warps per block (build-time tunables, defaults measured
+// best), whether groups of 128 take this kernel (1) or the fp32 one above (0),
+// and the layer size from which a single token takes it.
+#ifndef AWQ_DECODE_MMA
+#define AWQ_DECODE_MMA 1
+#endif
+#ifndef AWQ_MMA_STAGES
+#define AWQ_MMA_STAGES 6
+#endif
+#ifndef AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS
+#define AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS (int64_t(1) << 27)
+#endif
+#ifndef AWQ_MMA_WARPS
+#define AWQ_MMA_WARPS 16
+#endif
+constexpr int kMmaWarps = AWQ_MMA_WARPS;
+constexpr int kMmaThreads = kMmaWarps * 32;
+constexpr int kMmaStages = AWQ_MMA_STAGES;  // groups of codes per warp in the ring: kMmaStages - 1 in flight
+constexpr int kMmaQStride = 20;             // staged words per (token, group, quarter): 16 + 4 of padding
+constexpr int kMmaStageUnroll = 4;          // 16-byte loads of x in flight per thread while staging
+constexpr int kMmaRingBytes = kMmaWarps * kMmaStages * 2 * 32 * 16;
+constexpr int kMmaRedBytes = kMmaWarps * 2 * 4 * 32 * 4;  // per warp: a first and a last partial tile, 4 per lane
+
+// Words per token region: 16 more than a multiple of 32, so two tokens read in one phase meet distinct banks.
+__host__ __device__ constexpr int mma_token_words(int K) {
+  return (K / 128) * 4 * kMmaQStride + (((K / 128) & 1) ? 0 : 16);
+}
+// Every accepted (n_tok, in) fits one block's shared memory (227 KB): the staged x of n_tok * in channels
+// takes at most 2.5 bytes per channel plus 64 bytes per token.
+static_assert(kMmaRingBytes + kMmaRedBytes + AWQ_W4A16_MAX_TOKEN_CHANNELS / 128 * 4 * kMmaQStride * 4 +
+                      AWQ_W4A16_MAX_TOKENS * 16 * 4 <=
+                  227 * 1024,
+              "ring, partial sums and the largest staged x must fit one block's shared memory");
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (128 + n, 128 + n') as a bf16 pair from a word whose nibbles n, n' sit at bits 0 and 16, minus the pair zz.
+__device__ __forceinline__ uint32_t code_pair(uint32_t ws, uint32_t zz) {
+  const uint32_t p = (ws & 0x000F000Fu) | 0x43004300u;
+  const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&zz));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t bf16_pair_bits(float v) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(v, v);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Output rows ra, rb (= ra + 8) of tokens 2c, 2c + 1.
+__device__ __forceinline__ void mma_store(float* __restrict__ y, int M, int N, int ra, int c, const float (&out)[4]) {
+  const int rb = ra + 8, n0 = 2 * c, n1 = 2 * c + 1;
+  if (ra < N && n0 < M && AWQ_IN((size_t)n0 * N + ra, 1, (size_t)M * N)) y[(size_t)n0 * N + ra] = out[0];
+  if (ra < N && n1 < M && AWQ_IN((size_t)n1 * N + ra, 1, (size_t)M * N)) y[(size_t)n1 * N + ra] = out[1];
+  if (rb < N && n0 < M && AWQ_IN((size_t)n0 * N + rb, 1, (size_t)M * N)) y[(size_t)n0 * N + rb] = out[2];
+  if (rb < N && n1 < M && AWQ_IN((size_t)n1 * N + rb, 1, (size_t)M * N)) y[(size_t)n1 * N + rb] = out[3];
+}
+
+__global__ void __launch_bounds__(kMmaThreads, 1)
+    w4a16_mma_kernel(const uint16_t* __restrict__ x, int M, int K, const int32_t* __restrict__ qweight,
+                     const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros, int N, float* __restrict__ y) {
+  extern __shared__ uint4 mma_smem[];
+  float* red = reinterpret_cast<float*>(mma_smem + kMmaRingBytes / 16);  // [warp][slot][4][32]
+  // staged x: [token][group][quarter][20 words]
+  uint32_t* xw = reinterpret_cast<uint32_t*>(mma_smem + (kMmaRingBytes + kMmaRedBytes) / 16);
+  const int G = K >> 7;   // groups of 128 per row
+  const int kw = K >> 3;  // code words per row
+  const int tw = mma_token_words(K);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int quad = lane & ~3;
+  const int tiles = (N + 15) >> 4;
+  // this block's tiles, and this warp's steps within them (step = tile-major (tile, group) index from t_lo)
+  const int t_lo = (int)((int64_t)tiles * blockIdx.x / gridDim.x);
+  const int t_hi = (int)((int64_t)tiles * (blockIdx.x + 1) / gridDim.x);
+  const int64_t work = (int64_t)(t_hi - t_lo) * G;
+  const int it_lo = (int)(work * warp / kMmaWarps), it_hi = (int)(work * (warp + 1) / kMmaWarps);
+  const int first_tile = it_lo / G;  // block-relative
+  const int first_g = it_lo - first_tile * G;
+
+  uint4* ring = mma_smem + (size_t)warp * kMmaStages * 64 + lane;  // slot st, row r at [(2 st + r) * 32]
+  // lane c of a quad carries, for each group: c 0 the step of row ra, 1 of row rb, 2 the zero of ra, 3 of rb
+  const uint16_t* sz_src = (c & 2) ? zeros : scales;
+  uint32_t sz[kMmaStages];  // raw fp16 bits of the lane's step or zero, per ring slot
+  // fetch state: the lane's code pieces of rows ra, rb and its step or zero, at the next group to fetch
+  const int32_t* fa = nullptr;
+  const int32_t* fb = nullptr;
+  const uint16_t* fs = nullptr;
+  bool fva = false, fvb = false, fvo = false;
+  int f_tile = first_tile, f_left = it_hi - it_lo, f_left_tile = G - first_g;
+  auto aim = [&](int gi) {  // point the fetch state at group gi of tile f_tile
+    const int ra = (t_lo + f_tile) * 16 + g, rb = ra + 8, r_own = (c & 1) ? rb : ra;
+    fva = ra < N && AWQ_IN((size_t)ra * kw + gi * 16 + 4 * c, 4, (size_t)N * kw);
+    fvb = rb < N && AWQ_IN((size_t)rb * kw + gi * 16 + 4 * c, 4, (size_t)N * kw);
+    fvo = r_own < N;
+    fa = qweight + (size_t)(fva ? ra : 0) * kw + gi * 16 + 4 * c;
+    fb = qweight + (size_t)(fvb ? rb : 0) * kw + gi * 16 + 4 * c;
+    fs = sz_src + (size_t)(fvo ? r_own : 0) * G + gi;
+  };
+  aim(first_g);
+  // the next group's codes into ring slot st and its step or zero into sz[st]; nothing past the range
+  auto fetch = [&](int st) {
+    if (f_left > 0) {
+      if (fva) cp_async16(ring + st * 64, fa);
+      if (fvb) cp_async16(ring + st * 64 + 32, fb);
+      uint32_t v = 0u;
+      if (fvo && AWQ_IN((size_t)(fs - sz_src), 1, (size_t)N * G)) v = *fs;
+      sz[st] = v;
+      fa += 16;
+      fb += 16;
+      fs += 1;
+      --f_left;
+      if (--f_left_tile == 0 && f_left > 0) {
+        ++f_tile;
+        f_left_tile = G;
+        aim(0);
+      }
+    }
+    cp_async_commit();
+  };
+  // the first groups' codes are in flight while x is staged
+#pragma unroll
+  for (int st = 0; st < kMmaStages - 1; ++st) fetch(st);
+
+  // stage x: chunk i (8 channels) of token n is (group gi, quarter c, chunk m) = (i / 16, i / 4 % 4, i % 4)
+  {
+    const int chunks = M * (K >> 3);
+    const uint4* x4 = reinterpret_cast<const uint4*>(x);
+    for (int base = threadIdx.x; base < chunks; base += kMmaThreads * kMmaStageUnroll) {
+      uint4 v[kMmaStageUnroll];
+#pragma unroll
+      for (int u = 0; u < kMmaStageUnroll; ++u) {
+        const int i = base + u * kMmaThreads;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < chunks && AWQ_IN((size_t)i * 8, 8, (size_t)M * K)) v[u] = x4[i];
+      }
+#pragma unroll
+      for (int u = 0; u < kMmaStageUnroll; ++u) {
+        const int i = base + u * kMmaThreads;
+        if (i >= chunks) break;
+        const int n = i / (K >> 3), r = i - n * (K >> 3);
+        const int gi = r >> 4, cq = (r >> 2) & 3, m = r & 3;
+        const uint4 w = make_uint4(__byte_perm(v[u].x, v[u].z, 0x5410), __byte_perm(v[u].x, v[u].z, 0x7632),
+                                   __byte_perm(v[u].y, v[u].w, 0x5410), __byte_perm(v[u].y, v[u].w, 0x7632));
+        *reinterpret_cast<uint4*>(xw + n * tw + (gi * 4 + cq) * kMmaQStride + 4 * m) = w;
+      }
+    }
+  }
+  __syncthreads();
+
+  // MMA column g is token g; columns past the last token read token 0 (column j of the product depends on
+  // column j of x only, and those columns are never stored)
+  const uint32_t* xrow = xw + (size_t)(g < M ? g : 0) * tw + c * kMmaQStride;
+  float* red_mine = red + warp * 256 + lane;  // slot s, output i at [s * 128 + i * 32]
+  float acc[4][4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[p][i] = 0.0f;
+  // the tile's sums: to y (whole tile here) or to this warp's first or last slot
+  auto flush = [&](int tile, bool whole) {
+    float out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) acc[p][i] = 0.0f;
+    }
+    if (whole) {
+      mma_store(y, M, N, (t_lo + tile) * 16 + g, c, out);
+    } else {
+      float* slot = red_mine + (tile == first_tile ? 0 : 128);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) slot[i * 32] = out[i];
+    }
+  };
+  // one group: codes from ring slot st, this lane's step or zero from sz[st]
+  int c_tile = first_tile, c_g = first_g;
+  auto step = [&](int st) {
+    cp_async_wait<kMmaStages - 2>();  // this group's codes have landed (this thread's copies)
+    const uint4 qa = ring[st * 64], qb = ring[st * 64 + 32];
+    // the lane's value as the MMA side uses it: a step as fp32 bits, a zero z = z_lo + 256 k (z_lo in
+    // [-128, 128]) as the bf16 pair 128 + z_lo, exact like (q - z_lo); -256 k is exact in bf16 too
+    const float f = __half2float(__ushort_as_half((unsigned short)sz[st]));
+    fetch((st + kMmaStages - 1) % kMmaStages);  // into the slot the previous group used
+    const float kf = rintf(f * (1.0f / 256.0f));
+    const uint32_t mine = (c & 2) ? bf16_pair_bits(128.0f + (f - 256.0f * kf)) : __float_as_uint(f);
+    const float sfa = __uint_as_float(__shfl_sync(0xffffffffu, mine, quad));
+    const float sfb = __uint_as_float(__shfl_sync(0xffffffffu, mine, quad + 1));
+    const uint32_t zza = __shfl_sync(0xffffffffu, mine, quad + 2);
+    const uint32_t zzb = __shfl_sync(0xffffffffu, mine, quad + 3);
+    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+    const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+    const uint32_t* xg = xrow + c_g * (4 * kMmaQStride);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(xg + 4 * m);  // b0, b1 of k-steps 2m and 2m + 1
+      mma_bf16_16816(d, code_pair(wa[m], zza), code_pair(wb[m], zzb), code_pair(wa[m] >> 4, zza),
+                     code_pair(wb[m] >> 4, zzb), xv.x, xv.y);
+      mma_bf16_16816(d, code_pair(wa[m] >> 8, zza), code_pair(wb[m] >> 8, zzb), code_pair(wa[m] >> 12, zza),
+                     code_pair(wb[m] >> 12, zzb), xv.z, xv.w);
+    }
+    if (__any_sync(0xffffffffu, (c & 2) && kf != 0.0f)) {
+      // the constant -256 k of each row against the group's activations
+      const float kfa = __shfl_sync(0xffffffffu, kf, quad + 2), kfb = __shfl_sync(0xffffffffu, kf, quad + 3);
+      const uint32_t ka = bf16_pair_bits(-256.0f * kfa), kb2 = bf16_pair_bits(-256.0f * kfb);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xg + 4 * m);
+        mma_bf16_16816(d, ka, kb2, ka, kb2, xv.x, xv.y);
+        mma_bf16_16816(d, ka, kb2, ka, kb2, xv.z, xv.w);
+      }
+    }
+    float (&ac)[4] = acc[st & 3];
+    ac[0] = fmaf(sfa, d[0], ac[0]);
+    ac[1] = fmaf(sfa, d[1], ac[1]);
+    ac[2] = fmaf(sfb, d[2], ac[2]);
+    ac[3] = fmaf(sfb, d[3], ac[3]);
+    if (++c_g == G) {  // the tile's last group: whole if this warp also had its first
+      flush(c_tile, c_tile != first_tile || first_g == 0);
+      c_g = 0;
+      ++c_tile;
+    }
+  };
+  int it = it_lo;
+#pragma unroll 1
+  for (; it + kMmaStages <= it_hi; it += kMmaStages) {
+#pragma unroll
+    for (int st = 0; st < kMmaStages; ++st) step(st);
+  }
+#pragma unroll
+  for (int st = 0; st < kMmaStages - 1; ++st)
+    if (it + st < it_hi) step(st);
+  if (c_g != 0) flush(c_tile, false);  // the range ends inside a tile
+  cp_async_wait<0>();
+  __syncthreads();
+  // a tile cut between warps: the warp holding its first group adds the later warps' first-slot partials
+  if (it_hi > it_lo && it_hi % G != 0) {
+    const int lt = it_hi / G;  // this warp's last tile, continued by later warps
+    if (lt * G >= it_lo) {
+      float out[4];
+      const float* own_slot = red_mine + (lt == first_tile ? 0 : 128);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) out[i] = own_slot[i * 32];
+      for (int w2 = warp + 1; w2 < kMmaWarps; ++w2) {
+        const int lo2 = (int)(work * w2 / kMmaWarps), hi2 = (int)(work * (w2 + 1) / kMmaWarps);
+        if (lo2 >= (lt + 1) * G) break;
+        if (hi2 == lo2) continue;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) out[i] += red[w2 * 256 + i * 32 + lane];
+      }
+      mma_store(y, M, N, (t_lo + lt) * 16 + g, c, out);
+    }
+  }
+}
+
 // ------------------------------------------------------------ prefill: expand, then the tensor-core product
 //
 // For token counts past the decode kernel's, the packed layer is expanded
@@ -278,6 +586,21 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int
                               const uint16_t* zeros, int64_t N, int group, float* y, cudaStream_t st) {
   const int gsh = group == 32 ? 0 : (group == 64 ? 1 : (group == 128 ? 2 : -1));
   if (gsh < 0) return cudaErrorInvalidValue;
+  // groups of 128: the tensor-core product, except one token on a small layer, where the fp32 kernel's
+  // shorter start wins (measured)
+  if (AWQ_DECODE_MMA && group == 128 && M >= 1 && M <= 8 && (M >= 2 || N * K >= AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS)) {
+    int sms = 0;
+    cudaError_t e = sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    const int smem = kMmaRingBytes + kMmaRedBytes + (int)(M * mma_token_words((int)K) * 4);
+    e = ensure_dynamic_smem((const void*)w4a16_mma_kernel, smem);
+    if (e != cudaSuccess) return e;
+    // one block per SM, each with a contiguous run of row tiles
+    const int64_t tiles = (N + 15) / 16;
+    const int64_t grid = tiles < (int64_t)sms ? tiles : (int64_t)sms;
+    w4a16_mma_kernel<<<(unsigned)grid, kMmaThreads, smem, st>>>(x, (int)M, (int)K, qweight, scales, zeros, (int)N, y);
+    return cudaGetLastError();
+  }
   switch (M) {
     case 1: return launch_w4_t<1>(x, K, qweight, scales, zeros, N, gsh, y, st);
     case 2: return launch_w4_t<2>(x, K, qweight, scales, zeros, N, gsh, y, st);

@@ -23,11 +23,15 @@ def _lib():
 
 
 def _bound(x, W_hat):
-    # exact products (bf16 x times small integers), fp32 pair sums over 16
-    # terms, one pair add, one fused scale per 32 columns, at most K/1024
-    # chunk sums per lane and a 5-level lane tree: under 64 roundings of 2^-24
-    # of sum |x| |w|
-    return 64 * 2.0**-24 * (np.abs(x) @ np.abs(W_hat).T) + 1e-30
+    # exact products (bf16 x times small integers), then fp32 sums. Groups of
+    # 32 or 64: pair sums over 16 terms, one pair add, one fused scale per 32
+    # columns, at most K/1024 chunk sums per lane and a 5-level lane tree.
+    # Groups of 128: eight tensor-core accumulations per group, one fused
+    # scale into one of four running sums (K/512 each), three final adds and
+    # at most three split sums. Either way under max(64, 24 + K/512)
+    # roundings of 2^-24 of sum |x| |w|.
+    n_round = max(64, 24 + x.shape[1] // 512)
+    return n_round * 2.0**-24 * (np.abs(x) @ np.abs(W_hat).T) + 1e-30
 
 
 def _random_packed(rng, N, K, group=128):
@@ -61,6 +65,29 @@ def test_w4a16_matches_oracle(M, N, K):
     assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got - ref).max():.3e}"
 
 
+@pytest.mark.parametrize("M,N,K", [(3, 300, 4096), (1, 4096, 2048), (8, 130, 5632)])
+def test_w4a16_zero_points_far_outside_the_code_range(M, N, K):
+    """Groups offset far from 0 (one-signed groups): the zero point is not
+    clamped, so stored zeros reach the thousands and the group-128 kernel
+    takes its split z = z_lo + 256 k. Its two partial sums carry at most
+    |q - z_lo| + 256 |k| <= |q - z| + 256 per product, under 4 times |q - z|
+    for |z| > 128, so the bound is widened by 4."""
+    rng = np.random.default_rng(M * 7 + N + K)
+    W = rng.standard_normal((N, K)) * 0.02
+    offsets = rng.choice([0.0, 0.5, -0.5, 2.0, -2.0, 20.0, -20.0], size=(N, K // 128))
+    W = W + np.repeat(offsets, 128, axis=1)
+    s = O.f32(rng.uniform(0.999, 1.001, K))  # a near-flat scale keeps each offset group narrow
+    pk = O.quantize_pack(W, s)
+    z = pk["zeros"].astype(np.float64)
+    assert np.isfinite(z).all() and (z < -128).any() and (z > 127).any() and (np.abs(z) > 2048).any()
+    x = workloads.round_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32)).astype(np.float64)
+    got = _run(x.astype(np.float32), pk)
+    ref = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"])
+    W_hat = O.dequantize_groups(O.unpack_words(pk["qweight"], K), pk["scales"].astype(np.float64), z)
+    bad = np.abs(got - ref) > 4 * _bound(x, W_hat)
+    assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got - ref).max():.3e}"
+
+
 @pytest.mark.parametrize("group", [32, 64])
 @pytest.mark.parametrize("M,N,K", [(1, 300, 1024), (4, 130, 640), (8, 520, 4096), (1, 4096, 4096)])
 def test_w4a16_finer_groups_match_oracle(group, M, N, K):
@@ -89,6 +116,43 @@ def test_w4a16_at_the_largest_token_channel_count(M, K):
     W_hat = O.dequantize_groups(O.unpack_words(pk["qweight"], K), pk["scales"].astype(np.float64),
                                 pk["zeros"].astype(np.float64))
     assert not (np.abs(got - ref) > _bound(x, W_hat)).any()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 28672, 8192), (4, 28672, 8192), (8, 28672, 5632), (1, 16400, 8192)])
+def test_w4a16_full_size_sampled_rows(M, N, K):
+    """70B-class MLP shapes in the launch configuration the benchmark times
+    (one token on a layer above the single-token size threshold takes the
+    tensor-core kernel), on random codes, steps and zero points (a tenth of
+    them far outside the code range), checked on 512 sampled rows, the first
+    and the last row tile included."""
+    rng = np.random.default_rng(M * 7 + N + K)
+    G = K // 128
+    qweight = rng.integers(-2**31, 2**31, size=(N, K // 8), dtype=np.int64).astype(np.int32)
+    scales = rng.uniform(1e-3, 1e-2, size=(N, G)).astype(np.float16)
+    zeros = rng.integers(0, 16, size=(N, G)).astype(np.float64)
+    far = rng.random((N, G)) < 0.1
+    zeros[far] = rng.integers(-3000, 3000, size=far.sum())
+    zeros = zeros.astype(np.float16)
+    x = workloads.round_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32)).astype(np.float64)
+    y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    capi.awq_w4a16_gemv(dev_bf16(x.astype(np.float32)), torch.from_numpy(qweight).cuda(),
+                        torch.from_numpy(scales.view(np.int16)).cuda(), torch.from_numpy(zeros.view(np.int16)).cuda(),
+                        capi.config(), y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    # the order of every sum is fixed: a second call gives the same bits
+    y2 = torch.empty_like(y)
+    capi.awq_w4a16_gemv(dev_bf16(x.astype(np.float32)), torch.from_numpy(qweight).cuda(),
+                        torch.from_numpy(scales.view(np.int16)).cuda(), torch.from_numpy(zeros.view(np.int16)).cuda(),
+                        capi.config(), y2)
+    assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
+    rows = np.unique(np.concatenate([np.arange(16), np.arange(N - 16, N), rng.choice(N, 480, replace=False)]))
+    ref = O.w4a16_linear(x, qweight[rows], scales[rows], zeros[rows])
+    W_hat = O.dequantize_groups(O.unpack_words(qweight[rows], K), scales[rows].astype(np.float64),
+                                zeros[rows].astype(np.float64))
+    # far zero points: the split z = z_lo + 256 k widens the bound by 4 (see the far-zero-point test)
+    bad = np.abs(got[:, rows] - ref) > 4 * _bound(x, W_hat)
+    assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got[:, rows] - ref).max():.3e}"
 
 
 def test_layer_packed_on_gpu_reproduces_the_searched_weight():
