@@ -272,9 +272,21 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// (128 + n, 128 + n') as a bf16 pair from a word whose nibbles n, n' sit at bits 0 and 16, minus the pair zz.
-__device__ __forceinline__ uint32_t code_pair(uint32_t ws, uint32_t zz) {
-  const uint32_t p = (ws & 0x000F000Fu) | 0x43004300u;
+// The two constants of code_pair, held in registers for the kernel's life: with both as immediates the
+// compiler spends a second integer instruction per pair.
+struct PairConsts {
+  uint32_t mask, bias;  // 0x000F000F, 0x43004300
+  __device__ __forceinline__ PairConsts() {
+    asm volatile("mov.b32 %0, 0x000F000F;" : "=r"(mask));
+    asm volatile("mov.b32 %0, 0x43004300;" : "=r"(bias));
+  }
+};
+
+// (128 + n, 128 + n') as a bf16 pair from a word whose nibbles n, n' sit at bits 0 and 16 (one
+// three-input logic instruction: (ws & mask) | bias), minus the pair zz.
+__device__ __forceinline__ uint32_t code_pair(uint32_t ws, uint32_t zz, const PairConsts& k) {
+  uint32_t p;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(p) : "r"(ws), "r"(k.mask), "r"(k.bias));
   const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&p),
                                    *reinterpret_cast<const __nv_bfloat162*>(&zz));
   return *reinterpret_cast<const uint32_t*>(&r);
@@ -389,6 +401,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // MMA column g is token g; columns past the last token read token 0 (column j of the product depends on
   // column j of x only, and those columns are never stored)
   const uint32_t* xrow = xw + (size_t)(g < M ? g : 0) * tw + c * kMmaQStride;
+  const PairConsts pk;
   float* red_mine = red + warp * 256 + lane;  // slot s, output i at [s * 128 + i * 32]
   float acc[4][4];
 #pragma unroll
@@ -434,10 +447,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const uint4 xv = *reinterpret_cast<const uint4*>(xg + 4 * m);  // b0, b1 of k-steps 2m and 2m + 1
-      mma_bf16_16816(d, code_pair(wa[m], zza), code_pair(wb[m], zzb), code_pair(wa[m] >> 4, zza),
-                     code_pair(wb[m] >> 4, zzb), xv.x, xv.y);
-      mma_bf16_16816(d, code_pair(wa[m] >> 8, zza), code_pair(wb[m] >> 8, zzb), code_pair(wa[m] >> 12, zza),
-                     code_pair(wb[m] >> 12, zzb), xv.z, xv.w);
+      mma_bf16_16816(d, code_pair(wa[m], zza, pk), code_pair(wb[m], zzb, pk), code_pair(wa[m] >> 4, zza, pk),
+                     code_pair(wb[m] >> 4, zzb, pk), xv.x, xv.y);
+      mma_bf16_16816(d, code_pair(wa[m] >> 8, zza, pk), code_pair(wb[m] >> 8, zzb, pk),
+                     code_pair(wa[m] >> 12, zza, pk), code_pair(wb[m] >> 12, zzb, pk), xv.z, xv.w);
     }
     if (__any_sync(0xffffffffu, (c & 2) && kf != 0.0f)) {
       // the constant -256 k of each row against the group's activations
