@@ -236,20 +236,20 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 #define AWQ_DECODE_MMA 1
 #endif
 #ifndef AWQ_MMA_STAGES
-#define AWQ_MMA_STAGES 6
+#define AWQ_MMA_STAGES 3
 #endif
 #ifndef AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS
 #define AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS (int64_t(1) << 27)
 #endif
 #ifndef AWQ_MMA_WARPS
-#define AWQ_MMA_WARPS 16
+#define AWQ_MMA_WARPS 12
 #endif
 constexpr int kMmaWarps = AWQ_MMA_WARPS;
 constexpr int kMmaThreads = kMmaWarps * 32;
-constexpr int kMmaStages = AWQ_MMA_STAGES;  // groups of codes per warp in the ring: kMmaStages - 1 in flight
+constexpr int kMmaStages = AWQ_MMA_STAGES;  // pairs of groups per warp in the ring: kMmaStages - 1 in flight
 constexpr int kMmaQStride = 20;             // staged words per (token, group, quarter): 16 + 4 of padding
 constexpr int kMmaStageUnroll = 4;          // 16-byte loads of x in flight per thread while staging
-constexpr int kMmaRingBytes = kMmaWarps * kMmaStages * 2 * 32 * 16;
+constexpr int kMmaRingBytes = kMmaWarps * kMmaStages * 2 * 2 * 32 * 16;
 constexpr int kMmaRedBytes = kMmaWarps * 2 * 4 * 32 * 4;  // per warp: a first and a last partial tile, 4 per lane
 
 // Words per token region: 16 more than a multiple of 32, so two tokens read in one phase meet distinct banks.
@@ -313,62 +313,70 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   float* red = reinterpret_cast<float*>(mma_smem + kMmaRingBytes / 16);  // [warp][slot][4][32]
   // staged x: [token][group][quarter][20 words]
   uint32_t* xw = reinterpret_cast<uint32_t*>(mma_smem + (kMmaRingBytes + kMmaRedBytes) / 16);
-  const int G = K >> 7;   // groups of 128 per row
+  const int G = K >> 7;   // groups of 128 per row (even)
+  const int P = G >> 1;   // steps per row: pairs of groups
   const int kw = K >> 3;  // code words per row
   const int tw = mma_token_words(K);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int quad = lane & ~3;
   const int tiles = (N + 15) >> 4;
-  // this block's tiles, and this warp's steps within them (step = tile-major (tile, group) index from t_lo)
+  // this block's tiles, and this warp's steps within them (step = tile-major (tile, pair) index from t_lo)
   const int t_lo = (int)((int64_t)tiles * blockIdx.x / gridDim.x);
   const int t_hi = (int)((int64_t)tiles * (blockIdx.x + 1) / gridDim.x);
-  const int64_t work = (int64_t)(t_hi - t_lo) * G;
+  const int64_t work = (int64_t)(t_hi - t_lo) * P;
   const int it_lo = (int)(work * warp / kMmaWarps), it_hi = (int)(work * (warp + 1) / kMmaWarps);
-  const int first_tile = it_lo / G;  // block-relative
-  const int first_g = it_lo - first_tile * G;
+  const int first_tile = it_lo / P;  // block-relative
+  const int first_p = it_lo - first_tile * P;
 
-  uint4* ring = mma_smem + (size_t)warp * kMmaStages * 64 + lane;  // slot st, row r at [(2 st + r) * 32]
+  // ring slot st: group 2p (uint4 [st * 128 + r * 32 + lane], r = 0 for row ra, 1 for rb), group 2p + 1 64 further
+  uint4* ring = mma_smem + (size_t)warp * kMmaStages * 128 + lane;
   // lane c of a quad carries, for each group: c 0 the step of row ra, 1 of row rb, 2 the zero of ra, 3 of rb
   const uint16_t* sz_src = (c & 2) ? zeros : scales;
-  uint32_t sz[kMmaStages];  // raw fp16 bits of the lane's step or zero, per ring slot
-  // fetch state: the lane's code pieces of rows ra, rb and its step or zero, at the next group to fetch
+  uint32_t sz[kMmaStages];  // raw fp16 bits of the lane's step or zero for the pair's two groups, per ring slot
+  // fetch state: the lane's code pieces of rows ra, rb and its steps or zeros, at the next pair to fetch
   const int32_t* fa = nullptr;
   const int32_t* fb = nullptr;
   const uint16_t* fs = nullptr;
   bool fva = false, fvb = false, fvo = false;
-  int f_tile = first_tile, f_left = it_hi - it_lo, f_left_tile = G - first_g;
-  auto aim = [&](int gi) {  // point the fetch state at group gi of tile f_tile
+  int f_tile = first_tile, f_left = it_hi - it_lo, f_left_tile = P - first_p;
+  auto aim = [&](int gi) {  // point the fetch state at group gi (even) of tile f_tile
     const int ra = (t_lo + f_tile) * 16 + g, rb = ra + 8, r_own = (c & 1) ? rb : ra;
-    fva = ra < N && AWQ_IN((size_t)ra * kw + gi * 16 + 4 * c, 4, (size_t)N * kw);
-    fvb = rb < N && AWQ_IN((size_t)rb * kw + gi * 16 + 4 * c, 4, (size_t)N * kw);
+    fva = ra < N && AWQ_IN((size_t)ra * kw + gi * 16 + 4 * c, 20, (size_t)N * kw);
+    fvb = rb < N && AWQ_IN((size_t)rb * kw + gi * 16 + 4 * c, 20, (size_t)N * kw);
     fvo = r_own < N;
     fa = qweight + (size_t)(fva ? ra : 0) * kw + gi * 16 + 4 * c;
     fb = qweight + (size_t)(fvb ? rb : 0) * kw + gi * 16 + 4 * c;
     fs = sz_src + (size_t)(fvo ? r_own : 0) * G + gi;
   };
-  aim(first_g);
-  // the next group's codes into ring slot st and its step or zero into sz[st]; nothing past the range
+  aim(2 * first_p);
+  // the next pair's codes into ring slot st and its two steps or zeros into sz[st]; nothing past the range
   auto fetch = [&](int st) {
     if (f_left > 0) {
-      if (fva) cp_async16(ring + st * 64, fa);
-      if (fvb) cp_async16(ring + st * 64 + 32, fb);
-      uint32_t v = 0u;
-      if (fvo && AWQ_IN((size_t)(fs - sz_src), 1, (size_t)N * G)) v = *fs;
+      if (fva) {
+        cp_async16(ring + st * 128, fa);
+        cp_async16(ring + st * 128 + 64, fa + 16);
+      }
+      if (fvb) {
+        cp_async16(ring + st * 128 + 32, fb);
+        cp_async16(ring + st * 128 + 96, fb + 16);
+      }
+      uint32_t v = 0u;  // both groups' values in one aligned 32-bit load (row * G + gi is even)
+      if (fvo && AWQ_IN((size_t)(fs - sz_src), 2, (size_t)N * G)) v = *reinterpret_cast<const uint32_t*>(fs);
       sz[st] = v;
-      fa += 16;
-      fb += 16;
-      fs += 1;
+      fa += 32;
+      fb += 32;
+      fs += 2;
       --f_left;
       if (--f_left_tile == 0 && f_left > 0) {
         ++f_tile;
-        f_left_tile = G;
+        f_left_tile = P;
         aim(0);
       }
     }
     cp_async_commit();
   };
-  // the first groups' codes are in flight while x is staged
+  // the first pairs' codes are in flight while x is staged
 #pragma unroll
   for (int st = 0; st < kMmaStages - 1; ++st) fetch(st);
 
@@ -425,25 +433,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int i = 0; i < 4; ++i) slot[i * 32] = out[i];
     }
   };
-  // one group: codes from ring slot st, this lane's step or zero from sz[st]
-  int c_tile = first_tile, c_g = first_g;
-  auto step = [&](int st) {
-    cp_async_wait<kMmaStages - 2>();  // this group's codes have landed (this thread's copies)
-    const uint4 qa = ring[st * 64], qb = ring[st * 64 + 32];
-    // the lane's value as the MMA side uses it: a step as fp32 bits, a zero z = z_lo + 256 k (z_lo in
-    // [-128, 128]) as the bf16 pair 128 + z_lo, exact like (q - z_lo); -256 k is exact in bf16 too
-    const float f = __half2float(__ushort_as_half((unsigned short)sz[st]));
-    fetch((st + kMmaStages - 1) % kMmaStages);  // into the slot the previous group used
-    const float kf = rintf(f * (1.0f / 256.0f));
-    const uint32_t mine = (c & 2) ? bf16_pair_bits(128.0f + (f - 256.0f * kf)) : __float_as_uint(f);
-    const float sfa = __uint_as_float(__shfl_sync(0xffffffffu, mine, quad));
-    const float sfb = __uint_as_float(__shfl_sync(0xffffffffu, mine, quad + 1));
-    const uint32_t zza = __shfl_sync(0xffffffffu, mine, quad + 2);
-    const uint32_t zzb = __shfl_sync(0xffffffffu, mine, quad + 3);
-    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  // the lane's value as the MMA side uses it: a step as fp32 bits, a zero z = z_lo + 256 k (z_lo in
+  // [-128, 128]) as the bf16 pair 128 + z_lo, exact like (q - z_lo); -256 k is exact in bf16 too
+  auto lane_value = [&](uint32_t bits, float& kf) {
+    const float f = __half2float(__ushort_as_half((unsigned short)bits));
+    kf = rintf(f * (1.0f / 256.0f));
+    return (c & 2) ? bf16_pair_bits(128.0f + (f - 256.0f * kf)) : __float_as_uint(f);
+  };
+  // 8 MMAs of one group of 16 rows: codes wa (row ra), wb (row rb), zero pairs zza, zzb, x at xg
+  auto group_mma = [&](float (&d)[4], const uint4& qa, const uint4& qb, uint32_t zza, uint32_t zzb,
+                       const uint32_t* xg) {
     const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
     const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
-    const uint32_t* xg = xrow + c_g * (4 * kMmaQStride);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const uint4 xv = *reinterpret_cast<const uint4*>(xg + 4 * m);  // b0, b1 of k-steps 2m and 2m + 1
@@ -452,25 +453,58 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       mma_bf16_16816(d, code_pair(wa[m] >> 8, zza, pk), code_pair(wb[m] >> 8, zzb, pk),
                      code_pair(wa[m] >> 12, zza, pk), code_pair(wb[m] >> 12, zzb, pk), xv.z, xv.w);
     }
-    if (__any_sync(0xffffffffu, (c & 2) && kf != 0.0f)) {
-      // the constant -256 k of each row against the group's activations
-      const float kfa = __shfl_sync(0xffffffffu, kf, quad + 2), kfb = __shfl_sync(0xffffffffu, kf, quad + 3);
-      const uint32_t ka = bf16_pair_bits(-256.0f * kfa), kb2 = bf16_pair_bits(-256.0f * kfb);
+  };
+  // the constant -256 k of each row against one group's activations (zero points outside [-128, 127])
+  auto far_zero_mma = [&](float (&d)[4], float kf, const uint32_t* xg) {
+    const float kfa = __shfl_sync(0xffffffffu, kf, quad + 2), kfb = __shfl_sync(0xffffffffu, kf, quad + 3);
+    const uint32_t ka = bf16_pair_bits(-256.0f * kfa), kb2 = bf16_pair_bits(-256.0f * kfb);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(xg + 4 * m);
-        mma_bf16_16816(d, ka, kb2, ka, kb2, xv.x, xv.y);
-        mma_bf16_16816(d, ka, kb2, ka, kb2, xv.z, xv.w);
-      }
+    for (int m = 0; m < 4; ++m) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(xg + 4 * m);
+      mma_bf16_16816(d, ka, kb2, ka, kb2, xv.x, xv.y);
+      mma_bf16_16816(d, ka, kb2, ka, kb2, xv.z, xv.w);
     }
-    float (&ac)[4] = acc[st & 3];
-    ac[0] = fmaf(sfa, d[0], ac[0]);
-    ac[1] = fmaf(sfa, d[1], ac[1]);
-    ac[2] = fmaf(sfb, d[2], ac[2]);
-    ac[3] = fmaf(sfb, d[3], ac[3]);
-    if (++c_g == G) {  // the tile's last group: whole if this warp also had its first
-      flush(c_tile, c_tile != first_tile || first_g == 0);
-      c_g = 0;
+  };
+  // one pair of groups: codes from ring slot st, this lane's two steps or zeros from sz[st]
+  int c_tile = first_tile, c_p = first_p;
+  auto step = [&](int st) {
+    cp_async_wait<kMmaStages - 2>();  // this pair's codes have landed (this thread's copies)
+    const uint4 qa0 = ring[st * 128], qb0 = ring[st * 128 + 32];
+    const uint4 qa1 = ring[st * 128 + 64], qb1 = ring[st * 128 + 96];
+    const uint32_t own = sz[st];
+    fetch((st + kMmaStages - 1) % kMmaStages);  // into the slot the previous pair used
+    float kf0, kf1;
+    const uint32_t mine0 = lane_value(own, kf0), mine1 = lane_value(own >> 16, kf1);
+    const float sfa0 = __uint_as_float(__shfl_sync(0xffffffffu, mine0, quad));
+    const float sfb0 = __uint_as_float(__shfl_sync(0xffffffffu, mine0, quad + 1));
+    const uint32_t zza0 = __shfl_sync(0xffffffffu, mine0, quad + 2);
+    const uint32_t zzb0 = __shfl_sync(0xffffffffu, mine0, quad + 3);
+    const float sfa1 = __uint_as_float(__shfl_sync(0xffffffffu, mine1, quad));
+    const float sfb1 = __uint_as_float(__shfl_sync(0xffffffffu, mine1, quad + 1));
+    const uint32_t zza1 = __shfl_sync(0xffffffffu, mine1, quad + 2);
+    const uint32_t zzb1 = __shfl_sync(0xffffffffu, mine1, quad + 3);
+    const uint32_t* xg0 = xrow + (2 * c_p) * (4 * kMmaQStride);
+    const uint32_t* xg1 = xg0 + 4 * kMmaQStride;
+    float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    group_mma(d0, qa0, qb0, zza0, zzb0, xg0);
+    group_mma(d1, qa1, qb1, zza1, zzb1, xg1);
+    if (__any_sync(0xffffffffu, (c & 2) && (kf0 != 0.0f || kf1 != 0.0f))) {
+      far_zero_mma(d0, kf0, xg0);
+      far_zero_mma(d1, kf1, xg1);
+    }
+    float (&a0)[4] = acc[(2 * st) & 3];
+    float (&a1)[4] = acc[(2 * st + 1) & 3];
+    a0[0] = fmaf(sfa0, d0[0], a0[0]);
+    a0[1] = fmaf(sfa0, d0[1], a0[1]);
+    a0[2] = fmaf(sfb0, d0[2], a0[2]);
+    a0[3] = fmaf(sfb0, d0[3], a0[3]);
+    a1[0] = fmaf(sfa1, d1[0], a1[0]);
+    a1[1] = fmaf(sfa1, d1[1], a1[1]);
+    a1[2] = fmaf(sfb1, d1[2], a1[2]);
+    a1[3] = fmaf(sfb1, d1[3], a1[3]);
+    if (++c_p == P) {  // the tile's last pair: whole if this warp also had its first
+      flush(c_tile, c_tile != first_tile || first_p == 0);
+      c_p = 0;
       ++c_tile;
     }
   };
@@ -483,20 +517,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
   for (int st = 0; st < kMmaStages - 1; ++st)
     if (it + st < it_hi) step(st);
-  if (c_g != 0) flush(c_tile, false);  // the range ends inside a tile
+  if (c_p != 0) flush(c_tile, false);  // the range ends inside a tile
   cp_async_wait<0>();
   __syncthreads();
-  // a tile cut between warps: the warp holding its first group adds the later warps' first-slot partials
-  if (it_hi > it_lo && it_hi % G != 0) {
-    const int lt = it_hi / G;  // this warp's last tile, continued by later warps
-    if (lt * G >= it_lo) {
+  // a tile cut between warps: the warp holding its first pair adds the later warps' first-slot partials
+  if (it_hi > it_lo && it_hi % P != 0) {
+    const int lt = it_hi / P;  // this warp's last tile, continued by later warps
+    if (lt * P >= it_lo) {
       float out[4];
       const float* own_slot = red_mine + (lt == first_tile ? 0 : 128);
 #pragma unroll
       for (int i = 0; i < 4; ++i) out[i] = own_slot[i * 32];
       for (int w2 = warp + 1; w2 < kMmaWarps; ++w2) {
         const int lo2 = (int)(work * w2 / kMmaWarps), hi2 = (int)(work * (w2 + 1) / kMmaWarps);
-        if (lo2 >= (lt + 1) * G) break;
+        if (lo2 >= (lt + 1) * P) break;
         if (hi2 == lo2) continue;
 #pragma unroll
         for (int i = 0; i < 4; ++i) out[i] += red[w2 * 256 + i * 32 + lane];
@@ -599,9 +633,13 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int
                               const uint16_t* zeros, int64_t N, int group, float* y, cudaStream_t st) {
   const int gsh = group == 32 ? 0 : (group == 64 ? 1 : (group == 128 ? 2 : -1));
   if (gsh < 0) return cudaErrorInvalidValue;
-  // groups of 128: the tensor-core product, except one token on a small layer, where the fp32 kernel's
-  // shorter start wins (measured)
-  if (AWQ_DECODE_MMA && group == 128 && M >= 1 && M <= 8 && (M >= 2 || N * K >= AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS)) {
+  // groups of 128 with an even number of groups per row and 4-byte aligned steps and zeros: the
+  // tensor-core product (it steps by pairs of groups, reading both groups' step or zero in one load), except
+  // one token on a small layer, where the fp32 kernel's shorter start wins (measured)
+  const bool pairs_ok = (K / 128) % 2 == 0 && (reinterpret_cast<uintptr_t>(scales) & 3u) == 0 &&
+                        (reinterpret_cast<uintptr_t>(zeros) & 3u) == 0;
+  if (AWQ_DECODE_MMA && group == 128 && pairs_ok && M >= 1 && M <= 8 &&
+      (M >= 2 || N * K >= AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS)) {
     int sms = 0;
     cudaError_t e = sm_count(&sms);
     if (e != cudaSuccess) return e;

@@ -27,10 +27,11 @@ def _bound(x, W_hat):
     # 32 or 64: pair sums over 16 terms, one pair add, one fused scale per 32
     # columns, at most K/1024 chunk sums per lane and a 5-level lane tree.
     # Groups of 128: eight tensor-core accumulations per group, one fused
-    # scale into one of four running sums (K/512 each), three final adds and
-    # at most three split sums. Either way under max(64, 24 + K/512)
-    # roundings of 2^-24 of sum |x| |w|.
-    n_round = max(64, 24 + x.shape[1] // 512)
+    # scale into one of four running sums (at most a third of the K/128
+    # groups each), three final adds and the split sums of a tile cut
+    # between warps. Either way under max(64, 24 + K/384) roundings of 2^-24
+    # of sum |x| |w|.
+    n_round = max(64, 24 + x.shape[1] // 384)
     return n_round * 2.0**-24 * (np.abs(x) @ np.abs(W_hat).T) + 1e-30
 
 
@@ -58,6 +59,36 @@ def test_w4a16_matches_oracle(M, N, K):
     pk = _random_packed(rng, N, K)
     x = workloads.round_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32)).astype(np.float64)
     got = _run(x.astype(np.float32), pk)
+    ref = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"])
+    W_hat = O.dequantize_groups(O.unpack_words(pk["qweight"], K), pk["scales"].astype(np.float64),
+                                pk["zeros"].astype(np.float64))
+    bad = np.abs(got - ref) > _bound(x, W_hat)
+    assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got - ref).max():.3e}"
+
+
+def _at_2_byte_offset(a16):
+    """The fp16 array on the device at an address 2 bytes past a 4-byte boundary (the API asks for 2)."""
+    flat = torch.from_numpy(a16.view(np.int16).reshape(-1)).cuda()
+    big = torch.empty(flat.numel() + 1, dtype=torch.int16, device="cuda")
+    big[1:] = flat
+    view = big[1:].view(a16.shape)
+    assert view.data_ptr() % 4 == 2
+    return view
+
+
+@pytest.mark.parametrize("M,N,K", [(2, 300, 4096), (4, 130, 8192)])
+def test_w4a16_steps_and_zeros_at_2_byte_offsets(M, N, K):
+    """Steps and zeros only 2-byte aligned (what the call requires): the product is still right (the
+    tensor-core kernel reads both groups of a pair in one 4-byte load, so such pointers take the fp32
+    kernel)."""
+    rng = np.random.default_rng(M * 5 + N + K)
+    pk = _random_packed(rng, N, K)
+    x = workloads.round_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32)).astype(np.float64)
+    y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    capi.awq_w4a16_gemv(dev_bf16(x.astype(np.float32)), torch.from_numpy(pk["qweight"]).cuda(),
+                        _at_2_byte_offset(pk["scales"]), _at_2_byte_offset(pk["zeros"]), capi.config(), y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
     ref = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"])
     W_hat = O.dequantize_groups(O.unpack_words(pk["qweight"], K), pk["scales"].astype(np.float64),
                                 pk["zeros"].astype(np.float64))
