@@ -433,13 +433,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int i = 0; i < 4; ++i) slot[i * 32] = out[i];
     }
   };
-  // the lane's value as the MMA side uses it: a step as fp32 bits, a zero z = z_lo + 256 k (z_lo in
-  // [-128, 128]) as the bf16 pair 128 + z_lo, exact like (q - z_lo); -256 k is exact in bf16 too
-  auto lane_value = [&](uint32_t bits, float& kf) {
-    const float f = __half2float(__ushort_as_half((unsigned short)bits));
-    kf = rintf(f * (1.0f / 256.0f));
-    return (c & 2) ? bf16_pair_bits(128.0f + (f - 256.0f * kf)) : __float_as_uint(f);
-  };
   // 8 MMAs of one group of 16 rows: codes wa (row ra), wb (row rb), zero pairs zza, zzb, x at xg
   auto group_mma = [&](float (&d)[4], const uint4& qa, const uint4& qb, uint32_t zza, uint32_t zzb,
                        const uint32_t* xg) {
@@ -471,18 +464,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     cp_async_wait<kMmaStages - 2>();  // this pair's codes have landed (this thread's copies)
     const uint4 qa0 = ring[st * 128], qb0 = ring[st * 128 + 32];
     const uint4 qa1 = ring[st * 128 + 64], qb1 = ring[st * 128 + 96];
-    const uint32_t own = sz[st];
+    const uint32_t own = sz[st];  // fp16 bits: group 2p low, 2p + 1 high
     fetch((st + kMmaStages - 1) % kMmaStages);  // into the slot the previous pair used
-    float kf0, kf1;
-    const uint32_t mine0 = lane_value(own, kf0), mine1 = lane_value(own >> 16, kf1);
-    const float sfa0 = __uint_as_float(__shfl_sync(0xffffffffu, mine0, quad));
-    const float sfb0 = __uint_as_float(__shfl_sync(0xffffffffu, mine0, quad + 1));
-    const uint32_t zza0 = __shfl_sync(0xffffffffu, mine0, quad + 2);
-    const uint32_t zzb0 = __shfl_sync(0xffffffffu, mine0, quad + 3);
-    const float sfa1 = __uint_as_float(__shfl_sync(0xffffffffu, mine1, quad));
-    const float sfb1 = __uint_as_float(__shfl_sync(0xffffffffu, mine1, quad + 1));
-    const uint32_t zza1 = __shfl_sync(0xffffffffu, mine1, quad + 2);
-    const uint32_t zzb1 = __shfl_sync(0xffffffffu, mine1, quad + 3);
+    // A zero z = z_lo + 256 k (z_lo in [-128, 128]) enters the MMAs as the bf16 value 128 + z_lo, exact like
+    // (q - z_lo); -256 k is exact in bf16 too. The zero lanes (c = 2, 3) pack both groups' 128 + z_lo into
+    // one word, the step lanes pass their two fp16 steps on as loaded: one shuffle per row and kind.
+    const float f0 = __half2float(__ushort_as_half((unsigned short)own));
+    const float f1 = __half2float(__ushort_as_half((unsigned short)(own >> 16)));
+    const float kf0 = rintf(f0 * (1.0f / 256.0f)), kf1 = rintf(f1 * (1.0f / 256.0f));
+    const __nv_bfloat162 zp = __floats2bfloat162_rn(128.0f + (f0 - 256.0f * kf0), 128.0f + (f1 - 256.0f * kf1));
+    const uint32_t mine = (c & 2) ? *reinterpret_cast<const uint32_t*>(&zp) : own;
+    const uint32_t sa = __shfl_sync(0xffffffffu, mine, quad), sb = __shfl_sync(0xffffffffu, mine, quad + 1);
+    const uint32_t za = __shfl_sync(0xffffffffu, mine, quad + 2), zb = __shfl_sync(0xffffffffu, mine, quad + 3);
+    const float sfa0 = __half2float(__ushort_as_half((unsigned short)sa));
+    const float sfa1 = __half2float(__ushort_as_half((unsigned short)(sa >> 16)));
+    const float sfb0 = __half2float(__ushort_as_half((unsigned short)sb));
+    const float sfb1 = __half2float(__ushort_as_half((unsigned short)(sb >> 16)));
+    const uint32_t zza0 = __byte_perm(za, 0u, 0x1010), zza1 = __byte_perm(za, 0u, 0x3232);  // (v, v) pairs
+    const uint32_t zzb0 = __byte_perm(zb, 0u, 0x1010), zzb1 = __byte_perm(zb, 0u, 0x3232);
     const uint32_t* xg0 = xrow + (2 * c_p) * (4 * kMmaQStride);
     const uint32_t* xg1 = xg0 + 4 * kMmaQStride;
     float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
