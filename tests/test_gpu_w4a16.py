@@ -66,27 +66,28 @@ def test_w4a16_matches_oracle(M, N, K):
     assert not bad.any(), f"{bad.sum()} outputs off, max err {np.abs(got - ref).max():.3e}"
 
 
-def _at_2_byte_offset(a16):
-    """The fp16 array on the device at an address 2 bytes past a 4-byte boundary (the API asks for 2)."""
+def _at_offset(a16, elems):
+    """The fp16 array on the device `elems` values (2 bytes each) past an 8-byte boundary."""
     flat = torch.from_numpy(a16.view(np.int16).reshape(-1)).cuda()
-    big = torch.empty(flat.numel() + 1, dtype=torch.int16, device="cuda")
-    big[1:] = flat
-    view = big[1:].view(a16.shape)
-    assert view.data_ptr() % 4 == 2
+    big = torch.empty(flat.numel() + 4, dtype=torch.int16, device="cuda")
+    big[elems:elems + flat.numel()] = flat
+    view = big[elems:elems + flat.numel()].view(a16.shape)
+    assert view.data_ptr() % 8 == 2 * elems
     return view
 
 
+@pytest.mark.parametrize("elems", [1, 2])
 @pytest.mark.parametrize("M,N,K", [(2, 300, 4096), (4, 130, 8192)])
-def test_w4a16_steps_and_zeros_at_2_byte_offsets(M, N, K):
-    """Steps and zeros only 2-byte aligned (what the call requires): the product is still right (the
-    tensor-core kernel reads both groups of a pair in one 4-byte load, so such pointers take the fp32
-    kernel)."""
+def test_w4a16_steps_and_zeros_at_unaligned_offsets(M, N, K, elems):
+    """Steps and zeros only 2- or 4-byte aligned (the call requires 2): the product is still right. The
+    tensor-core kernel reads both groups' values of a step in one 4-byte load, so 2-byte aligned pointers
+    take the fp32 kernel and 4-byte aligned ones the tensor-core kernel."""
     rng = np.random.default_rng(M * 5 + N + K)
     pk = _random_packed(rng, N, K)
     x = workloads.round_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32)).astype(np.float64)
     y = torch.empty(M, N, dtype=torch.float32, device="cuda")
     capi.awq_w4a16_gemv(dev_bf16(x.astype(np.float32)), torch.from_numpy(pk["qweight"]).cuda(),
-                        _at_2_byte_offset(pk["scales"]), _at_2_byte_offset(pk["zeros"]), capi.config(), y)
+                        _at_offset(pk["scales"], elems), _at_offset(pk["zeros"], elems), capi.config(), y)
     torch.cuda.synchronize()
     got = y.cpu().numpy().astype(np.float64)
     ref = O.w4a16_linear(x, pk["qweight"], pk["scales"], pk["zeros"])
