@@ -204,29 +204,32 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 // of x gives one 16-byte chunk of the staged words. Each (group, quarter) row
 // of 16 words is padded to 20, so the four quarters' reads of one token fall
 // in distinct banks. The MMA
-// adds exact products in fp32; after the group's 8 steps the partial is
-// scaled by the group's fp16 step and added to one of four running sums
-// (group index mod 4), which are added at the end: every operation on the
-// way keeps the error within a few dozen fp32 roundings of sum |x| |w|.
+// adds exact products in fp32; after the group's 8 MMAs the partial is
+// scaled by the group's fp16 step and added to one of four running sums (in
+// a fixed rotation, none taking more than a third of the groups), which are
+// added at the end: every operation on the way keeps the error within a few
+// dozen fp32 roundings of sum |x| |w| plus one per three groups.
 // A zero point outside [-128, 127] (never produced for groups that contain
 // both signs) is split as z = z_lo + 256 k, and the group takes one more MMA
 // with the constant -256 k.
 //
-// The codes stream through a per-warp ring of kMmaStages groups in shared
-// memory, filled by per-thread asynchronous copies (each thread copies the
-// 16 bytes of each of its two rows that it reads itself, so no thread waits
-// on another). Rows past the layer's end are not copied: their sums land in
-// output rows that are never stored. Each lane of a quad also loads one of
-// its rows' steps or zeros for the same group, turns it into what the MMA
-// side needs (the step as fp32, the zero as the bf16 pair 128 + z_lo) and
-// shares it within the quad by shuffles.
+// A step of a warp covers two consecutive groups of its 16 rows: 16 MMAs in
+// two independent chains. The codes stream through a per-warp ring of
+// kMmaStages steps in shared memory, filled by per-thread asynchronous
+// copies (each thread copies the 16-byte pieces of its two rows that it
+// reads itself, so no thread waits on another). Rows past the layer's end
+// are not copied: their sums land in output rows that are never stored.
+// Each lane of a quad also loads one of its rows' steps or zeros for both
+// groups of the step in one 4-byte load. The zero lanes pack both groups'
+// bf16 128 + z_lo into one word and the step lanes pass their two fp16 steps
+// on as loaded, so one shuffle per row and kind serves both groups.
 //
 // Work split: one block per SM owns a contiguous run of row tiles, and its
-// (tile, group) steps are cut into kMmaWarps equal contiguous ranges, one per
+// (tile, step) pairs are cut into kMmaWarps equal contiguous ranges, one per
 // warp, so every SM and every warp has the same number of groups to within
 // one tile per block. A tile that lies inside one warp's range is written
 // directly; a tile cut between warps leaves partial sums in shared memory,
-// and the warp holding the tile's first group adds the later warps' partials
+// and the warp holding the tile's first step adds the later warps' partials
 // in warp order, so the result does not depend on timing.
 
 // Ring depth and warps per block (build-time tunables, defaults measured
