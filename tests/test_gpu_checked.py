@@ -61,3 +61,16 @@ def test_parity_suite_under_bounds_checks(checked_lib, tmp_path):
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
     failures, unit, line, offset = (int(x) for x in open(report).read().split())
     assert failures == 0, f"{failures} failed bounds checks, first in unit {unit} line {line} offset {offset}"
+
+
+def test_full_size_layers_under_bounds_checks(checked_lib, tmp_path):
+    """The full-size cases (every layer shape the benchmark times, and the
+    70B-class decode shapes) under the bounds-checked build: no access
+    outside its buffer."""
+    report = str(tmp_path / "bounds.txt")
+    cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+           "tests/test_gpu_w4a16.py", "tests/test_gpu_layers.py", "-k", "full_size"]
+    r = subprocess.run(cmd, cwd=ROOT, env=_env(checked_lib, report), capture_output=True, text=True, timeout=1800)
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
+    failures, unit, line, offset = (int(x) for x in open(report).read().split())
+    assert failures == 0, f"{failures} failed bounds checks, first in unit {unit} line {line} offset {offset}"
