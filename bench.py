@@ -444,8 +444,8 @@ def decode_line(R, dev, flush, pk, reps):
         torch.cuda.synchronize()
         ms = timed(g.replay, flush, reps) / copies
         gbytes = layer_bytes + 2 * M * K + 4 * M * N
-        # groups of 128: the tensor-core kernel for two or more tokens and for one token on 2^27 weights or more
-        kernel = "w4a16_mma_kernel" if (M >= 2 or N * K >= 1 << 27) else f"w4a16_gemv_kernel<{M}, R>"
+        # groups of 128: the tensor-core kernel for two or more tokens and for one token on 3 * 2^24 weights or more
+        kernel = "w4a16_mma_kernel" if (M >= 2 or N * K >= 3 << 24) else f"w4a16_gemv_kernel<{M}, R>"
         out["tokens"][str(M)] = {"kernel": kernel, "ms_per_layer": round(ms, 5), "bytes_per_layer": gbytes,
                                  "gbs": round(gbytes / (ms * 1e-3) / 1e9, 1),
                                  "frac_hbm": round(gbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3)}

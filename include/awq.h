@@ -340,7 +340,7 @@ AWQ_API awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count
    of 128: tensor-core products of bf16 x with the exact (q - z), summed in
    fp32 per group, then scaled by the group's step in fp32 (when `in` / 128 is
    even and scales_f16 and zeros_f16 are 4-byte aligned, for two or more
-   tokens, and for one token on a layer of at least 2^27 weights; otherwise
+   tokens, and for one token on a layer of at least 3 * 2^24 weights; otherwise
    the fp32 path). The order of every sum is fixed
    by the shapes and the device's SM count: repeated calls give the same
    bits. */

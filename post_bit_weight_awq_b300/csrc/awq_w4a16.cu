@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 #define AWQ_MMA_STAGES 3
 #endif
 #ifndef AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS
-#define AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS (int64_t(1) << 27)
+#define AWQ_MMA_MIN_ONE_TOKEN_WEIGHTS (int64_t(3) << 24)
 #endif
 #ifndef AWQ_MMA_WARPS
 #define AWQ_MMA_WARPS 12
