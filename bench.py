@@ -689,7 +689,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--oracle-rows", type=int, default=128, help="output rows of the cpu_baseline sample")
+    ap.add_argument("--oracle-rows", type=int, default=512, help="output rows of the cpu_baseline sample (about 10 s)")
     ap.add_argument("--reference-rows", type=int, default=64, help="output rows per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side", action="store_true", help="skip the entries of the other workloads")
