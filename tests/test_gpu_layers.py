@@ -165,6 +165,25 @@ def test_ragged_shapes(n, N, K):
     _check_pack(L, O.f32(res["s_best"]))
 
 
+def test_dead_channels_and_zero_rows():
+    """Degenerate data the method meets in practice: activation channels that
+    are zero for every token (their statistic is clamped to 1e-4, so at
+    alpha = 0.95 their scale is about 1.6e-4 of the others'), an all-zero
+    weight row (every group constant: the step floor) and an all-zero group
+    inside an otherwise normal row. Levels 1 to 3 against the oracle."""
+    L = workloads.make_layer("llama7b_q_proj", n_tok=256, out_features=384, in_features=640, seed=11)
+    L["X"] = L["X"].copy()
+    L["X"][:, [3, 200, 201, 639]] = 0.0
+    L["W"] = L["W"].copy()
+    L["W"][5, :] = 0.0
+    L["W"][7, 128:256] = 0.0
+    res = _oracle_losses(L["W"], L["X"])
+    q = _run_layer(L, capi.config())
+    np.testing.assert_allclose(q.mean_abs.cpu().numpy(), O.channel_importance(L["X"]), rtol=1e-5)
+    _check_levels(q.losses.cpu().numpy(), int(q.best_idx[0]), res["losses"])
+    _check_pack(L, O.f32(res["s_best"]))
+
+
 def test_loss_forms_agree():
     L = workloads.make_layer("llama7b_q_proj", n_tok=512, out_features=768, in_features=1024)
     a = _run_layer(L, capi.config(loss_form=capi.AWQ_LOSS_RESIDUAL)).losses.cpu().numpy()
