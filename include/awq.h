@@ -108,15 +108,32 @@ typedef enum {
 
 typedef enum { AWQ_BF16 = 0, AWQ_FP32 = 1 } awq_dtype;
 
-/* How the search scores each alpha. Both give the same number in exact
-   arithmetic, since X W_hat^T - X W^T = X (W_hat - W)^T.
+/* How the search scores each alpha. All give the same number in exact
+   arithmetic, since X W_hat^T - X W^T = X (W_hat - W)^T and
+   sum_t sum_r (X D^T)[t][r]^2 = sum_r D[r] (X^T X) D[r]^T.
    RESIDUAL:  one bf16 product per alpha, X (W_hat - W)^T, squared and summed
-              in the GEMM epilogue (default, fastest).
+              in the GEMM epilogue: 2 n_tok out in flops per alpha (default).
    REFERENCE: the output X W^T of the unquantised weight is computed once per
               output tile, kept resident in tensor memory, and subtracted from
               X W_hat^T in the epilogue, as the search_scale listing of the
-              first page writes it. */
-typedef enum { AWQ_LOSS_RESIDUAL = 0, AWQ_LOSS_REFERENCE = 1 } awq_loss_form;
+              first page writes it.
+   GRAM:      C = X^T X is formed once per search (fp32 accumulation, kept as
+              bf16, only the 256-channel blocks on and below the diagonal),
+              then each alpha costs out in^2 flops: P = D C over each output
+              tile's prefix of channel blocks, and the epilogue adds
+              P[r][c] * D[r][c]. Fewer flops than RESIDUAL when in < 2 n_tok.
+              The losses differ from RESIDUAL's by the bf16 rounding of C
+              (about 2^-9 / sqrt(in) relative when C's diagonal dominates).
+   AUTO:      GRAM when its tensor-core flops (C plus the alphas' products)
+              are below 0.7 of RESIDUAL's, else RESIDUAL (default). The choice
+              depends on the shape and n_grid only; awq_search_form reports it.
+              The per-kernel calls of awq_stages.h take AUTO as RESIDUAL. */
+typedef enum {
+  AWQ_LOSS_RESIDUAL = 0,
+  AWQ_LOSS_REFERENCE = 1,
+  AWQ_LOSS_GRAM = 2,
+  AWQ_LOSS_AUTO = 3
+} awq_loss_form;
 
 typedef struct {
   int32_t w_bit;            /* 4: bits per code (2..8 in the search; 2, 4 or 8 packed; 4 in the products) */
@@ -127,7 +144,7 @@ typedef struct {
   int32_t normalize;        /* 1: divide s by sqrt(max(s) * min(s)) */
   float sx_clamp_min;       /* 1e-4: sx is clamped from below before the power */
   float delta_floor;        /* 1e-5: lower bound of a group's step */
-  int32_t loss_form;        /* awq_loss_form */
+  int32_t loss_form;        /* awq_loss_form (AUTO) */
   uint32_t wait_timeout_ms; /* bound of each device-side wait; 0 = 2000 ms */
 } awq_config;
 
@@ -185,9 +202,15 @@ AWQ_API awq_status awq_act_stats_noalloc(const void* X, int32_t x_dtype, int64_t
 /* Device bytes of scratch that awq_search_layer needs. Host-only. It holds a
    status word, s and 1/s for every alpha ([n_grid][in] fp32 each), the bf16
    search operand for every alpha ([n_grid (+1 in REFERENCE form)][out][in]),
-   the per-tile partial sums and the operand-tile ready counters. */
+   the per-tile partial sums and the operand-tile ready counters; in GRAM
+   form also X^T X as bf16 [in][in] (X^T itself shares the operand's space). */
 AWQ_API awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, const awq_config* cfg,
                               size_t* bytes);
+
+/* The loss form awq_search_layer runs for this shape and configuration:
+   cfg->loss_form itself, or for AWQ_LOSS_AUTO the form it resolves to
+   (AWQ_LOSS_GRAM or AWQ_LOSS_RESIDUAL). Host-only. */
+AWQ_API awq_status awq_search_form(int64_t n_tok, int64_t out, int64_t in, const awq_config* cfg, int32_t* form);
 
 /* The alpha grid search of "AWQ: How Activation-Aware Quantization Saves
    4-bit LLMs", "How does AWQ protect channels without mixed precision?"

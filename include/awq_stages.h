@@ -81,8 +81,34 @@ AWQ_API awq_status awq_search_fused(const void* W, int32_t w_dtype, int64_t out,
                                     uint16_t* op, float* partials, uint32_t* ready, uint32_t* status,
                                     awq_stream_t stream);
 
-/* losses[i] = (sum of partials[i]) / (n_tok * out): fp32 sums per thread
-   over a fixed stride, fp64 across threads in a fixed tree (deterministic);
+/* Sizes of the GRAM form's buffers (elements): xt, the transposed copy of X
+   (bf16 [in][n_pad], n_pad = n_tok rounded up to 64); H (bf16 [in][in]);
+   partials per alpha (fp32). Host-only. */
+AWQ_API awq_status awq_gram_sizes(int64_t n_tok, int64_t out, int64_t in, int64_t* xt_elems, int64_t* h_elems,
+                                  int64_t* partials_per_alpha);
+
+/* H[c][j] = bf16(f * sum_t X[t][c] X[t][j]) for the 256-channel blocks
+   jb(j) <= jb(c) (f = 2 below the block diagonal, 1 on it; the blocks above
+   it are not written): the Gram matrix of the GRAM loss form, fp32
+   accumulation on tcgen05 tensor cores. X: device bf16 [n_tok][in]. xt:
+   device scratch of awq_gram_sizes' xt_elems bf16 (overwritten with X^T,
+   zero past n_tok). H: device bf16 [in][in]. status: as awq_search_gemm. */
+AWQ_API awq_status awq_gram_matrix(const void* X, int64_t n_tok, int64_t in, uint16_t* xt, uint16_t* H,
+                                   const awq_config* cfg, uint32_t* status, awq_stream_t stream);
+
+/* The GRAM form's per-alpha sums: for every alpha_i, partial sums of
+   sum_r sum_c op_i[r][c] sum_{j: jb(j) <= jb(c)} H[c][j] op_i[r][j]
+   = sum_r op_i[r] (X^T X) op_i[r]^T (op_i = bf16(W_hat_i - W) from
+   awq_fakequant, RESIDUAL form; H from awq_gram_matrix), as
+   partials[i][awq_gram_sizes' partials_per_alpha] (fp32). The alphas'
+   products run on tcgen05 tensor cores, 128 x 256 tiles over each tile's
+   prefix of channel blocks, their epilogue adding product x op_i. */
+AWQ_API awq_status awq_gram_loss(const uint16_t* op, int64_t out, int64_t in, const uint16_t* H,
+                                 const awq_config* cfg, float* partials, uint32_t* status, awq_stream_t stream);
+
+/* losses[i] = (sum of partials[i]) / (n_tok * out), partials as written by
+   awq_search_gemm (or, with cfg->loss_form GRAM, by awq_gram_loss): fp32
+   sums per thread over a fixed stride, fp64 across threads in a fixed tree (deterministic);
    best_idx = first i with the smallest fp32 loss (the strict "<" of the
    search_scale listing); s_best = s[best_idx]. A non-finite loss sets
    *status to AWQ_ERR_NONFINITE. */

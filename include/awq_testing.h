@@ -57,7 +57,8 @@ AWQ_API awq_status awq_search_fused_withhold_unit(const void* W, int32_t w_dtype
    access skipped, so an indexing error shows up as a count instead of a
    memory fault. awq_bounds_report returns the number of failed checks since
    the previous report and, for the first recorded one, the source unit
-   (1 awq_kernels.cu, 2 awq_search_gemm.cu, 3 awq_w4a16.cu; 0 if none), line
+   (1 awq_kernels.cu, 2 awq_search_gemm.cu, 3 awq_w4a16.cu, 4 awq_gram.cu;
+   0 if none), line
    and element offset, then clears the records; it synchronises the device.
    awq_bounds_selftest launches one check that fails by construction (the
    element one past `buf[0..n)`; nothing is written). Both return

@@ -28,6 +28,8 @@ AWQ_FP32 = 1
 
 AWQ_LOSS_RESIDUAL = 0
 AWQ_LOSS_REFERENCE = 1
+AWQ_LOSS_GRAM = 2
+AWQ_LOSS_AUTO = 3
 
 # limits of include/awq.h
 AWQ_W4A16_MAX_TOKENS = 8
@@ -42,6 +44,7 @@ EXPORTED = (
     "awq_act_stats",
     "awq_act_stats_noalloc",
     "awq_workspace_size",
+    "awq_search_form",
     "awq_search_layer",
     "awq_search_block_workspace_size",
     "awq_search_block",
@@ -118,6 +121,7 @@ def lib() -> ctypes.CDLL:
         "awq_act_stats": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _SZ, _P]),
         "awq_act_stats_noalloc": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P]),
         "awq_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _CFG, ctypes.POINTER(_SZ)]),
+        "awq_search_form": (ctypes.c_int, [_I64, _I64, _I64, _CFG, ctypes.POINTER(_I32)]),
         "awq_search_layer": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I32, _I64, _P, _CFG, _P, _P, _P, _P, _P, _SZ,
                                             _P]),
         "awq_search_block_workspace_size": (ctypes.c_int, [_I64, _P, _I32, _I64, _I32, _CFG, ctypes.POINTER(_SZ)]),
@@ -151,7 +155,7 @@ def _check(status: int, where: str) -> None:
 
 def config(**kw) -> AwqConfig:
     """Default configuration (4 bits, groups of 128, 20 alphas, zero point,
-    normalised scales, RESIDUAL loss form) with fields overridden by ``kw``."""
+    normalised scales, AUTO loss form) with fields overridden by ``kw``."""
     c = AwqConfig()
     lib().awq_config_default(ctypes.byref(c))
     for k, v in kw.items():
@@ -211,6 +215,14 @@ def awq_workspace_size(n_tok: int, out_features: int, in_features: int, cfg: Awq
     _check(lib().awq_workspace_size(n_tok, out_features, in_features, ctypes.byref(cfg), ctypes.byref(b)),
            "awq_workspace_size")
     return b.value
+
+
+def awq_search_form(n_tok: int, out_features: int, in_features: int, cfg: AwqConfig) -> int:
+    """The loss form awq_search_layer runs for this shape (AUTO resolved)."""
+    f = _I32(0)
+    _check(lib().awq_search_form(n_tok, out_features, in_features, ctypes.byref(cfg), ctypes.byref(f)),
+           "awq_search_form")
+    return f.value
 
 
 

@@ -25,6 +25,9 @@ STAGE_EXPORTED = (
     "awq_search_tiles",
     "awq_search_gemm",
     "awq_search_fused",
+    "awq_gram_sizes",
+    "awq_gram_matrix",
+    "awq_gram_loss",
     "awq_loss_select",
 )
 
@@ -54,6 +57,10 @@ def lib() -> ctypes.CDLL:
                                             ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
         "awq_search_gemm": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
         "awq_search_fused": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I64, _P, _P, _CFG, _P, _P, _P, _P, _P]),
+        "awq_gram_sizes": (ctypes.c_int, [_I64, _I64, _I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                                          ctypes.POINTER(_I64)]),
+        "awq_gram_matrix": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _CFG, _P, _P]),
+        "awq_gram_loss": (ctypes.c_int, [_P, _I64, _I64, _P, _CFG, _P, _P, _P]),
         "awq_loss_select": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _CFG, _P, _P, _P, _P, _P]),
         "awq_search_gemm_dump": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P, _I32, _P]),
         "awq_search_gemm_withhold_fill": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
@@ -110,6 +117,29 @@ def awq_search_fused(W, X, s, inv_s, cfg: AwqConfig, op, partials, ready, status
     wd = _dtype_code(W) if w_dtype is None else w_dtype
     _check(lib().awq_search_fused(_ptr(W), wd, N, K, _ptr(X), n, _ptr(s), _ptr(inv_s), ctypes.byref(cfg), _ptr(op),
                                   _ptr(partials), _ptr(ready), _ptr(status), _stream(stream)), "awq_search_fused")
+
+
+def awq_gram_sizes(n_tok: int, out_features: int, in_features: int):
+    """(xt elements, H elements, partial sums per alpha) of the GRAM loss form."""
+    xt, h, pa = _I64(0), _I64(0), _I64(0)
+    _check(lib().awq_gram_sizes(n_tok, out_features, in_features, ctypes.byref(xt), ctypes.byref(h), ctypes.byref(pa)),
+           "awq_gram_sizes")
+    return xt.value, h.value, pa.value
+
+
+def awq_gram_matrix(X, xt, H, cfg: AwqConfig, status, stream=None, *, n_tok=None, in_features=None) -> None:
+    n = X.shape[0] if n_tok is None else n_tok
+    K = X.shape[1] if in_features is None else in_features
+    _check(lib().awq_gram_matrix(_ptr(X), n, K, _ptr(xt), _ptr(H), ctypes.byref(cfg), _ptr(status), _stream(stream)),
+           "awq_gram_matrix")
+
+
+def awq_gram_loss(op, H, cfg: AwqConfig, partials, status, stream=None, *, out_features=None,
+                  in_features=None) -> None:
+    N = op.shape[-2] if out_features is None else out_features
+    K = op.shape[-1] if in_features is None else in_features
+    _check(lib().awq_gram_loss(_ptr(op), N, K, _ptr(H), ctypes.byref(cfg), _ptr(partials), _ptr(status),
+                               _stream(stream)), "awq_gram_loss")
 
 
 def awq_loss_select(partials, s, cfg: AwqConfig, losses, best_idx, s_best, status, stream=None, *, n_tok,

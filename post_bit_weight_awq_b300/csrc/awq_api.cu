@@ -4,6 +4,7 @@
 // carving, and the launch sequence of each step.
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "awq.h"
@@ -34,6 +35,34 @@ inline double search_flops(int64_t n_tok, int64_t out, int64_t in, const awq_con
 }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tensor-core flops of the GRAM form: X^T X over the 128 x 256 tiles on and
+// below the block diagonal, then per alpha the 128 x 256 tiles of every row
+// block over their prefix of channel blocks.
+double gram_flops(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg) {
+  const int64_t ct = in / kTileM, m = ct / 2, b = ct % 2;
+  const double h = 2.0 * (double)((m + 1) * (m + b)) * kTileM * kTileN * (double)gram_tokens_padded(n_tok);
+  const int64_t nC = (in + kTileN - 1) / kTileN, nR = (out + kTileM - 1) / kTileM;
+  double prefix = 0.0;
+  for (int64_t c = 0; c < nC; ++c) prefix += (double)std::min<int64_t>(kTileN * (c + 1), in);
+  return h + 2.0 * cfg.n_grid * (double)nR * kTileM * kTileN * prefix;
+}
+
+// The form a search runs: AUTO resolves to GRAM when that form's flops are
+// below 0.7 of the direct product's (the GRAM form adds X^T X, a transpose
+// and a separate fake-quant launch), else to RESIDUAL.
+int32_t resolve_form(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg) {
+  if (cfg.loss_form != AWQ_LOSS_AUTO) return cfg.loss_form;
+  return gram_flops(n_tok, out, in, cfg) < 0.7 * search_flops(n_tok, out, in, cfg) ? AWQ_LOSS_GRAM
+                                                                                 : AWQ_LOSS_RESIDUAL;
+}
+
+// The configuration a per-kernel stage call runs with: AUTO is RESIDUAL there.
+awq_config stage_cfg(const awq_config* cfg) {
+  awq_config c = *cfg;
+  if (c.loss_form == AWQ_LOSS_AUTO) c.loss_form = AWQ_LOSS_RESIDUAL;
+  return c;
+}
+
 // Largest sizes accepted: every index the kernels form stays below 2^31 per
 // matrix dimension, and the TMA coordinates are 32-bit.
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
@@ -43,7 +72,7 @@ awq_status check_cfg(const awq_config* cfg) {
   if (cfg->n_grid < 1 || cfg->n_grid > kMaxGrid) return AWQ_ERR_INVALID_ARG;
   if (cfg->group <= 0 || cfg->w_bit <= 0) return AWQ_ERR_INVALID_ARG;
   if (!(cfg->sx_clamp_min > 0.0f) || !(cfg->delta_floor > 0.0f)) return AWQ_ERR_INVALID_ARG;
-  if (cfg->loss_form != AWQ_LOSS_RESIDUAL && cfg->loss_form != AWQ_LOSS_REFERENCE) return AWQ_ERR_INVALID_ARG;
+  if (cfg->loss_form < AWQ_LOSS_RESIDUAL || cfg->loss_form > AWQ_LOSS_AUTO) return AWQ_ERR_INVALID_ARG;
   if (cfg->zero_point != 0 && cfg->zero_point != 1) return AWQ_ERR_INVALID_ARG;
   // groups of 32, 64 or 128 weights (one or two groups per lane run of the
   // quantiser kernels); 2 to 8 bits per code in the search, whose codes are
@@ -89,11 +118,14 @@ awq_status check_xdtype(int32_t x_dtype) {
 awq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? AWQ_OK : AWQ_ERR_CUDA; }
 
 struct SearchLayout {
-  size_t status, s, inv_s, op, partials, ready, row_acc, total;
+  size_t status, s, inv_s, op, partials, ready, row_acc, gram_h, total;
   int64_t mt, nt;
+  int64_t per_alpha;  // partial sums per alpha
 };
 
-SearchLayout search_layout(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg) {
+SearchLayout search_layout(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg_in) {
+  awq_config cfg = cfg_in;
+  cfg.loss_form = resolve_form(n_tok, out, in, cfg_in);
   SearchLayout L;
   const int64_t G = cfg.n_grid;
   const int64_t slots = cfg.loss_form == AWQ_LOSS_REFERENCE ? G + 1 : G;
@@ -106,14 +138,21 @@ SearchLayout search_layout(int64_t n_tok, int64_t out, int64_t in, const awq_con
   off = align_up(off + (size_t)G * in * 4, kAlign);
   L.inv_s = off;
   off = align_up(off + (size_t)G * in * 4, kAlign);
+  const bool gram = cfg.loss_form == AWQ_LOSS_GRAM;
+  // GRAM form: X^T (bf16 [in][n_pad]) lives in the operand's space until the fake-quant writes it
+  size_t op_bytes = (size_t)slots * out * in * 2;
+  if (gram && (size_t)gram_tokens_padded(n_tok) * in * 2 > op_bytes) op_bytes = (size_t)gram_tokens_padded(n_tok) * in * 2;
   L.op = off;
-  off = align_up(off + (size_t)slots * out * in * 2, kAlign);
+  off = align_up(off + op_bytes, kAlign);
+  L.per_alpha = gram ? gram_partials_per_alpha(out) : L.mt * L.nt * 4;
   L.partials = off;
-  off = align_up(off + (size_t)G * L.mt * L.nt * 4 * 4, kAlign);
+  off = align_up(off + (size_t)G * L.per_alpha * 4, kAlign);
   L.ready = off;
   off = align_up(off + fused_ready_words(G, L.nt) * 4, kAlign);
   L.row_acc = off;  // fp64 [G][out], used when per-row losses are asked for
   off = align_up(off + (size_t)G * out * 8, kAlign);
+  L.gram_h = off;  // GRAM form: bf16 [in][in]
+  if (gram) off = align_up(off + (size_t)in * in * 2, kAlign);
   L.total = off;
   return L;
 }
@@ -230,7 +269,7 @@ void awq_config_default(awq_config* cfg) {
   cfg->normalize = 1;
   cfg->sx_clamp_min = 1e-4f;
   cfg->delta_floor = 1e-5f;
-  cfg->loss_form = AWQ_LOSS_RESIDUAL;
+  cfg->loss_form = AWQ_LOSS_AUTO;
   cfg->wait_timeout_ms = 0;
 }
 
@@ -281,6 +320,16 @@ awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, const awq_
   st = check_dims(n_tok, out, in);
   if (st != AWQ_OK) return st;
   *bytes = search_layout(n_tok, out, in, *cfg).total;
+  return AWQ_OK;
+}
+
+awq_status awq_search_form(int64_t n_tok, int64_t out, int64_t in, const awq_config* cfg, int32_t* form) {
+  if (form == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  *form = resolve_form(n_tok, out, in, *cfg);
   return AWQ_OK;
 }
 
@@ -346,7 +395,8 @@ awq_status awq_search_fused(const void* W, int32_t w_dtype, int64_t out, int64_t
     return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
-  if (cfg->loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
+  const awq_config c = stage_cfg(cfg);
+  if (c.loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
   st = check_wdtype(w_dtype);
   if (st != AWQ_OK) return st;
   st = check_dims(n_tok, out, in);
@@ -354,7 +404,7 @@ awq_status awq_search_fused(const void* W, int32_t w_dtype, int64_t out, int64_t
   if (!aligned16(W) || !aligned16(X) || !aligned16(s) || !aligned16(inv_s) || !aligned16(op) ||
       !aligned16(partials) || !aligned16(ready) || !aligned16(status))
     return AWQ_ERR_MISALIGNED;
-  return from_cuda(launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, s, inv_s, out, *cfg, op, partials,
+  return from_cuda(launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, s, inv_s, out, c, op, partials,
                                        ready, status, (cudaStream_t)stream));
 }
 
@@ -368,7 +418,8 @@ awq_status awq_search_fused_withhold_unit(const void* W, int32_t w_dtype, int64_
     return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
-  if (cfg->loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
+  const awq_config c = stage_cfg(cfg);
+  if (c.loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
   st = check_wdtype(w_dtype);
   if (st != AWQ_OK) return st;
   st = check_dims(n_tok, out, in);
@@ -376,7 +427,7 @@ awq_status awq_search_fused_withhold_unit(const void* W, int32_t w_dtype, int64_
   if (!aligned16(W) || !aligned16(X) || !aligned16(s) || !aligned16(inv_s) || !aligned16(op) ||
       !aligned16(partials) || !aligned16(ready) || !aligned16(status))
     return AWQ_ERR_MISALIGNED;
-  return from_cuda(launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, s, inv_s, out, *cfg, op, partials,
+  return from_cuda(launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, s, inv_s, out, c, op, partials,
                                        ready, status, (cudaStream_t)stream, nullptr, 0));
 }
 
@@ -385,7 +436,8 @@ awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const 
                                 int32_t single_cta, awq_stream_t stream) {
   AWQ_TRACE("awq_search_gemm_dump");
   if (single_cta != 0 && single_cta != 1) return AWQ_ERR_INVALID_ARG;
-  if (cfg != nullptr && cfg->loss_form != AWQ_LOSS_RESIDUAL) return AWQ_ERR_UNSUPPORTED;
+  if (cfg != nullptr && cfg->loss_form != AWQ_LOSS_RESIDUAL && cfg->loss_form != AWQ_LOSS_AUTO)
+    return AWQ_ERR_UNSUPPORTED;
   if (X == nullptr || op == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
@@ -424,8 +476,45 @@ awq_status awq_loss_select(const float* partials, int64_t n_tok, int64_t out, in
   if (st != AWQ_OK) return st;
   if (!aligned16(partials) || !aligned16(s) || !aligned16(s_best)) return AWQ_ERR_MISALIGNED;
   const int64_t mt = (n_tok + kTileM - 1) / kTileM, nt = (out + kTileN - 1) / kTileN;
-  return from_cuda(launch_loss_select(partials, cfg->n_grid, mt * nt * 4, n_tok, out, s, in, losses, best_idx,
+  const int64_t per_alpha = cfg->loss_form == AWQ_LOSS_GRAM ? gram_partials_per_alpha(out) : mt * nt * 4;
+  return from_cuda(launch_loss_select(partials, cfg->n_grid, per_alpha, n_tok, out, s, in, losses, best_idx,
                                       s_best, status, (cudaStream_t)stream));
+}
+
+awq_status awq_gram_sizes(int64_t n_tok, int64_t out, int64_t in, int64_t* xt_elems, int64_t* h_elems,
+                          int64_t* partials_per_alpha) {
+  if (xt_elems == nullptr || h_elems == nullptr || partials_per_alpha == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  *xt_elems = gram_tokens_padded(n_tok) * in;
+  *h_elems = in * in;
+  *partials_per_alpha = gram_partials_per_alpha(out);
+  return AWQ_OK;
+}
+
+awq_status awq_gram_matrix(const void* X, int64_t n_tok, int64_t in, uint16_t* xt, uint16_t* H,
+                           const awq_config* cfg, uint32_t* status, awq_stream_t stream) {
+  AWQ_TRACE("awq_gram_matrix");
+  if (X == nullptr || xt == nullptr || H == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(n_tok, 1, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(X) || !aligned16(xt) || !aligned16(H) || !aligned16(status)) return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_gram_matrix((const uint16_t*)X, n_tok, in, xt, H, status, cfg->wait_timeout_ms,
+                                      (cudaStream_t)stream));
+}
+
+awq_status awq_gram_loss(const uint16_t* op, int64_t out, int64_t in, const uint16_t* H, const awq_config* cfg,
+                         float* partials, uint32_t* status, awq_stream_t stream) {
+  AWQ_TRACE("awq_gram_loss");
+  if (op == nullptr || H == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(1, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(op) || !aligned16(H) || !aligned16(partials) || !aligned16(status)) return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_gram_loss(op, out, in, *cfg, H, partials, status, (cudaStream_t)stream));
 }
 
 awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t in, const void* X,
@@ -517,7 +606,9 @@ awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, c
                       const float* mean_abs, const awq_config& c, float* losses, int32_t* best_idx, float* s_best,
                       uint8_t* base, const SearchLayout& L, cudaStream_t s, bool clear_status,
                       float* row_losses) {
-  const awq_config* cfg = &c;
+  awq_config resolved = c;
+  resolved.loss_form = resolve_form(n_tok, out, in, c);
+  const awq_config* cfg = &resolved;
   uint32_t* status = (uint32_t*)(base + L.status);
   float* sc = (float*)(base + L.s);
   float* inv = (float*)(base + L.inv_s);
@@ -531,7 +622,13 @@ awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, c
   if (e == cudaSuccess && row_acc != nullptr) e = cudaMemsetAsync(row_acc, 0, (size_t)cfg->n_grid * out * 8, s);
   if (e == cudaSuccess) e = launch_alpha_scales(mean_abs, in, *cfg, sc, inv, s);
   const double flops = search_flops(n_tok, out, in, *cfg);
-  if (cfg->loss_form == AWQ_LOSS_RESIDUAL && flops < kLargeSearchFlops) {
+  if (cfg->loss_form == AWQ_LOSS_GRAM) {
+    // X^T X once (X^T in the operand's space), then the fake-quant, then the alphas' products against it
+    uint16_t* H = (uint16_t*)(base + L.gram_h);
+    if (e == cudaSuccess) e = launch_gram_matrix((const uint16_t*)X, n_tok, in, op, H, status, cfg->wait_timeout_ms, s);
+    if (e == cudaSuccess) e = launch_fakequant(W, w_dtype, out, in, sc, inv, *cfg, op, s);
+    if (e == cudaSuccess) e = launch_gram_loss(op, out, in, *cfg, H, partials, status, s, row_acc);
+  } else if (cfg->loss_form == AWQ_LOSS_RESIDUAL && flops < kLargeSearchFlops) {
     // fake-quant runs inside the search kernel, ahead of the products that consume it
     if (e == cudaSuccess)
       e = launch_search_fused(W, w_dtype, (const uint16_t*)X, n_tok, in, sc, inv, out, *cfg, op, partials, ready,
@@ -547,8 +644,8 @@ awq_status run_search(const void* W, int32_t w_dtype, int64_t out, int64_t in, c
       e = launch_search_gemm((const uint16_t*)X, n_tok, in, op, out, *cfg, partials, status, s, nullptr, 0, 1, row_acc);
   }
   if (e == cudaSuccess)
-    e = launch_loss_select(partials, cfg->n_grid, L.mt * L.nt * 4, n_tok, out, sc, in, losses, best_idx, s_best,
-                           status, s);
+    e = launch_loss_select(partials, cfg->n_grid, L.per_alpha, n_tok, out, sc, in, losses, best_idx, s_best, status,
+                           s);
   if (e == cudaSuccess && row_acc != nullptr) e = launch_row_losses(row_acc, cfg->n_grid, out, n_tok, row_losses, s);
   return from_cuda(e);
 }
@@ -783,12 +880,13 @@ awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_
 awq_status awq_bounds_report(uint64_t* failures, int32_t* unit, uint64_t* line, uint64_t* offset) {
   if (failures == nullptr || unit == nullptr || line == nullptr || offset == nullptr) return AWQ_ERR_INVALID_ARG;
 #ifdef AWQ_CHECKED
-  cudaError_t (*const take[3])(unsigned long long*) = {take_oob_kernels, take_oob_search, take_oob_w4a16};
+  cudaError_t (*const take[4])(unsigned long long*) = {take_oob_kernels, take_oob_search, take_oob_w4a16,
+                                                       take_oob_gram};
   *failures = 0;
   *unit = 0;
   *line = 0;
   *offset = 0;
-  for (int u = 0; u < 3; ++u) {
+  for (int u = 0; u < 4; ++u) {
     unsigned long long rec[3] = {0, 0, 0};
     if (take[u](rec) != cudaSuccess) return AWQ_ERR_CUDA;
     if (rec[0] != 0 && *unit == 0) {

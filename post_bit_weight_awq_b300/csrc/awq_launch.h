@@ -2,6 +2,7 @@
 // kernel translation units. Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,6 +29,10 @@ cudaError_t sm_count(int* sms);
 // Allow `bytes` of dynamic shared memory for kernel `func` on the current
 // device (the attribute is set once per kernel, device and size increase).
 cudaError_t ensure_dynamic_smem(const void* func, int bytes);
+// TMA map of a bf16 tensor of rank 2 or 3 (dims innermost first, densely
+// packed), 128-byte swizzle, zero fill outside the extents. False if the
+// driver entry point is missing or the map cannot be encoded.
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint32_t* box);
 
 inline int stats_strips(int64_t in) { return (int)((in + 255) / 256); }
 // Tokens per statistics chunk: the token range split into
@@ -102,8 +107,34 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int
 cudaError_t take_oob_kernels(unsigned long long* out);
 cudaError_t take_oob_search(unsigned long long* out);
 cudaError_t take_oob_w4a16(unsigned long long* out);
+cudaError_t take_oob_gram(unsigned long long* out);
 cudaError_t launch_bounds_selftest(float* buf, int n, cudaStream_t st);
 #endif
+
+// Gram form of the search loss (awq_gram.cu). kGramShares: equal shares of
+// each band's work, one per CTA (fixed, so that the result does not depend on
+// the GPU); kGramBandRows: 128-row blocks of the operand per band.
+constexpr int kGramShares = 148;
+#ifndef AWQ_GRAM_BAND_ROWS
+#define AWQ_GRAM_BAND_ROWS 16
+#endif
+constexpr int kGramBandRows = AWQ_GRAM_BAND_ROWS;
+inline int64_t gram_tokens_padded(int64_t n_tok) { return (n_tok + 63) / 64 * 64; }
+inline int64_t gram_bands(int64_t N) {
+  const int64_t row_blocks = (N + kTileM - 1) / kTileM;
+  return (row_blocks + kGramBandRows - 1) / kGramBandRows;
+}
+// fp32 partial sums of one alpha: [bands][kGramShares][8 epilogue warps].
+inline int64_t gram_partials_per_alpha(int64_t N) { return gram_bands(N) * kGramShares * 8; }
+// H (bf16 [K][K], blocks on and below the 256-channel block diagonal) of X
+// (bf16 [n_tok][K], K a multiple of 128), through the transposed copy xt
+// (bf16 [K][gram_tokens_padded(n_tok)], overwritten).
+cudaError_t launch_gram_matrix(const uint16_t* X, int64_t n_tok, int64_t K, uint16_t* xt, uint16_t* H,
+                               uint32_t* status, uint32_t wait_timeout_ms, cudaStream_t st);
+// partials[a][...] of sum_r D_a[r] C D_a[r]^T, D_a = op slot a (bf16 [n_grid][N][K]).
+// row_acc: if not null, fp64 [n_grid][N] to which each row's sum is added.
+cudaError_t launch_gram_loss(const uint16_t* op, int64_t N, int64_t K, const awq_config& cfg, const uint16_t* H,
+                             float* partials, uint32_t* status, cudaStream_t st, double* row_acc = nullptr);
 
 // W_hat[r][k] = bf16((q[r][k] - z[r][g]) * scale[r][g]) for the whole packed
 // layer (bf16 [N][K]), the operand of the prefill product.

@@ -63,8 +63,42 @@ def test_config_default(lib):
     c = capi.config()
     assert (c.w_bit, c.group, c.n_grid, c.zero_point, c.normalize) == (4, 128, 20, 1, 1)
     assert c.sx_clamp_min == pytest.approx(1e-4) and c.delta_floor == pytest.approx(1e-5)
-    assert c.loss_form == capi.AWQ_LOSS_RESIDUAL
+    assert c.loss_form == capi.AWQ_LOSS_AUTO
     assert ctypes.sizeof(capi.AwqConfig) == 36
+
+
+@pytest.mark.parametrize("shape,form", [
+    ((128, 256, 256), "RESIDUAL"),         # tiny linear: X^T X costs more than the products it saves
+    ((4096, 4096, 4096), "GRAM"),         # Llama-7B q_proj: in == n_tok, about half the flops
+    ((4096, 11008, 4096), "GRAM"),        # Llama-7B up
+    ((4096, 4096, 11008), "RESIDUAL"),    # Llama-7B down: in > n_tok, the Gram form costs more
+    ((16384, 13824, 5120), "GRAM"),       # 13B-class up_proj
+    ((16384, 28672, 8192), "GRAM"),       # 70B-class MLP
+])
+def test_auto_form_resolution(lib, shape, form):
+    """AUTO picks the GRAM form exactly when its tensor-core flops (X^T X over the tiles on and below the block
+    diagonal, then per alpha each 128-row block over its prefix of 256-channel blocks) are below 0.7 of the
+    direct product's 2 n_grid n_tok out in; the workspace is sized for the form it picks."""
+    n, N, K = shape
+    cfg = capi.config()
+    assert capi.awq_search_form(n, N, K, cfg) == getattr(capi, "AWQ_LOSS_" + form)
+    assert capi.awq_workspace_size(n, N, K, cfg) == capi.awq_workspace_size(
+        n, N, K, capi.config(loss_form=getattr(capi, "AWQ_LOSS_" + form)))
+    for f in (capi.AWQ_LOSS_RESIDUAL, capi.AWQ_LOSS_REFERENCE, capi.AWQ_LOSS_GRAM):
+        assert capi.awq_search_form(n, N, K, capi.config(loss_form=f)) == f
+    # the rule written out from the tiling
+    ct = K // 128
+    m, b = ct // 2, ct % 2
+    n_pad = (n + 63) // 64 * 64
+    h = 2.0 * (m + 1) * (m + b) * 128 * 256 * n_pad
+    nC, nR = (K + 255) // 256, (N + 127) // 128
+    loss = 2.0 * 20 * nR * 128 * 256 * sum(min(256 * (c + 1), K) for c in range(nC))
+    assert (h + loss < 0.7 * 2.0 * 20 * n * N * K) == (form == "GRAM")
+
+
+def test_auto_form_rejects_unknown_forms(lib):
+    with pytest.raises(capi.AwqError):
+        capi.awq_search_form(128, 256, 256, capi.config(loss_form=4))
 
 
 def test_status_strings(lib):
@@ -83,10 +117,14 @@ def test_packed_bytes_matches_13b_arithmetic(lib):
 def test_workspace_sizes(lib):
     cfg = capi.config()
     n, N, K = 4096, 4096, 4096
-    ws = capi.awq_workspace_size(n, N, K, cfg)
+    ws = capi.awq_workspace_size(n, N, K, capi.config(loss_form=capi.AWQ_LOSS_RESIDUAL))
     assert ws >= 20 * N * K * 2 + 2 * 20 * K * 4
     ref = capi.awq_workspace_size(n, N, K, capi.config(loss_form=capi.AWQ_LOSS_REFERENCE))
     assert ref >= ws + N * K * 2
+    # the GRAM form adds X^T X (bf16 [in][in]); X^T itself shares the operands' space
+    gram = capi.awq_workspace_size(n, N, K, capi.config(loss_form=capi.AWQ_LOSS_GRAM))
+    assert gram >= ws + K * K * 2
+    assert capi.awq_workspace_size(n, N, K, cfg) == gram  # AUTO picks GRAM here
     assert capi.awq_act_stats_workspace_size(n, K) >= (n // 128) * K * 4
     mt, nt, tm, tn = capi_testing.awq_search_tiles(n, N, cfg)
     assert (mt, nt) == ((n + tm - 1) // tm, (N + tn - 1) // tn)
