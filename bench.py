@@ -58,6 +58,23 @@ def source_digest(files):
 
 GEMM_SOURCES = ["post_bit_weight_awq_b300/csrc/awq_search_gemm.cu", "post_bit_weight_awq_b300/csrc/awq_device.cuh",
                 "post_bit_weight_awq_b300/csrc/awq_quant.cuh"]
+GRAM_SOURCES = ["post_bit_weight_awq_b300/csrc/awq_gram.cu", "post_bit_weight_awq_b300/csrc/awq_device.cuh",
+                "post_bit_weight_awq_b300/csrc/awq_launch.h"]
+
+
+def gram_prefix_area(K):
+    """S = sum over 256-channel blocks cb of (channels in cb) x (channels in blocks 0..cb): the entries of
+    X^T X on and below the block diagonal."""
+    nC = (K + 255) // 256
+    return sum(min(256, K - 256 * c) * min(256 * (c + 1), K) for c in range(nC))
+
+
+def search_flops(n, N, K, G, form):
+    """Algorithmic tensor-core flops of one search: the direct products 2 G n N K, or for the GRAM form X^T X
+    on and below the block diagonal (2 n S) plus the alphas' products over the block prefixes (2 G N S)."""
+    if form == "gram":
+        return 2.0 * gram_prefix_area(K) * (n + G * N)
+    return 2.0 * G * n * N * K
 
 
 def profiled_traffic(kernel_tag, workload):
@@ -72,7 +89,8 @@ def profiled_traffic(kernel_tag, workload):
                   text, flags=re.S)
     if not m:
         return None
-    if m.group(2) != workload or m.group(3) != source_digest(GEMM_SOURCES):
+    sources = GRAM_SOURCES if kernel_tag == "gram" else GEMM_SOURCES
+    if m.group(2) != workload or m.group(3) != source_digest(sources):
         return None
     return int(m.group(1))
 
@@ -266,7 +284,11 @@ class LayerRun:
         self.qw = torch.empty(N, K // 8, dtype=torch.int32, device=dev)
         self.sc = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
         self.zr = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
-        self.flops = 2.0 * G * n * N * K
+        forms = {capi.AWQ_LOSS_RESIDUAL: "residual", capi.AWQ_LOSS_REFERENCE: "reference", capi.AWQ_LOSS_GRAM: "gram"}
+        self.form = forms[capi.awq_search_form(n, N, K, cfg)]
+        self.flops = search_flops(n, N, K, G, self.form)
+        # the dominant kernel's flops: the GRAM form's alpha products, else the whole direct search
+        self.loss_flops = 2.0 * G * N * gram_prefix_area(K) if self.form == "gram" else self.flops
 
     def step(self, ev=None):
         """awq_act_stats, awq_search_layer, awq_quantize_pack on the current stream (events between the calls)."""
@@ -328,6 +350,12 @@ def stage_kernels(R, flush, reps):
     best = torch.empty(1, dtype=torch.int32, device=dev)
     s_best = torch.empty(K, dtype=torch.float32, device=dev)
     capi_testing.awq_alpha_scales(R.mean_abs, R.cfg, s, inv)
+    gcfg = capi.config(loss_form=capi.AWQ_LOSS_GRAM)
+    xt_elems, h_elems, per_alpha = capi_testing.awq_gram_sizes(n, N, K)
+    xt = torch.empty(xt_elems, dtype=torch.bfloat16, device=dev)
+    H = torch.empty(h_elems, dtype=torch.bfloat16, device=dev)
+    gparts = torch.empty(G, per_alpha, dtype=torch.float32, device=dev)
+    capi_testing.awq_gram_matrix(R.X, xt, H, gcfg, status)
     calls = {
         "stats": lambda: capi.awq_act_stats(R.X, R.mean_abs, R.ws),
         "alpha_scales": lambda: capi_testing.awq_alpha_scales(R.mean_abs, R.cfg, s, inv),
@@ -338,6 +366,8 @@ def stage_kernels(R, flush, reps):
         "loss_select": lambda: capi_testing.awq_loss_select(parts, s, R.cfg, losses, best, s_best, status, n_tok=n,
                                                             out_features=N, in_features=K),
         "fused_search": lambda: capi_testing.awq_search_fused(R.W, R.X, s, inv, R.cfg, op, parts, ready, status),
+        "gram_matrix": lambda: capi_testing.awq_gram_matrix(R.X, xt, H, gcfg, status),
+        "gram_loss": lambda: capi_testing.awq_gram_loss(op, H, gcfg, gparts, status),
     }
     out = {}
     torch.cuda.synchronize()
@@ -345,12 +375,12 @@ def stage_kernels(R, flush, reps):
     for nm, fn in calls.items():
         fn()
         torch.cuda.synchronize()
-        short = nm not in ("search_gemm", "fused_search")
+        short = nm not in ("search_gemm", "fused_search", "gram_loss")
         # the short kernels: a few untimed launches bring the clock up from idle, then the median of many
         out[nm] = timed(fn, flush, max(reps, 15) if short else reps, warm=5 if short else 0)
     if int(status[0]) != 0:
         raise RuntimeError("device status " + capi.status_string(int(status[0])))
-    del op
+    del op, xt, H
     return out
 
 
@@ -363,13 +393,25 @@ def fractions(R, ms, pk):
         if nm in hb:
             gbs = hb[nm] / (t * 1e-3) / 1e9
             e.update({"bytes": hb[nm], "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)})
-        if nm in ("fused_search", "search_gemm"):
-            tf = R.flops / (t * 1e-3) / 1e12
+        if nm in ("fused_search", "search_gemm", "gram_loss", "gram_matrix"):
+            f = {"gram_loss": 2.0 * R.G * R.N * gram_prefix_area(R.K), "gram_matrix": 2.0 * R.n * gram_prefix_area(R.K)}
+            tf = f.get(nm, 2.0 * R.G * R.n * R.N * R.K) / (t * 1e-3) / 1e12
             e.update({"tflops": round(tf, 1), "frac_bf16_burst": round(tf / pk["bf16_tflops"], 3)})
             if pk.get("bf16_tflops_sustained"):
                 e["frac_bf16_sustained"] = round(tf / pk["bf16_tflops_sustained"], 3)
         d[nm] = e
     return d
+
+
+def search_path(R):
+    """What awq_search_layer runs for this layer (the form AUTO resolved to, then the kernels)."""
+    from post_bit_weight_awq_b300 import capi_testing
+
+    if R.form == "gram":
+        return "gram: X^T X, fake-quant launch, D H^T products over block prefixes"
+    if R.flops < capi_testing.AWQ_SEARCH_FUSED_MAX_FLOPS:
+        return f"{R.form}: fused fake-quant + CTA-pair products"
+    return f"{R.form}: fake-quant launch + single-CTA products"
 
 
 def side_workload(name, dev, flush, pk, reps):
@@ -402,8 +444,7 @@ def side_workload(name, dev, flush, pk, reps):
             "stats_ms": round(st[0], 4), "stats_frac_hbm": round(hb["stats"] / (st[0] * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
             "search_ms": round(st[1], 4), "search_tflops": round(tf, 1),
             "search_frac_bf16_burst": round(tf / pk["bf16_tflops"], 3),
-            "search_path": ("fused fake-quant + CTA-pair products" if R.flops < capi_testing.AWQ_SEARCH_FUSED_MAX_FLOPS
-                            else "fake-quant launch + single-CTA products"),
+            "search_path": search_path(R), "search_flops": R.flops,
             "pack_ms": round(st[2], 4), "pack_frac_hbm": round(hb["pack"] / (st[2] * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
             "parity_vs_oracle": R.parity()})
         del R
@@ -571,10 +612,13 @@ def gpu_arm(args, rank, world, local_rank):
 
     # each kernel alone (stage calls), for the per-kernel rooflines
     kern = fractions(R, stage_kernels(R, flush, max(3, args.steps // 4)), pk)
-    fused_path = flops < capi_testing.AWQ_SEARCH_FUSED_MAX_FLOPS
-    search_kernel = "fused_search" if fused_path else "search_gemm"
+    fused_path = R.form != "gram" and flops < capi_testing.AWQ_SEARCH_FUSED_MAX_FLOPS
+    search_kernel = "gram_loss" if R.form == "gram" else ("fused_search" if fused_path else "search_gemm")
+    traffic_tag = "gram" if R.form == "gram" else ("fused" if fused_path else "single")
     search_ms = kern[search_kernel]["ms"]
-    achieved = flops / (search_ms * 1e-3) / 1e12
+    kernel_flops = R.loss_flops
+    achieved = kernel_flops / (search_ms * 1e-3) / 1e12
+    form, path = R.form, search_path(R)
     long_step = ms_step > 100.0  # a timed region of seconds settles at the power cap
     sustained = pk.get("bf16_tflops_sustained")
     peak, peak_kind = (sustained, "sustained") if (long_step and sustained) else (pk["bf16_tflops"], "burst")
@@ -603,26 +647,30 @@ def gpu_arm(args, rank, world, local_rank):
                          f"[0,{args.oracle_rows}) ({tr:.1f} s), the rows scaled by out/rows = {scale:g} to one layer"}
 
     kernel_names = {"fused_search": "search_gemm_pair_kernel<fused> (quantiser warps + tcgen05 pair products)",
-                    "search_gemm": "search_gemm_kernel (tcgen05 single-CTA products; fake-quant launched before it)"}
+                    "search_gemm": "search_gemm_kernel (tcgen05 single-CTA products; fake-quant launched before it)",
+                    "gram_loss": "gram_kernel<LOSS> (tcgen05 single-CTA D_i H^T tiles over channel-block prefixes, "
+                                 "stream-K shares; fake-quant and X^T X launched before it)"}
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "layer": name, "W": [N, K], "X": [n, K], "w_dtype": L["w_dtype"],
-                   "n_grid": G, "group": 128, "loss_form": "residual", "parallelism": f"replicas{world}",
+                   "n_grid": G, "group": 128, "loss_form": f"auto -> {form}", "search_path": path,
+                   "search_flops": flops, "parallelism": f"replicas{world}",
                    "calls": "awq_act_stats + awq_search_layer + awq_quantize_pack",
                    "launch": "the three calls captured as one CUDA graph and replayed",
                    "l2": "inputs larger than L2, and L2 flushed between steps (512 MiB write outside the timed events)"},
         "roofline": {"bound": "tensor", "kernel": kernel_names[search_kernel], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
-                     "traffic": profiled_traffic("fused" if fused_path else "single", args.workload),
-                     "peak_source": f"{pk['source']} bf16 {peak_kind}", "algorithmic_flops_per_launch": flops,
+                     "traffic": profiled_traffic(traffic_tag, args.workload),
+                     "peak_source": f"{pk['source']} bf16 {peak_kind}", "algorithmic_flops_per_launch": kernel_flops,
                      "launch_ms": search_ms},
         "calls": {k: round(v, 4) for k, v in calls_ms.items()},
         "kernels": kern,
         "e2e": e2e,
-        # stats, alpha scales, [fake-quant,] search product, loss reduce, select, pack
-        "gpu_launches": (6 if fused_path else 7) * args.steps,
+        # stats, alpha scales, [fake-quant,] search product, loss reduce, select, pack; the GRAM form adds
+        # the transpose and X^T X
+        "gpu_launches": (9 if form == "gram" else (6 if fused_path else 7)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
         "parity_vs_oracle": parity,
