@@ -664,6 +664,10 @@ def gpu_arm(args, rank, world, local_rank):
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 3),
                      "traffic": profiled_traffic(traffic_tag, args.workload),
                      "peak_source": f"{pk['source']} bf16 {peak_kind}", "algorithmic_flops_per_launch": kernel_flops,
+                     "direct_form_flops": 2.0 * G * n * N * K,
+                     "note": ("GRAM form: the same per-alpha loss as sum_r D[r] (X^T X) D[r]^T; the launch's flops are "
+                              "2 n_grid out S (S = entries of X^T X on and below the 256-channel block diagonal), "
+                              "not the direct form's 2 n_grid n_tok out in" if R.form == "gram" else None),
                      "launch_ms": search_ms},
         "calls": {k: round(v, 4) for k, v in calls_ms.items()},
         "kernels": kern,

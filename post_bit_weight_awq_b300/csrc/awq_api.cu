@@ -144,7 +144,7 @@ SearchLayout search_layout(int64_t n_tok, int64_t out, int64_t in, const awq_con
   if (gram && (size_t)gram_tokens_padded(n_tok) * in * 2 > op_bytes) op_bytes = (size_t)gram_tokens_padded(n_tok) * in * 2;
   L.op = off;
   off = align_up(off + op_bytes, kAlign);
-  L.per_alpha = gram ? gram_partials_per_alpha(out) : L.mt * L.nt * 4;
+  L.per_alpha = gram ? gram_partials_per_alpha(out, in) : L.mt * L.nt * 4;
   L.partials = off;
   off = align_up(off + (size_t)G * L.per_alpha * 4, kAlign);
   L.ready = off;
@@ -476,7 +476,7 @@ awq_status awq_loss_select(const float* partials, int64_t n_tok, int64_t out, in
   if (st != AWQ_OK) return st;
   if (!aligned16(partials) || !aligned16(s) || !aligned16(s_best)) return AWQ_ERR_MISALIGNED;
   const int64_t mt = (n_tok + kTileM - 1) / kTileM, nt = (out + kTileN - 1) / kTileN;
-  const int64_t per_alpha = cfg->loss_form == AWQ_LOSS_GRAM ? gram_partials_per_alpha(out) : mt * nt * 4;
+  const int64_t per_alpha = cfg->loss_form == AWQ_LOSS_GRAM ? gram_partials_per_alpha(out, in) : mt * nt * 4;
   return from_cuda(launch_loss_select(partials, cfg->n_grid, per_alpha, n_tok, out, s, in, losses, best_idx,
                                       s_best, status, (cudaStream_t)stream));
 }
@@ -488,7 +488,7 @@ awq_status awq_gram_sizes(int64_t n_tok, int64_t out, int64_t in, int64_t* xt_el
   if (st != AWQ_OK) return st;
   *xt_elems = gram_tokens_padded(n_tok) * in;
   *h_elems = in * in;
-  *partials_per_alpha = gram_partials_per_alpha(out);
+  *partials_per_alpha = gram_partials_per_alpha(out, in);
   return AWQ_OK;
 }
 

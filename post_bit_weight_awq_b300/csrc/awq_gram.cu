@@ -38,18 +38,18 @@
 // columns, so that the chain of tensor-memory loads per warp is short).
 // Every wait is bounded.
 //
-// Work of the loss kernel: the tiles (alpha a, row block rb of 128 output
-// rows, column block cb of 256 channels) cost 4 (cb + 1) k-blocks of 64
-// (fewer for a last, half block). They are taken alpha by alpha, and within
-// an alpha in bands of about kGramBandRows row blocks (the band's rows of D_i and the
-// lower triangle of H stay in L2 while the band is worked on); a band's
-// k-blocks, row block by row block and within a row in the zigzag order of
-// column blocks 0, nC-1, 1, nC-2, ..., are cut into kGramShares equal shares,
-// one per CTA (stream-K). A tile cut between two shares is accumulated in two parts;
-// the loss is linear in the accumulator, so each part's epilogue adds its
-// share of the tile's sum. Each share writes one fp32 sum per epilogue warp:
-// partials [n_grid][bands][kGramShares][8]. The cut points depend only on the
-// shape, so the result does not depend on the GPU.
+// Work of the loss kernel: the tile (alpha a, row block rb of 128 output
+// rows, column block cb of 256 channels) costs 4 (cb + 1) k-blocks of 64
+// (fewer for a last, half block). An item is row block rb with the column
+// blocks cb and nC-1-cb, so every item costs 4 (nC + 1) k-blocks (an odd
+// middle block is an item of its own). Items are dealt to the CTAs round
+// robin in the order (alpha, group of kGramRowGroup row blocks, column-block
+// pair, row block): neighbouring CTAs take the same pair for neighbouring
+// rows, all CTAs start their items together and take equally long, so the
+// CTAs of a group load the same tiles of H at the same time, which the L2
+// serves as one stream instead of many. Each item writes one fp32 sum per
+// epilogue warp: partials [n_grid][items per alpha][8]. The order of all
+// sums is fixed by the shape, so the result does not depend on the GPU.
 //
 // Rounding: C is accumulated in fp32 over all tokens and rounded to bf16
 // once (relative 2^-9 per entry, the x2 is exact). With the diagonal of C
@@ -67,7 +67,7 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
-constexpr int EPI_WARPS = 8;                   // two per tensor-memory lane quarter
+constexpr int EPI_WARPS = kGramEpilogueWarps;  // two per tensor-memory lane quarter
 constexpr int EPI_COLS = BN * 4 / EPI_WARPS;   // accumulator columns per epilogue warp
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int BAR_BYTES = 256;
@@ -85,13 +85,14 @@ struct GramParams {
   // loss kernel
   int nC;             // 256-channel column blocks: ceil(K / 256)
   int kbK;            // K / 64
-  int bands;          // bands per alpha (row blocks split evenly)
   int nR;             // 128-row blocks of D_i: ceil(N / 128)
+  int nP;             // column-block pairs: ceil(nC / 2)
+  int per_alpha;      // items per alpha: nR * nP
   uint64_t timeout_ns;
   uint32_t* status;
   uint16_t* H;          // [K][K] bf16 (H kernel output)
   const uint16_t* op;   // [G][N][K] bf16 D_i (loss epilogue)
-  float* partials;      // [G][bands][kGramShares][4]
+  float* partials;      // [G][nR * nP][EPI_WARPS]
   double* row_acc;      // optional [G][N], per-row sums added (loss kernel)
 };
 
@@ -121,76 +122,32 @@ __device__ __forceinline__ int tile_kblocks(const GramParams& p, int cb) {
   return min(KB_PER_COL_BLOCK * (cb + 1), p.kbK);
 }
 
-// k-blocks of one row block: sum over cb of tile_kblocks(cb).
-__device__ __forceinline__ int64_t row_units(const GramParams& p) {
-  const int64_t full = 2ll * p.nC * (p.nC + 1);  // sum of 4 (cb + 1)
-  return full - (KB_PER_COL_BLOCK * (int64_t)p.nC - p.kbK);
-}
-
-// Column block at position z of a row's zigzag order 0, nC-1, 1, nC-2, ...:
-// a short tile next to a long one, so that a share's time follows its
-// k-blocks (a short tile's epilogue outlasts its MMAs; the long neighbour's
-// MMAs hide it).
-__device__ __forceinline__ int zigzag_cb(const GramParams& p, int z) {
-  return (z & 1) ? p.nC - 1 - (z >> 1) : (z >> 1);
-}
-
-// A share's walk over its k-blocks [u, u1) of one band (row blocks in
-// order, each row's tiles in zigzag order): position (rbi, z, kb).
-struct Walk {
-  int64_t u, u1;
-  int row0, rows, rbi, z, kb;
-};
-
-__device__ __forceinline__ void walk_begin(const GramParams& p, int band, int share, Walk& w) {
-  // the bands split the row blocks as evenly as they can
-  w.row0 = (int)((int64_t)band * p.nR / p.bands);
-  w.rows = (int)((int64_t)(band + 1) * p.nR / p.bands) - w.row0;
-  const int64_t per_row = row_units(p);
-  const int64_t total = per_row * w.rows;
-  w.u = total * share / kGramShares;
-  w.u1 = total * (share + 1) / kGramShares;
-  w.rbi = 0;
-  w.z = 0;
-  w.kb = 0;
-  if (w.u >= w.u1) return;
-  w.rbi = (int)(w.u / per_row);
-  int64_t rem = w.u - (int64_t)w.rbi * per_row;
-  int z = 0;
-  for (; z < p.nC - 1; ++z) {
-    const int kc = tile_kblocks(p, zigzag_cb(p, z));
-    if (rem < kc) break;
-    rem -= kc;
+// Item t (< G * per_alpha) of the loss kernel: alpha a, row block rb and
+// column-block pair pp (blocks pp and nC-1-pp). Within an alpha the row
+// blocks go in groups of kGramRowGroup (the last group may be shorter), and
+// within a group pair-major, row-minor.
+__device__ __forceinline__ void decode_item(const GramParams& p, int t, int& a, int& rb, int& pp) {
+  a = t / p.per_alpha;
+  const int u = t - a * p.per_alpha;
+  const int full = p.nR / kGramRowGroup;  // whole groups
+  const int span = p.nP * kGramRowGroup;   // items of a whole group
+  int g, local, rows;
+  if (u < full * span) {
+    g = u / span;
+    local = u - g * span;
+    rows = kGramRowGroup;
+  } else {
+    g = full;
+    local = u - full * span;
+    rows = p.nR - full * kGramRowGroup;
   }
-  w.z = z;
-  w.kb = (int)rem;
-}
-
-// Next piece of the share: tile (rbi, cb), k-blocks [kb0, kb1). False when done.
-__device__ __forceinline__ bool walk_next(const GramParams& p, Walk& w, int& cb, int& rbi, int& kb0, int& kb1) {
-  if (w.u >= w.u1) return false;
-  cb = zigzag_cb(p, w.z);
-  const int kc = tile_kblocks(p, cb);
-  const int64_t left = w.u1 - w.u;
-  const int take = left < (int64_t)(kc - w.kb) ? (int)left : kc - w.kb;
-  rbi = w.rbi;
-  kb0 = w.kb;
-  kb1 = w.kb + take;
-  w.u += take;
-  w.kb = kb1;
-  if (w.kb == kc) {
-    w.kb = 0;
-    if (++w.z == p.nC) {
-      w.z = 0;
-      ++w.rbi;
-    }
-  }
-  return true;
+  pp = local / rows;
+  rb = g * kGramRowGroup + (local - pp * rows);
 }
 
 // The roles of both kernels walk the same sequence of pieces: fn(a, m_tile,
-// n_tile, kb0, kb1, share_first, share_last, flat_share) for every piece, and
-// for an empty share once with kb0 == kb1. Returns false if fn does.
+// n_tile, kb0, kb1, item_first, item_last, item) for every tile of every
+// item this CTA takes. Returns false if fn does.
 template <bool LOSS, typename Fn>
 __device__ __forceinline__ bool for_each_piece(const GramParams& p, int cta, int ncta, Fn&& fn) {
   if constexpr (!LOSS) {
@@ -200,23 +157,12 @@ __device__ __forceinline__ bool for_each_piece(const GramParams& p, int cta, int
       if (!fn(0, ct, jt, 0, p.kb_tok, true, true, it)) return false;
     }
   } else {
-    for (int ab = 0; ab < p.G * p.bands; ++ab) {
-      const int a = ab / p.bands, band = ab - a * p.bands;
-      for (int s = cta; s < kGramShares; s += ncta) {
-        Walk w;
-        walk_begin(p, band, s, w);
-        const int flat = ab * kGramShares + s;
-        if (w.u >= w.u1) {
-          if (!fn(a, 0, 0, 0, 0, true, true, flat)) return false;
-          continue;
-        }
-        bool first = true;
-        int cb, rbi, kb0, kb1;
-        while (walk_next(p, w, cb, rbi, kb0, kb1)) {
-          if (!fn(a, w.row0 + rbi, cb, kb0, kb1, first, w.u >= w.u1, flat)) return false;
-          first = false;
-        }
-      }
+    for (int it = cta; it < p.G * p.per_alpha; it += ncta) {
+      int a, rb, pp;
+      decode_item(p, it, a, rb, pp);
+      const int cb2 = p.nC - 1 - pp;  // the long tile; the same block for an odd middle one
+      if (!fn(a, rb, pp, 0, tile_kblocks(p, pp), true, cb2 == pp, it)) return false;
+      if (cb2 != pp && !fn(a, rb, cb2, 0, tile_kblocks(p, cb2), false, true, it)) return false;
     }
   }
   return true;
@@ -437,7 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           float ss = share_sum;
 #pragma unroll
           for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-          [[maybe_unused]] const size_t n_part = (size_t)p.G * p.bands * kGramShares * EPI_WARPS;
+          [[maybe_unused]] const size_t n_part = (size_t)p.G * p.per_alpha * EPI_WARPS;
           if (lane == 0 && AWQ_IN((size_t)flat * EPI_WARPS + ew, 1, n_part))
             p.partials[(size_t)flat * EPI_WARPS + ew] = ss;
         }
@@ -555,13 +501,15 @@ cudaError_t launch_gram_loss(const uint16_t* op, int64_t N, int64_t K, const awq
   p.nC = (int)((K + BN - 1) / BN);
   p.kbK = (int)(K / BK);
   p.nR = (int)((N + BM - 1) / BM);
-  p.bands = (int)gram_bands(N);
+  p.nP = (p.nC + 1) / 2;
+  p.per_alpha = p.nR * p.nP;
   p.timeout_ns = timeout_of(&cfg);
   p.status = status;
   p.op = op;
   p.partials = partials;
   p.row_acc = row_acc;
-  return launch_gram_kernel<true>(tmA, tmB, p, kGramShares, st);
+  const int64_t items = (int64_t)p.G * p.per_alpha;
+  return launch_gram_kernel<true>(tmA, tmB, p, items < (1 << 30) ? (int)items : (1 << 30), st);
 }
 
 #ifdef AWQ_CHECKED

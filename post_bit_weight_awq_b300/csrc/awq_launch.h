@@ -111,21 +111,20 @@ cudaError_t take_oob_gram(unsigned long long* out);
 cudaError_t launch_bounds_selftest(float* buf, int n, cudaStream_t st);
 #endif
 
-// Gram form of the search loss (awq_gram.cu). kGramShares: equal shares of
-// each band's work, one per CTA (fixed, so that the result does not depend on
-// the GPU); kGramBandRows: 128-row blocks of the operand per band.
-constexpr int kGramShares = 148;
-#ifndef AWQ_GRAM_BAND_ROWS
-#define AWQ_GRAM_BAND_ROWS 16
+// Gram form of the search loss (awq_gram.cu). kGramRowGroup: 128-row blocks
+// whose items for one column-block pair run on neighbouring CTAs.
+#ifndef AWQ_GRAM_ROW_GROUP
+#define AWQ_GRAM_ROW_GROUP 16
 #endif
-constexpr int kGramBandRows = AWQ_GRAM_BAND_ROWS;
+constexpr int kGramRowGroup = AWQ_GRAM_ROW_GROUP;
+constexpr int kGramEpilogueWarps = 8;
 inline int64_t gram_tokens_padded(int64_t n_tok) { return (n_tok + 63) / 64 * 64; }
-inline int64_t gram_bands(int64_t N) {
-  const int64_t row_blocks = (N + kTileM - 1) / kTileM;
-  return (row_blocks + kGramBandRows - 1) / kGramBandRows;
+// Column-block pairs (blocks cb and nC-1-cb of 256 channels) of in channels.
+inline int64_t gram_pairs(int64_t K) { return ((K + 255) / 256 + 1) / 2; }
+// fp32 partial sums of one alpha: [row blocks x pairs][epilogue warps].
+inline int64_t gram_partials_per_alpha(int64_t N, int64_t K) {
+  return (N + kTileM - 1) / kTileM * gram_pairs(K) * kGramEpilogueWarps;
 }
-// fp32 partial sums of one alpha: [bands][kGramShares][8 epilogue warps].
-inline int64_t gram_partials_per_alpha(int64_t N) { return gram_bands(N) * kGramShares * 8; }
 // H (bf16 [K][K], blocks on and below the 256-channel block diagonal) of X
 // (bf16 [n_tok][K], K a multiple of 128), through the transposed copy xt
 // (bf16 [K][gram_tokens_padded(n_tok)], overwritten).
