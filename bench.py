@@ -364,7 +364,7 @@ def stage_kernels(R, flush, reps):
     inv = torch.empty_like(s)
     op = torch.empty(G, N, K, dtype=torch.bfloat16, device=dev)
     mt, nt, _, _ = capi_testing.awq_search_tiles(n, N, R.cfg)
-    parts = torch.empty(G, mt, nt, 4, dtype=torch.float32, device=dev)
+    parts = torch.zeros(G, mt, nt, 4, dtype=torch.float32, device=dev)  # loss_select may run before the products
     ready = torch.zeros(G * (nt + 1) + 1, dtype=torch.int32, device=dev)
     status = torch.zeros(4, dtype=torch.int32, device=dev)
     losses = torch.empty(G, dtype=torch.float32, device=dev)
@@ -378,17 +378,19 @@ def stage_kernels(R, flush, reps):
     gparts = torch.empty(G, per_alpha, dtype=torch.float32, device=dev)
     capi_testing.awq_gram_matrix(R.X, xt, H, gcfg, status)
     calls = {
+        # short kernels first, rested
         "stats": lambda: capi.awq_act_stats(R.X, R.mean_abs, R.ws),
         "alpha_scales": lambda: capi_testing.awq_alpha_scales(R.mean_abs, R.cfg, s, inv),
         "fakequant": lambda: capi_testing.awq_fakequant(R.W, s, inv, R.cfg, op),
         "pack": lambda: capi.awq_quantize_pack(R.W, R.s_best, R.cfg, R.qw, R.sc, R.zr),
-        "search_gemm": lambda: capi_testing.awq_search_gemm(R.X, op, R.cfg, parts, status, n_tok=n, in_features=K,
-                                                            out_features=N),
+        "gram_matrix": lambda: capi_testing.awq_gram_matrix(R.X, xt, H, gcfg, status),
         "loss_select": lambda: capi_testing.awq_loss_select(parts, s, R.cfg, losses, best, s_best, status, n_tok=n,
                                                             out_features=N, in_features=K),
-        "fused_search": lambda: capi_testing.awq_search_fused(R.W, R.X, s, inv, R.cfg, op, parts, ready, status),
-        "gram_matrix": lambda: capi_testing.awq_gram_matrix(R.X, xt, H, gcfg, status),
+        # then the products: the GRAM form's, then the direct form's two kernels for comparison
         "gram_loss": lambda: capi_testing.awq_gram_loss(op, H, gcfg, gparts, status),
+        "search_gemm": lambda: capi_testing.awq_search_gemm(R.X, op, R.cfg, parts, status, n_tok=n, in_features=K,
+                                                            out_features=N),
+        "fused_search": lambda: capi_testing.awq_search_fused(R.W, R.X, s, inv, R.cfg, op, parts, ready, status),
     }
     out = {}
     torch.cuda.synchronize()
