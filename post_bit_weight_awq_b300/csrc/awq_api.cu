@@ -182,12 +182,24 @@ struct PipeLayout {
   size_t total;
 };
 
+// Bytes of search workspace that hold a search of any shape within the given
+// maxima. Every region of a form's layout grows with each dimension; AUTO
+// resolves per shape, so a smaller layer may take the other form than the
+// maxima would: the bound is the larger of the two forms' layouts.
+size_t search_bytes_bound(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg) {
+  if (cfg.loss_form != AWQ_LOSS_AUTO) return search_layout(n_tok, out, in, cfg).total;
+  awq_config r = cfg, g = cfg;
+  r.loss_form = AWQ_LOSS_RESIDUAL;
+  g.loss_form = AWQ_LOSS_GRAM;
+  return std::max(search_layout(n_tok, out, in, r).total, search_layout(n_tok, out, in, g).total);
+}
+
 PipeLayout pipe_layout(int64_t n_tok, int64_t out, int64_t in, int32_t w_dtype, const awq_config& cfg) {
   PipeLayout P;
   const size_t wbytes = w_dtype == AWQ_BF16 ? 2 : 4;
   size_t off = 0;
   P.search = off;
-  off = align_up(off + search_layout(n_tok, out, in, cfg).total, kAlign);
+  off = align_up(off + search_bytes_bound(n_tok, out, in, cfg), kAlign);
   P.stats = off;
   size_t stats_bytes = 0;
   awq_act_stats_workspace_size(n_tok, in, &stats_bytes);
@@ -803,9 +815,13 @@ awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_
     in_max = layers[i].in > in_max ? layers[i].in : in_max;
   }
   // every region of the layout grows with each dimension, so the layout of
-  // the largest dimensions holds every layer at the same offsets
+  // the largest dimensions holds every layer at the same offsets (for the
+  // search region, whichever loss form each layer resolves to)
   const PipeLayout P = pipe_layout(n_max, out_max, in_max, w_dtype, *cfg);
   if (ws_bytes < P.total) return AWQ_ERR_WORKSPACE;
+  for (int32_t i = 0; i < count; ++i)  // holds by construction; checked before anything is queued
+    if (search_layout(layers[i].n_tok, layers[i].out, layers[i].in, *cfg).total > P.stats - P.search)
+      return AWQ_ERR_WORKSPACE;
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return AWQ_ERR_CUDA;

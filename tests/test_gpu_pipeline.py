@@ -92,6 +92,22 @@ def test_layers_from_host_equal_the_device_path(w_dtype_name):
         _assert_same(o, _device_path(L, cfg))
 
 
+def test_layers_of_both_loss_forms_in_one_call():
+    """AUTO resolves per layer: GRAM for layers with in < 2 n_tok and many rows, RESIDUAL for the others. A
+    pipeline call mixing both (the largest dimensions come from different layers) equals the device path bit
+    for bit; its workspace holds either form's scratch for every layer."""
+    shapes = [(2048, 1024, 1024), (300, 520, 1024), (1024, 1536, 768), (64, 256, 2048)]
+    cfg = capi.config()
+    forms = [capi.awq_search_form(n, N, K, cfg) for n, N, K in shapes]
+    assert forms == [capi.AWQ_LOSS_GRAM, capi.AWQ_LOSS_RESIDUAL, capi.AWQ_LOSS_GRAM, capi.AWQ_LOSS_RESIDUAL]
+    Ls = [workloads.make_layer("llama7b_q_proj", n_tok=n, out_features=N, in_features=K, seed=40 + i)
+          for i, (n, N, K) in enumerate(shapes)]
+    outs, status = _run_pipeline(Ls, cfg, capi.AWQ_BF16)
+    assert status == capi.AWQ_OK
+    for L, o in zip(Ls, outs):
+        _assert_same(o, _device_path(L, cfg))
+
+
 def test_layers_from_host_meet_the_oracle_levels():
     """Levels 2 and 3 (losses within 1e-2, argmin within 0.5%) and level 1 (the pack with the oracle's
     scale, where the GPU chose the same alpha) for two layers with other quantiser knobs."""
