@@ -26,6 +26,16 @@ AWQ_API awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in
                                         const awq_config* cfg, float* partials, uint32_t* status, float* dump,
                                         int32_t single_cta, awq_stream_t stream);
 
+/* The bounded waits of the GRAM form's products: awq_gram_loss with the
+   first ring fill of every CTA left out, so the MMA issuer's wait on that
+   stage can never complete. As for awq_search_gemm_withhold_fill: each wait
+   gives up after cfg->wait_timeout_ms, the kernel writes AWQ_ERR_TIMEOUT to
+   *status, stops all its roles, lets what it issued finish, frees its tensor
+   memory and returns. partials are not meaningful. */
+AWQ_API awq_status awq_gram_loss_withhold_fill(const uint16_t* op, int64_t out, int64_t in, const uint16_t* H,
+                                               const awq_config* cfg, float* partials, uint32_t* status,
+                                               awq_stream_t stream);
+
 /* The bounded waits of the single-CTA search kernel: awq_search_gemm with
    the first operand fill of every CTA left out, so the MMA issuer's wait on
    that pipeline stage can never complete. Each wait gives up after

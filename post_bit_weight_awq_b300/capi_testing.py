@@ -36,6 +36,7 @@ TESTING_EXPORTED = (
     "awq_search_gemm_dump",
     "awq_search_gemm_withhold_fill",
     "awq_search_fused_withhold_unit",
+    "awq_gram_loss_withhold_fill",
     "awq_bounds_report",
     "awq_bounds_selftest",
 )
@@ -66,6 +67,7 @@ def lib() -> ctypes.CDLL:
         "awq_search_gemm_withhold_fill": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _CFG, _P, _P, _P]),
         "awq_search_fused_withhold_unit": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _I64, _P, _P, _CFG, _P, _P, _P,
                                                           _P, _P]),
+        "awq_gram_loss_withhold_fill": (ctypes.c_int, [_P, _I64, _I64, _P, _CFG, _P, _P, _P]),
         "awq_bounds_report": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_I32),
                                              ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
         "awq_bounds_selftest": (ctypes.c_int, [_P, _I32, _P]),
@@ -189,3 +191,11 @@ def awq_bounds_report():
 def awq_bounds_selftest(buf, stream=None, *, n=None) -> None:
     _check(lib().awq_bounds_selftest(_ptr(buf), buf.numel() if n is None else n, _stream(stream)),
            "awq_bounds_selftest")
+
+
+def awq_gram_loss_withhold_fill(op, H, cfg: AwqConfig, partials, status, stream=None, *, out_features=None,
+                                in_features=None) -> None:
+    N = op.shape[-2] if out_features is None else out_features
+    K = op.shape[-1] if in_features is None else in_features
+    _check(lib().awq_gram_loss_withhold_fill(_ptr(op), N, K, _ptr(H), ctypes.byref(cfg), _ptr(partials),
+                                             _ptr(status), _stream(stream)), "awq_gram_loss_withhold_fill")

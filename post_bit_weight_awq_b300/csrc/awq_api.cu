@@ -461,6 +461,19 @@ awq_status awq_search_gemm_dump(const void* X, int64_t n_tok, int64_t in, const 
                                       (cudaStream_t)stream, dump, 0, single_cta));
 }
 
+awq_status awq_gram_loss_withhold_fill(const uint16_t* op, int64_t out, int64_t in, const uint16_t* H,
+                                       const awq_config* cfg, float* partials, uint32_t* status,
+                                       awq_stream_t stream) {
+  AWQ_TRACE("awq_gram_loss_withhold_fill");
+  if (op == nullptr || H == nullptr || partials == nullptr || status == nullptr) return AWQ_ERR_INVALID_ARG;
+  awq_status st = check_cfg(cfg);
+  if (st != AWQ_OK) return st;
+  st = check_dims(1, out, in);
+  if (st != AWQ_OK) return st;
+  if (!aligned16(op) || !aligned16(H) || !aligned16(partials) || !aligned16(status)) return AWQ_ERR_MISALIGNED;
+  return from_cuda(launch_gram_loss(op, out, in, *cfg, H, partials, status, (cudaStream_t)stream, nullptr, 1));
+}
+
 awq_status awq_search_gemm_withhold_fill(const void* X, int64_t n_tok, int64_t in, const uint16_t* op,
                                          int64_t out, const awq_config* cfg, float* partials, uint32_t* status,
                                          awq_stream_t stream) {

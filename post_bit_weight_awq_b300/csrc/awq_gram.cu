@@ -94,6 +94,7 @@ struct GramParams {
   const uint16_t* op;   // [G][N][K] bf16 D_i (loss epilogue)
   float* partials;      // [G][nR * nP][EPI_WARPS]
   double* row_acc;      // optional [G][N], per-row sums added (loss kernel)
+  int withhold_first_fill;  // test aid: leave out each CTA's first ring fill (loss kernel)
 };
 
 // ---------------------------------------------------------------- H tiles
@@ -234,18 +235,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------------ producer
       uint32_t stage = 0, phase = 0;
       uint32_t used = 0, last_par = 0;  // per-stage bit: stage used; parity of its last fill
+      bool withhold = p.withhold_first_fill != 0;
       for_each_piece<LOSS>(p, cta, ncta, [&](int a, int mt, int nt, int kb0, int kb1, bool, bool, int) {
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.status)) return false;
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          if constexpr (LOSS) {
-            tma_load_3d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, mt * BM, a);
+          if (withhold) {
+            // test aid: this stage is never filled, so the wait on it cannot complete
+            withhold = false;
           } else {
-            tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, mt * BM);
+            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+            if constexpr (LOSS) {
+              tma_load_3d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, mt * BM, a);
+            } else {
+              tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, mt * BM);
+            }
+            tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nt * BN);
+            used |= 1u << stage;
+            last_par = (last_par & ~(1u << stage)) | (phase << stage);
           }
-          tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nt * BN);
-          used |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -487,7 +494,8 @@ cudaError_t launch_gram_matrix(const uint16_t* X, int64_t n_tok, int64_t K, uint
 }
 
 cudaError_t launch_gram_loss(const uint16_t* op, int64_t N, int64_t K, const awq_config& cfg, const uint16_t* H,
-                             float* partials, uint32_t* status, cudaStream_t st, double* row_acc) {
+                             float* partials, uint32_t* status, cudaStream_t st, double* row_acc,
+                             int withhold_first_fill) {
   CUtensorMap tmA, tmB;
   const cuuint64_t da[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)cfg.n_grid};
   const cuuint32_t ba[3] = {(cuuint32_t)BK, (cuuint32_t)BM, 1u};
@@ -508,6 +516,7 @@ cudaError_t launch_gram_loss(const uint16_t* op, int64_t N, int64_t K, const awq
   p.op = op;
   p.partials = partials;
   p.row_acc = row_acc;
+  p.withhold_first_fill = withhold_first_fill;
   const int64_t items = (int64_t)p.G * p.per_alpha;
   return launch_gram_kernel<true>(tmA, tmB, p, items < (1 << 30) ? (int)items : (1 << 30), st);
 }

@@ -132,8 +132,10 @@ cudaError_t launch_gram_matrix(const uint16_t* X, int64_t n_tok, int64_t K, uint
                                uint32_t* status, uint32_t wait_timeout_ms, cudaStream_t st);
 // partials[a][...] of sum_r D_a[r] C D_a[r]^T, D_a = op slot a (bf16 [n_grid][N][K]).
 // row_acc: if not null, fp64 [n_grid][N] to which each row's sum is added.
+// withhold_first_fill: test aid, each CTA's first ring stage is never filled.
 cudaError_t launch_gram_loss(const uint16_t* op, int64_t N, int64_t K, const awq_config& cfg, const uint16_t* H,
-                             float* partials, uint32_t* status, cudaStream_t st, double* row_acc = nullptr);
+                             float* partials, uint32_t* status, cudaStream_t st, double* row_acc = nullptr,
+                             int withhold_first_fill = 0);
 
 // W_hat[r][k] = bf16((q[r][k] - z[r][g]) * scale[r][g]) for the whole packed
 // layer (bf16 [N][K]), the operand of the prefill product.

@@ -53,6 +53,42 @@ def test_stuck_wait_ends_with_timeout_status_and_device_stays_usable():
         assert P[i] == pytest.approx(ref, rel=1e-4)
 
 
+def test_gram_loss_stuck_wait_ends_with_timeout_and_device_stays_usable():
+    """The GRAM form's products with every CTA's first ring stage left unfilled: the MMA issuer's wait runs
+    out after the limit, the kernel reports AWQ_ERR_TIMEOUT and returns, and the next launch on the same
+    device gives the right sums (checked against sum_r D[r] X^T X D[r]^T in fp64)."""
+    n, N, K, G = 512, 640, 768, 2
+    rng = np.random.default_rng(5)
+    X = workloads.round_to_bf16(rng.standard_normal((n, K)).astype(np.float32))
+    D = workloads.round_to_bf16((rng.standard_normal((G, N, K)) * 0.01).astype(np.float32))
+    Xd, Dd = dev_bf16(X), dev_bf16(D.reshape(G * N, K))
+    cfg = capi.config(n_grid=G, wait_timeout_ms=100, loss_form=capi.AWQ_LOSS_GRAM)
+    xt_elems, h_elems, per_alpha = capi_testing.awq_gram_sizes(n, N, K)
+    xt = torch.empty(xt_elems, dtype=torch.bfloat16, device="cuda")
+    H = torch.empty(h_elems, dtype=torch.bfloat16, device="cuda")
+    partials = torch.zeros(G, per_alpha, dtype=torch.float32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    capi_testing.awq_gram_matrix(Xd, xt, H, cfg, status, n_tok=n, in_features=K)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    t0 = time.perf_counter()
+    capi_testing.awq_gram_loss_withhold_fill(Dd, H, cfg, partials, status, out_features=N, in_features=K)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status[0]) == capi.AWQ_ERR_TIMEOUT
+    assert elapsed < 5.0
+    status.zero_()
+    capi_testing.awq_gram_loss(Dd, H, cfg, partials, status, out_features=N, in_features=K)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    C = X.astype(np.float64).T @ X.astype(np.float64)
+    P = partials.cpu().numpy().astype(np.float64).sum(axis=1)
+    for i in range(G):
+        Di = D[i].astype(np.float64)
+        ref = float(np.einsum("rc,cj,rj->", Di, C, Di))
+        assert P[i] == pytest.approx(ref, rel=1e-3)
+
+
 def test_fused_search_stuck_tile_ends_with_timeout_and_device_stays_usable():
     """The cross-CTA wait of the fused search: one quantiser unit is never
     published, so the producers needing its tile wait until the limit; the
