@@ -115,7 +115,7 @@ __device__ __forceinline__ void decode_h_tile(int i, int& ct, int& jt) {
   }
 }
 
-// ---------------------------------------------------------------- loss shares
+// ---------------------------------------------------------------- loss items
 //
 // k-blocks of a tile in column block cb: the prefix of 256-channel blocks up
 // to and including cb (a last, half block has 2 instead of 4).
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t ph = 0;  // bit b: parity of accumulator buffer b
       uint32_t local = 0;
       for_each_piece<LOSS>(p, cta, ncta, [&](int, int, int, int kb0, int kb1, bool, bool, int) {
-        if (kb0 == kb1) return true;  // empty share: no accumulator
+        if (kb0 == kb1) return true;  // an empty piece uses no accumulator
         const int buf = (int)(local & 1u);
         if (!mbar_wait(&tempty[buf], ((ph >> buf) & 1u) ^ 1u, p.timeout_ns, abort_flag, p.status)) return false;
         tc_fence_after();
@@ -308,10 +308,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t ph = 0;
     uint32_t local = 0;
-    float share_sum = 0.0f;
+    float item_sum = 0.0f;
     for_each_piece<LOSS>(p, cta, ncta, [&](int a, int mt, int nt, int kb0, int kb1, bool first, bool last, int flat) {
       if constexpr (LOSS) {
-        if (first) share_sum = 0.0f;
+        if (first) item_sum = 0.0f;
       }
       if (kb0 < kb1) {
         const int buf = (int)(local & 1u);
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const float lane_sum = s0 + s1;
           if (p.row_acc != nullptr && row_ok && AWQ_IN((size_t)a * p.N + row, 1, (size_t)p.G * p.N))
             atomicAdd(&p.row_acc[(size_t)a * p.N + row], (double)lane_sum);
-          share_sum += lane_sum;
+          item_sum += lane_sum;
         } else {
           if (!__all_sync(0xffffffffu,
                           mbar_wait(&tfull[buf], (ph >> buf) & 1u, p.timeout_ns, abort_flag, p.status)))
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if constexpr (LOSS) {
         if (last) {
-          float ss = share_sum;
+          float ss = item_sum;
 #pragma unroll
           for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
           [[maybe_unused]] const size_t n_part = (size_t)p.G * p.per_alpha * EPI_WARPS;

@@ -379,9 +379,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     cp_async_commit();
   };
+  // Programmatic dependent launch: the next kernel on the stream may start
+  // launching now (its blocks take SMs as this kernel's leave). The codes,
+  // steps and zeros of a packed layer are not written by the kernels before
+  // this one, so the first pairs are fetched before waiting for them to
+  // finish; x (the previous layer's output, in a decode step) and y are
+  // touched only after. Without the launch attribute the wait returns at once.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the first pairs' codes are in flight while x is staged
 #pragma unroll
   for (int st = 0; st < kMmaStages - 1; ++st) fetch(st);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // stage x: chunk i (8 channels) of token n is (group gi, quarter c, chunk m) = (i / 16, i / 4 % 4, i % 4)
   {
@@ -651,7 +659,20 @@ cudaError_t launch_w4a16_gemv(const uint16_t* x, int64_t M, int64_t K, const int
     // one block per SM, each with a contiguous run of row tiles
     const int64_t tiles = (N + 15) / 16;
     const int64_t grid = tiles < (int64_t)sms ? tiles : (int64_t)sms;
-    w4a16_mma_kernel<<<(unsigned)grid, kMmaThreads, smem, st>>>(x, (int)M, (int)K, qweight, scales, zeros, (int)N, y);
+    // launched so that it may overlap the previous kernel's tail (the kernel
+    // waits for that kernel before it reads x)
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.gridDim = dim3((unsigned)grid);
+    lc.blockDim = dim3(kMmaThreads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = st;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&lc, w4a16_mma_kernel, x, (int)M, (int)K, qweight, scales, zeros, (int)N, y);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
   switch (M) {
