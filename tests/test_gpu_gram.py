@@ -28,7 +28,8 @@ import oracle as O
 import workloads
 from gpu_util import dev_bf16, dev_f32, dev_weight, host_bf16_to_f64
 from post_bit_weight_awq_b300 import build, capi, capi_testing, layer
-from test_gpu_layers import LOSS_RTOL, _arithmetic_bound, _check_levels, _check_pack, _oracle_losses
+from test_gpu_layers import (LOSS_RTOL, _arithmetic_bound, _check_levels, _check_pack, _oracle_losses,
+                             _search_with_statistic)
 
 pytestmark = pytest.mark.gpu
 
@@ -167,6 +168,20 @@ def test_gram_search_layer_ragged(n, N, K):
                   bound=_gram_bound(L, sx32) if degenerate else None)
     if int(best[0]) == res["best_idx"]:
         np.testing.assert_array_equal(s_best.cpu().numpy(), O.f32(res["s_best"]))
+
+
+@pytest.mark.parametrize("kw", [dict(group=64), dict(group=32), dict(w_bit=3), dict(group=64, w_bit=2),
+                                dict(zero_point=0)])
+def test_gram_search_other_quantisers(kw):
+    """The GRAM form with the other quantiser settings (groups of 64 and 32, 3 and 2 bits, the symmetric
+    quantiser): levels 2 and 3 against the oracle run with the same settings."""
+    L = workloads.make_layer("llama7b_q_proj", n_tok=1024, out_features=640, in_features=1024,
+                             seed=17 + sum(kw.values()))
+    sx32 = O.f32(O.channel_importance(L["X"]))
+    okw = {k: (bool(v) if k == "zero_point" else v) for k, v in kw.items()}
+    res = _oracle_losses(L["W"], L["X"], sx=sx32, **okw)
+    losses, best, _ = _search_with_statistic(L, sx32, capi.config(loss_form=GRAM, **kw))
+    _check_levels(losses, best, res["losses"])
 
 
 def test_gram_tiny_layer_all_levels():
