@@ -124,8 +124,11 @@ typedef enum { AWQ_BF16 = 0, AWQ_FP32 = 1 } awq_dtype;
               P[r][c] * D[r][c]. Fewer flops than RESIDUAL when in < 2 n_tok.
               The losses differ from RESIDUAL's by the bf16 rounding of C
               (about 2^-9 / sqrt(in) relative when C's diagonal dominates).
+              in <= 65535 * 64 (else AWQ_ERR_UNSUPPORTED); the workspace
+              holds C, in * in bf16.
    AUTO:      GRAM when its tensor-core flops (C plus the alphas' products)
-              are below 0.7 of RESIDUAL's, else RESIDUAL (default). The choice
+              are below 0.7 of RESIDUAL's and in <= 65535 * 64, else
+              RESIDUAL (default). The choice
               depends on the shape and n_grid only; awq_search_form reports it.
               The per-kernel calls of awq_stages.h take AUTO as RESIDUAL. */
 typedef enum {

@@ -47,13 +47,23 @@ double gram_flops(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg)
   return h + 2.0 * cfg.n_grid * (double)nR * kTileM * kTileN * prefix;
 }
 
+// Largest `in` of the GRAM form: the transpose's grid has in / 64 rows of
+// tiles, at most 65535.
+constexpr int64_t kGramMaxIn = (int64_t)65535 * 64;
+
 // The form a search runs: AUTO resolves to GRAM when that form's flops are
 // below 0.7 of the direct product's (the GRAM form adds X^T X, a transpose
 // and a separate fake-quant launch), else to RESIDUAL.
 int32_t resolve_form(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg) {
   if (cfg.loss_form != AWQ_LOSS_AUTO) return cfg.loss_form;
+  if (in > kGramMaxIn) return AWQ_LOSS_RESIDUAL;
   return gram_flops(n_tok, out, in, cfg) < 0.7 * search_flops(n_tok, out, in, cfg) ? AWQ_LOSS_GRAM
                                                                                  : AWQ_LOSS_RESIDUAL;
+}
+
+// AWQ_ERR_UNSUPPORTED for a search whose form is GRAM beyond kGramMaxIn.
+awq_status check_form(int64_t n_tok, int64_t out, int64_t in, const awq_config& cfg) {
+  return resolve_form(n_tok, out, in, cfg) == AWQ_LOSS_GRAM && in > kGramMaxIn ? AWQ_ERR_UNSUPPORTED : AWQ_OK;
 }
 
 // The configuration a per-kernel stage call runs with: AUTO is RESIDUAL there.
@@ -191,7 +201,9 @@ size_t search_bytes_bound(int64_t n_tok, int64_t out, int64_t in, const awq_conf
   awq_config r = cfg, g = cfg;
   r.loss_form = AWQ_LOSS_RESIDUAL;
   g.loss_form = AWQ_LOSS_GRAM;
-  return std::max(search_layout(n_tok, out, in, r).total, search_layout(n_tok, out, in, g).total);
+  // AUTO takes the GRAM form only up to kGramMaxIn channels
+  return std::max(search_layout(n_tok, out, in, r).total,
+                  search_layout(n_tok, out, std::min(in, kGramMaxIn), g).total);
 }
 
 PipeLayout pipe_layout(int64_t n_tok, int64_t out, int64_t in, int32_t w_dtype, const awq_config& cfg) {
@@ -331,6 +343,8 @@ awq_status awq_workspace_size(int64_t n_tok, int64_t out, int64_t in, const awq_
   if (st != AWQ_OK) return st;
   st = check_dims(n_tok, out, in);
   if (st != AWQ_OK) return st;
+  st = check_form(n_tok, out, in, *cfg);
+  if (st != AWQ_OK) return st;
   *bytes = search_layout(n_tok, out, in, *cfg).total;
   return AWQ_OK;
 }
@@ -340,6 +354,8 @@ awq_status awq_search_form(int64_t n_tok, int64_t out, int64_t in, const awq_con
   awq_status st = check_cfg(cfg);
   if (st != AWQ_OK) return st;
   st = check_dims(n_tok, out, in);
+  if (st != AWQ_OK) return st;
+  st = check_form(n_tok, out, in, *cfg);
   if (st != AWQ_OK) return st;
   *form = resolve_form(n_tok, out, in, *cfg);
   return AWQ_OK;
@@ -525,6 +541,7 @@ awq_status awq_gram_matrix(const void* X, int64_t n_tok, int64_t in, uint16_t* x
   if (st != AWQ_OK) return st;
   st = check_dims(n_tok, 1, in);
   if (st != AWQ_OK) return st;
+  if (in > kGramMaxIn) return AWQ_ERR_UNSUPPORTED;
   if (!aligned16(X) || !aligned16(xt) || !aligned16(H) || !aligned16(status)) return AWQ_ERR_MISALIGNED;
   return from_cuda(launch_gram_matrix((const uint16_t*)X, n_tok, in, xt, H, status, cfg->wait_timeout_ms,
                                       (cudaStream_t)stream));
@@ -560,6 +577,8 @@ awq_status awq_search_layer(const void* W, int32_t w_dtype, int64_t out, int64_t
   if (st != AWQ_OK) return st;
   if (!aligned16(W) || !aligned16(X) || !aligned16(mean_abs) || !aligned16(s_best) || !aligned16(ws))
     return AWQ_ERR_MISALIGNED;
+  st = check_form(n_tok, out, in, *cfg);
+  if (st != AWQ_OK) return st;
   const SearchLayout L = search_layout(n_tok, out, in, *cfg);
   if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE;
 
@@ -581,6 +600,8 @@ awq_status awq_search_block_workspace_size(int64_t n_tok, const int64_t* outs, i
     total += outs[i];
   }
   st = check_dims(n_tok, total, in);
+  if (st != AWQ_OK) return st;
+  st = check_form(n_tok, total, in, *cfg);
   if (st != AWQ_OK) return st;
   const size_t wbytes = w_dtype == AWQ_BF16 ? 2 : 4;
   *bytes = search_layout(n_tok, total, in, *cfg).total + align_up((size_t)total * in * wbytes, kAlign);
@@ -806,6 +827,7 @@ awq_status awq_pipeline_workspace_size(int64_t max_n_tok, int64_t max_out, int64
   if (st != AWQ_OK) return st;
   st = check_dims(max_n_tok, max_out, max_in);
   if (st != AWQ_OK) return st;
+  if (cfg->loss_form == AWQ_LOSS_GRAM && max_in > kGramMaxIn) return AWQ_ERR_UNSUPPORTED;
   *bytes = pipe_layout(max_n_tok, max_out, max_in, w_dtype, *cfg).total;
   return AWQ_OK;
 }
@@ -832,9 +854,12 @@ awq_status awq_quantize_layers(const awq_layer_io* layers, int32_t count, int32_
   // search region, whichever loss form each layer resolves to)
   const PipeLayout P = pipe_layout(n_max, out_max, in_max, w_dtype, *cfg);
   if (ws_bytes < P.total) return AWQ_ERR_WORKSPACE;
-  for (int32_t i = 0; i < count; ++i)  // holds by construction; checked before anything is queued
+  for (int32_t i = 0; i < count; ++i) {  // checked before anything is queued
+    st = check_form(layers[i].n_tok, layers[i].out, layers[i].in, *cfg);
+    if (st != AWQ_OK) return st;
     if (search_layout(layers[i].n_tok, layers[i].out, layers[i].in, *cfg).total > P.stats - P.search)
-      return AWQ_ERR_WORKSPACE;
+      return AWQ_ERR_WORKSPACE;  // holds by construction
+  }
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return AWQ_ERR_CUDA;

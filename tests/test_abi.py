@@ -96,6 +96,21 @@ def test_auto_form_resolution(lib, shape, form):
     assert (h + loss < 0.7 * 2.0 * 20 * n * N * K) == (form == "GRAM")
 
 
+def test_gram_form_channel_limit(lib):
+    """The GRAM form's transpose takes in / 64 rows of tiles on one grid axis (at most 65535): past
+    65535 * 64 channels AUTO keeps the direct form and an explicit GRAM request is refused up front."""
+    n, N, K = 1 << 23, 128, 65536 * 64
+    assert capi.awq_search_form(n, N, K, capi.config()) == capi.AWQ_LOSS_RESIDUAL
+    gram = capi.config(loss_form=capi.AWQ_LOSS_GRAM)
+    for fn in (lambda: capi.awq_search_form(n, N, K, gram), lambda: capi.awq_workspace_size(n, N, K, gram),
+               lambda: capi.awq_pipeline_workspace_size(n, N, K, capi.AWQ_BF16, gram)):
+        with pytest.raises(capi.AwqError) as e:
+            fn()
+        assert e.value.status == capi.AWQ_ERR_UNSUPPORTED
+    # just inside the limit the explicit form is accepted
+    assert capi.awq_search_form(1 << 16, N, 65535 * 64 - 64, gram) == capi.AWQ_LOSS_GRAM
+
+
 def test_auto_form_rejects_unknown_forms(lib):
     with pytest.raises(capi.AwqError):
         capi.awq_search_form(128, 256, 256, capi.config(loss_form=4))
